@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark of the keep-quant GEMV / MoE routed-expert path (libggq) on GB300.
+
+Headline workload (one "step"): the non-grouped K-quant GEMV, W = 14336 x 4096
+in each of Q8_0, Q4_K, Q5_K and Q6_K, at 1, 2, 4 and 8 tokens (16 GEMVs; x is
+quantized to Q8_K once per token count and shared by the four formats).
+Metric: packed weight bytes streamed per second (GB/s) and its fraction of the
+measured HBM copy bandwidth.  Each format has 3 rotating weight copies, so the
+weights of one step (736 MB) and the live set (551 MB) are far larger than the
+129 MB L2.  The step is captured once in a CUDA graph and replayed.
+
+Secondary lines (same JSON, "workloads"): the Q4_0 1024 x 4096 GEMV, the MoE
+decode layer (128 experts, H 2048, I 768, Q4_K gate/up, Q6_K down, top-8,
+1-4 tokens) and the MXFP4 routed experts (256 experts, H 4096, I 2048, top-8,
+1-5 tokens); MoE GB/s counts the distinct experts actually selected.
+
+--impl reference times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ggq_synth as syn  # noqa: E402
+
+KQ = syn.GEMV_KQUANT
+FMTS = KQ["fmts"]
+TOKENS = KQ["T"]
+N, K = KQ["N"], KQ["K"]
+ROTATE = 3
+METRIC = "decode GEMV/MoE packed-weight GB/s (% of HBM); prefill expert GEMM int8 TOPS"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- CUDA runtime (events in graphs)
+
+class Cudart:
+    def __init__(self):
+        self.lib = None
+        for name in ("libcudart.so.13", "libcudart.so", "/usr/local/cuda/lib64/libcudart.so"):
+            try:
+                self.lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.lib is None:
+            raise RuntimeError("libcudart not found")
+        self.lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.lib.cudaEventSynchronize.argtypes = [ctypes.c_void_p]
+
+    def event(self):
+        e = ctypes.c_void_p()
+        assert self.lib.cudaEventCreate(ctypes.byref(e)) == 0
+        return e
+
+    def record(self, ev, stream, external=False):
+        rc = self.lib.cudaEventRecordWithFlags(ev, ctypes.c_void_p(stream.cuda_stream), 1 if external else 0)
+        if rc != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags rc={rc}")
+
+    def elapsed_ms(self, a, b):
+        self.lib.cudaEventSynchronize(b)
+        ms = ctypes.c_float()
+        rc = self.lib.cudaEventElapsedTime(ctypes.byref(ms), a, b)
+        if rc != 0:
+            raise RuntimeError(f"cudaEventElapsedTime rc={rc}")
+        return ms.value
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- distributed plumbing
+
+def dist_init(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_rate(target_s=12.0):
+    """The oracle's integer-dot GEMV over the headline workload, on a row
+    sample sized for ~target_s seconds on all host cores.  Returns (GB/s of
+    packed weights, cores, sample description, seconds)."""
+    import oracle as orc
+    cores = os.cpu_count() or 1
+    orc.set_threads(cores)
+    g = syn.rng(KQ["index"], 900)
+    xq = {T: orc.quantize("Q8_K", syn.activations(T, K, g)) for T in TOKENS}
+    probe_rows = 64
+    Wp = {f: syn.weights(f, probe_rows, K, g) for f in FMTS}
+    t0 = time.perf_counter()
+    for f in FMTS:
+        for T in TOKENS:
+            orc.gemv(f, Wp[f], probe_rows, K, xq[T], T)
+    dt = time.perf_counter() - t0
+    rows = int(max(probe_rows, min(N, probe_rows * target_s / max(dt, 1e-6))))
+    W = {f: syn.weights(f, rows, K, g) for f in FMTS}
+    t0 = time.perf_counter()
+    for f in FMTS:
+        for T in TOKENS:
+            orc.gemv(f, W[f], rows, K, xq[T], T)
+    dt = time.perf_counter() - t0
+    nbytes = sum(rows * syn.row_bytes(f, K) for f in FMTS) * len(TOKENS)
+    sample = (f"{rows} of {N} rows of each of Q8_0/Q4_K/Q5_K/Q6_K (K={K}) at T=1,2,4,8: "
+              f"{nbytes / 1e6:.1f} MB of packed weights, oracle integer-dot GEMV, {cores} OpenMP threads")
+    return nbytes / dt / 1e9, orc.threads(), sample, dt, rows
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    orc.set_threads(cores)
+    g = syn.rng(KQ["index"], 900)
+    xq = {T: orc.quantize("Q8_K", syn.activations(T, K, g)) for T in TOKENS}
+    # bounded sample: each step is 256 rows of every matrix, all token counts
+    rows = 256
+    W = {f: syn.weights(f, rows, K, g) for f in FMTS}
+
+    def step():
+        for f in FMTS:
+            for T in TOKENS:
+                orc.gemv(f, W[f], rows, K, xq[T], T)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    nbytes = sum(rows * syn.row_bytes(f, K) for f in FMTS) * len(TOKENS)
+    value = nbytes * args.steps / dt / 1e9
+    sample = (f"{rows} of {N} rows per matrix per step (Q8_0/Q4_K/Q5_K/Q6_K, K={K}, T=1,2,4,8), "
+              f"{nbytes / 1e6:.2f} MB packed weights per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 dot, f64 epilogue",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "kquant_gemv_14336x4096_T1-2-4-8 (CPU oracle, row sample)", "sample": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import gguf_block_quant_ggq_gb300 as ggq
+    from gguf_block_quant_ggq_gb300 import _build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    _build.build()
+    ctx = ggq.Context(local)
+    rt = Cudart()
+    hbm_peak, peak_kind = peaks()
+
+    # ---- inputs (seeded; per-rank replica: same workload on every GPU)
+    Wdev = {}
+    for fi, f in enumerate(FMTS):
+        g = syn.rng(KQ["index"], 10 + fi)
+        Wdev[f] = [torch.from_numpy(syn.weights(f, N, K, g)).cuda() for _ in range(ROTATE)]
+    gx = syn.rng(KQ["index"], 200)
+    x_host = {T: torch.from_numpy(syn.activations(T, K, gx)).pin_memory() for T in TOKENS}
+    x_dev = {T: x_host[T].cuda() for T in TOKENS}
+    xq_dev = {T: torch.empty((T, syn.row_bytes("Q8_K", K)), dtype=torch.uint8, device="cuda") for T in TOKENS}
+    y_dev = {(f, T): torch.empty((T, N), dtype=torch.float32, device="cuda") for f in FMTS for T in TOKENS}
+    ctx.reserve(max_tokens=8, max_k=K)
+    # rotate copies: the c-th call on a format uses copy c % ROTATE
+    plan = []
+    for f in FMTS:
+        for c, T in enumerate(TOKENS):
+            plan.append((f, T, c % ROTATE))
+    wbytes = {f: N * syn.row_bytes(f, K) for f in FMTS}
+    step_wbytes = sum(wbytes[f] for f, _, _ in plan)
+    # algorithmic bytes of one GEMV launch: packed W + quantized x + fp32 y
+    alg_bytes = {(f, T): wbytes[f] + T * syn.row_bytes("Q8_K", K) + T * N * 4 for f in FMTS for T in TOKENS}
+
+    kev = [(rt.event(), rt.event()) for _ in plan]
+    stream = torch.cuda.Stream()
+
+    def step(external):
+        s = torch.cuda.current_stream()
+        for T in TOKENS:
+            ctx.quantize_act("Q8_K", x_dev[T], out=xq_dev[T])
+        for j, (f, T, c) in enumerate(plan):
+            rt.record(kev[j][0], s, external)
+            ctx.mul_mat_vec_q(f, Wdev[f][c], N, K, xq_dev[T], T, Y=y_dev[(f, T)])
+            rt.record(kev[j][1], s, external)
+
+    # eager warm-up (sets kernel attributes outside capture), then capture one step
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step(False)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(True)
+    torch.cuda.synchronize()
+
+    t_ev = (rt.event(), rt.event())
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    rt.record(t_ev[0], stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    rt.record(t_ev[1], stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = max_over_ranks(rt.elapsed_ms(*t_ev), world)
+    ms_per_step = total_ms / args.steps
+    value = step_wbytes * world / (ms_per_step / 1e3) / 1e9
+
+    # per-launch GEMV kernel durations (events inside the graph, last replay)
+    per_launch = {}
+    for j, (f, T, c) in enumerate(plan):
+        per_launch[(f, T)] = rt.elapsed_ms(*kev[j])
+    sum_alg = sum(alg_bytes[k] for k in per_launch)
+    sum_ms = sum(per_launch.values())
+    achieved = sum_alg / (sum_ms / 1e3) / 1e9
+    breakdown = {f"{f}_T{T}": {"us": round(ms * 1e3, 2), "GBps": round(alg_bytes[(f, T)] / (ms / 1e3) / 1e9, 1)}
+                 for (f, T), ms in per_launch.items()}
+
+    # ---- end to end through the public API with host buffers
+    y_host = {k: torch.empty(v.shape, dtype=torch.float32).pin_memory() for k, v in y_dev.items()}
+    h2d = sum(x_host[T].numel() * 4 for T in TOKENS)
+    d2h = sum(v.numel() * 4 for v in y_dev.values())
+
+    def e2e_step():
+        for T in TOKENS:
+            x_dev[T].copy_(x_host[T], non_blocking=True)
+        for (f, T, c) in plan:
+            ctx.mul_mat_vec(f, Wdev[f][c], N, K, x_dev[T], Y=y_dev[(f, T)], reserve=False)
+        for k, v in y_dev.items():
+            y_host[k].copy_(v, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ev = (rt.event(), rt.event())
+        rt.record(e_ev[0], stream)
+        for _ in range(args.steps):
+            e2e_step()
+        rt.record(e_ev[1], stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(rt.elapsed_ms(*e_ev), world) / args.steps
+    e2e_value = step_wbytes * world / (e2e_ms / 1e3) / 1e9
+    ctx.sync_status()
+
+    # ---- secondary workloads (1 GPU lines, rank 0 only)
+    workloads = {}
+    if rank == 0 and not args.headline_only:
+        workloads = secondary_workloads(ctx, rt, hbm_peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, secs, _ = oracle_sample_rate()
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(secs, 2)}
+
+    gpu_launches = (len(TOKENS) + len(plan)) * args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a, f32 epilogue", "data": "synthetic (seeded)",
+            "config": {"workload": "kquant_gemv_14336x4096_Q8_0-Q4_K-Q5_K-Q6_K_T1-2-4-8",
+                       "packed_weight_bytes_per_step": step_wbytes,
+                       "l2": f"inputs larger than L2: {ROTATE} rotating copies per format "
+                             f"({sum(wbytes.values()) * ROTATE / 1e6:.0f} MB live), no L2 flush",
+                       "graph": "one step captured in a CUDA graph, replayed",
+                       "fraction_of_hbm": round(value / world / hbm_peak, 4), "peak": f"{hbm_peak} GB/s ({peak_kind})"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                         "kernel": "k_stream<GEMV> (all 16 launches of a step; algorithmic bytes = packed W + "
+                                   "Q8_K x + fp32 y per launch)",
+                         "peak_kind": peak_kind, "per_launch": breakdown},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": gpu_launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "workloads": workloads,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+
+
+def _graph_time(fn, reps, rt, stream, warm=2):
+    """Capture fn() once; return the mean ms of one replay over `reps` replays."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    ev = (rt.event(), rt.event())
+    torch.cuda.synchronize()
+    rt.record(ev[0], stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    rt.record(ev[1], stream)
+    torch.cuda.synchronize()
+    return rt.elapsed_ms(*ev) / reps
+
+
+def secondary_workloads(ctx, rt, hbm_peak):
+    import torch
+
+    out = {}
+    stream = torch.cuda.Stream()
+    # Q4_0 1024 x 4096, T = 1: 64 rotating copies (151 MB) per replay
+    cfg = syn.GEMV_Q4_0
+    Nq, Kq = cfg["N"], cfg["K"]
+    gq = syn.rng(cfg["index"], 0)
+    copies = [torch.from_numpy(syn.weights("Q4_0", Nq, Kq, gq)).cuda() for _ in range(64)]
+    xq4 = torch.from_numpy(syn.activations(1, Kq, syn.rng(cfg["index"], 1))).cuda()
+    y4 = torch.empty((1, Nq), dtype=torch.float32, device="cuda")
+    ctx.reserve(max_tokens=1, max_k=Kq)
+
+    def q4():
+        for Wc in copies:
+            ctx.mul_mat_vec("Q4_0", Wc, Nq, Kq, xq4, Y=y4, reserve=False)
+
+    ms = _graph_time(q4, 5, rt, stream)
+    bytes_ = len(copies) * Nq * syn.row_bytes("Q4_0", Kq)
+    out["q4_0_gemv_1024x4096_T1"] = {"GBps": round(bytes_ / (ms / 1e3) / 1e9, 1),
+                                     "frac": round(bytes_ / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                                     "us_per_call": round(ms * 1e3 / len(copies), 2)}
+    del copies
+
+    # MoE layers: rotate 16 seeded router-logit sets so the expert sets differ per call
+    for cfg, E, Ts in ((syn.MOE_DECODE, syn.MOE_DECODE["E"], (1, 2, 3, 4)),
+                       (syn.MOE_MXFP4, syn.MOE_MXFP4["E"], (1, 2, 3, 4, 5))):
+        H, I, k = cfg["H"], cfg["I"], cfg["k"]
+        g = syn.rng(cfg["index"], 1)
+        banks = [torch.from_numpy(syn.expert_bank(cfg[n], E, r, c, g)).cuda()
+                 for n, r, c in (("gate", I, H), ("up", I, H), ("down", H, I))]
+        w8 = ctx.moe_weights(cfg["gate"], banks[0], cfg["up"], banks[1], cfg["down"], banks[2])
+        per_expert = 2 * I * syn.row_bytes(cfg["gate"], H) + H * syn.row_bytes(cfg["down"], I)
+        for T in Ts:
+            R = 16
+            xs = [torch.from_numpy(syn.activations(T, H, g)).cuda() for _ in range(R)]
+            lgs = [syn.router_logits(T, E, g) for _ in range(R)]
+            # distinct experts per layer: top-k by logit (stable sort keeps ties on the lower index)
+            distinct = sum(len(np.unique(np.argsort(-lg, axis=1, kind="stable")[:, :k])) for lg in lgs)
+            lgd = [torch.from_numpy(lg).cuda() for lg in lgs]
+            ys = torch.empty((T, H), dtype=torch.float32, device="cuda")
+            ctx.reserve(max_tokens=T, n_experts=E, hidden=H, inter=I, top_k=k)
+
+            def moe():
+                for r in range(R):
+                    ctx.moe_experts(w8, E, H, I, k, xs[r], logits=lgd[r], Y=ys, reserve=False)
+
+            ms = _graph_time(moe, 5, rt, stream)
+            gbps = distinct * per_expert / (ms / 1e3) / 1e9
+            name = f"moe_{cfg['gate'].lower()}_{cfg['down'].lower()}_E{E}_H{H}_I{I}_T{T}"
+            out[name] = {"GBps": round(gbps, 1), "frac": round(gbps / hbm_peak, 4),
+                         "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R}
+        del banks
+        torch.cuda.empty_cache()
+    ctx.sync_status()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ggq", choices=["ggq", "reference"])
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

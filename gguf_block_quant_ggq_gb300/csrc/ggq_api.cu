@@ -1,0 +1,523 @@
+// ggq_api.cu -- the C ABI of libggq (include/ggq.h): context, grow-only
+// scratch pool, argument checks, launch planning.
+//
+// Pool discipline follows the review of vllm.cpp PR #523 "grouped +
+// non-grouped keep-quant expert GEMM": no per-call cudaMalloc/cudaFree or
+// stream synchronisation (both illegal under graph capture), a grow-only pool
+// whose old generations are retired rather than freed, per-format availability
+// instead of a boolean, and refusals that name the unsupported formats.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/ggq.h"
+#include "ggq_device.cuh"
+#include "ggq_internal.h"
+
+namespace ggq {
+cudaError_t launch_gemv_a(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_gemv_b(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_moe_gateup(int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_moe_down(int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+
+cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
+    if (kind == KIND_GATEUP) return launch_moe_gateup(fmt, nt, p, grid, smem, s);
+    if (kind == KIND_DOWN) return launch_moe_down(fmt, nt, p, grid, smem, s);
+    if (fmt == F_Q4_0 || fmt == F_Q8_0 || fmt == F_MXFP4) return launch_gemv_a(kind, fmt, nt, p, grid, smem, s);
+    return launch_gemv_b(kind, fmt, nt, p, grid, smem, s);
+}
+}  // namespace ggq
+
+using namespace ggq;
+
+namespace {
+
+constexpr int kCounterInts = 16384;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// Layout of the control block (allocated once at create).
+struct Ctrl {
+    int err;
+    int pad[31];
+    int counters[kCounterInts];
+    MoePlan plan;
+};
+
+int fmt_of(int t) {
+    switch (t) {
+    case GGQ_TYPE_Q4_0: return F_Q4_0;
+    case GGQ_TYPE_Q8_0: return F_Q8_0;
+    case GGQ_TYPE_Q4_K: return F_Q4_K;
+    case GGQ_TYPE_Q5_K: return F_Q5_K;
+    case GGQ_TYPE_Q6_K: return F_Q6_K;
+    case GGQ_TYPE_MXFP4: return F_MXFP4;
+    default: return -1;
+    }
+}
+
+const char* type_name(int t) {
+    switch (t) {
+    case GGQ_TYPE_Q4_0: return "Q4_0";
+    case GGQ_TYPE_Q8_0: return "Q8_0";
+    case GGQ_TYPE_Q8_1: return "Q8_1";
+    case GGQ_TYPE_Q4_K: return "Q4_K";
+    case GGQ_TYPE_Q5_K: return "Q5_K";
+    case GGQ_TYPE_Q6_K: return "Q6_K";
+    case GGQ_TYPE_Q8_K: return "Q8_K";
+    case GGQ_TYPE_MXFP4: return "MXFP4";
+    default: return "unknown";
+    }
+}
+
+int64_t act_row_bytes(bool q81, int64_t K) { return q81 ? K / 32 * 36 : K / 256 * 292; }
+
+int64_t w_row_bytes(int f, int64_t K) { return K / fmt_qk(f) * fmt_bytes(f); }
+
+size_t gemv_scratch(int64_t T, int64_t K) {
+    // quantized X in the wider of the two activation layouts
+    const int64_t q81 = K / 32 * 36, q8k = (K + 255) / 256 * 292;
+    return align_up(static_cast<size_t>(T) * static_cast<size_t>(q81 > q8k ? q81 : q8k));
+}
+
+struct MoeScratch {
+    size_t xq, ids, w, h, hq, o, total;
+};
+
+MoeScratch moe_scratch(int64_t T, int64_t H, int64_t I, int64_t k) {
+    MoeScratch m{};
+    const size_t P = static_cast<size_t>(T * k);
+    size_t off = 0;
+    m.xq = off; off += align_up(static_cast<size_t>(T) * (H / 256) * 292);
+    m.ids = off; off += align_up(P * 4);
+    m.w = off; off += align_up(P * 4);
+    m.h = off; off += align_up(P * static_cast<size_t>(I) * 4);
+    m.hq = off; off += align_up(P * (I / 256) * 292);
+    m.o = off; off += align_up(P * static_cast<size_t>(H) * 4);
+    m.total = off;
+    return m;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+struct ggq_ctx {
+    int device = 0;
+    int nsm = 0;
+    uint8_t* pool = nullptr;
+    size_t pool_bytes = 0;
+    std::vector<void*> retired;
+    Ctrl* ctrl = nullptr;
+    std::string err;
+};
+
+namespace {
+
+ggq_status fail(ggq_ctx* c, ggq_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c) c->err = buf;
+    return s;
+}
+
+ggq_status cuda_fail(ggq_ctx* c, cudaError_t e, const char* what) {
+    return fail(c, GGQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+ggq_status need_scratch(ggq_ctx* c, size_t bytes) {
+    if (bytes <= c->pool_bytes) return GGQ_OK;
+    return fail(c, GGQ_ERR_CAPACITY, "call needs %zu scratch bytes but the pool holds %zu: call ggq_reserve first",
+                bytes, c->pool_bytes);
+}
+
+// Shared-memory plan of one streaming launch.
+struct StreamShape {
+    int stages, stride, x_bytes, smem;
+};
+
+bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s) {
+    s->stride = static_cast<int>(align_up(static_cast<size_t>(stage_bytes) + 16, 128));
+    s->x_bytes = x_region_bytes(xrows, K, q81);
+    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + 64;
+    if (fixed + s->stride > kSmemLimit) return false;
+    s->stages = (kSmemLimit - fixed) / s->stride;
+    if (s->stages > kMaxStages) s->stages = kMaxStages;
+    s->smem = s->stages * s->stride + fixed;
+    return true;
+}
+
+int pow2_tokens(int64_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
+
+ggq_status check_ctx(ggq_ctx* c) {
+    if (!c) return GGQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaSetDevice(c->device);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
+    return GGQ_OK;
+}
+
+ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const void* X, int64_t T,
+                       const void* Y) {
+    const int f = fmt_of(w);
+    if (f < 0 || w == GGQ_TYPE_Q8_1 || w == GGQ_TYPE_Q8_K)
+        return fail(c, GGQ_ERR_UNSUPPORTED,
+                    "mul_mat_vec: weight type %d (%s) is not supported; supported: Q4_0 x Q8_1, and Q8_0, Q4_K, "
+                    "Q5_K, Q6_K, MXFP4 x Q8_K",
+                    w, type_name(w));
+    if (!W || !X || !Y) return fail(c, GGQ_ERR_INVALID_ARG, "mul_mat_vec: null pointer");
+    if (!aligned16(W) || !aligned16(X) || !aligned16(Y))
+        return fail(c, GGQ_ERR_INVALID_ARG, "mul_mat_vec: pointers must be 16-byte aligned");
+    if (T < 1 || T > 8) return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: T=%lld out of 1..8", static_cast<long long>(T));
+    if (N < 1) return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: N=%lld", static_cast<long long>(N));
+    const int64_t ablk = f == F_Q4_0 ? 32 : 256;
+    if (K < 1 || K % fmt_qk(f) || K % ablk)
+        return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld must be a multiple of %lld for %s", static_cast<long long>(K),
+                    static_cast<long long>(ablk > fmt_qk(f) ? ablk : fmt_qk(f)), type_name(w));
+    if (K > (1 << 20)) return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K too large");
+    return GGQ_OK;
+}
+
+ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
+                            int64_t T, float* Y, int32_t* coefs, cudaStream_t st) {
+    const int f = fmt_of(w);
+    StreamParams p{};
+    p.W = static_cast<const uint8_t*>(W);
+    p.rowbytes = w_row_bytes(f, K);
+    p.N = N;
+    p.K = static_cast<int>(K);
+    p.xq = static_cast<const uint8_t*>(Xq);
+    p.xrows = static_cast<int>(T);
+    p.T = static_cast<int>(T);
+    p.Y = Y;
+    p.coefs = coefs;
+    p.err = &c->ctrl->err;
+    StreamShape sh;
+    if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh))
+        return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld with T=%lld does not fit in shared memory",
+                    static_cast<long long>(K), static_cast<long long>(T));
+    p.stages = sh.stages;
+    p.stage_stride = sh.stride;
+    p.x_bytes = sh.x_bytes;
+    const int64_t tiles = (N + kTileRows - 1) / kTileRows;
+    const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
+    cudaError_t e = launch_stream(kind, f, pow2_tokens(T), p, grid, sh.smem, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec launch");
+    return GGQ_OK;
+}
+
+ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k, const float* X,
+                   const float* logits, const int32_t* ids, const float* weights, int64_t T, float* Y,
+                   const ggq_moe_dump* dump, void* stream) {
+    if (!w || !X || !Y || (!logits && (!ids || !weights)))
+        return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null pointer");
+    const int fg = fmt_of(w->gate_type), fu = fmt_of(w->up_type), fd = fmt_of(w->down_type);
+    for (int t : {w->gate_type, w->up_type, w->down_type}) {
+        const int f = fmt_of(t);
+        if (f < 0 || f == F_Q4_0)
+            return fail(c, GGQ_ERR_UNSUPPORTED,
+                        "moe_experts: expert weight type %d (%s) is not supported; supported with Q8_K activations: "
+                        "Q8_0, Q4_K, Q5_K, Q6_K, MXFP4",
+                        t, type_name(t));
+    }
+    if (fg != fu)
+        return fail(c, GGQ_ERR_UNSUPPORTED, "moe_experts: gate (%s) and up (%s) banks must share one format",
+                    type_name(w->gate_type), type_name(w->up_type));
+    if (!w->gate || !w->up || !w->down) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null bank");
+    if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down) || !aligned16(X) || !aligned16(Y))
+        return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: pointers must be 16-byte aligned");
+    if (H < 256 || H % 256 || I < 256 || I % 256)
+        return fail(c, GGQ_ERR_SHAPE, "moe_experts: H=%lld and I=%lld must be positive multiples of 256",
+                    static_cast<long long>(H), static_cast<long long>(I));
+    if (top_k < 1 || top_k > 8 || E < top_k || E > 4096)
+        return fail(c, GGQ_ERR_SHAPE, "moe_experts: need 1 <= top_k <= 8 and top_k <= E <= 4096");
+    if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
+    if (T > kPlanMaxTokens)
+        return fail(c, GGQ_ERR_UNSUPPORTED,
+                    "moe_experts: T=%lld needs the expert-sorted route for more than %d tokens, not built in this "
+                    "library version",
+                    static_cast<long long>(T), kPlanMaxTokens);
+    const MoeScratch ms = moe_scratch(T, H, I, top_k);
+    ggq_status s = need_scratch(c, ms.total);
+    if (s != GGQ_OK) return s;
+    if (I / 256 * kPlanMaxPairs > kCounterInts / 2 || H / kTileRows > kCounterInts / 2)
+        return fail(c, GGQ_ERR_SHAPE, "moe_experts: H or I too large for the counter block");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* xq = c->pool + ms.xq;
+    int32_t* ids_s = reinterpret_cast<int32_t*>(c->pool + ms.ids);
+    float* w_s = reinterpret_cast<float*>(c->pool + ms.w);
+    float* h = reinterpret_cast<float*>(c->pool + ms.h);
+    uint8_t* hq = c->pool + ms.hq;
+    float* o = reinterpret_cast<float*>(c->pool + ms.o);
+    MoePlan* plan = &c->ctrl->plan;
+
+    cudaError_t e = launch_moe_route(logits, ids, weights, X, static_cast<int>(T), static_cast<int>(E), top_k,
+                                     static_cast<int>(H), xq, plan, ids_s, w_s, &c->ctrl->err, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe route launch");
+
+    const int nt = pow2_tokens(T);
+    // gate/up: rows of I, input width H, activations x^ (T rows)
+    {
+        StreamParams p{};
+        p.W = static_cast<const uint8_t*>(w->gate);
+        p.W2 = static_cast<const uint8_t*>(w->up);
+        p.rowbytes = w_row_bytes(fg, H);
+        p.N = I;
+        p.K = static_cast<int>(H);
+        p.xq = xq;
+        p.xrows = static_cast<int>(T);
+        p.T = static_cast<int>(T);
+        p.top_k = top_k;
+        p.plan = plan;
+        p.h = h;
+        p.g_dump = dump ? dump->g : nullptr;
+        p.u_dump = dump ? dump->u : nullptr;
+        p.hq = hq;
+        p.counters = c->ctrl->counters;
+        p.err = &c->ctrl->err;
+        StreamShape sh;
+        if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, false, &sh))
+            return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
+        p.stages = sh.stages;
+        p.stage_stride = sh.stride;
+        p.x_bytes = sh.x_bytes;
+        e = launch_stream(KIND_GATEUP, fg, nt, p, c->nsm, sh.smem, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe gate/up launch");
+    }
+    // down: rows of H, input width I, activations h^ (T*k rows), combine into Y
+    {
+        StreamParams p{};
+        p.W = static_cast<const uint8_t*>(w->down);
+        p.rowbytes = w_row_bytes(fd, I);
+        p.N = H;
+        p.K = static_cast<int>(I);
+        p.xq = hq;
+        p.xrows = static_cast<int>(T * top_k);
+        p.T = static_cast<int>(T);
+        p.top_k = top_k;
+        p.plan = plan;
+        p.o = o;
+        p.Y = Y;
+        p.counters = c->ctrl->counters + kCounterInts / 2;
+        p.err = &c->ctrl->err;
+        StreamShape sh;
+        if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, false, &sh))
+            return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
+        p.stages = sh.stages;
+        p.stage_stride = sh.stride;
+        p.x_bytes = sh.x_bytes;
+        e = launch_stream(KIND_DOWN, fd, nt, p, c->nsm, sh.smem, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe down launch");
+    }
+    if (dump) {
+        const size_t P = static_cast<size_t>(T * top_k);
+        struct Cp { void* dst; const void* src; size_t n; } cps[] = {
+            {dump->ids, ids_s, P * 4},
+            {dump->weights, w_s, P * 4},
+            {dump->xq, xq, static_cast<size_t>(T) * (H / 256) * 292},
+            {dump->h, h, P * I * 4},
+            {dump->hq, hq, P * (I / 256) * 292},
+            {dump->o, o, P * H * 4},
+        };
+        for (const Cp& cp : cps)
+            if (cp.dst) {
+                e = cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToDevice, st);
+                if (e != cudaSuccess) return cuda_fail(c, e, "moe dump copy");
+            }
+    }
+    return GGQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ggq_status ggq_create(ggq_ctx** out, int device) {
+    if (!out) return GGQ_ERR_INVALID_ARG;
+    *out = nullptr;
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess) return GGQ_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return GGQ_ERR_ARCH;
+    e = cudaSetDevice(device);
+    if (e != cudaSuccess) return GGQ_ERR_CUDA;
+    ggq_ctx* c = new ggq_ctx();
+    c->device = device;
+    c->nsm = prop.multiProcessorCount;
+    e = cudaMalloc(&c->ctrl, sizeof(Ctrl));
+    if (e == cudaSuccess) e = cudaMemset(c->ctrl, 0, sizeof(Ctrl));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        if (c->ctrl) cudaFree(c->ctrl);
+        delete c;
+        return GGQ_ERR_CUDA;
+    }
+    *out = c;
+    return GGQ_OK;
+}
+
+ggq_status ggq_destroy(ggq_ctx* c) {
+    if (!c) return GGQ_ERR_INVALID_ARG;
+    cudaSetDevice(c->device);
+    for (void* p : c->retired) cudaFree(p);
+    if (c->pool) cudaFree(c->pool);
+    if (c->ctrl) cudaFree(c->ctrl);
+    delete c;
+    return GGQ_OK;
+}
+
+const char* ggq_last_error(const ggq_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+size_t ggq_scratch_bytes(const ggq_ctx* c) { return c ? c->pool_bytes : 0; }
+
+ggq_status ggq_reserve(ggq_ctx* c, const ggq_plan* plan, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    if (!plan) return fail(c, GGQ_ERR_INVALID_ARG, "reserve: null plan");
+    size_t need = 0;
+    const int64_t T = plan->max_tokens > 0 ? plan->max_tokens : 1;
+    if (plan->max_k > 0) need = gemv_scratch(T, plan->max_k);
+    if (plan->hidden > 0 && plan->inter > 0) {
+        const int64_t k = plan->top_k > 0 ? plan->top_k : 8;
+        const size_t m = moe_scratch(T, plan->hidden, plan->inter, k).total;
+        if (m > need) need = m;
+    }
+    if (need <= c->pool_bytes) return GGQ_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+    if (e != cudaSuccess) return cuda_fail(c, e, "reserve: cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(c, GGQ_ERR_CAPTURE_ALLOC, "reserve: pool must grow to %zu bytes while the stream is capturing",
+                    need);
+    void* p = nullptr;
+    e = cudaMalloc(&p, need);
+    if (e != cudaSuccess) return cuda_fail(c, e, "reserve: cudaMalloc");
+    if (c->pool) c->retired.push_back(c->pool);  // work in flight may still use it
+    c->pool = static_cast<uint8_t*>(p);
+    c->pool_bytes = need;
+    return GGQ_OK;
+}
+
+int ggq_supported(int w, int act, int op) {
+    const int f = fmt_of(w);
+    switch (op) {
+    case GGQ_OP_QUANTIZE_ACT: return act == GGQ_TYPE_Q8_1 || act == GGQ_TYPE_Q8_K;
+    case GGQ_OP_DEQUANT: return f >= 0;
+    case GGQ_OP_MUL_MAT_VEC:
+        if (f < 0) return 0;
+        return f == F_Q4_0 ? act == GGQ_TYPE_Q8_1 : act == GGQ_TYPE_Q8_K;
+    case GGQ_OP_MOE: return f >= 0 && f != F_Q4_0 && act == GGQ_TYPE_Q8_K;
+    default: return 0;
+    }
+}
+
+ggq_status ggq_quantize_act(ggq_ctx* c, int act, const float* x, int64_t T, int64_t K, void* out, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    if (act != GGQ_TYPE_Q8_1 && act != GGQ_TYPE_Q8_K)
+        return fail(c, GGQ_ERR_UNSUPPORTED, "quantize_act: activation type %d (%s); supported: Q8_1, Q8_K", act,
+                    type_name(act));
+    if (!x || !out) return fail(c, GGQ_ERR_INVALID_ARG, "quantize_act: null pointer");
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(out) & 3))
+        return fail(c, GGQ_ERR_INVALID_ARG, "quantize_act: x must be 16-byte and out 4-byte aligned");
+    const int64_t blk = act == GGQ_TYPE_Q8_1 ? 32 : 256;
+    if (T < 0 || K < 0 || K % blk)
+        return fail(c, GGQ_ERR_SHAPE, "quantize_act: K=%lld must be a multiple of %lld", static_cast<long long>(K),
+                    static_cast<long long>(blk));
+    cudaError_t e = launch_quantize(act == GGQ_TYPE_Q8_1 ? 0 : 1, x, T, K, static_cast<uint8_t*>(out),
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GGQ_OK : cuda_fail(c, e, "quantize_act launch");
+}
+
+ggq_status ggq_dequant(ggq_ctx* c, int w, const void* blocks, int64_t rows, int64_t K, float* out, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    const int f = fmt_of(w);
+    if (f < 0)
+        return fail(c, GGQ_ERR_UNSUPPORTED,
+                    "dequant: weight type %d (%s); supported: Q4_0, Q8_0, Q4_K, Q5_K, Q6_K, MXFP4", w, type_name(w));
+    if (!blocks || !out) return fail(c, GGQ_ERR_INVALID_ARG, "dequant: null pointer");
+    if (rows < 0 || K < 0 || K % fmt_qk(f))
+        return fail(c, GGQ_ERR_SHAPE, "dequant: K=%lld must be a multiple of %d", static_cast<long long>(K),
+                    fmt_qk(f));
+    cudaError_t e = launch_dequant(f, static_cast<const uint8_t*>(blocks), rows, K, out,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GGQ_OK : cuda_fail(c, e, "dequant launch");
+}
+
+ggq_status ggq_mul_mat_vec_q(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
+                             float* Y, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    s = gemv_checks(c, w, W, N, K, Xq, T, Y);
+    if (s != GGQ_OK) return s;
+    return launch_gemv_kind(c, KIND_GEMV, w, W, N, K, Xq, T, Y, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+ggq_status ggq_mul_mat_vec(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
+                           float* Y, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    s = gemv_checks(c, w, W, N, K, X, T, Y);
+    if (s != GGQ_OK) return s;
+    s = need_scratch(c, gemv_scratch(T, K));
+    if (s != GGQ_OK) return s;
+    const bool q81 = w == GGQ_TYPE_Q4_0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_quantize(q81 ? 0 : 1, X, T, K, c->pool, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec quantize launch");
+    return launch_gemv_kind(c, KIND_GEMV, w, W, N, K, c->pool, T, Y, nullptr, st);
+}
+
+ggq_status ggq_block_dots(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
+                          int32_t* coefs, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    s = gemv_checks(c, w, W, N, K, Xq, T, coefs);
+    if (s != GGQ_OK) return s;
+    return launch_gemv_kind(c, KIND_DUMP, w, W, N, K, Xq, T, nullptr, coefs, static_cast<cudaStream_t>(stream));
+}
+
+ggq_status ggq_moe_experts(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
+                           const float* X, const float* router_logits, int64_t T, float* Y, const ggq_moe_dump* dump,
+                           void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    if (!router_logits) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null router_logits");
+    return moe_run(c, w, E, H, I, top_k, X, router_logits, nullptr, nullptr, T, Y, dump, stream);
+}
+
+ggq_status ggq_moe_experts_routed(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I,
+                                  int top_k, const float* X, const int32_t* ids, const float* weights, int64_t T,
+                                  float* Y, const ggq_moe_dump* dump, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    if (!ids || !weights) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts_routed: null ids/weights");
+    return moe_run(c, w, E, H, I, top_k, X, nullptr, ids, weights, T, Y, dump, stream);
+}
+
+ggq_status ggq_sync_status(ggq_ctx* c, void* stream) {
+    ggq_status s = check_ctx(c);
+    if (s != GGQ_OK) return s;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(c, e, "sync_status: stream");
+    int word = 0;
+    e = cudaMemcpy(&word, &c->ctrl->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "sync_status: read");
+    if (word != 0) {
+        cudaMemset(&c->ctrl->err, 0, sizeof(int));
+        return fail(c, GGQ_ERR_DEVICE, "device error word %d (%s)", word,
+                    word == DEV_ERR_TIMEOUT ? "a bounded wait ran out" : "invalid routing ids");
+    }
+    return GGQ_OK;
+}
+
+}  // extern "C"

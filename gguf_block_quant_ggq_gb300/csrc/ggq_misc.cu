@@ -1,0 +1,233 @@
+// ggq_misc.cu -- activation quantizer, dequantizer and the decode-size MoE
+// router / planner.
+//
+// Quantizer: the fixed IEEE fp32 sequence d = amax/127, q = round-half-away(x *
+// (1/d)) clamped to +-127 (Q8_1 and Q8_K activation blocks; vllm.cpp PR #523
+// "grouped + non-grouped keep-quant expert GEMM", What changed: activation
+// quantizers).  Dequantizer: the GGUF element formulas (FreeToken PR #136
+// "enable native GGUF kernels on ROCm", Summary: Q4_0 dequantization).
+// Router: softmax top-k with renormalisation; ids are chosen by logit, ties to
+// the lower expert index.
+#include "ggq_device.cuh"
+#include "ggq_internal.h"
+
+namespace ggq {
+
+// ---------------------------------------------------------------- quantize
+
+__global__ void k_quant_q8k(const float* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= nblocks) return;
+    warp_quant_q8k(x + b * 256, out + b * 292, lane);
+}
+
+__global__ void k_quant_q8_1(const float* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= nblocks) return;
+    warp_quant_q8_1(x + b * 32, out + b * 36, lane);
+}
+
+cudaError_t launch_quantize(int act, const float* x, int64_t T, int64_t K, uint8_t* out, cudaStream_t s) {
+    const int64_t nb = T * K / (act == 0 ? 32 : 256);  // act: 0 = Q8_1, 1 = Q8_K
+    if (nb == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = (nb * 32 + threads - 1) / threads;
+    if (act == 0)
+        k_quant_q8_1<<<static_cast<unsigned>(blocks), threads, 0, s>>>(x, nb, out);
+    else
+        k_quant_q8k<<<static_cast<unsigned>(blocks), threads, 0, s>>>(x, nb, out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- dequantize
+
+__device__ __forceinline__ float half_at(const uint8_t* p) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(p[0] | (p[1] << 8))));
+}
+
+// One thread per weight block; element formulas of each GGUF format.
+template <int F>
+__global__ void k_dequant(const uint8_t* __restrict__ blocks, int64_t nblocks, float* __restrict__ out) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= nblocks) return;
+    const uint8_t* b = blocks + i * fmt_bytes(F);
+    float* y = out + i * fmt_qk(F);
+    if constexpr (F == F_Q4_0) {
+        const float d = half_at(b);
+        for (int j = 0; j < 16; ++j) {
+            y[j] = d * static_cast<float>((b[2 + j] & 15) - 8);
+            y[j + 16] = d * static_cast<float>((b[2 + j] >> 4) - 8);
+        }
+    } else if constexpr (F == F_Q8_0) {
+        const float d = half_at(b);
+        for (int j = 0; j < 32; ++j) y[j] = d * static_cast<float>(static_cast<int8_t>(b[2 + j]));
+    } else if constexpr (F == F_MXFP4) {
+        const float sc = e8m0_half_scale(b[0]);
+        const int tab[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
+        for (int j = 0; j < 16; ++j) {
+            y[j] = sc * static_cast<float>(tab[b[1 + j] & 15]);
+            y[j + 16] = sc * static_cast<float>(tab[b[1 + j] >> 4]);
+        }
+    } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
+        const float d = half_at(b), dmin = half_at(b + 2);
+        const uint8_t* sc = b + 4;
+        const uint8_t* qh = b + 16;
+        const uint8_t* qs = b + (F == F_Q4_K ? 16 : 48);
+        for (int s = 0; s < 8; ++s) {
+            int scv, mv;
+            if (s < 4) {
+                scv = sc[s] & 63;
+                mv = sc[s + 4] & 63;
+            } else {
+                scv = (sc[s + 4] & 15) | ((sc[s - 4] >> 6) << 4);
+                mv = (sc[s + 4] >> 4) | ((sc[s] >> 6) << 4);
+            }
+            const float a = d * static_cast<float>(scv), m = dmin * static_cast<float>(mv);
+            for (int l = 0; l < 32; ++l) {
+                const uint8_t byte = qs[32 * (s >> 1) + l];
+                int q = (s & 1) ? (byte >> 4) : (byte & 15);
+                if constexpr (F == F_Q5_K) q += 16 * ((qh[l] >> s) & 1);
+                y[32 * s + l] = a * static_cast<float>(q) - m;
+            }
+        }
+    } else {  // Q6_K
+        const float d = half_at(b + 208);
+        for (int e = 0; e < 256; ++e) {
+            const int h = e >> 7, g = (e >> 5) & 3, l = e & 31;
+            const uint8_t lo = b[64 * h + 32 * (g & 1) + l];
+            const int nib = (g < 2) ? (lo & 15) : (lo >> 4);
+            const int hi = (b[128 + 32 * h + l] >> (2 * g)) & 3;
+            y[e] = d * static_cast<float>(static_cast<int8_t>(b[192 + (e >> 4)])) * static_cast<float>((nib | (hi << 4)) - 32);
+        }
+    }
+}
+
+cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t rows, int64_t K, float* out, cudaStream_t s) {
+    const int64_t nb = rows * (K / fmt_qk(fmt));
+    if (nb == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((nb + 127) / 128);
+    switch (fmt) {
+    case F_Q4_0: k_dequant<F_Q4_0><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    case F_Q8_0: k_dequant<F_Q8_0><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    case F_Q4_K: k_dequant<F_Q4_K><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    case F_Q5_K: k_dequant<F_Q5_K><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    case F_Q6_K: k_dequant<F_Q6_K><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    default: k_dequant<F_MXFP4><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- decode MoE router + planner
+
+// CTA 0: warp t routes token t (softmax top-k by logit, ties to the lower
+// index, weights renormalised over the selected experts), then thread 0 groups
+// the T*k (token, slot) pairs by distinct expert.  Every CTA quantizes a share
+// of the T*H/256 Q8_K blocks of x.
+__global__ void __launch_bounds__(256) k_moe_route(const float* __restrict__ logits, const int32_t* __restrict__ ids_in,
+                                                   const float* __restrict__ w_in, const float* __restrict__ X, int T,
+                                                   int E, int k, int H, uint8_t* __restrict__ xq, MoePlan* plan,
+                                                   int32_t* ids_out, float* w_out, int* err) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // x^ = Q8_K(x): one warp per 256-block, all CTAs
+    {
+        const int nb = T * (H >> 8);
+        for (int b = blockIdx.x * 8 + warp; b < nb; b += gridDim.x * 8)
+            warp_quant_q8k(X + static_cast<int64_t>(b) * 256, xq + static_cast<int64_t>(b) * 292, lane);
+    }
+    if (blockIdx.x != 0) return;
+    __shared__ int s_ids[kPlanMaxPairs];
+    __shared__ float s_w[kPlanMaxPairs];
+    if (warp < T) {
+        const int t = warp;
+        if (logits) {
+            const float* l = logits + static_cast<int64_t>(t) * E;
+            // selection keeps a per-lane bitmask of taken experts (E <= 4096: 128 per lane)
+            uint32_t taken[4] = {0u, 0u, 0u, 0u};
+            float lmax = 0.0f, wsum = 0.0f;
+            float wj[8];
+            int idj[8];
+            for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+                for (int i = 0, e = lane; e < E; ++i, e += 32) {
+                    if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
+                    const float v = l[e];
+                    if (v > bv || (v == bv && e < bi)) {
+                        bv = v;
+                        bi = e;
+                    }
+                }
+#pragma unroll
+                for (int s = 16; s >= 1; s >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
+                    if (ov > bv || (ov == bv && oi < bi)) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+                if ((bi & 31) == lane) {
+                    const int i = bi >> 5;
+                    taken[i >> 5] |= 1u << (i & 31);
+                }
+                if (j == 0) lmax = bv;
+                idj[j] = bi;
+                wj[j] = expf(bv - lmax);
+                wsum += wj[j];
+            }
+            if (lane == 0)
+                for (int j = 0; j < k; ++j) {
+                    s_ids[t * k + j] = idj[j];
+                    s_w[t * k + j] = wj[j] / wsum;
+                }
+        } else if (lane < k) {
+            s_ids[t * k + lane] = ids_in[t * k + lane];
+            s_w[t * k + lane] = w_in[t * k + lane];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int D = 0, bad = 0;
+        for (int pp = 0; pp < T * k; ++pp) {
+            const int e = s_ids[pp];
+            ids_out[pp] = e;
+            w_out[pp] = s_w[pp];
+            plan->wt[pp] = s_w[pp];
+            if (e < 0 || e >= E) {
+                bad = 1;
+                continue;
+            }
+            int u = 0;
+            while (u < D && plan->expert[u] != e) ++u;
+            if (u == D) {
+                plan->expert[D] = e;
+                plan->npairs[D] = 0;
+                ++D;
+            }
+            const int n = plan->npairs[u];
+            if (n < kPlanMaxTokens) {
+                plan->pair[u][n] = pp;
+                plan->token[u][n] = pp / k;
+                plan->npairs[u] = n + 1;
+            } else {
+                bad = 1;  // more than kPlanMaxTokens pairs on one expert
+            }
+        }
+        plan->D = bad ? 0 : D;
+        plan->err = bad;
+        if (bad) set_error(err, 2);
+    }
+}
+
+cudaError_t launch_moe_route(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
+                             int E, int k, int H, uint8_t* xq, MoePlan* plan, int32_t* ids_out, float* w_out,
+                             int* err, cudaStream_t s) {
+    const int nb = T * (H >> 8);
+    const int grid = (nb + 7) / 8 > 1 ? (nb + 7) / 8 : 1;
+    k_moe_route<<<grid, 256, 0, s>>>(logits, ids_in, w_in, X, T, E, k, H, xq, plan, ids_out, w_out, err);
+    return cudaGetLastError();
+}
+
+}  // namespace ggq

@@ -1,0 +1,144 @@
+"""GPU parity of the quantizers, the dequantizer, the integer block dots and the
+decode GEMV (ggq_mul_mat_vec / _q / ggq_block_dots) against the CPU oracle.
+
+Bars: quantized activation bytes and per-block int32 coefficients bit-exact;
+fp32 outputs within 1e-5 * sum |w x| per output and NMSE <= 1e-10."""
+import numpy as np
+import pytest
+
+import ggq_synth as syn
+import oracle as orc
+from tests.gpu_util import check_outputs, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import gguf_block_quant_ggq_gb300 as ggq  # noqa: E402
+
+FORMATS = list(syn.WEIGHT_FORMATS)
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from gguf_block_quant_ggq_gb300 import _build
+    _build.build()
+    orc.set_threads(__import__("os").cpu_count() or 1)
+    c = ggq.Context(0)
+    yield c
+    c.close()
+
+
+def _acts(T, K, seed, scale=1.0):
+    g = syn.rng(50, seed)
+    x = syn.activations(T, K, g) * np.float32(scale)
+    if T > 1:
+        x[1, :32] = 0.0                       # an all-zero Q8_1 block
+        x[-1, 40:48] = np.float32(2.5)        # exact ties of |x| = amax
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("act,K,T", [("Q8_1", 4096, 3), ("Q8_1", 32, 1), ("Q8_K", 4096, 8), ("Q8_K", 256, 5),
+                                     ("Q8_K", 768, 2)])
+def test_quantize_act_bytes_bit_exact(ctx, act, K, T):
+    for scale in (1.0, 1e-3, 300.0):
+        x = _acts(T, K, K + T, scale)
+        got = to_host(ctx.quantize_act(act, to_dev(x)))
+        ref = orc.quantize(act, x)
+        assert np.array_equal(got, ref), f"{act}: {np.count_nonzero(got != ref)} bytes differ"
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_dequant_matches_oracle(ctx, fmt):
+    K = 512 if syn.BLOCK_ELEMS[fmt] == 256 else 96
+    rows = 37
+    W = syn.weights(fmt, rows, K, syn.rng(51, FORMATS.index(fmt)))
+    got = to_host(ctx.dequant(fmt, to_dev(W), rows, K)).astype(np.float64)
+    ref = orc.dequant(fmt, W, rows, K)
+    # fp32 products of exact fp16/int fields: relative error of one or two roundings
+    assert np.all(np.abs(got - ref) <= 3e-7 * (np.abs(ref) + 1e-30) + 1e-12 * np.abs(ref).max())
+
+
+def _case(fmt, N, K, T, seed):
+    g = syn.rng(52, seed)
+    W = syn.weights(fmt, N, K, g)
+    x = _acts(T, K, seed)
+    return W, x
+
+
+SHAPES = [  # (N, K, T): several 16-row tiles with a ragged tail; one and several superblocks
+    (16 * 9 + 5, 1024, 1), (16 * 9 + 5, 1024, 2), (101, 512, 3), (67, 2048, 4), (33, 768, 5), (16 * 20 + 7, 1024, 8),
+    (1, 256, 1), (17, 4096, 6), (50, 256, 7),
+]
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("N,K,T", SHAPES)
+def test_block_dots_bit_exact_and_gemv_within_tolerance(ctx, fmt, N, K, T):
+    W, x = _case(fmt, N, K, T, N * 31 + K + T + FORMATS.index(fmt))
+    act = orc.act_type(fmt)
+    xq = orc.quantize(act, x)
+    dW, dxq = to_dev(W), to_dev(xq)
+    # integer core
+    coefs = to_host(ctx.block_dots(fmt, dW, N, K, dxq, T))
+    ref_coefs = orc.gemv_coefs(fmt, W, N, K, xq, T)
+    assert np.array_equal(coefs, ref_coefs), f"{np.count_nonzero(coefs != ref_coefs)} coefficients differ"
+    # prequantized GEMV and the full call (quantize inside)
+    ref, absdot = orc.gemv_dequant(fmt, W, N, K, xq, T)
+    y_q = to_host(ctx.mul_mat_vec_q(fmt, dW, N, K, dxq, T))
+    check_outputs(y_q, ref, absdot, f"{fmt} mul_mat_vec_q N={N} K={K} T={T}")
+    y = to_host(ctx.mul_mat_vec(fmt, dW, N, K, to_dev(x)))
+    check_outputs(y, ref, absdot, f"{fmt} mul_mat_vec N={N} K={K} T={T}")
+
+
+def test_q4_0_workload_1024x4096(ctx):
+    cfg = syn.GEMV_Q4_0
+    g = syn.rng(cfg["index"], 0)
+    W = syn.weights("Q4_0", cfg["N"], cfg["K"], g)
+    x = syn.activations(1, cfg["K"], syn.rng(cfg["index"], 1))
+    xq = orc.quantize("Q8_1", x)
+    ref, absdot = orc.gemv_dequant("Q4_0", W, cfg["N"], cfg["K"], xq, 1)
+    y = to_host(ctx.mul_mat_vec("Q4_0", to_dev(W), cfg["N"], cfg["K"], to_dev(x)))
+    check_outputs(y, ref, absdot, "Q4_0 1024x4096")
+    assert np.array_equal(to_host(ctx.quantize_act("Q8_1", to_dev(x))), xq)
+
+
+@pytest.mark.parametrize("fmt", ["Q8_0", "Q4_K", "Q5_K", "Q6_K"])
+def test_full_size_14336x4096_sampled_rows(ctx, fmt):
+    """Full workload size in the bench's launch configuration (T = 8 and 1);
+    the oracle computes a sample of rows one by one, including both ends."""
+    cfg = syn.GEMV_KQUANT
+    N, K = cfg["N"], cfg["K"]
+    W = syn.weights(fmt, N, K, syn.rng(cfg["index"], FORMATS.index(fmt)))
+    dW = to_dev(W)
+    rows = np.unique(np.concatenate([[0, 1, 15, 16, N - 17, N - 1], syn.rng(53, 0).integers(0, N, 58)]))
+    for T in (8, 1):
+        x = syn.activations(T, K, syn.rng(cfg["index"], 100 + T))
+        y = to_host(ctx.mul_mat_vec(fmt, dW, N, K, to_dev(x)))
+        xq = orc.quantize("Q8_K", x)
+        Ws = np.ascontiguousarray(W[rows])
+        ref, absdot = orc.gemv_dequant(fmt, Ws, len(rows), K, xq, T)
+        check_outputs(y[:, rows], ref, absdot, f"{fmt} full-size sampled T={T}")
+        assert np.all(np.isfinite(y))
+
+
+def test_errors_are_refused_loudly(ctx):
+    W = to_dev(syn.weights("Q4_K", 16, 256, syn.rng(54, 0)))
+    x = to_dev(np.zeros((9, 256), np.float32))
+    with pytest.raises(ggq.GGQError, match="SHAPE"):
+        ctx.mul_mat_vec("Q4_K", W, 16, 256, x)  # T = 9
+    with pytest.raises(ggq.GGQError, match="SHAPE"):
+        ctx.mul_mat_vec("Q4_K", W, 16, 255, x[:1])
+    with pytest.raises(KeyError):
+        ctx.mul_mat_vec("Q2_K", W, 16, 256, x[:1])
+    h = ggq.load()
+    y = torch.empty((1, 16), dtype=torch.float32, device="cuda")
+    st = h.ggq_mul_mat_vec(ctx.handle, 10, W.data_ptr(), 16, 256, x.data_ptr(), 1, y.data_ptr(), None)
+    assert st == 3 and b"Q2_K" not in h.ggq_last_error(ctx.handle) and b"supported" in h.ggq_last_error(ctx.handle)
+    fresh = ggq.Context(0)
+    try:  # no reserve yet: the call refuses instead of allocating
+        st = h.ggq_mul_mat_vec(fresh.handle, 12, W.data_ptr(), 16, 256, x.data_ptr(), 1, y.data_ptr(), None)
+        assert st == 6
+    finally:
+        fresh.close()
+    ctx.sync_status()
