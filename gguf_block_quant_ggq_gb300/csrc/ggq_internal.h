@@ -12,6 +12,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileRows = 16;
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per CTA
+constexpr int kMaxDevices = 64;     // device ordinals with per-device launch state
 
 // Decode-size MoE plan (T <= 8, so at most 64 (token, slot) pairs).
 constexpr int kPlanMaxPairs = 64;

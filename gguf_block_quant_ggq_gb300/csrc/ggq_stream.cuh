@@ -403,12 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
 
 template <int KIND, int F, int NT>
 cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s) {
-    static bool attr_set = false;  // set once per instantiation, before any capture
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_stream<KIND, F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemLimit);
+    // The dynamic shared-memory limit is a per-device function attribute: set it
+    // on the first launch of each instantiation on each device (before capture).
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(k_stream<KIND, F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     k_stream<KIND, F, NT><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
