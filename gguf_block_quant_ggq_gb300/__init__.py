@@ -39,6 +39,7 @@ SIGNATURES = {
     "ggq_moe_experts": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _P]),
     "ggq_moe_experts_routed": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _P]),
     "ggq_sync_status": (_I32, [_P, _P]),
+    "ggq_mul_mat_vec_noalloc": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _P]),
 }
 
 

@@ -208,6 +208,29 @@ ggq_status ggq_moe_experts_routed(ggq_ctx* ctx, const ggq_moe_weights* w, int64_
                                   int top_k, const float* X, const int32_t* ids, const float* weights, int64_t T,
                                   float* Y, const ggq_moe_dump* dump, void* stream);
 
+/* ggq_mul_mat_vec without a context and without any allocation.  (The pages
+ * have no counterpart of this call; it exists for deployment.)
+ * For callers that cannot allocate device memory: code that runs while a CUDA
+ * graph is being captured in a mode that forbids cudaMalloc, plugins whose
+ * host framework owns every device byte through its own allocator, serving
+ * processes whose HBM is partitioned up front and whose request path may not
+ * allocate, and plain C callers that have nowhere to keep a context (creating
+ * one allocates its control block).
+ * The quantized activations live in a fixed array of 152 KB in the library's
+ * device data, one per device that loads the library, held until the process
+ * exits: T * (K/32 * 36) bytes for w = Q4_0, T * (K/256 * 292) otherwise, which
+ * allows 8 tokens x 16384 inputs.  Larger shapes return GGQ_ERR_CAPACITY and
+ * launch nothing.  Arguments, layouts and results are those of ggq_mul_mat_vec
+ * on the CURRENT device; other errors: GGQ_ERR_UNSUPPORTED, _INVALID_ARG,
+ * _SHAPE, _ARCH (not sm_103), _CUDA.  The first call on a device checks the
+ * architecture and looks up the array's device address; make that first call
+ * before any stream capture.  Every call on a device shares the one array and
+ * it keeps the last call's contents: calls whose work overlaps on the GPU
+ * (other streams, or other host threads) race on it, so order them on one
+ * stream.  Bounded-wait timeouts inside the kernels are not reported here. */
+ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
+                                   void* stream);
+
 /* Synchronise `stream` and read the device error word: GGQ_OK, or
  * GGQ_ERR_DEVICE (a bounded wait inside a kernel ran out; the word is cleared),
  * or GGQ_ERR_CUDA. */
