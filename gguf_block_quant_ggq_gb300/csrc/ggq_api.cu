@@ -10,6 +10,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -105,6 +106,40 @@ MoeScratch moe_scratch(int64_t T, int64_t H, int64_t I, int64_t k) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Expert-sorted route (5 tokens and up): pitched activation rows for the
+// grouped kernel's 16-byte row copies.
+struct SortedScratch {
+    size_t xq, ids, w, counts, offsets, cursor, ngroups, gexp, goff, gcnt, perm, h, hq, o, total;
+};
+
+SortedScratch sorted_scratch(int64_t T, int64_t E, int64_t H, int64_t I, int64_t k) {
+    SortedScratch m{};
+    const size_t P = static_cast<size_t>(T * k);
+    const size_t xp = static_cast<size_t>((H / 256 * 292 + 15) / 16 * 16);
+    const size_t hp = static_cast<size_t>((I / 256 * 292 + 15) / 16 * 16);
+    size_t off = 0;
+    auto take = [&](size_t& field, size_t bytes) {
+        field = off;
+        off += align_up(bytes);
+    };
+    take(m.xq, static_cast<size_t>(T) * xp);
+    take(m.ids, P * 4);
+    take(m.w, P * 4);
+    take(m.counts, static_cast<size_t>(E) * 4);
+    take(m.offsets, static_cast<size_t>(E + 1) * 4);
+    take(m.cursor, static_cast<size_t>(E) * 4);
+    take(m.ngroups, 4);
+    take(m.gexp, static_cast<size_t>(E) * 4);
+    take(m.goff, static_cast<size_t>(E) * 4);
+    take(m.gcnt, static_cast<size_t>(E) * 4);
+    take(m.perm, P * 4);
+    take(m.h, P * static_cast<size_t>(I) * 4);
+    take(m.hq, P * hp);
+    take(m.o, P * static_cast<size_t>(H) * 4);
+    m.total = off;
+    return m;
+}
+
 }  // namespace
 
 struct ggq_ctx {
@@ -147,7 +182,7 @@ struct StreamShape {
 bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s) {
     s->stride = static_cast<int>(align_up(static_cast<size_t>(stage_bytes) + 16, 128));
     s->x_bytes = x_region_bytes(xrows, K, q81);
-    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + 64;
+    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + 1024;
     if (fixed + s->stride > kSmemLimit) return false;
     s->stages = (kSmemLimit - fixed) / s->stride;
     if (s->stages > kMaxStages) s->stages = kMaxStages;
@@ -156,6 +191,41 @@ bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s
 }
 
 int pow2_tokens(int64_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
+
+// Smallest token count that the decode GEMV sends to the grouped int8
+// tensor-core kernel (below it the dp4a streaming kernel is cheaper).
+constexpr int kGroupMinTokens = 3;
+
+// Pad a 16-byte-multiple row so that its stride in 32-bit words is 4 mod 32:
+// eight rows then land on distinct bank quads for the mma fragment loads.
+int bank_stride(int64_t bytes) {
+    const int64_t words = bytes / 4;
+    const int64_t pad = ((4 - words % 32) % 32 + 32) % 32;
+    return static_cast<int>(bytes + 4 * pad);
+}
+
+int64_t q8k_pitch(int64_t K) { return (K / 256 * 292 + 15) / 16 * 16; }
+
+// Shared-memory plan of a grouped launch; false if one weight slot and one
+// activation slot do not fit.
+bool plan_group(GroupParams& p, int nmat, bool resident_x, int* smem) {
+    p.wcontig = (p.rowbytes % 16) != 0;
+    p.wrow = p.wcontig ? static_cast<int>(p.rowbytes) : bank_stride(p.rowbytes);
+    p.wslot = static_cast<int>(align_up(static_cast<size_t>(nmat * kGroupRows * p.wrow + 16), 128));
+    p.xcopy = static_cast<int>((p.K / 256 * 292 + 15) / 16 * 16);
+    p.xstride = bank_stride(p.xcopy);
+    p.xslot = static_cast<int>(align_up(static_cast<size_t>(kGroupCols * p.xstride + 16), 128));
+    const int fixed = kGroupConsumerWarps * nmat * 128 * 4 + 32 * 8 + 64;
+    if (p.wslot + p.xslot + fixed > kSmemLimit) return false;
+    int ws = 4, xs = resident_x ? 1 : 8;
+    while (ws > 1 && ws * p.wslot + 2 * p.xslot + fixed > kSmemLimit) --ws;
+    if (!resident_x)
+        while (xs > 1 && ws * p.wslot + xs * p.xslot + fixed > kSmemLimit) --xs;
+    p.wstages = ws;
+    p.xstages = xs;
+    *smem = ws * p.wslot + xs * p.xslot + fixed;
+    return true;
+}
 
 ggq_status check_ctx(ggq_ctx* c) {
     if (!c) return GGQ_ERR_INVALID_ARG;
@@ -188,6 +258,27 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st) {
     const int f = fmt_of(w);
+    if (kind == KIND_GEMV && T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
+        // several activation columns: the int8 tensor-core kernel (Q8_K rows are 16-byte multiples)
+        GroupParams g{};
+        g.W = static_cast<const uint8_t*>(W);
+        g.rowbytes = w_row_bytes(f, K);
+        g.N = N;
+        g.K = static_cast<int>(K);
+        g.T = static_cast<int>(T);
+        g.xq = static_cast<const uint8_t*>(Xq);
+        g.x_pitch = K / 256 * 292;
+        g.Y = Y;
+        g.err = &c->ctrl->err;
+        int smem = 0;
+        if (plan_group(g, 1, true, &smem)) {
+            const int64_t tiles = (N + kGroupRows - 1) / kGroupRows;
+            const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
+            cudaError_t e = launch_group(G_GEMV, f, g, grid, smem, st);
+            if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec grouped launch");
+            return GGQ_OK;
+        }
+    }
     StreamParams p{};
     p.W = static_cast<const uint8_t*>(W);
     p.rowbytes = w_row_bytes(f, K);
@@ -210,6 +301,103 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
     cudaError_t e = launch_stream(kind, f, pow2_tokens(T), p, grid, sh.smem, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec launch");
+    return GGQ_OK;
+}
+
+// Largest token count on the direct tiny-batch route (ds4 PR #656 "Add ROCm
+// MXFP4 routed expert kernels", Summary: 2-4 tokens go to direct kernels; 5
+// and above use expert-sorted tiles).
+constexpr int kDirectMaxTokens = 4;
+
+ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
+                      const float* X, const float* logits, const int32_t* ids_in, const float* w_in, int64_t T,
+                      float* Y, const ggq_moe_dump* dump, void* stream) {
+    const int fg = fmt_of(w->gate_type), fd = fmt_of(w->down_type);
+    const SortedScratch ms = sorted_scratch(T, E, H, I, top_k);
+    ggq_status s = need_scratch(c, ms.total);
+    if (s != GGQ_OK) return s;
+    if (T * top_k > (int64_t(1) << 30) / std::max<int64_t>(H, I))
+        return fail(c, GGQ_ERR_SHAPE, "moe_experts: T*top_k*max(H, I) too large");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* base = c->pool;
+    auto I32 = [&](size_t off) { return reinterpret_cast<int*>(base + off); };
+    uint8_t* xq = base + ms.xq;
+    uint8_t* hq = base + ms.hq;
+    float* wts = reinterpret_cast<float*>(base + ms.w);
+    float* h = reinterpret_cast<float*>(base + ms.h);
+    float* o = reinterpret_cast<float*>(base + ms.o);
+    const int64_t xp = q8k_pitch(H), hp = q8k_pitch(I);
+    const int P = static_cast<int>(T * top_k);
+
+    cudaError_t e = cudaMemsetAsync(I32(ms.counts), 0, static_cast<size_t>(E) * 4, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: memset");
+    e = launch_route_sorted(logits, ids_in, w_in, X, static_cast<int>(T), static_cast<int>(E), top_k,
+                            static_cast<int>(H), xq, xp, I32(ms.ids), wts, I32(ms.counts), &c->ctrl->err, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: route launch");
+    e = launch_group_plan(I32(ms.counts), static_cast<int>(E), I32(ms.offsets), I32(ms.cursor), I32(ms.ngroups),
+                          I32(ms.gexp), I32(ms.goff), I32(ms.gcnt), st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: plan launch");
+    e = launch_scatter(I32(ms.ids), P, static_cast<int>(E), I32(ms.offsets), I32(ms.cursor), I32(ms.perm), st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: scatter launch");
+
+    GroupParams g{};
+    g.ngroups = I32(ms.ngroups);
+    g.group_expert = I32(ms.gexp);
+    g.group_off = I32(ms.goff);
+    g.group_cnt = I32(ms.gcnt);
+    g.perm = I32(ms.perm);
+    g.top_k = top_k;
+    g.err = &c->ctrl->err;
+    // gate/up + SwiGLU -> h
+    g.W = static_cast<const uint8_t*>(w->gate);
+    g.W2 = static_cast<const uint8_t*>(w->up);
+    g.rowbytes = w_row_bytes(fg, H);
+    g.N = I;
+    g.K = static_cast<int>(H);
+    g.xq = xq;
+    g.x_pitch = xp;
+    g.h = h;
+    g.g_dump = dump ? dump->g : nullptr;
+    g.u_dump = dump ? dump->u : nullptr;
+    int smem = 0;
+    if (!plan_group(g, 2, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
+    e = launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
+    // h^ = Q8_K(h)
+    e = launch_quantize_pitched(h, P, I, hq, hp, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: quantize h launch");
+    // down -> o
+    GroupParams d = g;
+    d.W = static_cast<const uint8_t*>(w->down);
+    d.W2 = nullptr;
+    d.rowbytes = w_row_bytes(fd, I);
+    d.N = H;
+    d.K = static_cast<int>(I);
+    d.xq = hq;
+    d.x_pitch = hp;
+    d.h = nullptr;
+    d.g_dump = d.u_dump = nullptr;
+    d.o = o;
+    if (!plan_group(d, 1, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
+    e = launch_group(G_DOWN, fd, d, c->nsm, smem, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: down launch");
+    e = launch_combine(o, wts, static_cast<int>(T), top_k, H, Y, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: combine launch");
+    if (dump) {
+        const size_t xb = static_cast<size_t>(H / 256 * 292), hb = static_cast<size_t>(I / 256 * 292);
+        if (dump->ids) e = cudaMemcpyAsync(dump->ids, I32(ms.ids), P * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && dump->weights)
+            e = cudaMemcpyAsync(dump->weights, wts, P * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && dump->xq)
+            e = cudaMemcpy2DAsync(dump->xq, xb, xq, xp, xb, T, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && dump->h)
+            e = cudaMemcpyAsync(dump->h, h, static_cast<size_t>(P) * I * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && dump->hq)
+            e = cudaMemcpy2DAsync(dump->hq, hb, hq, hp, hb, P, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && dump->o)
+            e = cudaMemcpyAsync(dump->o, o, static_cast<size_t>(P) * H * 4, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe dump copy");
+    }
     return GGQ_OK;
 }
 
@@ -239,11 +427,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     if (top_k < 1 || top_k > 8 || E < top_k || E > 4096)
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: need 1 <= top_k <= 8 and top_k <= E <= 4096");
     if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
-    if (T > kPlanMaxTokens)
-        return fail(c, GGQ_ERR_UNSUPPORTED,
-                    "moe_experts: T=%lld needs the expert-sorted route for more than %d tokens, not built in this "
-                    "library version",
-                    static_cast<long long>(T), kPlanMaxTokens);
+    if (T > kDirectMaxTokens) return moe_sorted(c, w, E, H, I, top_k, X, logits, ids, weights, T, Y, dump, stream);
     const MoeScratch ms = moe_scratch(T, H, I, top_k);
     ggq_status s = need_scratch(c, ms.total);
     if (s != GGQ_OK) return s;
@@ -387,7 +571,12 @@ ggq_status ggq_reserve(ggq_ctx* c, const ggq_plan* plan, void* stream) {
     if (plan->max_k > 0) need = gemv_scratch(T, plan->max_k);
     if (plan->hidden > 0 && plan->inter > 0) {
         const int64_t k = plan->top_k > 0 ? plan->top_k : 8;
-        const size_t m = moe_scratch(T, plan->hidden, plan->inter, k).total;
+        const int64_t E = plan->n_experts > 0 ? plan->n_experts : 4096;
+        size_t m = moe_scratch(T < kDirectMaxTokens ? T : kDirectMaxTokens, plan->hidden, plan->inter, k).total;
+        if (T > kDirectMaxTokens) {
+            const size_t ms = sorted_scratch(T, E, plan->hidden, plan->inter, k).total;
+            if (ms > m) m = ms;
+        }
         if (m > need) need = m;
     }
     if (need <= c->pool_bytes) return GGQ_OK;

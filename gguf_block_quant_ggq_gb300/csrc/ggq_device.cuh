@@ -2,8 +2,8 @@
 //
 //  * PTX wrappers: mbarrier (bounded waits only), 1-D bulk async copy
 //    (cp.async.bulk, the TMA engine's linear mode) global -> shared.
-//  * Per-format decoders of one 32-weight "chunk" into eight int8x4 words plus
-//    its integer scale fields, and the int8 dp4a integer core per token.
+//  * Per-format decoders of one 64-weight "unit" of a row into sixteen int8x4
+//    words plus its integer scale fields, and the int8 dp4a integer core.
 //  * The activation quantizer (bit-exact IEEE fp32 sequence).
 //  * A warp "transpose reduction" that sums V per-lane partials in V-1 shuffles.
 //
@@ -56,11 +56,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Non-blocking probe of a phase (test_wait never suspends the thread; the
+// blocking try_wait form sleeps for a fixed time slice when the phase is not
+// yet complete, which quantizes short kernels to multiples of that slice).
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)
@@ -68,8 +71,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Bounded: gives up
-// after ~2^32 SM cycles (about 2 s at 2 GHz) and returns false.
+// Wait for the phase with the given parity to complete, polling.  Bounded:
+// gives up after ~2^32 SM cycles (about 2 s at 2 GHz) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
@@ -108,21 +111,54 @@ __device__ __forceinline__ void set_error(int* err, int code) {
     if (err) atomicCAS(err, DEV_OK, code);
 }
 
-// ---------------------------------------------------------------- loads
+// ---------------------------------------------------------------- shared-memory loads
 
-__device__ __forceinline__ uint4 ld128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ float ldh(const uint8_t* p) { return __half2float(*reinterpret_cast<const __half*>(p)); }
+// Hot-path reads of shared memory go through explicit ld.shared on 32-bit
+// shared-window addresses: integer arithmetic on generic pointers (needed for
+// unaligned block layouts) would otherwise turn them into generic loads.
+using saddr = uint32_t;
+
+__device__ __forceinline__ uint32_t ld_s32(saddr a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_s128(saddr a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ int ld_s8(saddr a) {
+    int v;
+    asm volatile("ld.shared.s8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_u8(saddr a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ int ld_s16(saddr a) {
+    int v;
+    asm volatile("ld.shared.s16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float ld_f32(saddr a) { return __uint_as_float(ld_s32(a)); }
+__device__ __forceinline__ float ld_h(saddr a) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v)));
+}
 
 // N consecutive little-endian 32-bit words starting at any byte address of
 // shared memory (reads up to 4 bytes past the end: buffers are padded).
 template <int N>
-__device__ __forceinline__ void ld_words_any(const uint8_t* p, uint32_t* out) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3) * 8u;
+__device__ __forceinline__ void ld_words_any(saddr a, uint32_t* out) {
+    const saddr base = a & ~3u;
+    const uint32_t sh = (a & 3u) * 8u;
     uint32_t w[N + 1];
 #pragma unroll
-    for (int i = 0; i <= N; ++i) w[i] = base[i];
+    for (int i = 0; i <= N; ++i) w[i] = ld_s32(base + 4u * i);
 #pragma unroll
     for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], sh);
 }
@@ -130,25 +166,30 @@ __device__ __forceinline__ void ld_words_any(const uint8_t* p, uint32_t* out) {
 // ---------------------------------------------------------------- activations in shared memory
 
 // Quantized activations, one row per "slot", structure-of-arrays in shared
-// memory so that every 16-element group is one aligned 128-bit load.
+// memory.  Quants are stored with 16 bytes of padding after every 64, so the
+// 64-element runs that consecutive lanes read fall on distinct bank groups.
+// Row stride: 80 bytes per (possibly partial) 64-element unit, a multiple of 16.
+__host__ __device__ constexpr int xq_row_bytes(int K) { return ((K + 63) >> 6) * 80; }
+__device__ __forceinline__ int xq_addr(int e) { return e + ((e >> 6) << 4); }
+
 struct XS {
-    const int8_t* q;     // [rows][K]
-    const float* d;      // [rows][K/ablk]  (ablk = 32 for Q8_1, 256 for Q8_K)
-    const int16_t* bs;   // [rows][K/16]    Q8_K only
-    const int32_t* qs32; // [rows][K/32]    Q8_1 only: sum of the 32 quants
+    saddr q;    // int8 [rows][xq_row_bytes(K)] padded quants
+    saddr d;    // f32 [rows][K/ablk] scales (ablk = 32 for Q8_1, 256 for Q8_K)
+    saddr s32;  // i32 [rows][K/32] sum of the quants of each 32-block
+    saddr bs;   // i16 [rows][K/16] Q8_K sums of 16 (Q8_K only)
     int K;
 };
 
-// ---------------------------------------------------------------- weight chunks
+// ---------------------------------------------------------------- weight units
 
-// 32 weights of one row: eight int8x4 words w[0..3] (16 weights that pair with
-// activations x[xo0 .. xo0+15]) and w[4..7] (pair with x[xo1 .. xo1+15]), plus
-// the block's scale fields.
-struct Chunk {
-    uint32_t w[8];
-    int s0, s1, m0, m1;
-    float da, db;
-    int xo0, xo1;
+// 64 weights of one row, as four groups of 16: w[4g .. 4g+3] are int8x4 words
+// that pair with the activations x[xo[g] .. xo[g]+15].
+struct Unit {
+    uint32_t w[16];
+    int xo[4];
+    int sc[4];     // integer scale per group (K-quants)
+    int mn[2];     // Q4_K/Q5_K mins of the unit's two sub-blocks
+    float da, db;  // K-quants: d and dmin (Q6_K: d); 32-block formats: scale of block 0 and block 1
 };
 
 // E2M1 code -> doubled value + 12, as PRMT tables (codes 0..7 and 8..15).
@@ -170,49 +211,86 @@ __device__ __forceinline__ float e8m0_half_scale(uint32_t e) {
     return __int_as_float(0x7fc00000);
 }
 
-// Decode chunk c (weights 32c .. 32c+31 in the chunk order below) of a row.
+__device__ __forceinline__ float half_lo(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t v) { return half_lo(v >> 16); }
+
+// Number of 64-weight units in a row of K weights (32-block formats may end
+// with a half unit: its second block is absent and contributes nothing).
+__host__ __device__ constexpr int units_per_row(int K) { return (K + 63) >> 6; }
+
+// Decode unit u (weights 64u .. 64u+63 in the order below) of a row.
 template <int F>
-__device__ __forceinline__ void load_chunk(const uint8_t* row, int c, Chunk& ch) {
+__device__ __forceinline__ void load_unit(saddr row, int u, int nblk32, Unit& un) {
     if constexpr (F == F_Q4_0) {
-        const uint8_t* b = row + 18 * c;
-        uint32_t q[4];
-        ld_words_any<4>(b + 2, q);
-        ch.da = ldh(b);
+        // two blocks of 18 B: fp16 d, 16 B nibbles (element j low, j+16 high nibble of byte j)
+        const saddr b = row + 36u * u;
+        const bool two = 2 * u + 1 < nblk32;
+        uint32_t q0[4], q1[4];
+        ld_words_any<4>(b + 2, q0);
+        un.da = ld_h(b);
+        if (two) {
+            ld_words_any<4>(b + 20, q1);
+            un.db = ld_h(b + 18);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q1[k] = 0u;  // absent block: zero words, zero scale
+            un.db = 0.0f;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            ch.w[k] = q[k] & 0x0F0F0F0Fu;
-            ch.w[4 + k] = (q[k] >> 4) & 0x0F0F0F0Fu;
+            un.w[k] = q0[k] & 0x0F0F0F0Fu;
+            un.w[4 + k] = (q0[k] >> 4) & 0x0F0F0F0Fu;
+            un.w[8 + k] = q1[k] & 0x0F0F0F0Fu;
+            un.w[12 + k] = (q1[k] >> 4) & 0x0F0F0F0Fu;
         }
-        ch.xo0 = 32 * c;
-        ch.xo1 = 32 * c + 16;
     } else if constexpr (F == F_Q8_0) {
-        const uint8_t* b = row + 34 * c;
-        ld_words_any<8>(b + 2, ch.w);
-        ch.da = ldh(b);
-        ch.xo0 = 32 * c;
-        ch.xo1 = 32 * c + 16;
+        const saddr b = row + 68u * u;
+        const bool two = 2 * u + 1 < nblk32;
+        ld_words_any<8>(b + 2, un.w);
+        un.da = ld_h(b);
+        if (two) {
+            ld_words_any<8>(b + 36, un.w + 8);
+            un.db = ld_h(b + 34);
+        } else {
+#pragma unroll
+            for (int k = 8; k < 16; ++k) un.w[k] = 0u;
+            un.db = 0.0f;
+        }
     } else if constexpr (F == F_MXFP4) {
         // element j (0..15) = low nibble of byte j, element j+16 = high nibble.
         // The lookup keeps PRMT's nibble order (j, j+16, j+1, j+17, ...); the
         // activations are stored in the same interleaved order.
-        const uint8_t* b = row + 17 * c;
-        uint32_t q[4];
-        ld_words_any<4>(b + 1, q);
-        ch.da = e8m0_half_scale(b[0]);
+        const saddr b = row + 34u * u;
+        const bool two = 2 * u + 1 < nblk32;
+        uint32_t q0[4], q1[4];
+        ld_words_any<4>(b + 1, q0);
+        un.da = e8m0_half_scale(ld_u8(b));
+        if (two) {
+            ld_words_any<4>(b + 18, q1);
+            un.db = e8m0_half_scale(ld_u8(b + 17));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q1[k] = 0u;
+            un.db = 0.0f;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            ch.w[2 * k] = mx_lookup(q[k] & 0xFFFFu);
-            ch.w[2 * k + 1] = mx_lookup(q[k] >> 16);
+            un.w[2 * k] = mx_lookup(q0[k] & 0xFFFFu);
+            un.w[2 * k + 1] = mx_lookup(q0[k] >> 16);
+            un.w[8 + 2 * k] = mx_lookup(q1[k] & 0xFFFFu);
+            un.w[8 + 2 * k + 1] = mx_lookup(q1[k] >> 16);
         }
-        ch.xo0 = 32 * c;
-        ch.xo1 = 32 * c + 16;
     } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
-        const int sb = c >> 3, p = c & 7, cc = p >> 1, hf = p & 1;
-        const uint8_t* b = row + (F == F_Q4_K ? 144 : 176) * sb;
-        const uint4 hd = ld128(b);
-        const uint4 qv = ld128(b + (F == F_Q4_K ? 16 : 48) + 32 * cc + 16 * hf);
-        ch.da = __half2float(__ushort_as_half(static_cast<unsigned short>(hd.x & 0xFFFFu)));
-        ch.db = __half2float(__ushort_as_half(static_cast<unsigned short>(hd.x >> 16)));
+        // unit = sub-blocks 2cc (low nibbles of qs chunk cc) and 2cc+1 (high nibbles)
+        const int sb = u >> 2, cc = u & 3;
+        const saddr b = row + (F == F_Q4_K ? 144u : 176u) * sb;
+        const uint4 hd = ld_s128(b);
+        const saddr qsp = b + (F == F_Q4_K ? 16u : 48u) + 32u * cc;
+        const uint4 qa = ld_s128(qsp), qb = ld_s128(qsp + 16);
+        un.da = half_lo(hd.x);
+        un.db = half_hi(hd.x);
         // all eight 6-bit scales (sc) and mins (m), four per word
         const uint32_t a0 = hd.y, a1 = hd.z, a2 = hd.w;
         const uint32_t sc_lo = a0 & 0x3F3F3F3Fu, m_lo = a1 & 0x3F3F3F3Fu;
@@ -220,94 +298,119 @@ __device__ __forceinline__ void load_chunk(const uint8_t* row, int c, Chunk& ch)
         const uint32_t m_hi = ((a2 >> 4) & 0x0F0F0F0Fu) | ((a1 >> 2) & 0x30303030u);
         const uint32_t scw = cc < 2 ? sc_lo : sc_hi, mw = cc < 2 ? m_lo : m_hi;
         const int sh = 16 * (cc & 1);
-        ch.s0 = (scw >> sh) & 0xFF;
-        ch.s1 = (scw >> (sh + 8)) & 0xFF;
-        ch.m0 = (mw >> sh) & 0xFF;
-        ch.m1 = (mw >> (sh + 8)) & 0xFF;
-        const uint32_t q[4] = {qv.x, qv.y, qv.z, qv.w};
+        const int s0 = (scw >> sh) & 0xFF, s1 = (scw >> (sh + 8)) & 0xFF;
+        un.sc[0] = un.sc[1] = s0;
+        un.sc[2] = un.sc[3] = s1;
+        un.mn[0] = (mw >> sh) & 0xFF;
+        un.mn[1] = (mw >> (sh + 8)) & 0xFF;
+        const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
         if constexpr (F == F_Q4_K) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                ch.w[k] = q[k] & 0x0F0F0F0Fu;
-                ch.w[4 + k] = (q[k] >> 4) & 0x0F0F0F0Fu;
+            for (int k = 0; k < 8; ++k) {
+                un.w[k] = q[k] & 0x0F0F0F0Fu;
+                un.w[8 + k] = (q[k] >> 4) & 0x0F0F0F0Fu;
             }
         } else {
-            const uint4 hv = ld128(b + 16 + 16 * hf);
-            const uint32_t h[4] = {hv.x, hv.y, hv.z, hv.w};
+            const uint4 ha = ld_s128(b + 16), hb = ld_s128(b + 32);
+            const uint32_t hq[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                ch.w[k] = (q[k] & 0x0F0F0F0Fu) | (((h[k] >> (2 * cc)) & 0x01010101u) << 4);
-                ch.w[4 + k] = ((q[k] >> 4) & 0x0F0F0F0Fu) | (((h[k] >> (2 * cc + 1)) & 0x01010101u) << 4);
+            for (int k = 0; k < 8; ++k) {
+                un.w[k] = (q[k] & 0x0F0F0F0Fu) | (((hq[k] >> (2 * cc)) & 0x01010101u) << 4);
+                un.w[8 + k] = ((q[k] >> 4) & 0x0F0F0F0Fu) | (((hq[k] >> (2 * cc + 1)) & 0x01010101u) << 4);
             }
         }
-        ch.xo0 = 256 * sb + 64 * cc + 16 * hf;
-        ch.xo1 = ch.xo0 + 32;
     } else {  // F_Q6_K
         // element 128h + 32g + l: ql[64h + 32(g&1) + l] nibble g>>1, qh[32h + l] bits 2g..2g+1,
-        // scale index (128h + 32g + l)/16.  Chunk p: h = p>>2, g1 = (p>>1)&1, half = p&1;
-        // w[0..3] are group g1 (low nibbles), w[4..7] group g1+2 (high nibbles).
-        const int sb = c >> 3, p = c & 7, h = p >> 2, g1 = (p >> 1) & 1, hf = p & 1;
-        const uint8_t* b = row + 210 * sb;
-        uint32_t ql[4], qh[4];
-        ld_words_any<4>(b + 64 * h + 32 * g1 + 16 * hf, ql);
-        ld_words_any<4>(b + 128 + 32 * h + 16 * hf, qh);
-        const int j0 = 8 * h + 2 * g1 + hf;
-        ch.s0 = static_cast<int8_t>(b[192 + j0]);
-        ch.s1 = static_cast<int8_t>(b[192 + j0 + 4]);
-        ch.da = ldh(b + 208);
+        // scale index (128h + 32g + l)/16.  Unit v = u&3: h = v>>1, g1 = v&1; w[0..7] are
+        // group g1 (low nibbles), w[8..15] group g1+2 (high nibbles).
+        const int sb = u >> 2, v = u & 3, h = v >> 1, g1 = v & 1;
+        const saddr b = row + 210u * sb;
+        uint32_t ql[8], qh[8];
+        ld_words_any<8>(b + 64 * h + 32 * g1, ql);
+        ld_words_any<8>(b + 128 + 32 * h, qh);
+        const int j0 = 8 * h + 2 * g1;
+        un.sc[0] = ld_s8(b + 192 + j0);
+        un.sc[1] = ld_s8(b + 192 + j0 + 1);
+        un.sc[2] = ld_s8(b + 192 + j0 + 4);
+        un.sc[3] = ld_s8(b + 192 + j0 + 5);
+        un.da = ld_h(b + 208);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            ch.w[k] = (ql[k] & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1)) & 0x03030303u) << 4);
-            ch.w[4 + k] = ((ql[k] >> 4) & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1 + 4)) & 0x03030303u) << 4);
+        for (int k = 0; k < 8; ++k) {
+            un.w[k] = (ql[k] & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1)) & 0x03030303u) << 4);
+            un.w[8 + k] = ((ql[k] >> 4) & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1 + 4)) & 0x03030303u) << 4);
         }
-        ch.xo0 = 256 * sb + 128 * h + 32 * g1 + 16 * hf;
-        ch.xo1 = ch.xo0 + 64;
     }
 }
 
-// Integer core of one chunk against activation row `r`: the coefficients A
-// (and B for Q4_K/Q5_K) whose scale epilogue gives the chunk's contribution.
+// x^ element offsets of the unit's four groups.
 template <int F>
-__device__ __forceinline__ void chunk_ints(const Chunk& ch, const XS& xs, int r, int c, int& A, int& B) {
-    const int8_t* xq = xs.q + static_cast<size_t>(r) * xs.K;
-    const uint4 x0 = *reinterpret_cast<const uint4*>(xq + ch.xo0);
-    const uint4 x1 = *reinterpret_cast<const uint4*>(xq + ch.xo1);
-    int S0 = __dp4a(static_cast<int>(ch.w[0]), static_cast<int>(x0.x), 0);
-    S0 = __dp4a(static_cast<int>(ch.w[1]), static_cast<int>(x0.y), S0);
-    S0 = __dp4a(static_cast<int>(ch.w[2]), static_cast<int>(x0.z), S0);
-    S0 = __dp4a(static_cast<int>(ch.w[3]), static_cast<int>(x0.w), S0);
-    int S1 = __dp4a(static_cast<int>(ch.w[4]), static_cast<int>(x1.x), 0);
-    S1 = __dp4a(static_cast<int>(ch.w[5]), static_cast<int>(x1.y), S1);
-    S1 = __dp4a(static_cast<int>(ch.w[6]), static_cast<int>(x1.z), S1);
-    S1 = __dp4a(static_cast<int>(ch.w[7]), static_cast<int>(x1.w), S1);
-    B = 0;
-    if constexpr (F == F_Q4_0) {
-        A = S0 + S1 - 8 * xs.qs32[r * (xs.K >> 5) + c];  // sum (nib - 8) q
-    } else if constexpr (F == F_Q8_0) {
-        A = S0 + S1;
-    } else if constexpr (F == F_MXFP4) {
-        const int16_t* bs = xs.bs + r * (xs.K >> 4);
-        A = S0 + S1 - 12 * (bs[2 * c] + bs[2 * c + 1]);  // tables hold 2*value + 12
-    } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
-        const int16_t* bs = xs.bs + r * (xs.K >> 4);
-        A = ch.s0 * S0 + ch.s1 * S1;
-        B = ch.m0 * bs[ch.xo0 >> 4] + ch.m1 * bs[ch.xo1 >> 4];
-    } else {  // Q6_K: 6-bit codes are stored unsigned; subtract 32 * sum(q) per group
-        const int16_t* bs = xs.bs + r * (xs.K >> 4);
-        A = ch.s0 * (S0 - 32 * bs[ch.xo0 >> 4]) + ch.s1 * (S1 - 32 * bs[ch.xo1 >> 4]);
-    }
-}
-
-// Scale epilogue of chunk c: fp32 contribution of (A, B).
-template <int F>
-__device__ __forceinline__ float chunk_value(const Chunk& ch, const XS& xs, int r, int c, int A, int B) {
-    if constexpr (F == F_Q4_0) {
-        return static_cast<float>(A) * (ch.da * xs.d[r * (xs.K >> 5) + c]);
-    } else if constexpr (F == F_Q8_0 || F == F_MXFP4 || F == F_Q6_K) {
-        return static_cast<float>(A) * (ch.da * xs.d[r * (xs.K >> 8) + (c >> 3)]);
+__device__ __forceinline__ void unit_offsets(int u, int* xo) {
+    if constexpr (F == F_Q6_K) {
+        const int sb = u >> 2, v = u & 3;
+        const int base = 256 * sb + 128 * (v >> 1) + 32 * (v & 1);
+        xo[0] = base;
+        xo[1] = base + 16;
+        xo[2] = base + 64;
+        xo[3] = base + 80;
     } else {
-        const float dx = xs.d[r * (xs.K >> 8) + (c >> 3)];
-        return dx * (ch.da * static_cast<float>(A) - ch.db * static_cast<float>(B));
+#pragma unroll
+        for (int g = 0; g < 4; ++g) xo[g] = 64 * u + 16 * g;
+    }
+}
+
+// Integer core of one unit against activation row r: per-group dp4a sums, then
+// the format's integer coefficients (A, and B for Q4_K/Q5_K mins; for 32-block
+// formats A0/A1 are the two blocks).
+template <int F>
+__device__ __forceinline__ void unit_ints(const Unit& un, const int* xo, const XS& xs, int r, int u, int& A0,
+                                          int& A1) {
+    const saddr xq = xs.q + static_cast<uint32_t>(r * xq_row_bytes(xs.K));
+    int S[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint4 x = ld_s128(xq + xq_addr(xo[g]));
+        int a = __dp4a(static_cast<int>(un.w[4 * g]), static_cast<int>(x.x), 0);
+        a = __dp4a(static_cast<int>(un.w[4 * g + 1]), static_cast<int>(x.y), a);
+        a = __dp4a(static_cast<int>(un.w[4 * g + 2]), static_cast<int>(x.z), a);
+        S[g] = __dp4a(static_cast<int>(un.w[4 * g + 3]), static_cast<int>(x.w), a);
+    }
+    const saddr s32 = xs.s32 + 4u * static_cast<uint32_t>(r * (xs.K >> 5));
+    if constexpr (F == F_Q4_0) {
+        A0 = S[0] + S[1] - 8 * static_cast<int>(ld_s32(s32 + 8 * u));  // sum (nib - 8) q
+        A1 = S[2] + S[3] - 8 * (2 * u + 1 < (xs.K >> 5) ? static_cast<int>(ld_s32(s32 + 8 * u + 4)) : 0);
+    } else if constexpr (F == F_Q8_0) {
+        A0 = S[0] + S[1];
+        A1 = S[2] + S[3];
+    } else if constexpr (F == F_MXFP4) {
+        A0 = S[0] + S[1] - 12 * static_cast<int>(ld_s32(s32 + 8 * u));  // tables hold 2*value + 12
+        A1 = S[2] + S[3] - 12 * (2 * u + 1 < (xs.K >> 5) ? static_cast<int>(ld_s32(s32 + 8 * u + 4)) : 0);
+    } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
+        A0 = un.sc[0] * (S[0] + S[1]) + un.sc[2] * (S[2] + S[3]);
+        A1 = un.mn[0] * static_cast<int>(ld_s32(s32 + 8 * u)) + un.mn[1] * static_cast<int>(ld_s32(s32 + 8 * u + 4));
+    } else {  // Q6_K: 6-bit codes stored unsigned; subtract 32 * sum(q) per group of 16
+        const saddr bs = xs.bs + 2u * static_cast<uint32_t>(r * (xs.K >> 4));
+        A0 = un.sc[0] * (S[0] - 32 * ld_s16(bs + 2 * (xo[0] >> 4))) + un.sc[1] * (S[1] - 32 * ld_s16(bs + 2 * (xo[1] >> 4))) +
+             un.sc[2] * (S[2] - 32 * ld_s16(bs + 2 * (xo[2] >> 4))) + un.sc[3] * (S[3] - 32 * ld_s16(bs + 2 * (xo[3] >> 4)));
+        A1 = 0;
+    }
+}
+
+// Scale epilogue of unit u: fp32 contribution of (A0, A1).
+template <int F>
+__device__ __forceinline__ float unit_value(const Unit& un, const XS& xs, int r, int u, int A0, int A1) {
+    if constexpr (F == F_Q4_0) {
+        const saddr d = xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 5));
+        const float d1 = 2 * u + 1 < (xs.K >> 5) ? ld_f32(d + 8 * u + 4) : 0.0f;
+        return static_cast<float>(A0) * (un.da * ld_f32(d + 8 * u)) + static_cast<float>(A1) * (un.db * d1);
+    } else if constexpr (F == F_Q8_0 || F == F_MXFP4) {
+        const float dx = ld_f32(xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 8) + (u >> 2)));
+        return dx * (static_cast<float>(A0) * un.da + static_cast<float>(A1) * un.db);
+    } else if constexpr (F == F_Q6_K) {
+        const float dx = ld_f32(xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 8) + (u >> 2)));
+        return static_cast<float>(A0) * (dx * un.da);
+    } else {
+        const float dx = ld_f32(xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 8) + (u >> 2)));
+        return dx * (un.da * static_cast<float>(A0) - un.db * static_cast<float>(A1));
     }
 }
 

@@ -5,9 +5,10 @@
 
 namespace ggq {
 
-// Streaming-kernel geometry: eight consumer warps + one producer warp per CTA,
-// two weight rows per consumer warp per stage (16 rows; gate/up: 8 row pairs).
-constexpr int kConsumerWarps = 8;
+// Streaming-kernel geometry: sixteen consumer warps + one producer warp per
+// CTA, one weight row per consumer warp per stage (16 rows; gate/up: 8 gate
+// rows and the 8 matching up rows).
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileRows = 16;
 constexpr int kMaxStages = 8;
@@ -54,19 +55,71 @@ struct StreamParams {
     int x_bytes;        // bytes of the staged-activation region
 };
 
-// Bytes of the structure-of-arrays activation region for `rows` rows of width K.
+// Bytes of the structure-of-arrays activation region for `rows` rows of width
+// K: padded quants (80 bytes per 64-element unit), scales, per-32 sums, Q8_K
+// per-16 sums.
+// Offsets of the parts are the running sums, each rounded up to 128 bytes.
+__host__ __device__ inline size_t x_up128(size_t v) { return (v + 127) / 128 * 128; }
 inline int x_region_bytes(int rows, int K, bool q81) {
-    const size_t q = static_cast<size_t>(rows) * K;
+    const size_t q = static_cast<size_t>(rows) * (((K + 63) / 64) * 80);  // xq_row_bytes
     const size_t d = static_cast<size_t>(rows) * (K / (q81 ? 32 : 256)) * 4;
-    const size_t extra = q81 ? static_cast<size_t>(rows) * (K / 32) * 4 : static_cast<size_t>(rows) * (K / 16) * 2;
-    auto up = [](size_t v) { return (v + 127) / 128 * 128; };
-    return static_cast<int>(up(q) + up(d) + up(extra));
+    const size_t s32 = static_cast<size_t>(rows) * (K / 32) * 4;
+    const size_t bs = q81 ? 0 : static_cast<size_t>(rows) * (K / 16) * 2;
+    return static_cast<int>(x_up128(q) + x_up128(d) + x_up128(s32) + x_up128(bs));
 }
+
+// Grouped tensor-core kernel geometry (ggq_group.cuh).
+constexpr int kGroupConsumerWarps = 8;
+constexpr int kGroupThreads = (kGroupConsumerWarps + 1) * 32;
+constexpr int kGroupCols = 8;   // activation columns per mma n8 chunk
+constexpr int kGroupRows = 16;  // weight rows per item (per matrix)
+
+enum GKind : int { G_GEMV = 0, G_GATEUP = 1, G_DOWN = 2 };
+
+struct GroupParams {
+    const uint8_t* W;    // GEMV matrix, gate bank, or down bank
+    const uint8_t* W2;   // up bank (gate/up only)
+    int64_t rowbytes;    // bytes of one weight row in global
+    int64_t N;           // rows per matrix
+    int K;               // input width (multiple of 256)
+    // groups (MoE): non-empty experts, their column ranges in perm
+    const int* ngroups;
+    const int* group_expert;
+    const int* group_off;
+    const int* group_cnt;
+    const int* perm;     // pairs sorted by expert
+    int top_k;
+    int T;               // GEMV: tokens (columns)
+    // activations: packed Q8_K rows, x_pitch bytes apart in global
+    const uint8_t* xq;
+    int64_t x_pitch;
+    // outputs
+    float* Y;            // GEMV [T][N]
+    float* h;            // gate/up [pairs][N]
+    float* g_dump;
+    float* u_dump;
+    float* o;            // down [pairs][N]
+    int* err;
+    // shared-memory plan
+    int wstages, wslot, wrow, wcontig;  // weight ring: slots, slot bytes, row stride, one contiguous copy
+    int xstages, xslot, xstride, xcopy; // activation ring: slots, slot bytes, row stride, bytes per row copy
+};
 
 // Host launchers (one per kernel family); return the launch error.
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_quantize(int act, const float* x, int64_t T, int64_t K, uint8_t* out, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t rows, int64_t K, float* out, cudaStream_t s);
+cudaError_t launch_group(int kind, int fmt, const GroupParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
+                                    cudaStream_t s);
+cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
+                                int E, int k, int H, uint8_t* xq, int64_t x_pitch, int32_t* ids, float* w,
+                                int* counts, int* err, cudaStream_t s);
+cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
+                              int* group_off, int* group_cnt, cudaStream_t s);
+cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
+                           cudaStream_t s);
+cudaError_t launch_combine(const float* o, const float* w, int T, int k, int64_t H, float* Y, cudaStream_t s);
 cudaError_t launch_moe_route(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
                              int E, int k, int H, uint8_t* xq, MoePlan* plan, int32_t* ids_out, float* w_out,
                              int* err, cudaStream_t s);

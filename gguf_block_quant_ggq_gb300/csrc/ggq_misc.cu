@@ -231,3 +231,207 @@ cudaError_t launch_moe_route(const float* logits, const int32_t* ids_in, const f
 }
 
 }  // namespace ggq
+
+// ---------------------------------------------------------------- expert-sorted route (5 tokens and up)
+
+namespace ggq {
+
+// Q8_K rows written pitch bytes apart (the grouped kernel copies whole rows
+// with 16-byte bulk copies, so its activation rows start on 16-byte marks).
+__global__ void k_quant_q8k_pitched(const float* __restrict__ x, int64_t rows, int nbr, uint8_t* __restrict__ out,
+                                    int64_t pitch) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= rows * nbr) return;
+    const int64_t r = b / nbr, c = b - r * nbr;
+    warp_quant_q8k(x + b * 256, out + r * pitch + c * 292, lane);
+}
+
+cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
+                                    cudaStream_t s) {
+    const int64_t nb = rows * (K / 256);
+    if (nb == 0) return cudaSuccess;
+    k_quant_q8k_pitched<<<static_cast<unsigned>((nb * 32 + 255) / 256), 256, 0, s>>>(x, rows, static_cast<int>(K / 256),
+                                                                                     out, pitch);
+    return cudaGetLastError();
+}
+
+// One warp per token: top-k by logit (ties to the lower index) and the
+// renormalised softmax weights over the selected experts; or copy given ids.
+// Every pair's expert is counted into counts[] (zeroed by the caller).  The
+// remaining warps quantize x to Q8_K rows x_pitch bytes apart.
+__global__ void __launch_bounds__(256) k_route_sorted(const float* __restrict__ logits,
+                                                      const int32_t* __restrict__ ids_in,
+                                                      const float* __restrict__ w_in, const float* __restrict__ X,
+                                                      int T, int E, int k, int H, uint8_t* __restrict__ xq,
+                                                      int64_t x_pitch, int32_t* ids, float* w, int* counts, int* err) {
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    const int nbr = H >> 8;
+    // quantize: all warps, one 256-block each
+    for (int b = gw; b < T * nbr; b += nw) {
+        const int r = b / nbr, c = b - r * nbr;
+        warp_quant_q8k(X + static_cast<int64_t>(b) * 256, xq + r * x_pitch + c * 292, lane);
+    }
+    for (int t = gw; t < T; t += nw) {
+        if (logits) {
+            const float* l = logits + static_cast<int64_t>(t) * E;
+            uint32_t taken[4] = {0u, 0u, 0u, 0u};
+            float lmax = 0.0f, wsum = 0.0f;
+            float wj[8];
+            int idj[8];
+            for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+                for (int i = 0, e = lane; e < E; ++i, e += 32) {
+                    if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
+                    const float v = l[e];
+                    if (v > bv || (v == bv && e < bi)) {
+                        bv = v;
+                        bi = e;
+                    }
+                }
+#pragma unroll
+                for (int sft = 16; sft >= 1; sft >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, sft);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, sft);
+                    if (ov > bv || (ov == bv && oi < bi)) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+                if ((bi & 31) == lane) {
+                    const int i = bi >> 5;
+                    taken[i >> 5] |= 1u << (i & 31);
+                }
+                if (j == 0) lmax = bv;
+                idj[j] = bi;
+                wj[j] = expf(bv - lmax);
+                wsum += wj[j];
+            }
+            if (lane < k) {
+                int id = 0;
+                float wv = 0.0f;
+                for (int j = 0; j < k; ++j)
+                    if (j == lane) {
+                        id = idj[j];
+                        wv = wj[j];
+                    }
+                ids[t * k + lane] = id;
+                w[t * k + lane] = wv / wsum;
+                atomicAdd(&counts[id], 1);
+            }
+        } else if (lane < k) {
+            const int id = ids_in[t * k + lane];
+            ids[t * k + lane] = id;
+            w[t * k + lane] = w_in[t * k + lane];
+            if (id >= 0 && id < E)
+                atomicAdd(&counts[id], 1);
+            else
+                set_error(err, 2);
+        }
+    }
+}
+
+cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
+                                int E, int k, int H, uint8_t* xq, int64_t x_pitch, int32_t* ids, float* w,
+                                int* counts, int* err, cudaStream_t s) {
+    const int warps = T > T * (H >> 8) ? T : T * (H >> 8);
+    const int grid = (warps + 7) / 8 < 1184 ? (warps + 7) / 8 : 1184;
+    k_route_sorted<<<grid > 0 ? grid : 1, 256, 0, s>>>(logits, ids_in, w_in, X, T, E, k, H, xq, x_pitch, ids, w,
+                                                       counts, err);
+    return cudaGetLastError();
+}
+
+// One CTA: exclusive scan of the expert counts, the list of non-empty experts
+// (the groups of the grouped kernel) and zeroed scatter cursors.
+__global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ counts, int E, int* offsets, int* cursor,
+                                                     int* ngroups, int* group_expert, int* group_off, int* group_cnt) {
+    __shared__ int s_sum[1024];
+    __shared__ int s_ne[1024];
+    const int tid = threadIdx.x;
+    const int per = (E + 1023) / 1024;  // experts per thread (E <= 4096)
+    int loc = 0, ne = 0;
+    for (int i = 0; i < per; ++i) {
+        const int e = tid * per + i;
+        if (e < E) {
+            loc += counts[e];
+            ne += counts[e] > 0;
+        }
+    }
+    s_sum[tid] = loc;
+    s_ne[tid] = ne;
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {  // inclusive Hillis-Steele scan
+        const int a = tid >= d ? s_sum[tid - d] : 0, b = tid >= d ? s_ne[tid - d] : 0;
+        __syncthreads();
+        s_sum[tid] += a;
+        s_ne[tid] += b;
+        __syncthreads();
+    }
+    int run = s_sum[tid] - loc, grun = s_ne[tid] - ne;
+    for (int i = 0; i < per; ++i) {
+        const int e = tid * per + i;
+        if (e < E) {
+            const int c = counts[e];
+            offsets[e] = run;
+            cursor[e] = 0;
+            if (c > 0) {
+                group_expert[grun] = e;
+                group_off[grun] = run;
+                group_cnt[grun] = c;
+                ++grun;
+            }
+            run += c;
+        }
+    }
+    if (tid == 1023) {
+        offsets[E] = s_sum[1023];
+        *ngroups = s_ne[1023];
+    }
+}
+
+cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
+                              int* group_off, int* group_cnt, cudaStream_t s) {
+    k_group_plan<<<1, 1024, 0, s>>>(counts, E, offsets, cursor, ngroups, group_expert, group_off, group_cnt);
+    return cudaGetLastError();
+}
+
+// Scatter pair p to its expert's range.  The order inside a range does not
+// matter: every column of the grouped kernel is computed on its own.
+__global__ void k_scatter(const int32_t* __restrict__ ids, int P, int E, const int* __restrict__ offsets, int* cursor,
+                          int* perm) {
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= P) return;
+    const int e = ids[p];
+    if (e < 0 || e >= E) return;  // reported by the route kernel
+    perm[offsets[e] + atomicAdd(&cursor[e], 1)] = p;
+}
+
+cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
+                           cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    k_scatter<<<(P + 255) / 256, 256, 0, s>>>(ids, P, E, offsets, cursor, perm);
+    return cudaGetLastError();
+}
+
+// y[t][n] = sum_j w[t][j] * o[t*k + j][n], slots in order.
+__global__ void k_combine(const float* __restrict__ o, const float* __restrict__ w, int T, int k, int64_t H,
+                          float* __restrict__ Y) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= T * H) return;
+    const int64_t t = i / H, n = i - t * H;
+    float acc = 0.0f;
+    for (int j = 0; j < k; ++j) acc += w[t * k + j] * o[(t * k + j) * H + n];
+    Y[i] = acc;
+}
+
+cudaError_t launch_combine(const float* o, const float* w, int T, int k, int64_t H, float* Y, cudaStream_t s) {
+    const int64_t n = T * H;
+    if (n == 0) return cudaSuccess;
+    k_combine<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(o, w, T, k, H, Y);
+    return cudaGetLastError();
+}
+
+}  // namespace ggq

@@ -109,7 +109,7 @@ extern "C" ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, i
     p.err = nullptr;  // bounded-wait timeouts are not reported by this entry point
     const int stride = static_cast<int>((kTileRows * p.rowbytes + 16 + 127) / 128 * 128);
     const int x_bytes = x_region_bytes(p.xrows, p.K, q81);
-    const int fixed = x_bytes + 2 * kMaxStages * 8 + 64;
+    const int fixed = x_bytes + 2 * kMaxStages * 8 + 1024;
     if (fixed + stride > kSmemLimit) return GGQ_ERR_SHAPE;
     int stages = (kSmemLimit - fixed) / stride;
     if (stages > kMaxStages) stages = kMaxStages;

@@ -6,11 +6,13 @@
 //   * a producer warp streams each item's weight rows (a contiguous byte range
 //     per matrix: rows are stored back to back) into a ring of shared-memory
 //     stages with cp.async.bulk, completion counted on an mbarrier in bytes, so
-//     several tens of KB per SM are in flight without tying up registers;
-//   * eight consumer warps take two rows each per stage; lanes stride over the
-//     rows' 32-weight chunks, unpack nibbles / 6-bit scales in registers and
-//     run the int8 dp4a integer core against the quantized activations, which
-//     were staged once per CTA into shared memory (structure of arrays);
+//     tens of KB per SM are in flight without tying up registers;
+//   * sixteen consumer warps take one row each per stage; each lane decodes
+//     64-weight units of its row (nibbles and 6-bit scales unpacked in
+//     registers, the scale decode paid once per 64 weights) and runs the int8
+//     dp4a integer core against the quantized activations, staged once per
+//     CTA into shared memory (structure of arrays, padded against bank
+//     conflicts);
 //   * per-lane fp32 partials of (row, token) are summed with one transpose
 //     reduction per stage.
 // Every wait is bounded; on timeout the kernel records an error word, drains
@@ -23,103 +25,139 @@ namespace ggq {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
 
+// Shared-memory activation region (layout of x_region_bytes).
+struct XRegion {
+    int8_t* q;
+    float* d;
+    int32_t* s32;
+    int16_t* bs;
+};
+
+__device__ __forceinline__ XRegion x_region(uint8_t* base, int rows, int K, bool q81) {
+    XRegion r;
+    const size_t qb = x_up128(static_cast<size_t>(rows) * xq_row_bytes(K));
+    const size_t db = x_up128(static_cast<size_t>(rows) * (K / (q81 ? 32 : 256)) * 4);
+    const size_t sb = x_up128(static_cast<size_t>(rows) * (K / 32) * 4);
+    r.q = reinterpret_cast<int8_t*>(base);
+    r.d = reinterpret_cast<float*>(base + qb);
+    r.s32 = reinterpret_cast<int32_t*>(base + qb + db);
+    r.bs = reinterpret_cast<int16_t*>(base + qb + db + sb);
+    return r;
+}
+
 // Stage packed activation blocks (Q8_K: 292 B, or Q8_1: 36 B) from global into
 // the structure-of-arrays region.  PERM stores each 32-block's quants in the
-// interleaved order (0,16,1,17,...) that the MXFP4 lookup produces.
+// interleaved order (0,16,1,17,...) that the MXFP4 lookup produces.  The Q8_1
+// per-32 sums must be zero on entry (they are accumulated with atomics).
 template <bool Q81, bool PERM>
-__device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, int8_t* q, float* d, int16_t* bs,
-                           int32_t* qs32, int tid, int nthr) {
+__device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, const XRegion& x, int tid, int nthr) {
+    const int rb = xq_row_bytes(K);
     if constexpr (!Q81) {
-        const int nb = rows * (K >> 8);
+        const int nbr = K >> 8;
+        const int nb = rows * nbr;
         const int words = nb * 73;
         for (int i = tid; i < words; i += nthr) {
             const int b = i / 73, w = i - b * 73;
             const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(b) * 292) + w);
+            const int row = b / nbr, cb = b - row * nbr;
             if (w == 0) {
-                d[b] = __uint_as_float(v);
+                x.d[b] = __uint_as_float(v);
             } else if (w <= 64) {
-                int8_t* dq = q + static_cast<size_t>(b) * 256;
-                const int e = 4 * (w - 1);
+                int8_t* dq = x.q + static_cast<size_t>(row) * rb;
+                const int e = 256 * cb + 4 * (w - 1);
                 if constexpr (!PERM) {
-                    *reinterpret_cast<uint32_t*>(dq + e) = v;
+                    *reinterpret_cast<uint32_t*>(dq + xq_addr(e)) = v;
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int el = e + j, r = el & 31;
-                        dq[(el & ~31) + 2 * (r & 15) + (r >> 4)] = static_cast<int8_t>((v >> (8 * j)) & 0xFF);
+                        dq[xq_addr((el & ~31) + 2 * (r & 15) + (r >> 4))] = static_cast<int8_t>((v >> (8 * j)) & 0xFF);
                     }
                 }
             } else {
-                reinterpret_cast<uint32_t*>(bs + static_cast<size_t>(b) * 16)[w - 65] = v;
+                const int j = w - 65;  // bsums 2j, 2j+1 of block b
+                reinterpret_cast<uint32_t*>(x.bs + static_cast<size_t>(b) * 16)[j] = v;
+                x.s32[static_cast<size_t>(b) * 8 + j] =
+                    static_cast<int>(static_cast<int16_t>(v & 0xFFFFu)) + static_cast<int>(static_cast<int16_t>(v >> 16));
             }
         }
     } else {
-        const int nb = rows * (K >> 5);
+        const int nbr = K >> 5;
+        const int nb = rows * nbr;
         const int words = nb * 9;
         for (int i = tid; i < words; i += nthr) {
             const int b = i / 9, w = i - b * 9;
             const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(b) * 36) + w);
             if (w == 0) {
-                d[b] = __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+                x.d[b] = half_lo(v);
             } else {
-                reinterpret_cast<uint32_t*>(q + static_cast<size_t>(b) * 32)[w - 1] = v;
-                int s = __dp4a(static_cast<int>(v), 0x01010101, 0);
-                atomicAdd(&qs32[b], s);
+                const int row = b / nbr, cb = b - row * nbr;
+                *reinterpret_cast<uint32_t*>(x.q + static_cast<size_t>(row) * rb + xq_addr(32 * cb + 4 * (w - 1))) = v;
+                atomicAdd(&x.s32[b], __dp4a(static_cast<int>(v), 0x01010101, 0));
             }
         }
     }
 }
 
+// Accumulate one row against the activation rows xr[0..nslots) into acc[].
 template <int F, int NT>
-__device__ __forceinline__ void row_accumulate(const uint8_t* row, const XS& xs, const int* xr, int nslots,
+__device__ __forceinline__ void row_accumulate(saddr row, const XS& xs, const int* xr, int nslots,
                                                float* acc, int lane) {
-    const int nc = xs.K >> 5;
-    for (int c = lane; c < nc; c += 32) {
-        Chunk ch;
-        load_chunk<F>(row, c, ch);
+    const int nu = units_per_row(xs.K), nb32 = xs.K >> 5;
+    for (int u = lane; u < nu; u += 32) {
+        Unit un;
+        load_unit<F>(row, u, nb32, un);
+        int xo[4];
+        unit_offsets<F>(u, xo);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             if (j < nslots) {
-                int A, B;
-                chunk_ints<F>(ch, xs, xr[j], c, A, B);
-                acc[j] += chunk_value<F>(ch, xs, xr[j], c, A, B);
+                int A0, A1;
+                unit_ints<F>(un, xo, xs, xr[j], u, A0, A1);
+                acc[j] += unit_value<F>(un, xs, xr[j], u, A0, A1);
             }
         }
     }
 }
 
-// Integer coefficients of one row for the dump.
+// Integer coefficients of one row for the dump: out[j][row_index][...].
 template <int F, int NT>
-__device__ __forceinline__ void row_coefs(const uint8_t* row, const XS& xs, int nslots, int64_t row_index,
+__device__ __forceinline__ void row_coefs(saddr row, const XS& xs, int nslots, int64_t row_index,
                                           int64_t N, int32_t* out, int lane) {
-    const int nc = xs.K >> 5;
+    const int nu = units_per_row(xs.K), nb32 = xs.K >> 5;
     const int ncoef = (xs.K / fmt_qk(F)) * fmt_coefs(F);
-    for (int c0 = 0; c0 < nc; c0 += 32) {
-        const int c = c0 + lane;
-        const bool valid = c < nc;
-        Chunk ch;
-        if (valid) load_chunk<F>(row, c, ch);
+    for (int u0 = 0; u0 < nu; u0 += 32) {
+        const int u = u0 + lane;
+        const bool valid = u < nu;
+        Unit un;
+        int xo[4];
+        if (valid) {
+            load_unit<F>(row, u, nb32, un);
+            unit_offsets<F>(u, xo);
+        }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             if (j < nslots) {
-                int A = 0, B = 0;
-                if (valid) chunk_ints<F>(ch, xs, j, c, A, B);
+                int A0 = 0, A1 = 0;
+                if (valid) unit_ints<F>(un, xo, xs, j, u, A0, A1);
                 int32_t* o = out + (static_cast<int64_t>(j) * N + row_index) * ncoef;
                 if constexpr (fmt_qk(F) == 32) {
-                    if (valid) o[c] = A;
-                } else {
-                    // the 8 chunks of a superblock sit on 8 consecutive lanes
-#pragma unroll
-                    for (int s = 1; s < 8; s <<= 1) {
-                        A += __shfl_xor_sync(0xffffffffu, A, s);
-                        B += __shfl_xor_sync(0xffffffffu, B, s);
+                    if (valid) {
+                        o[2 * u] = A0;
+                        if (2 * u + 1 < nb32) o[2 * u + 1] = A1;
                     }
-                    if (valid && (c & 7) == 0) {
+                } else {
+                    // the four units of a superblock sit on four consecutive lanes
+                    A0 += __shfl_xor_sync(0xffffffffu, A0, 1);
+                    A1 += __shfl_xor_sync(0xffffffffu, A1, 1);
+                    A0 += __shfl_xor_sync(0xffffffffu, A0, 2);
+                    A1 += __shfl_xor_sync(0xffffffffu, A1, 2);
+                    if (valid && (u & 3) == 0) {
                         if constexpr (fmt_coefs(F) == 2) {
-                            o[2 * (c >> 3)] = A;
-                            o[2 * (c >> 3) + 1] = B;
+                            o[2 * (u >> 2)] = A0;
+                            o[2 * (u >> 2) + 1] = A1;
                         } else {
-                            o[c >> 3] = A;
+                            o[u >> 2] = A0;
                         }
                     }
                 }
@@ -132,22 +170,19 @@ template <int KIND, int F, int NT>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool Q81 = fmt_q81(F);
-    constexpr int LV = NT == 1 ? 1 : NT == 2 ? 2 : NT == 4 ? 3 : 4;  // log2(2 * NT)
+    constexpr int LV = NT == 1 ? 0 : NT == 2 ? 1 : NT == 4 ? 2 : 3;  // log2(NT)
+    constexpr int SH = 5 - LV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- shared memory layout: ring | activations | barriers | misc
     uint8_t* ring = smem;
     uint8_t* xreg = smem + static_cast<size_t>(p.stages) * p.stage_stride;
     const int K = p.K;
-    const size_t qbytes = (static_cast<size_t>(p.xrows) * K + 127) / 128 * 128;
-    const size_t dbytes = (static_cast<size_t>(p.xrows) * (K / (Q81 ? 32 : 256)) * 4 + 127) / 128 * 128;
-    int8_t* xs_q = reinterpret_cast<int8_t*>(xreg);
-    float* xs_d = reinterpret_cast<float*>(xreg + qbytes);
-    int16_t* xs_bs = reinterpret_cast<int16_t*>(xreg + qbytes + dbytes);
-    int32_t* xs_s32 = reinterpret_cast<int32_t*>(xreg + qbytes + dbytes);
+    const XRegion xr_ = x_region(xreg, p.xrows, K, Q81);
     uint64_t* full = reinterpret_cast<uint64_t*>(xreg + p.x_bytes);
     uint64_t* empty = full + kMaxStages;
     int* s_flag = reinterpret_cast<int*>(empty + kMaxStages);  // [0] last-CTA flag, [1] abort
+    float* s_gu = reinterpret_cast<float*>(s_flag + 4);        // [2][8][NT] gate/up exchange
 
     // ---- work items
     int nitems;
@@ -161,7 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         D = p.plan->D;
         nitems = D * static_cast<int>(p.N / kTileRows);
     }
-
     if (static_cast<int>(blockIdx.x) >= nitems) return;  // whole CTA idle (uniform)
 
     if (tid == 0) {
@@ -174,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         fence_barrier_init();
     }
     if constexpr (Q81) {
-        for (int i = tid; i < p.xrows * (K >> 5); i += kThreads) xs_s32[i] = 0;
+        for (int i = tid; i < p.xrows * (K >> 5); i += kThreads) xr_.s32[i] = 0;
     }
     __syncthreads();
 
@@ -183,13 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int j = 0;
-            bool ok = true;
-            for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++j) {
+            for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
                 const int s = j % p.stages;
                 const uint32_t ph = static_cast<uint32_t>(j / p.stages) & 1u;
                 if (!mbar_wait(&empty[s], ph ^ 1u)) {
                     set_error(p.err, DEV_ERR_TIMEOUT);
-                    ok = false;
                     break;
                 }
                 const uint8_t* src[2];
@@ -243,16 +275,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         return;
     }
 
-    // ================= consumers (256 threads)
+    // ================= consumers (512 threads)
     const int ctid = tid;
-    stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xs_q, xs_d, xs_bs, xs_s32, ctid, kConsumerWarps * 32);
+    stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
     consumer_sync();
     XS xs;
-    xs.q = xs_q;
-    xs.d = xs_d;
-    xs.bs = xs_bs;
-    xs.qs32 = xs_s32;
+    xs.q = smem_addr(xr_.q);
+    xs.d = smem_addr(xr_.d);
+    xs.s32 = smem_addr(xr_.s32);
+    xs.bs = smem_addr(xr_.bs);
     xs.K = K;
+    const saddr ring_s = smem_addr(ring);
 
     int j = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
@@ -263,37 +296,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
             set_error(p.err, DEV_ERR_TIMEOUT);
             s_flag[1] = 1;
         }
-        const uint8_t* stage = ring + static_cast<size_t>(s) * p.stage_stride;
+        const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
 
         if constexpr (KIND == KIND_GEMV || KIND == KIND_DUMP) {
-            const int64_t r0 = static_cast<int64_t>(item) * kTileRows;
+            const int64_t r = static_cast<int64_t>(item) * kTileRows + warp;
             int xr[NT];
 #pragma unroll
             for (int t = 0; t < NT; ++t) xr[t] = t;
-            if (ready) {
+            if (ready && r < p.N) {
                 if constexpr (KIND == KIND_GEMV) {
-                    float acc[2 * NT];
+                    float acc[NT];
 #pragma unroll
-                    for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        const int64_t r = r0 + 2 * warp + g;
-                        if (r < p.N)
-                            row_accumulate<F, NT>(stage + (2 * warp + g) * p.rowbytes, xs, xr, p.T, acc + g * NT,
-                                                  lane);
-                    }
+                    for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
+                    row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, p.T, acc, lane);
                     const float v = warp_transpose_reduce<LV>(acc, lane);
-                    const int idx = lane >> (5 - LV);  // = g * NT + t
-                    const int g = idx / NT, t = idx - g * NT;
-                    const int64_t r = r0 + 2 * warp + g;
-                    if ((lane & ((1 << (5 - LV)) - 1)) == 0 && t < p.T && r < p.N) p.Y[t * p.N + r] = v;
+                    const int t = lane >> SH;
+                    if ((lane & ((1 << SH) - 1)) == 0 && t < p.T) p.Y[t * p.N + r] = v;
                 } else {
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        const int64_t r = r0 + 2 * warp + g;
-                        if (r < p.N)
-                            row_coefs<F, NT>(stage + (2 * warp + g) * p.rowbytes, xs, p.T, r, p.N, p.coefs, lane);
-                    }
+                    row_coefs<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, p.T, r, p.N, p.coefs, lane);
                 }
             }
             __syncwarp();
@@ -302,34 +322,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
             const int nt = static_cast<int>(p.N / (kTileRows / 2));
             const int u = item / nt, tile = item - u * nt;
             const int np = p.plan->npairs[u];
-            int xr[NT], pr[NT];
+            int xr[NT];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                xr[t] = t < np ? p.plan->token[u][t] : 0;
-                pr[t] = t < np ? p.plan->pair[u][t] : 0;
-            }
-            const int64_t row = static_cast<int64_t>(tile) * (kTileRows / 2) + warp;
+            for (int t = 0; t < NT; ++t) xr[t] = t < np ? p.plan->token[u][t] : 0;
+            const int half = warp >> 3, rr = warp & 7;  // warps 0..7: gate rows, 8..15: up rows
             if (ready) {
-                float acc[2 * NT];
+                float acc[NT];
 #pragma unroll
-                for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
-                row_accumulate<F, NT>(stage + warp * p.rowbytes, xs, xr, np, acc, lane);                       // gate
-                row_accumulate<F, NT>(stage + (kTileRows / 2 + warp) * p.rowbytes, xs, xr, np, acc + NT, lane);  // up
+                for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
+                row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
                 const float v = warp_transpose_reduce<LV>(acc, lane);
-                const int sh = 5 - LV;
-                const float uval = __shfl_down_sync(0xffffffffu, v, NT << sh);
-                const int idx = lane >> sh;
-                if ((lane & ((1 << sh) - 1)) == 0 && idx < NT && idx < np) {
-                    const float gval = v;
+                const int t = lane >> SH;
+                if ((lane & ((1 << SH) - 1)) == 0) s_gu[(half * 8 + rr) * NT + t] = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            consumer_sync();
+            if (ready && ctid < 8 * NT) {
+                const int row_l = ctid / NT, t = ctid - row_l * NT;
+                if (t < np) {
+                    const float gval = s_gu[row_l * NT + t], uval = s_gu[(8 + row_l) * NT + t];
                     const float hval = __fmul_rn(__fdiv_rn(gval, 1.0f + expf(-gval)), uval);
-                    const int64_t o = static_cast<int64_t>(pr[idx]) * p.N + row;
+                    const int64_t o = static_cast<int64_t>(p.plan->pair[u][t]) * p.N +
+                                      static_cast<int64_t>(tile) * (kTileRows / 2) + row_l;
                     p.h[o] = hval;
                     if (p.g_dump) p.g_dump[o] = gval;
                     if (p.u_dump) p.u_dump[o] = uval;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
             // last CTA to finish a 256-row block of this expert quantizes h there
             __threadfence();
             consumer_sync();
@@ -357,18 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
 #pragma unroll
             for (int t = 0; t < NT; ++t) xr[t] = t < np ? p.plan->pair[u][t] : 0;
             if (ready) {
-                float acc[2 * NT];
+                float acc[NT];
 #pragma unroll
-                for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
-#pragma unroll
-                for (int g = 0; g < 2; ++g)
-                    row_accumulate<F, NT>(stage + (2 * warp + g) * p.rowbytes, xs, xr, np, acc + g * NT, lane);
+                for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
+                row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
                 const float v = warp_transpose_reduce<LV>(acc, lane);
-                const int sh = 5 - LV;
-                const int idx = lane >> sh;
-                const int g = idx / NT, t = idx - g * NT;
-                if ((lane & ((1 << sh) - 1)) == 0 && t < np) {
-                    const int64_t r = static_cast<int64_t>(tile) * kTileRows + 2 * warp + g;
+                const int t = lane >> SH;
+                if ((lane & ((1 << SH) - 1)) == 0 && t < np) {
+                    const int64_t r = static_cast<int64_t>(tile) * kTileRows + warp;
                     p.o[static_cast<int64_t>(xr[t]) * p.N + r] = v;
                 }
             }

@@ -69,7 +69,9 @@ def _case(fmt, N, K, T, seed):
 SHAPES = [  # (N, K, T): several 16-row tiles with a ragged tail; one and several superblocks
     (16 * 9 + 5, 1024, 1), (16 * 9 + 5, 1024, 2), (101, 512, 3), (67, 2048, 4), (33, 768, 5), (16 * 20 + 7, 1024, 8),
     (1, 256, 1), (17, 4096, 6), (50, 256, 7),
+    (16 * 11 + 3, 1024, 3), (40, 2048, 5), (16 * 9 + 9, 3072, 7),  # int8 tensor-core route (K % 1024 == 0)
 ]
+Q4_0_ODD_SHAPES = [(21, 96, 2), (40, 32, 1), (35, 160, 8)]  # K % 64 == 32: a half 64-weight unit per row
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -89,6 +91,16 @@ def test_block_dots_bit_exact_and_gemv_within_tolerance(ctx, fmt, N, K, T):
     check_outputs(y_q, ref, absdot, f"{fmt} mul_mat_vec_q N={N} K={K} T={T}")
     y = to_host(ctx.mul_mat_vec(fmt, dW, N, K, to_dev(x)))
     check_outputs(y, ref, absdot, f"{fmt} mul_mat_vec N={N} K={K} T={T}")
+
+
+@pytest.mark.parametrize("N,K,T", Q4_0_ODD_SHAPES)
+def test_q4_0_widths_with_a_half_unit(ctx, N, K, T):
+    W, x = _case("Q4_0", N, K, T, 7 * N + K)
+    xq = orc.quantize("Q8_1", x)
+    dW, dxq = to_dev(W), to_dev(xq)
+    assert np.array_equal(to_host(ctx.block_dots("Q4_0", dW, N, K, dxq, T)), orc.gemv_coefs("Q4_0", W, N, K, xq, T))
+    ref, absdot = orc.gemv_dequant("Q4_0", W, N, K, xq, T)
+    check_outputs(to_host(ctx.mul_mat_vec("Q4_0", dW, N, K, to_dev(x))), ref, absdot, f"Q4_0 N={N} K={K} T={T}")
 
 
 def test_q4_0_workload_1024x4096(ctx):

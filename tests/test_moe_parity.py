@@ -62,7 +62,11 @@ def _dump_buffers(T, k, H, I):
     }
 
 
-def _run_and_check(ctx, cfg, E, T, routed=False, seed=0):
+def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
+    """Run the layer with every dump, then check stage by stage.  With
+    sample_tokens, the per-pair oracle checks cover only the pairs of that many
+    seeded tokens (routing is per token, so a token's whole layer can be
+    recomputed on its own); ids, weights, x^ and h^ are always checked in full."""
     H, I, k = cfg["H"], cfg["I"], cfg["k"]
     host, dev = _banks(cfg, E)
     g = syn.rng(cfg["index"], 2000 + 17 * T + seed)
@@ -79,6 +83,8 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0):
     ctx.sync_status()
     y = to_host(y).astype(np.float64)
     r = {n: to_host(t) for n, t in d.items()}
+    toks = np.arange(T) if sample_tokens is None else np.unique(
+        np.concatenate([[0, T - 1], syn.rng(61, T).integers(0, T, sample_tokens)]))
 
     # (i) routing
     assert np.array_equal(r["ids"], ids_ref)
@@ -87,39 +93,42 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0):
     xq = orc.quantize("Q8_K", x)
     assert np.array_equal(r["xq"], xq)
     P = T * k
-    for p in range(P):
+    pairs = np.array([t * k + j for t in toks for j in range(k)])
+    for p in pairs:
         t, e = p // k, int(ids_ref.flat[p])
         gref, gabs = orc.gemv_dequant(cfg["gate"], host["gate"][e], I, H, xq[t:t + 1], 1)
         uref, uabs = orc.gemv_dequant(cfg["up"], host["up"][e], I, H, xq[t:t + 1], 1)
         check_outputs(r["g"][p][None], gref, gabs, f"gate pair {p}")
         check_outputs(r["u"][p][None], uref, uabs, f"up pair {p}")
-    gg, uu = r["g"].astype(np.float64), r["u"].astype(np.float64)
+    gg, uu = r["g"][pairs].astype(np.float64), r["u"][pairs].astype(np.float64)
     h64 = gg / (1.0 + np.exp(-gg)) * uu
-    assert np.all(np.abs(r["h"] - h64) <= 6e-7 * np.abs(h64) + 1e-30)
-    # (iii) h^ = Q8_K(h) bit-exact on the GPU's own h
+    assert np.all(np.abs(r["h"][pairs] - h64) <= 6e-7 * np.abs(h64) + 1e-30)
+    # (iii) h^ = Q8_K(h) bit-exact on the GPU's own h (every pair)
     assert np.array_equal(orc.quantize("Q8_K", r["h"].astype(np.float32)), r["hq"])
     # (iv) down on the GPU's h^
-    o_tf = np.empty((P, H))
-    o_abs = np.empty((P, H))
-    for p in range(P):
+    o_tf = np.zeros((P, H))
+    o_abs = np.zeros((P, H))
+    for p in pairs:
         e = int(ids_ref.flat[p])
         oref, oabs = orc.gemv_dequant(cfg["down"], host["down"][e], H, I, r["hq"][p:p + 1], 1)
         check_outputs(r["o"][p][None], oref, oabs, f"down pair {p}")
         o_tf[p], o_abs[p] = oref[0], oabs[0]
     # (v) combine
-    y_tf = orc.moe_combine(o_tf, w_ref, T, k, H)
-    y_abs = orc.moe_combine(o_abs, w_ref, T, k, H)
+    y_tf = orc.moe_combine(o_tf, w_ref, T, k, H)[toks]
+    y_abs = orc.moe_combine(o_abs, w_ref, T, k, H)[toks]
     # routing weights carry fp32 rounding (<= 2e-6 relative): widen the scale by 30 %
-    check_outputs(y, y_tf, 1.3 * y_abs, "combine")
-    # free running against the whole oracle layer
-    ref = orc.moe(cfg["gate"], host["gate"], cfg["up"], host["up"], cfg["down"], host["down"], E, H, I, k, x, logits)
+    check_outputs(y[toks], y_tf, 1.3 * y_abs, "combine")
+    # free running against the whole oracle layer on the checked tokens
+    ref = orc.moe(cfg["gate"], host["gate"], cfg["up"], host["up"], cfg["down"], host["down"], E, H, I, k,
+                  x[toks], logits[toks])
     # The GPU's fp32 h differs from the oracle's double h within the gate/up
     # tolerance, so a few quants sitting at a rounding boundary land on the
     # neighbouring integer.  Every such flip must be a +-1 step of a block whose
     # scale agrees, and the flips must stay rare; the teacher-forced checks above
     # are the acceptance.
-    gq = r["hq"].reshape(P, I // 256, 292)
-    oq = ref["hq"].reshape(P, I // 256, 292)
+    nP = len(pairs)
+    gq = r["hq"][pairs].reshape(nP, I // 256, 292)
+    oq = ref["hq"].reshape(nP, I // 256, 292)
     d_gpu, d_orc = gq[..., :4].copy().view(np.float32), oq[..., :4].copy().view(np.float32)
     same_d = np.abs(d_gpu - d_orc) <= 1e-5 * np.abs(d_orc)
     qg = gq[..., 4:260].view(np.int8).astype(int)
@@ -127,8 +136,8 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0):
     diff = np.abs(qg - qo)
     assert np.all(diff[same_d[..., 0]] <= 1), "an h^ quant moved by more than one step"
     flips = int(np.count_nonzero(diff))
-    assert flips <= 0.01 * P * I, f"{flips} of {P * I} h^ quants differ from the free-running oracle"
-    nmse = float(np.sum((y - ref["y"]) ** 2) / np.sum(ref["y"] ** 2))
+    assert flips <= 0.01 * nP * I, f"{flips} of {nP * I} h^ quants differ from the free-running oracle"
+    nmse = float(np.sum((y[toks] - ref["y"]) ** 2) / np.sum(ref["y"] ** 2))
     assert nmse <= (1e-10 if flips == 0 else 1e-4), f"free-running NMSE {nmse:.3e} with {flips} flips"
     return flips
 
@@ -155,6 +164,29 @@ def test_moe_q8_0_gate_q4k_down_decode(ctx):
     cfg["E"] = 16
     for T in (1, 4):
         _run_and_check(ctx, cfg, 16, T)
+
+
+@pytest.mark.parametrize("T", [5, 8, 32, 128])
+def test_moe_sorted_route_mxfp4(ctx, T):
+    """5 tokens and up: expert-sorted tiles on the grouped int8 tensor-core kernel."""
+    _run_and_check(ctx, syn.MOE_MXFP4, 32, T, sample_tokens=None if T <= 8 else 6)
+
+
+@pytest.mark.parametrize("T", [5, 16])
+def test_moe_sorted_route_q4k_q6k(ctx, T):
+    cfg = syn.MOE_DECODE
+    _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 8 else 6)
+
+
+def test_moe_sorted_route_routed_entry(ctx):
+    _run_and_check(ctx, syn.MOE_MXFP4, 32, 9, routed=True, seed=3)
+
+
+def test_moe_prefill_4096_tokens_zipf(ctx):
+    """The prefill workload at full size: 4096 tokens, 128 experts, Zipf(1.1)
+    expert bias, Q8_0 gate/up and Q4_K down; sampled tokens against the oracle."""
+    cfg = syn.MOE_PREFILL
+    _run_and_check(ctx, cfg, cfg["E"], cfg["T"][0], sample_tokens=5)
 
 
 def test_moe_mxfp4_full_bank_256_experts(ctx):
