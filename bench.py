@@ -186,13 +186,18 @@ def oracle_sample_rate(target_s=12.0):
     dt = time.perf_counter() - t0
     rows = int(max(probe_rows, min(N, probe_rows * target_s / max(dt, 1e-6))))
     W = {f: syn.weights(f, rows, K, g) for f in FMTS}
+    reps = 0
     t0 = time.perf_counter()
-    for f in FMTS:
-        for T in TOKENS:
-            orc.gemv(f, W[f], rows, K, xq[T], T)
-    dt = time.perf_counter() - t0
-    nbytes = sum(rows * syn.row_bytes(f, K) for f in FMTS) * len(TOKENS)
-    sample = (f"{rows} of {N} rows of each of Q8_0/Q4_K/Q5_K/Q6_K (K={K}) at T=1,2,4,8: "
+    while True:  # whole passes over the sample until ~target_s / 2 of CPU time
+        for f in FMTS:
+            for T in TOKENS:
+                orc.gemv(f, W[f], rows, K, xq[T], T)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 2 or reps >= 50:
+            break
+    nbytes = sum(rows * syn.row_bytes(f, K) for f in FMTS) * len(TOKENS) * reps
+    sample = (f"{rows} of {N} rows of each of Q8_0/Q4_K/Q5_K/Q6_K (K={K}) at T=1,2,4,8, {reps} pass(es): "
               f"{nbytes / 1e6:.1f} MB of packed weights, oracle integer-dot GEMV, {cores} OpenMP threads")
     return nbytes / dt / 1e9, orc.threads(), sample, dt, rows
 
@@ -276,23 +281,31 @@ def run_gpu(args, rank, world):
 
     kev = [(rt.event(), rt.event()) for _ in plan]
     stream = torch.cuda.Stream()
+    ctx.set_static_weights(True)  # weights are never written while calls run: kernels overlap
 
-    def step(external):
+    def step(events):
         s = torch.cuda.current_stream()
         for T in TOKENS:
             ctx.quantize_act("Q8_K", x_dev[T], out=xq_dev[T])
         for j, (f, T, c) in enumerate(plan):
-            rt.record(kev[j][0], s, external)
+            if events:
+                rt.record(kev[j][0], s, True)
             ctx.mul_mat_vec_q(f, Wdev[f][c], N, K, xq_dev[T], T, Y=y_dev[(f, T)])
-            rt.record(kev[j][1], s, external)
+            if events:
+                rt.record(kev[j][1], s, True)
 
-    # eager warm-up (sets kernel attributes outside capture), then capture one step
+    # eager warm-up (sets kernel attributes outside capture), then capture the
+    # step twice: plain (timed; consecutive kernels overlap through programmatic
+    # dependent launch) and with an event pair around every GEMV (kernel times)
     with torch.cuda.stream(stream):
         for _ in range(2):
             step(False)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
+        step(False)
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=stream):
         step(True)
     torch.cuda.synchronize()
 
@@ -316,10 +329,15 @@ def run_gpu(args, rank, world):
     ms_per_step = total_ms / args.steps
     value = step_wbytes * world / (ms_per_step / 1e3) / 1e9
 
-    # per-launch GEMV kernel durations (events inside the graph, last replay)
-    per_launch = {}
-    for j, (f, T, c) in enumerate(plan):
-        per_launch[(f, T)] = rt.elapsed_ms(*kev[j])
+    # per-launch GEMV kernel durations: events inside the second graph, median of 5 replays
+    samples = {k: [] for k in plan}
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            graph_ev.replay()
+            torch.cuda.synchronize()
+            for j, key in enumerate(plan):
+                samples[key].append(rt.elapsed_ms(*kev[j]))
+    per_launch = {(f, T): statistics.median(samples[(f, T, c)]) for (f, T, c) in plan}
     sum_alg = sum(alg_bytes[k] for k in per_launch)
     sum_ms = sum(per_launch.values())
     achieved = sum_alg / (sum_ms / 1e3) / 1e9
@@ -339,6 +357,7 @@ def run_gpu(args, rank, world):
         for k, v in y_dev.items():
             y_host[k].copy_(v, non_blocking=True)
 
+    ctx.set_static_weights(False)  # the public call as a generic caller makes it
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             e2e_step()
@@ -364,7 +383,7 @@ def run_gpu(args, rank, world):
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(secs, 2)}
 
-    gpu_launches = (len(TOKENS) + len(plan)) * args.steps
+    gpu_launches = (len(TOKENS) + len(plan)) * args.steps  # 4 quantize + 16 GEMV kernels per step
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -378,8 +397,9 @@ def run_gpu(args, rank, world):
                        "fraction_of_hbm": round(value / world / hbm_peak, 4), "peak": f"{hbm_peak} GB/s ({peak_kind})"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                         "kernel": "k_stream<GEMV> (all 16 launches of a step; algorithmic bytes = packed W + "
-                                   "Q8_K x + fp32 y per launch)",
+                         "kernel": "decode GEMV kernels (k_stream dp4a at T<=2, k_group int8 mma at T>=3): "
+                                   "all 16 launches of a step; algorithmic bytes = packed W + Q8_K x + fp32 y",
+                         "timing": "CUDA events around each GEMV inside a captured graph, median of 5 replays",
                          "peak_kind": peak_kind, "per_launch": breakdown},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -441,9 +461,11 @@ def secondary_workloads(ctx, rt, hbm_peak):
                                      "us_per_call": round(ms * 1e3 / len(copies), 2)}
     del copies
 
-    # MoE layers: rotate 16 seeded router-logit sets so the expert sets differ per call
+    # MoE layers: rotate seeded router-logit sets so the expert sets differ per call
+    ctx.set_static_weights(True)
     for cfg, E, Ts in ((syn.MOE_DECODE, syn.MOE_DECODE["E"], (1, 2, 3, 4)),
-                       (syn.MOE_MXFP4, syn.MOE_MXFP4["E"], (1, 2, 3, 4, 5))):
+                       (syn.MOE_MXFP4, syn.MOE_MXFP4["E"], (1, 2, 3, 4, 5, 32, 128, 512)),
+                       (syn.MOE_PREFILL, syn.MOE_PREFILL["E"], (4096,))):
         H, I, k = cfg["H"], cfg["I"], cfg["k"]
         g = syn.rng(cfg["index"], 1)
         banks = [torch.from_numpy(syn.expert_bank(cfg[n], E, r, c, g)).cuda()
@@ -451,9 +473,9 @@ def secondary_workloads(ctx, rt, hbm_peak):
         w8 = ctx.moe_weights(cfg["gate"], banks[0], cfg["up"], banks[1], cfg["down"], banks[2])
         per_expert = 2 * I * syn.row_bytes(cfg["gate"], H) + H * syn.row_bytes(cfg["down"], I)
         for T in Ts:
-            R = 16
+            R = 16 if T <= 8 else (4 if T <= 512 else 2)
             xs = [torch.from_numpy(syn.activations(T, H, g)).cuda() for _ in range(R)]
-            lgs = [syn.router_logits(T, E, g) for _ in range(R)]
+            lgs = [syn.router_logits(T, E, g, cfg.get("zipf")) for _ in range(R)]
             # distinct experts per layer: top-k by logit (stable sort keeps ties on the lower index)
             distinct = sum(len(np.unique(np.argsort(-lg, axis=1, kind="stable")[:, :k])) for lg in lgs)
             lgd = [torch.from_numpy(lg).cuda() for lg in lgs]
@@ -464,15 +486,61 @@ def secondary_workloads(ctx, rt, hbm_peak):
                 for r in range(R):
                     ctx.moe_experts(w8, E, H, I, k, xs[r], logits=lgd[r], Y=ys, reserve=False)
 
-            ms = _graph_time(moe, 5, rt, stream)
+            ms = _graph_time(moe, 3 if T > 512 else 5, rt, stream)
             gbps = distinct * per_expert / (ms / 1e3) / 1e9
+            ops = 2.0 * T * k * 3 * I * H * R  # int multiply-adds x 2
             name = f"moe_{cfg['gate'].lower()}_{cfg['down'].lower()}_E{E}_H{H}_I{I}_T{T}"
             out[name] = {"GBps": round(gbps, 1), "frac": round(gbps / hbm_peak, 4),
-                         "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R}
-        del banks
+                         "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R,
+                         "int_TOPS": round(ops / (ms / 1e3) / 1e12, 2),
+                         "route": "direct" if T <= 4 else "expert-sorted"}
+        del banks, w8
         torch.cuda.empty_cache()
+    ctx.set_static_weights(False)
     ctx.sync_status()
     return out
+
+
+def profile_case(args):
+    """Small launch sequences for ncu captures (not a benchmark).
+    gemv: 4 warm-up launches of a 14336 x 4096 GEMV at T=1, then one at T=1 and
+          one at T=8, over 5 rotating weight copies (165 MB for Q4_K > L2).
+    moe:  the MoE decode layer (128 experts, H 2048, I 768, Q4_K/Q6_K, top-8)
+          at T tokens: 2 warm-up layers, then 1 layer.
+    prefill: the expert-sorted route on the prefill workload at T tokens
+          (128 experts, H 4096, I 1536, Q8_0 gate/up, Q4_K down, Zipf 1.1)."""
+    import torch
+
+    import gguf_block_quant_ggq_gb300 as ggq
+    from gguf_block_quant_ggq_gb300 import _build
+
+    _build.build()
+    ctx = ggq.Context(0)
+    if args.profile_case == "gemv":
+        fmt = args.fmt
+        Ws = [torch.from_numpy(syn.weights(fmt, N, K, syn.rng(1, i))).cuda() for i in range(5)]
+        xq = {T: ctx.quantize_act("Q8_K", torch.from_numpy(syn.activations(T, K, syn.rng(1, 50 + T))).cuda())
+              for T in (1, 8)}
+        for i in range(4):
+            ctx.mul_mat_vec_q(fmt, Ws[i % 5], N, K, xq[1], 1)
+        ctx.mul_mat_vec_q(fmt, Ws[4], N, K, xq[1], 1)
+        ctx.mul_mat_vec_q(fmt, Ws[0], N, K, xq[8], 8)
+    else:
+        cfg = syn.MOE_DECODE if args.profile_case == "moe" else syn.MOE_PREFILL
+        E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
+        g = syn.rng(cfg["index"], 1)
+        banks = [torch.from_numpy(syn.expert_bank(cfg[n], E, r, c, g)).cuda()
+                 for n, r, c in (("gate", I, H), ("up", I, H), ("down", H, I))]
+        w8 = ctx.moe_weights(cfg["gate"], banks[0], cfg["up"], banks[1], cfg["down"], banks[2])
+        T = args.tokens
+        for r in range(3):
+            x = torch.from_numpy(syn.activations(T, H, g)).cuda()
+            lg = torch.from_numpy(syn.router_logits(T, E, g, cfg.get("zipf"))).cuda()
+            ctx.moe_experts(w8, E, H, I, k, x, logits=lg)
+    torch.cuda.synchronize()
+    ctx.sync_status()
+    ctx.close()
+    print("profile case done")
 
 
 def main():
@@ -483,7 +551,14 @@ def main():
     ap.add_argument("--impl", default="ggq", choices=["ggq", "reference"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["gemv", "moe", "prefill"], default=None,
+                    help="run a small launch sequence for an ncu capture instead of the benchmark")
+    ap.add_argument("--fmt", default="Q4_K")
+    ap.add_argument("--tokens", type=int, default=1)
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank, world = dist_init(args.gpus)

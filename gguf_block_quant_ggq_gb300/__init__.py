@@ -30,6 +30,7 @@ SIGNATURES = {
     "ggq_last_error": (ctypes.c_char_p, [_P]),
     "ggq_reserve": (_I32, [_P, _P, _P]),
     "ggq_scratch_bytes": (ctypes.c_size_t, [_P]),
+    "ggq_set_static_weights": (_I32, [_P, _I32]),
     "ggq_supported": (_I32, [_I32, _I32, _I32]),
     "ggq_quantize_act": (_I32, [_P, _I32, _P, _I64, _I64, _P, _P]),
     "ggq_dequant": (_I32, [_P, _I32, _P, _I64, _I64, _P, _P]),
@@ -144,6 +145,9 @@ class Context:
     def reserve(self, max_tokens=0, max_k=0, n_experts=0, hidden=0, inter=0, top_k=0, stream=None):
         plan = ggq_plan(max_tokens, max_k, n_experts, hidden, inter, top_k)
         self._check(load().ggq_reserve(self.handle, ctypes.byref(plan), self._stream(stream)))
+
+    def set_static_weights(self, on: bool = True):
+        self._check(load().ggq_set_static_weights(self.handle, 1 if on else 0))
 
     def scratch_bytes(self) -> int:
         return load().ggq_scratch_bytes(self.handle)

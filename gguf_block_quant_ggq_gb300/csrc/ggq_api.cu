@@ -17,17 +17,16 @@
 
 #include "../../include/ggq.h"
 #include "ggq_device.cuh"
+#include "ggq_direct.cuh"
 #include "ggq_internal.h"
 
 namespace ggq {
 cudaError_t launch_gemv_a(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_gemv_b(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
-cudaError_t launch_moe_gateup(int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
-cudaError_t launch_moe_down(int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_direct_gateup(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_direct_down(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
-    if (kind == KIND_GATEUP) return launch_moe_gateup(fmt, nt, p, grid, smem, s);
-    if (kind == KIND_DOWN) return launch_moe_down(fmt, nt, p, grid, smem, s);
     if (fmt == F_Q4_0 || fmt == F_Q8_0 || fmt == F_MXFP4) return launch_gemv_a(kind, fmt, nt, p, grid, smem, s);
     return launch_gemv_b(kind, fmt, nt, p, grid, smem, s);
 }
@@ -37,7 +36,6 @@ using namespace ggq;
 
 namespace {
 
-constexpr int kCounterInts = 16384;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -45,9 +43,7 @@ size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 // Layout of the control block (allocated once at create).
 struct Ctrl {
     int err;
-    int pad[31];
-    int counters[kCounterInts];
-    MoePlan plan;
+    int pad[63];
 };
 
 int fmt_of(int t) {
@@ -87,19 +83,19 @@ size_t gemv_scratch(int64_t T, int64_t K) {
 }
 
 struct MoeScratch {
-    size_t xq, ids, w, h, hq, o, total;
+    size_t ids, w, h, hq, total;
 };
 
+// Direct route (1-4 tokens): routed ids/weights, fp32 h, packed h^ (dumps).
 MoeScratch moe_scratch(int64_t T, int64_t H, int64_t I, int64_t k) {
+    (void)H;
     MoeScratch m{};
     const size_t P = static_cast<size_t>(T * k);
     size_t off = 0;
-    m.xq = off; off += align_up(static_cast<size_t>(T) * (H / 256) * 292);
     m.ids = off; off += align_up(P * 4);
     m.w = off; off += align_up(P * 4);
     m.h = off; off += align_up(P * static_cast<size_t>(I) * 4);
     m.hq = off; off += align_up(P * (I / 256) * 292);
-    m.o = off; off += align_up(P * static_cast<size_t>(H) * 4);
     m.total = off;
     return m;
 }
@@ -149,6 +145,7 @@ struct ggq_ctx {
     size_t pool_bytes = 0;
     std::vector<void*> retired;
     Ctrl* ctrl = nullptr;
+    int static_weights = 0;  // weights never written while calls are in flight
     std::string err;
 };
 
@@ -179,10 +176,10 @@ struct StreamShape {
     int stages, stride, x_bytes, smem;
 };
 
-bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s) {
+bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s, int extra = 1024) {
     s->stride = static_cast<int>(align_up(static_cast<size_t>(stage_bytes) + 16, 128));
     s->x_bytes = x_region_bytes(xrows, K, q81);
-    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + 1024;
+    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + extra;
     if (fixed + s->stride > kSmemLimit) return false;
     s->stages = (kSmemLimit - fixed) / s->stride;
     if (s->stages > kMaxStages) s->stages = kMaxStages;
@@ -270,6 +267,7 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
         g.x_pitch = K / 256 * 292;
         g.Y = Y;
         g.err = &c->ctrl->err;
+        g.early_weights = c->static_weights;
         int smem = 0;
         if (plan_group(g, 1, true, &smem)) {
             const int64_t tiles = (N + kGroupRows - 1) / kGroupRows;
@@ -290,6 +288,7 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     p.Y = Y;
     p.coefs = coefs;
     p.err = &c->ctrl->err;
+    p.early_weights = c->static_weights;
     StreamShape sh;
     if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh))
         return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld with T=%lld does not fit in shared memory",
@@ -431,89 +430,70 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     const MoeScratch ms = moe_scratch(T, H, I, top_k);
     ggq_status s = need_scratch(c, ms.total);
     if (s != GGQ_OK) return s;
-    if (I / 256 * kPlanMaxPairs > kCounterInts / 2 || H / kTileRows > kCounterInts / 2)
-        return fail(c, GGQ_ERR_SHAPE, "moe_experts: H or I too large for the counter block");
-
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* xq = c->pool + ms.xq;
-    int32_t* ids_s = reinterpret_cast<int32_t*>(c->pool + ms.ids);
-    float* w_s = reinterpret_cast<float*>(c->pool + ms.w);
-    float* h = reinterpret_cast<float*>(c->pool + ms.h);
-    uint8_t* hq = c->pool + ms.hq;
-    float* o = reinterpret_cast<float*>(c->pool + ms.o);
-    MoePlan* plan = &c->ctrl->plan;
-
-    cudaError_t e = launch_moe_route(logits, ids, weights, X, static_cast<int>(T), static_cast<int>(E), top_k,
-                                     static_cast<int>(H), xq, plan, ids_s, w_s, &c->ctrl->err, st);
-    if (e != cudaSuccess) return cuda_fail(c, e, "moe route launch");
-
+    const int P = static_cast<int>(T * top_k);
+    DirectParams p{};
+    p.T = static_cast<int>(T);
+    p.E = static_cast<int>(E);
+    p.top_k = top_k;
+    p.X = X;
+    p.logits = logits;
+    p.ids_in = ids;
+    p.w_in = weights;
+    p.ids = reinterpret_cast<int32_t*>(c->pool + ms.ids);
+    p.w = reinterpret_cast<float*>(c->pool + ms.w);
+    p.h = reinterpret_cast<float*>(c->pool + ms.h);
+    p.xq_dump = dump ? static_cast<uint8_t*>(dump->xq) : nullptr;
+    p.hq = c->pool + ms.hq;
+    p.g_dump = dump ? dump->g : nullptr;
+    p.u_dump = dump ? dump->u : nullptr;
+    p.o_dump = dump ? dump->o : nullptr;
+    p.Y = Y;
+    p.err = &c->ctrl->err;
     const int nt = pow2_tokens(T);
-    // gate/up: rows of I, input width H, activations x^ (T rows)
+    const int direct_fixed = 2 * kMaxStages * 8 + static_cast<int>(sizeof(DirectPlan)) + 256;
+    // gate/up: 16 gate rows + the 16 matching up rows per stage; x^ of the T tokens
     {
-        StreamParams p{};
         p.W = static_cast<const uint8_t*>(w->gate);
         p.W2 = static_cast<const uint8_t*>(w->up);
         p.rowbytes = w_row_bytes(fg, H);
         p.N = I;
         p.K = static_cast<int>(H);
-        p.xq = xq;
-        p.xrows = static_cast<int>(T);
-        p.T = static_cast<int>(T);
-        p.top_k = top_k;
-        p.plan = plan;
-        p.h = h;
-        p.g_dump = dump ? dump->g : nullptr;
-        p.u_dump = dump ? dump->u : nullptr;
-        p.hq = hq;
-        p.counters = c->ctrl->counters;
-        p.err = &c->ctrl->err;
         StreamShape sh;
-        if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, false, &sh))
+        if (!plan_stream(2 * kTileRows * p.rowbytes, static_cast<int>(T), p.K, false, &sh, direct_fixed))
             return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
         p.stages = sh.stages;
         p.stage_stride = sh.stride;
         p.x_bytes = sh.x_bytes;
-        e = launch_stream(KIND_GATEUP, fg, nt, p, c->nsm, sh.smem, st);
+        cudaError_t e = launch_direct_gateup(fg, nt, p, c->nsm, sh.smem, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe gate/up launch");
     }
-    // down: rows of H, input width I, activations h^ (T*k rows), combine into Y
+    // down: 16-row output tile of every selected expert; h^ of the T*k pairs
     {
-        StreamParams p{};
         p.W = static_cast<const uint8_t*>(w->down);
+        p.W2 = nullptr;
         p.rowbytes = w_row_bytes(fd, I);
         p.N = H;
         p.K = static_cast<int>(I);
-        p.xq = hq;
-        p.xrows = static_cast<int>(T * top_k);
-        p.T = static_cast<int>(T);
-        p.top_k = top_k;
-        p.plan = plan;
-        p.o = o;
-        p.Y = Y;
-        p.counters = c->ctrl->counters + kCounterInts / 2;
-        p.err = &c->ctrl->err;
         StreamShape sh;
-        if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, false, &sh))
+        if (!plan_stream(kTileRows * p.rowbytes, P, p.K, false, &sh, direct_fixed))
             return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
         p.stages = sh.stages;
         p.stage_stride = sh.stride;
         p.x_bytes = sh.x_bytes;
-        e = launch_stream(KIND_DOWN, fd, nt, p, c->nsm, sh.smem, st);
+        cudaError_t e = launch_direct_down(fd, nt, p, c->nsm, sh.smem, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe down launch");
     }
     if (dump) {
-        const size_t P = static_cast<size_t>(T * top_k);
         struct Cp { void* dst; const void* src; size_t n; } cps[] = {
-            {dump->ids, ids_s, P * 4},
-            {dump->weights, w_s, P * 4},
-            {dump->xq, xq, static_cast<size_t>(T) * (H / 256) * 292},
-            {dump->h, h, P * I * 4},
-            {dump->hq, hq, P * (I / 256) * 292},
-            {dump->o, o, P * H * 4},
+            {dump->ids, p.ids, static_cast<size_t>(P) * 4},
+            {dump->weights, p.w, static_cast<size_t>(P) * 4},
+            {dump->h, p.h, static_cast<size_t>(P) * I * 4},
+            {dump->hq, p.hq, static_cast<size_t>(P) * (I / 256) * 292},
         };
         for (const Cp& cp : cps)
             if (cp.dst) {
-                e = cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToDevice, st);
+                cudaError_t e = cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToDevice, st);
                 if (e != cudaSuccess) return cuda_fail(c, e, "moe dump copy");
             }
     }
@@ -561,6 +541,12 @@ ggq_status ggq_destroy(ggq_ctx* c) {
 const char* ggq_last_error(const ggq_ctx* c) { return c ? c->err.c_str() : "null context"; }
 
 size_t ggq_scratch_bytes(const ggq_ctx* c) { return c ? c->pool_bytes : 0; }
+
+ggq_status ggq_set_static_weights(ggq_ctx* c, int static_weights) {
+    if (!c) return GGQ_ERR_INVALID_ARG;
+    c->static_weights = static_weights ? 1 : 0;
+    return GGQ_OK;
+}
 
 ggq_status ggq_reserve(ggq_ctx* c, const ggq_plan* plan, void* stream) {
     ggq_status s = check_ctx(c);

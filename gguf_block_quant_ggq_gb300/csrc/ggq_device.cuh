@@ -107,6 +107,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
+// Programmatic dependent launch.  Every kernel lets the next kernel in the
+// stream start launching as soon as all of its CTAs are running, and waits for
+// the previous kernel (completion and memory) before it reads anything that
+// kernel may have produced or writes any output.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void set_error(int* err, int code) {
     if (err) atomicCAS(err, DEV_OK, code);
 }

@@ -1,0 +1,390 @@
+// ggq_direct.cuh -- the direct tiny-batch MoE route (1 to 4 tokens): two
+// kernels per layer, with no cross-CTA counters, fences or extra launches.
+//
+// ds4 PR #656 "Add ROCm MXFP4 routed expert kernels" (Summary): 2-4 token
+// batches go through direct kernels instead of partially filled expert-sorted
+// tiles, and gate/up, SwiGLU and down stay register-resident.  Here:
+//   gate/up kernel: every CTA routes the tokens itself (top-k of softmax by
+//     logit, ties to the lower index), groups the <= 32 (token, slot) pairs by
+//     distinct expert with one warp match, and quantizes x to Q8_K straight
+//     into shared memory.  Each consumer warp owns one gate row and the same
+//     up row of a 16-row tile, so h = silu(g) * u is formed in the warp and
+//     written once to global memory (fp32).
+//   down kernel: rebuilds the same grouping from the routed ids, quantizes h
+//     to Q8_K into shared memory (bit-exactly the same quantizer), and for
+//     each 16-row tile of the output streams that tile of every selected
+//     expert, accumulating y = sum_j w_j o_j in registers in a fixed expert
+//     order, so the result is deterministic.
+// Both kernels stream weights with the producer warp / mbarrier ring of the
+// streaming kernel and use its dp4a consumer (row_accumulate).
+#pragma once
+#include "ggq_stream.cuh"
+
+namespace ggq {
+
+constexpr int kDirectMaxPairs = 32;  // 4 tokens x top-8
+
+struct DirectPlan {
+    int D;                                        // distinct experts
+    int expert[kDirectMaxPairs];                  // expert of distinct slot u
+    int npairs[kDirectMaxPairs];                  // pairs on it
+    int pair[kDirectMaxPairs][4];                 // pair indices p = t*k + j (one per token)
+    float wt[kDirectMaxPairs];                    // routing weight of pair p
+    int ids[kDirectMaxPairs];                     // expert of pair p
+    int bad;                                      // a routed id was out of range
+};
+
+// Group the P <= 32 pairs (expert ids in s->ids) by distinct expert, in order
+// of first appearance.  One warp.
+__device__ __forceinline__ void direct_group(DirectPlan* s, int P, int E, int lane) {
+    const bool active = lane < P;
+    const int e = active ? s->ids[lane] : -1 - lane;
+    const unsigned act = __ballot_sync(0xffffffffu, active);
+    const unsigned same = __match_any_sync(0xffffffffu, e) & act;
+    const unsigned lt = (1u << lane) - 1u;
+    const bool leader = active && (same & lt) == 0u;
+    const unsigned leaders = __ballot_sync(0xffffffffu, leader);
+    const int lead = active ? __ffs(same) - 1 : 0;
+    const int u = __popc(leaders & ((1u << lead) - 1u));
+    const int slot = __popc(same & lt);
+    const bool bad = active && (e < 0 || e >= E || slot >= 4);
+    const unsigned anybad = __ballot_sync(0xffffffffu, bad);
+    if (active && !anybad) {
+        s->pair[u][slot] = lane;
+        if (leader) {
+            s->expert[u] = e;
+            s->npairs[u] = __popc(same);
+        }
+    }
+    if (lane == 0) {
+        s->D = anybad ? 0 : __popc(leaders);
+        s->bad = anybad != 0u;
+    }
+}
+
+// Routing of token t by one warp: top-k by logit (ties to the lower expert
+// index) and the softmax weights renormalised over the selected experts.
+__device__ __forceinline__ void direct_route_token(const float* __restrict__ l, int E, int k, int* ids, float* w,
+                                                   int lane) {
+    uint32_t taken[4] = {0u, 0u, 0u, 0u};
+    float lmax = 0.0f, wsum = 0.0f, myw = 0.0f;
+    int myid = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = 0, e = lane; e < E; ++i, e += 32) {
+            if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
+            const float v = __ldg(l + e);
+            if (v > bv || (v == bv && e < bi)) {
+                bv = v;
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) {
+            const int i = bi >> 5;
+            taken[i >> 5] |= 1u << (i & 31);
+        }
+        if (j == 0) lmax = bv;
+        const float p = expf(bv - lmax);
+        wsum += p;
+        if (lane == j) {
+            myid = bi;
+            myw = p;
+        }
+    }
+    if (lane < k) {
+        ids[lane] = myid;
+        w[lane] = myw / wsum;
+    }
+}
+
+// Quantize the 256-element block `blk` of an fp32 row (global memory) to Q8_K
+// straight into the shared-memory activation region (row `row`), with the
+// same arithmetic as warp_quant_q8k.  Optionally also writes the packed block.
+template <bool PERM>
+__device__ __forceinline__ void warp_quant_to_smem(const float* src, int row, int blk, int K, const XRegion& x,
+                                                   uint8_t* packed, int lane) {
+    float v[8];
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + 2 * lane);
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 2 * lane + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    const float amax = warp_max(m);
+    float id;
+    const float d = quant_scale(amax, &id);
+    int q[8], s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q[i] = quant_one(v[i], id);
+        s += q[i];
+    }
+    const uint32_t w0 = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | (static_cast<uint32_t>(q[3] & 0xFF) << 24);
+    const uint32_t w1 = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | (static_cast<uint32_t>(q[7] & 0xFF) << 24);
+    int8_t* dq = x.q + static_cast<size_t>(row) * xq_row_bytes(K);
+    const int e0 = 256 * blk + 8 * lane;
+    if constexpr (!PERM) {
+        *reinterpret_cast<uint32_t*>(dq + xq_addr(e0)) = w0;
+        *reinterpret_cast<uint32_t*>(dq + xq_addr(e0 + 4)) = w1;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int el = e0 + i, r = el & 31;
+            dq[xq_addr((el & ~31) + 2 * (r & 15) + (r >> 4))] = static_cast<int8_t>(q[i]);
+        }
+    }
+    int s16 = s + __shfl_xor_sync(0xffffffffu, s, 1);   // 16-element group: lanes 2g, 2g+1
+    int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 2);  // 32-element block: lanes 4b..4b+3
+    if ((lane & 1) == 0) x.bs[static_cast<size_t>(row) * (K >> 4) + 16 * blk + (lane >> 1)] = static_cast<int16_t>(s16);
+    if ((lane & 3) == 0) x.s32[static_cast<size_t>(row) * (K >> 5) + 8 * blk + (lane >> 2)] = s32;
+    if (lane == 0) x.d[static_cast<size_t>(row) * (K >> 8) + blk] = d;
+    if (packed) {
+        uint32_t* pq = reinterpret_cast<uint32_t*>(packed + 4 + 8 * lane);
+        pq[0] = w0;
+        pq[1] = w1;
+        if ((lane & 1) == 0) reinterpret_cast<int16_t*>(packed + 260)[lane >> 1] = static_cast<int16_t>(s16);
+        if (lane == 0) *reinterpret_cast<float*>(packed) = d;
+    }
+}
+
+struct DirectParams {
+    const uint8_t* W;    // gate bank (gate/up) or down bank
+    const uint8_t* W2;   // up bank
+    int64_t rowbytes;
+    int64_t N;           // I (gate/up) or H (down)
+    int K;               // H (gate/up) or I (down)
+    int T, E, top_k;
+    const float* X;              // gate/up: x [T][H]
+    const float* logits;         // gate/up: [T][E] or null (routed)
+    const int32_t* ids_in;       // gate/up routed ids
+    const float* w_in;
+    int32_t* ids;                // routed ids [T*k] (written by gate/up CTA 0, read by down)
+    float* w;                    // routed weights [T*k]
+    float* h;                    // [T*k][I]
+    uint8_t* xq_dump;            // optional packed Q8_K of x
+    uint8_t* hq;                 // optional packed Q8_K of h (down CTA 0)
+    float* g_dump;
+    float* u_dump;
+    float* o_dump;               // optional [T*k][H]
+    float* Y;                    // down: [T][H]
+    int* err;
+    int stages, stage_stride, x_bytes;
+};
+
+// Gate/up (KIND_GATEUP) or down (KIND_DOWN) of the direct route.
+template <int KIND, int F, int NT>
+__global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int LV = NT == 1 ? 0 : NT == 2 ? 1 : 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = p.K, P = p.T * p.top_k;
+    pdl_launch_dependents();
+    pdl_wait();  // logits, x, routed ids and h come from earlier kernels
+
+    uint8_t* ring = smem;
+    uint8_t* xreg = smem + static_cast<size_t>(p.stages) * p.stage_stride;
+    const int xrows = KIND == KIND_GATEUP ? p.T : P;
+    const XRegion xr_ = x_region(xreg, xrows, K, false);
+    uint64_t* full = reinterpret_cast<uint64_t*>(xreg + p.x_bytes);
+    uint64_t* empty = full + kMaxStages;
+    DirectPlan* plan = reinterpret_cast<DirectPlan*>(empty + kMaxStages);
+
+    // ---- routing and grouping (every CTA), activation quantization
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    if constexpr (KIND == KIND_GATEUP) {
+        if (warp < p.T) {
+            if (p.logits) {
+                direct_route_token(p.logits + static_cast<int64_t>(warp) * p.E, p.E, p.top_k,
+                                   plan->ids + warp * p.top_k, plan->wt + warp * p.top_k, lane);
+            } else if (lane < p.top_k) {
+                plan->ids[warp * p.top_k + lane] = p.ids_in[warp * p.top_k + lane];
+                plan->wt[warp * p.top_k + lane] = p.w_in[warp * p.top_k + lane];
+            }
+        }
+    } else {
+        if (tid < P) {
+            plan->ids[tid] = __ldcg(p.ids + tid);
+            plan->wt[tid] = __ldcg(p.w + tid);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) direct_group(plan, P, p.E, lane);
+    __syncthreads();
+    const int D = plan->D;
+    if (KIND == KIND_GATEUP && blockIdx.x == 0 && tid < P) {
+        p.ids[tid] = plan->ids[tid];
+        p.w[tid] = plan->wt[tid];
+        if (plan->bad && tid == 0) set_error(p.err, 2);
+    }
+    const int tiles = static_cast<int>(p.N / kTileRows);
+    const int nitems = KIND == KIND_GATEUP ? D * tiles : (D > 0 ? tiles : 0);
+    if (static_cast<int>(blockIdx.x) >= nitems) return;
+
+    if (warp == kConsumerWarps) {
+        // ================= producer: one stage per (expert, tile) pair
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int j = 0;
+            for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+                const int ne = KIND == KIND_GATEUP ? 1 : D;
+                for (int q = 0; q < ne; ++q, ++j) {
+                    const int u = KIND == KIND_GATEUP ? item / tiles : q;
+                    const int tile = KIND == KIND_GATEUP ? item - u * tiles : item;
+                    const int s = j % p.stages;
+                    if (!mbar_wait(&empty[s], (static_cast<uint32_t>(j / p.stages) & 1u) ^ 1u)) {
+                        set_error(p.err, DEV_ERR_TIMEOUT);
+                        goto drain;
+                    }
+                    const int64_t e = plan->expert[u];
+                    const int64_t off = (e * p.N + static_cast<int64_t>(tile) * kTileRows) * p.rowbytes;
+                    const uint32_t bytes = static_cast<uint32_t>(kTileRows * p.rowbytes);  // multiple of 16
+                    uint8_t* dst = ring + static_cast<size_t>(s) * p.stage_stride;
+                    mbar_arrive_expect_tx(&full[s], KIND == KIND_GATEUP ? 2 * bytes : bytes);
+                    bulk_g2s(dst, p.W + off, bytes, &full[s], pol);
+                    if (KIND == KIND_GATEUP) bulk_g2s(dst + bytes, p.W2 + off, bytes, &full[s], pol);
+                }
+            }
+        drain:
+            for (int q = (j > p.stages ? j - p.stages : 0); q < j; ++q)
+                if (!mbar_wait(&full[q % p.stages], static_cast<uint32_t>(q / p.stages) & 1u)) break;
+        }
+        return;
+    }
+
+    // ================= consumers: quantize the activations into shared memory
+    {
+        const int nbr = K >> 8;
+        for (int b = warp; b < xrows * nbr; b += kConsumerWarps) {
+            const int r = b / nbr, c = b - r * nbr;
+            if constexpr (KIND == KIND_GATEUP) {
+                uint8_t* pk = (blockIdx.x == 0 && p.xq_dump) ? p.xq_dump + static_cast<int64_t>(b) * 292 : nullptr;
+                warp_quant_to_smem<F == F_MXFP4>(p.X + static_cast<int64_t>(b) * 256, r, c, K, xr_, pk, lane);
+            } else {
+                uint8_t* pk = (blockIdx.x == 0 && p.hq) ? p.hq + static_cast<int64_t>(b) * 292 : nullptr;
+                warp_quant_to_smem<F == F_MXFP4>(p.h + static_cast<int64_t>(b) * 256, r, c, K, xr_, pk, lane);
+            }
+        }
+    }
+    consumer_sync();
+    XS xs;
+    xs.q = smem_addr(xr_.q);
+    xs.d = smem_addr(xr_.d);
+    xs.s32 = smem_addr(xr_.s32);
+    xs.bs = smem_addr(xr_.bs);
+    xs.K = K;
+    const saddr ring_s = smem_addr(ring);
+    constexpr int SH = 5 - (LV + (KIND == KIND_GATEUP ? 1 : 0));
+
+    int j = 0;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        if constexpr (KIND == KIND_GATEUP) {
+            const int u = item / tiles, tile = item - u * tiles;
+            const int s = j % p.stages;
+            const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(j / p.stages) & 1u));
+            ++j;
+            const int np = plan->npairs[u];
+            int xr[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->pair[u][t] / p.top_k : 0;
+            const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+            const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
+            if (ready) {
+                float acc[2 * NT];
+#pragma unroll
+                for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
+                row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
+                row_accumulate<F, NT>(stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes), xs, xr, np,
+                                      acc + NT, lane);
+                const float v = warp_transpose_reduce<LV + 1>(acc, lane);  // index = gate/up * NT + slot
+                const float uval = __shfl_down_sync(0xffffffffu, v, NT << SH);
+                const int idx = lane >> SH;
+                if ((lane & ((1 << SH) - 1)) == 0 && idx < NT && idx < np) {
+                    const float hval = __fmul_rn(__fdiv_rn(v, 1.0f + expf(-v)), uval);
+                    const int64_t o = static_cast<int64_t>(plan->pair[u][idx]) * p.N + row;
+                    p.h[o] = hval;
+                    if (p.g_dump) p.g_dump[o] = v;
+                    if (p.u_dump) p.u_dump[o] = uval;
+                }
+            } else {
+                set_error(p.err, DEV_ERR_TIMEOUT);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            if (!ready) break;
+        } else {
+            const int tile = item;
+            const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
+            // y for the T tokens of this row, accumulated over the experts in plan order
+            float yacc = 0.0f;  // lane t (t < T) holds y[t][row] after each reduction
+            bool ok = true;
+            for (int u = 0; u < D; ++u, ++j) {
+                const int s = j % p.stages;
+                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(j / p.stages) & 1u));
+                const int np = plan->npairs[u];
+                int xr[NT];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->pair[u][t] : 0;
+                if (ready && ok) {
+                    const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+                    float acc[NT];
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
+                    row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
+                    const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = slot
+                    const int slot = lane >> SH;
+                    const int pp = slot < np ? xr[slot] : -1;
+                    if (pp >= 0 && (lane & ((1 << SH) - 1)) == 0 && p.o_dump) p.o_dump[static_cast<int64_t>(pp) * p.N + row] = v;
+                    // move each slot's weighted value to the lane of its token
+                    const float contrib = pp >= 0 ? plan->wt[pp] * v : 0.0f;
+                    const int tok = pp >= 0 ? pp / p.top_k : -1;
+#pragma unroll
+                    for (int q = 0; q < NT; ++q) {
+                        const float cq = __shfl_sync(0xffffffffu, contrib, q << SH);
+                        const int tq = __shfl_sync(0xffffffffu, tok, q << SH);
+                        if (q < np && lane == tq) yacc += cq;
+                    }
+                } else if (!ready) {
+                    set_error(p.err, DEV_ERR_TIMEOUT);
+                    ok = false;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            if (ok && lane < p.T) p.Y[static_cast<int64_t>(lane) * p.N + row] = yacc;
+            if (!ok) break;
+        }
+    }
+}
+
+template <int KIND, int F, int NT>
+cudaError_t launch_direct_one(const DirectParams& p, int grid, int smem, cudaStream_t s) {
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(k_direct<KIND, F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return launch_pdl(k_direct<KIND, F, NT>, dim3(grid), dim3(kThreads), smem, s, p);
+}
+
+}  // namespace ggq

@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
     uint64_t* xempty = xfull + 8;
     int* s_abort = reinterpret_cast<int*>(xempty + 8);
 
+    pdl_launch_dependents();
+    if (KIND != G_GEMV) pdl_wait();  // the grouping comes from the previous kernels
     const int ngroups = KIND == G_GEMV ? 1 : *p.ngroups;
     const int tiles = static_cast<int>(p.N / kGroupRows);  // N % 16 == 0 except the GEMV tail
     const int tiles_all = KIND == G_GEMV ? static_cast<int>((p.N + kGroupRows - 1) / kGroupRows) : tiles;
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
         // ================= producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            if (KIND == G_GEMV && !p.early_weights) pdl_wait();
             int wj = 0, xj = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++wj) {
@@ -347,6 +350,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
                 }
                 // activation chunks (the GEMV's single chunk is loaded once and kept)
                 const int nchunks = KIND == G_GEMV ? (wj == 0 ? 1 : 0) : (cnt + kGroupCols - 1) / kGroupCols;
+                if (KIND == G_GEMV && wj == 0 && p.early_weights) pdl_wait();  // x^ comes from the previous kernel
                 for (int ch = 0; ch < nchunks; ++ch, ++xj) {
                     const int s = xj % p.xstages;
                     if (!mbar_wait(&xempty[s], (static_cast<uint32_t>(xj / p.xstages) & 1u) ^ 1u)) {
@@ -372,6 +376,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
     }
 
     // ================= consumers (256 threads)
+    if (KIND == G_GEMV) pdl_wait();  // outputs are written after the previous kernel finished
     const int g = lane >> 2, tig = lane & 3;
     const int nsb = p.K >> 8;
     const saddr wring_s = smem_addr(wring), xring_s = smem_addr(xring);
@@ -473,8 +478,7 @@ cudaError_t launch_group_one(const GroupParams& p, int grid, int smem, cudaStrea
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    k_group<KIND, F><<<grid, kGroupThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k_group<KIND, F>, dim3(grid), dim3(kGroupThreads), smem, s, p);
 }
 
 }  // namespace ggq

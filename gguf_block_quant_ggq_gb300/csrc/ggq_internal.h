@@ -15,41 +15,20 @@ constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per CTA
 constexpr int kMaxDevices = 64;     // device ordinals with per-device launch state
 
-// Decode-size MoE plan (T <= 8, so at most 64 (token, slot) pairs).
-constexpr int kPlanMaxPairs = 64;
-constexpr int kPlanMaxTokens = 8;
-struct MoePlan {
-    int D;                                  // distinct experts selected
-    int err;                                // nonzero: an expert id was out of range
-    int expert[kPlanMaxPairs];              // expert id of distinct slot u
-    int npairs[kPlanMaxPairs];              // pairs routed to it
-    int pair[kPlanMaxPairs][kPlanMaxTokens];   // pair index p = t*k + j
-    int token[kPlanMaxPairs][kPlanMaxTokens];  // token of that pair
-    float wt[kPlanMaxTokens * 8];           // routing weight of pair p
-};
-
 enum Kind : int { KIND_GEMV = 0, KIND_DUMP = 1, KIND_GATEUP = 2, KIND_DOWN = 3 };
 
 struct StreamParams {
-    const uint8_t* W;   // weights: GEMV matrix, gate bank, or down bank
-    const uint8_t* W2;  // up bank (gate/up only)
+    const uint8_t* W;   // GEMV weight matrix
     int64_t rowbytes;   // bytes of one weight row
-    int64_t N;          // GEMV rows; MoE rows per expert (I for gate/up, H for down)
+    int64_t N;          // rows
     int K;              // input width
-    const uint8_t* xq;  // packed activations: GEMV [T][K/blk]; gate/up x^ [T][H/256]; down h^ [T*k][I/256]
+    const uint8_t* xq;  // packed activations [T][K/blk]
     int xrows;          // activation rows staged in shared memory
     int T;
-    int top_k;
-    float* Y;           // GEMV out [T][N]; down: y [T][H]
+    float* Y;           // out [T][N]
     int32_t* coefs;     // block-dot dump [T][N][K/blk*c]
-    const MoePlan* plan;
-    float* h;           // [T*k][I] fp32 (gate/up output)
-    float* g_dump;      // optional [T*k][I]
-    float* u_dump;      // optional [T*k][I]
-    uint8_t* hq;        // [T*k][I/256] Q8_K (gate/up quantizes h into it)
-    float* o;           // [T*k][H] down outputs
-    int* counters;      // last-CTA counters (self-resetting)
     int* err;           // device error word
+    int early_weights;  // 1: stream weights before waiting for the previous kernel
     int stages;
     int stage_stride;   // bytes per ring slot (multiple of 128)
     int x_bytes;        // bytes of the staged-activation region
@@ -100,10 +79,29 @@ struct GroupParams {
     float* u_dump;
     float* o;            // down [pairs][N]
     int* err;
+    int early_weights;   // 1: stream weights before waiting for the previous kernel (GEMV only)
     // shared-memory plan
     int wstages, wslot, wrow, wcontig;  // weight ring: slots, slot bytes, row stride, one contiguous copy
     int xstages, xslot, xstride, xcopy; // activation ring: slots, slot bytes, row stride, bytes per row copy
 };
+
+// Launch with the programmatic-dependent-launch attribute (the kernels call
+// pdl_wait before touching data of earlier kernels, so this is always safe).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Host launchers (one per kernel family); return the launch error.
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
@@ -120,8 +118,5 @@ cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* curso
 cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
                            cudaStream_t s);
 cudaError_t launch_combine(const float* o, const float* w, int T, int k, int64_t H, float* Y, cudaStream_t s);
-cudaError_t launch_moe_route(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
-                             int E, int k, int H, uint8_t* xq, MoePlan* plan, int32_t* ids_out, float* w_out,
-                             int* err, cudaStream_t s);
 
 }  // namespace ggq

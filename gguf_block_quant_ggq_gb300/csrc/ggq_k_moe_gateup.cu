@@ -1,25 +1,25 @@
-// ggq_k_moe_gateup.cu -- instantiations of the streaming kernel: decode MoE gateup stage.
-#include "ggq_stream.cuh"
+// ggq_k_moe_gateup.cu -- instantiations of the direct tiny-batch MoE route: gateup kernel.
+#include "ggq_direct.cuh"
 
 namespace ggq {
 
 template <int F>
-static cudaError_t launch_direct(int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
+static cudaError_t launch_direct_nt(int nt, const DirectParams& p, int grid, int smem, cudaStream_t s) {
     switch (nt) {  // the direct route serves at most 4 tokens
-    case 1: return launch_one<KIND_GATEUP, F, 1>(p, grid, smem, s);
-    case 2: return launch_one<KIND_GATEUP, F, 2>(p, grid, smem, s);
-    case 4: return launch_one<KIND_GATEUP, F, 4>(p, grid, smem, s);
+    case 1: return launch_direct_one<KIND_GATEUP, F, 1>(p, grid, smem, s);
+    case 2: return launch_direct_one<KIND_GATEUP, F, 2>(p, grid, smem, s);
+    case 4: return launch_direct_one<KIND_GATEUP, F, 4>(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_moe_gateup(int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
+cudaError_t launch_direct_gateup(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s) {
     switch (fmt) {
-    case F_Q8_0: return launch_direct<F_Q8_0>(nt, p, grid, smem, s);
-    case F_Q4_K: return launch_direct<F_Q4_K>(nt, p, grid, smem, s);
-    case F_Q5_K: return launch_direct<F_Q5_K>(nt, p, grid, smem, s);
-    case F_Q6_K: return launch_direct<F_Q6_K>(nt, p, grid, smem, s);
-    case F_MXFP4: return launch_direct<F_MXFP4>(nt, p, grid, smem, s);
+    case F_Q8_0: return launch_direct_nt<F_Q8_0>(nt, p, grid, smem, s);
+    case F_Q4_K: return launch_direct_nt<F_Q4_K>(nt, p, grid, smem, s);
+    case F_Q5_K: return launch_direct_nt<F_Q5_K>(nt, p, grid, smem, s);
+    case F_Q6_K: return launch_direct_nt<F_Q6_K>(nt, p, grid, smem, s);
+    case F_MXFP4: return launch_direct_nt<F_MXFP4>(nt, p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }

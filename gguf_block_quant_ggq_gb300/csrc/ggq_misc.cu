@@ -7,7 +7,7 @@
 // quantizers).  Dequantizer: the GGUF element formulas (FreeToken PR #136
 // "enable native GGUF kernels on ROCm", Summary: Q4_0 dequantization).
 // Router: softmax top-k with renormalisation; ids are chosen by logit, ties to
-// the lower expert index.
+// the lower expert index.  Also the expert-sorted route's grouping kernels.
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
 
@@ -16,6 +16,8 @@ namespace ggq {
 // ---------------------------------------------------------------- quantize
 
 __global__ void k_quant_q8k(const float* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (b >= nblocks) return;
@@ -23,6 +25,8 @@ __global__ void k_quant_q8k(const float* __restrict__ x, int64_t nblocks, uint8_
 }
 
 __global__ void k_quant_q8_1(const float* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (b >= nblocks) return;
@@ -35,9 +39,9 @@ cudaError_t launch_quantize(int act, const float* x, int64_t T, int64_t K, uint8
     const int threads = 256;
     const int64_t blocks = (nb * 32 + threads - 1) / threads;
     if (act == 0)
-        k_quant_q8_1<<<static_cast<unsigned>(blocks), threads, 0, s>>>(x, nb, out);
+        return launch_pdl(k_quant_q8_1, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, x, nb, out);
     else
-        k_quant_q8k<<<static_cast<unsigned>(blocks), threads, 0, s>>>(x, nb, out);
+        return launch_pdl(k_quant_q8k, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, x, nb, out);
     return cudaGetLastError();
 }
 
@@ -50,6 +54,8 @@ __device__ __forceinline__ float half_at(const uint8_t* p) {
 // One thread per weight block; element formulas of each GGUF format.
 template <int F>
 __global__ void k_dequant(const uint8_t* __restrict__ blocks, int64_t nblocks, float* __restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= nblocks) return;
     const uint8_t* b = blocks + i * fmt_bytes(F);
@@ -109,124 +115,13 @@ cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t rows, int64_t
     if (nb == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((nb + 127) / 128);
     switch (fmt) {
-    case F_Q4_0: k_dequant<F_Q4_0><<<grid, 128, 0, s>>>(blocks, nb, out); break;
-    case F_Q8_0: k_dequant<F_Q8_0><<<grid, 128, 0, s>>>(blocks, nb, out); break;
-    case F_Q4_K: k_dequant<F_Q4_K><<<grid, 128, 0, s>>>(blocks, nb, out); break;
-    case F_Q5_K: k_dequant<F_Q5_K><<<grid, 128, 0, s>>>(blocks, nb, out); break;
-    case F_Q6_K: k_dequant<F_Q6_K><<<grid, 128, 0, s>>>(blocks, nb, out); break;
-    default: k_dequant<F_MXFP4><<<grid, 128, 0, s>>>(blocks, nb, out); break;
+    case F_Q4_0: return launch_pdl(k_dequant<F_Q4_0>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    case F_Q8_0: return launch_pdl(k_dequant<F_Q8_0>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    case F_Q4_K: return launch_pdl(k_dequant<F_Q4_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    case F_Q5_K: return launch_pdl(k_dequant<F_Q5_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    case F_Q6_K: return launch_pdl(k_dequant<F_Q6_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    default: return launch_pdl(k_dequant<F_MXFP4>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
     }
-    return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------- decode MoE router + planner
-
-// CTA 0: warp t routes token t (softmax top-k by logit, ties to the lower
-// index, weights renormalised over the selected experts), then thread 0 groups
-// the T*k (token, slot) pairs by distinct expert.  Every CTA quantizes a share
-// of the T*H/256 Q8_K blocks of x.
-__global__ void __launch_bounds__(256) k_moe_route(const float* __restrict__ logits, const int32_t* __restrict__ ids_in,
-                                                   const float* __restrict__ w_in, const float* __restrict__ X, int T,
-                                                   int E, int k, int H, uint8_t* __restrict__ xq, MoePlan* plan,
-                                                   int32_t* ids_out, float* w_out, int* err) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // x^ = Q8_K(x): one warp per 256-block, all CTAs
-    {
-        const int nb = T * (H >> 8);
-        for (int b = blockIdx.x * 8 + warp; b < nb; b += gridDim.x * 8)
-            warp_quant_q8k(X + static_cast<int64_t>(b) * 256, xq + static_cast<int64_t>(b) * 292, lane);
-    }
-    if (blockIdx.x != 0) return;
-    __shared__ int s_ids[kPlanMaxPairs];
-    __shared__ float s_w[kPlanMaxPairs];
-    if (warp < T) {
-        const int t = warp;
-        if (logits) {
-            const float* l = logits + static_cast<int64_t>(t) * E;
-            // selection keeps a per-lane bitmask of taken experts (E <= 4096: 128 per lane)
-            uint32_t taken[4] = {0u, 0u, 0u, 0u};
-            float lmax = 0.0f, wsum = 0.0f;
-            float wj[8];
-            int idj[8];
-            for (int j = 0; j < k; ++j) {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
-                for (int i = 0, e = lane; e < E; ++i, e += 32) {
-                    if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
-                    const float v = l[e];
-                    if (v > bv || (v == bv && e < bi)) {
-                        bv = v;
-                        bi = e;
-                    }
-                }
-#pragma unroll
-                for (int s = 16; s >= 1; s >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
-                    if (ov > bv || (ov == bv && oi < bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                if ((bi & 31) == lane) {
-                    const int i = bi >> 5;
-                    taken[i >> 5] |= 1u << (i & 31);
-                }
-                if (j == 0) lmax = bv;
-                idj[j] = bi;
-                wj[j] = expf(bv - lmax);
-                wsum += wj[j];
-            }
-            if (lane == 0)
-                for (int j = 0; j < k; ++j) {
-                    s_ids[t * k + j] = idj[j];
-                    s_w[t * k + j] = wj[j] / wsum;
-                }
-        } else if (lane < k) {
-            s_ids[t * k + lane] = ids_in[t * k + lane];
-            s_w[t * k + lane] = w_in[t * k + lane];
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int D = 0, bad = 0;
-        for (int pp = 0; pp < T * k; ++pp) {
-            const int e = s_ids[pp];
-            ids_out[pp] = e;
-            w_out[pp] = s_w[pp];
-            plan->wt[pp] = s_w[pp];
-            if (e < 0 || e >= E) {
-                bad = 1;
-                continue;
-            }
-            int u = 0;
-            while (u < D && plan->expert[u] != e) ++u;
-            if (u == D) {
-                plan->expert[D] = e;
-                plan->npairs[D] = 0;
-                ++D;
-            }
-            const int n = plan->npairs[u];
-            if (n < kPlanMaxTokens) {
-                plan->pair[u][n] = pp;
-                plan->token[u][n] = pp / k;
-                plan->npairs[u] = n + 1;
-            } else {
-                bad = 1;  // more than kPlanMaxTokens pairs on one expert
-            }
-        }
-        plan->D = bad ? 0 : D;
-        plan->err = bad;
-        if (bad) set_error(err, 2);
-    }
-}
-
-cudaError_t launch_moe_route(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
-                             int E, int k, int H, uint8_t* xq, MoePlan* plan, int32_t* ids_out, float* w_out,
-                             int* err, cudaStream_t s) {
-    const int nb = T * (H >> 8);
-    const int grid = (nb + 7) / 8 > 1 ? (nb + 7) / 8 : 1;
-    k_moe_route<<<grid, 256, 0, s>>>(logits, ids_in, w_in, X, T, E, k, H, xq, plan, ids_out, w_out, err);
     return cudaGetLastError();
 }
 
@@ -240,6 +135,8 @@ namespace ggq {
 // with 16-byte bulk copies, so its activation rows start on 16-byte marks).
 __global__ void k_quant_q8k_pitched(const float* __restrict__ x, int64_t rows, int nbr, uint8_t* __restrict__ out,
                                     int64_t pitch) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (b >= rows * nbr) return;
@@ -251,9 +148,8 @@ cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uin
                                     cudaStream_t s) {
     const int64_t nb = rows * (K / 256);
     if (nb == 0) return cudaSuccess;
-    k_quant_q8k_pitched<<<static_cast<unsigned>((nb * 32 + 255) / 256), 256, 0, s>>>(x, rows, static_cast<int>(K / 256),
-                                                                                     out, pitch);
-    return cudaGetLastError();
+    return launch_pdl(k_quant_q8k_pitched, dim3(static_cast<unsigned>((nb * 32 + 255) / 256)), dim3(256), 0, s, x, rows,
+                      static_cast<int>(K / 256), out, pitch);
 }
 
 // One warp per token: top-k by logit (ties to the lower index) and the
@@ -265,6 +161,8 @@ __global__ void __launch_bounds__(256) k_route_sorted(const float* __restrict__ 
                                                       const float* __restrict__ w_in, const float* __restrict__ X,
                                                       int T, int E, int k, int H, uint8_t* __restrict__ xq,
                                                       int64_t x_pitch, int32_t* ids, float* w, int* counts, int* err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -339,15 +237,16 @@ cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, cons
                                 int* counts, int* err, cudaStream_t s) {
     const int warps = T > T * (H >> 8) ? T : T * (H >> 8);
     const int grid = (warps + 7) / 8 < 1184 ? (warps + 7) / 8 : 1184;
-    k_route_sorted<<<grid > 0 ? grid : 1, 256, 0, s>>>(logits, ids_in, w_in, X, T, E, k, H, xq, x_pitch, ids, w,
-                                                       counts, err);
-    return cudaGetLastError();
+    return launch_pdl(k_route_sorted, dim3(grid > 0 ? grid : 1), dim3(256), 0, s, logits, ids_in, w_in, X, T, E, k, H,
+                      xq, x_pitch, ids, w, counts, err);
 }
 
 // One CTA: exclusive scan of the expert counts, the list of non-empty experts
 // (the groups of the grouped kernel) and zeroed scatter cursors.
 __global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ counts, int E, int* offsets, int* cursor,
                                                      int* ngroups, int* group_expert, int* group_off, int* group_cnt) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int s_sum[1024];
     __shared__ int s_ne[1024];
     const int tid = threadIdx.x;
@@ -394,14 +293,16 @@ __global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ cou
 
 cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
                               int* group_off, int* group_cnt, cudaStream_t s) {
-    k_group_plan<<<1, 1024, 0, s>>>(counts, E, offsets, cursor, ngroups, group_expert, group_off, group_cnt);
-    return cudaGetLastError();
+    return launch_pdl(k_group_plan, dim3(1), dim3(1024), 0, s, counts, E, offsets, cursor, ngroups, group_expert,
+                      group_off, group_cnt);
 }
 
 // Scatter pair p to its expert's range.  The order inside a range does not
 // matter: every column of the grouped kernel is computed on its own.
 __global__ void k_scatter(const int32_t* __restrict__ ids, int P, int E, const int* __restrict__ offsets, int* cursor,
                           int* perm) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p >= P) return;
     const int e = ids[p];
@@ -412,13 +313,14 @@ __global__ void k_scatter(const int32_t* __restrict__ ids, int P, int E, const i
 cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
                            cudaStream_t s) {
     if (P == 0) return cudaSuccess;
-    k_scatter<<<(P + 255) / 256, 256, 0, s>>>(ids, P, E, offsets, cursor, perm);
-    return cudaGetLastError();
+    return launch_pdl(k_scatter, dim3((P + 255) / 256), dim3(256), 0, s, ids, P, E, offsets, cursor, perm);
 }
 
 // y[t][n] = sum_j w[t][j] * o[t*k + j][n], slots in order.
 __global__ void k_combine(const float* __restrict__ o, const float* __restrict__ w, int T, int k, int64_t H,
                           float* __restrict__ Y) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= T * H) return;
     const int64_t t = i / H, n = i - t * H;
@@ -430,8 +332,7 @@ __global__ void k_combine(const float* __restrict__ o, const float* __restrict__
 cudaError_t launch_combine(const float* o, const float* w, int T, int k, int64_t H, float* Y, cudaStream_t s) {
     const int64_t n = T * H;
     if (n == 0) return cudaSuccess;
-    k_combine<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(o, w, T, k, H, Y);
-    return cudaGetLastError();
+    return launch_pdl(k_combine, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s, o, w, T, k, H, Y);
 }
 
 }  // namespace ggq

@@ -1,5 +1,6 @@
-// ggq_stream.cuh -- the weight-streaming kernel behind the decode GEMV, the
-// block-dot dump and the decode-size MoE gate/up and down stages.
+// ggq_stream.cuh -- the weight-streaming kernel behind the decode GEMV at 1-2
+// tokens and the block-dot dump; its consumer (row_accumulate) also serves the
+// direct tiny-batch MoE route (ggq_direct.cuh).
 //
 // HBM-bound design for sm_103a:
 //   * one CTA per SM (persistent: items blockIdx.x, +gridDim.x, ...);
@@ -100,11 +101,34 @@ __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, con
 }
 
 // Accumulate one row against the activation rows xr[0..nslots) into acc[].
+// For 1-2 slots two units per lane are kept in flight (units u and u+32) so
+// that their load, decode and dp4a chains overlap.
 template <int F, int NT>
 __device__ __forceinline__ void row_accumulate(saddr row, const XS& xs, const int* xr, int nslots,
                                                float* acc, int lane) {
     const int nu = units_per_row(xs.K), nb32 = xs.K >> 5;
-    for (int u = lane; u < nu; u += 32) {
+    int u = lane;
+    // two units in flight for 1-2 slots; at 4+ slots the slot loop supplies the
+    // independent work and a second unit would only spill (17 warps cap a
+    // thread at 96 registers)
+    for (; NT <= 2 && u + 32 < nu; u += 64) {
+        Unit ua, ub;
+        load_unit<F>(row, u, nb32, ua);
+        load_unit<F>(row, u + 32, nb32, ub);
+        int xa[4], xb[4];
+        unit_offsets<F>(u, xa);
+        unit_offsets<F>(u + 32, xb);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            if (j < nslots) {
+                int A0, A1, B0, B1;
+                unit_ints<F>(ua, xa, xs, xr[j], u, A0, A1);
+                unit_ints<F>(ub, xb, xs, xr[j], u + 32, B0, B1);
+                acc[j] += unit_value<F>(ua, xs, xr[j], u, A0, A1) + unit_value<F>(ub, xs, xr[j], u + 32, B0, B1);
+            }
+        }
+    }
+    for (; u < nu; u += 32) {
         Unit un;
         load_unit<F>(row, u, nb32, un);
         int xo[4];
@@ -173,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     constexpr int LV = NT == 1 ? 0 : NT == 2 ? 1 : NT == 4 ? 2 : 3;  // log2(NT)
     constexpr int SH = 5 - LV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();
 
     // ---- shared memory layout: ring | activations | barriers | misc
     uint8_t* ring = smem;
@@ -181,21 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     const XRegion xr_ = x_region(xreg, p.xrows, K, Q81);
     uint64_t* full = reinterpret_cast<uint64_t*>(xreg + p.x_bytes);
     uint64_t* empty = full + kMaxStages;
-    int* s_flag = reinterpret_cast<int*>(empty + kMaxStages);  // [0] last-CTA flag, [1] abort
-    float* s_gu = reinterpret_cast<float*>(s_flag + 4);        // [2][8][NT] gate/up exchange
+    int* s_flag = reinterpret_cast<int*>(empty + kMaxStages);  // [1] abort
 
-    // ---- work items
-    int nitems;
-    int D = 0;
-    if constexpr (KIND == KIND_GEMV || KIND == KIND_DUMP) {
-        nitems = static_cast<int>((p.N + kTileRows - 1) / kTileRows);
-    } else if constexpr (KIND == KIND_GATEUP) {
-        D = p.plan->D;
-        nitems = D * static_cast<int>(p.N / (kTileRows / 2));
-    } else {
-        D = p.plan->D;
-        nitems = D * static_cast<int>(p.N / kTileRows);
-    }
+    // ---- work items: 16-row tiles
+    const int nitems = static_cast<int>((p.N + kTileRows - 1) / kTileRows);
     if (static_cast<int>(blockIdx.x) >= nitems) return;  // whole CTA idle (uniform)
 
     if (tid == 0) {
@@ -216,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         // ================= producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            if (!p.early_weights) pdl_wait();  // the previous kernel may still be writing the weights
             int j = 0;
             for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
                 const int s = j % p.stages;
@@ -232,20 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                     const int64_t nr = p.N - r0 < kTileRows ? p.N - r0 : kTileRows;
                     src[0] = p.W + r0 * p.rowbytes;
                     bytes[0] = static_cast<uint32_t>(nr * p.rowbytes);
-                } else if constexpr (KIND == KIND_GATEUP) {
-                    const int nt = static_cast<int>(p.N / (kTileRows / 2));
-                    const int u = item / nt, tile = item - u * nt;
-                    const int64_t e = p.plan->expert[u];
-                    const int64_t off = (e * p.N + static_cast<int64_t>(tile) * (kTileRows / 2)) * p.rowbytes;
-                    src[0] = p.W + off;
-                    src[1] = p.W2 + off;
-                    bytes[0] = bytes[1] = static_cast<uint32_t>((kTileRows / 2) * p.rowbytes);
-                    ncopy = 2;
-                } else {
-                    const int u = item % D, tile = item / D;
-                    const int64_t e = p.plan->expert[u];
-                    src[0] = p.W + (e * p.N + static_cast<int64_t>(tile) * kTileRows) * p.rowbytes;
-                    bytes[0] = static_cast<uint32_t>(kTileRows * p.rowbytes);
                 }
                 uint8_t* dst = ring + static_cast<size_t>(s) * p.stage_stride;
                 uint32_t total = 0;
@@ -277,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
 
     // ================= consumers (512 threads)
     const int ctid = tid;
+    pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
     stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
     consumer_sync();
     XS xs;
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         }
         const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
 
-        if constexpr (KIND == KIND_GEMV || KIND == KIND_DUMP) {
+        {
             const int64_t r = static_cast<int64_t>(item) * kTileRows + warp;
             int xr[NT];
 #pragma unroll
@@ -318,101 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-        } else if constexpr (KIND == KIND_GATEUP) {
-            const int nt = static_cast<int>(p.N / (kTileRows / 2));
-            const int u = item / nt, tile = item - u * nt;
-            const int np = p.plan->npairs[u];
-            int xr[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t) xr[t] = t < np ? p.plan->token[u][t] : 0;
-            const int half = warp >> 3, rr = warp & 7;  // warps 0..7: gate rows, 8..15: up rows
-            if (ready) {
-                float acc[NT];
-#pragma unroll
-                for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
-                row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
-                const float v = warp_transpose_reduce<LV>(acc, lane);
-                const int t = lane >> SH;
-                if ((lane & ((1 << SH) - 1)) == 0) s_gu[(half * 8 + rr) * NT + t] = v;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            consumer_sync();
-            if (ready && ctid < 8 * NT) {
-                const int row_l = ctid / NT, t = ctid - row_l * NT;
-                if (t < np) {
-                    const float gval = s_gu[row_l * NT + t], uval = s_gu[(8 + row_l) * NT + t];
-                    const float hval = __fmul_rn(__fdiv_rn(gval, 1.0f + expf(-gval)), uval);
-                    const int64_t o = static_cast<int64_t>(p.plan->pair[u][t]) * p.N +
-                                      static_cast<int64_t>(tile) * (kTileRows / 2) + row_l;
-                    p.h[o] = hval;
-                    if (p.g_dump) p.g_dump[o] = gval;
-                    if (p.u_dump) p.u_dump[o] = uval;
-                }
-            }
-            // last CTA to finish a 256-row block of this expert quantizes h there
-            __threadfence();
-            consumer_sync();
-            const int nblk = static_cast<int>(p.N >> 8);
-            const int blk = static_cast<int>((static_cast<int64_t>(tile) * (kTileRows / 2)) >> 8);
-            if (ctid == 0) {
-                const int old = atomicAdd(&p.counters[u * nblk + blk], 1);
-                s_flag[0] = (old == 256 / (kTileRows / 2) - 1);
-            }
-            consumer_sync();
-            if (s_flag[0]) {
-                __threadfence();
-                for (int q = warp; q < np; q += kConsumerWarps) {
-                    const int pp = p.plan->pair[u][q];
-                    warp_quant_q8k(p.h + static_cast<int64_t>(pp) * p.N + 256 * blk,
-                                   p.hq + (static_cast<int64_t>(pp) * nblk + blk) * 292, lane);
-                }
-                if (ctid == 0) p.counters[u * nblk + blk] = 0;
-            }
-            if (s_flag[1]) break;
-        } else {  // KIND_DOWN
-            const int u = item % D, tile = item / D;
-            const int np = p.plan->npairs[u];
-            int xr[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t) xr[t] = t < np ? p.plan->pair[u][t] : 0;
-            if (ready) {
-                float acc[NT];
-#pragma unroll
-                for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
-                row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
-                const float v = warp_transpose_reduce<LV>(acc, lane);
-                const int t = lane >> SH;
-                if ((lane & ((1 << SH) - 1)) == 0 && t < np) {
-                    const int64_t r = static_cast<int64_t>(tile) * kTileRows + warp;
-                    p.o[static_cast<int64_t>(xr[t]) * p.N + r] = v;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            // last of the D experts of this row tile combines y = sum_j w_j o_j
-            __threadfence();
-            consumer_sync();
-            if (ctid == 0) {
-                const int old = atomicAdd(&p.counters[tile], 1);
-                s_flag[0] = (old == D - 1);
-            }
-            consumer_sync();
-            if (s_flag[0]) {
-                __threadfence();
-                for (int i = ctid; i < kTileRows * p.T; i += kConsumerWarps * 32) {
-                    const int t = i / kTileRows;
-                    const int64_t r = static_cast<int64_t>(tile) * kTileRows + (i - t * kTileRows);
-                    float acc = 0.0f;
-                    for (int q = 0; q < p.top_k; ++q) {
-                        const int pp = t * p.top_k + q;
-                        acc += p.plan->wt[pp] * __ldcg(&p.o[static_cast<int64_t>(pp) * p.N + r]);
-                    }
-                    p.Y[static_cast<int64_t>(t) * p.N + r] = acc;
-                }
-                if (ctid == 0) p.counters[tile] = 0;
-            }
-            if (s_flag[1]) break;
         }
     }
 }
@@ -431,8 +338,7 @@ cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    k_stream<KIND, F, NT><<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k_stream<KIND, F, NT>, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
 template <int KIND, int F>

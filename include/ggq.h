@@ -142,6 +142,17 @@ ggq_status ggq_reserve(ggq_ctx* ctx, const ggq_plan* plan, void* stream);
 /* Current pool size in bytes. */
 size_t ggq_scratch_bytes(const ggq_ctx* ctx);
 
+/* Declare that no kernel writes any weight buffer passed to this context while
+ * calls of the context are in flight (the usual case in inference).  Every
+ * kernel of the library is launched with programmatic dependent launch: it
+ * may start while the previous kernel in the stream is finishing, and waits
+ * for that kernel before it reads activations or writes outputs.  With static
+ * weights the GEMV kernels also start streaming their weights before that
+ * wait, overlapping one call's weight reads with the previous call's tail.
+ * Default 0 (weights are read only after the wait).  Takes effect for calls
+ * enqueued after it. */
+ggq_status ggq_set_static_weights(ggq_ctx* ctx, int static_weights);
+
 /* Per-format availability: 1 if (weight format w, activation format act, op)
  * runs on this library, else 0.  For GGQ_OP_QUANTIZE_ACT w is ignored and act
  * is Q8_1 or Q8_K; for GGQ_OP_DEQUANT act is ignored.  Callers decide at load
