@@ -507,6 +507,8 @@ def profile_case(args):
           one at T=8, over 5 rotating weight copies (165 MB for Q4_K > L2).
     moe:  the MoE decode layer (128 experts, H 2048, I 768, Q4_K/Q6_K, top-8)
           at T tokens: 2 warm-up layers, then 1 layer.
+    mxfp4: the MXFP4 expert layer (256 experts, H 4096, I 2048, top-8) at T
+          tokens: 2 warm-up layers, then 1 layer.
     prefill: the expert-sorted route on the prefill workload at T tokens
           (128 experts, H 4096, I 1536, Q8_0 gate/up, Q4_K down, Zipf 1.1)."""
     import torch
@@ -526,7 +528,7 @@ def profile_case(args):
         ctx.mul_mat_vec_q(fmt, Ws[4], N, K, xq[1], 1)
         ctx.mul_mat_vec_q(fmt, Ws[0], N, K, xq[8], 8)
     else:
-        cfg = syn.MOE_DECODE if args.profile_case == "moe" else syn.MOE_PREFILL
+        cfg = {"moe": syn.MOE_DECODE, "mxfp4": syn.MOE_MXFP4, "prefill": syn.MOE_PREFILL}[args.profile_case]
         E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
         g = syn.rng(cfg["index"], 1)
         banks = [torch.from_numpy(syn.expert_bank(cfg[n], E, r, c, g)).cuda()
@@ -551,7 +553,7 @@ def main():
     ap.add_argument("--impl", default="ggq", choices=["ggq", "reference"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["gemv", "moe", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["gemv", "moe", "mxfp4", "prefill"], default=None,
                     help="run a small launch sequence for an ncu capture instead of the benchmark")
     ap.add_argument("--fmt", default="Q4_K")
     ap.add_argument("--tokens", type=int, default=1)

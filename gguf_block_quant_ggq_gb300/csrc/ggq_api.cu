@@ -252,9 +252,57 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
     return GGQ_OK;
 }
 
+// Shared-memory plan of the tensor-path decode GEMV (2-8 tokens); false when
+// the shape is not covered (rows not a multiple of 16 bytes, K above 16 chunks
+// of 256, Q6_K chunks below 128 inputs, or no room for two stages).
+bool plan_mmav(int f, MmavParams& p, int* smem) {
+    if (p.rowbytes % 16 != 0 || p.K > 16 * 256 || p.K % 256 != 0) return false;
+    int chunk = 64;
+    while (p.K / chunk > 16) chunk *= 2;
+    if (f == F_Q6_K && chunk < 128) chunk = 128;
+    p.chunk = chunk;
+    p.nch = p.K / chunk;
+    p.wrow = bank_stride(2 * p.rowbytes);  // one stride per pair of rows
+    p.stage_stride = static_cast<int>(align_up(static_cast<size_t>(kTileRows / 2 * p.wrow + 16), 128));
+    const int red_bytes = 2 * kConsumerWarps * 130 * 4, x_bytes = p.T * p.xrow;  // partials: [2][16][130] floats
+    p.x_bytes = static_cast<int>(align_up(static_cast<size_t>(red_bytes > x_bytes ? red_bytes : x_bytes), 128));
+    p.x_bulk = (x_bytes % 16 == 0 && aligned16(p.xq)) ? 1 : 0;
+    const int fixed = p.x_bytes + kConsumerWarps * 4 * 16 * 4 + (2 * kMaxStages + 1) * 8 + 256;
+    int stages = (kSmemLimit - fixed) / p.stage_stride;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return false;
+    p.stages = stages;
+    *smem = stages * p.stage_stride + fixed;
+    return true;
+}
+
+// Smallest token count that the decode GEMV sends to the tensor path.
+constexpr int kMmaMinTokens = 2;
+
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st) {
     const int f = fmt_of(w);
+    if (kind == KIND_GEMV && T >= kMmaMinTokens && f != F_Q4_0 && aligned16(Xq)) {
+        MmavParams m{};
+        m.W = static_cast<const uint8_t*>(W);
+        m.rowbytes = w_row_bytes(f, K);
+        m.N = N;
+        m.K = static_cast<int>(K);
+        m.xq = static_cast<const uint8_t*>(Xq);
+        m.xrow = static_cast<int>(K / 256 * 292);
+        m.T = static_cast<int>(T);
+        m.Y = Y;
+        m.err = &c->ctrl->err;
+        m.early_weights = c->static_weights;
+        int smem = 0;
+        if (plan_mmav(f, m, &smem)) {
+            const int64_t tiles = (N + kTileRows - 1) / kTileRows;
+            const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
+            cudaError_t e = launch_mmav(f, m, grid, smem, st);
+            if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec tensor-path launch");
+            return GGQ_OK;
+        }
+    }
     if (kind == KIND_GEMV && T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
         // several activation columns: the int8 tensor-core kernel (Q8_K rows are 16-byte multiples)
         GroupParams g{};

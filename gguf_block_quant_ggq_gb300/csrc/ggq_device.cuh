@@ -421,6 +421,199 @@ __device__ __forceinline__ float unit_value(const Unit& un, const XS& xs, int r,
     }
 }
 
+// ---------------------------------------------------------------- one token, activations in registers
+
+// dp4a with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// A single token's activations for one 64-weight unit, loaded once per kernel
+// and kept in registers: the lane that owns unit u reads the same 64 quants for
+// every row.  x[4g..4g+3] pair with weight group g (the unit's group order);
+// c[] are the integer offsets of the format's epilogue (Q4_0: 8 * sum q per
+// block, MXFP4: 12 * sum q per block, Q4_K/Q5_K: sum q per sub-block for the
+// mins, Q6_K: 32 * sum q per group of 16); d0/d1 the activation scales.
+struct XUnit {
+    uint32_t x[16];
+    int c[4];
+    float d0, d1;
+};
+
+template <int F>
+__device__ __forceinline__ void load_xunit(const XS& xs, int u, XUnit& xu) {
+    const int nb32 = xs.K >> 5;
+    int xo[4];
+    unit_offsets<F>(u, xo);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint4 v = ld_s128(xs.q + xq_addr(xo[g]));
+        xu.x[4 * g] = v.x;
+        xu.x[4 * g + 1] = v.y;
+        xu.x[4 * g + 2] = v.z;
+        xu.x[4 * g + 3] = v.w;
+    }
+    const bool two = 2 * u + 1 < nb32;
+    const int s0 = static_cast<int>(ld_s32(xs.s32 + 8u * u));
+    const int s1 = two ? static_cast<int>(ld_s32(xs.s32 + 8u * u + 4)) : 0;
+    xu.c[0] = xu.c[1] = xu.c[2] = xu.c[3] = 0;
+    if constexpr (F == F_Q4_0) {
+        xu.d0 = ld_f32(xs.d + 8u * u);
+        xu.d1 = two ? ld_f32(xs.d + 8u * u + 4) : 0.0f;
+        xu.c[0] = 8 * s0;
+        xu.c[1] = 8 * s1;
+    } else {
+        xu.d0 = ld_f32(xs.d + 4u * static_cast<uint32_t>(u >> 2));
+        xu.d1 = 0.0f;
+        if constexpr (F == F_MXFP4) {
+            xu.c[0] = 12 * s0;
+            xu.c[1] = 12 * s1;
+        } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
+            xu.c[0] = s0;
+            xu.c[1] = s1;
+        } else if constexpr (F == F_Q6_K) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) xu.c[g] = 32 * ld_s16(xs.bs + 2u * static_cast<uint32_t>(xo[g] >> 4));
+        }
+    }
+}
+
+// fp32 contribution of unit u of a row (shared memory) against one token's
+// register-resident activations.  High nibbles are masked in place (16x their
+// value, as unsigned bytes) and the exact factor 16 is shifted out of the
+// integer sum, which saves a shift per weight word.
+template <int F>
+__device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const XUnit& xu) {
+    if constexpr (F == F_Q4_0) {
+        const saddr b = row + 36u * u;
+        const bool two = 2 * u + 1 < nb32;
+        uint32_t q0[4], q1[4];
+        ld_words_any<4>(b + 2, q0);
+        const float da = ld_h(b);
+        float db = 0.0f;
+        if (two) {
+            ld_words_any<4>(b + 20, q1);
+            db = ld_h(b + 18);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q1[k] = 0u;
+        }
+        int l0 = 0, h0 = 0, l1 = 0, h1 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            l0 = __dp4a(static_cast<int>(q0[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[k]), l0);
+            h0 = dp4a_us(q0[k] & 0xF0F0F0F0u, xu.x[4 + k], h0);
+            l1 = __dp4a(static_cast<int>(q1[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[8 + k]), l1);
+            h1 = dp4a_us(q1[k] & 0xF0F0F0F0u, xu.x[12 + k], h1);
+        }
+        const int A0 = l0 + (h0 >> 4) - xu.c[0];
+        const int A1 = l1 + (h1 >> 4) - xu.c[1];
+        return static_cast<float>(A0) * (da * xu.d0) + static_cast<float>(A1) * (db * xu.d1);
+    } else if constexpr (F == F_Q8_0) {
+        const saddr b = row + 68u * u;
+        const bool two = 2 * u + 1 < nb32;
+        uint32_t w[16];
+        ld_words_any<8>(b + 2, w);
+        const float da = ld_h(b);
+        float db = 0.0f;
+        if (two) {
+            ld_words_any<8>(b + 36, w + 8);
+            db = ld_h(b + 34);
+        } else {
+#pragma unroll
+            for (int k = 8; k < 16; ++k) w[k] = 0u;
+        }
+        int S0 = 0, S1 = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            S0 = __dp4a(static_cast<int>(w[k]), static_cast<int>(xu.x[k]), S0);
+            S1 = __dp4a(static_cast<int>(w[8 + k]), static_cast<int>(xu.x[8 + k]), S1);
+        }
+        return xu.d0 * (static_cast<float>(S0) * da + static_cast<float>(S1) * db);
+    } else if constexpr (F == F_MXFP4) {
+        const saddr b = row + 34u * u;
+        const bool two = 2 * u + 1 < nb32;
+        uint32_t q0[4], q1[4];
+        ld_words_any<4>(b + 1, q0);
+        const float da = e8m0_half_scale(ld_u8(b));
+        float db = 0.0f;
+        if (two) {
+            ld_words_any<4>(b + 18, q1);
+            db = e8m0_half_scale(ld_u8(b + 17));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q1[k] = 0u;
+        }
+        int S0 = 0, S1 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            S0 = __dp4a(static_cast<int>(mx_lookup(q0[k] & 0xFFFFu)), static_cast<int>(xu.x[2 * k]), S0);
+            S0 = __dp4a(static_cast<int>(mx_lookup(q0[k] >> 16)), static_cast<int>(xu.x[2 * k + 1]), S0);
+            S1 = __dp4a(static_cast<int>(mx_lookup(q1[k] & 0xFFFFu)), static_cast<int>(xu.x[8 + 2 * k]), S1);
+            S1 = __dp4a(static_cast<int>(mx_lookup(q1[k] >> 16)), static_cast<int>(xu.x[8 + 2 * k + 1]), S1);
+        }
+        return xu.d0 * (static_cast<float>(S0 - xu.c[0]) * da + static_cast<float>(S1 - xu.c[1]) * db);
+    } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
+        const int sb = u >> 2, cc = u & 3;
+        const saddr b = row + (F == F_Q4_K ? 144u : 176u) * sb;
+        const uint4 hd = ld_s128(b);
+        const saddr qsp = b + (F == F_Q4_K ? 16u : 48u) + 32u * cc;
+        const uint4 qa = ld_s128(qsp), qb = ld_s128(qsp + 16);
+        const float da = half_lo(hd.x), dm = half_hi(hd.x);
+        const uint32_t a0 = hd.y, a1 = hd.z, a2 = hd.w;
+        const uint32_t scw = cc < 2 ? (a0 & 0x3F3F3F3Fu) : ((a2 & 0x0F0F0F0Fu) | ((a0 >> 2) & 0x30303030u));
+        const uint32_t mw = cc < 2 ? (a1 & 0x3F3F3F3Fu) : (((a2 >> 4) & 0x0F0F0F0Fu) | ((a1 >> 2) & 0x30303030u));
+        const int sh = 16 * (cc & 1);
+        const int s0 = (scw >> sh) & 0xFF, s1 = (scw >> (sh + 8)) & 0xFF;
+        const int m0 = (mw >> sh) & 0xFF, m1 = (mw >> (sh + 8)) & 0xFF;
+        const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        int lo = 0, hi = 0;
+        if constexpr (F == F_Q4_K) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                lo = __dp4a(static_cast<int>(q[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[k]), lo);
+                hi = dp4a_us(q[k] & 0xF0F0F0F0u, xu.x[8 + k], hi);
+            }
+            hi >>= 4;
+        } else {
+            const uint4 ha = ld_s128(b + 16), hb = ld_s128(b + 32);
+            const uint32_t hq[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t h = hq[k] >> (2 * cc);
+                lo = __dp4a(static_cast<int>((q[k] & 0x0F0F0F0Fu) | ((h << 4) & 0x10101010u)), static_cast<int>(xu.x[k]), lo);
+                hi = __dp4a(static_cast<int>(((q[k] >> 4) & 0x0F0F0F0Fu) | ((h << 3) & 0x10101010u)),
+                            static_cast<int>(xu.x[8 + k]), hi);
+            }
+        }
+        const int A0 = s0 * lo + s1 * hi;
+        const int A1 = m0 * xu.c[0] + m1 * xu.c[1];
+        return xu.d0 * (da * static_cast<float>(A0) - dm * static_cast<float>(A1));
+    } else {  // F_Q6_K (element layout as in load_unit)
+        const int sb = u >> 2, v = u & 3, h = v >> 1, g1 = v & 1;
+        const saddr b = row + 210u * sb;
+        uint32_t ql[8], qh[8];
+        ld_words_any<8>(b + 64 * h + 32 * g1, ql);
+        ld_words_any<8>(b + 128 + 32 * h, qh);
+        const int j0 = 8 * h + 2 * g1;
+        const int sc0 = ld_s8(b + 192 + j0), sc1 = ld_s8(b + 192 + j0 + 1);
+        const int sc2 = ld_s8(b + 192 + j0 + 4), sc3 = ld_s8(b + 192 + j0 + 5);
+        const float da = ld_h(b + 208);
+        int S[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t lo = (ql[k] & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1)) & 0x03030303u) << 4);
+            const uint32_t hi = ((ql[k] >> 4) & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1 + 4)) & 0x03030303u) << 4);
+            S[k >> 2] = __dp4a(static_cast<int>(lo), static_cast<int>(xu.x[k]), S[k >> 2]);
+            S[2 + (k >> 2)] = __dp4a(static_cast<int>(hi), static_cast<int>(xu.x[8 + k]), S[2 + (k >> 2)]);
+        }
+        const int A0 = sc0 * (S[0] - xu.c[0]) + sc1 * (S[1] - xu.c[1]) + sc2 * (S[2] - xu.c[2]) + sc3 * (S[3] - xu.c[3]);
+        return static_cast<float>(A0) * (xu.d0 * da);
+    }
+}
+
 // ---------------------------------------------------------------- reductions
 
 // Sum each of V = 2^L per-lane values across the warp.  Afterwards lane l holds

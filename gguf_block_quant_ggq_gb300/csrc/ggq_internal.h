@@ -85,6 +85,29 @@ struct GroupParams {
     int xstages, xslot, xstride, xcopy; // activation ring: slots, slot bytes, row stride, bytes per row copy
 };
 
+// Decode GEMV at 2-8 tokens on the int8 tensor path (ggq_mmav.cuh): the
+// streaming geometry above, rows copied one by one into bank-padded rows, K
+// split into one chunk per consumer warp.
+struct MmavParams {
+    const uint8_t* W;
+    int64_t rowbytes;   // bytes of one weight row in global (a multiple of 16)
+    int64_t N;
+    int K;
+    const uint8_t* xq;  // packed Q8_K rows [T][K/256]
+    int xrow;           // bytes between activation rows
+    int T;
+    float* Y;           // [T][N]
+    int* err;
+    int early_weights;
+    int stages;
+    int stage_stride;
+    int x_bytes;        // shared region: staged activations, then the partials
+    int x_bulk;         // 1: the activation rows arrive by one bulk copy (16-byte multiple)
+    int wrow;           // stride of a pair of rows in shared memory (padded)
+    int chunk;          // inputs per consumer warp (64, 128 or 256)
+    int nch;            // chunks (<= 16)
+};
+
 // Launch with the programmatic-dependent-launch attribute (the kernels call
 // pdl_wait before touching data of earlier kernels, so this is always safe).
 template <typename... KArgs, typename... Args>
@@ -108,6 +131,7 @@ cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int 
 cudaError_t launch_quantize(int act, const float* x, int64_t T, int64_t K, uint8_t* out, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t rows, int64_t K, float* out, cudaStream_t s);
 cudaError_t launch_group(int kind, int fmt, const GroupParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_mmav(int fmt, const MmavParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
                                     cudaStream_t s);
 cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,

@@ -1,0 +1,608 @@
+// ggq_mmav.cuh -- the decode GEMV at 2-8 tokens on the int8 tensor path.
+//
+// y[t][n] = sum over blocks of (weight scale) * (activation scale) * (exact
+// int32 block dot), as in the keep-quant matmul of vllm.cpp PR #523 "grouped +
+// non-grouped keep-quant expert GEMM" (What changed: DotQ8_0/DotQ4K/DotQ5K/
+// DotQ6K superblock dots), with the integer dots of 16 rows x 8 token columns
+// x 32 inputs done by one mma.sync.m16n8k32 (Q6_K: m16n8k16, one per 16-group
+// because every 16 weights carry their own scale).
+//
+// Layout on the SM:
+//   * one CTA per SM; a producer warp copies each 16-row tile of W into a ring
+//     of shared-memory stages, one bulk copy per pair of rows (eight lanes
+//     issue the eight copies of a tile at once), pairs padded so that the
+//     eight even rows fall on distinct bank quads; mma row g is tile row 2g and
+//     mma row g + 8 is tile row 2g + 1, so every fragment load is conflict-free;
+//   * sixteen consumer warps split K into sixteen chunks of 64, 128 or 256
+//     inputs.  A warp's chunk never changes, so its activation fragments (the
+//     mma B operand), activation scales and per-block sums are loaded once into
+//     registers, straight from the packed Q8_K rows in global memory;
+//   * per tile each warp produces a 16 x 8 partial of its chunk; partials meet
+//     in a double-buffered shared array behind one barrier per tile.
+// Every wait is bounded; on timeout the kernel records an error word, drains
+// its copies and returns.
+#pragma once
+#include "ggq_device.cuh"
+#include "ggq_internal.h"
+
+namespace ggq {
+
+constexpr int kRedStride = 130;  // floats per warp in the partials buffer
+
+__device__ __forceinline__ void mmav_start_arrive() { asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void mmav_start_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory"); }
+
+__device__ __forceinline__ void mmav_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
+
+__device__ __forceinline__ void mma_k32_s8(int* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                           uint32_t b1, int c0, int c1) {
+    asm(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(c0), "r"(c1));
+}
+
+// A as unsigned bytes (high nibbles masked in place: 16x their value).
+__device__ __forceinline__ void mma_k32_u8(int* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                           uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
+}
+
+// Q6_K codes are unsigned (0..63): A as u8, C = -32 * (sum of the 16 quants).
+__device__ __forceinline__ void mma_k16_u8(int* d, uint32_t a0, uint32_t a1, uint32_t b0, int c0, int c1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%7,%8};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0), "r"(c0), "r"(c1));
+}
+
+// (a & mask) | c in one LOP3 (mask an immediate, c a register).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+
+// Byte i of w, zero-extended / sign-extended (i a compile-time constant after unrolling).
+__device__ __forceinline__ int byte_u(uint32_t w, int i) { return static_cast<int>(prmt(w, 0u, 0x4440u | i)); }
+__device__ __forceinline__ int byte_s(uint32_t w, int i) {
+    const uint32_t s = 0x8u | static_cast<uint32_t>(i);
+    return static_cast<int>(prmt(w, 0u, (s << 12) | (s << 8) | (s << 4) | static_cast<uint32_t>(i)));
+}
+
+// m16n8k16 with f16 operands and f32 accumulation.  Used with integer-valued
+// operands only (weight codes and int8 activations are exact in f16); every
+// product is exact and so is every partial sum below 2^24.
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four signed bytes (x0 x1 x2 x3) -> f16 pairs (x0, x2) and (x1, x3):
+// 1024 + (x + 128) built in the mantissa, then 1152 subtracted (exact).
+__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& p02, uint32_t& p13) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+    const uint32_t a = prmt(u, 0u, 0x4240u) | 0x64006400u, b = prmt(u, 0u, 0x4341u) | 0x64006400u;
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), off);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), off);
+    p02 = *reinterpret_cast<const uint32_t*>(&ha);
+    p13 = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+__device__ __forceinline__ uint32_t f16pair(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// One warp's register-resident activations for its chunk.  Thread (g, t) of
+// the mma holds the B fragment of token g and the scales and sums of its two
+// accumulator columns c0 = 2t, c1 = 2t + 1.
+struct MmaX {
+    uint32_t b[32];  // int8 path: b[2i], b[2i+1] = sub-block i (Q6_K: b[j] = 16-group j);
+                     // f16 path (Q4_K): b[4i + 2s], b[4i + 2s + 1] = sub-block i, 16-step s
+    int s[16];       // Q4_K/Q5_K: sum q of sub-block i (s[2i]: c0, s[2i+1]: c1); MXFP4: 12x that;
+                     // Q6_K: 16-group sums of c0 (low half) and c1 (high half)
+    uint32_t bm[2];  // f16 path: B of the mins product (16-group sums of token g)
+    float dx0, dx1;  // Q8_K scale of the chunk's superblock, columns c0 and c1
+};
+
+// Build a warp's fragments from the packed Q8_K rows staged in shared memory
+// (xs: row c at xs + c * xrow).
+template <int F>
+__device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk, int e0, int g, int t, MmaX& X,
+                                            float* cs) {
+    const int sb = e0 >> 8, off = e0 & 255;
+    const int c0 = 2 * t, c1 = 2 * t + 1;
+    const saddr rb = xs + static_cast<uint32_t>(g * xrow + 292 * sb);  // B: token g
+    const saddr r0 = xs + static_cast<uint32_t>(c0 * xrow + 292 * sb);  // column c0
+    const saddr r1 = xs + static_cast<uint32_t>(c1 * xrow + 292 * sb);
+    const bool vg = g < T, v0 = c0 < T, v1 = c1 < T;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) X.b[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) X.s[i] = 0;
+    X.bm[0] = X.bm[1] = 0u;
+    X.dx0 = v0 ? ld_f32(r0) : 0.0f;
+    X.dx1 = v1 ? ld_f32(r1) : 0.0f;
+    if constexpr (F == F_Q6_K) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (16 * j < chunk) {
+                const int e = off + 16 * j;
+                if (vg) X.b[j] = ld_s32(rb + 4 + e + 4 * t);
+                const uint32_t w0 = v0 ? ld_s32(r0 + 260 + 2 * ((e >> 4) & ~1)) : 0u;
+                const uint32_t w1 = v1 ? ld_s32(r1 + 260 + 2 * ((e >> 4) & ~1)) : 0u;
+                const int sh = 16 * ((e >> 4) & 1);
+                X.s[j] = static_cast<int>(((w0 >> sh) & 0xFFFFu) | (((w1 >> sh) & 0xFFFFu) << 16));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (32 * i < chunk) {
+                const int e = off + 32 * i;
+                uint32_t lo = 0u, hi = 0u;
+                if (vg) {
+                    lo = ld_s32(rb + 4 + e + 4 * t);
+                    hi = ld_s32(rb + 4 + e + 16 + 4 * t);
+                }
+                if constexpr (F == F_MXFP4) {
+                    // the E2M1 lookup yields elements (j, j+16, j+1, j+17 | j+2, j+18, j+3, j+19):
+                    // the activation fragment takes the same order
+                    X.b[2 * i] = prmt(lo, hi, 0x5140u);
+                    X.b[2 * i + 1] = prmt(lo, hi, 0x7362u);
+                } else if constexpr (F == F_Q4_K) {
+                    // f16 fragments; a thread's k slots (2t, 2t+1 | 2t+8, 2t+9) of a
+                    // 16-step hold elements (4t, 4t+2 | 4t+1, 4t+3), matching the
+                    // weight-side unpack of one 32-bit word
+                    s8x4_to_f16(lo, X.b[4 * i], X.b[4 * i + 1]);
+                    s8x4_to_f16(hi, X.b[4 * i + 2], X.b[4 * i + 3]);
+                } else {
+                    X.b[2 * i] = lo;
+                    X.b[2 * i + 1] = hi;
+                }
+                if constexpr (F != F_Q8_0) {
+                    const uint32_t w0 = v0 ? ld_s32(r0 + 260 + 2 * (e >> 4)) : 0u;  // bsums 2js, 2js+1
+                    const uint32_t w1 = v1 ? ld_s32(r1 + 260 + 2 * (e >> 4)) : 0u;
+                    const int s0 = static_cast<int>(static_cast<int16_t>(w0 & 0xFFFFu)) +
+                                   static_cast<int>(static_cast<int16_t>(w0 >> 16));
+                    const int s1 = static_cast<int>(static_cast<int16_t>(w1 & 0xFFFFu)) +
+                                   static_cast<int>(static_cast<int16_t>(w1 >> 16));
+                    const int m = F == F_MXFP4 ? 12 : 1;
+                    X.s[2 * i] = m * s0;
+                    X.s[2 * i + 1] = m * s1;
+                }
+            }
+        }
+        if constexpr (F == F_Q4_K) {
+            // C of each sub-block's f16 products: -1024 * (sum of its activations), columns c0, c1
+            if (g == 0) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) cs[i] = -1024.0f * static_cast<float>(X.s[i]);
+            }
+            // mins product: k slot q <-> 16-group q of the chunk (sub-block q/2)
+            if (vg) {
+                const int q0 = 2 * t, q1 = 2 * t + 8;  // groups (q0, q0+1) and (q1, q1+1)
+                const int ng = chunk >> 4;
+                const int a = q0 < ng ? ld_s16(rb + 260 + 2 * ((off >> 4) + q0)) : 0;
+                const int b = q0 < ng ? ld_s16(rb + 260 + 2 * ((off >> 4) + q0 + 1)) : 0;
+                const int c = q1 < ng ? ld_s16(rb + 260 + 2 * ((off >> 4) + q1)) : 0;
+                const int d = q1 < ng ? ld_s16(rb + 260 + 2 * ((off >> 4) + q1 + 1)) : 0;
+                X.bm[0] = f16pair(static_cast<float>(a), static_cast<float>(b));
+                X.bm[1] = f16pair(static_cast<float>(c), static_cast<float>(d));
+            }
+        }
+    }
+}
+
+// Scales (or mins) of sub-blocks js0 .. js0+7 of one Q4_K/Q5_K row as bytes of
+// (lo, hi): the 6-bit packed fields of the superblock header words a0..a2.
+__device__ __forceinline__ void k4_scale_words(uint32_t a0, uint32_t a1, uint32_t a2, int js0, uint32_t& sl,
+                                               uint32_t& sh, uint32_t& ml, uint32_t& mh) {
+    const uint32_t sc_lo = a0 & 0x3F3F3F3Fu, m_lo = a1 & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (a2 & 0x0F0F0F0Fu) | ((a0 >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((a2 >> 4) & 0x0F0F0F0Fu) | ((a1 >> 2) & 0x30303030u);
+    if (js0 == 0) {
+        sl = sc_lo, sh = sc_hi, ml = m_lo, mh = m_hi;
+    } else if (js0 < 4) {
+        sl = __funnelshift_r(sc_lo, sc_hi, 8 * js0), sh = 0u;
+        ml = __funnelshift_r(m_lo, m_hi, 8 * js0), mh = 0u;
+    } else {
+        sl = sc_hi >> (8 * (js0 - 4)), sh = 0u;
+        ml = m_hi >> (8 * (js0 - 4)), mh = 0u;
+    }
+}
+
+// 16 x 8 partial of one chunk: rows (g, g+8) at r0/r1, columns (2t, 2t+1).
+template <int F>
+__device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk, const MmaX& X, saddr cs, int t,
+                                           float* acc) {
+    const int sb = e0 >> 8;
+    if constexpr (F == F_Q4_K) {
+        // f16 operands: a nibble n placed in the mantissa of 1024.0 reads 1024 + n
+        // (low nibble) or 1024 + 16n (high nibble masked in place); each sub-block
+        // starts from C = -1024 * (sum of its activations), so D is the exact
+        // integer dot (times 16 for high nibbles)
+        const int js0 = (e0 & 255) >> 5;
+        const saddr b0 = r0 + 144u * sb, b1 = r1 + 144u * sb;
+        const uint4 h0 = ld_s128(b0), h1 = ld_s128(b1);
+        uint32_t s0l, s0h, m0l, m0h, s1l, s1h, m1l, m1h;
+        k4_scale_words(h0.y, h0.z, h0.w, js0, s0l, s0h, m0l, m0h);
+        k4_scale_words(h1.y, h1.z, h1.w, js0, s1l, s1h, m1l, m1h);
+        constexpr uint32_t M = 0x64006400u;
+        // mins: sum over sub-blocks of m_j * (sum of the activations of j), one
+        // f16 product with k slot q <-> 16-group q (sub-block q/2) of the chunk
+        const auto mpair = [](uint32_t w, int idx) -> uint32_t {  // (m, m) as f16: byte idx of w
+            const uint32_t v = prmt(w, 0u, 0x4040u | static_cast<uint32_t>(idx) | (static_cast<uint32_t>(idx) << 8)) | M;
+            const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v),
+                                      __halves2half2(__ushort_as_half(0x6400u), __ushort_as_half(0x6400u)));
+            return *reinterpret_cast<const uint32_t*>(&h);
+        };
+        float DM[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16(DM, mpair(m0l, t), mpair(m1l, t), mpair(m0h, t), mpair(m1h, t), X.bm[0], X.bm[1]);
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        uint32_t Mr = M;  // the magic exponent in a register: one LOP3 per operand word
+        asm("" : "+r"(Mr));
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            if (32 * i < chunk) {
+                const uint32_t q = 16u + 32u * static_cast<uint32_t>((js0 + i) >> 1) + 4u * t;
+                const uint32_t w00 = ld_s32(b0 + q), w01 = ld_s32(b0 + q + 16);  // row g: bytes 4t.. and 16+4t..
+                const uint32_t w10 = ld_s32(b1 + q), w11 = ld_s32(b1 + q + 16);  // row g+8
+                const uint4 cc = ld_s128(cs + 8u * i);  // C of sub-blocks i and i + 1, columns c0, c1
+                float DL[4] = {__uint_as_float(cc.x), __uint_as_float(cc.y), __uint_as_float(cc.x), __uint_as_float(cc.y)};
+                const uint32_t v00 = w00 >> 8, v01 = w01 >> 8, v10 = w10 >> 8, v11 = w11 >> 8;
+                mma_f16(DL, and_or<0x000F000Fu>(w00, Mr), and_or<0x000F000Fu>(w10, Mr), and_or<0x000F000Fu>(v00, Mr),
+                        and_or<0x000F000Fu>(v10, Mr), X.b[4 * i], X.b[4 * i + 1]);
+                mma_f16(DL, and_or<0x000F000Fu>(w01, Mr), and_or<0x000F000Fu>(w11, Mr), and_or<0x000F000Fu>(v01, Mr),
+                        and_or<0x000F000Fu>(v11, Mr), X.b[4 * i + 2], X.b[4 * i + 3]);
+                float DH[4] = {__uint_as_float(cc.z), __uint_as_float(cc.w), __uint_as_float(cc.z), __uint_as_float(cc.w)};
+                mma_f16(DH, and_or<0x00F000F0u>(w00, Mr), and_or<0x00F000F0u>(w10, Mr), and_or<0x00F000F0u>(v00, Mr),
+                        and_or<0x00F000F0u>(v10, Mr), X.b[4 * i + 4], X.b[4 * i + 5]);
+                mma_f16(DH, and_or<0x00F000F0u>(w01, Mr), and_or<0x00F000F0u>(w11, Mr), and_or<0x00F000F0u>(v01, Mr),
+                        and_or<0x00F000F0u>(v11, Mr), X.b[4 * i + 6], X.b[4 * i + 7]);
+                const uint32_t w0s = i < 4 ? s0l : s0h, w1s = i < 4 ? s1l : s1h;
+                // high-nibble products are 16x: their scales carry the exact 1/16
+                const float sa0 = static_cast<float>(byte_u(w0s, i & 3));
+                const float sa1 = static_cast<float>(byte_u(w1s, i & 3));
+                const float sb0 = 0.0625f * static_cast<float>(byte_u(w0s, (i + 1) & 3));
+                const float sb1 = 0.0625f * static_cast<float>(byte_u(w1s, (i + 1) & 3));
+                a[0] += sa0 * DL[0] + sb0 * DH[0];
+                a[1] += sa0 * DL[1] + sb0 * DH[1];
+                a[2] += sa1 * DL[2] + sb1 * DH[2];
+                a[3] += sa1 * DL[3] + sb1 * DH[3];
+            }
+        }
+        const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
+        acc[0] = X.dx0 * (d0 * a[0] - dm0 * DM[0]);
+        acc[1] = X.dx1 * (d0 * a[1] - dm0 * DM[1]);
+        acc[2] = X.dx0 * (d1 * a[2] - dm1 * DM[2]);
+        acc[3] = X.dx1 * (d1 * a[3] - dm1 * DM[3]);
+    } else if constexpr (F == F_Q5_K) {
+        constexpr uint32_t SB = F == F_Q4_K ? 144u : 176u;
+        constexpr uint32_t QS = F == F_Q4_K ? 16u : 48u;
+        const int js0 = (e0 & 255) >> 5;
+        const saddr b0 = r0 + SB * sb, b1 = r1 + SB * sb;
+        const uint4 h0 = ld_s128(b0), h1 = ld_s128(b1);
+        uint32_t s0l, s0h, m0l, m0h, s1l, s1h, m1l, m1h;
+        k4_scale_words(h0.y, h0.z, h0.w, js0, s0l, s0h, m0l, m0h);
+        k4_scale_words(h1.y, h1.z, h1.w, js0, s1l, s1h, m1l, m1h);
+        uint32_t qh0a = 0u, qh0b = 0u, qh1a = 0u, qh1b = 0u;
+        if constexpr (F == F_Q5_K) {  // high bits of elements 4t.. and 16+4t.., bit js of each byte
+            qh0a = ld_s32(b0 + 16 + 4 * t) >> js0;
+            qh0b = ld_s32(b0 + 32 + 4 * t) >> js0;
+            qh1a = ld_s32(b1 + 16 + 4 * t) >> js0;
+            qh1b = ld_s32(b1 + 32 + 4 * t) >> js0;
+        }
+        int iA[4] = {0, 0, 0, 0}, iH[4] = {0, 0, 0, 0}, iB[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            if (32 * i < chunk) {
+                const uint32_t q = QS + 32u * static_cast<uint32_t>((js0 + i) >> 1) + 4u * t;
+                const uint32_t qa0 = ld_s32(b0 + q), qb0 = ld_s32(b0 + q + 16);
+                const uint32_t qa1 = ld_s32(b1 + q), qb1 = ld_s32(b1 + q + 16);
+                int D[4], E[4];
+                if constexpr (F == F_Q4_K) {
+                    mma_k32_s8(D, qa0 & 0x0F0F0F0Fu, qa1 & 0x0F0F0F0Fu, qb0 & 0x0F0F0F0Fu, qb1 & 0x0F0F0F0Fu,
+                               X.b[2 * i], X.b[2 * i + 1], 0, 0);
+                    mma_k32_u8(E, qa0 & 0xF0F0F0F0u, qa1 & 0xF0F0F0F0u, qb0 & 0xF0F0F0F0u, qb1 & 0xF0F0F0F0u,
+                               X.b[2 * i + 2], X.b[2 * i + 3]);
+                } else {
+                    // high bit of sub-block js0 + i (+1) into bit 4 of each byte
+                    const auto hb = [](uint32_t w, int k) -> uint32_t {
+                        return (k <= 4 ? (w << (4 - k)) : (w >> (k - 4))) & 0x10101010u;
+                    };
+                    mma_k32_s8(D, (qa0 & 0x0F0F0F0Fu) | hb(qh0a, i), (qa1 & 0x0F0F0F0Fu) | hb(qh1a, i),
+                               (qb0 & 0x0F0F0F0Fu) | hb(qh0b, i), (qb1 & 0x0F0F0F0Fu) | hb(qh1b, i), X.b[2 * i],
+                               X.b[2 * i + 1], 0, 0);
+                    mma_k32_s8(E, ((qa0 >> 4) & 0x0F0F0F0Fu) | hb(qh0a, i + 1),
+                               ((qa1 >> 4) & 0x0F0F0F0Fu) | hb(qh1a, i + 1), ((qb0 >> 4) & 0x0F0F0F0Fu) | hb(qh0b, i + 1),
+                               ((qb1 >> 4) & 0x0F0F0F0Fu) | hb(qh1b, i + 1), X.b[2 * i + 2], X.b[2 * i + 3], 0, 0);
+                }
+                const uint32_t w0s = i < 4 ? s0l : s0h, w1s = i < 4 ? s1l : s1h;
+                const uint32_t w0m = i < 4 ? m0l : m0h, w1m = i < 4 ? m1l : m1h;
+                const int sa0 = byte_u(w0s, i & 3), sb0 = byte_u(w0s, (i + 1) & 3);
+                const int sa1 = byte_u(w1s, i & 3), sb1 = byte_u(w1s, (i + 1) & 3);
+                const int ma0 = byte_u(w0m, i & 3), mb0 = byte_u(w0m, (i + 1) & 3);
+                const int ma1 = byte_u(w1m, i & 3), mb1 = byte_u(w1m, (i + 1) & 3);
+                iA[0] += sa0 * D[0];
+                iA[1] += sa0 * D[1];
+                iA[2] += sa1 * D[2];
+                iA[3] += sa1 * D[3];
+                iH[0] += sb0 * E[0];
+                iH[1] += sb0 * E[1];
+                iH[2] += sb1 * E[2];
+                iH[3] += sb1 * E[3];
+                iB[0] += ma0 * X.s[2 * i] + mb0 * X.s[2 * i + 2];
+                iB[1] += ma0 * X.s[2 * i + 1] + mb0 * X.s[2 * i + 3];
+                iB[2] += ma1 * X.s[2 * i] + mb1 * X.s[2 * i + 2];
+                iB[3] += ma1 * X.s[2 * i + 1] + mb1 * X.s[2 * i + 3];
+            }
+        }
+        if constexpr (F == F_Q4_K) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) iA[k] += iH[k] >> 4;  // iH is 16x an integer: exact
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) iA[k] += iH[k];
+        }
+        const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
+        acc[0] = X.dx0 * (d0 * static_cast<float>(iA[0]) - dm0 * static_cast<float>(iB[0]));
+        acc[1] = X.dx1 * (d0 * static_cast<float>(iA[1]) - dm0 * static_cast<float>(iB[1]));
+        acc[2] = X.dx0 * (d1 * static_cast<float>(iA[2]) - dm1 * static_cast<float>(iB[2]));
+        acc[3] = X.dx1 * (d1 * static_cast<float>(iA[3]) - dm1 * static_cast<float>(iB[3]));
+    } else if constexpr (F == F_Q6_K) {
+        // chunk = one or two 128-element halves; element 128h + 32g6 + l of a
+        // superblock: low 4 bits in ql[64h + 32(g6&1) + l] (nibble g6>>1), high
+        // 2 bits in qh[32h + l] (bits 2g6), scale of 16-group (128h + 32g6 + l)/16
+        const int h0 = (e0 & 255) >> 7;
+        const saddr b0 = r0 + 210u * sb, b1 = r1 + 210u * sb;
+        uint32_t sw0[4], sw1[4];  // int8 scales of the chunk's 16-groups, four per word
+        ld_words_any<4>(b0 + 192, sw0);
+        ld_words_any<4>(b1 + 192, sw1);
+        if (h0) {  // second half only: its eight scales are words 2 and 3
+            sw0[0] = sw0[2], sw0[1] = sw0[3], sw1[0] = sw1[2], sw1[1] = sw1[3];
+        }
+        int iA[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            if (128 * hh < chunk) {
+                const int h = h0 + hh;
+#pragma unroll
+                for (int lh = 0; lh < 2; ++lh) {
+                    const uint32_t l = 16u * lh + 4u * t;
+                    uint32_t qla0, qlb0, qhw0, qla1, qlb1, qhw1;
+                    ld_words_any<1>(b0 + 64 * h + l, &qla0);
+                    ld_words_any<1>(b0 + 64 * h + 32 + l, &qlb0);
+                    ld_words_any<1>(b0 + 128 + 32 * h + l, &qhw0);
+                    ld_words_any<1>(b1 + 64 * h + l, &qla1);
+                    ld_words_any<1>(b1 + 64 * h + 32 + l, &qlb1);
+                    ld_words_any<1>(b1 + 128 + 32 * h + l, &qhw1);
+#pragma unroll
+                    for (int g6 = 0; g6 < 4; ++g6) {
+                        const int jl = 8 * hh + 2 * g6 + lh;  // 16-group within the chunk
+                        const int js = 2 * g6 + lh;           // 16-group within the half
+                        const uint32_t w0 = (g6 & 1) ? qlb0 : qla0, w1 = (g6 & 1) ? qlb1 : qla1;
+                        const uint32_t a0 = ((w0 >> (4 * (g6 >> 1))) & 0x0F0F0F0Fu) | (((qhw0 >> (2 * g6)) & 0x03030303u) << 4);
+                        const uint32_t a1 = ((w1 >> (4 * (g6 >> 1))) & 0x0F0F0F0Fu) | (((qhw1 >> (2 * g6)) & 0x03030303u) << 4);
+                        const int cs0 = -32 * static_cast<int>(static_cast<int16_t>(X.s[jl] & 0xFFFF));
+                        const int cs1 = -32 * (X.s[jl] >> 16);
+                        int D[4];
+                        mma_k16_u8(D, a0, a1, X.b[jl], cs0, cs1);
+                        const int sj = 8 * hh + js;  // scale index within the chunk
+                        const int sc0 = byte_s(sw0[sj >> 2], sj & 3), sc1 = byte_s(sw1[sj >> 2], sj & 3);
+                        iA[0] += sc0 * D[0];
+                        iA[1] += sc0 * D[1];
+                        iA[2] += sc1 * D[2];
+                        iA[3] += sc1 * D[3];
+                    }
+                }
+            }
+        }
+        const float d0 = ld_h(b0 + 208), d1 = ld_h(b1 + 208);
+        acc[0] = static_cast<float>(iA[0]) * (X.dx0 * d0);
+        acc[1] = static_cast<float>(iA[1]) * (X.dx1 * d0);
+        acc[2] = static_cast<float>(iA[2]) * (X.dx0 * d1);
+        acc[3] = static_cast<float>(iA[3]) * (X.dx1 * d1);
+    } else {  // Q8_0 and MXFP4: one scale per 32-block
+        const int blk0 = e0 >> 5;  // even: chunks start at multiples of 64
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (32 * i < chunk) {
+                const int blk = blk0 + i;
+                uint32_t a0, a1, a2, a3;
+                float w0, w1;
+                int c0 = 0, c1 = 0;
+                if constexpr (F == F_Q8_0) {
+                    const saddr p0 = r0 + 34u * blk, p1 = r1 + 34u * blk;
+                    if (i & 1) {  // odd block: quants start on a 4-byte boundary
+                        a0 = ld_s32(p0 + 2 + 4 * t);
+                        a2 = ld_s32(p0 + 18 + 4 * t);
+                        a1 = ld_s32(p1 + 2 + 4 * t);
+                        a3 = ld_s32(p1 + 18 + 4 * t);
+                    } else {  // even block: two aligned words, take the middle
+                        a0 = prmt(ld_s32(p0 + 4 * t), ld_s32(p0 + 4 + 4 * t), 0x5432u);
+                        a2 = prmt(ld_s32(p0 + 16 + 4 * t), ld_s32(p0 + 20 + 4 * t), 0x5432u);
+                        a1 = prmt(ld_s32(p1 + 4 * t), ld_s32(p1 + 4 + 4 * t), 0x5432u);
+                        a3 = prmt(ld_s32(p1 + 16 + 4 * t), ld_s32(p1 + 20 + 4 * t), 0x5432u);
+                    }
+                    w0 = ld_h(p0);
+                    w1 = ld_h(p1);
+                } else {
+                    const saddr p0 = r0 + 17u * blk, p1 = r1 + 17u * blk;
+                    uint32_t q0, q1;
+                    ld_words_any<1>(p0 + 1 + 4 * t, &q0);
+                    ld_words_any<1>(p1 + 1 + 4 * t, &q1);
+                    a0 = mx_lookup(q0 & 0xFFFFu);
+                    a2 = mx_lookup(q0 >> 16);
+                    a1 = mx_lookup(q1 & 0xFFFFu);
+                    a3 = mx_lookup(q1 >> 16);
+                    w0 = e8m0_half_scale(ld_u8(p0));
+                    w1 = e8m0_half_scale(ld_u8(p1));
+                    c0 = -X.s[2 * i];  // the tables hold 2*value + 12
+                    c1 = -X.s[2 * i + 1];
+                }
+                int D[4];
+                mma_k32_s8(D, a0, a1, a2, a3, X.b[2 * i], X.b[2 * i + 1], c0, c1);
+                acc[0] += static_cast<float>(D[0]) * (w0 * X.dx0);
+                acc[1] += static_cast<float>(D[1]) * (w0 * X.dx1);
+                acc[2] += static_cast<float>(D[2]) * (w1 * X.dx0);
+                acc[3] += static_cast<float>(D[3]) * (w1 * X.dx1);
+            }
+        }
+    }
+}
+
+template <int F>
+__global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();
+
+    // ---- shared memory: ring | activations, later the partials [2][16 rows x 8 columns][16 warps]
+    //      | f16-path C values | barriers
+    uint8_t* ring = smem;
+    uint8_t* xreg = smem + static_cast<size_t>(p.stages) * p.stage_stride;
+    float* red = reinterpret_cast<float*>(xreg);
+    float* creg = reinterpret_cast<float*>(xreg + p.x_bytes);  // [16 warps][4][16]
+    uint64_t* full = reinterpret_cast<uint64_t*>(creg + kConsumerWarps * 4 * 16);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* xbar = empty + kMaxStages;
+
+    const int nitems = static_cast<int>((p.N + kTileRows - 1) / kTileRows);
+    if (static_cast<int>(blockIdx.x) >= nitems) return;  // whole CTA idle (uniform)
+    if (warp == kConsumerWarps) {
+        // ================= producer warp: initialises the barriers and releases the
+        // consumers (start barrier, no wait); lane 0 waits, lanes 0..7 copy the row pairs
+        if (lane == 0) {
+            for (int s = 0; s < p.stages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kConsumerWarps);
+            }
+            mbar_init(xbar, 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        mmav_start_arrive();
+        const uint64_t pol = policy_evict_first();
+        if (!p.early_weights) pdl_wait();  // the previous kernel may still be writing the weights
+        int j = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
+            const int s = j % p.stages;
+            const int64_t r0 = static_cast<int64_t>(item) * kTileRows;
+            const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
+            if (lane == 0) {
+                ok = mbar_wait(&empty[s], (static_cast<uint32_t>(j / p.stages) & 1u) ^ 1u);
+                if (ok) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nr * p.rowbytes));
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) set_error(p.err, DEV_ERR_TIMEOUT);
+                break;
+            }
+            const int pr = 2 * lane;
+            if (pr < nr) {
+                const int rows = nr - pr < 2 ? nr - pr : 2;
+                bulk_g2s(ring + static_cast<size_t>(s) * p.stage_stride + static_cast<size_t>(lane) * p.wrow,
+                         p.W + (r0 + pr) * p.rowbytes, static_cast<uint32_t>(rows * p.rowbytes), &full[s], pol);
+            }
+        }
+        if (lane == 0) {
+            for (int q = (j > p.stages ? j - p.stages : 0); q < j; ++q) {
+                if (!mbar_wait(&full[q % p.stages], static_cast<uint32_t>(q / p.stages) & 1u)) {
+                    set_error(p.err, DEV_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ================= consumers
+    mmav_start_sync();  // barriers initialised
+    pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
+    const int xbytes = p.T * p.xrow;
+    bool xok = true;
+    if (p.x_bulk) {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(xbytes));
+            bulk_g2s(xreg, p.xq, static_cast<uint32_t>(xbytes), xbar, 0ull);
+        }
+        xok = mbar_wait(xbar, 0u);
+        if (!xok) set_error(p.err, DEV_ERR_TIMEOUT);
+    } else {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.xq);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(xreg);
+        for (int i = tid; i < xbytes / 4; i += kConsumerWarps * 32) dst[i] = __ldg(src + i);
+        mmav_sync();
+    }
+    const int g = lane >> 2, t = lane & 3;
+    const bool active = warp < p.nch;
+    const int e0 = warp * p.chunk;
+    MmaX X;
+    float* cs = creg + (warp * 4 + t) * 16;
+    mmav_load_x<F>(smem_addr(xreg), p.xrow, active ? p.T : 0, p.chunk, e0, g, t, X, cs);
+    mmav_sync();  // the region now holds partials
+    const saddr ring_s = smem_addr(ring);
+    int j = 0;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
+        const int s = j % p.stages;
+        const bool ready =
+            xok && __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(j / p.stages) & 1u));
+        if (!ready) set_error(p.err, DEV_ERR_TIMEOUT);
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (ready && active) {
+            const saddr r0 = ring_s + static_cast<uint32_t>(s * p.stage_stride + g * p.wrow);  // tile row 2g
+            mmav_chunk<F>(r0, r0 + static_cast<uint32_t>(p.rowbytes), e0, p.chunk, X, smem_addr(cs), t, acc);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        // partials of this tile -> buffer j & 1, laid out [warp][tile row x 8 + column]
+        // with a warp stride of kRedStride floats (2 mod 32: the reads below hit 32
+        // distinct banks); one barrier per tile (a warp writes buffer j & 1 again only
+        // after the next tile's barrier, which the readers of this tile reach after reading)
+        float* rb = red + (j & 1) * (kRedStride * kConsumerWarps);
+        float* rw = rb + warp * kRedStride;
+        *reinterpret_cast<float2*>(rw + (2 * g) * 8 + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2*>(rw + (2 * g + 1) * 8 + 2 * t) = make_float2(acc[2], acc[3]);
+        mmav_sync();
+        {
+            // output o = tid / 4 (tile row o / 8, column o % 8): four threads sum four warps each
+            const int o = tid >> 2, q = tid & 3;
+            const float* rr = rb + (4 * q) * kRedStride + o;
+            float v = (rr[0] + rr[kRedStride]) + (rr[2 * kRedStride] + rr[3 * kRedStride]);
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            const int row = o >> 3, col = o & 7;
+            const int64_t grow = static_cast<int64_t>(item) * kTileRows + row;
+            if (q == 0 && col < p.T && grow < p.N && ready) p.Y[static_cast<int64_t>(col) * p.N + grow] = v;
+        }
+    }
+}
+
+template <int F>
+cudaError_t launch_mmav_one(const MmavParams& p, int grid, int smem, cudaStream_t s) {
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(k_gemv_mma<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return launch_pdl(k_gemv_mma<F>, dim3(grid), dim3(kThreads), smem, s, p);
+}
+
+}  // namespace ggq

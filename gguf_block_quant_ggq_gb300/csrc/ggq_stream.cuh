@@ -24,6 +24,11 @@
 
 namespace ggq {
 
+// Start barrier between the producer warp (arrives once the mbarriers are
+// initialised, without waiting) and the consumer warps (wait for it).
+__device__ __forceinline__ void start_arrive() { asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void start_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory"); }
+
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
 
 // Shared-memory activation region (layout of x_region_bytes).
@@ -212,22 +217,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     const int nitems = static_cast<int>((p.N + kTileRows - 1) / kTileRows);
     if (static_cast<int>(blockIdx.x) >= nitems) return;  // whole CTA idle (uniform)
 
-    if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
-        }
-        s_flag[0] = 0;
-        s_flag[1] = 0;
-        fence_barrier_init();
-    }
-    if constexpr (Q81) {
-        for (int i = tid; i < p.xrows * (K >> 5); i += kThreads) xr_.s32[i] = 0;
-    }
-    __syncthreads();
-
     if (warp == kConsumerWarps) {
-        // ================= producer
+        // ================= producer: initialise the barriers, release the
+        // consumers (start barrier, no wait), then stream
+        if (lane == 0) {
+            for (int s = 0; s < p.stages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kConsumerWarps);
+            }
+            s_flag[0] = 0;
+            s_flag[1] = 0;
+            fence_barrier_init();
+        }
+        __syncwarp();
+        start_arrive();
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             if (!p.early_weights) pdl_wait();  // the previous kernel may still be writing the weights
@@ -278,6 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
 
     // ================= consumers (512 threads)
     const int ctid = tid;
+    if constexpr (Q81) {  // per-32 sums are accumulated with atomics
+        for (int i = tid; i < p.xrows * (K >> 5); i += kConsumerWarps * 32) xr_.s32[i] = 0;
+    }
+    start_sync();  // barriers initialised, sums zeroed
     pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
     stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
     consumer_sync();
@@ -288,6 +295,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     xs.bs = smem_addr(xr_.bs);
     xs.K = K;
     const saddr ring_s = smem_addr(ring);
+
+    if constexpr (KIND == KIND_GEMV && NT == 1) {
+        const int nu = units_per_row(K), nb32 = K >> 5;
+        if (nu <= 64) {
+            // One token, K <= 4096: lane l owns units l and l + 32 of every row,
+            // so its activations stay in registers for the whole kernel.
+            XUnit xa, xb;
+            const bool va = lane < nu, vb = lane + 32 < nu;
+            if (va) load_xunit<F>(xs, lane, xa);
+            if (vb) load_xunit<F>(xs, lane + 32, xb);
+            int j = 0;
+            for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
+                const int s = j % p.stages;
+                const uint32_t ph = static_cast<uint32_t>(j / p.stages) & 1u;
+                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));  // warp-uniform
+                if (!ready) set_error(p.err, DEV_ERR_TIMEOUT);
+                const int64_t r = static_cast<int64_t>(item) * kTileRows + warp;
+                if (ready && r < p.N) {
+                    const saddr row = ring_s + static_cast<uint32_t>(s * p.stage_stride + warp * p.rowbytes);
+                    float acc;
+                    if (nu > 32) {
+                        const float a = unit_dot_rx<F>(row, lane, nb32, xa);
+                        const float b = vb ? unit_dot_rx<F>(row, lane + 32, nb32, xb) : 0.0f;
+                        acc = a + b;
+                    } else {
+                        acc = va ? unit_dot_rx<F>(row, lane, nb32, xa) : 0.0f;
+                    }
+                    const float v = warp_transpose_reduce<0>(&acc, lane);
+                    if (lane == 0) p.Y[r] = v;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            return;
+        }
+    }
 
     int j = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
