@@ -1,11 +1,18 @@
-// ggq_mmav.cuh -- the decode GEMV at 2-8 tokens on the int8 tensor path.
+// ggq_mmav.cuh -- the decode GEMV at 2-8 tokens on the tensor cores.
 //
-// y[t][n] = sum over blocks of (weight scale) * (activation scale) * (exact
-// int32 block dot), as in the keep-quant matmul of vllm.cpp PR #523 "grouped +
+// y[t][n] = sum over blocks of (weight scale) * (activation scale) * (integer
+// block dot), as in the keep-quant matmul of vllm.cpp PR #523 "grouped +
 // non-grouped keep-quant expert GEMM" (What changed: DotQ8_0/DotQ4K/DotQ5K/
-// DotQ6K superblock dots), with the integer dots of 16 rows x 8 token columns
-// x 32 inputs done by one mma.sync.m16n8k32 (Q6_K: m16n8k16, one per 16-group
-// because every 16 weights carry their own scale).
+// DotQ6K superblock dots).  One mma covers 16 rows x 8 token columns:
+//   * Q4_K, Q5_K, Q6_K: mma.sync m16n8k16 with f16 operands and f32
+//     accumulation.  Weight codes are placed in the mantissa of 1024.0 (one
+//     LOP3 per pair of codes) and int8 activations are exact in f16, so every
+//     product is exact; C starts at -1024 (Q6_K: -1056) times the activation
+//     sum of the block, which leaves the exact integer dot of each sub-block
+//     (Q6_K: each 16-group, whose own scale it needs) in D.  Block scales are
+//     applied in f32; the Q4_K/Q5_K mins term is one more f16 product.  On this
+//     part the f16 mma runs at four times the rate of the int8 one.
+//   * Q8_0, MXFP4: mma.sync m16n8k32 on int8 (one 32-block per mma).
 //
 // Layout on the SM:
 //   * one CTA per SM; a producer warp copies each 16-row tile of W into a ring
@@ -15,8 +22,9 @@
 //     mma row g + 8 is tile row 2g + 1, so every fragment load is conflict-free;
 //   * sixteen consumer warps split K into sixteen chunks of 64, 128 or 256
 //     inputs.  A warp's chunk never changes, so its activation fragments (the
-//     mma B operand), activation scales and per-block sums are loaded once into
-//     registers, straight from the packed Q8_K rows in global memory;
+//     mma B operand), activation scales and per-block sums are built once, from
+//     the activation rows that one bulk copy brings into shared memory, and
+//     kept in registers;
 //   * per tile each warp produces a 16 x 8 partial of its chunk; partials meet
 //     in a double-buffered shared array behind one barrier per tile.
 // Every wait is bounded; on timeout the kernel records an error word, drains
@@ -40,23 +48,6 @@ __device__ __forceinline__ void mma_k32_s8(int* d, uint32_t a0, uint32_t a1, uin
         "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};"
         : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(c0), "r"(c1));
-}
-
-// A as unsigned bytes (high nibbles masked in place: 16x their value).
-__device__ __forceinline__ void mma_k32_u8(int* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                           uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
-}
-
-// Q6_K codes are unsigned (0..63): A as u8, C = -32 * (sum of the 16 quants).
-__device__ __forceinline__ void mma_k16_u8(int* d, uint32_t a0, uint32_t a1, uint32_t b0, int c0, int c1) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%7,%8};"
-        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-        : "r"(a0), "r"(a1), "r"(b0), "r"(c0), "r"(c1));
 }
 
 // (a & mask) | c in one LOP3 (mask an immediate, c a register).
@@ -133,15 +124,20 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
     X.dx0 = v0 ? ld_f32(r0) : 0.0f;
     X.dx1 = v1 ? ld_f32(r1) : 0.0f;
     if constexpr (F == F_Q6_K) {
+        // f16 fragments of each 16-group (elements 4t, 4t+2 | 4t+1, 4t+3 of the
+        // group, as for Q4_K); C = -1056 * (sum of the group's activations): the
+        // codes enter as 1024 + code and the weights are code - 32
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             if (16 * j < chunk) {
                 const int e = off + 16 * j;
-                if (vg) X.b[j] = ld_s32(rb + 4 + e + 4 * t);
-                const uint32_t w0 = v0 ? ld_s32(r0 + 260 + 2 * ((e >> 4) & ~1)) : 0u;
-                const uint32_t w1 = v1 ? ld_s32(r1 + 260 + 2 * ((e >> 4) & ~1)) : 0u;
-                const int sh = 16 * ((e >> 4) & 1);
-                X.s[j] = static_cast<int>(((w0 >> sh) & 0xFFFFu) | (((w1 >> sh) & 0xFFFFu) << 16));
+                if (vg) s8x4_to_f16(ld_s32(rb + 4 + e + 4 * t), X.b[2 * j], X.b[2 * j + 1]);
+                const int bs0 = v0 ? ld_s16(r0 + 260 + 2 * (e >> 4)) : 0;
+                const int bs1 = v1 ? ld_s16(r1 + 260 + 2 * (e >> 4)) : 0;
+                if (g == 0) {
+                    cs[2 * j] = -1056.0f * static_cast<float>(bs0);
+                    cs[2 * j + 1] = -1056.0f * static_cast<float>(bs1);
+                }
             }
         }
     } else {
@@ -159,7 +155,7 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                     // the activation fragment takes the same order
                     X.b[2 * i] = prmt(lo, hi, 0x5140u);
                     X.b[2 * i + 1] = prmt(lo, hi, 0x7362u);
-                } else if constexpr (F == F_Q4_K) {
+                } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
                     // f16 fragments; a thread's k slots (2t, 2t+1 | 2t+8, 2t+9) of a
                     // 16-step hold elements (4t, 4t+2 | 4t+1, 4t+3), matching the
                     // weight-side unpack of one 32-bit word
@@ -182,12 +178,7 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                 }
             }
         }
-        if constexpr (F == F_Q4_K) {
-            // C of each sub-block's f16 products: -1024 * (sum of its activations), columns c0, c1
-            if (g == 0) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) cs[i] = -1024.0f * static_cast<float>(X.s[i]);
-            }
+        if constexpr (F == F_Q4_K || F == F_Q5_K) {
             // mins product: k slot q <-> 16-group q of the chunk (sub-block q/2)
             if (vg) {
                 const int q0 = 2 * t, q1 = 2 * t + 8;  // groups (q0, q0+1) and (q1, q1+1)
@@ -226,67 +217,13 @@ template <int F>
 __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk, const MmaX& X, saddr cs, int t,
                                            float* acc) {
     const int sb = e0 >> 8;
-    if constexpr (F == F_Q4_K) {
-        // f16 operands: a nibble n placed in the mantissa of 1024.0 reads 1024 + n
-        // (low nibble) or 1024 + 16n (high nibble masked in place); each sub-block
-        // starts from C = -1024 * (sum of its activations), so D is the exact
-        // integer dot (times 16 for high nibbles)
-        const int js0 = (e0 & 255) >> 5;
-        const saddr b0 = r0 + 144u * sb, b1 = r1 + 144u * sb;
-        const uint4 h0 = ld_s128(b0), h1 = ld_s128(b1);
-        uint32_t s0l, s0h, m0l, m0h, s1l, s1h, m1l, m1h;
-        k4_scale_words(h0.y, h0.z, h0.w, js0, s0l, s0h, m0l, m0h);
-        k4_scale_words(h1.y, h1.z, h1.w, js0, s1l, s1h, m1l, m1h);
-        constexpr uint32_t M = 0x64006400u;
-        // mins: sum over sub-blocks of m_j * (sum of the activations of j), one
-        // f16 product with k slot q <-> 16-group q (sub-block q/2) of the chunk
-        const auto mpair = [](uint32_t w, int idx) -> uint32_t {  // (m, m) as f16: byte idx of w
-            const uint32_t v = prmt(w, 0u, 0x4040u | static_cast<uint32_t>(idx) | (static_cast<uint32_t>(idx) << 8)) | M;
-            const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v),
-                                      __halves2half2(__ushort_as_half(0x6400u), __ushort_as_half(0x6400u)));
-            return *reinterpret_cast<const uint32_t*>(&h);
-        };
-        float DM[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mma_f16(DM, mpair(m0l, t), mpair(m1l, t), mpair(m0h, t), mpair(m1h, t), X.bm[0], X.bm[1]);
-        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        uint32_t Mr = M;  // the magic exponent in a register: one LOP3 per operand word
-        asm("" : "+r"(Mr));
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            if (32 * i < chunk) {
-                const uint32_t q = 16u + 32u * static_cast<uint32_t>((js0 + i) >> 1) + 4u * t;
-                const uint32_t w00 = ld_s32(b0 + q), w01 = ld_s32(b0 + q + 16);  // row g: bytes 4t.. and 16+4t..
-                const uint32_t w10 = ld_s32(b1 + q), w11 = ld_s32(b1 + q + 16);  // row g+8
-                const uint4 cc = ld_s128(cs + 8u * i);  // C of sub-blocks i and i + 1, columns c0, c1
-                float DL[4] = {__uint_as_float(cc.x), __uint_as_float(cc.y), __uint_as_float(cc.x), __uint_as_float(cc.y)};
-                const uint32_t v00 = w00 >> 8, v01 = w01 >> 8, v10 = w10 >> 8, v11 = w11 >> 8;
-                mma_f16(DL, and_or<0x000F000Fu>(w00, Mr), and_or<0x000F000Fu>(w10, Mr), and_or<0x000F000Fu>(v00, Mr),
-                        and_or<0x000F000Fu>(v10, Mr), X.b[4 * i], X.b[4 * i + 1]);
-                mma_f16(DL, and_or<0x000F000Fu>(w01, Mr), and_or<0x000F000Fu>(w11, Mr), and_or<0x000F000Fu>(v01, Mr),
-                        and_or<0x000F000Fu>(v11, Mr), X.b[4 * i + 2], X.b[4 * i + 3]);
-                float DH[4] = {__uint_as_float(cc.z), __uint_as_float(cc.w), __uint_as_float(cc.z), __uint_as_float(cc.w)};
-                mma_f16(DH, and_or<0x00F000F0u>(w00, Mr), and_or<0x00F000F0u>(w10, Mr), and_or<0x00F000F0u>(v00, Mr),
-                        and_or<0x00F000F0u>(v10, Mr), X.b[4 * i + 4], X.b[4 * i + 5]);
-                mma_f16(DH, and_or<0x00F000F0u>(w01, Mr), and_or<0x00F000F0u>(w11, Mr), and_or<0x00F000F0u>(v01, Mr),
-                        and_or<0x00F000F0u>(v11, Mr), X.b[4 * i + 6], X.b[4 * i + 7]);
-                const uint32_t w0s = i < 4 ? s0l : s0h, w1s = i < 4 ? s1l : s1h;
-                // high-nibble products are 16x: their scales carry the exact 1/16
-                const float sa0 = static_cast<float>(byte_u(w0s, i & 3));
-                const float sa1 = static_cast<float>(byte_u(w1s, i & 3));
-                const float sb0 = 0.0625f * static_cast<float>(byte_u(w0s, (i + 1) & 3));
-                const float sb1 = 0.0625f * static_cast<float>(byte_u(w1s, (i + 1) & 3));
-                a[0] += sa0 * DL[0] + sb0 * DH[0];
-                a[1] += sa0 * DL[1] + sb0 * DH[1];
-                a[2] += sa1 * DL[2] + sb1 * DH[2];
-                a[3] += sa1 * DL[3] + sb1 * DH[3];
-            }
-        }
-        const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
-        acc[0] = X.dx0 * (d0 * a[0] - dm0 * DM[0]);
-        acc[1] = X.dx1 * (d0 * a[1] - dm0 * DM[1]);
-        acc[2] = X.dx0 * (d1 * a[2] - dm1 * DM[2]);
-        acc[3] = X.dx1 * (d1 * a[3] - dm1 * DM[3]);
-    } else if constexpr (F == F_Q5_K) {
+    if constexpr (F == F_Q4_K || F == F_Q5_K) {
+        // f16 operands: a code q placed in the mantissa of 1024.0 reads 1024 + q
+        // (low nibble; Q5_K adds its fifth bit at 16) or 1024 + 16q (high nibble
+        // masked in place; fifth bit at 256).  One HFMA2 per operand word applies
+        // the 6-bit sub-block scale and removes the 1024: sc * q is an integer
+        // below 2048, exact in f16, so each mma adds exact products and the whole
+        // chunk accumulates in one f32 chain
         constexpr uint32_t SB = F == F_Q4_K ? 144u : 176u;
         constexpr uint32_t QS = F == F_Q4_K ? 16u : 48u;
         const int js0 = (e0 & 255) >> 5;
@@ -295,6 +232,24 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         uint32_t s0l, s0h, m0l, m0h, s1l, s1h, m1l, m1h;
         k4_scale_words(h0.y, h0.z, h0.w, js0, s0l, s0h, m0l, m0h);
         k4_scale_words(h1.y, h1.z, h1.w, js0, s1l, s1h, m1l, m1h);
+        uint32_t Mr = 0x64006400u;  // the magic exponent in a register: one LOP3 per operand word
+        asm("" : "+r"(Mr));
+        // (v, v) as f16 for byte idx of w (v <= 63)
+        const auto pair = [&](uint32_t w, int idx) -> __half2 {
+            const uint32_t u = and_or<0x00FF00FFu>(prmt(w, 0u, 0x4040u | static_cast<uint32_t>(idx) |
+                                                                   (static_cast<uint32_t>(idx) << 8)), Mr);
+            return __hsub2(*reinterpret_cast<const __half2*>(&u),
+                           __halves2half2(__ushort_as_half(0x6400u), __ushort_as_half(0x6400u)));
+        };
+        const auto as_u = [](__half2 h) -> uint32_t { return *reinterpret_cast<const uint32_t*>(&h); };
+        const auto fma2 = [&](uint32_t a, __half2 m, __half2 c) -> uint32_t {
+            return as_u(__hfma2(*reinterpret_cast<const __half2*>(&a), m, c));
+        };
+        // mins: sum over sub-blocks of m_j * (sum of the activations of j), one
+        // f16 product with k slot q <-> 16-group q (sub-block q/2) of the chunk
+        float DM[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16(DM, as_u(pair(m0l, t)), as_u(pair(m1l, t)), as_u(pair(m0h, t)), as_u(pair(m1h, t)), X.bm[0],
+                X.bm[1]);
         uint32_t qh0a = 0u, qh0b = 0u, qh1a = 0u, qh1b = 0u;
         if constexpr (F == F_Q5_K) {  // high bits of elements 4t.. and 16+4t.., bit js of each byte
             qh0a = ld_s32(b0 + 16 + 4 * t) >> js0;
@@ -302,67 +257,69 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
             qh1a = ld_s32(b1 + 16 + 4 * t) >> js0;
             qh1b = ld_s32(b1 + 32 + 4 * t) >> js0;
         }
-        int iA[4] = {0, 0, 0, 0}, iH[4] = {0, 0, 0, 0}, iB[4] = {0, 0, 0, 0};
+        const __half2 k1024 = __halves2half2(__ushort_as_half(0xE400u), __ushort_as_half(0xE400u));  // -1024
+        const __half2 k64 = __halves2half2(__ushort_as_half(0xD400u), __ushort_as_half(0xD400u));    // -64
+        const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00u), __ushort_as_half(0x2C00u));  // 1/16
+        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
             if (32 * i < chunk) {
                 const uint32_t q = QS + 32u * static_cast<uint32_t>((js0 + i) >> 1) + 4u * t;
-                const uint32_t qa0 = ld_s32(b0 + q), qb0 = ld_s32(b0 + q + 16);
-                const uint32_t qa1 = ld_s32(b1 + q), qb1 = ld_s32(b1 + q + 16);
-                int D[4], E[4];
-                if constexpr (F == F_Q4_K) {
-                    mma_k32_s8(D, qa0 & 0x0F0F0F0Fu, qa1 & 0x0F0F0F0Fu, qb0 & 0x0F0F0F0Fu, qb1 & 0x0F0F0F0Fu,
-                               X.b[2 * i], X.b[2 * i + 1], 0, 0);
-                    mma_k32_u8(E, qa0 & 0xF0F0F0F0u, qa1 & 0xF0F0F0F0u, qb0 & 0xF0F0F0F0u, qb1 & 0xF0F0F0F0u,
-                               X.b[2 * i + 2], X.b[2 * i + 3]);
-                } else {
-                    // high bit of sub-block js0 + i (+1) into bit 4 of each byte
-                    const auto hb = [](uint32_t w, int k) -> uint32_t {
-                        return (k <= 4 ? (w << (4 - k)) : (w >> (k - 4))) & 0x10101010u;
-                    };
-                    mma_k32_s8(D, (qa0 & 0x0F0F0F0Fu) | hb(qh0a, i), (qa1 & 0x0F0F0F0Fu) | hb(qh1a, i),
-                               (qb0 & 0x0F0F0F0Fu) | hb(qh0b, i), (qb1 & 0x0F0F0F0Fu) | hb(qh1b, i), X.b[2 * i],
-                               X.b[2 * i + 1], 0, 0);
-                    mma_k32_s8(E, ((qa0 >> 4) & 0x0F0F0F0Fu) | hb(qh0a, i + 1),
-                               ((qa1 >> 4) & 0x0F0F0F0Fu) | hb(qh1a, i + 1), ((qb0 >> 4) & 0x0F0F0F0Fu) | hb(qh0b, i + 1),
-                               ((qb1 >> 4) & 0x0F0F0F0Fu) | hb(qh1b, i + 1), X.b[2 * i + 2], X.b[2 * i + 3], 0, 0);
+                const uint32_t w00 = ld_s32(b0 + q), w01 = ld_s32(b0 + q + 16);  // row g: bytes 4t.. and 16+4t..
+                const uint32_t w10 = ld_s32(b1 + q), w11 = ld_s32(b1 + q + 16);  // row g+8
+                const uint32_t v00 = w00 >> 8, v01 = w01 >> 8, v10 = w10 >> 8, v11 = w11 >> 8;
+                // operand words: index k -> row (k & 1), k slots (k >> 1) & 1, 16-step k >> 2
+                uint32_t L[8] = {and_or<0x000F000Fu>(w00, Mr), and_or<0x000F000Fu>(w10, Mr), and_or<0x000F000Fu>(v00, Mr),
+                                 and_or<0x000F000Fu>(v10, Mr), and_or<0x000F000Fu>(w01, Mr), and_or<0x000F000Fu>(w11, Mr),
+                                 and_or<0x000F000Fu>(v01, Mr), and_or<0x000F000Fu>(v11, Mr)};
+                uint32_t H[8] = {and_or<0x00F000F0u>(w00, Mr), and_or<0x00F000F0u>(w10, Mr), and_or<0x00F000F0u>(v00, Mr),
+                                 and_or<0x00F000F0u>(v10, Mr), and_or<0x00F000F0u>(w01, Mr), and_or<0x00F000F0u>(w11, Mr),
+                                 and_or<0x00F000F0u>(v01, Mr), and_or<0x00F000F0u>(v11, Mr)};
+                if constexpr (F == F_Q5_K) {
+                    // fifth bit of sub-block js0 + i (low) at bit 4 and of js0 + i + 1 (high) at bit 8
+                    // of each half; the qh words were shifted down by js0
+                    const uint32_t hq[4] = {qh0a, qh1a, qh0b, qh1b};  // (row g, row g+8) x (step 0, step 1)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // bytes (0, 2) of the word feed pair (0, 2), bytes (1, 3) pair (1, 3)
+                        const uint32_t h02 = hq[k], h13 = hq[k] >> 8;
+                        const int a = (k & 1) + 4 * (k >> 1);  // L/H index of (row, step), pair (0, 2)
+                        L[a] = and_or<0x00100010u>(i <= 4 ? (h02 << (4 - i)) : (h02 >> (i - 4)), L[a]);
+                        L[a + 2] = and_or<0x00100010u>(i <= 4 ? (h13 << (4 - i)) : (h13 >> (i - 4)), L[a + 2]);
+                        H[a] = and_or<0x01000100u>(h02 << (7 - i), H[a]);
+                        H[a + 2] = and_or<0x01000100u>(h13 << (7 - i), H[a + 2]);
+                    }
                 }
+                // scales of sub-blocks i (low) and i + 1 (high) for rows g, g+8:
+                // low: q * sc = (1024 + q) * sc - 1024 sc; high: (1024 + 16q) * sc/16 - 64 sc
                 const uint32_t w0s = i < 4 ? s0l : s0h, w1s = i < 4 ? s1l : s1h;
-                const uint32_t w0m = i < 4 ? m0l : m0h, w1m = i < 4 ? m1l : m1h;
-                const int sa0 = byte_u(w0s, i & 3), sb0 = byte_u(w0s, (i + 1) & 3);
-                const int sa1 = byte_u(w1s, i & 3), sb1 = byte_u(w1s, (i + 1) & 3);
-                const int ma0 = byte_u(w0m, i & 3), mb0 = byte_u(w0m, (i + 1) & 3);
-                const int ma1 = byte_u(w1m, i & 3), mb1 = byte_u(w1m, (i + 1) & 3);
-                iA[0] += sa0 * D[0];
-                iA[1] += sa0 * D[1];
-                iA[2] += sa1 * D[2];
-                iA[3] += sa1 * D[3];
-                iH[0] += sb0 * E[0];
-                iH[1] += sb0 * E[1];
-                iH[2] += sb1 * E[2];
-                iH[3] += sb1 * E[3];
-                iB[0] += ma0 * X.s[2 * i] + mb0 * X.s[2 * i + 2];
-                iB[1] += ma0 * X.s[2 * i + 1] + mb0 * X.s[2 * i + 3];
-                iB[2] += ma1 * X.s[2 * i] + mb1 * X.s[2 * i + 2];
-                iB[3] += ma1 * X.s[2 * i + 1] + mb1 * X.s[2 * i + 3];
+                const __half2 sa0 = pair(w0s, i & 3), sa1 = pair(w1s, i & 3);
+                const __half2 sb0 = pair(w0s, (i + 1) & 3), sb1 = pair(w1s, (i + 1) & 3);
+                const __half2 ca0 = __hmul2(sa0, k1024), ca1 = __hmul2(sa1, k1024);
+                const __half2 cb0 = __hmul2(sb0, k64), cb1 = __hmul2(sb1, k64);
+                const __half2 hb0 = __hmul2(sb0, k16th), hb1 = __hmul2(sb1, k16th);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    L[k] = fma2(L[k], (k & 1) ? sa1 : sa0, (k & 1) ? ca1 : ca0);
+                    H[k] = fma2(H[k], (k & 1) ? hb1 : hb0, (k & 1) ? cb1 : cb0);
+                }
+                mma_f16(D, L[0], L[1], L[2], L[3], X.b[4 * i], X.b[4 * i + 1]);
+                mma_f16(D, L[4], L[5], L[6], L[7], X.b[4 * i + 2], X.b[4 * i + 3]);
+                mma_f16(D, H[0], H[1], H[2], H[3], X.b[4 * i + 4], X.b[4 * i + 5]);
+                mma_f16(D, H[4], H[5], H[6], H[7], X.b[4 * i + 6], X.b[4 * i + 7]);
             }
         }
-        if constexpr (F == F_Q4_K) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) iA[k] += iH[k] >> 4;  // iH is 16x an integer: exact
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) iA[k] += iH[k];
-        }
         const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
-        acc[0] = X.dx0 * (d0 * static_cast<float>(iA[0]) - dm0 * static_cast<float>(iB[0]));
-        acc[1] = X.dx1 * (d0 * static_cast<float>(iA[1]) - dm0 * static_cast<float>(iB[1]));
-        acc[2] = X.dx0 * (d1 * static_cast<float>(iA[2]) - dm1 * static_cast<float>(iB[2]));
-        acc[3] = X.dx1 * (d1 * static_cast<float>(iA[3]) - dm1 * static_cast<float>(iB[3]));
+        acc[0] = X.dx0 * (d0 * D[0] - dm0 * DM[0]);
+        acc[1] = X.dx1 * (d0 * D[1] - dm0 * DM[1]);
+        acc[2] = X.dx0 * (d1 * D[2] - dm1 * DM[2]);
+        acc[3] = X.dx1 * (d1 * D[3] - dm1 * DM[3]);
     } else if constexpr (F == F_Q6_K) {
         // chunk = one or two 128-element halves; element 128h + 32g6 + l of a
         // superblock: low 4 bits in ql[64h + 32(g6&1) + l] (nibble g6>>1), high
-        // 2 bits in qh[32h + l] (bits 2g6), scale of 16-group (128h + 32g6 + l)/16
+        // 2 bits in qh[32h + l] (bits 2g6), scale of 16-group (128h + 32g6 + l)/16.
+        // f16 operands 1024 + code (C removes 1056 x the activation sum: weight
+        // code - 32); one m16n8k16 per 16-group, scaled in f32
         const int h0 = (e0 & 255) >> 7;
         const saddr b0 = r0 + 210u * sb, b1 = r1 + 210u * sb;
         uint32_t sw0[4], sw1[4];  // int8 scales of the chunk's 16-groups, four per word
@@ -371,7 +328,9 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         if (h0) {  // second half only: its eight scales are words 2 and 3
             sw0[0] = sw0[2], sw0[1] = sw0[3], sw1[0] = sw1[2], sw1[1] = sw1[3];
         }
-        int iA[4] = {0, 0, 0, 0};
+        uint32_t Mr = 0x64006400u;
+        asm("" : "+r"(Mr));
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             if (128 * hh < chunk) {
@@ -379,39 +338,43 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
 #pragma unroll
                 for (int lh = 0; lh < 2; ++lh) {
                     const uint32_t l = 16u * lh + 4u * t;
-                    uint32_t qla0, qlb0, qhw0, qla1, qlb1, qhw1;
-                    ld_words_any<1>(b0 + 64 * h + l, &qla0);
-                    ld_words_any<1>(b0 + 64 * h + 32 + l, &qlb0);
-                    ld_words_any<1>(b0 + 128 + 32 * h + l, &qhw0);
-                    ld_words_any<1>(b1 + 64 * h + l, &qla1);
-                    ld_words_any<1>(b1 + 64 * h + 32 + l, &qlb1);
-                    ld_words_any<1>(b1 + 128 + 32 * h + l, &qhw1);
+                    uint32_t ql[2][2], qh[2];  // [row][g6 & 1], [row]
+                    ld_words_any<1>(b0 + 64 * h + l, &ql[0][0]);
+                    ld_words_any<1>(b0 + 64 * h + 32 + l, &ql[0][1]);
+                    ld_words_any<1>(b0 + 128 + 32 * h + l, &qh[0]);
+                    ld_words_any<1>(b1 + 64 * h + l, &ql[1][0]);
+                    ld_words_any<1>(b1 + 64 * h + 32 + l, &ql[1][1]);
+                    ld_words_any<1>(b1 + 128 + 32 * h + l, &qh[1]);
 #pragma unroll
                     for (int g6 = 0; g6 < 4; ++g6) {
                         const int jl = 8 * hh + 2 * g6 + lh;  // 16-group within the chunk
-                        const int js = 2 * g6 + lh;           // 16-group within the half
-                        const uint32_t w0 = (g6 & 1) ? qlb0 : qla0, w1 = (g6 & 1) ? qlb1 : qla1;
-                        const uint32_t a0 = ((w0 >> (4 * (g6 >> 1))) & 0x0F0F0F0Fu) | (((qhw0 >> (2 * g6)) & 0x03030303u) << 4);
-                        const uint32_t a1 = ((w1 >> (4 * (g6 >> 1))) & 0x0F0F0F0Fu) | (((qhw1 >> (2 * g6)) & 0x03030303u) << 4);
-                        const int cs0 = -32 * static_cast<int>(static_cast<int16_t>(X.s[jl] & 0xFFFF));
-                        const int cs1 = -32 * (X.s[jl] >> 16);
-                        int D[4];
-                        mma_k16_u8(D, a0, a1, X.b[jl], cs0, cs1);
-                        const int sj = 8 * hh + js;  // scale index within the chunk
-                        const int sc0 = byte_s(sw0[sj >> 2], sj & 3), sc1 = byte_s(sw1[sj >> 2], sj & 3);
-                        iA[0] += sc0 * D[0];
-                        iA[1] += sc0 * D[1];
-                        iA[2] += sc1 * D[2];
-                        iA[3] += sc1 * D[3];
+                        uint32_t A[4];  // (row g | row g+8) x (elements 0,2 | 1,3)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const uint32_t w = (g6 >> 1) ? ql[r][g6 & 1] >> 4 : ql[r][g6 & 1];
+                            const uint32_t hb = g6 == 0 ? qh[r] << 4 : g6 == 1 ? qh[r] << 2 : g6 == 2 ? qh[r] : qh[r] >> 2;
+                            A[r] = and_or<0x00300030u>(hb, and_or<0x000F000Fu>(w, Mr));
+                            A[2 + r] = and_or<0x00300030u>(hb >> 8, and_or<0x000F000Fu>(w >> 8, Mr));
+                        }
+                        const float c0 = ld_f32(cs + 8u * jl), c1 = ld_f32(cs + 8u * jl + 4);
+                        float D[4] = {c0, c1, c0, c1};
+                        mma_f16(D, A[0], A[1], A[2], A[3], X.b[2 * jl], X.b[2 * jl + 1]);
+                        const int sj = jl;  // scale index within the chunk
+                        const float sc0 = static_cast<float>(byte_s(sw0[sj >> 2], sj & 3));
+                        const float sc1 = static_cast<float>(byte_s(sw1[sj >> 2], sj & 3));
+                        a[0] += sc0 * D[0];
+                        a[1] += sc0 * D[1];
+                        a[2] += sc1 * D[2];
+                        a[3] += sc1 * D[3];
                     }
                 }
             }
         }
         const float d0 = ld_h(b0 + 208), d1 = ld_h(b1 + 208);
-        acc[0] = static_cast<float>(iA[0]) * (X.dx0 * d0);
-        acc[1] = static_cast<float>(iA[1]) * (X.dx1 * d0);
-        acc[2] = static_cast<float>(iA[2]) * (X.dx0 * d1);
-        acc[3] = static_cast<float>(iA[3]) * (X.dx1 * d1);
+        acc[0] = a[0] * (X.dx0 * d0);
+        acc[1] = a[1] * (X.dx1 * d0);
+        acc[2] = a[2] * (X.dx0 * d1);
+        acc[3] = a[3] * (X.dx1 * d1);
     } else {  // Q8_0 and MXFP4: one scale per 32-block
         const int blk0 = e0 >> 5;  // even: chunks start at multiples of 64
         acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
@@ -473,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     uint8_t* ring = smem;
     uint8_t* xreg = smem + static_cast<size_t>(p.stages) * p.stage_stride;
     float* red = reinterpret_cast<float*>(xreg);
-    float* creg = reinterpret_cast<float*>(xreg + p.x_bytes);  // [16 warps][4][16]
-    uint64_t* full = reinterpret_cast<uint64_t*>(creg + kConsumerWarps * 4 * 16);
+    float* creg = reinterpret_cast<float*>(xreg + p.x_bytes);  // [16 warps][4][32]
+    uint64_t* full = reinterpret_cast<uint64_t*>(creg + kConsumerWarps * 4 * 32);
     uint64_t* empty = full + kMaxStages;
     uint64_t* xbar = empty + kMaxStages;
 
@@ -550,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     const bool active = warp < p.nch;
     const int e0 = warp * p.chunk;
     MmaX X;
-    float* cs = creg + (warp * 4 + t) * 16;
+    float* cs = creg + (warp * 4 + t) * 32;
     mmav_load_x<F>(smem_addr(xreg), p.xrow, active ? p.T : 0, p.chunk, e0, g, t, X, cs);
     mmav_sync();  // the region now holds partials
     const saddr ring_s = smem_addr(ring);
