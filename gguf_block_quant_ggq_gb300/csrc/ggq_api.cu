@@ -493,6 +493,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     p.h = reinterpret_cast<float*>(c->pool + ms.h);
     p.xq_dump = dump ? static_cast<uint8_t*>(dump->xq) : nullptr;
     p.hq = c->pool + ms.hq;
+    p.early_weights = c->static_weights;
     p.g_dump = dump ? dump->g : nullptr;
     p.u_dump = dump ? dump->u : nullptr;
     p.o_dump = dump ? dump->o : nullptr;

@@ -32,6 +32,7 @@ struct DirectPlan {
     float wt[kDirectMaxPairs];                    // routing weight of pair p
     int ids[kDirectMaxPairs];                     // expert of pair p
     int bad;                                      // a routed id was out of range
+    int tok[kDirectMaxPairs];                     // token of pair p (p / top_k)
 };
 
 // Group the P <= 32 pairs (expert ids in s->ids) by distinct expert, in order
@@ -74,7 +75,7 @@ __device__ __forceinline__ void direct_route_token(const float* __restrict__ l, 
         int bi = 0x7fffffff;
         for (int i = 0, e = lane; e < E; ++i, e += 32) {
             if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
-            const float v = __ldg(l + e);
+            const float v = __ldcg(l + e);
             if (v > bv || (v == bv && e < bi)) {
                 bv = v;
                 bi = e;
@@ -107,15 +108,69 @@ __device__ __forceinline__ void direct_route_token(const float* __restrict__ l, 
     }
 }
 
+// The same routing with the token's logits held in registers (E <= 256).  Each
+// round is two warp reductions: the largest logit as an order-preserving
+// integer key (redux.sync max), then the lowest expert index carrying it
+// (redux.sync min) -- the fp32 comparison with ties to the lower index, without
+// a shuffle chain.  -0 counts as +0 (they compare equal); NaN and taken experts
+// get key 0, which no logit's key reaches.
+__device__ __forceinline__ unsigned route_key(float f) {
+    if (f != f) return 0u;
+    const unsigned b = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ void direct_route_token_reg(const float* __restrict__ l, int E, int k, int* ids, float* w,
+                                                       int lane) {
+    float v[8];
+    unsigned key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[i] = lane + 32 * i < E ? __ldcg(l + lane + 32 * i) : 0.0f;
+        key[i] = lane + 32 * i < E ? route_key(v[i]) : 0u;
+    }
+    float lmax = 0.0f, wsum = 0.0f, myw = 0.0f;
+    int myid = 0;
+    for (int j = 0; j < k; ++j) {
+        unsigned km = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) km = key[i] > km ? key[i] : km;
+        km = __reduce_max_sync(0xffffffffu, km);
+        unsigned im = 0xffffffffu;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (key[i] == km && im == 0xffffffffu) im = static_cast<unsigned>(lane + 32 * i);  // lowest of this lane
+        const int bi = static_cast<int>(__reduce_min_sync(0xffffffffu, im));
+        float bv = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (lane + 32 * i == bi) {
+                bv = v[i];
+                key[i] = 0u;
+            }
+        bv = __shfl_sync(0xffffffffu, bv, bi & 31);
+        if (j == 0) lmax = bv;
+        const float p = expf(bv - lmax);
+        wsum += p;
+        if (lane == j) {
+            myid = bi;
+            myw = p;
+        }
+    }
+    if (lane < k) {
+        ids[lane] = myid;
+        w[lane] = myw / wsum;
+    }
+}
+
 // Quantize the 256-element block `blk` of an fp32 row (global memory) to Q8_K
 // straight into the shared-memory activation region (row `row`), with the
 // same arithmetic as warp_quant_q8k.  Optionally also writes the packed block.
+// `a`, `b` are the lane's eight values (elements 8 lane .. 8 lane + 7 of the block).
 template <bool PERM>
-__device__ __forceinline__ void warp_quant_to_smem(const float* src, int row, int blk, int K, const XRegion& x,
+__device__ __forceinline__ void warp_quant_to_smem(float4 a, float4 b, int row, int blk, int K, const XRegion& x,
                                                    uint8_t* packed, int lane) {
     float v[8];
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + 2 * lane);
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 2 * lane + 1);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     float m = 0.0f;
 #pragma unroll
@@ -173,6 +228,7 @@ struct DirectParams {
     float* h;                    // [T*k][I]
     uint8_t* xq_dump;            // optional packed Q8_K of x
     uint8_t* hq;                 // optional packed Q8_K of h (down CTA 0)
+    int early_weights;           // 1: stream weights before waiting for the previous kernel
     float* g_dump;
     float* u_dump;
     float* o_dump;               // optional [T*k][H]
@@ -188,8 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     constexpr int LV = NT == 1 ? 0 : NT == 2 ? 1 : 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = p.K, P = p.T * p.top_k;
-    pdl_launch_dependents();
-    pdl_wait();  // logits, x, routed ids and h come from earlier kernels
+    if constexpr (KIND == KIND_GATEUP) {
+        pdl_wait();               // logits (or routed ids) and x come from earlier kernels
+        pdl_launch_dependents();  // the down kernel, once it runs, may read them without waiting
+    } else {
+        pdl_launch_dependents();  // h is read only after pdl_wait below
+    }
 
     uint8_t* ring = smem;
     uint8_t* xreg = smem + static_cast<size_t>(p.stages) * p.stage_stride;
@@ -207,22 +267,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
         }
         fence_barrier_init();
     }
-    if constexpr (KIND == KIND_GATEUP) {
-        if (warp < p.T) {
-            if (p.logits) {
+    // both kernels route from the same inputs with the same arithmetic
+    if (warp < p.T) {
+        if (p.logits) {
+            if (p.E <= 256)
+                direct_route_token_reg(p.logits + static_cast<int64_t>(warp) * p.E, p.E, p.top_k,
+                                       plan->ids + warp * p.top_k, plan->wt + warp * p.top_k, lane);
+            else
                 direct_route_token(p.logits + static_cast<int64_t>(warp) * p.E, p.E, p.top_k,
                                    plan->ids + warp * p.top_k, plan->wt + warp * p.top_k, lane);
-            } else if (lane < p.top_k) {
-                plan->ids[warp * p.top_k + lane] = p.ids_in[warp * p.top_k + lane];
-                plan->wt[warp * p.top_k + lane] = p.w_in[warp * p.top_k + lane];
-            }
-        }
-    } else {
-        if (tid < P) {
-            plan->ids[tid] = __ldcg(p.ids + tid);
-            plan->wt[tid] = __ldcg(p.w + tid);
+        } else if (lane < p.top_k) {
+            plan->ids[warp * p.top_k + lane] = __ldcg(p.ids_in + warp * p.top_k + lane);
+            plan->wt[warp * p.top_k + lane] = __ldcg(p.w_in + warp * p.top_k + lane);
         }
     }
+    if (tid < P) plan->tok[tid] = tid / p.top_k;
     __syncthreads();
     if (warp == 0) direct_group(plan, P, p.E, lane);
     __syncthreads();
@@ -240,14 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
         // ================= producer: one stage per (expert, tile) pair
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int j = 0;
+            if (KIND == KIND_DOWN && !p.early_weights) pdl_wait();  // the weights may come from earlier kernels
+            int j = 0, s = 0;
+            uint32_t ph = 0u;  // ring slot and phase of stage j
             for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
                 const int ne = KIND == KIND_GATEUP ? 1 : D;
-                for (int q = 0; q < ne; ++q, ++j) {
+                for (int q = 0; q < ne; ++q, ++j, s = s + 1 == p.stages ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
                     const int u = KIND == KIND_GATEUP ? item / tiles : q;
                     const int tile = KIND == KIND_GATEUP ? item - u * tiles : item;
-                    const int s = j % p.stages;
-                    if (!mbar_wait(&empty[s], (static_cast<uint32_t>(j / p.stages) & 1u) ^ 1u)) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u)) {
                         set_error(p.err, DEV_ERR_TIMEOUT);
                         goto drain;
                     }
@@ -267,17 +327,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
         return;
     }
 
-    // ================= consumers: quantize the activations into shared memory
-    {
-        const int nbr = K >> 8;
-        for (int b = warp; b < xrows * nbr; b += kConsumerWarps) {
-            const int r = b / nbr, c = b - r * nbr;
-            if constexpr (KIND == KIND_GATEUP) {
-                uint8_t* pk = (blockIdx.x == 0 && p.xq_dump) ? p.xq_dump + static_cast<int64_t>(b) * 292 : nullptr;
-                warp_quant_to_smem<F == F_MXFP4>(p.X + static_cast<int64_t>(b) * 256, r, c, K, xr_, pk, lane);
-            } else {
-                uint8_t* pk = (blockIdx.x == 0 && p.hq) ? p.hq + static_cast<int64_t>(b) * 292 : nullptr;
-                warp_quant_to_smem<F == F_MXFP4>(p.h + static_cast<int64_t>(b) * 256, r, c, K, xr_, pk, lane);
+    // ================= consumers: the activations into shared memory
+    if constexpr (KIND == KIND_GATEUP) {
+        // quantize x (every CTA; a few blocks per warp, their loads issued together)
+        const int nbr = K >> 8, nb = xrows * nbr;
+        for (int b0 = warp; b0 < nb; b0 += 4 * kConsumerWarps) {
+            float4 va[4], vb[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int b = b0 + h * kConsumerWarps;
+                if (b < nb) {
+                    const float4* src = reinterpret_cast<const float4*>(p.X + static_cast<int64_t>(b) * 256);
+                    va[h] = __ldcg(src + 2 * lane);
+                    vb[h] = __ldcg(src + 2 * lane + 1);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int b = b0 + h * kConsumerWarps;
+                if (b < nb) {
+                    const int r = b / nbr, c = b - r * nbr;
+                    uint8_t* pk = (blockIdx.x == 0 && p.xq_dump) ? p.xq_dump + static_cast<int64_t>(b) * 292 : nullptr;
+                    warp_quant_to_smem<F == F_MXFP4>(va[h], vb[h], r, c, K, xr_, pk, lane);
+                }
+            }
+        }
+    } else {
+        // quantize h (every CTA: all pairs, K/256 blocks each; loads of four blocks in flight)
+        pdl_wait();  // h comes from the gate/up kernel
+        const int nbr = K >> 8, nb = xrows * nbr;
+        for (int b0 = warp; b0 < nb; b0 += 4 * kConsumerWarps) {
+            float4 va[4], vb[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int b = b0 + h * kConsumerWarps;
+                if (b < nb) {
+                    const float4* src = reinterpret_cast<const float4*>(p.h + static_cast<int64_t>(b) * 256);
+                    va[h] = __ldcg(src + 2 * lane);
+                    vb[h] = __ldcg(src + 2 * lane + 1);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int b = b0 + h * kConsumerWarps;
+                if (b < nb) {
+                    const int r = b / nbr, c = b - r * nbr;
+                    uint8_t* pk = (blockIdx.x == 0 && p.hq) ? p.hq + static_cast<int64_t>(b) * 292 : nullptr;
+                    warp_quant_to_smem<F == F_MXFP4>(va[h], vb[h], r, c, K, xr_, pk, lane);
+                }
             }
         }
     }
@@ -291,17 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     const saddr ring_s = smem_addr(ring);
     constexpr int SH = 5 - (LV + (KIND == KIND_GATEUP ? 1 : 0));
 
-    int j = 0;
+    int s = 0;
+    uint32_t ph = 0u;  // ring slot and phase of the next stage
+    const auto next_stage = [&]() {
+        if (++s == p.stages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    };
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
         if constexpr (KIND == KIND_GATEUP) {
             const int u = item / tiles, tile = item - u * tiles;
-            const int s = j % p.stages;
-            const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(j / p.stages) & 1u));
-            ++j;
+            const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
             const int np = plan->npairs[u];
             int xr[NT];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->pair[u][t] / p.top_k : 0;
+            for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->tok[plan->pair[u][t]] : 0;
             const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
             const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
             if (ready) {
@@ -326,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            next_stage();
             if (!ready) break;
         } else {
             const int tile = item;
@@ -333,9 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
             // y for the T tokens of this row, accumulated over the experts in plan order
             float yacc = 0.0f;  // lane t (t < T) holds y[t][row] after each reduction
             bool ok = true;
-            for (int u = 0; u < D; ++u, ++j) {
-                const int s = j % p.stages;
-                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(j / p.stages) & 1u));
+            for (int u = 0; u < D; ++u) {
+                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
                 const int np = plan->npairs[u];
                 int xr[NT];
 #pragma unroll
@@ -352,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                     if (pp >= 0 && (lane & ((1 << SH) - 1)) == 0 && p.o_dump) p.o_dump[static_cast<int64_t>(pp) * p.N + row] = v;
                     // move each slot's weighted value to the lane of its token
                     const float contrib = pp >= 0 ? plan->wt[pp] * v : 0.0f;
-                    const int tok = pp >= 0 ? pp / p.top_k : -1;
+                    const int tok = pp >= 0 ? plan->tok[pp] : -1;
 #pragma unroll
                     for (int q = 0; q < NT; ++q) {
                         const float cq = __shfl_sync(0xffffffffu, contrib, q << SH);
@@ -365,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                next_stage();
             }
             if (ok && lane < p.T) p.Y[static_cast<int64_t>(lane) * p.N + row] = yacc;
             if (!ok) break;

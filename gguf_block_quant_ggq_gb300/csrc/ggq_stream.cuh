@@ -55,36 +55,76 @@ __device__ __forceinline__ XRegion x_region(uint8_t* base, int rows, int K, bool
 // the structure-of-arrays region.  PERM stores each 32-block's quants in the
 // interleaved order (0,16,1,17,...) that the MXFP4 lookup produces.  The Q8_1
 // per-32 sums must be zero on entry (they are accumulated with atomics).
+// Stage packed activation rows (Q8_K: 292-byte blocks, rows `pitch` bytes
+// apart (0: packed); Q8_1: 36-byte blocks) from global into the
+// structure-of-arrays region.  PERM stores each 32-block's quants in the
+// interleaved order (0,16,1,17,...) that the MXFP4 lookup produces.  The Q8_1
+// per-32 sums must be zero on entry (they are accumulated with atomics).
+// Q8_K work unit: one 32-element quant group (8 words) or the scale and the
+// sixteen sums of a block (9 words); two units per thread per round, all their
+// loads in flight together.
 template <bool Q81, bool PERM>
-__device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, const XRegion& x, int tid, int nthr) {
+__device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, const XRegion& x, int tid, int nthr,
+                           int pitch = 0) {
     const int rb = xq_row_bytes(K);
     if constexpr (!Q81) {
         const int nbr = K >> 8;
-        const int nb = rows * nbr;
-        const int words = nb * 73;
-        for (int i = tid; i < words; i += nthr) {
-            const int b = i / 73, w = i - b * 73;
-            const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(b) * 292) + w);
-            const int row = b / nbr, cb = b - row * nbr;
-            if (w == 0) {
-                x.d[b] = __uint_as_float(v);
-            } else if (w <= 64) {
-                int8_t* dq = x.q + static_cast<size_t>(row) * rb;
-                const int e = 256 * cb + 4 * (w - 1);
-                if constexpr (!PERM) {
-                    *reinterpret_cast<uint32_t*>(dq + xq_addr(e)) = v;
-                } else {
+        const int units = rows * nbr * 9;
+        if (pitch == 0) pitch = nbr * 292;
+        for (int u0 = tid; u0 < units; u0 += 2 * nthr) {
+            uint32_t w[2][9];
+            int blk[2], part[2], row[2], cb[2];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int el = e + j, r = el & 31;
-                        dq[xq_addr((el & ~31) + 2 * (r & 15) + (r >> 4))] = static_cast<int8_t>((v >> (8 * j)) & 0xFF);
+            for (int h = 0; h < 2; ++h) {
+                const int u = u0 + h * nthr;
+                blk[h] = u / 9;
+                part[h] = u - blk[h] * 9;
+                row[h] = blk[h] / nbr;
+                cb[h] = blk[h] - row[h] * nbr;
+                if (u < units) {
+                    const uint32_t* bp = reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(row[h]) * pitch +
+                                                                           static_cast<size_t>(cb[h]) * 292);
+                    if (part[h] < 8) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[h][i] = __ldcg(bp + 1 + 8 * part[h] + i);
+                        w[h][8] = 0u;
+                    } else {
+                        w[h][0] = __ldcg(bp);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[h][1 + i] = __ldcg(bp + 65 + i);
                     }
                 }
-            } else {
-                const int j = w - 65;  // bsums 2j, 2j+1 of block b
-                reinterpret_cast<uint32_t*>(x.bs + static_cast<size_t>(b) * 16)[j] = v;
-                x.s32[static_cast<size_t>(b) * 8 + j] =
-                    static_cast<int>(static_cast<int16_t>(v & 0xFFFFu)) + static_cast<int>(static_cast<int16_t>(v >> 16));
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (u0 + h * nthr >= units) break;
+                const int b = blk[h];
+                if (part[h] < 8) {
+                    const uint32_t* v = w[h];
+                    uint4 lo, hi;
+                    if constexpr (PERM) {  // (j, j+16, j+1, j+17) per output word
+                        lo = make_uint4(prmt(v[0], v[4], 0x5140u), prmt(v[0], v[4], 0x7362u), prmt(v[1], v[5], 0x5140u),
+                                        prmt(v[1], v[5], 0x7362u));
+                        hi = make_uint4(prmt(v[2], v[6], 0x5140u), prmt(v[2], v[6], 0x7362u), prmt(v[3], v[7], 0x5140u),
+                                        prmt(v[3], v[7], 0x7362u));
+                    } else {
+                        lo = make_uint4(v[0], v[1], v[2], v[3]);
+                        hi = make_uint4(v[4], v[5], v[6], v[7]);
+                    }
+                    // a 32-group lies inside one padded 64-element unit: 32 contiguous bytes, 16-aligned
+                    int8_t* dq = x.q + static_cast<size_t>(row[h]) * rb + xq_addr(256 * cb[h] + 32 * part[h]);
+                    reinterpret_cast<uint4*>(dq)[0] = lo;
+                    reinterpret_cast<uint4*>(dq)[1] = hi;
+                } else {
+                    x.d[b] = __uint_as_float(w[h][0]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t v = w[h][1 + j];  // bsums 2j, 2j+1
+                        reinterpret_cast<uint32_t*>(x.bs + static_cast<size_t>(b) * 16)[j] = v;
+                        x.s32[static_cast<size_t>(b) * 8 + j] = static_cast<int>(static_cast<int16_t>(v & 0xFFFFu)) +
+                                                               static_cast<int>(static_cast<int16_t>(v >> 16));
+                    }
+                }
             }
         }
     } else {
