@@ -25,6 +25,7 @@ cudaError_t launch_gemv_a(int kind, int fmt, int nt, const StreamParams& p, int 
 cudaError_t launch_gemv_b(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_gateup(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_down(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_direct_downf(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
     if (fmt == F_Q4_0 || fmt == F_Q8_0 || fmt == F_MXFP4) return launch_gemv_a(kind, fmt, nt, p, grid, smem, s);
@@ -517,20 +518,36 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         cudaError_t e = launch_direct_gateup(fg, nt, p, c->nsm, sh.smem, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe gate/up launch");
     }
-    // down: 16-row output tile of every selected expert; h^ of the T*k pairs
+    // down: 16-row output tile of every selected expert; h^ of the T*k pairs.
+    // Fused (no per-pair outputs requested): G experts per stage, the largest G
+    // that leaves three stages and at most 256 units per concatenated row
     {
         p.W = static_cast<const uint8_t*>(w->down);
         p.W2 = nullptr;
         p.rowbytes = w_row_bytes(fd, I);
         p.N = H;
         p.K = static_cast<int>(I);
+        const bool fused = !(dump && dump->o);
         StreamShape sh;
-        if (!plan_stream(kTileRows * p.rowbytes, P, p.K, false, &sh, direct_fixed))
+        int G = 1;
+        if (fused) {
+            for (int g = 8; g >= 1; --g) {
+                if (g * (I / 64) > 256) continue;
+                if (plan_stream(g * kTileRows * p.rowbytes, P, p.K, false, &sh, direct_fixed) &&
+                    (sh.stages >= 3 || g == 1)) {
+                    G = g;
+                    break;
+                }
+            }
+        }
+        if (!plan_stream(G * kTileRows * p.rowbytes, P, p.K, false, &sh, direct_fixed))
             return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
+        p.G = G;
         p.stages = sh.stages;
         p.stage_stride = sh.stride;
         p.x_bytes = sh.x_bytes;
-        cudaError_t e = launch_direct_down(fd, nt, p, c->nsm, sh.smem, st);
+        cudaError_t e = fused ? launch_direct_downf(fd, nt, p, c->nsm, sh.smem, st)
+                              : launch_direct_down(fd, nt, p, c->nsm, sh.smem, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe down launch");
     }
     if (dump) {

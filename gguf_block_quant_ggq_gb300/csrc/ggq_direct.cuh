@@ -10,11 +10,16 @@
 //     into shared memory.  Each consumer warp owns one gate row and the same
 //     up row of a 16-row tile, so h = silu(g) * u is formed in the warp and
 //     written once to global memory (fp32).
-//   down kernel: rebuilds the same grouping from the routed ids, quantizes h
-//     to Q8_K into shared memory (bit-exactly the same quantizer), and for
-//     each 16-row tile of the output streams that tile of every selected
-//     expert, accumulating y = sum_j w_j o_j in registers in a fixed expert
-//     order, so the result is deterministic.
+//   down kernel: routes again from the same inputs (so its weight stream can
+//     start while gate/up finishes), quantizes h to Q8_K into shared memory
+//     (bit-exactly the same quantizer), and for each 16-row tile of the output
+//     streams that tile of every selected expert, G experts per stage.  A
+//     warp's row of the G experts is one concatenated row spread over all 32
+//     lanes; each lane adds w_j * (its partial of pair j) straight into the
+//     sum of pair j's token, and one reduction per tile gives y, so the
+//     result is deterministic.  With a per-pair dump requested, the down
+//     kernel instead takes one expert per stage and reduces every pair
+//     (o_j) before combining.
 // Both kernels stream weights with the producer warp / mbarrier ring of the
 // streaming kernel and use its dp4a consumer (row_accumulate).
 #pragma once
@@ -23,6 +28,7 @@
 namespace ggq {
 
 constexpr int kDirectMaxPairs = 32;  // 4 tokens x top-8
+constexpr int kDownUnits = 8;        // fused down: 64-weight units per lane per stage (G * K/64 <= 256)
 
 struct DirectPlan {
     int D;                                        // distinct experts
@@ -228,7 +234,8 @@ struct DirectParams {
     float* h;                    // [T*k][I]
     uint8_t* xq_dump;            // optional packed Q8_K of x
     uint8_t* hq;                 // optional packed Q8_K of h (down CTA 0)
-    int early_weights;           // 1: stream weights before waiting for the previous kernel
+    int early_weights;
+    int G;                       // fused down: experts per stage           // 1: stream weights before waiting for the previous kernel
     float* g_dump;
     float* u_dump;
     float* o_dump;               // optional [T*k][H]
@@ -237,10 +244,12 @@ struct DirectParams {
     int stages, stage_stride, x_bytes;
 };
 
-// Gate/up (KIND_GATEUP) or down (KIND_DOWN) of the direct route.
+// Gate/up (KIND_GATEUP), down with per-pair outputs (KIND_DOWN) or fused
+// down (KIND_DOWNF) of the direct route.
 template <int KIND, int F, int NT>
 __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr bool DOWN = KIND != KIND_GATEUP;
     constexpr int LV = NT == 1 ? 0 : NT == 2 ? 1 : 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = p.K, P = p.T * p.top_k;
@@ -299,10 +308,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
         // ================= producer: one stage per (expert, tile) pair
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            if (KIND == KIND_DOWN && !p.early_weights) pdl_wait();  // the weights may come from earlier kernels
+            if (DOWN && !p.early_weights) pdl_wait();  // the weights may come from earlier kernels
             int j = 0, s = 0;
             uint32_t ph = 0u;  // ring slot and phase of stage j
             for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+                if constexpr (KIND == KIND_DOWNF) {
+                    // one stage per group of G experts: the item's tile of each
+                    for (int ug = 0; ug < D; ug += p.G, ++j, s = s + 1 == p.stages ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+                        if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                            set_error(p.err, DEV_ERR_TIMEOUT);
+                            goto drain;
+                        }
+                        const int gc = D - ug < p.G ? D - ug : p.G;
+                        const uint32_t bytes = static_cast<uint32_t>(kTileRows * p.rowbytes);  // multiple of 16
+                        uint8_t* dst = ring + static_cast<size_t>(s) * p.stage_stride;
+                        mbar_arrive_expect_tx(&full[s], gc * bytes);
+                        for (int g = 0; g < gc; ++g) {
+                            const int64_t e = plan->expert[ug + g];
+                            const int64_t off = (e * p.N + static_cast<int64_t>(item) * kTileRows) * p.rowbytes;
+                            bulk_g2s(dst + static_cast<size_t>(g) * bytes, p.W + off, bytes, &full[s], pol);
+                        }
+                    }
+                    continue;
+                }
                 const int ne = KIND == KIND_GATEUP ? 1 : D;
                 for (int q = 0; q < ne; ++q, ++j, s = s + 1 == p.stages ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
                     const int u = KIND == KIND_GATEUP ? item / tiles : q;
@@ -388,6 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     const saddr ring_s = smem_addr(ring);
     constexpr int SH = 5 - (LV + (KIND == KIND_GATEUP ? 1 : 0));
 
+    // fused down: the lane's units of a warp's concatenated row (G experts x nu
+    // units): slot i is unit lane + 32 i, expert vg[i] (>= G: none), unit vu[i]
+    const int nb32 = K >> 5;
+    int vg[kDownUnits], vu[kDownUnits];
+    if constexpr (KIND == KIND_DOWNF) {
+        const int nu = units_per_row(K);
+#pragma unroll
+        for (int i = 0; i < kDownUnits; ++i) {
+            const int v = lane + 32 * i;
+            vg[i] = v < p.G * nu ? v / nu : kDirectMaxPairs;
+            vu[i] = v < p.G * nu ? v - vg[i] * nu : 0;
+        }
+    }
     int s = 0;
     uint32_t ph = 0u;  // ring slot and phase of the next stage
     const auto next_stage = [&]() {
@@ -430,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
             if (lane == 0) mbar_arrive(&empty[s]);
             next_stage();
             if (!ready) break;
-        } else {
+        } else if constexpr (KIND == KIND_DOWN) {
             const int tile = item;
             const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
             // y for the T tokens of this row, accumulated over the experts in plan order
@@ -470,6 +511,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                 next_stage();
             }
             if (ok && lane < p.T) p.Y[static_cast<int64_t>(lane) * p.N + row] = yacc;
+            if (!ok) break;
+        } else {
+            // fused down: y[t][row] = sum over experts and their pairs of w * (W_e row . h^_pair),
+            // each lane adding the weighted partials of its units into its token sums
+            const int64_t row = static_cast<int64_t>(item) * kTileRows + warp;
+            float acc[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+            bool ok = true;
+            for (int ug = 0; ug < D; ug += p.G) {
+                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
+                if (ready && ok) {
+                    const int gc = D - ug < p.G ? D - ug : p.G;
+                    const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+#pragma unroll
+                    for (int i = 0; i < kDownUnits; ++i) {
+                        if (vg[i] < gc) {
+                            const int g = vg[i], ur = vu[i], u = ug + g;
+                            const int np = plan->npairs[u];
+                            const saddr rowp = stage + static_cast<uint32_t>((g * kTileRows + warp) * p.rowbytes);
+                            Unit un;
+                            load_unit<F>(rowp, ur, nb32, un);
+                            int xo[4];
+                            unit_offsets<F>(ur, xo);
+#pragma unroll
+                            for (int jj = 0; jj < NT; ++jj) {
+                                if (jj < np) {
+                                    const int pr = plan->pair[u][jj];
+                                    int A0, A1;
+                                    unit_ints<F>(un, xo, xs, pr, ur, A0, A1);
+                                    const float val = plan->wt[pr] * unit_value<F>(un, xs, pr, ur, A0, A1);
+                                    const int tk = plan->tok[pr];
+#pragma unroll
+                                    for (int t = 0; t < NT; ++t)
+                                        if (t == tk) acc[t] += val;
+                                }
+                            }
+                        }
+                    }
+                } else if (!ready) {
+                    set_error(p.err, DEV_ERR_TIMEOUT);
+                    ok = false;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                next_stage();
+            }
+            const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = token
+            const int t = lane >> SH;
+            if (ok && (lane & ((1 << SH) - 1)) == 0 && t < p.T) p.Y[static_cast<int64_t>(t) * p.N + row] = v;
             if (!ok) break;
         }
     }

@@ -15,7 +15,7 @@ constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per CTA
 constexpr int kMaxDevices = 64;     // device ordinals with per-device launch state
 
-enum Kind : int { KIND_GEMV = 0, KIND_DUMP = 1, KIND_GATEUP = 2, KIND_DOWN = 3 };
+enum Kind : int { KIND_GEMV = 0, KIND_DUMP = 1, KIND_GATEUP = 2, KIND_DOWN = 3, KIND_DOWNF = 4 };
 
 struct StreamParams {
     const uint8_t* W;   // GEMV weight matrix

@@ -118,6 +118,14 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     y_abs = orc.moe_combine(o_abs, w_ref, T, k, H)[toks]
     # routing weights carry fp32 rounding (<= 2e-6 relative): widen the scale by 30 %
     check_outputs(y[toks], y_tf, 1.3 * y_abs, "combine")
+    # (v') the same layer without dumps takes the fused down path (no per-pair
+    # outputs; partials added straight into the token sums): same h^, same bar
+    if routed:
+        y2 = ctx.moe_experts(w8, E, H, I, k, to_dev(x), ids=to_dev(ids_ref), route_w=to_dev(w_ref.astype(np.float32)))
+    else:
+        y2 = ctx.moe_experts(w8, E, H, I, k, to_dev(x), logits=to_dev(logits))
+    ctx.sync_status()
+    check_outputs(to_host(y2).astype(np.float64)[toks], y_tf, 1.3 * y_abs, "combine (fused down)")
     # free running against the whole oracle layer on the checked tokens
     ref = orc.moe(cfg["gate"], host["gate"], cfg["up"], host["up"], cfg["down"], host["down"], E, H, I, k,
                   x[toks], logits[toks])
