@@ -43,6 +43,31 @@ ROTATE = 3
 METRIC = "decode GEMV/MoE packed-weight GB/s (% of HBM); prefill expert GEMM int8 TOPS"
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_kquant_gemv_step.json")
+
+
+def csrc_hash():
+    """Hash of the kernel sources: a stored DRAM-traffic figure applies only to the kernels it was taken on."""
+    import hashlib
+    d = os.path.join(ROOT, "gguf_block_quant_ggq_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic():
+    """Mean DRAM bytes (read + write) per GEMV launch of one step, from the ncu summary, or None if stale."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        return float(t["mean_traffic_bytes"]) if t.get("csrc_hash") == csrc_hash() else None
+    except Exception:
+        return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -384,11 +409,16 @@ def run_gpu(args, rank, world):
                "seconds": round(secs, 2)}
 
     gpu_launches = (len(TOKENS) + len(plan)) * args.steps  # 4 quantize + 16 GEMV kernels per step
+    traffic = stored_traffic()
+    if traffic is not None:
+        traffic = round(traffic)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a, f32 epilogue", "data": "synthetic (seeded)",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 (dp4a, int8 mma) and f16 mma on integer-valued operands; f32 scales",
+            "data": "synthetic (seeded)",
             "config": {"workload": "kquant_gemv_14336x4096_Q8_0-Q4_K-Q5_K-Q6_K_T1-2-4-8",
                        "packed_weight_bytes_per_step": step_wbytes,
                        "l2": f"inputs larger than L2: {ROTATE} rotating copies per format "
@@ -396,9 +426,13 @@ def run_gpu(args, rank, world):
                        "graph": "one step captured in a CUDA graph, replayed",
                        "fraction_of_hbm": round(value / world / hbm_peak, 4), "peak": f"{hbm_peak} GB/s ({peak_kind})"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                         "kernel": "decode GEMV kernels (k_stream dp4a at T<=2, k_group int8 mma at T>=3): "
+                         "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": round(sum_alg / len(per_launch)),
+                         "kernel": "decode GEMV kernels (k_stream dp4a at T=1, k_gemv_mma tensor path at T=2-8): "
                                    "all 16 launches of a step; algorithmic bytes = packed W + Q8_K x + fp32 y",
+                         "traffic_source": "mean dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch of "
+                                           "one step (ncu; profiles/traffic_kquant_gemv_step.json), null when the "
+                                           "kernel sources changed since",
                          "timing": "CUDA events around each GEMV inside a captured graph, median of 5 replays",
                          "peak_kind": peak_kind, "per_launch": breakdown},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -518,7 +552,20 @@ def profile_case(args):
 
     _build.build()
     ctx = ggq.Context(0)
-    if args.profile_case == "gemv":
+    if args.profile_case == "headline":
+        # one step of the headline workload (one copy per format): 4 quantizations,
+        # 16 GEMVs; run twice, the second pass is the one to capture
+        Ws = {f: torch.from_numpy(syn.weights(f, N, K, syn.rng(KQ["index"], 10 + fi))).cuda()
+              for fi, f in enumerate(FMTS)}
+        gx = syn.rng(KQ["index"], 200)
+        xs = {T: torch.from_numpy(syn.activations(T, K, gx)).cuda() for T in TOKENS}
+        ctx.reserve(max_tokens=8, max_k=K)
+        for _ in range(2):
+            xq = {T: ctx.quantize_act("Q8_K", xs[T]) for T in TOKENS}
+            for f in FMTS:
+                for T in TOKENS:
+                    ctx.mul_mat_vec_q(f, Ws[f], N, K, xq[T], T)
+    elif args.profile_case == "gemv":
         fmt = args.fmt
         Ws = [torch.from_numpy(syn.weights(fmt, N, K, syn.rng(1, i))).cuda() for i in range(5)]
         xq = {T: ctx.quantize_act("Q8_K", torch.from_numpy(syn.activations(T, K, syn.rng(1, 50 + T))).cuda())
@@ -545,6 +592,53 @@ def profile_case(args):
     print("profile case done")
 
 
+def summarize_ncu(path):
+    """Per-launch DRAM traffic of the last 16 GEMV launches in an ncu CSV log."""
+    import csv
+    rows = []
+    with open(path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        rows.append(r)
+    launches = {}
+    for r in rows:
+        name = r["Kernel Name"]
+        if not ("k_stream" in name or "k_gemv_mma" in name):
+            continue
+        key = int(r["ID"])
+        d = launches.setdefault(key, {"kernel": name.split("(")[0]})
+        val = float(r["Metric Value"].replace(",", ""))
+        unit = r["Metric Unit"]
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1e-3, "nsecond": 1e-3, "us": 1,
+                 "usecond": 1, "ms": 1e3, "msecond": 1e3}
+        if r["Metric Name"].startswith("dram__bytes"):
+            d[r["Metric Name"]] = val * scale.get(unit, 1)
+        elif r["Metric Name"] == "gpu__time_duration.sum":
+            d["us"] = val * scale.get(unit, 1)
+    last = [launches[k] for k in sorted(launches)][-len(FMTS) * len(TOKENS):]
+    plan = [(f, T) for f in FMTS for T in TOKENS]
+    out = []
+    for (f, T), d in zip(plan, last):
+        alg = N * syn.row_bytes(f, K) + T * syn.row_bytes("Q8_K", K) + T * N * 4
+        tr = d.get("dram__bytes_read.sum", 0.0) + d.get("dram__bytes_write.sum", 0.0)
+        out.append({"launch": f"{f}_T{T}", "kernel": d["kernel"], "us_cold": round(d.get("us", 0.0), 2),
+                    "dram_bytes": round(tr), "algorithmic_bytes": alg, "ratio": round(tr / alg, 4)})
+    summary = {
+        "csrc_hash": csrc_hash(),
+        "command": "python bench.py --profile-case headline && ncu --metrics gpu__time_duration.sum,"
+                   "dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:'k_stream|k_gemv_mma' "
+                   "--csv --log-file gpurun_out/traffic.csv python bench.py --profile-case headline && "
+                   "python bench.py --summarize-ncu gpurun_out/traffic.csv",
+        "mean_traffic_bytes": round(sum(o["dram_bytes"] for o in out) / len(out)),
+        "mean_algorithmic_bytes": round(sum(o["algorithmic_bytes"] for o in out) / len(out)),
+        "launches": out,
+    }
+    os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(summary, f, indent=1)
+    print(json.dumps({k: summary[k] for k in ("mean_traffic_bytes", "mean_algorithmic_bytes", "csrc_hash")}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,11 +647,18 @@ def main():
     ap.add_argument("--impl", default="ggq", choices=["ggq", "reference"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["gemv", "moe", "mxfp4", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["headline", "gemv", "moe", "mxfp4", "prefill"], default=None,
                     help="run a small launch sequence for an ncu capture instead of the benchmark")
     ap.add_argument("--fmt", default="Q4_K")
+    ap.add_argument("--summarize-ncu", metavar="CSV", default=None,
+                    help="write the per-launch DRAM traffic of a --profile-case headline ncu capture "
+                         "(metrics gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum) "
+                         "to profiles/traffic_kquant_gemv_step.json")
     ap.add_argument("--tokens", type=int, default=1)
     args = ap.parse_args()
+    if args.summarize_ncu:
+        summarize_ncu(args.summarize_ncu)
+        return
     if args.profile_case:
         profile_case(args)
         return
