@@ -106,8 +106,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // Expert-sorted route (5 tokens and up): pitched activation rows for the
 // grouped kernel's 16-byte row copies.
 struct SortedScratch {
-    size_t xq, ids, w, counts, offsets, cursor, ngroups, gexp, goff, gcnt, perm, h, hq, o, total;
+    size_t xq, ids, w, counts, offsets, cursor, ngroups, gexp, goff, gcnt, perm, h, hq, o;
+    size_t x16, xbs, xdx, h16, hbs, hdx;  // f16 operands of the grouped f16 GEMM
+    size_t total;
 };
+
+// floats per row of the f32 block scales beside the f16 operands
+int64_t dx_pitch(int64_t K) { return (K / 256 + 3) / 4 * 4; }
 
 SortedScratch sorted_scratch(int64_t T, int64_t E, int64_t H, int64_t I, int64_t k) {
     SortedScratch m{};
@@ -133,6 +138,12 @@ SortedScratch sorted_scratch(int64_t T, int64_t E, int64_t H, int64_t I, int64_t
     take(m.h, P * static_cast<size_t>(I) * 4);
     take(m.hq, P * hp);
     take(m.o, P * static_cast<size_t>(H) * 4);
+    take(m.x16, static_cast<size_t>(T) * static_cast<size_t>(H) * 2);
+    take(m.xbs, static_cast<size_t>(T) * static_cast<size_t>(H / 16) * 2);
+    take(m.xdx, static_cast<size_t>(T) * static_cast<size_t>(dx_pitch(H)) * 4);
+    take(m.h16, P * static_cast<size_t>(I) * 2);
+    take(m.hbs, P * static_cast<size_t>(I / 16) * 2);
+    take(m.hdx, P * static_cast<size_t>(dx_pitch(I)) * 4);
     m.total = off;
     return m;
 }
@@ -407,9 +418,43 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     g.h = h;
     g.g_dump = dump ? dump->g : nullptr;
     g.u_dump = dump ? dump->u : nullptr;
+    // The grouped f16 GEMM (Q8_0, Q4_K) takes the activations as exact f16 rows.
+    GmmParams m{};
+    m.ngroups = g.ngroups;
+    m.group_expert = g.group_expert;
+    m.group_off = g.group_off;
+    m.group_cnt = g.group_cnt;
+    m.perm = g.perm;
+    m.top_k = top_k;
+    m.err = g.err;
+    __half* const x16 = reinterpret_cast<__half*>(base + ms.x16);
+    __half* const xbs = reinterpret_cast<__half*>(base + ms.xbs);
+    float* const xdx = reinterpret_cast<float*>(base + ms.xdx);
+    __half* const h16 = reinterpret_cast<__half*>(base + ms.h16);
+    __half* const hbs = reinterpret_cast<__half*>(base + ms.hbs);
+    float* const hdx = reinterpret_cast<float*>(base + ms.hdx);
     int smem = 0;
-    if (!plan_group(g, 2, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
-    e = launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
+    if (gmm_supported(fg)) {
+        e = launch_q8k_to_f16(xq, xp, T, H, x16, H, xbs, H / 16, xdx, dx_pitch(H), st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
+        GmmParams q = m;
+        q.W = g.W;
+        q.W2 = g.W2;
+        q.rowbytes = g.rowbytes;
+        q.N = I;
+        q.K = static_cast<int>(H);
+        q.x16 = x16;
+        q.bs16 = xbs;
+        q.dx = xdx;
+        q.dx_pitch = dx_pitch(H);
+        q.h = h;
+        q.g_dump = g.g_dump;
+        q.u_dump = g.u_dump;
+        e = launch_gmm(G_GATEUP, fg, q, c->nsm, gmm_smem_bytes(), st);
+    } else {
+        if (!plan_group(g, 2, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
+        e = launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
+    }
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
     // h^ = Q8_K(h)
     e = launch_quantize_pitched(h, P, I, hq, hp, st);
@@ -426,8 +471,24 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     d.h = nullptr;
     d.g_dump = d.u_dump = nullptr;
     d.o = o;
-    if (!plan_group(d, 1, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
-    e = launch_group(G_DOWN, fd, d, c->nsm, smem, st);
+    if (gmm_supported(fd)) {
+        e = launch_q8k_to_f16(hq, hp, P, I, h16, I, hbs, I / 16, hdx, dx_pitch(I), st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
+        GmmParams q = m;
+        q.W = d.W;
+        q.rowbytes = d.rowbytes;
+        q.N = H;
+        q.K = static_cast<int>(I);
+        q.x16 = h16;
+        q.bs16 = hbs;
+        q.dx = hdx;
+        q.dx_pitch = dx_pitch(I);
+        q.o = o;
+        e = launch_gmm(G_DOWN, fd, q, c->nsm, gmm_smem_bytes(), st);
+    } else {
+        if (!plan_group(d, 1, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
+        e = launch_group(G_DOWN, fd, d, c->nsm, smem, st);
+    }
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: down launch");
     e = launch_combine(o, wts, static_cast<int>(T), top_k, H, Y, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: combine launch");

@@ -1,5 +1,6 @@
 // ggq_internal.h -- host/device shared declarations inside libggq (not part of the ABI).
 #pragma once
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -108,6 +109,39 @@ struct MmavParams {
     int nch;            // chunks (<= 16)
 };
 
+// Expert-sorted grouped GEMM on f16 tensor cores (ggq_gmm.cuh): tiles of 64
+// weight rows (gate/up: 32 gate + the same 32 up rows) x 128 activation
+// columns of one expert; weights decoded once per tile into f16 shared memory,
+// activations pre-converted to exact f16 rows.
+constexpr int kGmmBM = 64;
+constexpr int kGmmBN = 128;
+constexpr int kGmmBK = 64;
+constexpr int kGmmThreads = 256;
+constexpr int kGmmStages = 4;
+
+struct GmmParams {
+    const uint8_t* W;     // gate bank or down bank [E][N][rowbytes]
+    const uint8_t* W2;    // up bank (gate/up)
+    int64_t rowbytes;
+    int64_t N;            // rows per matrix (I for gate/up, H for down)
+    int K;                // input width (multiple of 256)
+    const int* ngroups;
+    const int* group_expert;
+    const int* group_off;
+    const int* group_cnt;
+    const int* perm;
+    int top_k;
+    const __half* x16;    // [rows][K] exact f16 quants of the activation rows
+    const __half* bs16;   // [rows][K/16] f16 group sums
+    const float* dx;      // [rows][dx_pitch] Q8_K block scales
+    int64_t dx_pitch;     // floats per row (multiple of 4)
+    float* h;             // gate/up: h [pairs][N]
+    float* g_dump;
+    float* u_dump;
+    float* o;             // down: o [pairs][N]
+    int* err;
+};
+
 // Launch with the programmatic-dependent-launch attribute (the kernels call
 // pdl_wait before touching data of earlier kernels, so this is always safe).
 template <typename... KArgs, typename... Args>
@@ -141,6 +175,11 @@ cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* curso
                               int* group_off, int* group_cnt, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
                            cudaStream_t s);
+cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, int64_t rows, int64_t K, __half* x16, int64_t x16_pitch,
+                              __half* bs16, int64_t bs_pitch, float* dx, int64_t dx_pitch, cudaStream_t s);
+cudaError_t launch_gmm(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s);
+int gmm_supported(int fmt);
+int gmm_smem_bytes();
 cudaError_t launch_combine(const float* o, const float* w, int T, int k, int64_t H, float* Y, cudaStream_t s);
 
 }  // namespace ggq
