@@ -138,9 +138,9 @@ SortedScratch sorted_scratch(int64_t T, int64_t E, int64_t H, int64_t I, int64_t
     take(m.h, P * static_cast<size_t>(I) * 4);
     take(m.hq, P * hp);
     take(m.o, P * static_cast<size_t>(H) * 4);
-    take(m.x16, static_cast<size_t>(T) * static_cast<size_t>(H) * 2);
-    take(m.xbs, static_cast<size_t>(T) * static_cast<size_t>(H / 16) * 2);
-    take(m.xdx, static_cast<size_t>(T) * static_cast<size_t>(dx_pitch(H)) * 4);
+    take(m.x16, P * static_cast<size_t>(H) * 2);  // one row per (token, expert) pair, expert-sorted
+    take(m.xbs, P * static_cast<size_t>(H / 16) * 2);
+    take(m.xdx, P * static_cast<size_t>(dx_pitch(H)) * 4);
     take(m.h16, P * static_cast<size_t>(I) * 2);
     take(m.hbs, P * static_cast<size_t>(I / 16) * 2);
     take(m.hdx, P * static_cast<size_t>(dx_pitch(I)) * 4);
@@ -425,7 +425,6 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     m.group_off = g.group_off;
     m.group_cnt = g.group_cnt;
     m.perm = g.perm;
-    m.top_k = top_k;
     m.err = g.err;
     __half* const x16 = reinterpret_cast<__half*>(base + ms.x16);
     __half* const xbs = reinterpret_cast<__half*>(base + ms.xbs);
@@ -435,18 +434,14 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     float* const hdx = reinterpret_cast<float*>(base + ms.hdx);
     int smem = 0;
     if (gmm_supported(fg)) {
-        e = launch_q8k_to_f16(xq, xp, T, H, x16, H, xbs, H / 16, xdx, dx_pitch(H), st);
+        e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
         GmmParams q = m;
-        q.W = g.W;
-        q.W2 = g.W2;
-        q.rowbytes = g.rowbytes;
+        const int r = gmm_encode(q, G_GATEUP, fg, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), xbs, P,
+                                 static_cast<int>(H));
+        if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: gate/up tensor maps (CUresult %d)", r);
         q.N = I;
         q.K = static_cast<int>(H);
-        q.x16 = x16;
-        q.bs16 = xbs;
-        q.dx = xdx;
-        q.dx_pitch = dx_pitch(H);
         q.h = h;
         q.g_dump = g.g_dump;
         q.u_dump = g.u_dump;
@@ -472,17 +467,14 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     d.g_dump = d.u_dump = nullptr;
     d.o = o;
     if (gmm_supported(fd)) {
-        e = launch_q8k_to_f16(hq, hp, P, I, h16, I, hbs, I / 16, hdx, dx_pitch(I), st);
+        e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
         GmmParams q = m;
-        q.W = d.W;
-        q.rowbytes = d.rowbytes;
+        const int r = gmm_encode(q, G_DOWN, fd, d.W, nullptr, d.rowbytes, E * H, h16, hdx, dx_pitch(I), hbs, P,
+                                 static_cast<int>(I));
+        if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: down tensor maps (CUresult %d)", r);
         q.N = H;
         q.K = static_cast<int>(I);
-        q.x16 = h16;
-        q.bs16 = hbs;
-        q.dx = hdx;
-        q.dx_pitch = dx_pitch(I);
         q.o = o;
         e = launch_gmm(G_DOWN, fd, q, c->nsm, gmm_smem_bytes(), st);
     } else {

@@ -1,5 +1,6 @@
 // ggq_internal.h -- host/device shared declarations inside libggq (not part of the ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -112,33 +113,30 @@ struct MmavParams {
 // Expert-sorted grouped GEMM on f16 tensor cores (ggq_gmm.cuh): tiles of 64
 // weight rows (gate/up: 32 gate + the same 32 up rows) x 128 activation
 // columns of one expert; weights decoded once per tile into f16 shared memory,
-// activations pre-converted to exact f16 rows.
+// activations pre-converted to exact f16 rows in expert-sorted order, every
+// operand fetched as 2-D TMA boxes.
 constexpr int kGmmBM = 64;
 constexpr int kGmmBN = 128;
 constexpr int kGmmBK = 64;
-constexpr int kGmmThreads = 256;
-constexpr int kGmmStages = 4;
+constexpr int kGmmThreads = 384;  // 8 consumer + 4 producer warps
+constexpr int kGmmStages = 6;
 
 struct GmmParams {
-    const uint8_t* W;     // gate bank or down bank [E][N][rowbytes]
-    const uint8_t* W2;    // up bank (gate/up)
-    int64_t rowbytes;
-    int64_t N;            // rows per matrix (I for gate/up, H for down)
-    int K;                // input width (multiple of 256)
+    CUtensorMap tm_b;         // f16 activation rows, sorted positions [P][K]: box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_dx;        // f32 block scales [P][dx_pitch]: box 4 x 128
+    CUtensorMap tm_bs;        // f16 16-group sums [P][K/16]: box 16 x 128
+    CUtensorMap tm_w[2][2];   // weight bytes [E*N][rowbytes] of [gate or down, up][Q8_0 span or Q4_K header, Q4_K nibbles]
+    int64_t N;                // rows per matrix (I for gate/up, H for down)
+    int K;                    // input width (multiple of 256)
     const int* ngroups;
     const int* group_expert;
     const int* group_off;
     const int* group_cnt;
-    const int* perm;
-    int top_k;
-    const __half* x16;    // [rows][K] exact f16 quants of the activation rows
-    const __half* bs16;   // [rows][K/16] f16 group sums
-    const float* dx;      // [rows][dx_pitch] Q8_K block scales
-    int64_t dx_pitch;     // floats per row (multiple of 4)
-    float* h;             // gate/up: h [pairs][N]
+    const int* perm;          // sorted position -> pair
+    float* h;                 // gate/up: h [pairs][N]
     float* g_dump;
     float* u_dump;
-    float* o;             // down: o [pairs][N]
+    float* o;                 // down: o [pairs][N]
     int* err;
 };
 
@@ -175,8 +173,11 @@ cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* curso
                               int* group_off, int* group_cnt, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
                            cudaStream_t s);
-cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, int64_t rows, int64_t K, __half* x16, int64_t x16_pitch,
-                              __half* bs16, int64_t bs_pitch, float* dx, int64_t dx_pitch, cudaStream_t s);
+cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, int div, int64_t rows, int64_t K,
+                              __half* x16, __half* bs16, float* dx, int64_t dx_pitch, cudaStream_t s);
+// Tensor maps of one grouped GEMM launch (host encode; 0 or a CUresult).
+int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
+               const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K);
 cudaError_t launch_gmm(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s);
 int gmm_supported(int fmt);
 int gmm_smem_bytes();

@@ -154,9 +154,11 @@ cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uin
 
 // Q8_K rows (pitched) -> the operands of the f16 grouped GEMM: the quants as
 // f16 (exact), the 16-element group sums as f16 (|sum| <= 2032: exact) and the
-// block scales as f32, each in rows of 16-byte multiples.  One warp per block.
-__global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, int64_t rows, int nbr,
-                             __half* __restrict__ x16, int64_t x16_pitch, __half* __restrict__ bs16, int64_t bs_pitch,
+// block scales as f32.  Output row r takes input row map[r] / div (the
+// expert-sorted order of the (token, expert) pairs), or row r without a map.
+// One warp per block.
+__global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, const int* __restrict__ map, int div,
+                             int64_t rows, int nbr, __half* __restrict__ x16, __half* __restrict__ bs16,
                              float* __restrict__ dx, int64_t dx_pitch) {
     pdl_launch_dependents();
     pdl_wait();
@@ -164,7 +166,8 @@ __global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, int64
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (b >= rows * nbr) return;
     const int64_t r = b / nbr, c = b - r * nbr;
-    const uint8_t* blk = q + r * pitch + c * 292;
+    const int64_t src = map ? static_cast<int64_t>(__ldg(map + r) / div) : r;
+    const uint8_t* blk = q + src * pitch + c * 292;
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(blk + 4);
     uint32_t out[4];
 #pragma unroll
@@ -177,20 +180,21 @@ __global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, int64
         out[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
         out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
     }
-    *reinterpret_cast<uint4*>(x16 + r * x16_pitch + c * 256 + 8 * lane) = make_uint4(out[0], out[1], out[2], out[3]);
+    const int64_t K = static_cast<int64_t>(nbr) * 256;
+    *reinterpret_cast<uint4*>(x16 + r * K + c * 256 + 8 * lane) = make_uint4(out[0], out[1], out[2], out[3]);
     if (lane < 16) {
         const int v = static_cast<int>(reinterpret_cast<const int16_t*>(blk + 260)[lane]);
-        bs16[r * bs_pitch + c * 16 + lane] = __int2half_rn(v);
+        bs16[r * (K / 16) + c * 16 + lane] = __int2half_rn(v);
     }
     if (lane == 0) dx[r * dx_pitch + c] = __ldcg(reinterpret_cast<const float*>(blk));
 }
 
-cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, int64_t rows, int64_t K, __half* x16, int64_t x16_pitch,
-                              __half* bs16, int64_t bs_pitch, float* dx, int64_t dx_pitch, cudaStream_t s) {
+cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, int div, int64_t rows, int64_t K,
+                              __half* x16, __half* bs16, float* dx, int64_t dx_pitch, cudaStream_t s) {
     const int64_t nb = rows * (K / 256);
     if (nb == 0) return cudaSuccess;
-    return launch_pdl(k_q8k_to_f16, dim3(static_cast<unsigned>((nb * 32 + 255) / 256)), dim3(256), 0, s, q, pitch, rows,
-                      static_cast<int>(K / 256), x16, x16_pitch, bs16, bs_pitch, dx, dx_pitch);
+    return launch_pdl(k_q8k_to_f16, dim3(static_cast<unsigned>((nb * 32 + 255) / 256)), dim3(256), 0, s, q, pitch, map,
+                      div, rows, static_cast<int>(K / 256), x16, bs16, dx, dx_pitch);
 }
 
 // One warp per token: top-k by logit (ties to the lower index) and the
