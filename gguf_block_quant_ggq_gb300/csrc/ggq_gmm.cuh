@@ -17,23 +17,26 @@
 // 16-group sums.
 //
 // Tiling: a work item is (expert, 64 weight rows, 128 columns); gate/up items
-// take 32 gate rows and the same 32 up rows, interleaved by 16 so that every
-// warp holds a gate value and its up value in the same fragment slot and forms
-// SwiGLU in registers.  The activation operand is laid out in expert-sorted
+// take 32 gate rows and the same 32 up rows (one weight box each), and the
+// decode interleaves them by 16 in the f16 tile so that every warp holds a gate
+// value and its up value in the same fragment slot and forms SwiGLU in
+// registers.  The activation operand is laid out in expert-sorted
 // order (one f16 row per (token, expert) pair, gathered when it is converted),
 // so an item's columns are consecutive rows and every operand of a 64-wide
 // k-step is a 2-D TMA box:
 //   * activations: 128 rows x 128 bytes, 128-byte swizzle (conflict-free
 //     ldmatrix);
-//   * weights: the k-step's raw bytes of 16 or 64 rows (Q8_0: the 80-byte
+//   * weights: the k-step's raw bytes of 32 or 64 rows (Q8_0: the 80-byte
 //     16-aligned span holding its two blocks; Q4_K: the 16-byte header and
 //     the 32 nibble bytes), zero-filled past the row end;
 //   * at a superblock's end: the activation scales and 16-group sums.
 // Warp roles:
-//   * one elected producer thread issues the TMA boxes of a k-step into a
-//     6-stage ring (completion counted on one mbarrier per stage), four k-steps
-//     ahead of the decode, across item boundaries;
-//   * 4 producer warps decode the weight bytes of a k-step once into an f16
+//   * one thread of the last producer warp issues the TMA boxes of each k-step
+//     into a 6-stage ring (completion counted on one mbarrier per stage, slot
+//     release on another, arrived by the consumer warps), as far ahead as the
+//     ring allows, across item boundaries: a box instruction holds its thread
+//     for several hundred cycles, so this thread does nothing else;
+//   * 3 producer warps decode the weight bytes of a k-step once into an f16
 //     tile (double-buffered) that the consumer warps share;
 //   * 8 consumer warps (2 x 4, 32 x 32 each) read fragments with ldmatrix and
 //     run the mma, applying the block scales in registers.
@@ -52,8 +55,8 @@ constexpr int kGmmRaw = 80;         // Q8_0 raw bytes per row per stage
 constexpr int kGmmMaxGroups = 4096;
 constexpr int kGmmConsumers = 256;  // threads
 constexpr int kGmmProducers = 128;
-constexpr int kGmmAhead = kGmmStages - 2;  // k-steps in flight beyond the one being decoded
-constexpr int kGmmIssuers = 4;             // producer warps whose lane 0 issues TMA boxes
+constexpr int kGmmDecoders = 96;           // producer threads that decode (the last producer warp issues TMA)
+constexpr int kGmmSync = kGmmConsumers + kGmmDecoders;  // threads on the tile full / free barriers
 // named barrier ids (0 is __syncthreads)
 constexpr int kBarAFull = 2, kBarAEmpty = 4;
 static_assert(kGmmConsumers + kGmmProducers == kGmmThreads, "warp roles");
@@ -69,10 +72,28 @@ struct GmmSmem {
     static constexpr int oA16 = kGmmStages * kStage;
     static constexpr int oPrefix = oA16 + 2 * kA16;
     static constexpr int oBars = (oPrefix + kPrefix + 7) / 8 * 8;
-    static constexpr int kTotal = oBars + kGmmStages * 8 + 1024;  // + alignment slack of the dynamic base
+    static constexpr int kTotal = oBars + 2 * kGmmStages * 8 + 1024;  // + alignment slack of the dynamic base
 };
 static_assert(GmmSmem::kStage % 1024 == 0, "swizzled activation tiles stay 1024-aligned");
 static_assert(GmmSmem::kTotal <= kSmemLimit, "grouped GEMM shared memory");
+
+// Bounded wait that suspends between probes (try_wait) instead of spinning: for
+// the TMA thread, which runs ahead and should leave issue slots to the others.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > (1ll << 32)) return false;
+    }
+}
 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void named_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
@@ -125,12 +146,24 @@ __device__ __forceinline__ __half2 byte_pair(uint32_t w, int idx) {
     return __hsub2(u2h(prmt(w, 0u, sel) | 0x64006400u), h2c(0x6400u));
 }
 
+// Raw weight rows hold gate rows 0..31 then up rows 0..31 of a gate/up item; the
+// f16 tile row of raw row r swaps bits 4 and 5 of r (gate 16, up 16, gate 16,
+// up 16).  The map is its own inverse.
+template <int KIND>
+__device__ __forceinline__ int tile_row(int r) {
+    if constexpr (KIND == G_GATEUP) return (r & ~48) | ((r & 16) << 1) | ((r & 32) >> 1);
+    else return r;
+}
+
 // One work item: expert e, m tile mt, columns [n0, n0 + ncols) of group gi.
 struct GmmItem {
     int gi, mt, n0, ncols;
+    int y0;     // first sorted activation row of the item
+    int wrow;   // first weight row of the item in its bank (e * N + mt * rows per matrix)
     int64_t e;
 };
 
+template <int KIND>
 __device__ __forceinline__ GmmItem gmm_item(const GmmParams& p, const int* s_pref, int ngroups, int item) {
     int lo = 0, hi = ngroups - 1;  // last group with s_pref[g] <= item
     while (lo < hi) {
@@ -146,6 +179,8 @@ __device__ __forceinline__ GmmItem gmm_item(const GmmParams& p, const int* s_pre
     r.n0 = (local - r.mt * ntl) * kGmmBN;
     r.ncols = min(cnt - r.n0, kGmmBN);
     r.e = p.group_expert[lo];
+    r.y0 = p.group_off[lo] + r.n0;
+    r.wrow = static_cast<int>(r.e * p.N) + r.mt * (KIND == G_GATEUP ? kGmmBM / 2 : kGmmBM);
     return r;
 }
 
@@ -160,12 +195,16 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
     uint8_t* const a16 = smem + GmmSmem::oA16;
     int* const s_pref = reinterpret_cast<int*>(smem + GmmSmem::oPrefix);
     uint64_t* const full = reinterpret_cast<uint64_t*>(smem + GmmSmem::oBars);
+    uint64_t* const empty = full + kGmmStages;
     const auto B16 = [&](int s) { return smem + s * GmmSmem::kStage; };
     const auto RAW = [&](int s) { return smem + s * GmmSmem::kStage + GmmSmem::kB16; };
     const auto DXS = [&](int s) { return smem + s * GmmSmem::kStage + GmmSmem::kB16 + GmmSmem::kRaw; };
     const auto BSS = [&](int s) { return smem + s * GmmSmem::kStage + GmmSmem::kB16 + GmmSmem::kRaw + GmmSmem::kDX; };
     if (tid == 0) {
-        for (int s = 0; s < kGmmStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < kGmmStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kGmmConsumers / 32);
+        }
         fence_barrier_init();
     }
     pdl_wait();  // groups, permutation and activations come from the previous kernels
@@ -198,117 +237,133 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                              ? (nitems - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                              : 0;
     const int total = my_items * nk;  // k-steps of this CTA
-    constexpr uint32_t M = 0x64006400u;
     constexpr uint32_t kRawBytes = F == F_Q8_0 ? kGmmBM * kGmmRaw : kGmmBM * 48;
 
     if (tid >= kGmmConsumers) {
         // ================================================================ producers
         const int pt = tid - kGmmConsumers;
-        GmmItem cur{};
-        // TMA boxes of k-step c into its ring slot (nothing past the end).  Box j of the list
-        // (0 activations, 1..kRawBoxes weights, then scales and group sums at a superblock's
-        // end) is issued by lane 0 of producer warp j % kGmmIssuers: a TMA instruction keeps its
-        // thread for a while, so the boxes of a k-step leave from several threads.
-        constexpr int kRawBoxes = (KIND == G_GATEUP ? 4 : 1) * (F == F_Q8_0 ? 1 : 2);
-        const auto issue = [&](int c) {
-            const int role = pt >> 5;
-            if ((pt & 31) != 0 || role >= kGmmIssuers || c >= total) return;
-            const int it = c / nk, kt = c - it * nk, s = c % kGmmStages;
-            if (kt == 0) cur = gmm_item(p, s_pref, ngroups, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
-            const bool sb_end = (kt & 3) == 3;
-            if (role == 0) {
+        if (pt >= kGmmDecoders) {
+            // ---------------------------------------------------------- TMA issue
+            if (pt != kGmmDecoders) return;
+            for (const CUtensorMap* m : {&p.tm_b, &p.tm_dx, &p.tm_bs, &p.tm_w[0][0], &p.tm_w[0][1], &p.tm_w[1][0], &p.tm_w[1][1]})
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+            GmmItem cur{};
+            for (int c = 0; c < total; ++c) {
+                const int it = c / nk, kt = c - it * nk, s = c % kGmmStages;
+                if (kt == 0) cur = gmm_item<KIND>(p, s_pref, ngroups, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
+                // the slot's previous k-step (c - kGmmStages) is done: decoded and consumed
+                if (c >= kGmmStages && !mbar_wait_sleep(&empty[s], ((c / kGmmStages) - 1) & 1)) {
+                    set_error(p.err, DEV_ERR_TIMEOUT);
+                    return;
+                }
+                const bool sb_end = (kt & 3) == 3;
                 uint32_t bytes = GmmSmem::kB16 + kRawBytes;
                 if (sb_end) bytes += GmmSmem::kDX + (F == F_Q4_K ? GmmSmem::kBS : 0);
                 mbar_arrive_expect_tx(&full[s], bytes);
-            }
-            const int y0 = p.group_off[cur.gi] + cur.n0;  // first sorted activation row of the item
-            const saddr raw = smem_addr(RAW(s));
+                tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kGmmBK, cur.y0, &full[s]);
+                const saddr raw = smem_addr(RAW(s));
 #pragma unroll
-            for (int j = 0; j < kRawBoxes + 3; ++j) {
-                if (j % kGmmIssuers != role) continue;
-                if (j == 0) {
-                    tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kGmmBK, y0, &full[s]);
-                } else if (j <= kRawBoxes) {
-                    // gate/up: boxes of 16 rows alternate gate, up, gate, up
-                    constexpr int parts = F == F_Q8_0 ? 1 : 2, nbox = kRawBoxes / parts, rows = kGmmBM / nbox;
-                    const int k = (j - 1) / parts, part = (j - 1) % parts;
-                    const int m = KIND == G_GATEUP ? (k & 1) : 0;
-                    const int row = static_cast<int>(cur.e * p.N) + cur.mt * mrows + (KIND == G_GATEUP ? (k >> 1) * 16 : 0);
+                for (int k = 0; k < (KIND == G_GATEUP ? 2 : 1); ++k) {
+                    // gate/up: a box of 32 gate rows, then a box of the same 32 up rows
+                    constexpr int rows = KIND == G_GATEUP ? kGmmBM / 2 : kGmmBM;
                     if constexpr (F == F_Q8_0) {
-                        tma_2d(raw + static_cast<uint32_t>(k * rows * kGmmRaw), &p.tm_w[m][0], (68 * kt) & ~15, row, &full[s]);
-                    } else if (part == 0) {
-                        tma_2d(raw + static_cast<uint32_t>(k * rows * 16), &p.tm_w[m][0], (kt >> 2) * 144, row, &full[s]);
+                        tma_2d(raw + static_cast<uint32_t>(k * rows * kGmmRaw), &p.tm_w[k][0], (68 * kt) & ~15, cur.wrow, &full[s]);
                     } else {
-                        tma_2d(raw + static_cast<uint32_t>(kGmmBM * 16 + k * rows * 32), &p.tm_w[m][1],
-                               (kt >> 2) * 144 + 16 + 32 * (kt & 3), row, &full[s]);
+                        tma_2d(raw + static_cast<uint32_t>(k * rows * 16), &p.tm_w[k][0], (kt >> 2) * 144, cur.wrow, &full[s]);
+                        tma_2d(raw + static_cast<uint32_t>(kGmmBM * 16 + k * rows * 32), &p.tm_w[k][1],
+                               (kt >> 2) * 144 + 16 + 32 * (kt & 3), cur.wrow, &full[s]);
                     }
-                } else if (j == kRawBoxes + 1) {
-                    if (sb_end) tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, y0, &full[s]);
-                } else if (F == F_Q4_K && sb_end) {
-                    tma_2d(smem_addr(BSS(s)), &p.tm_bs, (kt >> 2) * 16, y0, &full[s]);
+                }
+                if (sb_end) {
+                    tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
+                    if constexpr (F == F_Q4_K) tma_2d(smem_addr(BSS(s)), &p.tm_bs, (kt >> 2) * 16, cur.y0, &full[s]);
                 }
             }
-        };
-        if (pt == 0) {  // descriptors into the TMA unit's cache before the first copies
-            for (const CUtensorMap* m : {&p.tm_b, &p.tm_dx, &p.tm_bs, &p.tm_w[0][0], &p.tm_w[0][1], &p.tm_w[1][0], &p.tm_w[1][1]})
-                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+            return;
         }
-        for (int c = 0; c < kGmmAhead; ++c) issue(c);
+        // -------------------------------------------------------------- decode
         bool live = true;  // false once a stage wait gave up: no further waits
         for (int d = 0; d < total; ++d) {
             // ---- decode k-step d into the f16 tile d & 1
             const int s = d % kGmmStages, b = d & 1, kt = d % nk;
-            if (d >= 2) named_sync(kBarAEmpty + b, kGmmThreads);  // consumers are done with k-step d-2 (tile b, its ring slot)
+            if (d >= 2) named_sync(kBarAEmpty + b, kGmmSync);  // consumers are done with k-step d-2 (tile b)
             if (live && !mbar_wait(&full[s], (d / kGmmStages) & 1)) {
                 set_error(p.err, DEV_ERR_TIMEOUT);
                 live = false;
             }
-            const uint8_t* raw = RAW(s);
+            const saddr raw = smem_addr(RAW(s));
             uint8_t* const at = a16 + b * GmmSmem::kA16;
+            // 256 units of 16 outputs per k-step, up to kUnits per thread; all shared-memory
+            // reads of the thread's units first, then the conversions (independent chains)
+            constexpr int kUnits = (kGmmBM * 4 + kGmmDecoders - 1) / kGmmDecoders;
+            if constexpr (F == F_Q8_0) {
+                // unit: 16 codes of one row (half of a 32-block): row u >> 2, block (u >> 1) & 1, half u & 1
+                const int o0 = (68 * kt) & 15;
+                uint32_t w[kUnits][4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int r = (pt >> 3) + 16 * h, ge = pt & 7;
-                uint32_t o4[4];
-                if constexpr (F == F_Q8_0) {
-                    const int o0 = (68 * kt) & 15;
-                    const saddr src = smem_addr(raw) + static_cast<uint32_t>(r * kGmmRaw + o0 + 34 * (ge >> 2) + 2 + 8 * (ge & 3));
-                    uint32_t w[2];
-                    ld_words_any<2>(src, w);
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = pt + kGmmDecoders * h;
+                    if (u < kGmmBM * 4)
+                        ld_words_any<4>(raw + static_cast<uint32_t>((u >> 2) * kGmmRaw + o0 + 34 * ((u >> 1) & 1) + 2 + 16 * (u & 1)), w[h]);
+                }
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const uint32_t u = w[k] ^ 0x80808080u;  // code + 128 per byte; 1152 = 1024 + 128
-                        o4[2 * k] = h2u(__hsub2(u2h(prmt(u, 0u, 0x4140u) | M), h2c(0x6480u)));
-                        o4[2 * k + 1] = h2u(__hsub2(u2h(prmt(u, 0u, 0x4342u) | M), h2c(0x6480u)));
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = pt + kGmmDecoders * h;
+                    if (u >= kGmmBM * 4) break;
+                    uint32_t o8[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // code + 128 per byte (xor), as 1024 + (code + 128) (prmt with 0x64 high bytes), minus 1152
+                        const uint32_t v = w[h][k] ^ 0x80808080u;
+                        o8[2 * k] = h2u(__hsub2(u2h(prmt(v, 0x64646464u, 0x4140u)), h2c(0x6480u)));
+                        o8[2 * k + 1] = h2u(__hsub2(u2h(prmt(v, 0x64646464u, 0x4342u)), h2c(0x6480u)));
                     }
-                } else {
-                    const uint4 hd = ld_s128(smem_addr(raw) + static_cast<uint32_t>(r * 16));
-                    uint32_t sl, sh, ml, mh;
-                    k4_words(hd.y, hd.z, hd.w, sl, sh, ml, mh);
-                    const int js = 2 * (kt & 3) + (ge >> 2);  // sub-block of this group of 8
-                    const __half2 sc = byte_pair(js < 4 ? sl : sh, js & 3);
-                    const saddr qa = smem_addr(raw) + static_cast<uint32_t>(kGmmBM * 16 + r * 32 + 8 * (ge & 3));
-                    const uint32_t qw[2] = {ld_s32(qa), ld_s32(qa + 4)};
-                    if (ge < 4) {  // low nibbles: (1024 + n) sc - 1024 sc
-                        const __half2 cc = __hmul2(sc, h2c(0xE400u));
+                    uint8_t* const dst = at + (tile_row<KIND>(u >> 2) * kGmmLd + 16 * (u & 3)) * 2;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+                    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+                }
+            } else {
+                // unit: 8 nibble bytes of one row, group u & 3: low nibbles are outputs 8 (u & 3) .. +7
+                // (sub-block 2 (kt & 3)), high nibbles outputs 32 + 8 (u & 3) .. +7 (the next sub-block)
+                uint4 hd[kUnits];
+                uint32_t qw[kUnits][2];
 #pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            o4[2 * k] = h2u(__hfma2(u2h((prmt(qw[k], 0u, 0x4140u) & 0x000F000Fu) | M), sc, cc));
-                            o4[2 * k + 1] = h2u(__hfma2(u2h((prmt(qw[k], 0u, 0x4342u) & 0x000F000Fu) | M), sc, cc));
-                        }
-                    } else {  // high nibbles masked in place: (1024 + 16 n) sc/16 - 64 sc
-                        const __half2 s16 = __hmul2(sc, h2c(0x2C00u));
-                        const __half2 cc = __hmul2(sc, h2c(0xD400u));
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            o4[2 * k] = h2u(__hfma2(u2h((prmt(qw[k], 0u, 0x4140u) & 0x00F000F0u) | M), s16, cc));
-                            o4[2 * k + 1] = h2u(__hfma2(u2h((prmt(qw[k], 0u, 0x4342u) & 0x00F000F0u) | M), s16, cc));
-                        }
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = pt + kGmmDecoders * h;
+                    if (u < kGmmBM * 4) {
+                        hd[h] = ld_s128(raw + static_cast<uint32_t>((u >> 2) * 16));
+                        const saddr qa = raw + static_cast<uint32_t>(kGmmBM * 16 + (u >> 2) * 32 + 8 * (u & 3));
+                        qw[h][0] = ld_s32(qa);
+                        qw[h][1] = ld_s32(qa + 4);
                     }
                 }
-                *reinterpret_cast<uint4*>(at + (r * kGmmLd + 8 * ge) * 2) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                const int cc = kt & 3;
+#pragma unroll
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = pt + kGmmDecoders * h;
+                    if (u >= kGmmBM * 4) break;
+                    // 6-bit scales of sub-blocks 2 cc (low nibbles) and 2 cc + 1 (high nibbles)
+                    const uint32_t sw = cc < 2 ? (hd[h].y & 0x3F3F3F3Fu)
+                                               : ((hd[h].w & 0x0F0F0F0Fu) | ((hd[h].y >> 2) & 0x30303030u));
+                    const __half2 slo = byte_pair(sw, 2 * (cc & 1)), shi = byte_pair(sw, 2 * (cc & 1) + 1);
+                    const __half2 clo = __hmul2(slo, h2c(0xE400u));                      // -1024 sc
+                    const __half2 s16 = __hmul2(shi, h2c(0x2C00u)), chi = __hmul2(shi, h2c(0xD400u));  // sc / 16, -64 sc
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint32_t x0 = prmt(qw[h][k], 0x64646464u, 0x4140u), x1 = prmt(qw[h][k], 0x64646464u, 0x4342u);
+                        // low nibble: (1024 + n) sc - 1024 sc; high nibble in place: (1024 + 16 n) sc/16 - 64 sc
+                        lo[2 * k] = h2u(__hfma2(u2h(x0 & 0xFF0FFF0Fu), slo, clo));
+                        lo[2 * k + 1] = h2u(__hfma2(u2h(x1 & 0xFF0FFF0Fu), slo, clo));
+                        hi[2 * k] = h2u(__hfma2(u2h(x0 & 0xFFF0FFF0u), s16, chi));
+                        hi[2 * k + 1] = h2u(__hfma2(u2h(x1 & 0xFFF0FFF0u), s16, chi));
+                    }
+                    uint8_t* const dst = at + (tile_row<KIND>(u >> 2) * kGmmLd + 8 * (u & 3)) * 2;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(dst + 64) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
             }
-            named_arrive(kBarAFull + b, kGmmThreads);
-            issue(d + kGmmAhead);  // into the ring slot of k-step d-2
+            named_arrive(kBarAFull + b, kGmmSync);
         }
         return;
     }
@@ -318,14 +373,14 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
     const int g = lane >> 2, t = lane & 3;
     bool live = true;
     for (int it = 0; it < my_items; ++it) {
-        const GmmItem cur = gmm_item(p, s_pref, ngroups, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
+        const GmmItem cur = gmm_item<KIND>(p, s_pref, ngroups, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
         int pc[4][2];  // output pair of each column this thread stores (-1: none)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int col = wn * 32 + 8 * j + 2 * t + cc;
-                pc[j][cc] = col < cur.ncols ? p.perm[p.group_off[cur.gi] + cur.n0 + col] : -1;
+                pc[j][cc] = col < cur.ncols ? p.perm[cur.y0 + col] : -1;
             }
         float acc[2][4][4], D[2][4][4], T[2][4][4];
 #pragma unroll
@@ -336,7 +391,7 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                 for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.0f;
         for (int kt = 0; kt < nk; ++kt) {
             const int c = it * nk + kt, s = c % kGmmStages, b = c & 1;
-            named_sync(kBarAFull + b, kGmmThreads);
+            named_sync(kBarAFull + b, kGmmSync);
             // the producers saw this stage land; observe it here too (already complete)
             if (live && !mbar_wait(&full[s], (c / kGmmStages) & 1)) {
                 set_error(p.err, DEV_ERR_TIMEOUT);
@@ -375,7 +430,7 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                         for (int i = 0; i < 2; ++i)
 #pragma unroll
                             for (int hh = 0; hh < 2; ++hh)
-                                dw[i][hh] = ld_h(raw + static_cast<uint32_t>((wm * 32 + 16 * i + g + 8 * hh) * kGmmRaw + o0 + 34 * blk));
+                                dw[i][hh] = ld_h(raw + static_cast<uint32_t>(tile_row<KIND>(wm * 32 + 16 * i + g + 8 * hh) * kGmmRaw + o0 + 34 * blk));
                         const bool first = blk == 0 && (kt & 3) == 0;
 #pragma unroll
                         for (int i = 0; i < 2; ++i)
@@ -408,7 +463,7 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                     for (int i = 0; i < 2; ++i)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const uint4 hd = ld_s128(raw + static_cast<uint32_t>((wm * 32 + 16 * i + g + 8 * hh) * 16));
+                            const uint4 hd = ld_s128(raw + static_cast<uint32_t>(tile_row<KIND>(wm * 32 + 16 * i + g + 8 * hh) * 16));
                             dd[i][hh] = half_lo(hd.x);
                             dm[i][hh] = half_hi(hd.x);
                             uint32_t sl, sh, ml, mh;
@@ -439,7 +494,9 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                             for (int q = 0; q < 4; ++q) acc[i][j][q] = fmaf(-D[i][j][q], dm[i][q >> 1] * dv[j][q & 1], acc[i][j][q]);
                 }
             }
-            if (c + 2 < total) named_arrive(kBarAEmpty + b, kGmmThreads);
+            if (c + 2 < total) named_arrive(kBarAEmpty + b, kGmmSync);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);  // the ring slot may take k-step c + kGmmStages
         }
         // ---- epilogue
         if constexpr (KIND == G_GATEUP) {

@@ -45,7 +45,7 @@ int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t*
                           static_cast<uint64_t>(dx_pitch) * 4, 4, kGmmBN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!r) r = encode_2d(&p.tm_bs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bs16, k / 16, np, k / 8, 16, kGmmBN,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
-    const uint32_t rows = kind == G_GATEUP ? 16 : kGmmBM;
+    const uint32_t rows = kind == G_GATEUP ? kGmmBM / 2 : kGmmBM;
     const int nm = kind == G_GATEUP ? 2 : 1;
     for (int m = 0; m < nm && !r; ++m) {
         const uint8_t* w = m ? W2 : W;
