@@ -46,15 +46,18 @@ METRIC = "decode GEMV/MoE packed-weight GB/s (% of HBM); prefill expert GEMM int
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_kquant_gemv_step.json")
 
 
+# sources of the decode GEMV kernels (k_stream, k_gemv_mma) that the stored traffic was taken on
+GEMV_SOURCES = ("ggq_device.cuh", "ggq_stream.cuh", "ggq_mmav.cuh", "ggq_k_gemv_a.cu", "ggq_k_gemv_b.cu", "ggq_k_mmav.cu")
+
+
 def csrc_hash():
-    """Hash of the kernel sources: a stored DRAM-traffic figure applies only to the kernels it was taken on."""
+    """Hash of the GEMV kernel sources: a stored DRAM-traffic figure applies only to the kernels it was taken on."""
     import hashlib
     d = os.path.join(ROOT, "gguf_block_quant_ggq_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in GEMV_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -75,6 +78,15 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense 16-bit tensor peak in TFLOP/s (measured cuBLAS bf16 burst; f16 runs at the same rate)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 # ----------------------------------------------------------------- CUDA runtime (events in graphs)
@@ -528,6 +540,12 @@ def secondary_workloads(ctx, rt, hbm_peak):
                          "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R,
                          "int_TOPS": round(ops / (ms / 1e3) / 1e12, 2),
                          "route": "direct" if T <= 4 else "expert-sorted"}
+            if T > 4 and cfg["gate"] in ("Q8_0", "Q4_K") and cfg["down"] in ("Q8_0", "Q4_K"):
+                # the grouped GEMM runs the integer multiply-adds on 16-bit tensor cores (f16
+                # operands holding integers): against the measured dense 16-bit peak
+                tp, tkind = tensor_peak()
+                out[name]["tensor_frac"] = round(ops / (ms / 1e3) / 1e12 / tp, 4)
+                out[name]["tensor_peak"] = f"{tp} TFLOP/s dense bf16/f16 ({tkind})"
         del banks, w8
         torch.cuda.empty_cache()
     ctx.set_static_weights(False)

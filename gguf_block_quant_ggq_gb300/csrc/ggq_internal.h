@@ -118,7 +118,7 @@ struct MmavParams {
 constexpr int kGmmBM = 64;
 constexpr int kGmmBN = 128;
 constexpr int kGmmBK = 64;
-constexpr int kGmmThreads = 384;  // 8 consumer + 4 producer warps
+constexpr int kGmmThreads = 384;  // 8 consumer warps, 3 decode warps, 1 TMA warp
 constexpr int kGmmStages = 6;
 
 struct GmmParams {
