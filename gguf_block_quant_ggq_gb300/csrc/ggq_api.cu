@@ -108,6 +108,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 struct SortedScratch {
     size_t xq, ids, w, counts, offsets, cursor, ngroups, gexp, goff, gcnt, perm, h, hq, o;
     size_t x16, xbs, xdx, h16, hbs, hdx;  // f16 operands of the grouped f16 GEMM
+    size_t u;                              // up outputs of the tcgen05 gate/up GEMM (g goes to h)
     size_t total;
 };
 
@@ -144,6 +145,7 @@ SortedScratch sorted_scratch(int64_t T, int64_t E, int64_t H, int64_t I, int64_t
     take(m.h16, P * static_cast<size_t>(I) * 2);
     take(m.hbs, P * static_cast<size_t>(I / 16) * 2);
     take(m.hdx, P * static_cast<size_t>(dx_pitch(I)) * 4);
+    take(m.u, P * static_cast<size_t>(I) * 4);
     m.total = off;
     return m;
 }
@@ -433,7 +435,33 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     __half* const hbs = reinterpret_cast<__half*>(base + ms.hbs);
     float* const hdx = reinterpret_cast<float*>(base + ms.hdx);
     int smem = 0;
-    if (gmm_supported(fg)) {
+    bool h_dumped = false;  // the SwiGLU quantizer wrote dump->h itself
+    if (fg == F_Q8_0 && I % 128 == 0) {
+        // Q8_0 gate/up on tcgen05: g and u per pair, then h = silu(g) u fused into its quantizer
+        e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
+        GmmTcParams t{};
+        const int r = gmmtc_encode(t, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), P, static_cast<int>(H));
+        if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: gate/up tensor maps (CUresult %d)", r);
+        t.N = I;
+        t.K = static_cast<int>(H);
+        t.nmat = 2;
+        t.ngroups = g.ngroups;
+        t.group_expert = g.group_expert;
+        t.group_off = g.group_off;
+        t.group_cnt = g.group_cnt;
+        t.perm = g.perm;
+        t.err = g.err;
+        float* const gbuf = dump && dump->g ? dump->g : h;
+        float* const ubuf = dump && dump->u ? dump->u : reinterpret_cast<float*>(base + ms.u);
+        t.out[0] = gbuf;
+        t.out[1] = ubuf;
+        e = launch_gmmtc(t, c->nsm, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
+        e = launch_quantize_silu(gbuf, ubuf, P, I, hq, hp, dump ? dump->h : nullptr, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: SwiGLU quantize launch");
+        h_dumped = dump != nullptr;
+    } else if (gmm_supported(fg)) {
         e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
         GmmParams q = m;
@@ -450,10 +478,12 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         if (!plan_group(g, 2, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
         e = launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
     }
-    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
-    // h^ = Q8_K(h)
-    e = launch_quantize_pitched(h, P, I, hq, hp, st);
-    if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: quantize h launch");
+    if (!(fg == F_Q8_0 && I % 128 == 0)) {
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
+        // h^ = Q8_K(h)
+        e = launch_quantize_pitched(h, P, I, hq, hp, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: quantize h launch");
+    }
     // down -> o
     GroupParams d = g;
     d.W = static_cast<const uint8_t*>(w->down);
@@ -491,7 +521,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
             e = cudaMemcpyAsync(dump->weights, wts, P * 4, cudaMemcpyDeviceToDevice, st);
         if (e == cudaSuccess && dump->xq)
             e = cudaMemcpy2DAsync(dump->xq, xb, xq, xp, xb, T, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess && dump->h)
+        if (e == cudaSuccess && dump->h && !h_dumped)
             e = cudaMemcpyAsync(dump->h, h, static_cast<size_t>(P) * I * 4, cudaMemcpyDeviceToDevice, st);
         if (e == cudaSuccess && dump->hq)
             e = cudaMemcpy2DAsync(dump->hq, hb, hq, hp, hb, P, cudaMemcpyDeviceToDevice, st);

@@ -669,11 +669,18 @@ __device__ __forceinline__ float quant_scale(float amax, float* id) {
 // One warp quantizes one 256-element block to Q8_K (292 bytes at dst, 4-byte
 // aligned).  src is read with __ldcg (L2) so data written by other CTAs of the
 // same kernel is seen after their fence.
+__device__ __forceinline__ void warp_quant_q8k_regs(const float (&x)[8], uint8_t* dst, int lane);
+
 __device__ __forceinline__ void warp_quant_q8k(const float* src, uint8_t* dst, int lane) {
     float x[8];
     const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + 2 * lane);
     const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 2 * lane + 1);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    warp_quant_q8k_regs(x, dst, lane);
+}
+
+// The same with the block's values already in registers (lane l holds elements 8 l .. 8 l + 7).
+__device__ __forceinline__ void warp_quant_q8k_regs(const float (&x)[8], uint8_t* dst, int lane) {
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));

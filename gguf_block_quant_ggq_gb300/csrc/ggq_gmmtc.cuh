@@ -1,0 +1,417 @@
+// ggq_gmmtc.cuh -- the expert-sorted grouped GEMM on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory) for Q8_0 expert banks.
+//
+// Same arithmetic as the keep-quant expert GEMM of vllm.cpp PR #523
+// "grouped + non-grouped keep-quant expert GEMM" (What changed: DotQ8_0 block
+// dots grouped over expert_ids): y = sum over 32-blocks of d_w * d_x * (integer
+// dot).  The integer dots run as tcgen05.mma kind::f16 with f16 operands that
+// hold the int8 codes exactly; each 32-block gets its own tensor-memory
+// accumulator (|dot| < 2^19: exact in f32), so the weight block scale, which
+// differs per row and block, is applied by the epilogue warps.
+//
+// Work item: (expert, matrix, 128 weight rows, 128 activation columns).  The
+// activation operand is f16 rows in expert-sorted order (one per (token,
+// expert) pair), so an item's columns are 128 consecutive rows.  Per 64-wide
+// k-step:
+//   * TMA (one elected lane of warp 14): the activation tile (128 rows x 128
+//     bytes, 128-byte swizzle = the UMMA K-major SW128 layout), the raw Q8_0
+//     bytes of the 128 weight rows (the 80-byte 16-aligned span holding the
+//     k-step's two blocks) and, at a superblock's end, the activation scales;
+//     4-stage ring, completion on one mbarrier per stage;
+//   * decode (warps 8-13): raw codes -> f16 weight tile in the same SW128
+//     K-major layout (3 buffers), then fence.proxy.async so the tensor core
+//     sees the generic-proxy stores;
+//   * MMA (one elected lane of warp 15): two K=16 MMAs per 32-block into one of
+//     two 128-column tensor-memory accumulators, tcgen05.commit to the
+//     accumulator's mbarrier; stage and tile release by commit as well;
+//   * epilogue (warps 0-7; warp w owns TMEM lanes 32 (w & 3) .. +31 = tile rows
+//     and 64 of the 128 columns): tcgen05.ld of each block accumulator,
+//     T += D * d_w (d_w: this thread's row), and at the superblock's end
+//     acc += T * d_x (d_x: per column) in a third tensor-memory region; at the
+//     item's end acc goes to the output rows (one f32 row per pair: lanes write
+//     consecutive rows, 128-byte segments).
+// Gate and up are separate items (SwiGLU is fused into the quantizer of h).
+// Every wait is bounded: a wait that gives up sets the error word and the
+// shared abort flag, and every role leaves its loop.
+#pragma once
+#include "ggq_device.cuh"
+#include "ggq_internal.h"
+
+namespace ggq {
+
+constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64;
+constexpr int kTcStages = 4;  // TMA ring
+constexpr int kTcABufs = 3;   // decoded weight tiles
+constexpr int kTcEpi = 256;   // epilogue threads (warps 0-7)
+constexpr int kTcDec = 192;   // decode threads (warps 8-13)
+constexpr int kTcTmaWarp = 14, kTcMmaWarp = 15;
+constexpr int kTcRaw = 80;  // raw bytes per weight row per k-step
+constexpr int kTcMaxGroups = 4096;
+static_assert(kTcThreads == kTcEpi + kTcDec + 64, "warp roles");
+
+struct TcSmem {
+    static constexpr int kB = kTcBN * kTcBK * 2;     // 16384, SW128 K-major
+    static constexpr int kRaw = kTcBM * kTcRaw;      // 10240
+    static constexpr int kDX = kTcBN * 16;           // 2048: 4 superblock scales per column
+    static constexpr int kStage = kB + kRaw + kDX;   // 28672 (28 KB: activation tiles stay 1024-aligned)
+    static constexpr int kA = kTcBM * kTcBK * 2;     // 16384, SW128 K-major
+    static constexpr int oA = kTcStages * kStage;
+    static constexpr int oPrefix = oA + kTcABufs * kA;
+    static constexpr int kPrefix = (kTcMaxGroups + 1) * 4;
+    static constexpr int oBars = (oPrefix + kPrefix + 7) / 8 * 8;
+    static constexpr int kBars = (2 * kTcStages + 2 * kTcABufs + 4) * 8 + 16;
+    static constexpr int kTotal = oBars + kBars + 1024;  // + alignment slack of the dynamic base
+};
+static_assert(TcSmem::kStage % 1024 == 0 && TcSmem::oA % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+static_assert(TcSmem::kTotal <= kSmemLimit, "tcgen05 grouped GEMM shared memory");
+
+// tensor-memory columns: two block accumulators, then the item accumulator
+constexpr uint32_t kTmemCols = 512, kTmemAcc = 256;
+
+// UMMA shared-memory descriptor of a K-major tile with 128-byte swizzle: rows of
+// 128 bytes, 8-row groups 1024 bytes apart (descriptor version 1).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+// instruction descriptor: f32 accumulate, f16 A and B, both K-major, M = 128, N = 128
+constexpr uint32_t kTcIdesc = (1u << 4) | ((static_cast<uint32_t>(kTcBN) >> 3) << 17) | ((static_cast<uint32_t>(kTcBM) >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive tensor-memory columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_tma_2d(saddr dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// One work item: matrix m of expert e, m tile mt (128 rows), columns [n0, n0 + ncols) of group gi.
+struct TcItem {
+    int m, mt, ncols, y0;  // y0: first sorted activation row
+    int wrow;              // first weight row in the bank (e * N + mt * 128)
+};
+
+__device__ __forceinline__ TcItem tc_item(const GmmTcParams& p, const int* s_pref, int ngroups, int mtiles, int item) {
+    int lo = 0, hi = ngroups - 1;  // last group with s_pref[g] <= item
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_pref[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    const int cnt = p.group_cnt[lo];
+    const int ntl = (cnt + kTcBN - 1) / kTcBN;
+    const int local = item - s_pref[lo];
+    const int mta = local / ntl, nt = local - mta * ntl;  // mta over nmat * mtiles
+    TcItem r;
+    r.m = mta / mtiles;
+    r.mt = mta - r.m * mtiles;
+    const int n0 = nt * kTcBN;
+    r.ncols = min(cnt - n0, kTcBN);
+    r.y0 = p.group_off[lo] + n0;
+    r.wrow = static_cast<int>(static_cast<int64_t>(p.group_expert[lo]) * p.N) + r.mt * kTcBM;
+    return r;
+}
+
+// Bounded wait by a whole warp (every lane polls); the result is the same in
+// every lane, so loops leave together.  On failure flags the CTA (abort) and
+// the error word.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+    bool ok = !*abort && mbar_wait(bar, parity);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (!ok) {
+        *abort = 1;
+        set_error(err, DEV_ERR_TIMEOUT);
+    }
+    return ok;
+}
+
+template <int F>
+__global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__ GmmTcParams p) {
+    static_assert(F == F_Q8_0, "tcgen05 grouped GEMM: Q8_0 banks");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* const smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();
+
+    int* const s_pref = reinterpret_cast<int*>(smem + TcSmem::oPrefix);
+    uint64_t* const full = reinterpret_cast<uint64_t*>(smem + TcSmem::oBars);
+    uint64_t* const empty = full + kTcStages;
+    uint64_t* const afull = empty + kTcStages;
+    uint64_t* const aempty = afull + kTcABufs;
+    uint64_t* const tfull = aempty + kTcABufs;
+    uint64_t* const tempty = tfull + 2;
+    uint32_t* const tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+    volatile int* const abort = reinterpret_cast<volatile int*>(tslot + 1);
+    const auto B16 = [&](int s) { return smem + s * TcSmem::kStage; };
+    const auto RAW = [&](int s) { return smem + s * TcSmem::kStage + TcSmem::kB; };
+    const auto DXS = [&](int s) { return smem + s * TcSmem::kStage + TcSmem::kB + TcSmem::kRaw; };
+    const auto ATILE = [&](int a) { return smem + TcSmem::oA + a * TcSmem::kA; };
+
+    if (tid == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + kTcDec + kTcEpi);  // MMA commit, decode threads, epilogue threads
+        }
+        for (int a = 0; a < kTcABufs; ++a) {
+            mbar_init(&afull[a], kTcDec);
+            mbar_init(&aempty[a], 1);
+        }
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(&tfull[d], 1);
+            mbar_init(&tempty[d], kTcEpi);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tslot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    pdl_wait();  // groups, permutation and activations come from the previous kernels
+
+    // ---- item table: per group, nmat * mtiles * ceil(cols / 128) items
+    const int ngroups = *p.ngroups;
+    const int mtiles = static_cast<int>(p.N / kTcBM);
+    if (warp == 0) {
+        const int per = (ngroups + 31) >> 5, b0 = lane * per, b1 = min(b0 + per, ngroups);
+        int own = 0;
+        for (int gi = b0; gi < b1; ++gi) own += p.nmat * mtiles * ((p.group_cnt[gi] + kTcBN - 1) / kTcBN);
+        int incl = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int acc = incl - own;
+        for (int gi = b0; gi < b1; ++gi) {
+            s_pref[gi] = acc;
+            acc += p.nmat * mtiles * ((p.group_cnt[gi] + kTcBN - 1) / kTcBN);
+        }
+        if (lane == 31) s_pref[ngroups] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int nitems = s_pref[ngroups];
+    const int nk = p.K / kTcBK;
+    const int my_items = static_cast<int>(blockIdx.x) < nitems
+                             ? (nitems - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+    const int total = my_items * nk;
+    const auto item_of = [&](int it) {
+        return tc_item(p, s_pref, ngroups, mtiles, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
+    };
+
+    if (warp == kTcTmaWarp) {
+        // ================================================================ TMA
+        TcItem cur{};
+        for (int c = 0; c < total; ++c) {
+            const int it = c / nk, kt = c - it * nk, s = c % kTcStages;
+            if (kt == 0) cur = item_of(it);
+            if (c >= kTcStages && !tc_wait(&empty[s], ((c / kTcStages) - 1) & 1, abort, p.err)) break;
+            if (lane == 0) {
+                const bool sb_end = (kt & 3) == 3;
+                mbar_arrive_expect_tx(&full[s], TcSmem::kB + TcSmem::kRaw + (sb_end ? TcSmem::kDX : 0));
+                tc_tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
+                tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);
+                if (sb_end) tc_tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
+            }
+            __syncwarp();
+        }
+    } else if (warp == kTcMmaWarp) {
+        // ================================================================ MMA
+        for (int c = 0; c < total; ++c) {
+            const int s = c % kTcStages, a = c % kTcABufs;
+            if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
+            if (!tc_wait(&afull[a], (c / kTcABufs) & 1, abort, p.err)) break;
+            tc_fence_after();
+            const uint32_t abase = smem_addr(ATILE(a)), bbase = smem_addr(B16(s));
+            bool ok = true;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int gb = 2 * c + b, db = gb & 1;
+                if (gb >= 2 && !tc_wait(&tempty[db], ((gb >> 1) - 1) & 1, abort, p.err)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t koff = static_cast<uint32_t>((2 * b + kk) * 32);
+                        tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), umma_desc_sw128(abase + koff),
+                               umma_desc_sw128(bbase + koff), static_cast<uint32_t>(kk));
+                    }
+                    tc_commit(&tfull[db]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) {
+                tc_commit(&aempty[a]);
+                tc_commit(&empty[s]);
+            }
+            __syncwarp();
+        }
+    } else if (warp >= kTcEpi / 32) {
+        // ================================================================ decode
+        const int dt = tid - kTcEpi;
+        constexpr int kUnits = (kTcBM * 4 + kTcDec - 1) / kTcDec;  // 16-code units of the 128 x 64 tile
+        for (int c = 0; c < total; ++c) {
+            const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
+            if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
+            if (c >= kTcABufs && !tc_wait(&aempty[a], ((c / kTcABufs) - 1) & 1, abort, p.err)) break;
+            const saddr raw = smem_addr(RAW(s));
+            uint8_t* const at = ATILE(a);
+            const int o0 = (68 * kt) & 15;
+            uint32_t w[kUnits][4];
+#pragma unroll
+            for (int h = 0; h < kUnits; ++h) {
+                const int u = dt + kTcDec * h;  // row u >> 2, block (u >> 1) & 1, half u & 1
+                if (u < kTcBM * 4)
+                    ld_words_any<4>(raw + static_cast<uint32_t>((u >> 2) * kTcRaw + o0 + 34 * ((u >> 1) & 1) + 2 + 16 * (u & 1)), w[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < kUnits; ++h) {
+                const int u = dt + kTcDec * h;
+                if (u >= kTcBM * 4) break;
+                uint32_t o8[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    // code + 128 per byte (xor), as 1024 + (code + 128) (prmt with 0x64 high bytes), minus 1152
+                    const uint32_t v = w[h][k] ^ 0x80808080u;
+                    const __half2 o = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
+                    const uint32_t x0 = prmt(v, 0x64646464u, 0x4140u), x1 = prmt(v, 0x64646464u, 0x4342u);
+                    const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&x0), o);
+                    const __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&x1), o);
+                    o8[2 * k] = *reinterpret_cast<const uint32_t*>(&h0);
+                    o8[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+                }
+                // 16 outputs = 16-byte chunks 2 (u & 3) and 2 (u & 3) + 1 of row u >> 2, XOR-swizzled by row
+                const int r = u >> 2, c0 = 2 * (u & 3);
+                *reinterpret_cast<uint4*>(at + r * 128 + ((c0 ^ (r & 7)) << 4)) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+                *reinterpret_cast<uint4*>(at + r * 128 + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> tensor-core reads
+            mbar_arrive(&afull[a]);
+            mbar_arrive(&empty[s]);
+        }
+    } else {
+        // ================================================================ epilogue
+        const int q = warp & 3, col0 = 64 * (warp >> 2), r = 32 * q + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        float T[64];
+        bool live = true;
+        for (int it = 0; it < my_items && live; ++it) {
+            const TcItem cur = item_of(it);
+            for (int kt = 0; kt < nk && live; ++kt) {
+                const int c = it * nk + kt, s = c % kTcStages;
+                const saddr raw = smem_addr(RAW(s));
+                const int o0 = (68 * kt) & 15;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const int gb = 2 * c + b, db = gb & 1;
+                    if (!tc_wait(&tfull[db], (gb >> 1) & 1, abort, p.err)) { live = false; break; }
+                    tc_fence_after();
+                    const float dw = ld_h(raw + static_cast<uint32_t>(r * kTcRaw + o0 + 34 * b));
+                    const bool first = b == 0 && (kt & 3) == 0;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        float v[32];
+                        tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) T[32 * h2 + j] = first ? v[j] * dw : fmaf(v[j], dw, T[32 * h2 + j]);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&tempty[db]);
+                }
+                if (!live) break;
+                if ((kt & 3) == 3) {  // superblock end: acc += T * d_x (per column)
+                    const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        float a[32];
+                        const uint32_t ta = lane_base + kTmemAcc + static_cast<uint32_t>(col0 + 32 * h2);
+                        if (kt == 3) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) a[j] = 0.0f;
+                        } else {
+                            tmem_ld32(ta, a);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) a[j] = fmaf(T[32 * h2 + j], ld_f32(dxs + 16u * (col0 + 32 * h2 + j)), a[j]);
+                        tmem_st32(ta, a);
+                    }
+                }
+                mbar_arrive(&empty[s]);
+            }
+            if (!live) break;
+            // item end: this thread's row of the item's columns
+            float* const out = p.out[cur.m];
+            const int64_t row = static_cast<int64_t>(cur.mt) * kTcBM + r;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float a[32];
+                tmem_ld32(lane_base + kTmemAcc + static_cast<uint32_t>(col0 + 32 * h2), a);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = col0 + 32 * h2 + j;
+                    if (col < cur.ncols) out[static_cast<int64_t>(p.perm[cur.y0 + col]) * p.N + row] = a[j];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+}  // namespace ggq

@@ -179,6 +179,36 @@ cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, i
 int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
                const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K);
 cudaError_t launch_gmm(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s);
+// Row-major 2-D tensor map [dim1][dim0] (rows stride1 bytes apart); 0 or a CUresult.
+int encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1,
+                   uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz);
+
+// Expert-sorted grouped GEMM on tcgen05 (ggq_gmmtc.cuh), Q8_0 banks: items of 128
+// weight rows x 128 activation columns; every matrix of the bank (gate and up
+// are separate items) writes its own f32 output rows per pair.
+constexpr int kTcThreads = 512;  // 8 epilogue, 6 decode, 1 TMA, 1 MMA warps
+
+struct GmmTcParams {
+    CUtensorMap tm_b;     // f16 activation rows, sorted positions [P][K]: box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_dx;    // f32 block scales [P][dx_pitch]: box 4 x 128
+    CUtensorMap tm_w[2];  // Q8_0 bytes [E*N][rowbytes] of gate (or down) and up: box 80 x 128
+    int64_t N;            // rows per matrix (multiple of 128)
+    int K;                // input width (multiple of 256)
+    int nmat;             // matrices per bank (2: gate and up)
+    const int* ngroups;
+    const int* group_expert;
+    const int* group_off;
+    const int* group_cnt;
+    const int* perm;      // sorted position -> pair
+    float* out[2];        // per matrix: [pairs][N]
+    int* err;
+};
+int gmmtc_encode(GmmTcParams& p, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
+                 const __half* x16, const float* dx, int64_t dx_pitch, int64_t P, int K);
+cudaError_t launch_gmmtc(const GmmTcParams& p, int grid, cudaStream_t s);
+// h = silu(g) * u row by row (optionally written to h_out), quantized to Q8_K rows at out + r * pitch.
+cudaError_t launch_quantize_silu(const float* g, const float* u, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
+                                 float* h_out, cudaStream_t s);
 int gmm_supported(int fmt);
 int gmm_smem_bytes();
 cudaError_t launch_combine(const float* o, const float* w, int T, int k, int64_t H, float* Y, cudaStream_t s);

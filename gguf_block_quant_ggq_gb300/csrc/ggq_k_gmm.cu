@@ -21,8 +21,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+}  // namespace
+
 // Row-major 2-D tensor [dim1][dim0] of one element type, rows stride1 bytes apart.
-int encode_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1, uint64_t stride1,
+int encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1, uint64_t stride1,
               uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
     const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
@@ -34,16 +36,14 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64
                                swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
-}  // namespace
-
 int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
                const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K) {
     const uint64_t k = static_cast<uint64_t>(K), np = static_cast<uint64_t>(P);
-    int r = encode_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, k, np, k * 2, kGmmBK, kGmmBN,
+    int r = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, k, np, k * 2, kGmmBK, kGmmBN,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!r) r = encode_2d(&p.tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, static_cast<uint64_t>(dx_pitch), np,
+    if (!r) r = encode_tmap_2d(&p.tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, static_cast<uint64_t>(dx_pitch), np,
                           static_cast<uint64_t>(dx_pitch) * 4, 4, kGmmBN, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!r) r = encode_2d(&p.tm_bs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bs16, k / 16, np, k / 8, 16, kGmmBN,
+    if (!r) r = encode_tmap_2d(&p.tm_bs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bs16, k / 16, np, k / 8, 16, kGmmBN,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     const uint32_t rows = kind == G_GATEUP ? kGmmBM / 2 : kGmmBM;
     const int nm = kind == G_GATEUP ? 2 : 1;
@@ -51,10 +51,10 @@ int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t*
         const uint8_t* w = m ? W2 : W;
         const uint64_t rb = static_cast<uint64_t>(rowbytes), nr = static_cast<uint64_t>(wrows);
         if (fmt == F_Q8_0) {
-            r = encode_2d(&p.tm_w[m][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, kGmmRaw, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+            r = encode_tmap_2d(&p.tm_w[m][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, kGmmRaw, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
         } else {
-            r = encode_2d(&p.tm_w[m][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, 16, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
-            if (!r) r = encode_2d(&p.tm_w[m][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, 32, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+            r = encode_tmap_2d(&p.tm_w[m][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, 16, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (!r) r = encode_tmap_2d(&p.tm_w[m][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, 32, rows, CU_TENSOR_MAP_SWIZZLE_NONE);
         }
     }
     return r;

@@ -1,0 +1,35 @@
+// ggq_k_gmmtc.cu -- tensor maps and launch of the tcgen05 grouped GEMM (Q8_0 banks).
+#include "ggq_gmmtc.cuh"
+
+namespace ggq {
+
+int gmmtc_encode(GmmTcParams& p, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
+                 const __half* x16, const float* dx, int64_t dx_pitch, int64_t P, int K) {
+    const uint64_t k = static_cast<uint64_t>(K), np = static_cast<uint64_t>(P);
+    int r = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, k, np, k * 2, kTcBK, kTcBN,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r) r = encode_tmap_2d(&p.tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, static_cast<uint64_t>(dx_pitch), np,
+                               static_cast<uint64_t>(dx_pitch) * 4, 4, kTcBN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const uint64_t rb = static_cast<uint64_t>(rowbytes), nr = static_cast<uint64_t>(wrows);
+    for (int m = 0; m < 2 && !r; ++m) {
+        const uint8_t* w = m ? (W2 ? W2 : W) : W;
+        r = encode_tmap_2d(&p.tm_w[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rb, nr, rb, kTcRaw, kTcBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    return r;
+}
+
+cudaError_t launch_gmmtc(const GmmTcParams& p, int grid, cudaStream_t s) {
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(k_gmmtc<F_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return launch_pdl(k_gmmtc<F_Q8_0>, dim3(grid), dim3(kTcThreads), TcSmem::kTotal, s, p);
+}
+
+}  // namespace ggq

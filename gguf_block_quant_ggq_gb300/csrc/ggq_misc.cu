@@ -152,6 +152,40 @@ cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uin
                       static_cast<int>(K / 256), out, pitch);
 }
 
+// h = silu(g) * u (the SwiGLU of the gate/up outputs, same rounding steps as the
+// grouped kernels' epilogues), then Q8_K: one warp per 256-block of a row.
+__global__ void k_quant_silu_q8k(const float* __restrict__ g, const float* __restrict__ u, int64_t rows, int nbr,
+                                 uint8_t* __restrict__ out, int64_t pitch, float* __restrict__ h_out) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= rows * nbr) return;
+    const int64_t r = b / nbr, c = b - r * nbr;
+    const float4* gp = reinterpret_cast<const float4*>(g + b * 256) + 2 * lane;
+    const float4* up = reinterpret_cast<const float4*>(u + b * 256) + 2 * lane;
+    const float4 g0 = __ldcg(gp), g1 = __ldcg(gp + 1), u0 = __ldcg(up), u1 = __ldcg(up + 1);
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(__fdiv_rn(gv[i], 1.0f + expf(-gv[i])), uv[i]);
+    if (h_out) {
+        float4* hp = reinterpret_cast<float4*>(h_out + b * 256) + 2 * lane;
+        hp[0] = make_float4(x[0], x[1], x[2], x[3]);
+        hp[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    warp_quant_q8k_regs(x, out + r * pitch + c * 292, lane);
+}
+
+cudaError_t launch_quantize_silu(const float* g, const float* u, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
+                                 float* h_out, cudaStream_t s) {
+    const int64_t nb = rows * (K / 256);
+    if (nb == 0) return cudaSuccess;
+    return launch_pdl(k_quant_silu_q8k, dim3(static_cast<unsigned>((nb * 32 + 255) / 256)), dim3(256), 0, s, g, u,
+                      rows, static_cast<int>(K / 256), out, pitch, h_out);
+}
+
 // Q8_K rows (pitched) -> the operands of the f16 grouped GEMM: the quants as
 // f16 (exact), the 16-element group sums as f16 (|sum| <= 2032: exact) and the
 // block scales as f32.  Output row r takes input row map[r] / div (the

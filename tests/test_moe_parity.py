@@ -174,6 +174,15 @@ def test_moe_q8_0_gate_q4k_down_decode(ctx):
         _run_and_check(ctx, cfg, 16, T)
 
 
+@pytest.mark.parametrize("T", [5, 40])
+def test_moe_q8_0_gate_q4k_down_sorted(ctx, T):
+    """Expert-sorted route with the prefill formats over a 16-expert bank: Q8_0
+    gate/up on the tcgen05 grouped GEMM, Q4_K down on the f16 grouped GEMM."""
+    cfg = dict(syn.MOE_PREFILL)
+    cfg["E"] = 16
+    _run_and_check(ctx, cfg, 16, T, sample_tokens=None if T <= 8 else 6)
+
+
 @pytest.mark.parametrize("T", [5, 8, 32, 128])
 def test_moe_sorted_route_mxfp4(ctx, T):
     """5 tokens and up: expert-sorted tiles on the grouped int8 tensor-core kernel."""
