@@ -23,7 +23,10 @@
 //     sees the generic-proxy stores;
 //   * MMA (one elected lane of warp 15): two K=16 MMAs per 32-block into one of
 //     two 128-column tensor-memory accumulators, tcgen05.commit to the
-//     accumulator's mbarrier; stage and tile release by commit as well;
+//     accumulator's mbarrier (the thread's only commits: a tcgen05 instruction
+//     costs its issuing thread ~90 cycles); the epilogue, having seen a k-step's
+//     last accumulator land (every earlier MMA has then completed), releases the
+//     k-step's weight tile and ring slot;
 //   * epilogue (warps 0-7; warp w owns TMEM lanes 32 (w & 3) .. +31 = tile rows
 //     and 64 of the 128 columns): tcgen05.ld of each block accumulator,
 //     T += D * d_w (d_w: this thread's row), and at the superblock's end
@@ -195,11 +198,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + kTcDec + kTcEpi);  // MMA commit, decode threads, epilogue threads
+            mbar_init(&empty[s], kTcDec + kTcEpi);  // decode threads, epilogue threads
         }
         for (int a = 0; a < kTcABufs; ++a) {
             mbar_init(&afull[a], kTcDec);
-            mbar_init(&aempty[a], 1);
+            mbar_init(&aempty[a], kTcEpi);
         }
         for (int d = 0; d < 2; ++d) {
             mbar_init(&tfull[d], 1);
@@ -273,7 +276,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
             if (!tc_wait(&afull[a], (c / kTcABufs) & 1, abort, p.err)) break;
             tc_fence_after();
-            const uint32_t abase = smem_addr(ATILE(a)), bbase = smem_addr(B16(s));
+            // descriptors are linear in the start address (16-byte units): K steps add 2 per 32 bytes
+            const uint64_t adesc = umma_desc_sw128(smem_addr(ATILE(a))), bdesc = umma_desc_sw128(smem_addr(B16(s)));
             bool ok = true;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
@@ -283,20 +287,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t koff = static_cast<uint32_t>((2 * b + kk) * 32);
-                        tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), umma_desc_sw128(abase + koff),
-                               umma_desc_sw128(bbase + koff), static_cast<uint32_t>(kk));
+                        const uint64_t koff = static_cast<uint64_t>((2 * b + kk) * 2);
+                        tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + koff, bdesc + koff, static_cast<uint32_t>(kk));
                     }
                     tc_commit(&tfull[db]);
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) {
-                tc_commit(&aempty[a]);
-                tc_commit(&empty[s]);
-            }
-            __syncwarp();
         }
     } else if (warp >= kTcEpi / 32) {
         // ================================================================ decode
@@ -369,6 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     }
                     tc_fence_before();
                     mbar_arrive(&tempty[db]);
+                    if (b == 1) mbar_arrive(&aempty[c % kTcABufs]);  // every MMA of the k-step has completed
                 }
                 if (!live) break;
                 if ((kt & 3) == 3) {  // superblock end: acc += T * d_x (per column)
