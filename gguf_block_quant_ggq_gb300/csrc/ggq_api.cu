@@ -441,7 +441,8 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
         GmmTcParams t{};
-        const int r = gmmtc_encode(t, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), P, static_cast<int>(H));
+        const int r = gmmtc_encode(t, F_Q8_0, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), nullptr, P,
+                                   static_cast<int>(H));
         if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: gate/up tensor maps (CUresult %d)", r);
         t.N = I;
         t.K = static_cast<int>(H);
@@ -456,7 +457,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         float* const ubuf = dump && dump->u ? dump->u : reinterpret_cast<float*>(base + ms.u);
         t.out[0] = gbuf;
         t.out[1] = ubuf;
-        e = launch_gmmtc(t, c->nsm, st);
+        e = launch_gmmtc(F_Q8_0, t, c->nsm, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
         e = launch_quantize_silu(gbuf, ubuf, P, I, hq, hp, dump ? dump->h : nullptr, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: SwiGLU quantize launch");
@@ -496,7 +497,26 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     d.h = nullptr;
     d.g_dump = d.u_dump = nullptr;
     d.o = o;
-    if (gmm_supported(fd)) {
+    if (fd == F_Q4_K && H % 128 == 0) {
+        // Q4_K down on tcgen05
+        e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
+        GmmTcParams t{};
+        const int r = gmmtc_encode(t, F_Q4_K, d.W, nullptr, d.rowbytes, E * H, h16, hdx, dx_pitch(I), hbs, P,
+                                   static_cast<int>(I));
+        if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: down tensor maps (CUresult %d)", r);
+        t.N = H;
+        t.K = static_cast<int>(I);
+        t.nmat = 1;
+        t.ngroups = g.ngroups;
+        t.group_expert = g.group_expert;
+        t.group_off = g.group_off;
+        t.group_cnt = g.group_cnt;
+        t.perm = g.perm;
+        t.err = g.err;
+        t.out[0] = t.out[1] = o;
+        e = launch_gmmtc(F_Q4_K, t, c->nsm, st);
+    } else if (gmm_supported(fd)) {
         e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
         GmmParams q = m;

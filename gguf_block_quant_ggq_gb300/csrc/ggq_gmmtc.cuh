@@ -1,13 +1,19 @@
 // ggq_gmmtc.cuh -- the expert-sorted grouped GEMM on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory) for Q8_0 expert banks.
+// cores (tcgen05, accumulators in tensor memory) for Q8_0 and Q4_K expert banks.
 //
 // Same arithmetic as the keep-quant expert GEMM of vllm.cpp PR #523
-// "grouped + non-grouped keep-quant expert GEMM" (What changed: DotQ8_0 block
-// dots grouped over expert_ids): y = sum over 32-blocks of d_w * d_x * (integer
-// dot).  The integer dots run as tcgen05.mma kind::f16 with f16 operands that
-// hold the int8 codes exactly; each 32-block gets its own tensor-memory
-// accumulator (|dot| < 2^19: exact in f32), so the weight block scale, which
-// differs per row and block, is applied by the epilogue warps.
+// "grouped + non-grouped keep-quant expert GEMM" (What changed: DotQ8_0 /
+// DotQ4K block dots grouped over expert_ids): per weight block, (weight scale)
+// * (activation scale) * (integer dot).  The integer dots run as tcgen05.mma
+// kind::f16 with f16 operands that hold integers exactly:
+//   * Q8_0: the int8 codes; each 32-block gets its own tensor-memory accumulator
+//     (|dot| < 2^19: exact in f32), so the weight block scale, which differs per
+//     row and block, is applied by the epilogue warps;
+//   * Q4_K: the codes already multiplied by their 6-bit sub-block scale
+//     (sc * q <= 945); one accumulator per 256-superblock (sums beyond 2^24 may
+//     round, relative 2^-24), and the mins term sum_j m_j * (16-group sums of x)
+//     is one more K = 16 MMA of the mins against the activations' exact group
+//     sums; the epilogue forms (D d - Dmin dmin) d_x once per superblock.
 //
 // Work item: (expert, matrix, 128 weight rows, 128 activation columns).  The
 // activation operand is f16 rows in expert-sorted order (one per (token,
@@ -59,7 +65,8 @@ struct TcSmem {
     static constexpr int kStage = kB + kRaw + kDX;   // 28672 (28 KB: activation tiles stay 1024-aligned)
     static constexpr int kA = kTcBM * kTcBK * 2;     // 16384, SW128 K-major
     static constexpr int oA = kTcStages * kStage;
-    static constexpr int oPrefix = oA + kTcABufs * kA;
+    static constexpr int oMin = oA + kTcABufs * kA;    // Q4_K mins-term operands: two SW128 tiles
+    static constexpr int oPrefix = oMin + 2 * kA;
     static constexpr int kPrefix = (kTcMaxGroups + 1) * 4;
     static constexpr int oBars = (oPrefix + kPrefix + 7) / 8 * 8;
     static constexpr int kBars = (2 * kTcStages + 2 * kTcABufs + 4) * 8 + 16;
@@ -69,7 +76,7 @@ static_assert(TcSmem::kStage % 1024 == 0 && TcSmem::oA % 1024 == 0, "SW128 tiles
 static_assert(TcSmem::kTotal <= kSmemLimit, "tcgen05 grouped GEMM shared memory");
 
 // tensor-memory columns: two block accumulators, then the item accumulator
-constexpr uint32_t kTmemCols = 512, kTmemAcc = 256;
+constexpr uint32_t kTmemCols = 512;
 
 // UMMA shared-memory descriptor of a K-major tile with 128-byte swizzle: rows of
 // 128 bytes, 8-row groups 1024 bytes apart (descriptor version 1).
@@ -134,6 +141,13 @@ __device__ __forceinline__ void tc_tma_2d(saddr dst, const CUtensorMap* map, int
         : "memory");
 }
 
+// (v, v) as f16 for byte idx (runtime) of w (v <= 255)
+__device__ __forceinline__ __half2 tc_byte_pair(uint32_t w, int idx) {
+    const uint32_t sel = 0x4040u | static_cast<uint32_t>(idx) | (static_cast<uint32_t>(idx) << 8);
+    const uint32_t u = prmt(w, 0u, sel) | 0x64006400u;
+    return __hsub2(*reinterpret_cast<const __half2*>(&u), __halves2half2(__ushort_as_half(0x6400u), __ushort_as_half(0x6400u)));
+}
+
 // One work item: matrix m of expert e, m tile mt (128 rows), columns [n0, n0 + ncols) of group gi.
 struct TcItem {
     int m, mt, ncols, y0;  // y0: first sorted activation row
@@ -175,7 +189,11 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
 
 template <int F>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__ GmmTcParams p) {
-    static_assert(F == F_Q8_0, "tcgen05 grouped GEMM: Q8_0 banks");
+    static_assert(F == F_Q8_0 || F == F_Q4_K, "tcgen05 grouped GEMM: Q8_0 and Q4_K banks");
+    constexpr bool Q8 = F == F_Q8_0;
+    // tensor-memory columns: block (Q8_0) or superblock (Q4_K) accumulators 0..255,
+    // Q4_K mins term 256..383, item accumulator
+    constexpr uint32_t kAcc = Q8 ? 256u : 384u, kDmin = 256u;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* const smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -194,15 +212,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     const auto RAW = [&](int s) { return smem + s * TcSmem::kStage + TcSmem::kB; };
     const auto DXS = [&](int s) { return smem + s * TcSmem::kStage + TcSmem::kB + TcSmem::kRaw; };
     const auto ATILE = [&](int a) { return smem + TcSmem::oA + a * TcSmem::kA; };
+    uint8_t* const min_a = smem + TcSmem::oMin;              // Q4_K: 6-bit mins per 16-group, SW128 rows
+    uint8_t* const min_b = smem + TcSmem::oMin + TcSmem::kA;  // Q4_K: activation 16-group sums, SW128 rows
 
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kTcDec + kTcEpi);  // decode threads, epilogue threads
+            // Q8_0: decode and epilogue threads (the epilogue has seen the k-step's MMAs complete);
+            // Q4_K: the MMA's commit, decode and epilogue threads
+            mbar_init(&empty[s], kTcDec + kTcEpi + (Q8 ? 0 : 1));
         }
         for (int a = 0; a < kTcABufs; ++a) {
             mbar_init(&afull[a], kTcDec);
-            mbar_init(&aempty[a], kTcEpi);
+            mbar_init(&aempty[a], Q8 ? kTcEpi : 1);
         }
         for (int d = 0; d < 2; ++d) {
             mbar_init(&tfull[d], 1);
@@ -252,6 +274,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     const auto item_of = [&](int it) {
         return tc_item(p, s_pref, ngroups, mtiles, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
     };
+    // raw bytes per k-step: Q8_0 the 80-byte spans; Q4_K headers [128][16], nibbles [128][32],
+    // then at a superblock's end the activation 16-group sums [128][32]
+    constexpr uint32_t kRawTx = Q8 ? TcSmem::kRaw : kTcBM * 48;
+    constexpr int kQsOff = kTcBM * 16, kBsOff = kTcBM * 48;
 
     if (warp == kTcTmaWarp) {
         // ================================================================ TMA
@@ -262,78 +288,176 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (c >= kTcStages && !tc_wait(&empty[s], ((c / kTcStages) - 1) & 1, abort, p.err)) break;
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
-                mbar_arrive_expect_tx(&full[s], TcSmem::kB + TcSmem::kRaw + (sb_end ? TcSmem::kDX : 0));
+                mbar_arrive_expect_tx(&full[s], TcSmem::kB + kRawTx + (sb_end ? TcSmem::kDX + (Q8 ? 0 : kTcBN * 32) : 0));
                 tc_tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
-                tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);
-                if (sb_end) tc_tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
+                if constexpr (Q8) {
+                    tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);
+                } else {
+                    const int x = (kt >> 2) * 144;
+                    tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[0], x, cur.wrow, &full[s]);
+                    tc_tma_2d(smem_addr(RAW(s)) + kQsOff, &p.tm_w[1], x + 16 + 32 * (kt & 3), cur.wrow, &full[s]);
+                }
+                if (sb_end) {
+                    tc_tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
+                    if constexpr (!Q8) tc_tma_2d(smem_addr(RAW(s)) + kBsOff, &p.tm_bs, (kt >> 2) * 16, cur.y0, &full[s]);
+                }
             }
             __syncwarp();
         }
     } else if (warp == kTcMmaWarp) {
         // ================================================================ MMA
         for (int c = 0; c < total; ++c) {
-            const int s = c % kTcStages, a = c % kTcABufs;
+            const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
             if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
             if (!tc_wait(&afull[a], (c / kTcABufs) & 1, abort, p.err)) break;
             tc_fence_after();
             // descriptors are linear in the start address (16-byte units): K steps add 2 per 32 bytes
             const uint64_t adesc = umma_desc_sw128(smem_addr(ATILE(a))), bdesc = umma_desc_sw128(smem_addr(B16(s)));
             bool ok = true;
+            if constexpr (Q8) {
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                const int gb = 2 * c + b, db = gb & 1;
-                if (gb >= 2 && !tc_wait(&tempty[db], ((gb >> 1) - 1) & 1, abort, p.err)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
+                for (int b = 0; b < 2; ++b) {
+                    const int gb = 2 * c + b, db = gb & 1;
+                    if (gb >= 2 && !tc_wait(&tempty[db], ((gb >> 1) - 1) & 1, abort, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint64_t koff = static_cast<uint64_t>((2 * b + kk) * 2);
-                        tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + koff, bdesc + koff, static_cast<uint32_t>(kk));
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint64_t koff = static_cast<uint64_t>((2 * b + kk) * 2);
+                            tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + koff, bdesc + koff, static_cast<uint32_t>(kk));
+                        }
+                        tc_commit(&tfull[db]);
                     }
-                    tc_commit(&tfull[db]);
+                    __syncwarp();
                 }
-                __syncwarp();
+            } else {
+                // one accumulator per superblock (4 k-steps), two buffers
+                const int sbi = c >> 2, db = sbi & 1;  // nk is a multiple of 4, so c and kt agree on (c & 3)
+                if ((kt & 3) == 0 && sbi >= 2 && !tc_wait(&tempty[db], ((sbi >> 1) - 1) & 1, abort, p.err)) ok = false;
+                if (ok && (kt & 3) == 3 && sbi >= 1 && !tc_wait(&tempty[db ^ 1], ((sbi - 1) >> 1) & 1, abort, p.err))
+                    ok = false;  // the mins region is single: superblock sbi - 1 must have been read
+                if (ok) {
+                    tc_fence_after();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + static_cast<uint64_t>(2 * kk),
+                                   bdesc + static_cast<uint64_t>(2 * kk), static_cast<uint32_t>((kt & 3) != 0 || kk != 0));
+                        if ((kt & 3) == 3) {
+                            tc_mma(tmem + kDmin, umma_desc_sw128(smem_addr(min_a)), umma_desc_sw128(smem_addr(min_b)), 0u);
+                            tc_commit(&tfull[db]);
+                        }
+                        tc_commit(&aempty[a]);
+                        tc_commit(&empty[s]);
+                    }
+                    __syncwarp();
+                }
             }
             if (!ok) break;
         }
     } else if (warp >= kTcEpi / 32) {
         // ================================================================ decode
         const int dt = tid - kTcEpi;
-        constexpr int kUnits = (kTcBM * 4 + kTcDec - 1) / kTcDec;  // 16-code units of the 128 x 64 tile
+        constexpr int kUnits = (kTcBM * 4 + kTcDec - 1) / kTcDec;  // 16-output units of the 128 x 64 tile
         for (int c = 0; c < total; ++c) {
             const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
             if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
             if (c >= kTcABufs && !tc_wait(&aempty[a], ((c / kTcABufs) - 1) & 1, abort, p.err)) break;
             const saddr raw = smem_addr(RAW(s));
             uint8_t* const at = ATILE(a);
-            const int o0 = (68 * kt) & 15;
-            uint32_t w[kUnits][4];
+            if constexpr (Q8) {
+                const int o0 = (68 * kt) & 15;
+                uint32_t w[kUnits][4];
 #pragma unroll
-            for (int h = 0; h < kUnits; ++h) {
-                const int u = dt + kTcDec * h;  // row u >> 2, block (u >> 1) & 1, half u & 1
-                if (u < kTcBM * 4)
-                    ld_words_any<4>(raw + static_cast<uint32_t>((u >> 2) * kTcRaw + o0 + 34 * ((u >> 1) & 1) + 2 + 16 * (u & 1)), w[h]);
-            }
-#pragma unroll
-            for (int h = 0; h < kUnits; ++h) {
-                const int u = dt + kTcDec * h;
-                if (u >= kTcBM * 4) break;
-                uint32_t o8[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // code + 128 per byte (xor), as 1024 + (code + 128) (prmt with 0x64 high bytes), minus 1152
-                    const uint32_t v = w[h][k] ^ 0x80808080u;
-                    const __half2 o = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
-                    const uint32_t x0 = prmt(v, 0x64646464u, 0x4140u), x1 = prmt(v, 0x64646464u, 0x4342u);
-                    const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&x0), o);
-                    const __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&x1), o);
-                    o8[2 * k] = *reinterpret_cast<const uint32_t*>(&h0);
-                    o8[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = dt + kTcDec * h;  // row u >> 2, block (u >> 1) & 1, half u & 1
+                    if (u < kTcBM * 4)
+                        ld_words_any<4>(raw + static_cast<uint32_t>((u >> 2) * kTcRaw + o0 + 34 * ((u >> 1) & 1) + 2 + 16 * (u & 1)), w[h]);
                 }
-                // 16 outputs = 16-byte chunks 2 (u & 3) and 2 (u & 3) + 1 of row u >> 2, XOR-swizzled by row
-                const int r = u >> 2, c0 = 2 * (u & 3);
-                *reinterpret_cast<uint4*>(at + r * 128 + ((c0 ^ (r & 7)) << 4)) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-                *reinterpret_cast<uint4*>(at + r * 128 + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+#pragma unroll
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = dt + kTcDec * h;
+                    if (u >= kTcBM * 4) break;
+                    uint32_t o8[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // code + 128 per byte (xor), as 1024 + (code + 128) (prmt with 0x64 high bytes), minus 1152
+                        const uint32_t v = w[h][k] ^ 0x80808080u;
+                        const __half2 o = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
+                        const uint32_t x0 = prmt(v, 0x64646464u, 0x4140u), x1 = prmt(v, 0x64646464u, 0x4342u);
+                        const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&x0), o);
+                        const __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&x1), o);
+                        o8[2 * k] = *reinterpret_cast<const uint32_t*>(&h0);
+                        o8[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+                    }
+                    // 16 outputs = 16-byte chunks 2 (u & 3) and 2 (u & 3) + 1 of row u >> 2, XOR-swizzled by row
+                    const int r = u >> 2, c0 = 2 * (u & 3);
+                    *reinterpret_cast<uint4*>(at + r * 128 + ((c0 ^ (r & 7)) << 4)) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+                    *reinterpret_cast<uint4*>(at + r * 128 + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+                }
+            } else {
+                // unit: 8 nibble bytes of row u >> 2, group u & 3: low nibbles are outputs 8 (u & 3) .. +7
+                // (sub-block 2 (kt & 3)), high nibbles outputs 32 + 8 (u & 3) .. +7 (the next sub-block),
+                // each already multiplied by its 6-bit scale (sc * q <= 945: exact)
+                uint4 hd[kUnits];
+                uint32_t qw[kUnits][2];
+#pragma unroll
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = dt + kTcDec * h;
+                    if (u < kTcBM * 4) {
+                        hd[h] = ld_s128(raw + static_cast<uint32_t>((u >> 2) * 16));
+                        const saddr qa = raw + static_cast<uint32_t>(kQsOff + (u >> 2) * 32 + 8 * (u & 3));
+                        qw[h][0] = ld_s32(qa);
+                        qw[h][1] = ld_s32(qa + 4);
+                    }
+                }
+                const int cc = kt & 3;
+#pragma unroll
+                for (int h = 0; h < kUnits; ++h) {
+                    const int u = dt + kTcDec * h;
+                    if (u >= kTcBM * 4) break;
+                    const uint32_t sw = cc < 2 ? (hd[h].y & 0x3F3F3F3Fu) : ((hd[h].w & 0x0F0F0F0Fu) | ((hd[h].y >> 2) & 0x30303030u));
+                    const __half2 slo = tc_byte_pair(sw, 2 * (cc & 1)), shi = tc_byte_pair(sw, 2 * (cc & 1) + 1);
+                    const __half2 clo = __hmul2(slo, __halves2half2(__ushort_as_half(0xE400u), __ushort_as_half(0xE400u)));
+                    const __half2 s16 = __hmul2(shi, __halves2half2(__ushort_as_half(0x2C00u), __ushort_as_half(0x2C00u)));
+                    const __half2 chi = __hmul2(shi, __halves2half2(__ushort_as_half(0xD400u), __ushort_as_half(0xD400u)));
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint32_t x0 = prmt(qw[h][k], 0x64646464u, 0x4140u), x1 = prmt(qw[h][k], 0x64646464u, 0x4342u);
+                        // low nibble: (1024 + n) sc - 1024 sc; high nibble in place: (1024 + 16 n) sc/16 - 64 sc
+                        const uint32_t l0 = x0 & 0xFF0FFF0Fu, l1 = x1 & 0xFF0FFF0Fu, h0 = x0 & 0xFFF0FFF0u, h1 = x1 & 0xFFF0FFF0u;
+                        const __half2 a0 = __hfma2(*reinterpret_cast<const __half2*>(&l0), slo, clo);
+                        const __half2 a1 = __hfma2(*reinterpret_cast<const __half2*>(&l1), slo, clo);
+                        const __half2 b0 = __hfma2(*reinterpret_cast<const __half2*>(&h0), s16, chi);
+                        const __half2 b1 = __hfma2(*reinterpret_cast<const __half2*>(&h1), s16, chi);
+                        lo[2 * k] = *reinterpret_cast<const uint32_t*>(&a0);
+                        lo[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&a1);
+                        hi[2 * k] = *reinterpret_cast<const uint32_t*>(&b0);
+                        hi[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+                    }
+                    const int r = u >> 2, g = u & 3;
+                    *reinterpret_cast<uint4*>(at + r * 128 + ((g ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(at + r * 128 + (((4 + g) ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                if (cc == 3) {
+                    // the mins term operands: A row r = the 16-group mins (m_j twice, j = 0..7), B row c =
+                    // the 16-group activation sums; only the first 32 bytes (K = 16) of each SW128 row
+                    for (int i = dt; i < 2 * kTcBM; i += kTcDec) {
+                        const int r = i >> 1, ch = i & 1;
+                        const uint4 h4 = ld_s128(raw + static_cast<uint32_t>(r * 16));
+                        const uint32_t mw = ch == 0 ? (h4.z & 0x3F3F3F3Fu) : (((h4.w >> 4) & 0x0F0F0F0Fu) | ((h4.z >> 2) & 0x30303030u));
+                        uint32_t m4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __half2 mk = tc_byte_pair(mw, k);
+                            m4[k] = *reinterpret_cast<const uint32_t*>(&mk);
+                        }
+                        *reinterpret_cast<uint4*>(min_a + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(m4[0], m4[1], m4[2], m4[3]);
+                        const uint4 b4 = ld_s128(raw + static_cast<uint32_t>(kBsOff + r * 32 + 16 * ch));
+                        *reinterpret_cast<uint4*>(min_b + r * 128 + ((ch ^ (r & 7)) << 4)) = b4;
+                    }
+                }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> tensor-core reads
             mbar_arrive(&afull[a]);
@@ -343,39 +467,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         // ================================================================ epilogue
         const int q = warp & 3, col0 = 64 * (warp >> 2), r = 32 * q + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        float T[64];
+        float T[Q8 ? 64 : 1];
         bool live = true;
         for (int it = 0; it < my_items && live; ++it) {
             const TcItem cur = item_of(it);
             for (int kt = 0; kt < nk && live; ++kt) {
                 const int c = it * nk + kt, s = c % kTcStages;
                 const saddr raw = smem_addr(RAW(s));
-                const int o0 = (68 * kt) & 15;
+                if constexpr (Q8) {
+                    const int o0 = (68 * kt) & 15;
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int gb = 2 * c + b, db = gb & 1;
-                    if (!tc_wait(&tfull[db], (gb >> 1) & 1, abort, p.err)) { live = false; break; }
-                    tc_fence_after();
-                    const float dw = ld_h(raw + static_cast<uint32_t>(r * kTcRaw + o0 + 34 * b));
-                    const bool first = b == 0 && (kt & 3) == 0;
+                    for (int b = 0; b < 2; ++b) {
+                        const int gb = 2 * c + b, db = gb & 1;
+                        if (!tc_wait(&tfull[db], (gb >> 1) & 1, abort, p.err)) { live = false; break; }
+                        tc_fence_after();
+                        const float dw = ld_h(raw + static_cast<uint32_t>(r * kTcRaw + o0 + 34 * b));
+                        const bool first = b == 0 && (kt & 3) == 0;
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        float v[32];
-                        tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            float v[32];
+                            tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) T[32 * h2 + j] = first ? v[j] * dw : fmaf(v[j], dw, T[32 * h2 + j]);
+                            for (int j = 0; j < 32; ++j) T[32 * h2 + j] = first ? v[j] * dw : fmaf(v[j], dw, T[32 * h2 + j]);
+                        }
+                        tc_fence_before();
+                        mbar_arrive(&tempty[db]);
+                        if (b == 1) mbar_arrive(&aempty[c % kTcABufs]);  // every MMA of the k-step has completed
                     }
-                    tc_fence_before();
-                    mbar_arrive(&tempty[db]);
-                    if (b == 1) mbar_arrive(&aempty[c % kTcABufs]);  // every MMA of the k-step has completed
-                }
-                if (!live) break;
-                if ((kt & 3) == 3) {  // superblock end: acc += T * d_x (per column)
+                    if (!live) break;
+                    if ((kt & 3) == 3) {  // superblock end: acc += T * d_x (per column)
+                        const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            float a[32];
+                            const uint32_t ta = lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2);
+                            if (kt == 3) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) a[j] = 0.0f;
+                            } else {
+                                tmem_ld32(ta, a);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) a[j] = fmaf(T[32 * h2 + j], ld_f32(dxs + 16u * (col0 + 32 * h2 + j)), a[j]);
+                            tmem_st32(ta, a);
+                        }
+                    }
+                } else if ((kt & 3) == 3) {
+                    // superblock end: acc += (D d - Dmin dmin) d_x
+                    const int sbi = c >> 2, db = sbi & 1;
+                    if (!tc_wait(&tfull[db], (sbi >> 1) & 1, abort, p.err)) { live = false; break; }
+                    tc_fence_after();
+                    const uint32_t dh = ld_s32(raw + static_cast<uint32_t>(r * 16));  // d, dmin of this row
+                    const float dd = half_lo(dh), dm = half_hi(dh);
                     const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        float a[32];
-                        const uint32_t ta = lane_base + kTmemAcc + static_cast<uint32_t>(col0 + 32 * h2);
+                        float v[32], m[32], a[32];
+                        tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
+                        tmem_ld32(lane_base + kDmin + static_cast<uint32_t>(col0 + 32 * h2), m);
+                        const uint32_t ta = lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2);
                         if (kt == 3) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) a[j] = 0.0f;
@@ -383,9 +533,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                             tmem_ld32(ta, a);
                         }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) a[j] = fmaf(T[32 * h2 + j], ld_f32(dxs + 16u * (col0 + 32 * h2 + j)), a[j]);
+                        for (int j = 0; j < 32; ++j)
+                            a[j] = fmaf(fmaf(v[j], dd, -m[j] * dm), ld_f32(dxs + 16u * (col0 + 32 * h2 + j)), a[j]);
                         tmem_st32(ta, a);
                     }
+                    tc_fence_before();
+                    mbar_arrive(&tempty[db]);
                 }
                 mbar_arrive(&empty[s]);
             }
@@ -396,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 float a[32];
-                tmem_ld32(lane_base + kTmemAcc + static_cast<uint32_t>(col0 + 32 * h2), a);
+                tmem_ld32(lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2), a);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int col = col0 + 32 * h2 + j;

@@ -183,7 +183,7 @@ cudaError_t launch_gmm(int kind, int fmt, const GmmParams& p, int grid, int smem
 int encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1,
                    uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz);
 
-// Expert-sorted grouped GEMM on tcgen05 (ggq_gmmtc.cuh), Q8_0 banks: items of 128
+// Expert-sorted grouped GEMM on tcgen05 (ggq_gmmtc.cuh), Q8_0 and Q4_K banks: items of 128
 // weight rows x 128 activation columns; every matrix of the bank (gate and up
 // are separate items) writes its own f32 output rows per pair.
 constexpr int kTcThreads = 512;  // 8 epilogue, 6 decode, 1 TMA, 1 MMA warps
@@ -191,7 +191,8 @@ constexpr int kTcThreads = 512;  // 8 epilogue, 6 decode, 1 TMA, 1 MMA warps
 struct GmmTcParams {
     CUtensorMap tm_b;     // f16 activation rows, sorted positions [P][K]: box 64 x 128, 128-byte swizzle
     CUtensorMap tm_dx;    // f32 block scales [P][dx_pitch]: box 4 x 128
-    CUtensorMap tm_w[2];  // Q8_0 bytes [E*N][rowbytes] of gate (or down) and up: box 80 x 128
+    CUtensorMap tm_bs;    // f16 16-group sums [P][K/16]: box 16 x 128 (Q4_K)
+    CUtensorMap tm_w[2];  // weight bytes [E*N][rowbytes]: Q8_0 gate and up (box 80 x 128); Q4_K header (16 x 128) and nibbles (32 x 128)
     int64_t N;            // rows per matrix (multiple of 128)
     int K;                // input width (multiple of 256)
     int nmat;             // matrices per bank (2: gate and up)
@@ -203,9 +204,9 @@ struct GmmTcParams {
     float* out[2];        // per matrix: [pairs][N]
     int* err;
 };
-int gmmtc_encode(GmmTcParams& p, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
-                 const __half* x16, const float* dx, int64_t dx_pitch, int64_t P, int K);
-cudaError_t launch_gmmtc(const GmmTcParams& p, int grid, cudaStream_t s);
+int gmmtc_encode(GmmTcParams& p, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
+                 const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K);
+cudaError_t launch_gmmtc(int fmt, const GmmTcParams& p, int grid, cudaStream_t s);
 // h = silu(g) * u row by row (optionally written to h_out), quantized to Q8_K rows at out + r * pitch.
 cudaError_t launch_quantize_silu(const float* g, const float* u, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
                                  float* h_out, cudaStream_t s);
