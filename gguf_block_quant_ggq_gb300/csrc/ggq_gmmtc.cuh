@@ -50,7 +50,6 @@ namespace ggq {
 
 constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64;
 constexpr int kTcStages = 4;  // TMA ring
-constexpr int kTcABufs = 3;   // decoded weight tiles
 constexpr int kTcEpi = 256;   // epilogue threads (warps 0-7)
 constexpr int kTcDec = 192;   // decode threads (warps 8-13)
 constexpr int kTcTmaWarp = 14, kTcMmaWarp = 15;
@@ -58,22 +57,28 @@ constexpr int kTcRaw = 80;  // raw bytes per weight row per k-step
 constexpr int kTcMaxGroups = 4096;
 static_assert(kTcThreads == kTcEpi + kTcDec + 64, "warp roles");
 
+// Shared-memory layout per format: the TMA ring, then the decoded weight tiles
+// (Q8_0: 5, Q4_K: 4 plus the two mins-term tiles), the item table, the barriers.
+// More weight tiles decouple the decode from the MMA's completion.
+template <int F>
 struct TcSmem {
+    static constexpr int kABufs = F == F_Q8_0 ? 5 : 4;
     static constexpr int kB = kTcBN * kTcBK * 2;     // 16384, SW128 K-major
     static constexpr int kRaw = kTcBM * kTcRaw;      // 10240
     static constexpr int kDX = kTcBN * 16;           // 2048: 4 superblock scales per column
     static constexpr int kStage = kB + kRaw + kDX;   // 28672 (28 KB: activation tiles stay 1024-aligned)
     static constexpr int kA = kTcBM * kTcBK * 2;     // 16384, SW128 K-major
     static constexpr int oA = kTcStages * kStage;
-    static constexpr int oMin = oA + kTcABufs * kA;    // Q4_K mins-term operands: two SW128 tiles
-    static constexpr int oPrefix = oMin + 2 * kA;
+    static constexpr int oMin = oA + kABufs * kA;    // Q4_K mins-term operands: two SW128 tiles
+    static constexpr int oPrefix = oMin + (F == F_Q8_0 ? 0 : 2 * kA);
     static constexpr int kPrefix = (kTcMaxGroups + 1) * 4;
     static constexpr int oBars = (oPrefix + kPrefix + 7) / 8 * 8;
-    static constexpr int kBars = (2 * kTcStages + 2 * kTcABufs + 4) * 8 + 16;
+    static constexpr int kBars = (2 * kTcStages + 2 * kABufs + 4) * 8 + 16;
     static constexpr int kTotal = oBars + kBars + 1024;  // + alignment slack of the dynamic base
 };
-static_assert(TcSmem::kStage % 1024 == 0 && TcSmem::oA % 1024 == 0, "SW128 tiles need 1024-byte alignment");
-static_assert(TcSmem::kTotal <= kSmemLimit, "tcgen05 grouped GEMM shared memory");
+static_assert(TcSmem<F_Q8_0>::kStage % 1024 == 0 && TcSmem<F_Q8_0>::oA % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+static_assert(TcSmem<F_Q8_0>::kTotal <= kSmemLimit && TcSmem<F_Q4_K>::kTotal <= kSmemLimit,
+              "tcgen05 grouped GEMM shared memory");
 
 // tensor-memory columns: two block accumulators, then the item accumulator
 constexpr uint32_t kTmemCols = 512;
@@ -194,13 +199,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     // tensor-memory columns: block (Q8_0) or superblock (Q4_K) accumulators 0..255,
     // Q4_K mins term 256..383, item accumulator
     constexpr uint32_t kAcc = Q8 ? 256u : 384u, kDmin = 256u;
+    using SM = TcSmem<F>;
+    constexpr int kTcABufs = SM::kABufs;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* const smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_launch_dependents();
 
-    int* const s_pref = reinterpret_cast<int*>(smem + TcSmem::oPrefix);
-    uint64_t* const full = reinterpret_cast<uint64_t*>(smem + TcSmem::oBars);
+    int* const s_pref = reinterpret_cast<int*>(smem + SM::oPrefix);
+    uint64_t* const full = reinterpret_cast<uint64_t*>(smem + SM::oBars);
     uint64_t* const empty = full + kTcStages;
     uint64_t* const afull = empty + kTcStages;
     uint64_t* const aempty = afull + kTcABufs;
@@ -208,12 +215,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     uint64_t* const tempty = tfull + 2;
     uint32_t* const tslot = reinterpret_cast<uint32_t*>(tempty + 2);
     volatile int* const abort = reinterpret_cast<volatile int*>(tslot + 1);
-    const auto B16 = [&](int s) { return smem + s * TcSmem::kStage; };
-    const auto RAW = [&](int s) { return smem + s * TcSmem::kStage + TcSmem::kB; };
-    const auto DXS = [&](int s) { return smem + s * TcSmem::kStage + TcSmem::kB + TcSmem::kRaw; };
-    const auto ATILE = [&](int a) { return smem + TcSmem::oA + a * TcSmem::kA; };
-    uint8_t* const min_a = smem + TcSmem::oMin;              // Q4_K: 6-bit mins per 16-group, SW128 rows
-    uint8_t* const min_b = smem + TcSmem::oMin + TcSmem::kA;  // Q4_K: activation 16-group sums, SW128 rows
+    const auto B16 = [&](int s) { return smem + s * SM::kStage; };
+    const auto RAW = [&](int s) { return smem + s * SM::kStage + SM::kB; };
+    const auto DXS = [&](int s) { return smem + s * SM::kStage + SM::kB + SM::kRaw; };
+    const auto ATILE = [&](int a) { return smem + SM::oA + a * SM::kA; };
+    uint8_t* const min_a = smem + SM::oMin;              // Q4_K: 6-bit mins per 16-group, SW128 rows
+    uint8_t* const min_b = smem + SM::oMin + SM::kA;  // Q4_K: activation 16-group sums, SW128 rows
 
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     };
     // raw bytes per k-step: Q8_0 the 80-byte spans; Q4_K headers [128][16], nibbles [128][32],
     // then at a superblock's end the activation 16-group sums [128][32]
-    constexpr uint32_t kRawTx = Q8 ? TcSmem::kRaw : kTcBM * 48;
+    constexpr uint32_t kRawTx = Q8 ? SM::kRaw : kTcBM * 48;
     constexpr int kQsOff = kTcBM * 16, kBsOff = kTcBM * 48;
 
     if (warp == kTcTmaWarp) {
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (c >= kTcStages && !tc_wait(&empty[s], ((c / kTcStages) - 1) & 1, abort, p.err)) break;
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
-                mbar_arrive_expect_tx(&full[s], TcSmem::kB + kRawTx + (sb_end ? TcSmem::kDX + (Q8 ? 0 : kTcBN * 32) : 0));
+                mbar_arrive_expect_tx(&full[s], SM::kB + kRawTx + (sb_end ? SM::kDX + (Q8 ? 0 : kTcBN * 32) : 0));
                 tc_tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
                 if constexpr (Q8) {
                     tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);

@@ -32,11 +32,11 @@ static cudaError_t launch_gmmtc_one(const GmmTcParams& p, int grid, cudaStream_t
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_gmmtc<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kTotal);
+        e = cudaFuncSetAttribute(k_gmmtc<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<F>::kTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    return launch_pdl(k_gmmtc<F>, dim3(grid), dim3(kTcThreads), TcSmem::kTotal, s, p);
+    return launch_pdl(k_gmmtc<F>, dim3(grid), dim3(kTcThreads), TcSmem<F>::kTotal, s, p);
 }
 
 cudaError_t launch_gmmtc(int fmt, const GmmTcParams& p, int grid, cudaStream_t s) {
