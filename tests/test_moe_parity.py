@@ -39,7 +39,7 @@ _BANKS = {}
 
 
 def _banks(cfg, E):
-    key = (cfg["index"], E)
+    key = (cfg["index"], E, cfg["gate"], cfg["up"], cfg["down"])
     if key not in _BANKS:
         g = syn.rng(cfg["index"], 1000 + E)
         H, I = cfg["H"], cfg["I"]
@@ -181,6 +181,15 @@ def test_moe_q8_0_gate_q4k_down_sorted(ctx, T):
     cfg = dict(syn.MOE_PREFILL)
     cfg["E"] = 16
     _run_and_check(ctx, cfg, 16, T, sample_tokens=None if T <= 8 else 6)
+
+
+def test_moe_q8_0_banks_sorted(ctx):
+    """Q8_0 gate/up and Q8_0 down on the expert-sorted route (16 experts): the
+    down bank takes the f16 mma.sync grouped GEMM."""
+    cfg = dict(syn.MOE_PREFILL)
+    cfg["E"] = 16
+    cfg["down"] = "Q8_0"
+    _run_and_check(ctx, cfg, 16, 24, sample_tokens=6)
 
 
 @pytest.mark.parametrize("T", [5, 8, 32, 128])
