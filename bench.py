@@ -203,6 +203,12 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
+def job_gbps(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: every rank streams the same per-step bytes (weak
+    scaling, independent replicas), divided by the slowest rank's time."""
+    return bytes_per_rank_step * world / (ms_per_step / 1e3) / 1e9
+
+
 # ----------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample_rate(target_s=12.0):
@@ -364,7 +370,7 @@ def run_gpu(args, rank, world):
     barrier(world)
     total_ms = max_over_ranks(rt.elapsed_ms(*t_ev), world)
     ms_per_step = total_ms / args.steps
-    value = step_wbytes * world / (ms_per_step / 1e3) / 1e9
+    value = job_gbps(step_wbytes, world, ms_per_step)
 
     # per-launch GEMV kernel durations: events inside the second graph, median of 5 replays
     samples = {k: [] for k in plan}
@@ -406,7 +412,7 @@ def run_gpu(args, rank, world):
         rt.record(e_ev[1], stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(rt.elapsed_ms(*e_ev), world) / args.steps
-    e2e_value = step_wbytes * world / (e2e_ms / 1e3) / 1e9
+    e2e_value = job_gbps(step_wbytes, world, e2e_ms)
     ctx.sync_status()
 
     # ---- secondary workloads (1 GPU lines, rank 0 only)
