@@ -19,6 +19,7 @@
 #include "ggq_device.cuh"
 #include "ggq_direct.cuh"
 #include "ggq_internal.h"
+#include "ggq_plan.h"
 
 namespace ggq {
 cudaError_t launch_gemv_a(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
@@ -185,22 +186,6 @@ ggq_status need_scratch(ggq_ctx* c, size_t bytes) {
                 bytes, c->pool_bytes);
 }
 
-// Shared-memory plan of one streaming launch.
-struct StreamShape {
-    int stages, stride, x_bytes, smem;
-};
-
-bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s, int extra = 1024) {
-    s->stride = static_cast<int>(align_up(static_cast<size_t>(stage_bytes) + 16, 128));
-    s->x_bytes = x_region_bytes(xrows, K, q81);
-    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + extra;
-    if (fixed + s->stride > kSmemLimit) return false;
-    s->stages = (kSmemLimit - fixed) / s->stride;
-    if (s->stages > kMaxStages) s->stages = kMaxStages;
-    s->smem = s->stages * s->stride + fixed;
-    return true;
-}
-
 int pow2_tokens(int64_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
 
 // Smallest token count that the decode GEMV sends to the grouped int8
@@ -352,7 +337,20 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     p.err = &c->ctrl->err;
     p.early_weights = c->static_weights;
     StreamShape sh;
-    if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh))
+    bool fits = plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh);
+    if (kind == KIND_GEMV && (!fits || sh.stages < 2)) {
+        // long rows: stream them in chunks rather than one (or no) whole-row stage
+        StreamShape ch;
+        int cu = 0, cb = 0, rs = 0;
+        if (plan_stream_chunked(f, p.rowbytes, p.xrows, p.K, f == F_Q4_0, &ch, &cu, &cb, &rs)) {
+            sh = ch;
+            p.chunk_units = cu;
+            p.chunk_bytes = cb;
+            p.row_slot = rs;
+            fits = true;
+        }
+    }
+    if (!fits)
         return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld with T=%lld does not fit in shared memory",
                     static_cast<long long>(K), static_cast<long long>(T));
     p.stages = sh.stages;
@@ -769,13 +767,14 @@ ggq_status ggq_quantize_act(ggq_ctx* c, int act, const float* x, int64_t T, int6
     if (act != GGQ_TYPE_Q8_1 && act != GGQ_TYPE_Q8_K)
         return fail(c, GGQ_ERR_UNSUPPORTED, "quantize_act: activation type %d (%s); supported: Q8_1, Q8_K", act,
                     type_name(act));
+    const int64_t blk = act == GGQ_TYPE_Q8_1 ? 32 : 256;
+    if (T < 0 || K < 0 || K % blk)
+        return fail(c, GGQ_ERR_SHAPE, "quantize_act: T=%lld, K=%lld (K must be a multiple of %lld)",
+                    static_cast<long long>(T), static_cast<long long>(K), static_cast<long long>(blk));
+    if (T == 0 || K == 0) return GGQ_OK;  // empty: nothing is read or written
     if (!x || !out) return fail(c, GGQ_ERR_INVALID_ARG, "quantize_act: null pointer");
     if (!aligned16(x) || (reinterpret_cast<uintptr_t>(out) & 3))
         return fail(c, GGQ_ERR_INVALID_ARG, "quantize_act: x must be 16-byte and out 4-byte aligned");
-    const int64_t blk = act == GGQ_TYPE_Q8_1 ? 32 : 256;
-    if (T < 0 || K < 0 || K % blk)
-        return fail(c, GGQ_ERR_SHAPE, "quantize_act: K=%lld must be a multiple of %lld", static_cast<long long>(K),
-                    static_cast<long long>(blk));
     cudaError_t e = launch_quantize(act == GGQ_TYPE_Q8_1 ? 0 : 1, x, T, K, static_cast<uint8_t*>(out),
                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GGQ_OK : cuda_fail(c, e, "quantize_act launch");
@@ -788,10 +787,11 @@ ggq_status ggq_dequant(ggq_ctx* c, int w, const void* blocks, int64_t rows, int6
     if (f < 0)
         return fail(c, GGQ_ERR_UNSUPPORTED,
                     "dequant: weight type %d (%s); supported: Q4_0, Q8_0, Q4_K, Q5_K, Q6_K, MXFP4", w, type_name(w));
-    if (!blocks || !out) return fail(c, GGQ_ERR_INVALID_ARG, "dequant: null pointer");
     if (rows < 0 || K < 0 || K % fmt_qk(f))
-        return fail(c, GGQ_ERR_SHAPE, "dequant: K=%lld must be a multiple of %d", static_cast<long long>(K),
-                    fmt_qk(f));
+        return fail(c, GGQ_ERR_SHAPE, "dequant: rows=%lld, K=%lld (K must be a multiple of %d)",
+                    static_cast<long long>(rows), static_cast<long long>(K), fmt_qk(f));
+    if (rows == 0 || K == 0) return GGQ_OK;  // empty: nothing is read or written
+    if (!blocks || !out) return fail(c, GGQ_ERR_INVALID_ARG, "dequant: null pointer");
     cudaError_t e = launch_dequant(f, static_cast<const uint8_t*>(blocks), rows, K, out,
                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GGQ_OK : cuda_fail(c, e, "dequant launch");

@@ -34,6 +34,10 @@ struct StreamParams {
     int stages;
     int stage_stride;   // bytes per ring slot (multiple of 128)
     int x_bytes;        // bytes of the staged-activation region
+    int chunk_units;    // GEMV only: 0 = whole rows per stage; else each stage holds
+                        // this many 64-weight units of each of the tile's rows
+    int chunk_bytes;    // bytes of chunk_units units
+    int row_slot;       // bytes between the rows of a chunked stage (a multiple of 16)
 };
 
 // Bytes of the structure-of-arrays activation region for `rows` rows of width

@@ -13,6 +13,7 @@
 #include "../../include/ggq.h"
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
+#include "ggq_plan.h"
 
 namespace ggq {
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
@@ -107,21 +108,29 @@ extern "C" ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, i
     p.T = static_cast<int>(T);
     p.Y = Y;
     p.err = nullptr;  // bounded-wait timeouts are not reported by this entry point
-    const int stride = static_cast<int>((kTileRows * p.rowbytes + 16 + 127) / 128 * 128);
-    const int x_bytes = x_region_bytes(p.xrows, p.K, q81);
-    const int fixed = x_bytes + 2 * kMaxStages * 8 + 1024;
-    if (fixed + stride > kSmemLimit) return GGQ_ERR_SHAPE;
-    int stages = (kSmemLimit - fixed) / stride;
-    if (stages > kMaxStages) stages = kMaxStages;
-    p.stages = stages;
-    p.stage_stride = stride;
-    p.x_bytes = x_bytes;
+    StreamShape sh;
+    bool fits = plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, q81, &sh);
+    if (!fits || sh.stages < 2) {  // long rows: streamed in chunks
+        StreamShape ch;
+        int cu = 0, cb = 0, rs = 0;
+        if (plan_stream_chunked(f, p.rowbytes, p.xrows, p.K, q81, &ch, &cu, &cb, &rs)) {
+            sh = ch;
+            p.chunk_units = cu;
+            p.chunk_bytes = cb;
+            p.row_slot = rs;
+            fits = true;
+        }
+    }
+    if (!fits) return GGQ_ERR_SHAPE;
+    p.stages = sh.stages;
+    p.stage_stride = sh.stride;
+    p.x_bytes = sh.x_bytes;
     const int64_t tiles = (N + kTileRows - 1) / kTileRows;
     const int grid = static_cast<int>(tiles < d->nsm ? tiles : d->nsm);
     const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_quantize(q81 ? 0 : 1, X, T, K, d->scratch, s) != cudaSuccess) return GGQ_ERR_CUDA;
-    if (launch_stream(KIND_GEMV, f, nt, p, grid, stages * stride + fixed, s) != cudaSuccess) return GGQ_ERR_CUDA;
+    if (launch_stream(KIND_GEMV, f, nt, p, grid, sh.smem, s) != cudaSuccess) return GGQ_ERR_CUDA;
     return GGQ_OK;
 }

@@ -1,0 +1,81 @@
+// ggq_plan.h -- shared-memory plans of the weight-streaming GEMV kernel
+// (k_stream), used by the pooled and the allocation-free entry points alike.
+#pragma once
+#include <stdint.h>
+
+#include "ggq_device.cuh"
+#include "ggq_internal.h"
+
+namespace ggq {
+
+// Shared-memory plan of one streaming launch.
+struct StreamShape {
+    int stages, stride, x_bytes, smem;
+};
+
+inline bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamShape* s, int extra = 1024) {
+    s->stride = static_cast<int>((static_cast<size_t>(stage_bytes) + 16 + 127) / 128 * 128);
+    s->x_bytes = x_region_bytes(xrows, K, q81);
+    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + extra;
+    if (fixed + s->stride > kSmemLimit) return false;
+    s->stages = (kSmemLimit - fixed) / s->stride;
+    if (s->stages > kMaxStages) s->stages = kMaxStages;
+    s->smem = s->stages * s->stride + fixed;
+    return true;
+}
+
+// The row chunk of format f that a chunked stage is a whole number of: it
+// starts on a unit (or superblock) boundary and, where the rows are 16-byte
+// multiples, is one too (then every chunk is a bulk copy of its own).
+// 64-weight units and bytes.
+inline void chunk_granule(int f, int64_t rowbytes, int* units, int* bytes) {
+    switch (f) {
+    case F_Q4_0: *units = 4, *bytes = 144; break;   // 8 blocks of 18 B
+    case F_Q8_0: *units = 4, *bytes = 272; break;   // 8 blocks of 34 B
+    case F_MXFP4: *units = 8, *bytes = 272; break;  // 16 blocks of 17 B
+    case F_Q4_K: *units = 4, *bytes = 144; break;   // one superblock
+    case F_Q5_K: *units = 4, *bytes = 176; break;   // one superblock
+    default:                                        // Q6_K: superblocks of 210 B
+        if (rowbytes % 16 == 0) *units = 32, *bytes = 1680;
+        else *units = 4, *bytes = 210;
+        break;
+    }
+}
+
+// Plan of the streaming GEMV for rows too long for whole-row stages: the
+// activations stay whole in shared memory and each stage holds one chunk of
+// every row of a 16-row tile (about six stages in the ring, at least two).
+// Rows that are not 16-byte multiples get 16 spare bytes per row slot: their
+// chunks land at the same offset modulo 16 as in global memory.  False if two
+// stages do not fit.
+inline bool plan_stream_chunked(int f, int64_t rowbytes, int xrows, int K, bool q81, StreamShape* s,
+                                int* chunk_units, int* chunk_bytes, int* row_slot, bool small_granule = false) {
+    int gu = 0, gb = 0;
+    chunk_granule(f, rowbytes, &gu, &gb);
+    if (small_granule && f == F_Q6_K) gu = 4, gb = 210;  // one superblock: unaligned chunks
+    s->x_bytes = x_region_bytes(xrows, K, q81);
+    const int fixed = s->x_bytes + 2 * kMaxStages * 8 + 1024;
+    const int avail = kSmemLimit - fixed;
+    if (avail <= 0) return false;
+    int g = avail / 6 / kTileRows / gb;
+    if (g < 1) g = 1;
+    if (static_cast<int64_t>(g) * gb > rowbytes) g = static_cast<int>((rowbytes + gb - 1) / gb);
+    const int cb = g * gb;
+    const bool aligned = rowbytes % 16 == 0 && cb % 16 == 0;
+    const int slot = aligned ? cb : (cb + 15) / 16 * 16 + 16;
+    s->stride = static_cast<int>((static_cast<size_t>(kTileRows) * slot + 16 + 127) / 128 * 128);
+    s->stages = avail / s->stride;
+    if (s->stages < 2) {
+        if (f == F_Q6_K && !small_granule)
+            return plan_stream_chunked(f, rowbytes, xrows, K, q81, s, chunk_units, chunk_bytes, row_slot, true);
+        return false;
+    }
+    if (s->stages > kMaxStages) s->stages = kMaxStages;
+    s->smem = s->stages * s->stride + fixed;
+    *chunk_units = g * gu;
+    *chunk_bytes = cb;
+    *row_slot = slot;
+    return true;
+}
+
+}  // namespace ggq

@@ -147,12 +147,14 @@ __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, con
 
 // Accumulate one row against the activation rows xr[0..nslots) into acc[].
 // For 1-2 slots two units per lane are kept in flight (units u and u+32) so
-// that their load, decode and dp4a chains overlap.
+// that their load, decode and dp4a chains overlap.  With ue >= 0 only units
+// [u0, ue) are taken; `row` is then the address the row's start would have,
+// so that unit u still sits at its offset in the row.
 template <int F, int NT>
 __device__ __forceinline__ void row_accumulate(saddr row, const XS& xs, const int* xr, int nslots,
-                                               float* acc, int lane) {
-    const int nu = units_per_row(xs.K), nb32 = xs.K >> 5;
-    int u = lane;
+                                               float* acc, int lane, int u0 = 0, int ue = -1) {
+    const int nu = ue < 0 ? units_per_row(xs.K) : ue, nb32 = xs.K >> 5;
+    int u = u0 + lane;
     // two units in flight for 1-2 slots; at 4+ slots the slot loop supplies the
     // independent work and a second unit would only spill (17 warps cap a
     // thread at 96 registers)
@@ -271,6 +273,66 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         }
         __syncwarp();
         start_arrive();
+        if (KIND == KIND_GEMV && p.chunk_units > 0) {
+            // rows too long for whole-row stages: stage j = (tile, chunk kc); lane i
+            // brings row i's chunk.  A row slot holds global byte x at slot + (x -
+            // x0), x0 the chunk start rounded down to 16 bytes: the 16-byte-aligned
+            // middle of the chunk is one bulk copy, the ragged ends (rows that are
+            // not 16-byte multiples only) are copied byte by byte
+            const uint64_t pol = policy_evict_first();
+            if (!p.early_weights) pdl_wait();
+            const int nkc = (units_per_row(K) + p.chunk_units - 1) / p.chunk_units;
+            int j = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
+                const int64_t r0 = static_cast<int64_t>(item) * kTileRows;
+                const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
+                for (int kc = 0; kc < nkc; ++kc, ++j) {
+                    const int s = j % p.stages;
+                    const int64_t off = static_cast<int64_t>(kc) * p.chunk_bytes;
+                    const int64_t cb = p.rowbytes - off < p.chunk_bytes ? p.rowbytes - off : p.chunk_bytes;
+                    if (lane == 0) ok = mbar_wait(&empty[s], (static_cast<uint32_t>(j / p.stages) & 1u) ^ 1u);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) set_error(p.err, DEV_ERR_TIMEOUT);
+                        break;
+                    }
+                    uint32_t bulk = 0u;
+                    if (lane < nr) {
+                        const uint8_t* src = p.W + (r0 + lane) * p.rowbytes + off;
+                        const uintptr_t x0 = reinterpret_cast<uintptr_t>(src) & ~static_cast<uintptr_t>(15);
+                        const uintptr_t a0 = (reinterpret_cast<uintptr_t>(src) + 15) & ~static_cast<uintptr_t>(15);
+                        const uintptr_t a1 = (reinterpret_cast<uintptr_t>(src) + cb) & ~static_cast<uintptr_t>(15);
+                        uint8_t* slot = ring + static_cast<size_t>(s) * p.stage_stride + static_cast<size_t>(lane) * p.row_slot;
+                        const uint8_t* end = src + cb;
+                        const uint8_t* mid0 = a1 > a0 ? reinterpret_cast<const uint8_t*>(a0) : end;
+                        const uint8_t* mid1 = a1 > a0 ? reinterpret_cast<const uint8_t*>(a1) : end;
+                        for (const uint8_t* q = src; q < mid0; ++q) slot[q - reinterpret_cast<const uint8_t*>(x0)] = __ldg(q);
+                        for (const uint8_t* q = mid1; q < end; ++q) slot[q - reinterpret_cast<const uint8_t*>(x0)] = __ldg(q);
+                        // this lane's byte stores (now and in earlier passes over the slot)
+                        // before the bulk copies that may later land on the same bytes
+                        if (mid0 != src || mid1 != end) fence_proxy_async_smem();
+                        if (a1 > a0) {
+                            bulk = static_cast<uint32_t>(a1 - a0);
+                            bulk_g2s(slot + (a0 - x0), reinterpret_cast<const uint8_t*>(a0), bulk, &full[s], pol);
+                        }
+                    }
+                    // the byte stores above happen before lane 0's arrive (release)
+                    const uint32_t total = __reduce_add_sync(0xffffffffu, bulk);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
+                }
+            }
+            if (lane == 0) {
+                for (int q = (j > p.stages ? j - p.stages : 0); q < j; ++q) {
+                    if (!mbar_wait(&full[q % p.stages], static_cast<uint32_t>(q / p.stages) & 1u)) {
+                        set_error(p.err, DEV_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            return;
+        }
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             if (!p.early_weights) pdl_wait();  // the previous kernel may still be writing the weights
@@ -338,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
 
     if constexpr (KIND == KIND_GEMV && NT == 1) {
         const int nu = units_per_row(K), nb32 = K >> 5;
-        if (nu <= 64) {
+        if (nu <= 64 && p.chunk_units == 0) {
             // One token, K <= 4096: lane l owns units l and l + 32 of every row,
             // so its activations stay in registers for the whole kernel.
             XUnit xa, xb;
@@ -367,6 +429,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            return;
+        }
+    }
+
+    if constexpr (KIND == KIND_GEMV) {
+        if (p.chunk_units > 0) {
+            // chunked rows: the warp's row sums its chunks in acc[] and is reduced once per tile
+            const int nu = units_per_row(K);
+            const int nkc = (nu + p.chunk_units - 1) / p.chunk_units;
+            int xr[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) xr[t] = t;
+            int j = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+                const int64_t r = static_cast<int64_t>(item) * kTileRows + warp;
+                float acc[NT];
+#pragma unroll
+                for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
+                for (int kc = 0; kc < nkc; ++kc, ++j) {
+                    const int s = j % p.stages;
+                    const uint32_t ph = static_cast<uint32_t>(j / p.stages) & 1u;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph))) {  // warp-uniform
+                        set_error(p.err, DEV_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    if (r < p.N) {
+                        const int u0 = kc * p.chunk_units;
+                        const int ue = u0 + p.chunk_units < nu ? u0 + p.chunk_units : nu;
+                        // the row's start, as if the whole row were staged: unit u keeps its
+                        // offset (the slot starts at the chunk's global address rounded down to 16)
+                        const uint32_t lead = static_cast<uint32_t>((r * p.rowbytes + static_cast<int64_t>(kc) * p.chunk_bytes) & 15);
+                        const saddr row = ring_s + static_cast<uint32_t>(s * p.stage_stride + warp * p.row_slot) + lead -
+                                          static_cast<uint32_t>(kc) * static_cast<uint32_t>(p.chunk_bytes);
+                        row_accumulate<F, NT>(row, xs, xr, p.T, acc, lane, u0, ue);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
+                const float v = warp_transpose_reduce<LV>(acc, lane);
+                const int t = lane >> SH;
+                if (ok && r < p.N && (lane & ((1 << SH) - 1)) == 0 && t < p.T) p.Y[t * p.N + r] = v;
+                if (!ok) break;
             }
             return;
         }

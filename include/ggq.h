@@ -164,11 +164,14 @@ int ggq_supported(int w, int act, int op);
  * (act = GGQ_TYPE_Q8_1: K % 32 == 0, 36 B blocks; GGQ_TYPE_Q8_K: K % 256 == 0,
  * 292 B blocks).  Per block: d = amax/127 (fp32), q = round-half-away(x * (1/d))
  * clamped to +-127; Q8_1 stores d and s = d*sum(q) as fp16, Q8_K stores d as
- * fp32 and the 16 sums of 16 quants.  Needs no scratch. */
+ * fp32 and the 16 sums of 16 quants.  T = 0 or K = 0 is an empty call: it
+ * returns GGQ_OK without reading or writing (the pointers may be NULL).
+ * Needs no scratch. */
 ggq_status ggq_quantize_act(ggq_ctx* ctx, int act, const float* x, int64_t T, int64_t K, void* out, void* stream);
 
 /* Dequantize rows x K weights of format w to fp32 out [rows][K] (FreeToken
  * PR #136, Summary: Q4_0 dequantization; all six weight formats here).
+ * rows = 0 or K = 0 is an empty call (GGQ_OK, nothing read or written).
  * Needs no scratch. */
 ggq_status ggq_dequant(ggq_ctx* ctx, int w, const void* blocks, int64_t rows, int64_t K, float* out, void* stream);
 
@@ -176,7 +179,12 @@ ggq_status ggq_dequant(ggq_ctx* ctx, int w, const void* blocks, int64_t rows, in
  * ("MatmulBT", vllm.cpp PR #523 op 74; ggml_mul_mat_vec_a8 of FreeToken
  * PR #136).  X is quantized inside the call (Q8_1 for Q4_0, Q8_K otherwise)
  * into the scratch pool.  1 <= T <= 8.  K must be a multiple of the weight
- * block (32 or 256); Q8_K activations also need K % 256 == 0. */
+ * block (32 or 256); Q8_K activations also need K % 256 == 0.  Rows of any
+ * length are streamed (in row chunks when a 16-row tile does not fit twice in
+ * shared memory); the T quantized activation rows are held whole in shared
+ * memory, about 1.52 bytes per input per token, which bounds T x K: every
+ * format runs K up to 18176 at T = 8, 36352 at T = 4, 73216 at T = 2 and
+ * 146432 at T = 1; larger shapes return GGQ_ERR_SHAPE. */
 ggq_status ggq_mul_mat_vec(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
                            float* Y, void* stream);
 

@@ -93,6 +93,46 @@ def test_block_dots_bit_exact_and_gemv_within_tolerance(ctx, fmt, N, K, T):
     check_outputs(y, ref, absdot, f"{fmt} mul_mat_vec N={N} K={K} T={T}")
 
 
+LONG_ROWS = [  # (fmt, N, K, T): rows too long for whole-row stages, streamed in row chunks
+    ("Q8_0", 16 * 160 + 7, 14336, 1),  # more tiles than SMs (a CTA streams several), ragged tail
+    ("Q8_0", 37, 14336, 2),
+    ("Q8_0", 45, 14336, 8),            # 28 chunks per tile: the ring wraps many times
+    ("Q4_K", 45, 28672, 1),
+    ("Q4_K", 29, 28672, 4),
+    ("Q6_K", 16 * 160 + 3, 14336, 1),  # 8-superblock chunks
+    ("Q5_K", 53, 14336, 3),
+    ("Q4_0", 21, 16384, 1),
+    ("MXFP4", 40, 16384, 2),
+    # rows that are not 16-byte multiples: chunk ends copied byte by byte
+    ("Q6_K", 16 * 9 + 7, 18944, 1),    # 74 superblocks: 15540-byte rows
+    ("Q6_K", 35, 18944, 4),
+    ("MXFP4", 40, 23296, 2),           # 12376-byte rows
+]
+
+
+@pytest.mark.parametrize("fmt,N,K,T", LONG_ROWS)
+def test_long_rows_stream_in_chunks(ctx, fmt, N, K, T):
+    W, x = _case(fmt, N, K, T, N + K + T + FORMATS.index(fmt))
+    xq = orc.quantize(orc.act_type(fmt), x)
+    dW = to_dev(W)
+    ref, absdot = orc.gemv_dequant(fmt, W, N, K, xq, T)
+    y_q = to_host(ctx.mul_mat_vec_q(fmt, dW, N, K, to_dev(xq), T))
+    check_outputs(y_q, ref, absdot, f"{fmt} long rows mul_mat_vec_q N={N} K={K} T={T}")
+    y = to_host(ctx.mul_mat_vec(fmt, dW, N, K, to_dev(x)))
+    check_outputs(y, ref, absdot, f"{fmt} long rows mul_mat_vec N={N} K={K} T={T}")
+    ctx.sync_status()
+
+
+def test_activations_too_large_for_shared_memory_are_refused(ctx):
+    # 8 tokens x 28672 inputs of staged activations exceed one SM's shared memory
+    K, T = 28672, 8
+    W = to_dev(syn.weights("Q4_K", 16, K, syn.rng(56, 0)))
+    xq = to_dev(orc.quantize("Q8_K", syn.activations(T, K, syn.rng(56, 1))))
+    with pytest.raises(ggq.GGQError, match="SHAPE"):
+        ctx.mul_mat_vec_q("Q4_K", W, 16, K, xq, T)
+    ctx.sync_status()
+
+
 @pytest.mark.parametrize("N,K,T", Q4_0_ODD_SHAPES)
 def test_q4_0_widths_with_a_half_unit(ctx, N, K, T):
     W, x = _case("Q4_0", N, K, T, 7 * N + K)
@@ -154,3 +194,25 @@ def test_errors_are_refused_loudly(ctx):
     finally:
         fresh.close()
     ctx.sync_status()
+
+
+def test_empty_inputs(ctx):
+    """Empty quantize/dequant calls are no-ops (NULL pointers allowed); the
+    GEMV, whose contract is 1 <= T <= 8 and N >= 1, refuses T = 0 and N = 0."""
+    h = ggq.load()
+    Q8_1, Q8_K, Q4_K = ggq.TYPE["Q8_1"], ggq.TYPE["Q8_K"], ggq.TYPE["Q4_K"]
+    assert h.ggq_quantize_act(ctx.handle, Q8_K, None, 0, 4096, None, None) == 0
+    assert h.ggq_quantize_act(ctx.handle, Q8_1, None, 3, 0, None, None) == 0
+    assert h.ggq_dequant(ctx.handle, Q4_K, None, 0, 256, None, None) == 0
+    # an empty call writes nothing: a sentinel-filled buffer stays as it was
+    out = torch.full((4, 292), 7, dtype=torch.uint8, device="cuda")
+    x = to_dev(np.ones((1, 256), np.float32))
+    assert h.ggq_quantize_act(ctx.handle, Q8_K, x.data_ptr(), 0, 256, out.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    assert bool(torch.all(out == 7))
+    W = to_dev(syn.weights("Q4_K", 16, 256, syn.rng(55, 0)))
+    y = torch.empty((1, 16), dtype=torch.float32, device="cuda")
+    assert h.ggq_mul_mat_vec(ctx.handle, Q4_K, W.data_ptr(), 16, 256, x.data_ptr(), 0, y.data_ptr(), None) == 2
+    assert h.ggq_mul_mat_vec(ctx.handle, Q4_K, W.data_ptr(), 0, 256, x.data_ptr(), 1, y.data_ptr(), None) == 2
+    ctx.sync_status()
+

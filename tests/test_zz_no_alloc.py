@@ -30,8 +30,10 @@ def test_noalloc_gemv_matches_pooled_entry_point():
     lib = ggq.load()
     ctx = ggq.Context(0)
     try:
-        # two different calls in a row: the second overwrites the first's scratch
-        for call, (fmt, N, K, T) in enumerate([("Q4_K", 300, 4096, 8), ("Q4_0", 77, 1024, 3)]):
+        # different calls in a row: each overwrites the previous one's scratch; the
+        # last has rows too long for whole-row stages (streamed in chunks)
+        for call, (fmt, N, K, T) in enumerate([("Q4_K", 300, 4096, 8), ("Q4_0", 77, 1024, 3),
+                                               ("Q8_0", 37, 14336, 2)]):
             W = syn.weights(fmt, N, K, syn.rng(70, call))
             x = syn.activations(T, K, syn.rng(70, 10 + call))
             dW, dx = to_dev(W), to_dev(x)
