@@ -47,17 +47,28 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_kquant_gemv_step.json")
 
 
 # sources of the decode GEMV kernels (k_stream, k_gemv_mma) that the stored traffic was taken on
-GEMV_SOURCES = ("ggq_device.cuh", "ggq_stream.cuh", "ggq_mmav.cuh", "ggq_k_gemv_a.cu", "ggq_k_gemv_b.cu", "ggq_k_mmav.cu")
+GEMV_SOURCES = ("ggq_device.cuh", "ggq_stream.cuh", "ggq_mmav.cuh", "ggq_k_gemv_a.cu", "ggq_k_gemv_b.cu", "ggq_k_mmav.cu",
+                "ggq_internal.h", "ggq_plan.h")
+
+
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed, so that
+    documentation edits leave the hash (and the stored measurement) valid."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
 
 
 def csrc_hash():
-    """Hash of the GEMV kernel sources: a stored DRAM-traffic figure applies only to the kernels it was taken on."""
+    """Hash of the GEMV kernel code (comments excluded): a stored DRAM-traffic
+    figure applies only to the kernels it was taken on."""
     import hashlib
     d = os.path.join(ROOT, "gguf_block_quant_ggq_gb300", "csrc")
     h = hashlib.sha256()
     for f in GEMV_SOURCES:
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

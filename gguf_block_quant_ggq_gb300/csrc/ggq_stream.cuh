@@ -15,7 +15,10 @@
 //     CTA into shared memory (structure of arrays, padded against bank
 //     conflicts);
 //   * per-lane fp32 partials of (row, token) are summed with one transpose
-//     reduction per stage.
+//     reduction per stage;
+//   * rows too long for two whole 16-row stages stream in row chunks (one
+//     chunk of each of the tile's rows per stage, a row's partials kept in
+//     registers across its chunks and reduced once per tile).
 // Every wait is bounded; on timeout the kernel records an error word, drains
 // its own copies and returns.
 #pragma once
@@ -51,10 +54,6 @@ __device__ __forceinline__ XRegion x_region(uint8_t* base, int rows, int K, bool
     return r;
 }
 
-// Stage packed activation blocks (Q8_K: 292 B, or Q8_1: 36 B) from global into
-// the structure-of-arrays region.  PERM stores each 32-block's quants in the
-// interleaved order (0,16,1,17,...) that the MXFP4 lookup produces.  The Q8_1
-// per-32 sums must be zero on entry (they are accumulated with atomics).
 // Stage packed activation rows (Q8_K: 292-byte blocks, rows `pitch` bytes
 // apart (0: packed); Q8_1: 36-byte blocks) from global into the
 // structure-of-arrays region.  PERM stores each 32-block's quants in the
