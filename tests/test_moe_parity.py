@@ -126,6 +126,19 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
         y2 = ctx.moe_experts(w8, E, H, I, k, to_dev(x), logits=to_dev(logits))
     ctx.sync_status()
     check_outputs(to_host(y2).astype(np.float64)[toks], y_tf, 1.3 * y_abs, "combine (fused down)")
+    # (v'') with every dump but the per-pair down outputs, the layer takes the
+    # same kernels as without dumps: routing, x^, g, u, h and h^ are
+    # bit-identical to the fully dumped run above, and y to the run without dumps
+    d3 = {n: t for n, t in _dump_buffers(T, k, H, I).items() if n != "o"}
+    if routed:
+        y3 = ctx.moe_experts(w8, E, H, I, k, to_dev(x), ids=to_dev(ids_ref), route_w=to_dev(w_ref.astype(np.float32)),
+                             dump=d3)
+    else:
+        y3 = ctx.moe_experts(w8, E, H, I, k, to_dev(x), logits=to_dev(logits), dump=d3)
+    ctx.sync_status()
+    for n, t in d3.items():
+        assert np.array_equal(to_host(t), r[n]), f"{n} differs from the fully dumped run"
+    assert np.array_equal(to_host(y3), to_host(y2)), "y differs with and without the dumps"
     # free running against the whole oracle layer on the checked tokens
     ref = orc.moe(cfg["gate"], host["gate"], cfg["up"], host["up"], cfg["down"], host["down"], E, H, I, k,
                   x[toks], logits[toks])
