@@ -9,10 +9,12 @@ measured HBM copy bandwidth.  Each format has 3 rotating weight copies, so the
 weights of one step (736 MB) and the live set (551 MB) are far larger than the
 129 MB L2.  The step is captured once in a CUDA graph and replayed.
 
-Secondary lines (same JSON, "workloads"): the Q4_0 1024 x 4096 GEMV, the MoE
-decode layer (128 experts, H 2048, I 768, Q4_K gate/up, Q6_K down, top-8,
-1-4 tokens) and the MXFP4 routed experts (256 experts, H 4096, I 2048, top-8,
-1-5 tokens); MoE GB/s counts the distinct experts actually selected.
+Secondary lines (same JSON, "workloads"): the Q4_0 1024 x 4096 GEMV, the
+4096 x 14336 long-row GEMV (Q8_0, Q6_K at 1 and 8 tokens), the MoE decode
+layer (128 experts, H 2048, I 768, Q4_K gate/up, Q6_K down, top-8, 1-4
+tokens), the MXFP4 routed experts (256 experts, H 4096, I 2048, top-8, 1-512
+tokens) and the 4096-token prefill layer; MoE GB/s counts the distinct
+experts actually selected.
 
 --impl reference times the CPU oracle on a bounded sample of the same workload.
 """
@@ -523,6 +525,32 @@ def secondary_workloads(ctx, rt, hbm_peak):
                                      "frac": round(bytes_ / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "us_per_call": round(ms * 1e3 / len(copies), 2)}
     del copies
+
+    # long rows: the 4096 x 14336 down-projection shape at T = 1 and 8 (rows of
+    # 15232 B in Q8_0, 11760 B in Q6_K stream in row chunks); 3 rotating copies
+    ctx.set_static_weights(True)
+    NL, KL = 4096, 14336
+    ctx.reserve(max_tokens=8, max_k=KL)
+    for fmt in ("Q8_0", "Q6_K"):
+        gl = syn.rng(KQ["index"], 300 + FMTS.index(fmt))
+        lcopies = [torch.from_numpy(syn.weights(fmt, NL, KL, gl)).cuda() for _ in range(3)]
+        for T in (1, 8):
+            xl = torch.from_numpy(syn.activations(T, KL, gl)).cuda()
+            yl = torch.empty((T, NL), dtype=torch.float32, device="cuda")
+            xql = torch.empty((T, syn.row_bytes("Q8_K", KL)), dtype=torch.uint8, device="cuda")
+            ctx.quantize_act("Q8_K", xl, out=xql)
+            torch.cuda.synchronize()
+
+            def longrow():
+                for Wc in lcopies:
+                    ctx.mul_mat_vec_q(fmt, Wc, NL, KL, xql, T, Y=yl)
+
+            ms = _graph_time(longrow, 10, rt, stream)
+            bytes_ = len(lcopies) * NL * syn.row_bytes(fmt, KL)
+            out[f"{fmt.lower()}_gemv_{NL}x{KL}_T{T}"] = {
+                "GBps": round(bytes_ / (ms / 1e3) / 1e9, 1), "frac": round(bytes_ / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                "us_per_call": round(ms * 1e3 / len(lcopies), 2)}
+        del lcopies
 
     # MoE layers: rotate seeded router-logit sets so the expert sets differ per call
     ctx.set_static_weights(True)
