@@ -216,6 +216,11 @@ ggq_status ggq_block_dots(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_t
  * streams the selected experts once; 2 <= T <= 4 is the direct tiny-batch
  * route (each distinct expert's rows are read once for every token that chose
  * it); T >= 5 groups (token, slot) pairs by expert into expert-sorted tiles.
+ * Widths are bounded by shared memory (16-row weight tiles and the quantized
+ * activations of the tokens or pairs are staged whole): the direct route
+ * (T <= 4) runs H up to 6400 for Q8_0 gate/up and 8192-12288 for the 4-6-bit
+ * and MXFP4 formats at one token (less at four tokens: 5632-9984), and I up
+ * to 3328-3840 at four tokens with top-8; wider shapes return GGQ_ERR_SHAPE.
  * `dump` may be NULL.  Scratch: ggq_reserve with the same E, H, I, top_k, T. */
 ggq_status ggq_moe_experts(ggq_ctx* ctx, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
                            const float* X, const float* router_logits, int64_t T, float* Y, const ggq_moe_dump* dump,
