@@ -337,22 +337,25 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     p.err = &c->ctrl->err;
     p.early_weights = c->static_weights;
     StreamShape sh;
-    bool fits = plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh);
-    if (kind == KIND_GEMV && (!fits || sh.stages < 2)) {
-        // long rows: stream them in chunks rather than one (or no) whole-row stage
-        StreamShape ch;
-        int cu = 0, cb = 0, rs = 0;
-        if (plan_stream_chunked(f, p.rowbytes, p.xrows, p.K, f == F_Q4_0, &ch, &cu, &cb, &rs)) {
-            sh = ch;
-            p.chunk_units = cu;
-            p.chunk_bytes = cb;
-            p.row_slot = rs;
-            fits = true;
+    if (kind == KIND_GEMV) {
+        const StreamPlan plan = plan_gemv_stream(f, p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh, &p.chunk_units,
+                                                 &p.chunk_bytes, &p.row_slot);
+        if (plan == StreamPlan::kSplit) {
+            // the tokens as two groups, each streaming the weights once
+            const int64_t xrow = f == F_Q4_0 ? K / 32 * 36 : K / 256 * 292;
+            const int64_t T0 = T / 2;
+            const ggq_status s0 = launch_gemv_kind(c, kind, w, W, N, K, Xq, T0, Y, coefs, st);
+            if (s0 != GGQ_OK) return s0;
+            return launch_gemv_kind(c, kind, w, W, N, K, static_cast<const uint8_t*>(Xq) + T0 * xrow, T - T0,
+                                    Y + T0 * N, coefs, st);
         }
-    }
-    if (!fits)
-        return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld with T=%lld does not fit in shared memory",
+        if (plan == StreamPlan::kNone)
+            return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld does not fit in shared memory",
+                        static_cast<long long>(K));
+    } else if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh)) {
+        return fail(c, GGQ_ERR_SHAPE, "block_dots: K=%lld with T=%lld does not fit in shared memory",
                     static_cast<long long>(K), static_cast<long long>(T));
+    }
     p.stages = sh.stages;
     p.stage_stride = sh.stride;
     p.x_bytes = sh.x_bytes;

@@ -78,6 +78,35 @@ ggq_status device_setup(NoAllocDevice** out) {
     return GGQ_OK;
 }
 
+// The streaming GEMV over tokens [0, T) of xq (rows xrow bytes apart), with
+// the plan of the pooled call: whole-row stages, row chunks, or the tokens in
+// two groups.
+ggq_status launch_groups(int f, StreamParams p, const uint8_t* xq, int64_t T, float* Y, int64_t xrow, int nsm,
+                         cudaStream_t s) {
+    StreamShape sh;
+    const bool q81 = f == F_Q4_0;
+    const StreamPlan plan = plan_gemv_stream(f, p.rowbytes, static_cast<int>(T), p.K, q81, &sh, &p.chunk_units,
+                                             &p.chunk_bytes, &p.row_slot);
+    if (plan == StreamPlan::kNone) return GGQ_ERR_SHAPE;
+    if (plan == StreamPlan::kSplit) {
+        const int64_t T0 = T / 2;
+        const ggq_status s0 = launch_groups(f, p, xq, T0, Y, xrow, nsm, s);
+        if (s0 != GGQ_OK) return s0;
+        return launch_groups(f, p, xq + T0 * xrow, T - T0, Y + T0 * p.N, xrow, nsm, s);
+    }
+    p.xq = xq;
+    p.xrows = static_cast<int>(T);
+    p.T = static_cast<int>(T);
+    p.Y = Y;
+    p.stages = sh.stages;
+    p.stage_stride = sh.stride;
+    p.x_bytes = sh.x_bytes;
+    const int64_t tiles = (p.N + kTileRows - 1) / kTileRows;
+    const int grid = static_cast<int>(tiles < nsm ? tiles : nsm);
+    const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+    return launch_stream(KIND_GEMV, f, nt, p, grid, sh.smem, s) == cudaSuccess ? GGQ_OK : GGQ_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
@@ -93,44 +122,24 @@ extern "C" ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, i
     const int64_t xbytes = T * (q81 ? K / 32 * 36 : K / 256 * 292);
     if (xbytes > static_cast<int64_t>(kNoAllocScratchBytes)) return GGQ_ERR_CAPACITY;
 
+    {  // refused before any launch: token groups shrink down to one token, so one token must fit
+        StreamShape sh;
+        int cu = 0, cb = 0, rs = 0;
+        if (plan_gemv_stream(f, K / fmt_qk(f) * fmt_bytes(f), 1, static_cast<int>(K), q81, &sh, &cu, &cb, &rs) ==
+            StreamPlan::kNone)
+            return GGQ_ERR_SHAPE;
+    }
     NoAllocDevice* d = nullptr;
     ggq_status st = device_setup(&d);
     if (st != GGQ_OK) return st;
 
-    // shared-memory plan of the streaming GEMV (same rule as the pooled call)
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_quantize(q81 ? 0 : 1, X, T, K, d->scratch, s) != cudaSuccess) return GGQ_ERR_CUDA;
     StreamParams p{};
     p.W = static_cast<const uint8_t*>(W);
     p.rowbytes = K / fmt_qk(f) * fmt_bytes(f);
     p.N = N;
     p.K = static_cast<int>(K);
-    p.xq = d->scratch;
-    p.xrows = static_cast<int>(T);
-    p.T = static_cast<int>(T);
-    p.Y = Y;
     p.err = nullptr;  // bounded-wait timeouts are not reported by this entry point
-    StreamShape sh;
-    bool fits = plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, q81, &sh);
-    if (!fits || sh.stages < 2) {  // long rows: streamed in chunks
-        StreamShape ch;
-        int cu = 0, cb = 0, rs = 0;
-        if (plan_stream_chunked(f, p.rowbytes, p.xrows, p.K, q81, &ch, &cu, &cb, &rs)) {
-            sh = ch;
-            p.chunk_units = cu;
-            p.chunk_bytes = cb;
-            p.row_slot = rs;
-            fits = true;
-        }
-    }
-    if (!fits) return GGQ_ERR_SHAPE;
-    p.stages = sh.stages;
-    p.stage_stride = sh.stride;
-    p.x_bytes = sh.x_bytes;
-    const int64_t tiles = (N + kTileRows - 1) / kTileRows;
-    const int grid = static_cast<int>(tiles < d->nsm ? tiles : d->nsm);
-    const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_quantize(q81 ? 0 : 1, X, T, K, d->scratch, s) != cudaSuccess) return GGQ_ERR_CUDA;
-    if (launch_stream(KIND_GEMV, f, nt, p, grid, sh.smem, s) != cudaSuccess) return GGQ_ERR_CUDA;
-    return GGQ_OK;
+    return launch_groups(f, p, d->scratch, T, Y, q81 ? K / 32 * 36 : K / 256 * 292, d->nsm, s);
 }

@@ -57,13 +57,23 @@ inline bool plan_stream_chunked(int f, int64_t rowbytes, int xrows, int K, bool 
     const int fixed = s->x_bytes + 2 * kMaxStages * 8 + 1024;
     const int avail = kSmemLimit - fixed;
     if (avail <= 0) return false;
+    // about six stages, but at least 32 units per chunk (one for every lane of
+    // a row's warp) while two stages still fit
+    const int g_lanes = (32 + gu - 1) / gu;
     int g = avail / 6 / kTileRows / gb;
-    if (g < 1) g = 1;
+    if (g < g_lanes) g = g_lanes;
     if (static_cast<int64_t>(g) * gb > rowbytes) g = static_cast<int>((rowbytes + gb - 1) / gb);
+    const auto slot_of = [&](int gg) {
+        const int cb = gg * gb;
+        return (rowbytes % 16 == 0 && cb % 16 == 0) ? cb : (cb + 15) / 16 * 16 + 16;
+    };
+    const auto stride_of = [&](int gg) {
+        return static_cast<int>((static_cast<size_t>(kTileRows) * slot_of(gg) + 16 + 127) / 128 * 128);
+    };
+    while (g > 1 && avail / stride_of(g) < 2) --g;
     const int cb = g * gb;
-    const bool aligned = rowbytes % 16 == 0 && cb % 16 == 0;
-    const int slot = aligned ? cb : (cb + 15) / 16 * 16 + 16;
-    s->stride = static_cast<int>((static_cast<size_t>(kTileRows) * slot + 16 + 127) / 128 * 128);
+    const int slot = slot_of(g);
+    s->stride = stride_of(g);
     s->stages = avail / s->stride;
     if (s->stages < 2) {
         if (f == F_Q6_K && !small_granule)
@@ -76,6 +86,32 @@ inline bool plan_stream_chunked(int f, int64_t rowbytes, int xrows, int K, bool 
     *chunk_bytes = cb;
     *row_slot = slot;
     return true;
+}
+
+// The streaming GEMV's plan for T tokens: whole-row stages when two fit; else
+// row chunks with at least a unit per lane; when the T tokens' staged
+// activations leave no room for that, kSplit: run the tokens as two groups
+// (T/2 and T - T/2), each planned the same way.  A single whole-row stage is
+// the last resort of one token.
+enum class StreamPlan { kNone, kRun, kSplit };
+
+inline StreamPlan plan_gemv_stream(int f, int64_t rowbytes, int T, int K, bool q81, StreamShape* sh,
+                                   int* chunk_units, int* chunk_bytes, int* row_slot) {
+    *chunk_units = *chunk_bytes = *row_slot = 0;
+    const bool whole = plan_stream(kTileRows * rowbytes, T, K, q81, sh);
+    if (whole && sh->stages >= 2) return StreamPlan::kRun;
+    StreamShape ch;
+    int cu = 0, cb = 0, rs = 0;
+    const bool chunked = plan_stream_chunked(f, rowbytes, T, K, q81, &ch, &cu, &cb, &rs);
+    if (T > 1 && (!chunked || cu < 32)) return StreamPlan::kSplit;
+    if (chunked) {
+        *sh = ch;
+        *chunk_units = cu;
+        *chunk_bytes = cb;
+        *row_slot = rs;
+        return StreamPlan::kRun;
+    }
+    return whole ? StreamPlan::kRun : StreamPlan::kNone;
 }
 
 }  // namespace ggq

@@ -179,12 +179,12 @@ ggq_status ggq_dequant(ggq_ctx* ctx, int w, const void* blocks, int64_t rows, in
  * ("MatmulBT", vllm.cpp PR #523 op 74; ggml_mul_mat_vec_a8 of FreeToken
  * PR #136).  X is quantized inside the call (Q8_1 for Q4_0, Q8_K otherwise)
  * into the scratch pool.  1 <= T <= 8.  K must be a multiple of the weight
- * block (32 or 256); Q8_K activations also need K % 256 == 0.  Rows of any
- * length are streamed (in row chunks when a 16-row tile does not fit twice in
- * shared memory); the T quantized activation rows are held whole in shared
- * memory, about 1.52 bytes per input per token, which bounds T x K: every
- * format runs K up to 18176 at T = 8, 36352 at T = 4, 73216 at T = 2 and
- * 146432 at T = 1; larger shapes return GGQ_ERR_SHAPE. */
+ * block (32 or 256); Q8_K activations also need K % 256 == 0.  Long rows
+ * stream in row chunks when a 16-row tile does not fit twice in shared memory;
+ * the quantized activations are held whole in shared memory (about 1.52 bytes
+ * per input per token), and when those of all T tokens leave too little room
+ * the tokens run in groups (each group streams the weights once).  Every
+ * format runs K up to 146432; larger K returns GGQ_ERR_SHAPE. */
 ggq_status ggq_mul_mat_vec(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
                            float* Y, void* stream);
 

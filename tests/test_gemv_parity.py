@@ -107,6 +107,10 @@ LONG_ROWS = [  # (fmt, N, K, T): rows too long for whole-row stages, streamed in
     ("Q6_K", 16 * 9 + 7, 18944, 1),    # 74 superblocks: 15540-byte rows
     ("Q6_K", 35, 18944, 4),
     ("MXFP4", 40, 23296, 2),           # 12376-byte rows
+    # the staged activations of all tokens do not fit: tokens run in groups
+    ("Q4_K", 29, 28672, 8),            # 4 + 4
+    ("Q6_K", 35, 18944, 8),
+    ("MXFP4", 40, 23296, 7),           # 3 + 4
 ]
 
 
@@ -123,13 +127,14 @@ def test_long_rows_stream_in_chunks(ctx, fmt, N, K, T):
     ctx.sync_status()
 
 
-def test_activations_too_large_for_shared_memory_are_refused(ctx):
-    # 8 tokens x 28672 inputs of staged activations exceed one SM's shared memory
-    K, T = 28672, 8
-    W = to_dev(syn.weights("Q4_K", 16, K, syn.rng(56, 0)))
+def test_rows_too_long_for_one_token_are_refused(ctx):
+    # one token's staged activations (about 1.52 bytes per input) plus two
+    # chunked stages no longer fit in one SM's shared memory beyond K = 146432
+    K, T = 147456, 1
+    W = to_dev(syn.weights("Q8_0", 16, K, syn.rng(56, 0)))
     xq = to_dev(orc.quantize("Q8_K", syn.activations(T, K, syn.rng(56, 1))))
     with pytest.raises(ggq.GGQError, match="SHAPE"):
-        ctx.mul_mat_vec_q("Q4_K", W, 16, K, xq, T)
+        ctx.mul_mat_vec_q("Q8_0", W, 16, K, xq, T)
     ctx.sync_status()
 
 
