@@ -690,8 +690,8 @@ def summarize_ncu(path):
         "csrc_hash": csrc_hash(),
         "command": "python bench.py --profile-case headline && ncu --metrics gpu__time_duration.sum,"
                    "dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:'k_stream|k_gemv_mma' "
-                   "--csv --log-file gpurun_out/traffic.csv python bench.py --profile-case headline && "
-                   "python bench.py --summarize-ncu gpurun_out/traffic.csv",
+                   f"--csv --log-file {path} python bench.py --profile-case headline && "
+                   f"python bench.py --summarize-ncu {path}",
         "mean_traffic_bytes": round(sum(o["dram_bytes"] for o in out) / len(out)),
         "mean_algorithmic_bytes": round(sum(o["algorithmic_bytes"] for o in out) / len(out)),
         "launches": out,
