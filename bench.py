@@ -602,6 +602,8 @@ def profile_case(args):
     """Small launch sequences for ncu captures (not a benchmark).
     gemv: 4 warm-up launches of a 14336 x 4096 GEMV at T=1, then one at T=1 and
           one at T=8, over 5 rotating weight copies (165 MB for Q4_K > L2).
+    longrow: the same for the 4096 x 14336 shape (rows streamed in chunks;
+          3 rotating copies, 187 MB for Q8_0).
     moe:  the MoE decode layer (128 experts, H 2048, I 768, Q4_K/Q6_K, top-8)
           at T tokens: 2 warm-up layers, then 1 layer.
     mxfp4: the MXFP4 expert layer (256 experts, H 4096, I 2048, top-8) at T
@@ -628,6 +630,18 @@ def profile_case(args):
             for f in FMTS:
                 for T in TOKENS:
                     ctx.mul_mat_vec_q(f, Ws[f], N, K, xq[T], T)
+    elif args.profile_case == "longrow":
+        # the 4096 x 14336 down-projection shape (rows streamed in chunks): 4 warm-up
+        # launches at T=1 over 3 rotating copies (> L2), then one at T=1 and one at T=8
+        fmt, NL, KL = args.fmt, 4096, 14336
+        Ws = [torch.from_numpy(syn.weights(fmt, NL, KL, syn.rng(1, 300 + i))).cuda() for i in range(3)]
+        ctx.reserve(max_tokens=8, max_k=KL)
+        xq = {T: ctx.quantize_act("Q8_K", torch.from_numpy(syn.activations(T, KL, syn.rng(1, 350 + T))).cuda())
+              for T in (1, 8)}
+        for i in range(4):
+            ctx.mul_mat_vec_q(fmt, Ws[i % 3], NL, KL, xq[1], 1)
+        ctx.mul_mat_vec_q(fmt, Ws[1], NL, KL, xq[1], 1)
+        ctx.mul_mat_vec_q(fmt, Ws[2], NL, KL, xq[8], 8)
     elif args.profile_case == "gemv":
         fmt = args.fmt
         Ws = [torch.from_numpy(syn.weights(fmt, N, K, syn.rng(1, i))).cuda() for i in range(5)]
@@ -710,7 +724,7 @@ def main():
     ap.add_argument("--impl", default="ggq", choices=["ggq", "reference"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["headline", "gemv", "moe", "mxfp4", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["headline", "gemv", "longrow", "moe", "mxfp4", "prefill"], default=None,
                     help="run a small launch sequence for an ncu capture instead of the benchmark")
     ap.add_argument("--fmt", default="Q4_K")
     ap.add_argument("--summarize-ncu", metavar="CSV", default=None,
