@@ -63,7 +63,8 @@ def test_half_encode_round_to_nearest_even_matches_numpy():
     # exact ties in the subnormal and normal ranges
     ties = (np.arange(1, 200, dtype=np.float64) + 0.5) * 2.0 ** -24
     xs = np.concatenate([xs, ties.astype(np.float32), -ties.astype(np.float32)])
-    ref = xs.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):  # values past 65519.99 round to infinity on purpose
+        ref = xs.astype(np.float16).view(np.uint16)
     got = np.array([orc.float_to_half(float(x)) for x in xs], dtype=np.uint16)
     assert np.array_equal(got, ref)
 
