@@ -248,6 +248,14 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
         return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld must be a multiple of %lld for %s", static_cast<long long>(K),
                     static_cast<long long>(ablk > fmt_qk(f) ? ablk : fmt_qk(f)), type_name(w));
     if (K > (1 << 20)) return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K too large");
+    {  // token groups shrink down to one token, so the call runs if one token fits: refuse before any launch
+        StreamShape sh;
+        int cu = 0, cb = 0, rs = 0;
+        if (plan_gemv_stream(f, w_row_bytes(f, K), 1, static_cast<int>(K), f == F_Q4_0, &sh, &cu, &cb, &rs) ==
+            StreamPlan::kNone)
+            return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: rows of K=%lld do not fit in shared memory",
+                        static_cast<long long>(K));
+    }
     return GGQ_OK;
 }
 
@@ -370,6 +378,42 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
 // MXFP4 routed expert kernels", Summary: 2-4 tokens go to direct kernels; 5
 // and above use expert-sorted tiles).
 constexpr int kDirectMaxTokens = 4;
+
+// Fixed shared memory of a direct-route kernel besides its ring and activations.
+constexpr int kDirectFixed = 2 * kMaxStages * 8 + static_cast<int>(sizeof(DirectPlan)) + 256;
+
+// Whether the layer's widths fit the shared-memory plans of the kernels that
+// would run it, checked before anything is enqueued: the refusal message, or
+// nullptr.  Direct route: 16 gate + 16 up rows of H per stage with x^ of the
+// tokens, and 16 down rows of I with h^ of the pairs; expert-sorted route: the
+// grouped int8 kernel's whole-row slots where the f16 / tcgen05 kernels (which
+// step through K) do not serve the format.
+const char* moe_width_refusal(int fg, int fd, int64_t H, int64_t I, int64_t T, int top_k) {
+    int smem = 0;
+    if (T <= kDirectMaxTokens) {
+        StreamShape sh;
+        if (!plan_stream(2 * kTileRows * w_row_bytes(fg, H), static_cast<int>(T), static_cast<int>(H), false, &sh,
+                         kDirectFixed))
+            return "moe_experts: H too wide for shared memory";
+        if (!plan_stream(kTileRows * w_row_bytes(fd, I), static_cast<int>(T * top_k), static_cast<int>(I), false,
+                         &sh, kDirectFixed))
+            return "moe_experts: I too wide for shared memory";
+        return nullptr;
+    }
+    if (!(fg == F_Q8_0 && I % 128 == 0) && !gmm_supported(fg)) {
+        GroupParams g{};
+        g.rowbytes = w_row_bytes(fg, H);
+        g.K = static_cast<int>(H);
+        if (!plan_group(g, 2, false, &smem)) return "moe_experts: H too wide for shared memory";
+    }
+    if (!(fd == F_Q4_K && H % 128 == 0) && !gmm_supported(fd)) {
+        GroupParams d{};
+        d.rowbytes = w_row_bytes(fd, I);
+        d.K = static_cast<int>(I);
+        if (!plan_group(d, 1, false, &smem)) return "moe_experts: I too wide for shared memory";
+    }
+    return nullptr;
+}
 
 ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
                       const float* X, const float* logits, const int32_t* ids_in, const float* w_in, int64_t T,
@@ -579,6 +623,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     if (top_k < 1 || top_k > 8 || E < top_k || E > 4096)
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: need 1 <= top_k <= 8 and top_k <= E <= 4096");
     if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
+    if (const char* why = moe_width_refusal(fg, fd, H, I, T, top_k)) return fail(c, GGQ_ERR_SHAPE, "%s", why);
     if (T > kDirectMaxTokens) return moe_sorted(c, w, E, H, I, top_k, X, logits, ids, weights, T, Y, dump, stream);
     const MoeScratch ms = moe_scratch(T, H, I, top_k);
     ggq_status s = need_scratch(c, ms.total);
@@ -605,7 +650,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     p.Y = Y;
     p.err = &c->ctrl->err;
     const int nt = pow2_tokens(T);
-    const int direct_fixed = 2 * kMaxStages * 8 + static_cast<int>(sizeof(DirectPlan)) + 256;
+    const int direct_fixed = kDirectFixed;
     // gate/up: 16 gate rows + the 16 matching up rows per stage; x^ of the T tokens
     {
         p.W = static_cast<const uint8_t*>(w->gate);

@@ -268,6 +268,17 @@ def test_moe_rejects_bad_arguments(ctx):
         ctx.moe_experts(w8, cfg["E"], cfg["H"], 700, 8, x, logits=lg)
     with pytest.raises(ggq.GGQError, match="SHAPE"):
         ctx.moe_experts(w8, cfg["E"], cfg["H"], cfg["I"], 9, x, logits=lg)
+    # widths beyond the kernels' shared-memory plans are refused before anything
+    # is enqueued (direct route, Q8_0 gate/up rows of H = 8192): Y keeps its bytes
+    dummy = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    wide = ctx.moe_weights("Q8_0", dummy, "Q8_0", dummy, "Q4_K", dummy)
+    xw = torch.zeros((1, 8192), dtype=torch.float32, device="cuda")
+    lgw = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+    yw = torch.full((1, 8192), 7.0, dtype=torch.float32, device="cuda")
+    with pytest.raises(ggq.GGQError, match="SHAPE"):
+        ctx.moe_experts(wide, 16, 8192, 256, 8, xw, logits=lgw, Y=yw)
+    torch.cuda.synchronize()
+    assert bool(torch.all(yw == 7.0))
     # an out-of-range routed id is caught on the device and reported
     ids = to_dev(np.array([[cfg["E"] + 3, 0, 1, 2, 3, 4, 5, 6]], np.int32))
     wts = to_dev(np.full((1, 8), 0.125, np.float32))
