@@ -52,7 +52,9 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
+            # GGQ_ORACLE_LIB: load another build of the oracle (the pin tests'
+            # mutation check runs them against deliberately broken builds)
+            L = ctypes.CDLL(os.environ.get("GGQ_ORACLE_LIB") or build())
             i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
             sig = {
                 "orc_set_threads": (None, [i32]),

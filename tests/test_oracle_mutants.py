@@ -1,0 +1,82 @@
+"""The oracle's pins catch plausible mistakes (CPU).
+
+Each case below plants one mistake in a copy of the oracle's C source -- a
+dropped term, a wrong sign, offset, bit index or byte index, a different
+rounding or tie rule -- builds that copy, and runs the pin tests
+(tests/test_oracle_pins.py) against it: at least one pin must fail.  The
+unmodified source, built the same way, must pass them all.  The mistakes are
+planted in the oracle only, on the CPU; nothing here touches the GPU path.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ggq_oracle.c")
+
+# (name, text in the source, replacement)
+MUTANTS = [
+    ("q4_0 offset", "return nib - 8;", "return nib - 7;"),
+    ("q4_k high scale bits from the wrong byte", "*sc = (sc12[s + 4] & 15) | ((sc12[s - 4] >> 6) << 4);",
+     "*sc = (sc12[s + 4] & 15) | ((sc12[s] >> 6) << 4);"),
+    ("q4_k min low bits", "*m = (sc12[s + 4] >> 4) | ((sc12[s] >> 6) << 4);",
+     "*m = (sc12[s + 4] & 15) | ((sc12[s] >> 6) << 4);"),
+    ("q5_k high bit index", "nib += 16 * ((b[16 + l] >> s) & 1);", "nib += 16 * ((b[16 + l] >> (s + 1)) & 1);"),
+    ("q6_k offset", "return (nib | (hi << 4)) - 32;", "return (nib | (hi << 4)) - 31;"),
+    ("q6_k high bits", "int hi = (qh[32 * h + l] >> (2 * g)) & 3;", "int hi = (qh[32 * h + l] >> (2 * g + 1)) & 3;"),
+    ("e2m1 exponent", "ldexp(1.0 + 0.5 * m, e - 1);", "ldexp(1.0 + 0.5 * m, e);"),
+    ("quantizer ties to even", "float r = roundf(v);", "float r = rintf(v);"),
+    ("k-quant mins sign", "- orc_half_to_double(rd16(b + 2)) * c[1]", "+ orc_half_to_double(rd16(b + 2)) * c[1]"),
+    ("k-quant mins: one bsum dropped",
+     "B += m * (rds16(xb + 260 + 2 * (2 * s)) + rds16(xb + 260 + 2 * (2 * s + 1)));",
+     "B += m * rds16(xb + 260 + 2 * (2 * s));"),
+    ("q6_k scale index", "A += (int8_t)b[192 + g] * S;", "A += (int8_t)b[192 + (g ^ 1)] * S;"),
+    ("router ties to the higher index", "if (best < 0 || l[e] > l[best]) best = e;",
+     "if (best < 0 || l[e] >= l[best]) best = e;"),
+    ("router without renormalisation", "for (int j = 0; j < k; ++j) weights[t * k + j] /= psel;", ""),
+    ("silu sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("combine without the routing weight", "s += weights[t * k + j] * o[(t * k + j) * H + n];",
+     "s += o[(t * k + j) * H + n];"),
+    ("q8_k sub-block offset", "qx = (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 32);",
+     "qx = (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 16);"),
+    ("fp16 subnormal scale", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -23);"),
+]
+
+
+def _build(text, path):
+    src = path + ".c"
+    with open(src, "w") as f:
+        f.write(text)
+    r = subprocess.run(["gcc", "-O1", "-std=gnu99", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                        "-fno-strict-aliasing", "-I", os.path.join(ROOT, "oracle"), src, "-o", path, "-lm"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return path
+
+
+def _pins_pass(lib_path):
+    env = dict(os.environ, GGQ_ORACLE_LIB=lib_path)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode == 0, r.stdout[-1500:]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+def test_unmodified_oracle_passes_the_pins(source, tmp_path):
+    ok, out = _pins_pass(_build(source, str(tmp_path / "liborc_ref.so")))
+    assert ok, out
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_a_planted_mistake_fails_a_pin(source, tmp_path, name, old, new):
+    assert source.count(old) == 1, f"mutation site of '{name}' not found once in the oracle source"
+    ok, out = _pins_pass(_build(source.replace(old, new), str(tmp_path / "liborc_mut.so")))
+    assert not ok, f"no pin caught the planted mistake '{name}'"
