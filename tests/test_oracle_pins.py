@@ -278,6 +278,9 @@ def test_quantizer_invariants(act):
                 d, s, q = _q8_1_fields(b)
                 assert d == np.float16(d32)
                 assert s == np.float16(np.float32(d32 * np.float32(q.sum())))
+                # independent of that formula: s stands for the block's sum, so it lies
+                # within the 32 quantization errors (and its own fp16 rounding) of sum(x)
+                assert abs(float(s) - xs.sum()) <= 16 * float(d32) * (1 + 1e-5) + abs(float(s)) * 2.0 ** -11 + 1e-7
             assert np.all(np.abs(q) <= 127)
             if amax == 0:
                 assert np.all(q == 0) and float(d) == 0.0
