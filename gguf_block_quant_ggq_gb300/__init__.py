@@ -101,9 +101,19 @@ def act_type(wfmt: str) -> str:
     return "Q8_1" if wfmt == "Q4_0" else "Q8_K"
 
 
-def _ptr(t):
+def _ptr(t, dtype: str | None = None):
+    """Device address of a torch CUDA tensor (None passes NULL).  The C calls
+    read and write dense rows from that address, so the tensor must be on a
+    CUDA device and contiguous; `dtype` (a torch dtype name) is checked where
+    the call has a fixed element type.  Packed weight blocks may have any dtype."""
     if t is None:
         return None
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"libggq takes CUDA tensors (device memory), got one on {getattr(t, 'device', type(t))}")
+    if not t.is_contiguous():
+        raise ValueError("libggq reads and writes dense rows: pass a contiguous tensor")
+    if dtype is not None and str(t.dtype) != "torch." + dtype:
+        raise ValueError(f"expected a {dtype} tensor, got {t.dtype}")
     return t.data_ptr()
 
 
@@ -159,13 +169,14 @@ class Context:
         T, K = x.shape
         if out is None:
             out = self._torch.empty((T, row_bytes(act, K)), dtype=self._torch.uint8, device=x.device)
-        self._check(load().ggq_quantize_act(self.handle, TYPE[act], _ptr(x), T, K, _ptr(out), self._stream(stream)))
+        self._check(load().ggq_quantize_act(self.handle, TYPE[act], _ptr(x, "float32"), T, K, _ptr(out, "uint8"),
+                                            self._stream(stream)))
         return out
 
     def dequant(self, fmt: str, blocks, rows: int, K: int, out=None, stream=None):
         if out is None:
             out = self._torch.empty((rows, K), dtype=self._torch.float32, device=blocks.device)
-        self._check(load().ggq_dequant(self.handle, TYPE[fmt], _ptr(blocks), rows, K, _ptr(out),
+        self._check(load().ggq_dequant(self.handle, TYPE[fmt], _ptr(blocks), rows, K, _ptr(out, "float32"),
                                        self._stream(stream)))
         return out
 
@@ -175,14 +186,14 @@ class Context:
             Y = self._torch.empty((T, N), dtype=self._torch.float32, device=X.device)
         if reserve:
             self.reserve(max_tokens=T, max_k=K, stream=stream)
-        self._check(load().ggq_mul_mat_vec(self.handle, TYPE[fmt], _ptr(W), N, K, _ptr(X), T, _ptr(Y),
-                                           self._stream(stream)))
+        self._check(load().ggq_mul_mat_vec(self.handle, TYPE[fmt], _ptr(W), N, K, _ptr(X, "float32"), T,
+                                           _ptr(Y, "float32"), self._stream(stream)))
         return Y
 
     def mul_mat_vec_q(self, fmt: str, W, N: int, K: int, Xq, T: int, Y=None, stream=None):
         if Y is None:
             Y = self._torch.empty((T, N), dtype=self._torch.float32, device=Xq.device)
-        self._check(load().ggq_mul_mat_vec_q(self.handle, TYPE[fmt], _ptr(W), N, K, _ptr(Xq), T, _ptr(Y),
+        self._check(load().ggq_mul_mat_vec_q(self.handle, TYPE[fmt], _ptr(W), N, K, _ptr(Xq), T, _ptr(Y, "float32"),
                                              self._stream(stream)))
         return Y
 
@@ -208,11 +219,12 @@ class Context:
             d = ggq_moe_dump(**{k: _ptr(v) for k, v in dump.items()})
         dp = ctypes.byref(d) if d is not None else None
         if logits is not None:
-            st = load().ggq_moe_experts(self.handle, ctypes.byref(weights), E, H, I, top_k, _ptr(X), _ptr(logits), T,
-                                        _ptr(Y), dp, self._stream(stream))
+            st = load().ggq_moe_experts(self.handle, ctypes.byref(weights), E, H, I, top_k, _ptr(X, "float32"),
+                                        _ptr(logits, "float32"), T, _ptr(Y, "float32"), dp, self._stream(stream))
         else:
-            st = load().ggq_moe_experts_routed(self.handle, ctypes.byref(weights), E, H, I, top_k, _ptr(X),
-                                               _ptr(ids), _ptr(route_w), T, _ptr(Y), dp, self._stream(stream))
+            st = load().ggq_moe_experts_routed(self.handle, ctypes.byref(weights), E, H, I, top_k, _ptr(X, "float32"),
+                                               _ptr(ids, "int32"), _ptr(route_w, "float32"), T, _ptr(Y, "float32"),
+                                               dp, self._stream(stream))
         self._check(st)
         return Y
 

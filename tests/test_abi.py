@@ -58,3 +58,12 @@ def test_null_context_is_rejected_without_touching_a_device(lib):
     assert lib.ggq_reserve(None, None, None) == 1
     assert lib.ggq_destroy(None) == 1
     assert lib.ggq_last_error(None) == b"null context"
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    # the C calls take device pointers: a host tensor is refused by the binding
+    # itself, before any pointer reaches the library; None passes NULL
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        ggq._ptr(torch.zeros(4))
+    assert ggq._ptr(None) is None
