@@ -55,7 +55,8 @@ class ggq_moe_weights(ctypes.Structure):
 
 
 class ggq_moe_dump(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("ids", "weights", "xq", "g", "u", "h", "hq", "o")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("ids", "weights", "xq", "g", "u", "h", "hq", "o", "coefs_gate",
+                                               "coefs_up", "coefs_down")]
 
 
 class GGQError(RuntimeError):

@@ -27,6 +27,8 @@ cudaError_t launch_gemv_b(int kind, int fmt, int nt, const StreamParams& p, int 
 cudaError_t launch_direct_gateup(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_down(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_downf(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_direct_gateup_dump(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_direct_down_dump(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
     if (fmt == F_Q4_0 || fmt == F_Q8_0 || fmt == F_MXFP4) return launch_gemv_a(kind, fmt, nt, p, grid, smem, s);
@@ -223,10 +225,25 @@ bool plan_group(GroupParams& p, int nmat, bool resident_x, int* smem) {
     return true;
 }
 
-ggq_status check_ctx(ggq_ctx* c) {
+// Makes the context's device current for one call and puts the caller's
+// device back when the call returns.
+struct DeviceScope {
+    int prev = -1;
+    ~DeviceScope() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+ggq_status check_ctx(ggq_ctx* c, DeviceScope& scope) {
     if (!c) return GGQ_ERR_INVALID_ARG;
-    cudaError_t e = cudaSetDevice(c->device);
-    if (e != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+    if (cur != c->device) {
+        e = cudaSetDevice(c->device);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
+        scope.prev = cur;
+    }
     return GGQ_OK;
 }
 
@@ -289,7 +306,9 @@ constexpr int kMmaMinTokens = 2;
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st) {
     const int f = fmt_of(w);
-    if (kind == KIND_GEMV && T >= kMmaMinTokens && f != F_Q4_0 && aligned16(Xq)) {
+    const bool dump = kind == KIND_DUMP;
+    const int ncoef = static_cast<int>(K / fmt_qk(f) * fmt_coefs(f));
+    if (T >= kMmaMinTokens && f != F_Q4_0 && aligned16(Xq)) {
         MmavParams m{};
         m.W = static_cast<const uint8_t*>(W);
         m.rowbytes = w_row_bytes(f, K);
@@ -301,16 +320,24 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
         m.Y = Y;
         m.err = &c->ctrl->err;
         m.early_weights = c->static_weights;
+        m.coefs = coefs;
+        m.ncoef = ncoef;
         int smem = 0;
         if (plan_mmav(f, m, &smem)) {
             const int64_t tiles = (N + kTileRows - 1) / kTileRows;
             const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
-            cudaError_t e = launch_mmav(f, m, grid, smem, st);
+            cudaError_t e = cudaSuccess;
+            if (dump) {  // superblock coefficients of several warps are added atomically
+                e = cudaMemsetAsync(coefs, 0, static_cast<size_t>(T) * N * ncoef * 4, st);
+                if (e == cudaSuccess) e = launch_mmav_dump(f, m, grid, smem, st);
+            } else {
+                e = launch_mmav(f, m, grid, smem, st);
+            }
             if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec tensor-path launch");
             return GGQ_OK;
         }
     }
-    if (kind == KIND_GEMV && T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
+    if (T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
         // several activation columns: the int8 tensor-core kernel (Q8_K rows are 16-byte multiples)
         GroupParams g{};
         g.W = static_cast<const uint8_t*>(W);
@@ -323,11 +350,19 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
         g.Y = Y;
         g.err = &c->ctrl->err;
         g.early_weights = c->static_weights;
+        g.coefs[0] = coefs;
+        g.ncoef = ncoef;
         int smem = 0;
         if (plan_group(g, 1, true, &smem)) {
             const int64_t tiles = (N + kGroupRows - 1) / kGroupRows;
             const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
-            cudaError_t e = launch_group(G_GEMV, f, g, grid, smem, st);
+            cudaError_t e = cudaSuccess;
+            if (dump) {  // block dots: the dump variant writes no Y (g.Y is null)
+                e = cudaMemsetAsync(coefs, 0, static_cast<size_t>(T) * N * ncoef * 4, st);
+                if (e == cudaSuccess) e = launch_group_dump(G_GEMV, f, g, grid, smem, st);
+            } else {
+                e = launch_group(G_GEMV, f, g, grid, smem, st);
+            }
             if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec grouped launch");
             return GGQ_OK;
         }
@@ -419,6 +454,10 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
                       const float* X, const float* logits, const int32_t* ids_in, const float* w_in, int64_t T,
                       float* Y, const ggq_moe_dump* dump, void* stream) {
     const int fg = fmt_of(w->gate_type), fd = fmt_of(w->down_type);
+    int32_t* const cg = dump ? dump->coefs_gate : nullptr;  // integer-core dumps (gate and up go together)
+    int32_t* const cu = dump ? dump->coefs_up : nullptr;
+    int32_t* const cd = dump ? dump->coefs_down : nullptr;
+    const int ncg = static_cast<int>(H / fmt_qk(fg) * fmt_coefs(fg)), ncd = static_cast<int>(I / fmt_qk(fd) * fmt_coefs(fd));
     const SortedScratch ms = sorted_scratch(T, E, H, I, top_k);
     ggq_status s = need_scratch(c, ms.total);
     if (s != GGQ_OK) return s;
@@ -502,7 +541,10 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         float* const ubuf = dump && dump->u ? dump->u : reinterpret_cast<float*>(base + ms.u);
         t.out[0] = gbuf;
         t.out[1] = ubuf;
-        e = launch_gmmtc(F_Q8_0, t, c->nsm, st);
+        t.coefs[0] = cg;
+        t.coefs[1] = cu;
+        t.ncoef = ncg;
+        e = cg ? launch_gmmtc_dump(F_Q8_0, t, c->nsm, st) : launch_gmmtc(F_Q8_0, t, c->nsm, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
         e = launch_quantize_silu(gbuf, ubuf, P, I, hq, hp, dump ? dump->h : nullptr, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: SwiGLU quantize launch");
@@ -519,10 +561,17 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         q.h = h;
         q.g_dump = g.g_dump;
         q.u_dump = g.u_dump;
-        e = launch_gmm(G_GATEUP, fg, q, c->nsm, gmm_smem_bytes(), st);
+        q.coefs[0] = cg;
+        q.coefs[1] = cu;
+        q.ncoef = ncg;
+        e = cg ? launch_gmm_dump(G_GATEUP, fg, q, c->nsm, gmm_smem_bytes(), st)
+               : launch_gmm(G_GATEUP, fg, q, c->nsm, gmm_smem_bytes(), st);
     } else {
         if (!plan_group(g, 2, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: H too wide for shared memory");
-        e = launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
+        g.coefs[0] = cg;
+        g.coefs[1] = cu;
+        g.ncoef = ncg;
+        e = cg ? launch_group_dump(G_GATEUP, fg, g, c->nsm, smem, st) : launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
     }
     if (!(fg == F_Q8_0 && I % 128 == 0)) {
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
@@ -542,6 +591,8 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     d.h = nullptr;
     d.g_dump = d.u_dump = nullptr;
     d.o = o;
+    d.coefs[0] = d.coefs[1] = cd;
+    d.ncoef = ncd;
     if (fd == F_Q4_K && H % 128 == 0) {
         // Q4_K down on tcgen05
         e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
@@ -560,7 +611,9 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         t.perm = g.perm;
         t.err = g.err;
         t.out[0] = t.out[1] = o;
-        e = launch_gmmtc(F_Q4_K, t, c->nsm, st);
+        t.coefs[0] = t.coefs[1] = cd;
+        t.ncoef = ncd;
+        e = cd ? launch_gmmtc_dump(F_Q4_K, t, c->nsm, st) : launch_gmmtc(F_Q4_K, t, c->nsm, st);
     } else if (gmm_supported(fd)) {
         e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
@@ -571,10 +624,13 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         q.N = H;
         q.K = static_cast<int>(I);
         q.o = o;
-        e = launch_gmm(G_DOWN, fd, q, c->nsm, gmm_smem_bytes(), st);
+        q.coefs[0] = q.coefs[1] = cd;
+        q.ncoef = ncd;
+        e = cd ? launch_gmm_dump(G_DOWN, fd, q, c->nsm, gmm_smem_bytes(), st)
+               : launch_gmm(G_DOWN, fd, q, c->nsm, gmm_smem_bytes(), st);
     } else {
         if (!plan_group(d, 1, false, &smem)) return fail(c, GGQ_ERR_SHAPE, "moe_experts: I too wide for shared memory");
-        e = launch_group(G_DOWN, fd, d, c->nsm, smem, st);
+        e = cd ? launch_group_dump(G_DOWN, fd, d, c->nsm, smem, st) : launch_group(G_DOWN, fd, d, c->nsm, smem, st);
     }
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: down launch");
     e = launch_combine(o, wts, static_cast<int>(T), top_k, H, Y, st);
@@ -614,6 +670,8 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     if (fg != fu)
         return fail(c, GGQ_ERR_UNSUPPORTED, "moe_experts: gate (%s) and up (%s) banks must share one format",
                     type_name(w->gate_type), type_name(w->up_type));
+    if (dump && (dump->coefs_gate == nullptr) != (dump->coefs_up == nullptr))
+        return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: coefs_gate and coefs_up are dumped together");
     if (!w->gate || !w->up || !w->down) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null bank");
     if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down) || !aligned16(X) || !aligned16(Y))
         return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: pointers must be 16-byte aligned");
@@ -647,6 +705,9 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     p.g_dump = dump ? dump->g : nullptr;
     p.u_dump = dump ? dump->u : nullptr;
     p.o_dump = dump ? dump->o : nullptr;
+    p.coefs[0] = dump ? dump->coefs_gate : nullptr;
+    p.coefs[1] = dump ? dump->coefs_up : nullptr;
+    p.ncoef = static_cast<int>(H / fmt_qk(fg) * fmt_coefs(fg));
     p.Y = Y;
     p.err = &c->ctrl->err;
     const int nt = pow2_tokens(T);
@@ -664,7 +725,8 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         p.stages = sh.stages;
         p.stage_stride = sh.stride;
         p.x_bytes = sh.x_bytes;
-        cudaError_t e = launch_direct_gateup(fg, nt, p, c->nsm, sh.smem, st);
+        cudaError_t e = p.coefs[0] ? launch_direct_gateup_dump(fg, nt, p, c->nsm, sh.smem, st)
+                                   : launch_direct_gateup(fg, nt, p, c->nsm, sh.smem, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe gate/up launch");
     }
     // down: 16-row output tile of every selected expert; h^ of the T*k pairs.
@@ -676,7 +738,10 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         p.rowbytes = w_row_bytes(fd, I);
         p.N = H;
         p.K = static_cast<int>(I);
-        const bool fused = !(dump && dump->o);
+        p.coefs[0] = dump ? dump->coefs_down : nullptr;
+        p.coefs[1] = nullptr;
+        p.ncoef = static_cast<int>(I / fmt_qk(fd) * fmt_coefs(fd));
+        const bool fused = !(dump && (dump->o || dump->coefs_down));
         StreamShape sh;
         int G = 1;
         if (fused) {
@@ -695,8 +760,9 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         p.stages = sh.stages;
         p.stage_stride = sh.stride;
         p.x_bytes = sh.x_bytes;
-        cudaError_t e = fused ? launch_direct_downf(fd, nt, p, c->nsm, sh.smem, st)
-                              : launch_direct_down(fd, nt, p, c->nsm, sh.smem, st);
+        cudaError_t e = fused         ? launch_direct_downf(fd, nt, p, c->nsm, sh.smem, st)
+                        : p.coefs[0] ? launch_direct_down_dump(fd, nt, p, c->nsm, sh.smem, st)
+                                     : launch_direct_down(fd, nt, p, c->nsm, sh.smem, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe down launch");
     }
     if (dump) {
@@ -726,6 +792,8 @@ ggq_status ggq_create(ggq_ctx** out, int device) {
     cudaError_t e = cudaGetDeviceProperties(&prop, device);
     if (e != cudaSuccess) return GGQ_ERR_CUDA;
     if (prop.major != 10 || prop.minor != 3) return GGQ_ERR_ARCH;
+    DeviceScope scope;
+    if (cudaGetDevice(&scope.prev) != cudaSuccess) return GGQ_ERR_CUDA;
     e = cudaSetDevice(device);
     if (e != cudaSuccess) return GGQ_ERR_CUDA;
     ggq_ctx* c = new ggq_ctx();
@@ -745,7 +813,8 @@ ggq_status ggq_create(ggq_ctx** out, int device) {
 
 ggq_status ggq_destroy(ggq_ctx* c) {
     if (!c) return GGQ_ERR_INVALID_ARG;
-    cudaSetDevice(c->device);
+    DeviceScope scope;
+    if (check_ctx(c, scope) != GGQ_OK) return GGQ_ERR_CUDA;
     for (void* p : c->retired) cudaFree(p);
     if (c->pool) cudaFree(c->pool);
     if (c->ctrl) cudaFree(c->ctrl);
@@ -764,7 +833,8 @@ ggq_status ggq_set_static_weights(ggq_ctx* c, int static_weights) {
 }
 
 ggq_status ggq_reserve(ggq_ctx* c, const ggq_plan* plan, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     if (!plan) return fail(c, GGQ_ERR_INVALID_ARG, "reserve: null plan");
     size_t need = 0;
@@ -810,7 +880,8 @@ int ggq_supported(int w, int act, int op) {
 }
 
 ggq_status ggq_quantize_act(ggq_ctx* c, int act, const float* x, int64_t T, int64_t K, void* out, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     if (act != GGQ_TYPE_Q8_1 && act != GGQ_TYPE_Q8_K)
         return fail(c, GGQ_ERR_UNSUPPORTED, "quantize_act: activation type %d (%s); supported: Q8_1, Q8_K", act,
@@ -829,7 +900,8 @@ ggq_status ggq_quantize_act(ggq_ctx* c, int act, const float* x, int64_t T, int6
 }
 
 ggq_status ggq_dequant(ggq_ctx* c, int w, const void* blocks, int64_t rows, int64_t K, float* out, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     const int f = fmt_of(w);
     if (f < 0)
@@ -847,7 +919,8 @@ ggq_status ggq_dequant(ggq_ctx* c, int w, const void* blocks, int64_t rows, int6
 
 ggq_status ggq_mul_mat_vec_q(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
                              float* Y, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     s = gemv_checks(c, w, W, N, K, Xq, T, Y);
     if (s != GGQ_OK) return s;
@@ -856,7 +929,8 @@ ggq_status ggq_mul_mat_vec_q(ggq_ctx* c, int w, const void* W, int64_t N, int64_
 
 ggq_status ggq_mul_mat_vec(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T,
                            float* Y, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     s = gemv_checks(c, w, W, N, K, X, T, Y);
     if (s != GGQ_OK) return s;
@@ -871,7 +945,8 @@ ggq_status ggq_mul_mat_vec(ggq_ctx* c, int w, const void* W, int64_t N, int64_t 
 
 ggq_status ggq_block_dots(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
                           int32_t* coefs, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     s = gemv_checks(c, w, W, N, K, Xq, T, coefs);
     if (s != GGQ_OK) return s;
@@ -881,7 +956,8 @@ ggq_status ggq_block_dots(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K
 ggq_status ggq_moe_experts(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
                            const float* X, const float* router_logits, int64_t T, float* Y, const ggq_moe_dump* dump,
                            void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     if (!router_logits) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null router_logits");
     return moe_run(c, w, E, H, I, top_k, X, router_logits, nullptr, nullptr, T, Y, dump, stream);
@@ -890,14 +966,16 @@ ggq_status ggq_moe_experts(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int6
 ggq_status ggq_moe_experts_routed(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I,
                                   int top_k, const float* X, const int32_t* ids, const float* weights, int64_t T,
                                   float* Y, const ggq_moe_dump* dump, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     if (!ids || !weights) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts_routed: null ids/weights");
     return moe_run(c, w, E, H, I, top_k, X, nullptr, ids, weights, T, Y, dump, stream);
 }
 
 ggq_status ggq_sync_status(ggq_ctx* c, void* stream) {
-    ggq_status s = check_ctx(c);
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(c, e, "sync_status: stream");
@@ -907,7 +985,9 @@ ggq_status ggq_sync_status(ggq_ctx* c, void* stream) {
     if (word != 0) {
         cudaMemset(&c->ctrl->err, 0, sizeof(int));
         return fail(c, GGQ_ERR_DEVICE, "device error word %d (%s)", word,
-                    word == DEV_ERR_TIMEOUT ? "a bounded wait ran out" : "invalid routing ids");
+                    word == DEV_ERR_TIMEOUT   ? "a bounded wait ran out"
+                    : word == DEV_ERR_BAD_IDS ? "a routed expert id out of range"
+                                              : "unknown device error");
     }
     return GGQ_OK;
 }

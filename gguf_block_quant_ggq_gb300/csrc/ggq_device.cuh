@@ -29,8 +29,8 @@ __host__ __device__ constexpr int fmt_bytes(int f) {
 __host__ __device__ constexpr int fmt_coefs(int f) { return (f == F_Q4_K || f == F_Q5_K) ? 2 : 1; }
 __host__ __device__ constexpr bool fmt_q81(int f) { return f == F_Q4_0; }
 
-// Device error word values.
-enum : int { DEV_OK = 0, DEV_ERR_TIMEOUT = 1 };
+// Device error word values (a bounded wait ran out; a routed expert id out of range).
+enum : int { DEV_OK = 0, DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_IDS = 2 };
 
 // ---------------------------------------------------------------- PTX
 

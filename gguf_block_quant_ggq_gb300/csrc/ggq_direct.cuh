@@ -23,6 +23,7 @@
 // Both kernels stream weights with the producer warp / mbarrier ring of the
 // streaming kernel and use its dp4a consumer (row_accumulate).
 #pragma once
+#include <atomic>
 #include "ggq_stream.cuh"
 
 namespace ggq {
@@ -242,11 +243,13 @@ struct DirectParams {
     float* Y;                    // down: [T][H]
     int* err;
     int stages, stage_stride, x_bytes;
+    int32_t* coefs[2];           // optional integer-core dump [T*k][N][ncoef]: gate and up, or down
+    int ncoef;                   // coefficients per row: K/blk * (2 for Q4_K/Q5_K, else 1)
 };
 
 // Gate/up (KIND_GATEUP), down with per-pair outputs (KIND_DOWN) or fused
 // down (KIND_DOWNF) of the direct route.
-template <int KIND, int F, int NT>
+template <int KIND, int F, int NT, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool DOWN = KIND != KIND_GATEUP;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     if (KIND == KIND_GATEUP && blockIdx.x == 0 && tid < P) {
         p.ids[tid] = plan->ids[tid];
         p.w[tid] = plan->wt[tid];
-        if (plan->bad && tid == 0) set_error(p.err, 2);
+        if (plan->bad && tid == 0) set_error(p.err, DEV_ERR_BAD_IDS);
     }
     const int tiles = static_cast<int>(p.N / kTileRows);
     const int nitems = KIND == KIND_GATEUP ? D * tiles : (D > 0 ? tiles : 0);
@@ -464,6 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                     if (p.g_dump) p.g_dump[o] = v;
                     if (p.u_dump) p.u_dump[o] = uval;
                 }
+                if constexpr (DUMP) {  // integer core of the gate and up rows for every pair on this expert
+                    for (int j = 0; j < np; ++j) {
+                        const int pr = plan->pair[u][j], tk = plan->tok[pr];
+                        const int64_t o = (static_cast<int64_t>(pr) * p.N + row) * p.ncoef;
+                        row_coefs_one<F>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, tk, p.coefs[0] + o, lane);
+                        row_coefs_one<F>(stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes), xs, tk,
+                                         p.coefs[1] + o, lane);
+                    }
+                }
             } else {
                 set_error(p.err, DEV_ERR_TIMEOUT);
             }
@@ -492,6 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                     const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = slot
                     const int slot = lane >> SH;
                     const int pp = slot < np ? xr[slot] : -1;
+                    if constexpr (DUMP) {  // integer core of this down row for every pair on the expert
+                        for (int j = 0; j < np; ++j) {
+                            const int pr = plan->pair[u][j];
+                            row_coefs_one<F>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, pr,
+                                             p.coefs[0] + (static_cast<int64_t>(pr) * p.N + row) * p.ncoef, lane);
+                        }
+                    }
                     if (pp >= 0 && (lane & ((1 << SH) - 1)) == 0 && p.o_dump) p.o_dump[static_cast<int64_t>(pp) * p.N + row] = v;
                     // move each slot's weighted value to the lane of its token
                     const float contrib = pp >= 0 ? plan->wt[pp] * v : 0.0f;
@@ -566,19 +585,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     }
 }
 
-template <int KIND, int F, int NT>
+template <int KIND, int F, int NT, bool DUMP = false>
 cudaError_t launch_direct_one(const DirectParams& p, int grid, int smem, cudaStream_t s) {
-    static bool attr_set[kMaxDevices] = {};
+    static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_direct<KIND, F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k_direct<KIND, F, NT, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_direct<KIND, F, NT>, dim3(grid), dim3(kThreads), smem, s, p);
+    return launch_pdl(k_direct<KIND, F, NT, DUMP>, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
 }  // namespace ggq

@@ -11,10 +11,10 @@
 // Q4_K codes enter already multiplied by their 6-bit sub-block scale
 // (sc * q <= 945, exact).  Every product is exact; Q8_0 partials are taken per
 // 32-block (|dot| < 2^19, exact) and scaled in f32 registers; Q4_K partials
-// accumulate over a 256-superblock (possible rounding beyond 2^24, relative
-// 2^-24) and take d, dmin and the activation scale at its end, the mins term
-// being one more f16 product of the 6-bit mins with the activations' exact
-// 16-group sums.
+// accumulate in two 128-wide chains per 256-superblock (|partial| <= 128 * 945
+// * 127 < 2^24: each chain holds its exact integer) and take d, dmin and the
+// activation scale at the superblock's end, the mins term being one more f16
+// product of the 6-bit mins with the activations' exact 16-group sums.
 //
 // Tiling: a work item is (expert, 64 weight rows, 128 columns); gate/up items
 // take 32 gate rows and the same 32 up rows (one weight box each), and the
@@ -47,6 +47,8 @@
 #pragma once
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
+
+#include <atomic>
 
 namespace ggq {
 
@@ -184,7 +186,31 @@ __device__ __forceinline__ GmmItem gmm_item(const GmmParams& p, const int* s_pre
     return r;
 }
 
-template <int KIND, int F>
+// Integer-core dump of a consumer warp's 32 x 32 tile: coefficient idx of each
+// of its outputs gets D (plus E when given: the second half-superblock chain),
+// each an exact integer held in f32.  Gate/up: m tile i of the warp is matrix i
+// (gate, up); down: both m tiles are rows of the one matrix.
+template <int KIND>
+__device__ __forceinline__ void dump_tile(const GmmParams& p, const float (&D)[2][4][4], const int (&pc)[4][2], int mt,
+                                          int wm, int g, int idx, const float (*E)[4][4] = nullptr) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int pair = pc[j][q & 1];
+                if (pair < 0) continue;
+                int v = __float2int_rn(D[i][j][q]);
+                if (E) v += __float2int_rn(E[i][j][q]);
+                const int m = KIND == G_GATEUP ? i : 0;
+                const int64_t row = KIND == G_GATEUP ? static_cast<int64_t>(mt) * 32 + wm * 16 + g + 8 * (q >> 1)
+                                                     : static_cast<int64_t>(mt) * kGmmBM + wm * 32 + 16 * i + g + 8 * (q >> 1);
+                p.coefs[m][(static_cast<int64_t>(pair) * p.N + row) * p.ncoef + idx] = v;
+            }
+}
+
+template <int KIND, int F, bool DUMP>
 __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ GmmParams p) {
     static_assert(F == F_Q8_0 || F == F_Q4_K, "grouped f16 GEMM formats");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -413,14 +439,17 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                     ldmatrix_x4(b_base + static_cast<uint32_t>((wn * 32 + 16 * jp + (lane & 7) + ((lane >> 4) << 3)) * 128 +
                                                                ((chunk ^ (lane & 7)) << 4)),
                                 bf[2 * jp][0], bf[2 * jp][1], bf[2 * jp + 1][0], bf[2 * jp + 1][1]);
-                // a fresh accumulator at the start of a 32-block (Q8_0) or of a superblock (Q4_K)
-                const bool fresh = F == F_Q8_0 ? (kk & 1) == 0 : (kk == 0 && (kt & 3) == 0);
+                // a fresh accumulator at the start of a 32-block (Q8_0) or of a 128-wide half
+                // superblock (Q4_K: first half in D, second half in T)
+                const bool fresh = F == F_Q8_0 ? (kk & 1) == 0 : (kk == 0 && (kt & 1) == 0);
+                const bool second = F == F_Q4_K && ((kt >> 1) & 1);
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        if (fresh) gmm_mma_z(D[i][j], af[i], bf[j][0], bf[j][1]);
-                        else gmm_mma(D[i][j], af[i], bf[j][0], bf[j][1]);
+                        float* const acc_c = second ? T[i][j] : D[i][j];
+                        if (fresh) gmm_mma_z(acc_c, af[i], bf[j][0], bf[j][1]);
+                        else gmm_mma(acc_c, af[i], bf[j][0], bf[j][1]);
                     }
                 if constexpr (F == F_Q8_0) {
                     if (kk & 1) {  // end of a 32-block: T (+)= D * d_w; the activation scale waits for the superblock
@@ -432,6 +461,7 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                             for (int hh = 0; hh < 2; ++hh)
                                 dw[i][hh] = ld_h(raw + static_cast<uint32_t>(tile_row<KIND>(wm * 32 + 16 * i + g + 8 * hh) * kGmmRaw + o0 + 34 * blk));
                         const bool first = blk == 0 && (kt & 3) == 0;
+                        if constexpr (DUMP) dump_tile<KIND>(p, D, pc, cur.mt, wm, g, 2 * kt + blk);
 #pragma unroll
                         for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -471,12 +501,16 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
                             amin[i][hh] = h2u(byte_pair(ml, t));      // k 2t, 2t+1: sub-block t
                             amin[i][2 + hh] = h2u(byte_pair(mh, t));  // k 2t+8, 2t+9: sub-block 4+t
                         }
+                    if constexpr (DUMP) dump_tile<KIND>(p, D, pc, cur.mt, wm, g, 2 * (kt >> 2), T);
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) acc[i][j][q] = fmaf(D[i][j][q], dd[i][q >> 1] * dv[j][q & 1], acc[i][j][q]);
+                            for (int q = 0; q < 4; ++q) {
+                                D[i][j][q] += T[i][j][q];  // the two exact half-superblock chains
+                                acc[i][j][q] = fmaf(D[i][j][q], dd[i][q >> 1] * dv[j][q & 1], acc[i][j][q]);
+                            }
                     const saddr bss = smem_addr(BSS(s));
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -486,6 +520,7 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
 #pragma unroll
                         for (int i = 0; i < 2; ++i) gmm_mma_z(D[i][j], amin[i], b0, b1);
                     }
+                    if constexpr (DUMP) dump_tile<KIND>(p, D, pc, cur.mt, wm, g, 2 * (kt >> 2) + 1);
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -530,19 +565,19 @@ __global__ void __launch_bounds__(kGmmThreads, 1) k_gmm(const __grid_constant__ 
     }
 }
 
-template <int KIND, int F>
+template <int KIND, int F, bool DUMP>
 cudaError_t launch_gmm_one(const GmmParams& p, int grid, int smem, cudaStream_t s) {
-    static bool attr_set[kMaxDevices] = {};
+    static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_gmm<KIND, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k_gmm<KIND, F, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_gmm<KIND, F>, dim3(grid), dim3(kGmmThreads), smem, s, p);
+    return launch_pdl(k_gmm<KIND, F, DUMP>, dim3(grid), dim3(kGmmThreads), smem, s, p);
 }
 
 }  // namespace ggq

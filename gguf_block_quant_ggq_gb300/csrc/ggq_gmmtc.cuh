@@ -10,10 +10,11 @@
 //     (|dot| < 2^19: exact in f32), so the weight block scale, which differs per
 //     row and block, is applied by the epilogue warps;
 //   * Q4_K: the codes already multiplied by their 6-bit sub-block scale
-//     (sc * q <= 945); one accumulator per 256-superblock (sums beyond 2^24 may
-//     round, relative 2^-24), and the mins term sum_j m_j * (16-group sums of x)
-//     is one more K = 16 MMA of the mins against the activations' exact group
-//     sums; the epilogue forms (D d - Dmin dmin) d_x once per superblock.
+//     (sc * q <= 945); one accumulator per 128-wide half superblock (|partial|
+//     <= 128 * 945 * 127 < 2^24: exact), and the mins term sum_j m_j * (16-group
+//     sums of x) is one more K = 16 MMA of the mins against the activations'
+//     exact group sums; the epilogue adds D d d_x after the first half and
+//     (D d - Dmin dmin) d_x after the second.
 //
 // Work item: (expert, matrix, 128 weight rows, 128 activation columns).  The
 // activation operand is f16 rows in expert-sorted order (one per (token,
@@ -192,7 +193,22 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
     return ok;
 }
 
-template <int F>
+// Integer-core dump of 32 accumulator columns of this thread's row: the exact
+// integer each holds goes to coefficient idx of the column's pair (added to
+// what is there with `add`: the second half of a Q4_K superblock).
+__device__ __forceinline__ void tc_dump32(const GmmTcParams& p, const TcItem& cur, int r, int col0, const float* v,
+                                          int idx, bool add) {
+    const int64_t row = static_cast<int64_t>(cur.mt) * kTcBM + r;
+    for (int j = 0; j < 32; ++j) {
+        const int col = col0 + j;
+        if (col >= cur.ncols) break;
+        int32_t* const q = p.coefs[cur.m] + (static_cast<int64_t>(p.perm[cur.y0 + col]) * p.N + row) * p.ncoef + idx;
+        const int iv = __float2int_rn(v[j]);
+        *q = add ? *q + iv : iv;
+    }
+}
+
+template <int F, bool DUMP>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__ GmmTcParams p) {
     static_assert(F == F_Q8_0 || F == F_Q4_K, "tcgen05 grouped GEMM: Q8_0 and Q4_K banks");
     constexpr bool Q8 = F == F_Q8_0;
@@ -295,7 +311,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (c >= kTcStages && !tc_wait(&empty[s], ((c / kTcStages) - 1) & 1, abort, p.err)) break;
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
-                mbar_arrive_expect_tx(&full[s], SM::kB + kRawTx + (sb_end ? SM::kDX + (Q8 ? 0 : kTcBN * 32) : 0));
+                const bool dx_load = Q8 ? sb_end : (kt & 1) == 1;  // Q4_K: at each half superblock's end
+                mbar_arrive_expect_tx(&full[s], SM::kB + kRawTx + (dx_load ? SM::kDX : 0) + (sb_end && !Q8 ? kTcBN * 32 : 0));
                 tc_tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
                 if constexpr (Q8) {
                     tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);
@@ -304,10 +321,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[0], x, cur.wrow, &full[s]);
                     tc_tma_2d(smem_addr(RAW(s)) + kQsOff, &p.tm_w[1], x + 16 + 32 * (kt & 3), cur.wrow, &full[s]);
                 }
-                if (sb_end) {
-                    tc_tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
-                    if constexpr (!Q8) tc_tma_2d(smem_addr(RAW(s)) + kBsOff, &p.tm_bs, (kt >> 2) * 16, cur.y0, &full[s]);
-                }
+                if (dx_load) tc_tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
+                if (!Q8 && sb_end) tc_tma_2d(smem_addr(RAW(s)) + kBsOff, &p.tm_bs, (kt >> 2) * 16, cur.y0, &full[s]);
             }
             __syncwarp();
         }
@@ -338,22 +353,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     __syncwarp();
                 }
             } else {
-                // one accumulator per superblock (4 k-steps), two buffers
-                const int sbi = c >> 2, db = sbi & 1;  // nk is a multiple of 4, so c and kt agree on (c & 3)
-                if ((kt & 3) == 0 && sbi >= 2 && !tc_wait(&tempty[db], ((sbi >> 1) - 1) & 1, abort, p.err)) ok = false;
-                if (ok && (kt & 3) == 3 && sbi >= 1 && !tc_wait(&tempty[db ^ 1], ((sbi - 1) >> 1) & 1, abort, p.err))
-                    ok = false;  // the mins region is single: superblock sbi - 1 must have been read
+                // one accumulator per half superblock (2 k-steps): buffer 0 takes the first
+                // halves, buffer 1 the second halves and, beside it, the mins term.  nk is a
+                // multiple of 4, so c and kt agree on (c & 3).  Waiting for buffer 1's previous
+                // drain also frees the single mins region (the epilogue reads both together).
+                const int hsi = c >> 1, db = hsi & 1;
+                if ((kt & 1) == 0 && hsi >= 2 && !tc_wait(&tempty[db], ((hsi >> 1) - 1) & 1, abort, p.err)) ok = false;
                 if (ok) {
                     tc_fence_after();
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + static_cast<uint64_t>(2 * kk),
-                                   bdesc + static_cast<uint64_t>(2 * kk), static_cast<uint32_t>((kt & 3) != 0 || kk != 0));
-                        if ((kt & 3) == 3) {
+                                   bdesc + static_cast<uint64_t>(2 * kk), static_cast<uint32_t>((kt & 1) != 0 || kk != 0));
+                        if ((kt & 3) == 3)
                             tc_mma(tmem + kDmin, umma_desc_sw128(smem_addr(min_a)), umma_desc_sw128(smem_addr(min_b)), 0u);
-                            tc_commit(&tfull[db]);
-                        }
+                        if ((kt & 1) == 1) tc_commit(&tfull[db]);
                         tc_commit(&aempty[a]);
                         tc_commit(&empty[s]);
                     }
@@ -494,6 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                         for (int h2 = 0; h2 < 2; ++h2) {
                             float v[32];
                             tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
+                            if constexpr (DUMP) tc_dump32(p, cur, r, col0 + 32 * h2, v, 2 * kt + b, false);
 #pragma unroll
                             for (int j = 0; j < 32; ++j) T[32 * h2 + j] = first ? v[j] * dw : fmaf(v[j], dw, T[32 * h2 + j]);
                         }
@@ -519,10 +535,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                             tmem_st32(ta, a);
                         }
                     }
-                } else if ((kt & 3) == 3) {
-                    // superblock end: acc += (D d - Dmin dmin) d_x
-                    const int sbi = c >> 2, db = sbi & 1;
-                    if (!tc_wait(&tfull[db], (sbi >> 1) & 1, abort, p.err)) { live = false; break; }
+                } else if ((kt & 1) == 1) {
+                    // half-superblock end: acc += D d d_x (first half) or (D d - Dmin dmin) d_x (second)
+                    const int hsi = c >> 1, db = hsi & 1;
+                    const bool second = (kt & 3) == 3;
+                    if (!tc_wait(&tfull[db], (hsi >> 1) & 1, abort, p.err)) { live = false; break; }
                     tc_fence_after();
                     const uint32_t dh = ld_s32(raw + static_cast<uint32_t>(r * 16));  // d, dmin of this row
                     const float dd = half_lo(dh), dm = half_hi(dh);
@@ -531,9 +548,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     for (int h2 = 0; h2 < 2; ++h2) {
                         float v[32], m[32], a[32];
                         tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
-                        tmem_ld32(lane_base + kDmin + static_cast<uint32_t>(col0 + 32 * h2), m);
+                        if (second) {
+                            tmem_ld32(lane_base + kDmin + static_cast<uint32_t>(col0 + 32 * h2), m);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) m[j] = 0.0f;
+                        }
+                        if constexpr (DUMP) {
+                            tc_dump32(p, cur, r, col0 + 32 * h2, v, 2 * (kt >> 2), second);
+                            if (second) tc_dump32(p, cur, r, col0 + 32 * h2, m, 2 * (kt >> 2) + 1, false);
+                        }
                         const uint32_t ta = lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2);
-                        if (kt == 3) {
+                        if (kt == 1) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) a[j] = 0.0f;
                         } else {

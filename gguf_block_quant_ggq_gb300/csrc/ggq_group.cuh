@@ -22,6 +22,8 @@
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
 
+#include <atomic>
+
 namespace ggq {
 
 __device__ __forceinline__ void group_sync() {
@@ -78,10 +80,12 @@ __device__ __forceinline__ int gx_s32(const GX& x, int c, int sb, int s) {
 
 // Accumulate superblock sb of rows g and g+8 (row addresses r0, r1) against
 // the chunk's columns into acc[4] = (row g, c0), (row g, c1), (row g+8, c0),
-// (row g+8, c1).
-template <int F>
+// (row g+8, c1).  With DUMP, dq[] are the coefficient rows of those four
+// outputs (null: no output) and receive the integer core of the superblock:
+// A and B (Q4_K/Q5_K), A (Q6_K) or the eight 32-block dots (Q8_0, MXFP4).
+template <int F, bool DUMP>
 __device__ __forceinline__ void group_superblock(saddr r0, saddr r1, int sb, const GX& x, int g, int tig,
-                                                 float* acc) {
+                                                 float* acc, int32_t* const* dq) {
     const int c0 = 2 * tig, c1 = 2 * tig + 1;
     const int zero[4] = {0, 0, 0, 0};
     if constexpr (F == F_Q4_K || F == F_Q5_K) {
@@ -138,6 +142,14 @@ __device__ __forceinline__ void group_superblock(saddr r0, saddr r1, int sb, con
                 iB[3] += mm1 * sbb;
             }
         }
+        if constexpr (DUMP) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (dq[q]) {
+                    dq[q][2 * sb] = iA[q];
+                    dq[q][2 * sb + 1] = iB[q];
+                }
+        }
         const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
         const float x0 = gx_d(x, c0, sb), x1 = gx_d(x, c1, sb);
         acc[0] += x0 * (d0 * static_cast<float>(iA[0]) - dm0 * static_cast<float>(iB[0]));
@@ -187,6 +199,11 @@ __device__ __forceinline__ void group_superblock(saddr r0, saddr r1, int sb, con
                 }
             }
         }
+        if constexpr (DUMP) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (dq[q]) dq[q][sb] = iA[q];
+        }
         const float d0 = ld_h(b0r + 208), d1 = ld_h(b1r + 208);
         const float x0 = gx_d(x, c0, sb), x1 = gx_d(x, c1, sb);
         acc[0] += static_cast<float>(iA[0]) * (x0 * d0);
@@ -232,6 +249,11 @@ __device__ __forceinline__ void group_superblock(saddr r0, saddr r1, int sb, con
             gx_b32(x, g, tig, sb, s, bb0, bb1);
             int d[4];
             mma_s8_k32(d, a, bb0, bb1, cinit);
+            if constexpr (DUMP) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (dq[q]) dq[q][blk] = d[q];
+            }
             acc[0] += static_cast<float>(d[0]) * (w0 * x0);
             acc[1] += static_cast<float>(d[1]) * (w0 * x1);
             acc[2] += static_cast<float>(d[2]) * (w1 * x0);
@@ -240,7 +262,7 @@ __device__ __forceinline__ void group_superblock(saddr r0, saddr r1, int sb, con
     }
 }
 
-template <int KIND, int F>
+template <int KIND, int F, bool DUMP>
 __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NMAT = KIND == G_GATEUP ? 2 : 1;
@@ -405,12 +427,28 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
             if (wready && xready) {
+                // dump: coefficient rows of this thread's outputs (rows g, g + 8; columns 2 tig, 2 tig + 1)
+                int32_t* dq[NMAT][4] = {};
+                if constexpr (DUMP) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int col = 2 * tig + (q & 1);
+                        const int64_t row = r0 + g + 8 * (q >> 1);
+                        if (col < x.ncols && row < p.N) {
+                            const int pos = off + ch * kGroupCols + col;
+                            const int64_t oc = KIND == G_GEMV ? pos : p.perm[pos];
+#pragma unroll
+                            for (int m = 0; m < NMAT; ++m) dq[m][q] = p.coefs[m] + (oc * p.N + row) * p.ncoef;
+                        }
+                    }
+                }
                 for (int sb = warp; sb < nsb; sb += kGroupConsumerWarps) {
 #pragma unroll
                     for (int m = 0; m < NMAT; ++m) {
                         const saddr rb = wslot + static_cast<uint32_t>(m * kGroupRows * p.wrow);
-                        group_superblock<F>(rb + static_cast<uint32_t>(g * p.wrow),
-                                            rb + static_cast<uint32_t>((g + 8) * p.wrow), sb, x, g, tig, acc[m]);
+                        group_superblock<F, DUMP>(rb + static_cast<uint32_t>(g * p.wrow),
+                                                  rb + static_cast<uint32_t>((g + 8) * p.wrow), sb, x, g, tig, acc[m],
+                                                  dq[m]);
                     }
                 }
             }
@@ -442,7 +480,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
                 if (col < x.ncols && grow < p.N && wready && xready) {
                     const int pos = off + ch * kGroupCols + col;
                     if constexpr (KIND == G_GEMV) {
-                        p.Y[static_cast<int64_t>(pos) * p.N + grow] = v[0];
+                        if (!DUMP || p.Y) p.Y[static_cast<int64_t>(pos) * p.N + grow] = v[0];
                     } else if constexpr (KIND == G_GATEUP) {
                         const int pair = p.perm[pos];
                         const float hval = __fmul_rn(__fdiv_rn(v[0], 1.0f + expf(-v[0])), v[NMAT - 1]);
@@ -466,19 +504,19 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
     }
 }
 
-template <int KIND, int F>
+template <int KIND, int F, bool DUMP>
 cudaError_t launch_group_one(const GroupParams& p, int grid, int smem, cudaStream_t s) {
-    static bool attr_set[kMaxDevices] = {};
+    static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_group<KIND, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k_group<KIND, F, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_group<KIND, F>, dim3(grid), dim3(kGroupThreads), smem, s, p);
+    return launch_pdl(k_group<KIND, F, DUMP>, dim3(grid), dim3(kGroupThreads), smem, s, p);
 }
 
 }  // namespace ggq

@@ -86,6 +86,8 @@ struct GroupParams {
     float* o;            // down [pairs][N]
     int* err;
     int early_weights;   // 1: stream weights before waiting for the previous kernel (GEMV only)
+    int32_t* coefs[2];   // integer-core dump per matrix: [columns or pairs][N][ncoef] (dump launches only)
+    int ncoef;           // coefficients per row: K/blk * (2 for Q4_K/Q5_K, else 1)
     // shared-memory plan
     int wstages, wslot, wrow, wcontig;  // weight ring: slots, slot bytes, row stride, one contiguous copy
     int xstages, xslot, xstride, xcopy; // activation ring: slots, slot bytes, row stride, bytes per row copy
@@ -112,6 +114,8 @@ struct MmavParams {
     int wrow;           // stride of a pair of rows in shared memory (padded)
     int chunk;          // inputs per consumer warp (64, 128 or 256)
     int nch;            // chunks (<= 16)
+    int32_t* coefs;     // integer-core dump [T][N][ncoef] (dump launches only; zeroed by the caller)
+    int ncoef;          // coefficients per row: K/blk * (2 for Q4_K/Q5_K, else 1)
 };
 
 // Expert-sorted grouped GEMM on f16 tensor cores (ggq_gmm.cuh): tiles of 64
@@ -142,6 +146,8 @@ struct GmmParams {
     float* u_dump;
     float* o;                 // down: o [pairs][N]
     int* err;
+    int32_t* coefs[2];        // integer-core dump per matrix [pairs][N][ncoef] (dump launches only)
+    int ncoef;                // coefficients per row: K/blk * (2 for Q4_K, else 1)
 };
 
 // Launch with the programmatic-dependent-launch attribute (the kernels call
@@ -167,7 +173,11 @@ cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int 
 cudaError_t launch_quantize(int act, const float* x, int64_t T, int64_t K, uint8_t* out, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t rows, int64_t K, float* out, cudaStream_t s);
 cudaError_t launch_group(int kind, int fmt, const GroupParams& p, int grid, int smem, cudaStream_t s);
+// The same kernel also writing its integer core to p.coefs (outputs unchanged).
+cudaError_t launch_group_dump(int kind, int fmt, const GroupParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_mmav(int fmt, const MmavParams& p, int grid, int smem, cudaStream_t s);
+// The same kernel writing its integer core to p.coefs instead of Y.
+cudaError_t launch_mmav_dump(int fmt, const MmavParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
                                     cudaStream_t s);
 cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
@@ -183,6 +193,8 @@ cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, i
 int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
                const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K);
 cudaError_t launch_gmm(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s);
+// The same kernel also writing its integer core to p.coefs (outputs unchanged).
+cudaError_t launch_gmm_dump(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s);
 // Row-major 2-D tensor map [dim1][dim0] (rows stride1 bytes apart); 0 or a CUresult.
 int encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1,
                    uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz);
@@ -207,10 +219,14 @@ struct GmmTcParams {
     const int* perm;      // sorted position -> pair
     float* out[2];        // per matrix: [pairs][N]
     int* err;
+    int32_t* coefs[2];    // integer-core dump per matrix [pairs][N][ncoef] (dump launches only)
+    int ncoef;            // coefficients per row: K/blk * (2 for Q4_K, else 1)
 };
 int gmmtc_encode(GmmTcParams& p, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
                  const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K);
 cudaError_t launch_gmmtc(int fmt, const GmmTcParams& p, int grid, cudaStream_t s);
+// The same kernel also writing its integer core to p.coefs (outputs unchanged).
+cudaError_t launch_gmmtc_dump(int fmt, const GmmTcParams& p, int grid, cudaStream_t s);
 // h = silu(g) * u row by row (optionally written to h_out), quantized to Q8_K rows at out + r * pitch.
 cudaError_t launch_quantize_silu(const float* g, const float* u, int64_t rows, int64_t K, uint8_t* out, int64_t pitch,
                                  float* h_out, cudaStream_t s);

@@ -7,17 +7,17 @@ namespace ggq {
 
 namespace {
 
+// The driver's tensor-map encoder, looked up once (a function-local static is
+// initialised exactly once even when several host threads get here together).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        tried = true;
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -63,19 +63,25 @@ int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t*
 int gmm_supported(int fmt) { return fmt == F_Q8_0 || fmt == F_Q4_K; }
 int gmm_smem_bytes() { return GmmSmem::kTotal; }
 
-template <int KIND>
+template <int KIND, bool DUMP>
 static cudaError_t launch_gmm_fmt(int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s) {
     switch (fmt) {
-    case F_Q8_0: return launch_gmm_one<KIND, F_Q8_0>(p, grid, smem, s);
-    case F_Q4_K: return launch_gmm_one<KIND, F_Q4_K>(p, grid, smem, s);
+    case F_Q8_0: return launch_gmm_one<KIND, F_Q8_0, DUMP>(p, grid, smem, s);
+    case F_Q4_K: return launch_gmm_one<KIND, F_Q4_K, DUMP>(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_gmm(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s) {
     if (smem != GmmSmem::kTotal) return cudaErrorInvalidValue;
-    return kind == G_GATEUP ? launch_gmm_fmt<G_GATEUP>(fmt, p, grid, smem, s)
-                            : launch_gmm_fmt<G_DOWN>(fmt, p, grid, smem, s);
+    return kind == G_GATEUP ? launch_gmm_fmt<G_GATEUP, false>(fmt, p, grid, smem, s)
+                            : launch_gmm_fmt<G_DOWN, false>(fmt, p, grid, smem, s);
+}
+
+cudaError_t launch_gmm_dump(int kind, int fmt, const GmmParams& p, int grid, int smem, cudaStream_t s) {
+    if (smem != GmmSmem::kTotal) return cudaErrorInvalidValue;
+    return kind == G_GATEUP ? launch_gmm_fmt<G_GATEUP, true>(fmt, p, grid, smem, s)
+                            : launch_gmm_fmt<G_DOWN, true>(fmt, p, grid, smem, s);
 }
 
 }  // namespace ggq

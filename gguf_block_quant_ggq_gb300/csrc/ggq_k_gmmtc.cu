@@ -1,6 +1,8 @@
 // ggq_k_gmmtc.cu -- tensor maps and launch of the tcgen05 grouped GEMM (Q8_0 and Q4_K banks).
 #include "ggq_gmmtc.cuh"
 
+#include <atomic>
+
 namespace ggq {
 
 int gmmtc_encode(GmmTcParams& p, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
@@ -24,25 +26,33 @@ int gmmtc_encode(GmmTcParams& p, int fmt, const uint8_t* W, const uint8_t* W2, i
     return r;
 }
 
-template <int F>
+template <int F, bool DUMP>
 static cudaError_t launch_gmmtc_one(const GmmTcParams& p, int grid, cudaStream_t s) {
-    static bool attr_set[kMaxDevices] = {};
+    static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_gmmtc<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<F>::kTotal);
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k_gmmtc<F, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<F>::kTotal);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_gmmtc<F>, dim3(grid), dim3(kTcThreads), TcSmem<F>::kTotal, s, p);
+    return launch_pdl(k_gmmtc<F, DUMP>, dim3(grid), dim3(kTcThreads), TcSmem<F>::kTotal, s, p);
 }
 
 cudaError_t launch_gmmtc(int fmt, const GmmTcParams& p, int grid, cudaStream_t s) {
     switch (fmt) {
-    case F_Q8_0: return launch_gmmtc_one<F_Q8_0>(p, grid, s);
-    case F_Q4_K: return launch_gmmtc_one<F_Q4_K>(p, grid, s);
+    case F_Q8_0: return launch_gmmtc_one<F_Q8_0, false>(p, grid, s);
+    case F_Q4_K: return launch_gmmtc_one<F_Q4_K, false>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gmmtc_dump(int fmt, const GmmTcParams& p, int grid, cudaStream_t s) {
+    switch (fmt) {
+    case F_Q8_0: return launch_gmmtc_one<F_Q8_0, true>(p, grid, s);
+    case F_Q4_K: return launch_gmmtc_one<F_Q4_K, true>(p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

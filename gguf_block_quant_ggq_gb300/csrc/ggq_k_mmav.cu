@@ -5,11 +5,11 @@ namespace ggq {
 
 cudaError_t launch_mmav(int fmt, const MmavParams& p, int grid, int smem, cudaStream_t s) {
     switch (fmt) {
-    case F_Q8_0: return launch_mmav_one<F_Q8_0>(p, grid, smem, s);
-    case F_Q4_K: return launch_mmav_one<F_Q4_K>(p, grid, smem, s);
-    case F_Q5_K: return launch_mmav_one<F_Q5_K>(p, grid, smem, s);
-    case F_Q6_K: return launch_mmav_one<F_Q6_K>(p, grid, smem, s);
-    case F_MXFP4: return launch_mmav_one<F_MXFP4>(p, grid, smem, s);
+    case F_Q8_0: return launch_mmav_one<F_Q8_0, false>(p, grid, smem, s);
+    case F_Q4_K: return launch_mmav_one<F_Q4_K, false>(p, grid, smem, s);
+    case F_Q5_K: return launch_mmav_one<F_Q5_K, false>(p, grid, smem, s);
+    case F_Q6_K: return launch_mmav_one<F_Q6_K, false>(p, grid, smem, s);
+    case F_MXFP4: return launch_mmav_one<F_MXFP4, false>(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(256) k_route_sorted(const float* __restrict__ 
             if (id >= 0 && id < E)
                 atomicAdd(&counts[id], 1);
             else
-                set_error(err, 2);
+                set_error(err, DEV_ERR_BAD_IDS);
         }
     }
 }

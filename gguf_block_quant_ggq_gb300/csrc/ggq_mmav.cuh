@@ -11,7 +11,11 @@
 //     sum of the block, which leaves the exact integer dot of each sub-block
 //     (Q6_K: each 16-group, whose own scale it needs) in D.  Block scales are
 //     applied in f32; the Q4_K/Q5_K mins term is one more f16 product.  On this
-//     part the f16 mma runs at four times the rate of the int8 one.
+//     part the f16 mma runs at four times the rate of the int8 one.  The
+//     scaled Q4_K codes accumulate in 128-wide chains and the Q5_K codes in
+//     64-wide chains (|partial| <= 128 * 945 * 127 and 64 * 1953 * 127, both
+//     below 2^24), so every chain holds its exact integer; the chains meet in
+//     the f32 epilogue.
 //   * Q8_0, MXFP4: mma.sync m16n8k32 on int8 (one 32-block per mma).
 //
 // Layout on the SM:
@@ -32,6 +36,8 @@
 #pragma once
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
+
+#include <atomic>
 
 namespace ggq {
 
@@ -212,10 +218,26 @@ __device__ __forceinline__ void k4_scale_words(uint32_t a0, uint32_t a1, uint32_
     }
 }
 
+// Integer-core dump of one thread's four outputs: coefficient rows of (row r0,
+// column c0), (r0, c1), (r1, c0), (r1, c1) in the [T][N][K/blk * c] array
+// (null where the output does not exist).  Per-superblock coefficients may be
+// split across warps (chunks below 256 inputs) and are added atomically into
+// a zeroed array; per-32-block coefficients have one owner and are stored.
+struct MmavDump {
+    int32_t* q[4];
+};
+
+__device__ __forceinline__ void dump_add(int32_t* row, int idx, int v) {
+    if (row) atomicAdd(row + idx, v);
+}
+__device__ __forceinline__ void dump_put(int32_t* row, int idx, int v) {
+    if (row) row[idx] = v;
+}
+
 // 16 x 8 partial of one chunk: rows (g, g+8) at r0/r1, columns (2t, 2t+1).
-template <int F>
+template <int F, bool DUMP>
 __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk, const MmaX& X, saddr cs, int t,
-                                           float* acc) {
+                                           float* acc, const MmavDump& dz) {
     const int sb = e0 >> 8;
     if constexpr (F == F_Q4_K || F == F_Q5_K) {
         // f16 operands: a code q placed in the mantissa of 1024.0 reads 1024 + q
@@ -260,9 +282,14 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         const __half2 k1024 = __halves2half2(__ushort_as_half(0xE400u), __ushort_as_half(0xE400u));  // -1024
         const __half2 k64 = __halves2half2(__ushort_as_half(0xD400u), __ushort_as_half(0xD400u));    // -64
         const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00u), __ushort_as_half(0x2C00u));  // 1/16
-        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // chain ci of i-step i: 64-wide (Q5_K) or 128-wide (Q4_K) runs of the chunk
+        constexpr int kChains = F == F_Q5_K ? 4 : 2;
+        float Dc[kChains][4];
+#pragma unroll
+        for (int ci = 0; ci < kChains; ++ci) Dc[ci][0] = Dc[ci][1] = Dc[ci][2] = Dc[ci][3] = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
+            float* const D = Dc[F == F_Q5_K ? i / 2 : i / 4];
             if (32 * i < chunk) {
                 const uint32_t q = QS + 32u * static_cast<uint32_t>((js0 + i) >> 1) + 4u * t;
                 const uint32_t w00 = ld_s32(b0 + q), w01 = ld_s32(b0 + q + 16);  // row g: bytes 4t.. and 16+4t..
@@ -309,6 +336,23 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
                 mma_f16(D, H[4], H[5], H[6], H[7], X.b[4 * i + 6], X.b[4 * i + 7]);
             }
         }
+        float D[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            D[q] = Dc[0][q] + Dc[1][q];
+            if constexpr (kChains == 4) D[q] += Dc[2][q] + Dc[3][q];
+        }
+        if constexpr (DUMP) {
+            const int sbi = e0 >> 8;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                int a = 0;
+#pragma unroll
+                for (int ci = 0; ci < kChains; ++ci) a += __float2int_rn(Dc[ci][q]);
+                dump_add(dz.q[q], 2 * sbi, a);
+                dump_add(dz.q[q], 2 * sbi + 1, __float2int_rn(DM[q]));
+            }
+        }
         const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
         acc[0] = X.dx0 * (d0 * D[0] - dm0 * DM[0]);
         acc[1] = X.dx1 * (d0 * D[1] - dm0 * DM[1]);
@@ -331,6 +375,7 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         uint32_t Mr = 0x64006400u;
         asm("" : "+r"(Mr));
         float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        int ia[4] = {0, 0, 0, 0};  // dump: sum_j sc_j S_j in int32 (each D is the exact S_j)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             if (128 * hh < chunk) {
@@ -366,9 +411,20 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
                         a[1] += sc0 * D[1];
                         a[2] += sc1 * D[2];
                         a[3] += sc1 * D[3];
+                        if constexpr (DUMP) {
+                            const int i0 = byte_s(sw0[sj >> 2], sj & 3), i1 = byte_s(sw1[sj >> 2], sj & 3);
+                            ia[0] += i0 * __float2int_rn(D[0]);
+                            ia[1] += i0 * __float2int_rn(D[1]);
+                            ia[2] += i1 * __float2int_rn(D[2]);
+                            ia[3] += i1 * __float2int_rn(D[3]);
+                        }
                     }
                 }
             }
+        }
+        if constexpr (DUMP) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dump_add(dz.q[q], sb, ia[q]);
         }
         const float d0 = ld_h(b0 + 208), d1 = ld_h(b1 + 208);
         acc[0] = a[0] * (X.dx0 * d0);
@@ -416,6 +472,10 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
                 }
                 int D[4];
                 mma_k32_s8(D, a0, a1, a2, a3, X.b[2 * i], X.b[2 * i + 1], c0, c1);
+                if constexpr (DUMP) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dump_put(dz.q[q], blk, D[q]);
+                }
                 acc[0] += static_cast<float>(D[0]) * (w0 * X.dx0);
                 acc[1] += static_cast<float>(D[1]) * (w0 * X.dx1);
                 acc[2] += static_cast<float>(D[2]) * (w1 * X.dx0);
@@ -425,7 +485,7 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
     }
 }
 
-template <int F>
+template <int F, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -526,7 +586,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (ready && active) {
             const saddr r0 = ring_s + static_cast<uint32_t>(s * p.stage_stride + g * p.wrow);  // tile row 2g
-            mmav_chunk<F>(r0, r0 + static_cast<uint32_t>(p.rowbytes), e0, p.chunk, X, smem_addr(cs), t, acc);
+            MmavDump dz{};
+            if constexpr (DUMP) {
+                // this thread's outputs: tile rows 2g, 2g + 1 and columns 2t, 2t + 1
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t row = static_cast<int64_t>(item) * kTileRows + 2 * g + (q >> 1);
+                    const int col = 2 * t + (q & 1);
+                    dz.q[q] = row < p.N && col < p.T ? p.coefs + (static_cast<int64_t>(col) * p.N + row) * p.ncoef
+                                                     : nullptr;
+                }
+            }
+            mmav_chunk<F, DUMP>(r0, r0 + static_cast<uint32_t>(p.rowbytes), e0, p.chunk, X, smem_addr(cs), t, acc, dz);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -548,24 +619,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
             v += __shfl_xor_sync(0xffffffffu, v, 2);
             const int row = o >> 3, col = o & 7;
             const int64_t grow = static_cast<int64_t>(item) * kTileRows + row;
-            if (q == 0 && col < p.T && grow < p.N && ready) p.Y[static_cast<int64_t>(col) * p.N + grow] = v;
+            if (!DUMP && q == 0 && col < p.T && grow < p.N && ready) p.Y[static_cast<int64_t>(col) * p.N + grow] = v;
         }
     }
 }
 
-template <int F>
+template <int F, bool DUMP>
 cudaError_t launch_mmav_one(const MmavParams& p, int grid, int smem, cudaStream_t s) {
-    static bool attr_set[kMaxDevices] = {};
+    static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_gemv_mma<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(k_gemv_mma<F, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_gemv_mma<F>, dim3(grid), dim3(kThreads), smem, s, p);
+    return launch_pdl(k_gemv_mma<F, DUMP>, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
 }  // namespace ggq

@@ -5,7 +5,10 @@
 // and quantizes X into the context's pool (grown by ggq_reserve).  This entry
 // point instead keeps the quantized activations in a fixed array in the
 // library's own device data segment, so it needs neither a context nor any
-// allocation.  The GEMV kernels are the same ones ggq_mul_mat_vec launches.
+// allocation.  It runs the quantizer and the dp4a streaming GEMV (with the
+// pooled call's shared-memory plans: whole rows, row chunks, token groups) at
+// every token count; the pooled call takes the tensor-path kernel at 2-8
+// tokens where that applies, so the two agree within the fp32 tolerance.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -22,6 +22,7 @@
 // Every wait is bounded; on timeout the kernel records an error word, drains
 // its own copies and returns.
 #pragma once
+#include <atomic>
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
 
@@ -230,6 +231,47 @@ __device__ __forceinline__ void row_coefs(saddr row, const XS& xs, int nslots, i
                             o[u >> 2] = A0;
                         }
                     }
+                }
+            }
+        }
+    }
+}
+
+// Integer coefficients of one staged row against one activation row (xrow)
+// into out[0 .. K/blk * c): the dp4a integer core of row_accumulate, for the
+// dumps of the kernels that use it.  Kept out of line so that the hot loops
+// do not carry its registers.
+template <int F>
+__device__ __noinline__ void row_coefs_one(saddr row, const XS& xs, int xrow, int32_t* out, int lane) {
+    const int nu = units_per_row(xs.K), nb32 = xs.K >> 5;
+    for (int u0 = 0; u0 < nu; u0 += 32) {
+        const int u = u0 + lane;
+        const bool valid = u < nu;
+        Unit un;
+        int xo[4];
+        int A0 = 0, A1 = 0;
+        if (valid) {
+            load_unit<F>(row, u, nb32, un);
+            unit_offsets<F>(u, xo);
+            unit_ints<F>(un, xo, xs, xrow, u, A0, A1);
+        }
+        if constexpr (fmt_qk(F) == 32) {
+            if (valid) {
+                out[2 * u] = A0;
+                if (2 * u + 1 < nb32) out[2 * u + 1] = A1;
+            }
+        } else {
+            // the four units of a superblock sit on four consecutive lanes
+            A0 += __shfl_xor_sync(0xffffffffu, A0, 1);
+            A1 += __shfl_xor_sync(0xffffffffu, A1, 1);
+            A0 += __shfl_xor_sync(0xffffffffu, A0, 2);
+            A1 += __shfl_xor_sync(0xffffffffu, A1, 2);
+            if (valid && (u & 3) == 0) {
+                if constexpr (fmt_coefs(F) == 2) {
+                    out[2 * (u >> 2)] = A0;
+                    out[2 * (u >> 2) + 1] = A1;
+                } else {
+                    out[u >> 2] = A0;
                 }
             }
         }
@@ -517,15 +559,15 @@ template <int KIND, int F, int NT>
 cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s) {
     // The dynamic shared-memory limit is a per-device function attribute: set it
     // on the first launch of each instantiation on each device (before capture).
-    static bool attr_set[kMaxDevices] = {};
+    static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(k_stream<KIND, F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     return launch_pdl(k_stream<KIND, F, NT>, dim3(grid), dim3(kThreads), smem, s, p);
 }

@@ -39,6 +39,8 @@
  *     message of the last error is ggq_last_error(ctx).  A call that returns
  *     an error has enqueued nothing.
  *   - Calls on one context are not thread-safe with each other.
+ *   - A call that takes a context runs on the context's device and leaves the
+ *     calling thread's current device as it found it.
  */
 #ifndef GGQ_H
 #define GGQ_H
@@ -105,7 +107,16 @@ typedef struct ggq_moe_weights {
 
 /* Optional device buffers that receive the MoE intermediates (any may be NULL).
  * For tests and debugging; filling them costs extra stores.  Slot j of token t
- * is pair p = t*k + j. */
+ * is pair p = t*k + j.
+ * The coefs_* arrays receive the integer core of the kernels that ran the
+ * layer: for each pair, each output row and each weight block, the int32
+ * coefficients that multiply the block's scale product, laid out
+ * [T*k][rows][K/blk * c] exactly as ggq_block_dots writes them (rows = I for
+ * gate/up, H for down; K = H for gate/up, I for down; c = 2 for Q4_K/Q5_K,
+ * else 1).  They are written by the same launches that compute the outputs
+ * (the kernels take a dump variant that also stores what their dp4a or
+ * tensor-core integer sums hold); entries of pairs that do not exist are not
+ * written. */
 typedef struct ggq_moe_dump {
     int32_t* ids;    /* [T][k]   selected experts                         */
     float* weights;  /* [T][k]   renormalised routing weights             */
@@ -115,6 +126,9 @@ typedef struct ggq_moe_dump {
     float* h;        /* [T*k][I] silu(g) * u                               */
     void* hq;        /* [T*k][I/256] Q8_K blocks of h                      */
     float* o;        /* [T*k][H] down outputs before the routing weight   */
+    int32_t* coefs_gate; /* [T*k][I][H/blk * c] gate integer core          */
+    int32_t* coefs_up;   /* [T*k][I][H/blk * c] up integer core            */
+    int32_t* coefs_down; /* [T*k][H][I/blk * c] down integer core (h^)     */
 } ggq_moe_dump;
 
 /* Create a context on `device` (a CUDA ordinal).  Refuses any device that is
@@ -201,7 +215,13 @@ ggq_status ggq_mul_mat_vec_q(ggq_ctx* ctx, int w, const void* W, int64_t N, int6
  *   Q4_K/Q5_K x Q8_K (c = 2): A = sum_s sc_s S_s and B = sum_s m_s bsum_s per
  *     superblock, y += d_x (d A - dmin B);
  *   Q6_K x Q8_K (c = 1): A = sum_j sc_j S_j per superblock, y += d_x d A.
- * Runs the same device dot routines as the GEMV. */
+ * Runs the kernel that ggq_mul_mat_vec_q picks for the same (w, N, K, T) --
+ * the dp4a streaming kernel, the tensor-path GEMV (2-8 tokens) or the grouped
+ * int8 tensor-core kernel -- in a variant that stores the integers its dp4a or
+ * mma units produce instead of the outputs.  The tensor paths hold them in
+ * f32 accumulators; every such chain is short enough that its partial sums
+ * stay below 2^24, so the stored value is the exact integer.  out must be
+ * 4-byte aligned; the call clears it first. */
 ggq_status ggq_block_dots(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
                           int32_t* coefs, void* stream);
 
@@ -244,14 +264,21 @@ ggq_status ggq_moe_experts_routed(ggq_ctx* ctx, const ggq_moe_weights* w, int64_
  * device data, one per device that loads the library, held until the process
  * exits: T * (K/32 * 36) bytes for w = Q4_0, T * (K/256 * 292) otherwise, which
  * allows 8 tokens x 16384 inputs.  Larger shapes return GGQ_ERR_CAPACITY and
- * launch nothing.  Arguments, layouts and results are those of ggq_mul_mat_vec
- * on the CURRENT device; other errors: GGQ_ERR_UNSUPPORTED, _INVALID_ARG,
- * _SHAPE, _ARCH (not sm_103), _CUDA.  The first call on a device checks the
- * architecture and looks up the array's device address; make that first call
- * before any stream capture.  Every call on a device shares the one array and
- * it keeps the last call's contents: calls whose work overlaps on the GPU
- * (other streams, or other host threads) race on it, so order them on one
- * stream.  Bounded-wait timeouts inside the kernels are not reported here. */
+ * launch nothing.  Arguments and layouts are those of ggq_mul_mat_vec, on the
+ * CURRENT device; other errors: GGQ_ERR_UNSUPPORTED, _INVALID_ARG, _SHAPE,
+ * _ARCH (not sm_103), _CUDA.  Every token count runs on the dp4a streaming
+ * kernel, whereas ggq_mul_mat_vec takes the tensor-path kernel at 2-8 tokens
+ * where it applies: the two agree within the fp32 tolerance of the keep-quant
+ * dot (the integer dots are the same; the order of the fp32 sums is not).
+ * The first call on a device checks the architecture and looks up the
+ * array's device address; make that first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents: calls whose work overlaps on the GPU (other streams, or other
+ * host threads) race on it, so order them on one stream.  The kernels' waits
+ * are bounded (about two seconds each); one that runs out is not reported by
+ * this entry point, and the output rows of the tiles it gave up keep what Y
+ * held before -- callers who need that failure reported use ggq_mul_mat_vec
+ * and ggq_sync_status. */
 ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                                    void* stream);
 

@@ -69,7 +69,8 @@ def _case(fmt, N, K, T, seed):
 SHAPES = [  # (N, K, T): several 16-row tiles with a ragged tail; one and several superblocks
     (16 * 9 + 5, 1024, 1), (16 * 9 + 5, 1024, 2), (101, 512, 3), (67, 2048, 4), (33, 768, 5), (16 * 20 + 7, 1024, 8),
     (1, 256, 1), (17, 4096, 6), (50, 256, 7),
-    (16 * 11 + 3, 1024, 3), (40, 2048, 5), (16 * 9 + 9, 3072, 7),  # int8 tensor-core route (K % 1024 == 0)
+    (16 * 11 + 3, 1024, 3), (40, 2048, 5), (16 * 9 + 9, 3072, 7),
+    (37, 8192, 3), (16 * 5 + 3, 8192, 8),  # K beyond the tensor-path GEMV: the grouped int8 kernel
 ]
 Q4_0_ODD_SHAPES = [(21, 96, 2), (40, 32, 1), (35, 160, 8)]  # K % 64 == 32: a half 64-weight unit per row
 
@@ -91,6 +92,52 @@ def test_block_dots_bit_exact_and_gemv_within_tolerance(ctx, fmt, N, K, T):
     check_outputs(y_q, ref, absdot, f"{fmt} mul_mat_vec_q N={N} K={K} T={T}")
     y = to_host(ctx.mul_mat_vec(fmt, dW, N, K, to_dev(x)))
     check_outputs(y, ref, absdot, f"{fmt} mul_mat_vec N={N} K={K} T={T}")
+
+
+def _extreme_block(fmt, sign):
+    """One block of the largest integer products the format allows: every code
+    at its extreme, every 6-bit scale and min 63 (K-quants), scales 127 or -128
+    (Q6_K), fp16 scale 1.  With activations of one sign at +-127 each integer
+    dot reaches its bound (e.g. Q4_K: 256 * 945 * 127 > 2^24 per superblock)."""
+    bb = syn.BLOCK_BYTES[fmt]
+    b = np.zeros(bb, np.uint8)
+    one = np.array([1.0], np.float16).view(np.uint8)
+    if fmt == "Q4_0":
+        b[0:2], b[2:] = one, 0xFF if sign > 0 else 0x00
+    elif fmt == "Q8_0":
+        b[0:2], b[2:] = one, (0x7F if sign > 0 else 0x80)
+    elif fmt == "MXFP4":
+        b[0], b[1:] = 127, (0x77 if sign > 0 else 0xFF)  # E2M1 codes 7 (6.0) or 15 (-6.0)
+    elif fmt in ("Q4_K", "Q5_K"):
+        b[0:2], b[2:4], b[4:] = one, np.array([0.0], np.float16).view(np.uint8), 0xFF
+    elif fmt == "Q6_K":
+        b[0:192] = 0xFF if sign > 0 else 0x00  # codes 63 (31 after the offset) or 0 (-32)
+        b[192:208] = 127
+        b[208:210] = one
+    return b
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("T", [1, 2, 3, 8])
+def test_block_dots_exact_at_the_integer_bounds(ctx, fmt, T):
+    """Blocks at the formats' extremes against activations quantized to +-127:
+    the largest integer sums the kernels' accumulators can meet.  The tensor
+    paths hold them in f32 chains short enough to stay exact (below 2^24), so
+    the dumped coefficients equal the oracle's integers bit for bit."""
+    K = 8192 if T == 3 else 4096  # T = 3 at K = 8192 takes the grouped int8 kernel
+    N = 35
+    W = np.stack([np.tile(_extreme_block(fmt, 1 if (r % 3) else -1), K // syn.BLOCK_ELEMS[fmt]) for r in range(N)])
+    x = np.full((T, K), 3.0, np.float32)
+    x[:, 1::7] = -3.0  # a few negatives: mixed signs inside blocks, still quantized to +-127
+    if T > 1:
+        x[1] = 5.0  # one token of a single sign: the bound itself
+    xq = orc.quantize(orc.act_type(fmt), x)
+    dW, dxq = to_dev(W), to_dev(xq)
+    coefs = to_host(ctx.block_dots(fmt, dW, N, K, dxq, T))
+    ref_coefs = orc.gemv_coefs(fmt, W, N, K, xq, T)
+    assert np.array_equal(coefs, ref_coefs), f"{np.count_nonzero(coefs != ref_coefs)} coefficients differ"
+    ref, absdot = orc.gemv_dequant(fmt, W, N, K, xq, T)
+    check_outputs(to_host(ctx.mul_mat_vec_q(fmt, dW, N, K, dxq, T)), ref, absdot, f"{fmt} extremes T={T}")
 
 
 LONG_ROWS = [  # (fmt, N, K, T): rows too long for whole-row stages, streamed in row chunks

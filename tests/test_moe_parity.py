@@ -53,13 +53,27 @@ def _banks(cfg, E):
     return _BANKS[key]
 
 
-def _dump_buffers(T, k, H, I):
+def _ncoef(fmt, K):
+    return K // syn.BLOCK_ELEMS[fmt] * orc.coefs_per_block(fmt)
+
+
+COEF_BYTES_MAX = 1 << 30  # integer-core dumps larger than this are skipped (full-size prefill)
+
+
+def _dump_buffers(T, k, H, I, cfg=None):
     P = T * k
     z = lambda *s, dt=torch.float32: torch.full(s, -7, dtype=dt, device="cuda")  # noqa: E731
-    return {
+    d = {
         "ids": z(T, k, dt=torch.int32), "weights": z(T, k), "xq": z(T, H // 256 * 292, dt=torch.uint8),
         "g": z(P, I), "u": z(P, I), "h": z(P, I), "hq": z(P, I // 256 * 292, dt=torch.uint8), "o": z(P, H),
     }
+    if cfg is not None:
+        ng, nd = _ncoef(cfg["gate"], H), _ncoef(cfg["down"], I)
+        if 4 * P * (2 * I * ng + H * nd) <= COEF_BYTES_MAX:
+            d["coefs_gate"] = z(P, I, ng, dt=torch.int32)
+            d["coefs_up"] = z(P, I, ng, dt=torch.int32)
+            d["coefs_down"] = z(P, H, nd, dt=torch.int32)
+    return d
 
 
 def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
@@ -74,7 +88,7 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     logits = syn.router_logits(T, E, g, cfg.get("zipf"))
     ids_ref, w_ref = orc.router(logits, k)
     w8 = ctx.moe_weights(cfg["gate"], dev["gate"], cfg["up"], dev["up"], cfg["down"], dev["down"])
-    d = _dump_buffers(T, k, H, I)
+    d = _dump_buffers(T, k, H, I, cfg)
     if routed:
         y = ctx.moe_experts(w8, E, H, I, k, to_dev(x), ids=to_dev(ids_ref),
                             route_w=to_dev(w_ref.astype(np.float32)), dump=d)
@@ -94,8 +108,14 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     assert np.array_equal(r["xq"], xq)
     P = T * k
     pairs = np.array([t * k + j for t in toks for j in range(k)])
+    coefs = "coefs_gate" in r
     for p in pairs:
         t, e = p // k, int(ids_ref.flat[p])
+        if coefs:  # the gate/up kernels' own integer core, bit-exact
+            for m in ("gate", "up"):
+                cref = orc.gemv_coefs(cfg[m], host[m][e], I, H, xq[t:t + 1], 1)[0]
+                assert np.array_equal(r["coefs_" + m][p], cref), \
+                    f"{m} pair {p}: {np.count_nonzero(r['coefs_' + m][p] != cref)} integer coefficients differ"
         gref, gabs = orc.gemv_dequant(cfg["gate"], host["gate"][e], I, H, xq[t:t + 1], 1)
         uref, uabs = orc.gemv_dequant(cfg["up"], host["up"][e], I, H, xq[t:t + 1], 1)
         check_outputs(r["g"][p][None], gref, gabs, f"gate pair {p}")
@@ -110,6 +130,10 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     o_abs = np.zeros((P, H))
     for p in pairs:
         e = int(ids_ref.flat[p])
+        if coefs:  # the down kernel's integer core on the GPU's own h^, bit-exact
+            cref = orc.gemv_coefs(cfg["down"], host["down"][e], H, I, r["hq"][p:p + 1], 1)[0]
+            assert np.array_equal(r["coefs_down"][p], cref), \
+                f"down pair {p}: {np.count_nonzero(r['coefs_down'][p] != cref)} integer coefficients differ"
         oref, oabs = orc.gemv_dequant(cfg["down"], host["down"][e], H, I, r["hq"][p:p + 1], 1)
         check_outputs(r["o"][p][None], oref, oabs, f"down pair {p}")
         o_tf[p], o_abs[p] = oref[0], oabs[0]
@@ -129,7 +153,7 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     # (v'') with every dump but the per-pair down outputs, the layer takes the
     # same kernels as without dumps: routing, x^, g, u, h and h^ are
     # bit-identical to the fully dumped run above, and y to the run without dumps
-    d3 = {n: t for n, t in _dump_buffers(T, k, H, I).items() if n != "o"}
+    d3 = {n: t for n, t in _dump_buffers(T, k, H, I).items() if n != "o" and not n.startswith("coefs")}
     if routed:
         y3 = ctx.moe_experts(w8, E, H, I, k, to_dev(x), ids=to_dev(ids_ref), route_w=to_dev(w_ref.astype(np.float32)),
                              dump=d3)
@@ -159,6 +183,7 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     flips = int(np.count_nonzero(diff))
     assert flips <= 0.01 * nP * I, f"{flips} of {nP * I} h^ quants differ from the free-running oracle"
     nmse = float(np.sum((y[toks] - ref["y"]) ** 2) / np.sum(ref["y"] ** 2))
+    print(f"free-running: {flips} of {nP * I} h^ quants flipped at fp32 ties, NMSE {nmse:.3e}")
     assert nmse <= (1e-10 if flips == 0 else 1e-4), f"free-running NMSE {nmse:.3e} with {flips} flips"
     return flips
 
@@ -211,6 +236,13 @@ def test_moe_sorted_route_mxfp4(ctx, T):
     _run_and_check(ctx, syn.MOE_MXFP4, 32, T, sample_tokens=None if T <= 8 else 6)
 
 
+def test_moe_q5k_banks_sorted(ctx):
+    """Q5_K gate/up and down on the expert-sorted route (grouped int8 kernel)."""
+    cfg = dict(syn.MOE_DECODE)
+    cfg.update(E=16, gate="Q5_K", up="Q5_K", down="Q5_K")
+    _run_and_check(ctx, cfg, 16, 12, sample_tokens=5)
+
+
 @pytest.mark.parametrize("T", [5, 16])
 def test_moe_sorted_route_q4k_q6k(ctx, T):
     cfg = syn.MOE_DECODE
@@ -228,10 +260,13 @@ def test_moe_prefill_4096_tokens_zipf(ctx):
     _run_and_check(ctx, cfg, cfg["E"], cfg["T"][0], sample_tokens=5)
 
 
-def test_moe_mxfp4_full_bank_256_experts(ctx):
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 32, 128, 512])
+def test_moe_mxfp4_full_bank_256_experts(ctx, T):
+    """The MXFP4 workload at full size (256 experts, H 4096, I 2048, top-8) at
+    every token count it names: 1-4 on the direct route, 5 and up on
+    expert-sorted tiles; larger counts check the pairs of sampled tokens."""
     cfg = syn.MOE_MXFP4
-    for T in (1, 2):
-        _run_and_check(ctx, cfg, cfg["E"], T)
+    _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 5 else 6)
 
 
 def test_moe_all_experts_uniform_equals_dense(ctx):
