@@ -5,9 +5,17 @@ Headline workload (one "step"): the non-grouped K-quant GEMV, W = 14336 x 4096
 in each of Q8_0, Q4_K, Q5_K and Q6_K, at 1, 2, 4 and 8 tokens (16 GEMVs; x is
 quantized to Q8_K once per token count and shared by the four formats).
 Metric: packed weight bytes streamed per second (GB/s) and its fraction of the
-measured HBM copy bandwidth.  Each format has 3 rotating weight copies, so the
-weights of one step (736 MB) and the live set (551 MB) are far larger than the
-129 MB L2.  The step is captured once in a CUDA graph and replayed.
+measured HBM copy bandwidth.  Each format has 8 weight copies; one step reads
+a different copy for each token count, so no copy is read twice within a step
+(736 MB per step, 1.47 GB live, far larger than the 129 MB L2).  The step is
+captured once in a CUDA graph and replayed.
+
+Roofline of the GEMV kernels: each (format, token count) GEMV is timed as a
+chain of 8 back-to-back launches over the 8 copies (one captured graph, CUDA
+events around its replays), so a launch's duration includes its share of the
+launch boundaries as it runs inside a decode step; the same launches timed one
+by one with events around each (which breaks the overlap of consecutive
+launches) are reported beside it.
 
 Secondary lines (same JSON, "workloads"): the Q4_0 1024 x 4096 GEMV, the
 4096 x 14336 long-row GEMV (Q8_0, Q6_K at 1 and 8 tokens), the MoE decode
@@ -41,7 +49,8 @@ KQ = syn.GEMV_KQUANT
 FMTS = KQ["fmts"]
 TOKENS = KQ["T"]
 N, K = KQ["N"], KQ["K"]
-ROTATE = 3
+ROTATE = 8
+CHAIN = 8  # launches per timed chain of one GEMV
 METRIC = "decode GEMV/MoE packed-weight GB/s (% of HBM); prefill expert GEMM int8 TOPS"
 
 
@@ -318,18 +327,19 @@ def run_gpu(args, rank, world):
     Wdev = {}
     for fi, f in enumerate(FMTS):
         g = syn.rng(KQ["index"], 10 + fi)
-        Wdev[f] = [torch.from_numpy(syn.weights(f, N, K, g)).cuda() for _ in range(ROTATE)]
+        w0 = torch.from_numpy(syn.weights(f, N, K, g)).cuda()
+        Wdev[f] = [w0] + [w0.clone() for _ in range(ROTATE - 1)]  # distinct addresses, same bytes
     gx = syn.rng(KQ["index"], 200)
     x_host = {T: torch.from_numpy(syn.activations(T, K, gx)).pin_memory() for T in TOKENS}
     x_dev = {T: x_host[T].cuda() for T in TOKENS}
     xq_dev = {T: torch.empty((T, syn.row_bytes("Q8_K", K)), dtype=torch.uint8, device="cuda") for T in TOKENS}
     y_dev = {(f, T): torch.empty((T, N), dtype=torch.float32, device="cuda") for f in FMTS for T in TOKENS}
     ctx.reserve(max_tokens=8, max_k=K)
-    # rotate copies: the c-th call on a format uses copy c % ROTATE
+    # each token count reads its own copy of every format: nothing is re-read within a step
     plan = []
     for f in FMTS:
         for c, T in enumerate(TOKENS):
-            plan.append((f, T, c % ROTATE))
+            plan.append((f, T, c))
     wbytes = {f: N * syn.row_bytes(f, K) for f in FMTS}
     step_wbytes = sum(wbytes[f] for f, _, _ in plan)
     # algorithmic bytes of one GEMV launch: packed W + quantized x + fp32 y
@@ -385,7 +395,7 @@ def run_gpu(args, rank, world):
     ms_per_step = total_ms / args.steps
     value = job_gbps(step_wbytes, world, ms_per_step)
 
-    # per-launch GEMV kernel durations: events inside the second graph, median of 5 replays
+    # isolated launches: events around every GEMV inside the second graph, median of 5 replays
     samples = {k: [] for k in plan}
     with torch.cuda.stream(stream):
         for _ in range(5):
@@ -393,12 +403,26 @@ def run_gpu(args, rank, world):
             torch.cuda.synchronize()
             for j, key in enumerate(plan):
                 samples[key].append(rt.elapsed_ms(*kev[j]))
-    per_launch = {(f, T): statistics.median(samples[(f, T, c)]) for (f, T, c) in plan}
-    sum_alg = sum(alg_bytes[k] for k in per_launch)
-    sum_ms = sum(per_launch.values())
+    isolated = {(f, T): statistics.median(samples[(f, T, c)]) for (f, T, c) in plan}
+    # kernel durations in a chain: CHAIN back-to-back launches of one GEMV over the
+    # copies (> 2x L2 between reuses), one captured graph, events around 5 replays
+    chain = {}
+    for f in FMTS:
+        for T in TOKENS:
+            def one_chain(f=f, T=T):
+                for c in range(CHAIN):
+                    ctx.mul_mat_vec_q(f, Wdev[f][c % ROTATE], N, K, xq_dev[T], T, Y=y_dev[(f, T)])
+            chain[(f, T)] = _graph_time(one_chain, 5, rt, stream) / CHAIN
+    sum_alg = sum(alg_bytes[k] for k in chain)
+    sum_ms = sum(chain.values())
     achieved = sum_alg / (sum_ms / 1e3) / 1e9
-    breakdown = {f"{f}_T{T}": {"us": round(ms * 1e3, 2), "GBps": round(alg_bytes[(f, T)] / (ms / 1e3) / 1e9, 1)}
-                 for (f, T), ms in per_launch.items()}
+    iso_achieved = sum_alg / (sum(isolated.values()) / 1e3) / 1e9
+    fam = {"k_gemv_mma (T=2-8)": [k for k in chain if k[1] > 1], "k_stream (T=1)": [k for k in chain if k[1] == 1]}
+    families = {name: round(sum(alg_bytes[k] for k in ks) / (sum(chain[k] for k in ks) / 1e3) / 1e9 / hbm_peak, 4)
+                for name, ks in fam.items()}
+    breakdown = {f"{f}_T{T}": {"us": round(ms * 1e3, 2), "GBps": round(alg_bytes[(f, T)] / (ms / 1e3) / 1e9, 1),
+                               "isolated_us": round(isolated[(f, T)] * 1e3, 2)}
+                 for (f, T), ms in chain.items()}
 
     # ---- end to end through the public API with host buffers
     y_host = {k: torch.empty(v.shape, dtype=torch.float32).pin_memory() for k, v in y_dev.items()}
@@ -452,19 +476,24 @@ def run_gpu(args, rank, world):
             "data": "synthetic (seeded)",
             "config": {"workload": "kquant_gemv_14336x4096_Q8_0-Q4_K-Q5_K-Q6_K_T1-2-4-8",
                        "packed_weight_bytes_per_step": step_wbytes,
-                       "l2": f"inputs larger than L2: {ROTATE} rotating copies per format "
-                             f"({sum(wbytes.values()) * ROTATE / 1e6:.0f} MB live), no L2 flush",
+                       "l2": f"inputs larger than L2: {ROTATE} copies per format ({sum(wbytes.values()) * ROTATE / 1e6:.0f} "
+                             "MB live), each read once per step, no L2 flush",
                        "graph": "one step captured in a CUDA graph, replayed",
                        "fraction_of_hbm": round(value / world / hbm_peak, 4), "peak": f"{hbm_peak} GB/s ({peak_kind})"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                         "algorithmic_bytes_per_launch": round(sum_alg / len(per_launch)),
+                         "algorithmic_bytes_per_launch": round(sum_alg / len(chain)),
                          "kernel": "decode GEMV kernels (k_stream dp4a at T=1, k_gemv_mma tensor path at T=2-8): "
                                    "all 16 launches of a step; algorithmic bytes = packed W + Q8_K x + fp32 y",
                          "traffic_source": "mean dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch of "
                                            "one step (ncu; profiles/traffic_kquant_gemv_step.json), null when the "
                                            "kernel sources changed since",
-                         "timing": "CUDA events around each GEMV inside a captured graph, median of 5 replays",
+                         "timing": f"average launch duration in a chain of {CHAIN} back-to-back launches of each "
+                                   "GEMV (CUDA events around 5 replays of the captured chain on its stream)",
+                         "frac_by_kernel": families,
+                         "isolated_frac": round(iso_achieved / hbm_peak, 4),
+                         "isolated_timing": "CUDA events around each GEMV inside the captured step (no overlap "
+                                            "with the neighbouring launches), median of 5 replays",
                          "peak_kind": peak_kind, "per_launch": breakdown},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},

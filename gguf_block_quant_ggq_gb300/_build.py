@@ -68,5 +68,52 @@ def build(force: bool = False, jobs: int | None = None) -> str:
     return LIB
 
 
+def ptxas_summary(report: str | None = None) -> str:
+    """Markdown table of every kernel's registers, stack and spills from the
+    ``-Xptxas -v`` report that build() writes (one row per kernel instance)."""
+    import re
+
+    text = open(report or os.path.join(PKG, "ptxas_report.txt")).read()
+    rows = []
+    cur = None
+    for line in text.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            cur = {"name": m.group(1)}
+            continue
+        if cur is None:
+            continue
+        m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m:
+            cur["stack"], cur["st"], cur["ld"] = (int(g) for g in m.groups())
+        m = re.search(r"Used (\d+) registers", line)
+        if m:
+            cur["regs"] = int(m.group(1))
+            rows.append(cur)
+            cur = None
+    def pretty(mangled):
+        # _ZN3ggq<len><name>I<template args>E... -> name<args> (Li5E -> 5, Lb1E -> true)
+        m = re.match(r"_ZN3ggq(\d+)", mangled)
+        if not m:
+            return mangled
+        n = int(m.group(1))
+        start = m.end()
+        name = mangled[start:start + n]
+        args = re.findall(r"L([ib])(\d+)E", mangled[start + n:])
+        vals = [("true" if v == "1" else "false") if t == "b" else v for t, v in args]
+        return f"{name}<{', '.join(vals)}>" if vals else name
+    out = ["| kernel | registers | stack (B) | spill stores (B) | spill loads (B) |", "|---|---|---|---|---|"]
+    for r in sorted(rows, key=lambda r: pretty(r["name"])):
+        out.append(f"| `{pretty(r['name'])}` | {r['regs']} | {r.get('stack', 0)} | {r.get('st', 0)} | {r.get('ld', 0)} |")
+    return "\n".join(out) + "\n"
+
+
 if __name__ == "__main__":
-    print(build(force=True))
+    import sys
+
+    if len(sys.argv) > 2 and sys.argv[1] == "--ptxas-summary":
+        build()
+        with open(sys.argv[2], "w") as f:
+            f.write(ptxas_summary())
+    else:
+        print(build(force=True))

@@ -295,6 +295,7 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
     int stages = (kSmemLimit - fixed) / p.stage_stride;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return false;
+    if (stages > kWholeRowStages) stages = kWholeRowStages;
     p.stages = stages;
     *smem = stages * p.stage_stride + fixed;
     return true;

@@ -9,13 +9,15 @@
 //     LOP3 per pair of codes) and int8 activations are exact in f16, so every
 //     product is exact; C starts at -1024 (Q6_K: -1056) times the activation
 //     sum of the block, which leaves the exact integer dot of each sub-block
-//     (Q6_K: each 16-group, whose own scale it needs) in D.  Block scales are
-//     applied in f32; the Q4_K/Q5_K mins term is one more f16 product.  On this
-//     part the f16 mma runs at four times the rate of the int8 one.  The
-//     scaled Q4_K codes accumulate in 128-wide chains and the Q5_K codes in
-//     64-wide chains (|partial| <= 128 * 945 * 127 and 64 * 1953 * 127, both
-//     below 2^24), so every chain holds its exact integer; the chains meet in
-//     the f32 epilogue.
+//     (Q6_K: each 16-group, whose own scale it needs) in D.  Q4_K and Q5_K
+//     fold the 6-bit sub-block scale into the operand instead (sc * q is an
+//     exact f16 integer) and accumulate in 128-wide (Q4_K) or 64-wide (Q5_K)
+//     chains, |partial| <= 128 * 945 * 127 and 64 * 1953 * 127, both below
+//     2^24, so every chain holds its exact integer; the chains meet in the f32
+//     epilogue.  Block scales are applied in f32; the Q4_K/Q5_K mins term is
+//     one more f16 product.  On this part the f16 mma runs at four times the
+//     rate of the int8 one.  (Applying the sub-block scale in f32 after
+//     per-sub-block mma pairs instead was measured slower.)
 //   * Q8_0, MXFP4: mma.sync m16n8k32 on int8 (one 32-block per mma).
 //
 // Layout on the SM:
@@ -47,6 +49,18 @@ __device__ __forceinline__ void mmav_start_arrive() { asm volatile("bar.arrive 2
 __device__ __forceinline__ void mmav_start_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory"); }
 
 __device__ __forceinline__ void mmav_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
+
+// Bounded wait that backs off between probes (a few tens of ns), leaving the
+// issue slots of a busy SM to the warps that have work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(32);
+        if (mbar_test(bar, parity)) return true;
+        if (clock64() - t0 > (1ll << 32)) return false;
+    }
+}
 
 __device__ __forceinline__ void mma_k32_s8(int* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                            uint32_t b1, int c0, int c1) {
@@ -235,9 +249,10 @@ __device__ __forceinline__ void dump_put(int32_t* row, int idx, int v) {
 }
 
 // 16 x 8 partial of one chunk: rows (g, g+8) at r0/r1, columns (2t, 2t+1).
-template <int F, bool DUMP>
-__device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk, const MmaX& X, saddr cs, int t,
+template <int F, bool DUMP, int CH>
+__device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk_rt, const MmaX& X, saddr cs, int t,
                                            float* acc, const MmavDump& dz) {
+    const int chunk = CH > 0 ? CH : chunk_rt;  // inputs of the chunk (compile-time for the common widths)
     const int sb = e0 >> 8;
     if constexpr (F == F_Q4_K || F == F_Q5_K) {
         // f16 operands: a code q placed in the mantissa of 1024.0 reads 1024 + q
@@ -485,7 +500,7 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
     }
 }
 
-template <int F, bool DUMP>
+template <int F, bool DUMP, int CH>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -518,14 +533,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
         mmav_start_arrive();
         const uint64_t pol = policy_evict_first();
         if (!p.early_weights) pdl_wait();  // the previous kernel may still be writing the weights
-        int j = 0;
+        int j = 0, s = 0;
+        uint32_t ph = 0u;  // ring slot and phase of tile j
         bool ok = true;
         for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
-            const int s = j % p.stages;
             const int64_t r0 = static_cast<int64_t>(item) * kTileRows;
             const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
             if (lane == 0) {
-                ok = mbar_wait(&empty[s], (static_cast<uint32_t>(j / p.stages) & 1u) ^ 1u);
+                ok = mbar_wait(&empty[s], ph ^ 1u);
                 if (ok) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nr * p.rowbytes));
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -538,6 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
                 const int rows = nr - pr < 2 ? nr - pr : 2;
                 bulk_g2s(ring + static_cast<size_t>(s) * p.stage_stride + static_cast<size_t>(lane) * p.wrow,
                          p.W + (r0 + pr) * p.rowbytes, static_cast<uint32_t>(rows * p.rowbytes), &full[s], pol);
+            }
+            if (++s == p.stages) {
+                s = 0;
+                ph ^= 1u;
             }
         }
         if (lane == 0) {
@@ -577,11 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     mmav_load_x<F>(smem_addr(xreg), p.xrow, active ? p.T : 0, p.chunk, e0, g, t, X, cs);
     mmav_sync();  // the region now holds partials
     const saddr ring_s = smem_addr(ring);
-    int j = 0;
+    int j = 0, s = 0;
+    uint32_t ph = 0u;  // ring slot and phase of tile j
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
-        const int s = j % p.stages;
-        const bool ready =
-            xok && __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(j / p.stages) & 1u));
+        const bool ready = xok && __all_sync(0xffffffffu, mbar_wait_backoff(&full[s], ph));
         if (!ready) set_error(p.err, DEV_ERR_TIMEOUT);
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (ready && active) {
@@ -597,10 +615,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
                                                      : nullptr;
                 }
             }
-            mmav_chunk<F, DUMP>(r0, r0 + static_cast<uint32_t>(p.rowbytes), e0, p.chunk, X, smem_addr(cs), t, acc, dz);
+            mmav_chunk<F, DUMP, CH>(r0, r0 + static_cast<uint32_t>(p.rowbytes), e0, p.chunk, X, smem_addr(cs), t, acc,
+                                    dz);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == p.stages) {
+            s = 0;
+            ph ^= 1u;
+        }
         // partials of this tile -> buffer j & 1, laid out [warp][tile row x 8 + column]
         // with a warp stride of kRedStride floats (2 mod 32: the reads below hit 32
         // distinct banks); one barrier per tile (a warp writes buffer j & 1 again only
@@ -624,19 +647,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     }
 }
 
-template <int F, bool DUMP>
-cudaError_t launch_mmav_one(const MmavParams& p, int grid, int smem, cudaStream_t s) {
+template <int F, bool DUMP, int CH>
+cudaError_t launch_mmav_ch(const MmavParams& p, int grid, int smem, cudaStream_t s) {
     static std::atomic<bool> attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(k_gemv_mma<F, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        e = cudaFuncSetAttribute(k_gemv_mma<F, DUMP, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_gemv_mma<F, DUMP>, dim3(grid), dim3(kThreads), smem, s, p);
+    return launch_pdl(k_gemv_mma<F, DUMP, CH>, dim3(grid), dim3(kThreads), smem, s, p);
+}
+
+// Chunks of 256 inputs (K = 4096: the decode widths of the 14336 x 4096 GEMV)
+// run a variant with the chunk width fixed at compile time; others take it
+// at run time.
+template <int F, bool DUMP>
+cudaError_t launch_mmav_one(const MmavParams& p, int grid, int smem, cudaStream_t s) {
+    return p.chunk == 256 ? launch_mmav_ch<F, DUMP, 256>(p, grid, smem, s) : launch_mmav_ch<F, DUMP, 0>(p, grid, smem, s);
 }
 
 }  // namespace ggq

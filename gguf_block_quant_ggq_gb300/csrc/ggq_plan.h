@@ -20,6 +20,7 @@ inline bool plan_stream(int64_t stage_bytes, int xrows, int K, bool q81, StreamS
     if (fixed + s->stride > kSmemLimit) return false;
     s->stages = (kSmemLimit - fixed) / s->stride;
     if (s->stages > kMaxStages) s->stages = kMaxStages;
+    if (s->stages > kWholeRowStages) s->stages = kWholeRowStages;
     s->smem = s->stages * s->stride + fixed;
     return true;
 }
@@ -81,6 +82,8 @@ inline bool plan_stream_chunked(int f, int64_t rowbytes, int xrows, int K, bool 
         return false;
     }
     if (s->stages > kMaxStages) s->stages = kMaxStages;
+    const int cap = kInFlightBytes / s->stride;
+    if (s->stages > 2 && s->stages > cap) s->stages = cap > 2 ? cap : 2;
     s->smem = s->stages * s->stride + fixed;
     *chunk_units = g * gu;
     *chunk_bytes = cb;
