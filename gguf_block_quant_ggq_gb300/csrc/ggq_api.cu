@@ -410,6 +410,17 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     return GGQ_OK;
 }
 
+// Expert banks that the expert-sorted route runs on the tcgen05 grouped GEMM
+// (128-row weight tiles): Q8_0 gate/up and Q4_K down.
+bool tc_gateup(int f, int64_t I, int64_t H) {
+    (void)H;
+    return f == F_Q8_0 && I % 128 == 0;
+}
+bool tc_down(int f, int64_t H, int64_t I) {
+    (void)I;
+    return f == F_Q4_K && H % 128 == 0;
+}
+
 // Largest token count on the direct tiny-batch route (ds4 PR #656 "Add ROCm
 // MXFP4 routed expert kernels", Summary: 2-4 tokens go to direct kernels; 5
 // and above use expert-sorted tiles).
@@ -436,13 +447,13 @@ const char* moe_width_refusal(int fg, int fd, int64_t H, int64_t I, int64_t T, i
             return "moe_experts: I too wide for shared memory";
         return nullptr;
     }
-    if (!(fg == F_Q8_0 && I % 128 == 0) && !gmm_supported(fg)) {
+    if (!tc_gateup(fg, I, H) && !gmm_supported(fg)) {
         GroupParams g{};
         g.rowbytes = w_row_bytes(fg, H);
         g.K = static_cast<int>(H);
         if (!plan_group(g, 2, false, &smem)) return "moe_experts: H too wide for shared memory";
     }
-    if (!(fd == F_Q4_K && H % 128 == 0) && !gmm_supported(fd)) {
+    if (!tc_down(fd, H, I) && !gmm_supported(fd)) {
         GroupParams d{};
         d.rowbytes = w_row_bytes(fd, I);
         d.K = static_cast<int>(I);
@@ -521,12 +532,13 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     float* const hdx = reinterpret_cast<float*>(base + ms.hdx);
     int smem = 0;
     bool h_dumped = false;  // the SwiGLU quantizer wrote dump->h itself
-    if (fg == F_Q8_0 && I % 128 == 0) {
+    const bool tcg = tc_gateup(fg, I, H);
+    if (tcg) {
         // Q8_0 gate/up on tcgen05: g and u per pair, then h = silu(g) u fused into its quantizer
         e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
         GmmTcParams t{};
-        const int r = gmmtc_encode(t, F_Q8_0, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), nullptr, P,
+        const int r = gmmtc_encode(t, fg, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), nullptr, P,
                                    static_cast<int>(H));
         if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: gate/up tensor maps (CUresult %d)", r);
         t.N = I;
@@ -545,7 +557,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         t.coefs[0] = cg;
         t.coefs[1] = cu;
         t.ncoef = ncg;
-        e = cg ? launch_gmmtc_dump(F_Q8_0, t, c->nsm, st) : launch_gmmtc(F_Q8_0, t, c->nsm, st);
+        e = cg ? launch_gmmtc_dump(fg, t, c->nsm, st) : launch_gmmtc(fg, t, c->nsm, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
         e = launch_quantize_silu(gbuf, ubuf, P, I, hq, hp, dump ? dump->h : nullptr, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: SwiGLU quantize launch");
@@ -574,7 +586,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         g.ncoef = ncg;
         e = cg ? launch_group_dump(G_GATEUP, fg, g, c->nsm, smem, st) : launch_group(G_GATEUP, fg, g, c->nsm, smem, st);
     }
-    if (!(fg == F_Q8_0 && I % 128 == 0)) {
+    if (!tcg) {
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
         // h^ = Q8_K(h)
         e = launch_quantize_pitched(h, P, I, hq, hp, st);
@@ -594,12 +606,12 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     d.o = o;
     d.coefs[0] = d.coefs[1] = cd;
     d.ncoef = ncd;
-    if (fd == F_Q4_K && H % 128 == 0) {
+    if (tc_down(fd, H, I)) {
         // Q4_K down on tcgen05
         e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
         GmmTcParams t{};
-        const int r = gmmtc_encode(t, F_Q4_K, d.W, nullptr, d.rowbytes, E * H, h16, hdx, dx_pitch(I), hbs, P,
+        const int r = gmmtc_encode(t, fd, d.W, nullptr, d.rowbytes, E * H, h16, hdx, dx_pitch(I), hbs, P,
                                    static_cast<int>(I));
         if (r) return fail(c, GGQ_ERR_CUDA, "moe sorted: down tensor maps (CUresult %d)", r);
         t.N = H;
@@ -614,7 +626,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         t.out[0] = t.out[1] = o;
         t.coefs[0] = t.coefs[1] = cd;
         t.ncoef = ncd;
-        e = cd ? launch_gmmtc_dump(F_Q4_K, t, c->nsm, st) : launch_gmmtc(F_Q4_K, t, c->nsm, st);
+        e = cd ? launch_gmmtc_dump(fd, t, c->nsm, st) : launch_gmmtc(fd, t, c->nsm, st);
     } else if (gmm_supported(fd)) {
         e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");

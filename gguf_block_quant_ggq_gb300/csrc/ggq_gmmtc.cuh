@@ -54,7 +54,7 @@ constexpr int kTcStages = 4;  // TMA ring
 constexpr int kTcEpi = 256;   // epilogue threads (warps 0-7)
 constexpr int kTcDec = 192;   // decode threads (warps 8-13)
 constexpr int kTcTmaWarp = 14, kTcMmaWarp = 15;
-constexpr int kTcRaw = 80;  // raw bytes per weight row per k-step
+constexpr int kTcRaw = 80;  // raw bytes per weight row per k-step (Q8_0: the 16-aligned span of two 34-byte blocks)
 constexpr int kTcMaxGroups = 4096;
 static_assert(kTcThreads == kTcEpi + kTcDec + 64, "warp roles");
 
@@ -65,7 +65,8 @@ template <int F>
 struct TcSmem {
     static constexpr int kABufs = F == F_Q8_0 ? 5 : 4;
     static constexpr int kB = kTcBN * kTcBK * 2;     // 16384, SW128 K-major
-    static constexpr int kRaw = kTcBM * kTcRaw;      // 10240
+    static constexpr int kRawRow = kTcRaw;           // raw bytes per weight row per k-step
+    static constexpr int kRaw = kTcBM * kRawRow;     // 10240
     static constexpr int kDX = kTcBN * 16;           // 2048: 4 superblock scales per column
     static constexpr int kStage = kB + kRaw + kDX;   // 28672 (28 KB: activation tiles stay 1024-aligned)
     static constexpr int kA = kTcBM * kTcBK * 2;     // 16384, SW128 K-major
@@ -90,14 +91,19 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
-// instruction descriptor: f32 accumulate, f16 A and B, both K-major, M = 128, N = 128
-constexpr uint32_t kTcIdesc = (1u << 4) | ((static_cast<uint32_t>(kTcBN) >> 3) << 17) | ((static_cast<uint32_t>(kTcBM) >> 4) << 24);
+// instruction descriptor: f32 accumulate, f16 A and B, both K-major, M = 128, N = n
+__host__ __device__ constexpr uint32_t tc_idesc(uint32_t n) {
+    return (1u << 4) | ((n >> 3) << 17) | ((static_cast<uint32_t>(kTcBM) >> 4) << 24);
+}
+// Items with at most this many columns load a 32-row activation box and run N = 32
+// MMAs (decode-sized token counts spread over many experts).
+constexpr int kTcNarrow = 32;
 
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -211,7 +217,8 @@ __device__ __forceinline__ void tc_dump32(const GmmTcParams& p, const TcItem& cu
 template <int F, bool DUMP>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__ GmmTcParams p) {
     static_assert(F == F_Q8_0 || F == F_Q4_K, "tcgen05 grouped GEMM: Q8_0 and Q4_K banks");
-    constexpr bool Q8 = F == F_Q8_0;
+    constexpr bool Q8 = F == F_Q8_0;  // one accumulator and one weight scale per 32-block
+    constexpr int kRawRow = TcSmem<F>::kRawRow;
     // tensor-memory columns: block (Q8_0) or superblock (Q4_K) accumulators 0..255,
     // Q4_K mins term 256..383, item accumulator
     constexpr uint32_t kAcc = Q8 ? 256u : 384u, kDmin = 256u;
@@ -312,8 +319,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
                 const bool dx_load = Q8 ? sb_end : (kt & 1) == 1;  // Q4_K: at each half superblock's end
-                mbar_arrive_expect_tx(&full[s], SM::kB + kRawTx + (dx_load ? SM::kDX : 0) + (sb_end && !Q8 ? kTcBN * 32 : 0));
-                tc_tma_2d(smem_addr(B16(s)), &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
+                const bool narrow = cur.ncols <= kTcNarrow;  // 32 activation rows suffice
+                mbar_arrive_expect_tx(&full[s], (narrow ? kTcNarrow * 128 : SM::kB) + kRawTx + (dx_load ? SM::kDX : 0) +
+                                                    (sb_end && !Q8 ? kTcBN * 32 : 0));
+                tc_tma_2d(smem_addr(B16(s)), narrow ? &p.tm_b32 : &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
                 if constexpr (Q8) {
                     tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);
                 } else {
@@ -328,8 +337,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         }
     } else if (warp == kTcMmaWarp) {
         // ================================================================ MMA
+        uint32_t idesc = tc_idesc(kTcBN);
         for (int c = 0; c < total; ++c) {
             const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
+            if (kt == 0) idesc = tc_idesc(item_of(c / nk).ncols <= kTcNarrow ? kTcNarrow : kTcBN);
             if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
             if (!tc_wait(&afull[a], (c / kTcABufs) & 1, abort, p.err)) break;
             tc_fence_after();
@@ -346,7 +357,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = static_cast<uint64_t>((2 * b + kk) * 2);
-                            tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + koff, bdesc + koff, static_cast<uint32_t>(kk));
+                            tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + koff, bdesc + koff, idesc,
+                                   static_cast<uint32_t>(kk));
                         }
                         tc_commit(&tfull[db]);
                     }
@@ -365,9 +377,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + static_cast<uint64_t>(2 * kk),
-                                   bdesc + static_cast<uint64_t>(2 * kk), static_cast<uint32_t>((kt & 1) != 0 || kk != 0));
+                                   bdesc + static_cast<uint64_t>(2 * kk), idesc, static_cast<uint32_t>((kt & 1) != 0 || kk != 0));
                         if ((kt & 3) == 3)
-                            tc_mma(tmem + kDmin, umma_desc_sw128(smem_addr(min_a)), umma_desc_sw128(smem_addr(min_b)), 0u);
+                            tc_mma(tmem + kDmin, umma_desc_sw128(smem_addr(min_a)), umma_desc_sw128(smem_addr(min_b)), idesc,
+                                   0u);
                         if ((kt & 1) == 1) tc_commit(&tfull[db]);
                         tc_commit(&aempty[a]);
                         tc_commit(&empty[s]);
@@ -493,6 +506,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         bool live = true;
         for (int it = 0; it < my_items && live; ++it) {
             const TcItem cur = item_of(it);
+            // column chunks h2 of this warp that hold accumulators (narrow items: the first 32 columns)
+            const int ncol_acc = cur.ncols <= kTcNarrow ? kTcNarrow : kTcBN;
+            const bool act[2] = {col0 < ncol_acc, col0 + 32 < ncol_acc};
             for (int kt = 0; kt < nk && live; ++kt) {
                 const int c = it * nk + kt, s = c % kTcStages;
                 const saddr raw = smem_addr(RAW(s));
@@ -503,10 +519,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                         const int gb = 2 * c + b, db = gb & 1;
                         if (!tc_wait(&tfull[db], (gb >> 1) & 1, abort, p.err)) { live = false; break; }
                         tc_fence_after();
-                        const float dw = ld_h(raw + static_cast<uint32_t>(r * kTcRaw + o0 + 34 * b));
+                        const float dw = ld_h(raw + static_cast<uint32_t>(r * kRawRow + o0 + 34 * b));
                         const bool first = b == 0 && (kt & 3) == 0;
 #pragma unroll
                         for (int h2 = 0; h2 < 2; ++h2) {
+                            if (!act[h2]) continue;
                             float v[32];
                             tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
                             if constexpr (DUMP) tc_dump32(p, cur, r, col0 + 32 * h2, v, 2 * kt + b, false);
@@ -522,6 +539,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                         const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
 #pragma unroll
                         for (int h2 = 0; h2 < 2; ++h2) {
+                            if (!act[h2]) continue;
                             float a[32];
                             const uint32_t ta = lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2);
                             if (kt == 3) {
@@ -546,6 +564,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
+                        if (!act[h2]) continue;
                         float v[32], m[32], a[32];
                         tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
                         if (second) {
@@ -581,6 +600,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             const int64_t row = static_cast<int64_t>(cur.mt) * kTcBM + r;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
+                if (!act[h2]) continue;
                 float a[32];
                 tmem_ld32(lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2), a);
 #pragma unroll

@@ -213,6 +213,7 @@ constexpr int kTcThreads = 512;  // 8 epilogue, 6 decode, 1 TMA, 1 MMA warps
 
 struct GmmTcParams {
     CUtensorMap tm_b;     // f16 activation rows, sorted positions [P][K]: box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_b32;   // the same rows, box 64 x 32 (items of at most 32 columns)
     CUtensorMap tm_dx;    // f32 block scales [P][dx_pitch]: box 4 x 128
     CUtensorMap tm_bs;    // f16 16-group sums [P][K/16]: box 16 x 128 (Q4_K)
     CUtensorMap tm_w[2];  // weight bytes [E*N][rowbytes]: Q8_0 gate and up (box 80 x 128); Q4_K header (16 x 128) and nibbles (32 x 128)

@@ -10,6 +10,8 @@ int gmmtc_encode(GmmTcParams& p, int fmt, const uint8_t* W, const uint8_t* W2, i
     const uint64_t k = static_cast<uint64_t>(K), np = static_cast<uint64_t>(P);
     int r = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, k, np, k * 2, kTcBK, kTcBN,
                            CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r) r = encode_tmap_2d(&p.tm_b32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, k, np, k * 2, kTcBK, kTcNarrow,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (!r) r = encode_tmap_2d(&p.tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, static_cast<uint64_t>(dx_pitch), np,
                                static_cast<uint64_t>(dx_pitch) * 4, 4, kTcBN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!r) r = encode_tmap_2d(&p.tm_bs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bs16 ? bs16 : x16, k / 16, np, k / 8, 16, kTcBN,
