@@ -66,6 +66,11 @@ def lib():
                 "orc_dequant": (None, [i32, p, i64, i64, p]),
                 "orc_quantize_q8_1": (None, [p, i64, i64, p]),
                 "orc_quantize_q8_k": (None, [p, i64, i64, p]),
+                "orc_quantize_q8_0": (None, [p, i64, i64, p]),
+                "orc_pair_ok": (i32, [i32, i32]),
+                "orc_gemv_a": (None, [i32, i32, p, i64, i64, p, i64, p]),
+                "orc_gemv_coefs_a": (None, [i32, i32, p, i64, i64, p, i64, p]),
+                "orc_gemv_dequant_a": (None, [i32, i32, p, i64, i64, p, i64, p, p]),
                 "orc_row_coefs": (None, [i32, p, p, i64, p]),
                 "orc_gemv": (None, [i32, p, i64, i64, p, i64, p]),
                 "orc_gemv_coefs": (None, [i32, p, i64, i64, p, i64, p]),
@@ -145,6 +150,8 @@ def quantize(act: str, x: np.ndarray) -> np.ndarray:
     out = np.zeros((T, row_bytes(act, K)), dtype=np.uint8)
     if act == "Q8_1":
         lib().orc_quantize_q8_1(_p(x), T, K, _p(out))
+    elif act == "Q8_0":
+        lib().orc_quantize_q8_0(_p(x), T, K, _p(out))
     elif act == "Q8_K":
         lib().orc_quantize_q8_k(_p(x), T, K, _p(out))
     else:
@@ -152,33 +159,45 @@ def quantize(act: str, x: np.ndarray) -> np.ndarray:
     return out
 
 
-def gemv(wtype: str, W: np.ndarray, N: int, K: int, Xq: np.ndarray, T: int) -> np.ndarray:
-    """Integer-dot form: Y[T][N] in float64."""
+def _act(wtype: str, act: str | None) -> str:
+    a = act or act_type(wtype)
+    if not lib().orc_pair_ok(FMT[wtype], FMT[a]):
+        raise ValueError(f"{wtype} weights do not pair with {a} activations")
+    return a
+
+
+def gemv(wtype: str, W: np.ndarray, N: int, K: int, Xq: np.ndarray, T: int, act: str | None = None) -> np.ndarray:
+    """Integer-dot form: Y[T][N] in float64 (act: the activation format of Xq, default the weight's)."""
+    a = _act(wtype, act)
     W = np.ascontiguousarray(W, dtype=np.uint8)
     Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
-    assert W.size >= N * row_bytes(wtype, K) and Xq.size >= T * row_bytes(act_type(wtype), K)
+    assert W.size >= N * row_bytes(wtype, K) and Xq.size >= T * row_bytes(a, K)
     Y = np.empty((T, N), dtype=np.float64)
-    lib().orc_gemv(FMT[wtype], _p(W), N, K, _p(Xq), T, _p(Y))
+    lib().orc_gemv_a(FMT[wtype], FMT[a], _p(W), N, K, _p(Xq), T, _p(Y))
     return Y
 
 
-def gemv_coefs(wtype: str, W: np.ndarray, N: int, K: int, Xq: np.ndarray, T: int) -> np.ndarray:
+def gemv_coefs(wtype: str, W: np.ndarray, N: int, K: int, Xq: np.ndarray, T: int, act: str | None = None) -> np.ndarray:
     """Per-block int32 coefficients: [T][N][K/blk * coefs_per_block]."""
+    a = _act(wtype, act)
     W = np.ascontiguousarray(W, dtype=np.uint8)
     Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    assert W.size >= N * row_bytes(wtype, K) and Xq.size >= T * row_bytes(a, K)
     nc = K // BLOCK_ELEMS[wtype] * coefs_per_block(wtype)
     out = np.empty((T, N, nc), dtype=np.int32)
-    lib().orc_gemv_coefs(FMT[wtype], _p(W), N, K, _p(Xq), T, _p(out))
+    lib().orc_gemv_coefs_a(FMT[wtype], FMT[a], _p(W), N, K, _p(Xq), T, _p(out))
     return out
 
 
-def gemv_dequant(wtype: str, W: np.ndarray, N: int, K: int, Xq: np.ndarray, T: int):
+def gemv_dequant(wtype: str, W: np.ndarray, N: int, K: int, Xq: np.ndarray, T: int, act: str | None = None):
     """Dequantize-then-double form: returns (Y, sum |w*x|), each [T][N]."""
+    a = _act(wtype, act)
     W = np.ascontiguousarray(W, dtype=np.uint8)
     Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    assert W.size >= N * row_bytes(wtype, K) and Xq.size >= T * row_bytes(a, K)
     Y = np.empty((T, N), dtype=np.float64)
     A = np.empty((T, N), dtype=np.float64)
-    lib().orc_gemv_dequant(FMT[wtype], _p(W), N, K, _p(Xq), T, _p(Y), _p(A))
+    lib().orc_gemv_dequant_a(FMT[wtype], FMT[a], _p(W), N, K, _p(Xq), T, _p(Y), _p(A))
     return Y, A
 
 

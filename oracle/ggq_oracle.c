@@ -244,6 +244,23 @@ void orc_quantize_q8_1(const float* x, int64_t T, int64_t K, uint8_t* out) {
         }
 }
 
+/* Q8_0 activation blocks ([VC523] What changed: the Q8_0 activation quantizer
+ * that pairs with Q8_0 weights): the same fp32 sequence per 32 elements, d
+ * stored as fp16 (nearest-even) followed by the 32 quants -- the Q8_0 weight
+ * layout. */
+void orc_quantize_q8_0(const float* x, int64_t T, int64_t K, uint8_t* out) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < K / 32; ++j) {
+            uint8_t* b = out + (t * (K / 32) + j) * 34;
+            int8_t q[32];
+            float d;
+            quant_block_f32(x + t * K + j * 32, 32, q, &d);
+            uint16_t hd = orc_float_to_half(d);
+            b[0] = hd & 255; b[1] = hd >> 8;
+            memcpy(b + 2, q, 32);
+        }
+}
+
 void orc_quantize_q8_k(const float* x, int64_t T, int64_t K, uint8_t* out) {
     for (int64_t t = 0; t < T; ++t)
         for (int64_t j = 0; j < K / 256; ++j) {
@@ -274,25 +291,45 @@ int orc_coefs_per_block(int wtype) {
     return (wtype == ORC_Q4_K || wtype == ORC_Q5_K) ? 2 : 1;
 }
 
+/* Whether the library pairs weight format wtype with activation format atype:
+ * every weight format with its default activation, and the Q8_0 activation
+ * blocks with the Q4_0 and Q8_0 weights ([VC523] What changed: Q8_0 x Q8_0). */
+int orc_pair_ok(int wtype, int atype) {
+    if (atype == orc_act_type(wtype)) return 1;
+    return atype == ORC_Q8_0 && (wtype == ORC_Q4_0 || wtype == ORC_Q8_0);
+}
+
+/* The 32 int8 quants and the scale of 32-element block j of an activation row. */
+static const int8_t* act_q32(int atype, const uint8_t* xrow, int64_t j) {
+    switch (atype) {
+    case ORC_Q8_1: return (const int8_t*)(xrow + j * 36 + 4);
+    case ORC_Q8_0: return (const int8_t*)(xrow + j * 34 + 2);
+    default: return (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 32);
+    }
+}
+static double act_d32(int atype, const uint8_t* xrow, int64_t j) {
+    switch (atype) {
+    case ORC_Q8_1: return orc_half_to_double(rd16(xrow + j * 36));
+    case ORC_Q8_0: return orc_half_to_double(rd16(xrow + j * 34));
+    default: return (double)rdf32(xrow + (j / 8) * 292);
+    }
+}
+
 /* Integer coefficients of one weight row against one quantized activation row
  * ([VC523] What changed: the keep-quant dot is an integer core per superblock
  * followed by the scale epilogue).  For each weight block b:
- *   Q4_0 x Q8_1 : S_b = sum_j (nib_j - 8) * qx_j
- *   Q8_0 x Q8_K : S_b = sum_j qw_j * qx_j
+ *   Q4_0 x Q8_1/Q8_0 : S_b = sum_j (nib_j - 8) * qx_j
+ *   Q8_0 x Q8_K/Q8_0 : S_b = sum_j qw_j * qx_j
  *   MXFP4 x Q8_K: S_b = sum_j code2_j * qx_j          (doubled E2M1 codes)
  *   Q4_K/Q5_K x Q8_K: A = sum_s sc_s * S_s,  B = sum_s m_s * (bsum_2s + bsum_2s+1)
  *   Q6_K x Q8_K : A = sum_j sc_j * S_j,  S_j over 16 elements of q6 - 32        */
-void orc_row_coefs(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* coefs) {
+void orc_row_coefs_a(int wtype, int atype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* coefs) {
     int be = orc_block_elems(wtype), bb = orc_block_bytes(wtype), nc = orc_coefs_per_block(wtype);
     for (int64_t j = 0; j < K / be; ++j) {
         const uint8_t* b = wrow + j * bb;
         int32_t* out = coefs + j * nc;
         if (be == 32) {
-            const int8_t* qx;
-            if (wtype == ORC_Q4_0)
-                qx = (const int8_t*)(xrow + j * 36 + 4);
-            else
-                qx = (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 32);
+            const int8_t* qx = act_q32(atype, xrow, j);
             int32_t S = 0;
             for (int i = 0; i < 32; ++i) S += elem_q(wtype, b, i) * qx[i];
             out[0] = S;
@@ -324,24 +361,26 @@ void orc_row_coefs(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t 
     }
 }
 
+void orc_row_coefs(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* coefs) {
+    orc_row_coefs_a(wtype, orc_act_type(wtype), wrow, xrow, K, coefs);
+}
+
 /* Scale epilogue: the dot of one weight row with one quantized activation row,
  * in double, from the integer coefficients (form A of the oracle). */
-static double row_dot_int(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* scratch) {
+static double row_dot_int(int wtype, int atype, const uint8_t* wrow, const uint8_t* xrow, int64_t K,
+                          int32_t* scratch) {
     int be = orc_block_elems(wtype), bb = orc_block_bytes(wtype), nc = orc_coefs_per_block(wtype);
-    orc_row_coefs(wtype, wrow, xrow, K, scratch);
+    orc_row_coefs_a(wtype, atype, wrow, xrow, K, scratch);
     double y = 0.0;
     for (int64_t j = 0; j < K / be; ++j) {
         const uint8_t* b = wrow + j * bb;
         const int32_t* c = scratch + j * nc;
         switch (wtype) {
-        case ORC_Q4_0:
-            y += orc_half_to_double(rd16(b)) * orc_half_to_double(rd16(xrow + j * 36)) * c[0];
-            break;
-        case ORC_Q8_0:
-            y += orc_half_to_double(rd16(b)) * (double)rdf32(xrow + (j / 8) * 292) * c[0];
+        case ORC_Q4_0: case ORC_Q8_0:
+            y += orc_half_to_double(rd16(b)) * act_d32(atype, xrow, j) * c[0];
             break;
         case ORC_MXFP4:
-            y += ldexp(1.0, (int)b[0] - 128) * (double)rdf32(xrow + (j / 8) * 292) * c[0];
+            y += ldexp(1.0, (int)b[0] - 128) * act_d32(atype, xrow, j) * c[0];
             break;
         case ORC_Q4_K: case ORC_Q5_K:
             y += (double)rdf32(xrow + j * 292) *
@@ -356,10 +395,12 @@ static double row_dot_int(int wtype, const uint8_t* wrow, const uint8_t* xrow, i
 }
 
 /* Y[t][n] = sum_k W[n][k] * Xq[t][k]  ("MatmulBT": [VC523] What changed, op 74;
- * [FT136] Summary, ggml_mul_mat_vec_a8).  Integer-dot form, double epilogue. */
-void orc_gemv(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, double* Y) {
+ * [FT136] Summary, ggml_mul_mat_vec_a8), Xq in activation format atype.
+ * Integer-dot form, double epilogue. */
+void orc_gemv_a(int wtype, int atype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T,
+                double* Y) {
     int64_t wrow = K / orc_block_elems(wtype) * orc_block_bytes(wtype);
-    int64_t xrow = K / orc_block_elems(orc_act_type(wtype)) * orc_block_bytes(orc_act_type(wtype));
+    int64_t xrow = K / orc_block_elems(atype) * orc_block_bytes(atype);
     int64_t ncoef = K / orc_block_elems(wtype) * orc_coefs_per_block(wtype);
 #pragma omp parallel num_threads(g_threads)
     {
@@ -367,25 +408,38 @@ void orc_gemv(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* 
 #pragma omp for schedule(static)
         for (int64_t n = 0; n < N; ++n)
             for (int64_t t = 0; t < T; ++t)
-                Y[t * N + n] = row_dot_int(wtype, W + n * wrow, Xq + t * xrow, K, scratch);
+                Y[t * N + n] = row_dot_int(wtype, atype, W + n * wrow, Xq + t * xrow, K, scratch);
     }
 }
 
+void orc_gemv(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, double* Y) {
+    orc_gemv_a(wtype, orc_act_type(wtype), W, N, K, Xq, T, Y);
+}
+
 /* Per-block integer coefficients of every (t, n) pair: out[t][n][K/blk * ncoef]. */
-void orc_gemv_coefs(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, int32_t* out) {
+void orc_gemv_coefs_a(int wtype, int atype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T,
+                      int32_t* out) {
     int64_t wrow = K / orc_block_elems(wtype) * orc_block_bytes(wtype);
-    int64_t xrow = K / orc_block_elems(orc_act_type(wtype)) * orc_block_bytes(orc_act_type(wtype));
+    int64_t xrow = K / orc_block_elems(atype) * orc_block_bytes(atype);
     int64_t ncoef = K / orc_block_elems(wtype) * orc_coefs_per_block(wtype);
     for (int64_t t = 0; t < T; ++t)
         for (int64_t n = 0; n < N; ++n)
-            orc_row_coefs(wtype, W + n * wrow, Xq + t * xrow, K, out + (t * N + n) * ncoef);
+            orc_row_coefs_a(wtype, atype, W + n * wrow, Xq + t * xrow, K, out + (t * N + n) * ncoef);
+}
+
+void orc_gemv_coefs(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, int32_t* out) {
+    orc_gemv_coefs_a(wtype, orc_act_type(wtype), W, N, K, Xq, T, out);
 }
 
 /* Form B: dequantize both operands to double and take the plain dot.
  * If absdot is non-null it receives sum_k |w_k * x_k| (the tolerance scale). */
 void orc_gemv_dequant(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, double* Y,
                       double* absdot) {
-    int atype = orc_act_type(wtype);
+    orc_gemv_dequant_a(wtype, orc_act_type(wtype), W, N, K, Xq, T, Y, absdot);
+}
+
+void orc_gemv_dequant_a(int wtype, int atype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T,
+                        double* Y, double* absdot) {
     int64_t wrow = K / orc_block_elems(wtype) * orc_block_bytes(wtype);
     int64_t xrow = K / orc_block_elems(atype) * orc_block_bytes(atype);
 #pragma omp parallel num_threads(g_threads)
@@ -460,8 +514,10 @@ void orc_moe_gate_up(int gtype, const uint8_t* gate_bank, int utype, const uint8
         for (int64_t tk = 0; tk < T * k; ++tk)
             for (int64_t i = 0; i < I; ++i) {
                 int64_t t = tk / k, e = ids[tk];
-                double gv = row_dot_int(gtype, gate_bank + (e * I + i) * grow, xq + t * xrow, H, scratch);
-                double uv = row_dot_int(utype, up_bank + (e * I + i) * urow, xq + t * xrow, H, scratch);
+                double gv = row_dot_int(gtype, orc_act_type(gtype), gate_bank + (e * I + i) * grow, xq + t * xrow, H,
+                                        scratch);
+                double uv = row_dot_int(utype, orc_act_type(utype), up_bank + (e * I + i) * urow, xq + t * xrow, H,
+                                        scratch);
                 if (g) g[tk * I + i] = gv;
                 if (u) u[tk * I + i] = uv;
                 h[tk * I + i] = orc_silu(gv) * uv;
@@ -481,7 +537,8 @@ void orc_moe_down(int dtype, const uint8_t* down_bank, int64_t H, int64_t I, con
 #pragma omp for schedule(static) collapse(2)
         for (int64_t tk = 0; tk < T * k; ++tk)
             for (int64_t n = 0; n < H; ++n)
-                o[tk * H + n] = row_dot_int(dtype, down_bank + (ids[tk] * H + n) * drow, hq + tk * hrow, I, scratch);
+                o[tk * H + n] = row_dot_int(dtype, orc_act_type(dtype), down_bank + (ids[tk] * H + n) * drow,
+                                            hq + tk * hrow, I, scratch);
     }
 }
 

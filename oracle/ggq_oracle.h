@@ -26,9 +26,18 @@ void orc_dequant_block(int type, const uint8_t* b, double* out);
 void orc_dequant(int type, const uint8_t* blocks, int64_t rows, int64_t K, double* out);
 
 void orc_quantize_q8_1(const float* x, int64_t T, int64_t K, uint8_t* out);
+void orc_quantize_q8_0(const float* x, int64_t T, int64_t K, uint8_t* out);
 void orc_quantize_q8_k(const float* x, int64_t T, int64_t K, uint8_t* out);
 
+int orc_pair_ok(int wtype, int atype);
 void orc_row_coefs(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* coefs);
+void orc_row_coefs_a(int wtype, int atype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* coefs);
+void orc_gemv_a(int wtype, int atype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T,
+                double* Y);
+void orc_gemv_coefs_a(int wtype, int atype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T,
+                      int32_t* out);
+void orc_gemv_dequant_a(int wtype, int atype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T,
+                        double* Y, double* absdot);
 void orc_gemv(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, double* Y);
 void orc_gemv_coefs(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, int32_t* out);
 void orc_gemv_dequant(int wtype, const uint8_t* W, int64_t N, int64_t K, const uint8_t* Xq, int64_t T, double* Y,

@@ -39,8 +39,8 @@ MUTANTS = [
     ("silu sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     ("combine without the routing weight", "s += weights[t * k + j] * o[(t * k + j) * H + n];",
      "s += o[(t * k + j) * H + n];"),
-    ("q8_k sub-block offset", "qx = (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 32);",
-     "qx = (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 16);"),
+    ("q8_k sub-block offset", "default: return (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 32);",
+     "default: return (const int8_t*)(xrow + (j / 8) * 292 + 4 + (j % 8) * 16);"),
     ("fp16 subnormal scale", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -23);"),
     ("fp16 encode truncates", "double r = rint(ldexp(a, 11 - e));", "double r = floor(ldexp(a, 11 - e));"),
     ("mxfp4 dequant scale", "out[i] = ldexp((double)q, (int)b[0] - 128);", "out[i] = ldexp((double)q, (int)b[0] - 127);"),
@@ -48,6 +48,10 @@ MUTANTS = [
      "out[i] = orc_half_to_double(rd16(b)) * sc * q + orc_half_to_double(rd16(b + 2)) * m;"),
     ("q6_k dequant scale group", "(int8_t)b[192 + i / 16] * q; break;", "(int8_t)b[192 + i / 32] * q; break;"),
     ("q8_1 s without d", "float s = d * (float)sum;", "float s = (float)sum;"),
+    ("q8_0 activation scale from the wrong block", "case ORC_Q8_0: return orc_half_to_double(rd16(xrow + j * 34));",
+     "case ORC_Q8_0: return orc_half_to_double(rd16(xrow + (j ^ 1) * 34));"),
+    ("q8_0 activation quants shifted", "case ORC_Q8_0: return (const int8_t*)(xrow + j * 34 + 2);",
+     "case ORC_Q8_0: return (const int8_t*)(xrow + j * 34 + 1);"),
     ("q8_k bsums over 8", "for (int i = 0; i < 16; ++i) s += q[16 * g + i];",
      "for (int i = 0; i < 8; ++i) s += q[16 * g + i];"),
 ]

@@ -256,14 +256,14 @@ def _random_acts(g, T, K):
     return x
 
 
-@pytest.mark.parametrize("act", ["Q8_K", "Q8_1"])
+@pytest.mark.parametrize("act", ["Q8_K", "Q8_1", "Q8_0"])
 def test_quantizer_invariants(act):
     g = np.random.default_rng(4)
     T, K = 3, 1024
     x = _random_acts(g, T, K)
     out = orc.quantize(act, x)
     blk = 256 if act == "Q8_K" else 32
-    bb = 292 if act == "Q8_K" else 36
+    bb = {"Q8_K": 292, "Q8_1": 36, "Q8_0": 34}[act]
     for t in range(T):
         for j in range(K // blk):
             b = out[t, j * bb:(j + 1) * bb]
@@ -274,6 +274,9 @@ def test_quantizer_invariants(act):
                 d, q, bs = _q8k_fields(b)
                 assert d == d32
                 assert np.array_equal(bs, q.reshape(16, 16).sum(1))
+            elif act == "Q8_0":  # fp16 d, then the 32 quants (the Q8_0 weight layout)
+                d, q = b[0:2].view(np.float16)[0], b[2:34].view(np.int8).astype(int)
+                assert d == np.float16(d32)
             else:
                 d, s, q = _q8_1_fields(b)
                 assert d == np.float16(d32)
@@ -319,17 +322,17 @@ def test_integer_form_equals_dequant_form(fmt):
     assert C.shape == (T, N, K // syn.BLOCK_ELEMS[fmt] * orc.coefs_per_block(fmt))
 
 
-@pytest.mark.parametrize("fmt", ["Q4_0", "Q8_0", "MXFP4"])
-def test_block_coefs_brute_force_32_block_formats(fmt):
+@pytest.mark.parametrize("fmt,act", [("Q4_0", "Q8_1"), ("Q8_0", "Q8_K"), ("MXFP4", "Q8_K"), ("Q4_0", "Q8_0"),
+                                     ("Q8_0", "Q8_0")])
+def test_block_coefs_brute_force_32_block_formats(fmt, act):
     """S_b = sum of integer quants products, recovered element by element from the
     dequantized values: w / d_w (resp. w / 2^(e-128)) and x / d_x are integers."""
     g = syn.rng(98, 0)
     N, K, T = 3, 512, 2
     W = syn.weights(fmt, N, K, g)
     x = syn.activations(T, K, g)
-    act = orc.act_type(fmt)
     xq = orc.quantize(act, x)
-    C = orc.gemv_coefs(fmt, W, N, K, xq, T)
+    C = orc.gemv_coefs(fmt, W, N, K, xq, T, act=act)
     wd = orc.dequant(fmt, W, N, K)
     xd = orc.dequant(act, xq, T, K)
     nb = K // 32
@@ -342,10 +345,35 @@ def test_block_coefs_brute_force_32_block_formats(fmt):
             for t in range(T):
                 if act == "Q8_1":
                     dx = float(xq[t, b * 36:b * 36 + 2].view(np.float16)[0])
+                elif act == "Q8_0":
+                    dx = float(xq[t, b * 34:b * 34 + 2].view(np.float16)[0])
                 else:
                     dx = float(xq[t, (b // 8) * 292:(b // 8) * 292 + 4].view(np.float32)[0])
                 qx = np.round(xd[t, 32 * b:32 * b + 32] / dx)
                 assert C[t, n, b] == int(np.dot(qw, qx))
+
+
+@pytest.mark.parametrize("fmt", ["Q4_0", "Q8_0"])
+def test_q8_0_activation_pairings_integer_form_equals_dequant_form(fmt):
+    """The Q8_0 activation blocks ([VC523] What changed: Q8_0 x Q8_0) pair with
+    Q4_0 and Q8_0 weights; the integer form equals the dequantized dot."""
+    g = syn.rng(97, 1 + (fmt == "Q8_0"))
+    N, K, T = 9, 1024, 3
+    W = syn.weights(fmt, N, K, g)
+    x = syn.activations(T, K, g) * np.float32(2.5)
+    xq = orc.quantize("Q8_0", x)
+    Yi = orc.gemv(fmt, W, N, K, xq, T, act="Q8_0")
+    Yd, A = orc.gemv_dequant(fmt, W, N, K, xq, T, act="Q8_0")
+    assert np.all(np.abs(Yi - Yd) <= 1e-12 * A)
+    # the same dot through the Q8_1 blocks of the same x: Q8_1 and Q8_0 share d and q
+    q81 = orc.quantize("Q8_1", x).reshape(T, K // 32, 36)
+    q80 = xq.reshape(T, K // 32, 34)
+    assert np.array_equal(q81[..., 0:2], q80[..., 0:2]) and np.array_equal(q81[..., 4:], q80[..., 2:])
+    if fmt == "Q4_0":
+        assert np.array_equal(orc.gemv_coefs(fmt, W, N, K, xq, T, act="Q8_0"),
+                              orc.gemv_coefs(fmt, W, N, K, q81.reshape(T, -1), T))
+    with pytest.raises(ValueError):
+        orc.gemv("Q4_K", syn.weights("Q4_K", 1, 256, g), 1, 256, orc.quantize("Q8_0", x[:1, :256]), 1, act="Q8_0")
 
 
 # ------------------------------------------------------------- router
