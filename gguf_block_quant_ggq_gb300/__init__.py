@@ -41,6 +41,10 @@ SIGNATURES = {
     "ggq_moe_experts_routed": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _P]),
     "ggq_sync_status": (_I32, [_P, _P]),
     "ggq_mul_mat_vec_noalloc": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "ggq_set_moe_counters": (_I32, [_P, _P, _I64, _P]),
+    "ggq_moe_experts_q": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _P, _P]),
+    "ggq_mul_mat_vec_qa": (_I32, [_P, _I32, _I32, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "ggq_block_dots_qa": (_I32, [_P, _I32, _I32, _P, _I64, _I64, _P, _I64, _P, _P]),
 }
 
 
@@ -163,6 +167,11 @@ class Context:
     def scratch_bytes(self) -> int:
         return load().ggq_scratch_bytes(self.handle)
 
+    def set_moe_counters(self, pairs=None, calls=None):
+        """Expert-load telemetry: int64 CUDA tensors pairs [E] and calls [2], or None to stop."""
+        n = 0 if pairs is None else pairs.numel()
+        self._check(load().ggq_set_moe_counters(self.handle, _ptr(pairs, "int64"), n, _ptr(calls, "int64")))
+
     def sync_status(self, stream=None):
         self._check(load().ggq_sync_status(self.handle, self._stream(stream)))
 
@@ -198,6 +207,20 @@ class Context:
                                              self._stream(stream)))
         return Y
 
+    def mul_mat_vec_qa(self, fmt: str, act: str, W, N: int, K: int, Xq, T: int, Y=None, stream=None):
+        if Y is None:
+            Y = self._torch.empty((T, N), dtype=self._torch.float32, device=Xq.device)
+        self._check(load().ggq_mul_mat_vec_qa(self.handle, TYPE[fmt], TYPE[act], _ptr(W), N, K, _ptr(Xq), T,
+                                              _ptr(Y, "float32"), self._stream(stream)))
+        return Y
+
+    def block_dots_qa(self, fmt: str, act: str, W, N: int, K: int, Xq, T: int, stream=None):
+        nc = K // BLOCK_ELEMS[fmt] * (2 if fmt in ("Q4_K", "Q5_K") else 1)
+        out = self._torch.empty((T, N, nc), dtype=self._torch.int32, device=Xq.device)
+        self._check(load().ggq_block_dots_qa(self.handle, TYPE[fmt], TYPE[act], _ptr(W), N, K, _ptr(Xq), T,
+                                             _ptr(out), self._stream(stream)))
+        return out
+
     def block_dots(self, fmt: str, W, N: int, K: int, Xq, T: int, stream=None):
         nc = K // BLOCK_ELEMS[fmt] * (2 if fmt in ("Q4_K", "Q5_K") else 1)
         out = self._torch.empty((T, N, nc), dtype=self._torch.int32, device=Xq.device)
@@ -228,6 +251,23 @@ class Context:
                                                dp, self._stream(stream))
         self._check(st)
         return Y
+
+
+def _moe_q(ctx, weights, E, H, I, top_k, Xq, logits, Y=None, dump=None, stream=None, reserve=True):
+    """ggq_moe_experts_q: the layer on pre-quantized Q8_K activations Xq [T][H/256*292] (uint8)."""
+    T = Xq.shape[0]
+    if Y is None:
+        Y = ctx._torch.empty((T, H), dtype=ctx._torch.float32, device=Xq.device)
+    if reserve:
+        ctx.reserve(max_tokens=T, n_experts=E, hidden=H, inter=I, top_k=top_k, stream=stream)
+    d = ggq_moe_dump(**{k: _ptr(v) for k, v in dump.items()}) if dump is not None else None
+    ctx._check(load().ggq_moe_experts_q(ctx.handle, ctypes.byref(weights), E, H, I, top_k, _ptr(Xq, "uint8"),
+                                        _ptr(logits, "float32"), T, _ptr(Y, "float32"),
+                                        ctypes.byref(d) if d is not None else None, ctx._stream(stream)))
+    return Y
+
+
+Context.moe_experts_q = _moe_q
 
 
 def supported(w: str, act: str, op: str) -> bool:

@@ -24,6 +24,7 @@
 namespace ggq {
 cudaError_t launch_gemv_a(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_gemv_b(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_gemv_q80(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_gateup(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_down(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_downf(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
@@ -163,6 +164,9 @@ struct ggq_ctx {
     std::vector<void*> retired;
     Ctrl* ctrl = nullptr;
     int static_weights = 0;  // weights never written while calls are in flight
+    unsigned long long* tel_pairs = nullptr;  // expert-load telemetry (caller's device buffers)
+    unsigned long long* tel_calls = nullptr;
+    int64_t tel_experts = 0;
     std::string err;
 };
 
@@ -248,8 +252,15 @@ ggq_status check_ctx(ggq_ctx* c, DeviceScope& scope) {
 }
 
 ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, const void* X, int64_t T,
-                       const void* Y) {
+                       const void* Y, int act = -1) {
     const int f = fmt_of(w);
+    if (act >= 0 && act != (f == F_Q4_0 ? GGQ_TYPE_Q8_1 : GGQ_TYPE_Q8_K) &&
+        !(act == GGQ_TYPE_Q8_0 && (f == F_Q4_0 || f == F_Q8_0)))
+        return fail(c, GGQ_ERR_UNSUPPORTED,
+                    "mul_mat_vec: weight type %d (%s) with activation type %d (%s) is not supported; supported: "
+                    "Q4_0 x Q8_1, Q4_0 x Q8_0, Q8_0 x Q8_0, and Q8_0, Q4_K, Q5_K, Q6_K, MXFP4 x Q8_K",
+                    w, type_name(w), act, type_name(act));
+    const bool a80 = act == GGQ_TYPE_Q8_0;
     if (f < 0 || w == GGQ_TYPE_Q8_1 || w == GGQ_TYPE_Q8_K)
         return fail(c, GGQ_ERR_UNSUPPORTED,
                     "mul_mat_vec: weight type %d (%s) is not supported; supported: Q4_0 x Q8_1, and Q8_0, Q4_K, "
@@ -260,7 +271,7 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
         return fail(c, GGQ_ERR_INVALID_ARG, "mul_mat_vec: pointers must be 16-byte aligned");
     if (T < 1 || T > 8) return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: T=%lld out of 1..8", static_cast<long long>(T));
     if (N < 1) return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: N=%lld", static_cast<long long>(N));
-    const int64_t ablk = f == F_Q4_0 ? 32 : 256;
+    const int64_t ablk = f == F_Q4_0 || a80 ? 32 : 256;
     if (K < 1 || K % fmt_qk(f) || K % ablk)
         return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld must be a multiple of %lld for %s", static_cast<long long>(K),
                     static_cast<long long>(ablk > fmt_qk(f) ? ablk : fmt_qk(f)), type_name(w));
@@ -268,7 +279,7 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
     {  // token groups shrink down to one token, so the call runs if one token fits: refuse before any launch
         StreamShape sh;
         int cu = 0, cb = 0, rs = 0;
-        if (plan_gemv_stream(f, w_row_bytes(f, K), 1, static_cast<int>(K), f == F_Q4_0, &sh, &cu, &cb, &rs) ==
+        if (plan_gemv_stream(f, w_row_bytes(f, K), 1, static_cast<int>(K), f == F_Q4_0 || a80, &sh, &cu, &cb, &rs) ==
             StreamPlan::kNone)
             return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: rows of K=%lld do not fit in shared memory",
                         static_cast<long long>(K));
@@ -305,11 +316,11 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
 constexpr int kMmaMinTokens = 2;
 
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
-                            int64_t T, float* Y, int32_t* coefs, cudaStream_t st) {
+                            int64_t T, float* Y, int32_t* coefs, cudaStream_t st, bool a80 = false) {
     const int f = fmt_of(w);
     const bool dump = kind == KIND_DUMP;
     const int ncoef = static_cast<int>(K / fmt_qk(f) * fmt_coefs(f));
-    if (T >= kMmaMinTokens && f != F_Q4_0 && aligned16(Xq)) {
+    if (!a80 && T >= kMmaMinTokens && f != F_Q4_0 && aligned16(Xq)) {
         MmavParams m{};
         m.W = static_cast<const uint8_t*>(W);
         m.rowbytes = w_row_bytes(f, K);
@@ -338,7 +349,7 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
             return GGQ_OK;
         }
     }
-    if (T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
+    if (!a80 && T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
         // several activation columns: the int8 tensor-core kernel (Q8_K rows are 16-byte multiples)
         GroupParams g{};
         g.W = static_cast<const uint8_t*>(W);
@@ -381,22 +392,23 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     p.err = &c->ctrl->err;
     p.early_weights = c->static_weights;
     StreamShape sh;
+    const bool a32 = f == F_Q4_0 || a80;  // activation scales per 32 elements
     if (kind == KIND_GEMV) {
-        const StreamPlan plan = plan_gemv_stream(f, p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh, &p.chunk_units,
+        const StreamPlan plan = plan_gemv_stream(f, p.rowbytes, p.xrows, p.K, a32, &sh, &p.chunk_units,
                                                  &p.chunk_bytes, &p.row_slot);
         if (plan == StreamPlan::kSplit) {
             // the tokens as two groups, each streaming the weights once
-            const int64_t xrow = f == F_Q4_0 ? K / 32 * 36 : K / 256 * 292;
+            const int64_t xrow = a80 ? K / 32 * 34 : f == F_Q4_0 ? K / 32 * 36 : K / 256 * 292;
             const int64_t T0 = T / 2;
-            const ggq_status s0 = launch_gemv_kind(c, kind, w, W, N, K, Xq, T0, Y, coefs, st);
+            const ggq_status s0 = launch_gemv_kind(c, kind, w, W, N, K, Xq, T0, Y, coefs, st, a80);
             if (s0 != GGQ_OK) return s0;
             return launch_gemv_kind(c, kind, w, W, N, K, static_cast<const uint8_t*>(Xq) + T0 * xrow, T - T0,
-                                    Y + T0 * N, coefs, st);
+                                    Y + T0 * N, coefs, st, a80);
         }
         if (plan == StreamPlan::kNone)
             return fail(c, GGQ_ERR_SHAPE, "mul_mat_vec: K=%lld does not fit in shared memory",
                         static_cast<long long>(K));
-    } else if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, f == F_Q4_0, &sh)) {
+    } else if (!plan_stream(kTileRows * p.rowbytes, p.xrows, p.K, a32, &sh)) {
         return fail(c, GGQ_ERR_SHAPE, "block_dots: K=%lld with T=%lld does not fit in shared memory",
                     static_cast<long long>(K), static_cast<long long>(T));
     }
@@ -405,7 +417,8 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     p.x_bytes = sh.x_bytes;
     const int64_t tiles = (N + kTileRows - 1) / kTileRows;
     const int grid = static_cast<int>(tiles < c->nsm ? tiles : c->nsm);
-    cudaError_t e = launch_stream(kind, f, pow2_tokens(T), p, grid, sh.smem, st);
+    cudaError_t e = a80 ? launch_gemv_q80(kind, f, pow2_tokens(T), p, grid, sh.smem, st)
+                        : launch_stream(kind, f, pow2_tokens(T), p, grid, sh.smem, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "mul_mat_vec launch");
     return GGQ_OK;
 }
@@ -463,8 +476,8 @@ const char* moe_width_refusal(int fg, int fd, int64_t H, int64_t I, int64_t T, i
 }
 
 ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
-                      const float* X, const float* logits, const int32_t* ids_in, const float* w_in, int64_t T,
-                      float* Y, const ggq_moe_dump* dump, void* stream) {
+                      const float* X, const uint8_t* xq_in, const float* logits, const int32_t* ids_in,
+                      const float* w_in, int64_t T, float* Y, const ggq_moe_dump* dump, void* stream) {
     const int fg = fmt_of(w->gate_type), fd = fmt_of(w->down_type);
     int32_t* const cg = dump ? dump->coefs_gate : nullptr;  // integer-core dumps (gate and up go together)
     int32_t* const cu = dump ? dump->coefs_up : nullptr;
@@ -479,6 +492,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     uint8_t* base = c->pool;
     auto I32 = [&](size_t off) { return reinterpret_cast<int*>(base + off); };
     uint8_t* xq = base + ms.xq;
+    const int64_t xrow = H / 256 * 292;
     uint8_t* hq = base + ms.hq;
     float* wts = reinterpret_cast<float*>(base + ms.w);
     float* h = reinterpret_cast<float*>(base + ms.h);
@@ -488,11 +502,16 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
 
     cudaError_t e = cudaMemsetAsync(I32(ms.counts), 0, static_cast<size_t>(E) * 4, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: memset");
-    e = launch_route_sorted(logits, ids_in, w_in, X, static_cast<int>(T), static_cast<int>(E), top_k,
+    if (xq_in) {  // x^ given: its rows at the 16-byte pitch of the grouped kernels' row copies
+        e = cudaMemcpy2DAsync(xq, static_cast<size_t>(q8k_pitch(H)), xq_in, static_cast<size_t>(xrow),
+                              static_cast<size_t>(xrow), static_cast<size_t>(T), cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x^ copy");
+    }
+    e = launch_route_sorted(logits, ids_in, w_in, xq_in ? nullptr : X, static_cast<int>(T), static_cast<int>(E), top_k,
                             static_cast<int>(H), xq, xp, I32(ms.ids), wts, I32(ms.counts), &c->ctrl->err, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: route launch");
     e = launch_group_plan(I32(ms.counts), static_cast<int>(E), I32(ms.offsets), I32(ms.cursor), I32(ms.ngroups),
-                          I32(ms.gexp), I32(ms.goff), I32(ms.gcnt), st);
+                          I32(ms.gexp), I32(ms.goff), I32(ms.gcnt), st, c->tel_pairs, c->tel_calls);
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: plan launch");
     e = launch_scatter(I32(ms.ids), P, static_cast<int>(E), I32(ms.offsets), I32(ms.cursor), I32(ms.perm), st);
     if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: scatter launch");
@@ -667,10 +686,12 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
 }
 
 ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k, const float* X,
-                   const float* logits, const int32_t* ids, const float* weights, int64_t T, float* Y,
-                   const ggq_moe_dump* dump, void* stream) {
-    if (!w || !X || !Y || (!logits && (!ids || !weights)))
+                   const uint8_t* xq_in, const float* logits, const int32_t* ids, const float* weights, int64_t T,
+                   float* Y, const ggq_moe_dump* dump, void* stream) {
+    if (!w || (!X && !xq_in) || !Y || (!logits && (!ids || !weights)))
         return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null pointer");
+    if (xq_in && (reinterpret_cast<uintptr_t>(xq_in) & 3))
+        return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts_q: Xq must be 4-byte aligned");
     const int fg = fmt_of(w->gate_type), fu = fmt_of(w->up_type), fd = fmt_of(w->down_type);
     for (int t : {w->gate_type, w->up_type, w->down_type}) {
         const int f = fmt_of(t);
@@ -686,7 +707,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     if (dump && (dump->coefs_gate == nullptr) != (dump->coefs_up == nullptr))
         return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: coefs_gate and coefs_up are dumped together");
     if (!w->gate || !w->up || !w->down) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null bank");
-    if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down) || !aligned16(X) || !aligned16(Y))
+    if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down) || (X && !aligned16(X)) || !aligned16(Y))
         return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: pointers must be 16-byte aligned");
     if (H < 256 || H % 256 || I < 256 || I % 256)
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: H=%lld and I=%lld must be positive multiples of 256",
@@ -695,7 +716,11 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: need 1 <= top_k <= 8 and top_k <= E <= 4096");
     if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
     if (const char* why = moe_width_refusal(fg, fd, H, I, T, top_k)) return fail(c, GGQ_ERR_SHAPE, "%s", why);
-    if (T > kDirectMaxTokens) return moe_sorted(c, w, E, H, I, top_k, X, logits, ids, weights, T, Y, dump, stream);
+    if (c->tel_pairs && E > c->tel_experts)
+        return fail(c, GGQ_ERR_SHAPE, "moe_experts: E=%lld exceeds the %lld experts of the telemetry buffer",
+                    static_cast<long long>(E), static_cast<long long>(c->tel_experts));
+    if (T > kDirectMaxTokens)
+        return moe_sorted(c, w, E, H, I, top_k, X, xq_in, logits, ids, weights, T, Y, dump, stream);
     const MoeScratch ms = moe_scratch(T, H, I, top_k);
     ggq_status s = need_scratch(c, ms.total);
     if (s != GGQ_OK) return s;
@@ -706,13 +731,14 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     p.E = static_cast<int>(E);
     p.top_k = top_k;
     p.X = X;
+    p.xq_in = xq_in;
     p.logits = logits;
     p.ids_in = ids;
     p.w_in = weights;
     p.ids = reinterpret_cast<int32_t*>(c->pool + ms.ids);
     p.w = reinterpret_cast<float*>(c->pool + ms.w);
     p.h = reinterpret_cast<float*>(c->pool + ms.h);
-    p.xq_dump = dump ? static_cast<uint8_t*>(dump->xq) : nullptr;
+    p.xq_dump = dump && !xq_in ? static_cast<uint8_t*>(dump->xq) : nullptr;
     p.hq = c->pool + ms.hq;
     p.early_weights = c->static_weights;
     p.g_dump = dump ? dump->g : nullptr;
@@ -721,6 +747,8 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     p.coefs[0] = dump ? dump->coefs_gate : nullptr;
     p.coefs[1] = dump ? dump->coefs_up : nullptr;
     p.ncoef = static_cast<int>(H / fmt_qk(fg) * fmt_coefs(fg));
+    p.tel_pairs = c->tel_pairs;
+    p.tel_calls = c->tel_calls;
     p.Y = Y;
     p.err = &c->ctrl->err;
     const int nt = pow2_tokens(T);
@@ -753,6 +781,8 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         p.K = static_cast<int>(I);
         p.coefs[0] = dump ? dump->coefs_down : nullptr;
         p.coefs[1] = nullptr;
+        p.tel_pairs = nullptr;  // counted once, by the gate/up kernel
+        p.tel_calls = nullptr;
         p.ncoef = static_cast<int>(I / fmt_qk(fd) * fmt_coefs(fd));
         const bool fused = !(dump && (dump->o || dump->coefs_down));
         StreamShape sh;
@@ -780,6 +810,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     }
     if (dump) {
         struct Cp { void* dst; const void* src; size_t n; } cps[] = {
+            {xq_in ? dump->xq : nullptr, xq_in, static_cast<size_t>(T) * (H / 256) * 292},
             {dump->ids, p.ids, static_cast<size_t>(P) * 4},
             {dump->weights, p.w, static_cast<size_t>(P) * 4},
             {dump->h, p.h, static_cast<size_t>(P) * I * 4},
@@ -882,10 +913,11 @@ ggq_status ggq_reserve(ggq_ctx* c, const ggq_plan* plan, void* stream) {
 int ggq_supported(int w, int act, int op) {
     const int f = fmt_of(w);
     switch (op) {
-    case GGQ_OP_QUANTIZE_ACT: return act == GGQ_TYPE_Q8_1 || act == GGQ_TYPE_Q8_K;
+    case GGQ_OP_QUANTIZE_ACT: return act == GGQ_TYPE_Q8_1 || act == GGQ_TYPE_Q8_K || act == GGQ_TYPE_Q8_0;
     case GGQ_OP_DEQUANT: return f >= 0;
     case GGQ_OP_MUL_MAT_VEC:
         if (f < 0) return 0;
+        if (act == GGQ_TYPE_Q8_0) return f == F_Q4_0 || f == F_Q8_0;
         return f == F_Q4_0 ? act == GGQ_TYPE_Q8_1 : act == GGQ_TYPE_Q8_K;
     case GGQ_OP_MOE: return f >= 0 && f != F_Q4_0 && act == GGQ_TYPE_Q8_K;
     default: return 0;
@@ -896,10 +928,10 @@ ggq_status ggq_quantize_act(ggq_ctx* c, int act, const float* x, int64_t T, int6
     DeviceScope scope;
     ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
-    if (act != GGQ_TYPE_Q8_1 && act != GGQ_TYPE_Q8_K)
-        return fail(c, GGQ_ERR_UNSUPPORTED, "quantize_act: activation type %d (%s); supported: Q8_1, Q8_K", act,
+    if (act != GGQ_TYPE_Q8_1 && act != GGQ_TYPE_Q8_K && act != GGQ_TYPE_Q8_0)
+        return fail(c, GGQ_ERR_UNSUPPORTED, "quantize_act: activation type %d (%s); supported: Q8_1, Q8_0, Q8_K", act,
                     type_name(act));
-    const int64_t blk = act == GGQ_TYPE_Q8_1 ? 32 : 256;
+    const int64_t blk = act == GGQ_TYPE_Q8_K ? 256 : 32;
     if (T < 0 || K < 0 || K % blk)
         return fail(c, GGQ_ERR_SHAPE, "quantize_act: T=%lld, K=%lld (K must be a multiple of %lld)",
                     static_cast<long long>(T), static_cast<long long>(K), static_cast<long long>(blk));
@@ -907,8 +939,8 @@ ggq_status ggq_quantize_act(ggq_ctx* c, int act, const float* x, int64_t T, int6
     if (!x || !out) return fail(c, GGQ_ERR_INVALID_ARG, "quantize_act: null pointer");
     if (!aligned16(x) || (reinterpret_cast<uintptr_t>(out) & 3))
         return fail(c, GGQ_ERR_INVALID_ARG, "quantize_act: x must be 16-byte and out 4-byte aligned");
-    cudaError_t e = launch_quantize(act == GGQ_TYPE_Q8_1 ? 0 : 1, x, T, K, static_cast<uint8_t*>(out),
-                                    static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_quantize(act == GGQ_TYPE_Q8_1 ? 0 : act == GGQ_TYPE_Q8_K ? 1 : 2, x, T, K,
+                                    static_cast<uint8_t*>(out), static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GGQ_OK : cuda_fail(c, e, "quantize_act launch");
 }
 
@@ -966,6 +998,28 @@ ggq_status ggq_block_dots(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K
     return launch_gemv_kind(c, KIND_DUMP, w, W, N, K, Xq, T, nullptr, coefs, static_cast<cudaStream_t>(stream));
 }
 
+ggq_status ggq_mul_mat_vec_qa(ggq_ctx* c, int w, int act, const void* W, int64_t N, int64_t K, const void* Xq,
+                              int64_t T, float* Y, void* stream) {
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
+    if (s != GGQ_OK) return s;
+    s = gemv_checks(c, w, W, N, K, Xq, T, Y, act);
+    if (s != GGQ_OK) return s;
+    return launch_gemv_kind(c, KIND_GEMV, w, W, N, K, Xq, T, Y, nullptr, static_cast<cudaStream_t>(stream),
+                            act == GGQ_TYPE_Q8_0);
+}
+
+ggq_status ggq_block_dots_qa(ggq_ctx* c, int w, int act, const void* W, int64_t N, int64_t K, const void* Xq,
+                             int64_t T, int32_t* coefs, void* stream) {
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
+    if (s != GGQ_OK) return s;
+    s = gemv_checks(c, w, W, N, K, Xq, T, coefs, act);
+    if (s != GGQ_OK) return s;
+    return launch_gemv_kind(c, KIND_DUMP, w, W, N, K, Xq, T, nullptr, coefs, static_cast<cudaStream_t>(stream),
+                            act == GGQ_TYPE_Q8_0);
+}
+
 ggq_status ggq_moe_experts(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
                            const float* X, const float* router_logits, int64_t T, float* Y, const ggq_moe_dump* dump,
                            void* stream) {
@@ -973,7 +1027,7 @@ ggq_status ggq_moe_experts(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int6
     ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     if (!router_logits) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts: null router_logits");
-    return moe_run(c, w, E, H, I, top_k, X, router_logits, nullptr, nullptr, T, Y, dump, stream);
+    return moe_run(c, w, E, H, I, top_k, X, nullptr, router_logits, nullptr, nullptr, T, Y, dump, stream);
 }
 
 ggq_status ggq_moe_experts_routed(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I,
@@ -983,7 +1037,32 @@ ggq_status ggq_moe_experts_routed(ggq_ctx* c, const ggq_moe_weights* w, int64_t 
     ggq_status s = check_ctx(c, scope);
     if (s != GGQ_OK) return s;
     if (!ids || !weights) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts_routed: null ids/weights");
-    return moe_run(c, w, E, H, I, top_k, X, nullptr, ids, weights, T, Y, dump, stream);
+    return moe_run(c, w, E, H, I, top_k, X, nullptr, nullptr, ids, weights, T, Y, dump, stream);
+}
+
+ggq_status ggq_set_moe_counters(ggq_ctx* c, int64_t* pairs, int64_t n_experts, int64_t* calls) {
+    if (!c) return GGQ_ERR_INVALID_ARG;
+    if ((pairs == nullptr) != (calls == nullptr))
+        return fail(c, GGQ_ERR_INVALID_ARG, "set_moe_counters: pairs and calls are set or cleared together");
+    if (pairs && (n_experts < 1 || n_experts > 4096))
+        return fail(c, GGQ_ERR_SHAPE, "set_moe_counters: n_experts=%lld out of 1..4096", static_cast<long long>(n_experts));
+    if ((reinterpret_cast<uintptr_t>(pairs) | reinterpret_cast<uintptr_t>(calls)) & 7)
+        return fail(c, GGQ_ERR_INVALID_ARG, "set_moe_counters: buffers must be 8-byte aligned");
+    c->tel_pairs = reinterpret_cast<unsigned long long*>(pairs);
+    c->tel_calls = reinterpret_cast<unsigned long long*>(calls);
+    c->tel_experts = pairs ? n_experts : 0;
+    return GGQ_OK;
+}
+
+ggq_status ggq_moe_experts_q(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
+                             const void* Xq, const float* router_logits, int64_t T, float* Y, const ggq_moe_dump* dump,
+                             void* stream) {
+    DeviceScope scope;
+    ggq_status s = check_ctx(c, scope);
+    if (s != GGQ_OK) return s;
+    if (!router_logits || !Xq) return fail(c, GGQ_ERR_INVALID_ARG, "moe_experts_q: null Xq or router_logits");
+    return moe_run(c, w, E, H, I, top_k, nullptr, static_cast<const uint8_t*>(Xq), router_logits, nullptr, nullptr, T,
+                   Y, dump, stream);
 }
 
 ggq_status ggq_sync_status(ggq_ctx* c, void* stream) {

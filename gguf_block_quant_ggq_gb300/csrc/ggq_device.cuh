@@ -407,9 +407,9 @@ __device__ __forceinline__ void unit_ints(const Unit& un, const int* xo, const X
 }
 
 // Scale epilogue of unit u: fp32 contribution of (A0, A1).
-template <int F>
+template <int F, bool A32 = (F == F_Q4_0)>
 __device__ __forceinline__ float unit_value(const Unit& un, const XS& xs, int r, int u, int A0, int A1) {
-    if constexpr (F == F_Q4_0) {
+    if constexpr (F == F_Q4_0 || (F == F_Q8_0 && A32)) {  // one activation scale per 32 elements
         const saddr d = xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 5));
         const float d1 = 2 * u + 1 < (xs.K >> 5) ? ld_f32(d + 8 * u + 4) : 0.0f;
         return static_cast<float>(A0) * (un.da * ld_f32(d + 8 * u)) + static_cast<float>(A1) * (un.db * d1);
@@ -446,7 +446,7 @@ struct XUnit {
     float d0, d1;
 };
 
-template <int F>
+template <int F, bool A32 = (F == F_Q4_0)>
 __device__ __forceinline__ void load_xunit(const XS& xs, int u, XUnit& xu) {
     const int nb32 = xs.K >> 5;
     int xo[4];
@@ -463,11 +463,13 @@ __device__ __forceinline__ void load_xunit(const XS& xs, int u, XUnit& xu) {
     const int s0 = static_cast<int>(ld_s32(xs.s32 + 8u * u));
     const int s1 = two ? static_cast<int>(ld_s32(xs.s32 + 8u * u + 4)) : 0;
     xu.c[0] = xu.c[1] = xu.c[2] = xu.c[3] = 0;
-    if constexpr (F == F_Q4_0) {
+    if constexpr (F == F_Q4_0 || (F == F_Q8_0 && A32)) {  // per-32 activation scales
         xu.d0 = ld_f32(xs.d + 8u * u);
         xu.d1 = two ? ld_f32(xs.d + 8u * u + 4) : 0.0f;
-        xu.c[0] = 8 * s0;
-        xu.c[1] = 8 * s1;
+        if constexpr (F == F_Q4_0) {
+            xu.c[0] = 8 * s0;
+            xu.c[1] = 8 * s1;
+        }
     } else {
         xu.d0 = ld_f32(xs.d + 4u * static_cast<uint32_t>(u >> 2));
         xu.d1 = 0.0f;
@@ -488,7 +490,7 @@ __device__ __forceinline__ void load_xunit(const XS& xs, int u, XUnit& xu) {
 // register-resident activations.  High nibbles are masked in place (16x their
 // value, as unsigned bytes) and the exact factor 16 is shifted out of the
 // integer sum, which saves a shift per weight word.
-template <int F>
+template <int F, bool A32 = (F == F_Q4_0)>
 __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const XUnit& xu) {
     if constexpr (F == F_Q4_0) {
         const saddr b = row + 36u * u;
@@ -535,6 +537,7 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
             S0 = __dp4a(static_cast<int>(w[k]), static_cast<int>(xu.x[k]), S0);
             S1 = __dp4a(static_cast<int>(w[8 + k]), static_cast<int>(xu.x[8 + k]), S1);
         }
+        if constexpr (A32) return static_cast<float>(S0) * (da * xu.d0) + static_cast<float>(S1) * (db * xu.d1);
         return xu.d0 * (static_cast<float>(S0) * da + static_cast<float>(S1) * db);
     } else if constexpr (F == F_MXFP4) {
         const saddr b = row + 34u * u;
@@ -722,6 +725,19 @@ __device__ __forceinline__ void warp_quant_q8_1(const float* src, uint8_t* dst, 
         reinterpret_cast<__half*>(dst)[0] = hd;
         reinterpret_cast<__half*>(dst)[1] = hs;
     }
+}
+
+// One warp quantizes one 32-element block to a Q8_0 activation block (34
+// bytes at dst, 2-byte aligned): fp16 d, then the 32 quants -- the Q8_0
+// weight layout, with the Q8_1 quantizer's arithmetic.
+__device__ __forceinline__ void warp_quant_q8_0(const float* src, uint8_t* dst, int lane) {
+    const float x = src[lane];
+    const float amax = warp_max(fabsf(x));
+    float id;
+    const float d = quant_scale(amax, &id);
+    const int q = quant_one(x, id);
+    dst[2 + lane] = static_cast<uint8_t>(q & 0xFF);
+    if (lane == 0) reinterpret_cast<__half*>(dst)[0] = __float2half_rn(d);
 }
 
 }  // namespace ggq

@@ -234,6 +234,7 @@ struct DirectParams {
     float* w;                    // routed weights [T*k]
     float* h;                    // [T*k][I]
     uint8_t* xq_dump;            // optional packed Q8_K of x
+    const uint8_t* xq_in;        // gate/up: x already quantized, packed Q8_K [T][K/256] (X then unused)
     uint8_t* hq;                 // optional packed Q8_K of h (down CTA 0)
     int early_weights;
     int G;                       // fused down: experts per stage           // 1: stream weights before waiting for the previous kernel
@@ -245,6 +246,8 @@ struct DirectParams {
     int stages, stage_stride, x_bytes;
     int32_t* coefs[2];           // optional integer-core dump [T*k][N][ncoef]: gate and up, or down
     int ncoef;                   // coefficients per row: K/blk * (2 for Q4_K/Q5_K, else 1)
+    unsigned long long* tel_pairs;  // optional expert-load telemetry: pairs per expert [E]
+    unsigned long long* tel_calls;  // and [calls, distinct experts]
 };
 
 // Gate/up (KIND_GATEUP), down with per-pair outputs (KIND_DOWN) or fused
@@ -302,6 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
         p.ids[tid] = plan->ids[tid];
         p.w[tid] = plan->wt[tid];
         if (plan->bad && tid == 0) set_error(p.err, DEV_ERR_BAD_IDS);
+        if (p.tel_pairs && tid < D) atomicAdd(p.tel_pairs + plan->expert[tid], static_cast<unsigned long long>(plan->npairs[tid]));
+        if (p.tel_calls && tid == 0) {
+            atomicAdd(p.tel_calls, 1ull);
+            atomicAdd(p.tel_calls + 1, static_cast<unsigned long long>(D));
+        }
     }
     const int tiles = static_cast<int>(p.N / kTileRows);
     const int nitems = KIND == KIND_GATEUP ? D * tiles : (D > 0 ? tiles : 0);
@@ -360,8 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
 
     // ================= consumers: the activations into shared memory
     if constexpr (KIND == KIND_GATEUP) {
-        // quantize x (every CTA; a few blocks per warp, their loads issued together)
-        const int nbr = K >> 8, nb = xrows * nbr;
+        // x^ given (the "Q8 prequant" entry): staged as it is
+        if (p.xq_in) stage_acts<false, F == F_MXFP4>(p.xq_in, xrows, K, xr_, tid, kConsumerWarps * 32);
+        // else quantize x (every CTA; a few blocks per warp, their loads issued together)
+        const int nbr = K >> 8, nb = p.xq_in ? 0 : xrows * nbr;
         for (int b0 = warp; b0 < nb; b0 += 4 * kConsumerWarps) {
             float4 va[4], vb[4];
 #pragma unroll

@@ -190,8 +190,10 @@ cudaError_t launch_quantize_pitched(const float* x, int64_t rows, int64_t K, uin
 cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, const float* w_in, const float* X, int T,
                                 int E, int k, int H, uint8_t* xq, int64_t x_pitch, int32_t* ids, float* w,
                                 int* counts, int* err, cudaStream_t s);
+// tel_pairs / tel_calls: optional expert-load telemetry (pairs per expert; calls and distinct experts).
 cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
-                              int* group_off, int* group_cnt, cudaStream_t s);
+                              int* group_off, int* group_cnt, cudaStream_t s, unsigned long long* tel_pairs = nullptr,
+                              unsigned long long* tel_calls = nullptr);
 cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
                            cudaStream_t s);
 cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, int div, int64_t rows, int64_t K,

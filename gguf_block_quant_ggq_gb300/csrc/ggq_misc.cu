@@ -33,16 +33,25 @@ __global__ void k_quant_q8_1(const float* __restrict__ x, int64_t nblocks, uint8
     warp_quant_q8_1(x + b * 32, out + b * 36, lane);
 }
 
+__global__ void k_quant_q8_0(const float* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= nblocks) return;
+    warp_quant_q8_0(x + b * 32, out + b * 34, lane);
+}
+
 cudaError_t launch_quantize(int act, const float* x, int64_t T, int64_t K, uint8_t* out, cudaStream_t s) {
-    const int64_t nb = T * K / (act == 0 ? 32 : 256);  // act: 0 = Q8_1, 1 = Q8_K
+    const int64_t nb = T * K / (act == 1 ? 256 : 32);  // act: 0 = Q8_1, 1 = Q8_K, 2 = Q8_0
     if (nb == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (nb * 32 + threads - 1) / threads;
     if (act == 0)
         return launch_pdl(k_quant_q8_1, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, x, nb, out);
-    else
-        return launch_pdl(k_quant_q8k, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, x, nb, out);
-    return cudaGetLastError();
+    if (act == 2)
+        return launch_pdl(k_quant_q8_0, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, x, nb, out);
+    return launch_pdl(k_quant_q8k, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, x, nb, out);
 }
 
 // ---------------------------------------------------------------- dequantize
@@ -246,8 +255,8 @@ __global__ void __launch_bounds__(256) k_route_sorted(const float* __restrict__ 
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nw = (gridDim.x * blockDim.x) >> 5;
     const int nbr = H >> 8;
-    // quantize: all warps, one 256-block each
-    for (int b = gw; b < T * nbr; b += nw) {
+    // quantize: all warps, one 256-block each (X null: x^ was given)
+    for (int b = gw; X && b < T * nbr; b += nw) {
         const int r = b / nbr, c = b - r * nbr;
         warp_quant_q8k(X + static_cast<int64_t>(b) * 256, xq + r * x_pitch + c * 292, lane);
     }
@@ -323,7 +332,8 @@ cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, cons
 // One CTA: exclusive scan of the expert counts, the list of non-empty experts
 // (the groups of the grouped kernel) and zeroed scatter cursors.
 __global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ counts, int E, int* offsets, int* cursor,
-                                                     int* ngroups, int* group_expert, int* group_off, int* group_cnt) {
+                                                     int* ngroups, int* group_expert, int* group_off, int* group_cnt,
+                                                     unsigned long long* tel_pairs, unsigned long long* tel_calls) {
     pdl_launch_dependents();
     pdl_wait();
     __shared__ int s_sum[1024];
@@ -360,6 +370,7 @@ __global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ cou
                 group_off[grun] = run;
                 group_cnt[grun] = c;
                 ++grun;
+                if (tel_pairs) atomicAdd(tel_pairs + e, static_cast<unsigned long long>(c));
             }
             run += c;
         }
@@ -367,13 +378,18 @@ __global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ cou
     if (tid == 1023) {
         offsets[E] = s_sum[1023];
         *ngroups = s_ne[1023];
+        if (tel_calls) {  // expert-load telemetry: one call, its distinct experts
+            atomicAdd(tel_calls, 1ull);
+            atomicAdd(tel_calls + 1, static_cast<unsigned long long>(s_ne[1023]));
+        }
     }
 }
 
 cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
-                              int* group_off, int* group_cnt, cudaStream_t s) {
+                              int* group_off, int* group_cnt, cudaStream_t s, unsigned long long* tel_pairs,
+                              unsigned long long* tel_calls) {
     return launch_pdl(k_group_plan, dim3(1), dim3(1024), 0, s, counts, E, offsets, cursor, ngroups, group_expert,
-                      group_off, group_cnt);
+                      group_off, group_cnt, tel_pairs, tel_calls);
 }
 
 // Scatter pair p to its expert's range.  The order inside a range does not

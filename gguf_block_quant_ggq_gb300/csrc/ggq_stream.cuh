@@ -145,12 +145,38 @@ __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, con
     }
 }
 
+// Stage packed Q8_0 activation rows (34-byte blocks: fp16 d, 32 quants) into
+// the per-32 structure-of-arrays region (the layout Q8_1 rows are staged in):
+// one thread per block, its 17 halfwords loaded together.
+__device__ inline void stage_acts_q8_0(const uint8_t* __restrict__ src, int rows, int K, const XRegion& x, int tid, int nthr) {
+    const int rb = xq_row_bytes(K), nbr = K >> 5;
+    for (int b = tid; b < rows * nbr; b += nthr) {
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(src + static_cast<size_t>(b) * 34);
+        uint32_t hw[17];
+#pragma unroll
+        for (int i = 0; i < 17; ++i) hw[i] = __ldg(h + i);
+        uint32_t w[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w[i] = hw[1 + 2 * i] | (hw[2 + 2 * i] << 16);
+            sum += __dp4a(static_cast<int>(w[i]), 0x01010101, 0);
+        }
+        const int row = b / nbr, cb = b - row * nbr;
+        uint4* dq = reinterpret_cast<uint4*>(x.q + static_cast<size_t>(row) * rb + xq_addr(32 * cb));
+        dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        x.d[b] = __half2float(__ushort_as_half(static_cast<unsigned short>(hw[0])));
+        x.s32[b] = sum;
+    }
+}
+
 // Accumulate one row against the activation rows xr[0..nslots) into acc[].
 // For 1-2 slots two units per lane are kept in flight (units u and u+32) so
 // that their load, decode and dp4a chains overlap.  With ue >= 0 only units
 // [u0, ue) are taken; `row` is then the address the row's start would have,
 // so that unit u still sits at its offset in the row.
-template <int F, int NT>
+template <int F, int NT, bool A32 = (F == F_Q4_0)>
 __device__ __forceinline__ void row_accumulate(saddr row, const XS& xs, const int* xr, int nslots,
                                                float* acc, int lane, int u0 = 0, int ue = -1) {
     const int nu = ue < 0 ? units_per_row(xs.K) : ue, nb32 = xs.K >> 5;
@@ -171,7 +197,7 @@ __device__ __forceinline__ void row_accumulate(saddr row, const XS& xs, const in
                 int A0, A1, B0, B1;
                 unit_ints<F>(ua, xa, xs, xr[j], u, A0, A1);
                 unit_ints<F>(ub, xb, xs, xr[j], u + 32, B0, B1);
-                acc[j] += unit_value<F>(ua, xs, xr[j], u, A0, A1) + unit_value<F>(ub, xs, xr[j], u + 32, B0, B1);
+                acc[j] += unit_value<F, A32>(ua, xs, xr[j], u, A0, A1) + unit_value<F, A32>(ub, xs, xr[j], u + 32, B0, B1);
             }
         }
     }
@@ -185,7 +211,7 @@ __device__ __forceinline__ void row_accumulate(saddr row, const XS& xs, const in
             if (j < nslots) {
                 int A0, A1;
                 unit_ints<F>(un, xo, xs, xr[j], u, A0, A1);
-                acc[j] += unit_value<F>(un, xs, xr[j], u, A0, A1);
+                acc[j] += unit_value<F, A32>(un, xs, xr[j], u, A0, A1);
             }
         }
     }
@@ -278,10 +304,12 @@ __device__ __noinline__ void row_coefs_one(saddr row, const XS& xs, int xrow, in
     }
 }
 
-template <int KIND, int F, int NT>
+// AK: the activation blocks -- 0: the format's own pairing (Q8_1 for Q4_0, Q8_K
+// otherwise); 1: Q8_0 activation blocks (with Q4_0 or Q8_0 weights).
+template <int KIND, int F, int NT, int AK = 0>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr bool Q81 = fmt_q81(F);
+    constexpr bool Q81 = fmt_q81(F) || AK == 1;  // per-32 activation scales
     constexpr int LV = NT == 1 ? 0 : NT == 2 ? 1 : NT == 4 ? 2 : 3;  // log2(NT)
     constexpr int SH = 5 - LV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -429,7 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     }
     start_sync();  // barriers initialised, sums zeroed
     pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
-    stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+    if constexpr (AK == 1)
+        stage_acts_q8_0(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+    else
+        stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
     consumer_sync();
     XS xs;
     xs.q = smem_addr(xr_.q);
@@ -446,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
             // so its activations stay in registers for the whole kernel.
             XUnit xa, xb;
             const bool va = lane < nu, vb = lane + 32 < nu;
-            if (va) load_xunit<F>(xs, lane, xa);
-            if (vb) load_xunit<F>(xs, lane + 32, xb);
+            if (va) load_xunit<F, Q81>(xs, lane, xa);
+            if (vb) load_xunit<F, Q81>(xs, lane + 32, xb);
             int j = 0;
             for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
                 const int s = j % p.stages;
@@ -459,11 +490,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                     const saddr row = ring_s + static_cast<uint32_t>(s * p.stage_stride + warp * p.rowbytes);
                     float acc;
                     if (nu > 32) {
-                        const float a = unit_dot_rx<F>(row, lane, nb32, xa);
-                        const float b = vb ? unit_dot_rx<F>(row, lane + 32, nb32, xb) : 0.0f;
+                        const float a = unit_dot_rx<F, Q81>(row, lane, nb32, xa);
+                        const float b = vb ? unit_dot_rx<F, Q81>(row, lane + 32, nb32, xb) : 0.0f;
                         acc = a + b;
                     } else {
-                        acc = va ? unit_dot_rx<F>(row, lane, nb32, xa) : 0.0f;
+                        acc = va ? unit_dot_rx<F, Q81>(row, lane, nb32, xa) : 0.0f;
                     }
                     const float v = warp_transpose_reduce<0>(&acc, lane);
                     if (lane == 0) p.Y[r] = v;
@@ -506,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                         const uint32_t lead = static_cast<uint32_t>((r * p.rowbytes + static_cast<int64_t>(kc) * p.chunk_bytes) & 15);
                         const saddr row = ring_s + static_cast<uint32_t>(s * p.stage_stride + warp * p.row_slot) + lead -
                                           static_cast<uint32_t>(kc) * static_cast<uint32_t>(p.chunk_bytes);
-                        row_accumulate<F, NT>(row, xs, xr, p.T, acc, lane, u0, ue);
+                        row_accumulate<F, NT, Q81>(row, xs, xr, p.T, acc, lane, u0, ue);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);
@@ -541,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                     float acc[NT];
 #pragma unroll
                     for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
-                    row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, p.T, acc, lane);
+                    row_accumulate<F, NT, Q81>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, p.T, acc, lane);
                     const float v = warp_transpose_reduce<LV>(acc, lane);
                     const int t = lane >> SH;
                     if ((lane & ((1 << SH) - 1)) == 0 && t < p.T) p.Y[t * p.N + r] = v;
@@ -555,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     }
 }
 
-template <int KIND, int F, int NT>
+template <int KIND, int F, int NT, int AK = 0>
 cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s) {
     // The dynamic shared-memory limit is a per-device function attribute: set it
     // on the first launch of each instantiation on each device (before capture).
@@ -565,20 +596,20 @@ cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(k_stream<KIND, F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        e = cudaFuncSetAttribute(k_stream<KIND, F, NT, AK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_stream<KIND, F, NT>, dim3(grid), dim3(kThreads), smem, s, p);
+    return launch_pdl(k_stream<KIND, F, NT, AK>, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
-template <int KIND, int F>
+template <int KIND, int F, int AK = 0>
 cudaError_t launch_nt(int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
     switch (nt) {
-    case 1: return launch_one<KIND, F, 1>(p, grid, smem, s);
-    case 2: return launch_one<KIND, F, 2>(p, grid, smem, s);
-    case 4: return launch_one<KIND, F, 4>(p, grid, smem, s);
-    default: return launch_one<KIND, F, 8>(p, grid, smem, s);
+    case 1: return launch_one<KIND, F, 1, AK>(p, grid, smem, s);
+    case 2: return launch_one<KIND, F, 2, AK>(p, grid, smem, s);
+    case 4: return launch_one<KIND, F, 4, AK>(p, grid, smem, s);
+    default: return launch_one<KIND, F, 8, AK>(p, grid, smem, s);
     }
 }
 

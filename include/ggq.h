@@ -68,7 +68,7 @@ typedef enum ggq_status {
  * reader can pass its type field through unchanged. */
 typedef enum ggq_type {
     GGQ_TYPE_Q4_0 = 2,   /* 32 weights: fp16 d, 16 B nibbles; w = (q - 8) d               */
-    GGQ_TYPE_Q8_0 = 8,   /* 32 weights: fp16 d, int8[32];     w = q d                     */
+    GGQ_TYPE_Q8_0 = 8,   /* 32 weights or activations: fp16 d, int8[32];  v = q d        */
     GGQ_TYPE_Q8_1 = 9,   /* 32 activations: fp16 d, fp16 s = d*sum(q), int8[32]            */
     GGQ_TYPE_Q4_K = 12,  /* 256: fp16 d, dmin, 12 B 6-bit scales/mins, 128 B nibbles       */
     GGQ_TYPE_Q5_K = 13,  /* 256: Q4_K header, 32 B high bits, 128 B nibbles                 */
@@ -80,7 +80,7 @@ typedef enum ggq_type {
 typedef enum ggq_op {
     GGQ_OP_QUANTIZE_ACT = 0, /* ggq_quantize_act                                  */
     GGQ_OP_DEQUANT = 1,      /* ggq_dequant                                        */
-    GGQ_OP_MUL_MAT_VEC = 2,  /* ggq_mul_mat_vec / _q / ggq_block_dots (op 74)      */
+    GGQ_OP_MUL_MAT_VEC = 2,  /* ggq_mul_mat_vec / _q / _qa / ggq_block_dots (op 74) */
     GGQ_OP_MOE = 3           /* ggq_moe_experts / _routed, as gate/up or down (op 75) */
 } ggq_op;
 
@@ -175,10 +175,12 @@ ggq_status ggq_set_static_weights(ggq_ctx* ctx, int static_weights);
 int ggq_supported(int w, int act, int op);
 
 /* Quantize x [T][K] fp32 to packed activation blocks out [T][K/blk]
- * (act = GGQ_TYPE_Q8_1: K % 32 == 0, 36 B blocks; GGQ_TYPE_Q8_K: K % 256 == 0,
- * 292 B blocks).  Per block: d = amax/127 (fp32), q = round-half-away(x * (1/d))
- * clamped to +-127; Q8_1 stores d and s = d*sum(q) as fp16, Q8_K stores d as
- * fp32 and the 16 sums of 16 quants.  T = 0 or K = 0 is an empty call: it
+ * (act = GGQ_TYPE_Q8_1: K % 32 == 0, 36 B blocks; GGQ_TYPE_Q8_0: K % 32 == 0,
+ * 34 B blocks; GGQ_TYPE_Q8_K: K % 256 == 0, 292 B blocks).  Per block:
+ * d = amax/127 (fp32), q = round-half-away(x * (1/d)) clamped to +-127; Q8_1
+ * stores d and s = d*sum(q) as fp16, Q8_0 stores d as fp16 (the Q8_0 activation
+ * quantizer of vllm.cpp PR #523, What changed), Q8_K stores d as fp32 and the
+ * 16 sums of 16 quants.  T = 0 or K = 0 is an empty call: it
  * returns GGQ_OK without reading or writing (the pointers may be NULL).
  * Needs no scratch. */
 ggq_status ggq_quantize_act(ggq_ctx* ctx, int act, const float* x, int64_t T, int64_t K, void* out, void* stream);
@@ -208,6 +210,15 @@ ggq_status ggq_mul_mat_vec(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_
 ggq_status ggq_mul_mat_vec_q(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
                              float* Y, void* stream);
 
+/* ggq_mul_mat_vec_q with the activation format named: act = the weight
+ * format's default (Q8_1 for Q4_0, Q8_K otherwise), or GGQ_TYPE_Q8_0 with
+ * Q4_0 or Q8_0 weights (the Q8_0 x Q8_0 pairing of vllm.cpp PR #523, What
+ * changed; Xq [T][K/32] 34-byte blocks from ggq_quantize_act, K % 32 == 0).
+ * Other pairings return GGQ_ERR_UNSUPPORTED.  Q8_0 activations run on the dp4a
+ * streaming kernel at every token count.  Needs no scratch. */
+ggq_status ggq_mul_mat_vec_qa(ggq_ctx* ctx, int w, int act, const void* W, int64_t N, int64_t K, const void* Xq,
+                              int64_t T, float* Y, void* stream);
+
 /* Debug dump of the integer core of ggq_mul_mat_vec_q: the int32 coefficients
  * that multiply each block's scale product, out [T][N][K/blk * c]:
  *   Q4_0 x Q8_1, Q8_0 x Q8_K, MXFP4 x Q8_K (c = 1): S = sum of integer products
@@ -224,6 +235,11 @@ ggq_status ggq_mul_mat_vec_q(ggq_ctx* ctx, int w, const void* W, int64_t N, int6
  * 4-byte aligned; the call clears it first. */
 ggq_status ggq_block_dots(ggq_ctx* ctx, int w, const void* W, int64_t N, int64_t K, const void* Xq, int64_t T,
                           int32_t* coefs, void* stream);
+
+/* ggq_block_dots for the pairings of ggq_mul_mat_vec_qa (Q4_0 x Q8_0 and
+ * Q8_0 x Q8_0: S = sum of integer products per 32-block). */
+ggq_status ggq_block_dots_qa(ggq_ctx* ctx, int w, int act, const void* W, int64_t N, int64_t K, const void* Xq,
+                             int64_t T, int32_t* coefs, void* stream);
 
 /* Routed-expert layer (ggml_moe_a8_vec / vllm.cpp PR #523 op 75 / ds4 PR #656):
  *   ids, weights = top_k of softmax(router_logits[t]) by logit (ties to the
@@ -251,6 +267,18 @@ ggq_status ggq_moe_experts(ggq_ctx* ctx, const ggq_moe_weights* w, int64_t E, in
 ggq_status ggq_moe_experts_routed(ggq_ctx* ctx, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I,
                                   int top_k, const float* X, const int32_t* ids, const float* weights, int64_t T,
                                   float* Y, const ggq_moe_dump* dump, void* stream);
+
+/* The routed-expert layer of ggq_moe_experts with x already quantized: Xq is
+ * [T][H/256] packed Q8_K blocks as ggq_quantize_act writes them (the "Q8
+ * prequant" path of ds4 PR #656 "Add ROCm MXFP4 routed expert kernels", A/B
+ * notes: quantize the activations once and reuse them, e.g. across the layers
+ * or calls that share one input).  Same routing, kernels, shapes, scratch and
+ * errors as ggq_moe_experts; Y is bit-identical to ggq_moe_experts on the x
+ * that Xq was quantized from.  Xq must be 4-byte aligned.  With a dump, dump->xq
+ * receives a copy of Xq. */
+ggq_status ggq_moe_experts_q(ggq_ctx* ctx, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k,
+                             const void* Xq, const float* router_logits, int64_t T, float* Y, const ggq_moe_dump* dump,
+                             void* stream);
 
 /* ggq_mul_mat_vec without a context and without any allocation.  (The pages
  * have no counterpart of this call; it exists for deployment.)
@@ -281,6 +309,20 @@ ggq_status ggq_moe_experts_routed(ggq_ctx* ctx, const ggq_moe_weights* w, int64_
  * and ggq_sync_status. */
 ggq_status ggq_mul_mat_vec_noalloc(int w, const void* W, int64_t N, int64_t K, const float* X, int64_t T, float* Y,
                                    void* stream);
+
+/* Expert-load telemetry of the routed-expert calls (FreeToken PR #260
+ * "ROCm: validate native gfx1151 serving on Strix Halo", MoE cache telemetry:
+ * active experts per layer).  With buffers set, every later ggq_moe_experts /
+ * _routed call on the context adds on the device, in stream order:
+ *   pairs[e]  += number of (token, slot) pairs the call routed to expert e
+ *                (int64 [n_experts]: how often each expert's weights are read);
+ *   calls[0]  += 1 and calls[1] += the number of distinct experts the call
+ *                used (int64 [2]: calls[1] / calls[0] = experts per layer).
+ * The buffers are caller-owned device memory, 8-byte aligned; the caller
+ * clears them and reads them after synchronising.  Calls with E > n_experts
+ * return GGQ_ERR_SHAPE while the telemetry is on.  pairs = calls = NULL turns
+ * it off.  No allocation, no synchronisation: capture-safe like the calls. */
+ggq_status ggq_set_moe_counters(ggq_ctx* ctx, int64_t* pairs, int64_t n_experts, int64_t* calls);
 
 /* Synchronise `stream` and read the device error word: GGQ_OK, or
  * GGQ_ERR_DEVICE (a bounded wait inside a kernel ran out; the word is cleared),

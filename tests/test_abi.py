@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_support_query_per_format(lib):
     ok = [("Q4_0", "Q8_1"), ("Q8_0", "Q8_K"), ("Q4_K", "Q8_K"), ("Q5_K", "Q8_K"), ("Q6_K", "Q8_K"),
-          ("MXFP4", "Q8_K")]
+          ("MXFP4", "Q8_K"), ("Q4_0", "Q8_0"), ("Q8_0", "Q8_0")]
     for w in ggq.TYPE:
         for a in ggq.TYPE:
             assert ggq.supported(w, a, "mul_mat_vec") == ((w, a) in ok)
@@ -43,6 +43,7 @@ def test_support_query_per_format(lib):
             assert ggq.supported(w, a, "moe") == moe_ok
         assert ggq.supported(w, "Q8_K", "dequant") == (w in ("Q4_0", "Q8_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4"))
     assert ggq.supported("Q4_0", "Q8_1", "quantize_act") and ggq.supported("Q4_0", "Q8_K", "quantize_act")
+    assert ggq.supported("Q4_0", "Q8_0", "quantize_act")
     assert not ggq.supported("Q4_0", "Q4_0", "quantize_act")
     # formats outside the six (e.g. Q2_K = 10, Q4_1 = 3) are refused, not mapped
     assert lib.ggq_supported(10, ggq.TYPE["Q8_K"], 2) == 0

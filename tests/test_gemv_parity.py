@@ -140,6 +140,42 @@ def test_block_dots_exact_at_the_integer_bounds(ctx, fmt, T):
     check_outputs(to_host(ctx.mul_mat_vec_q(fmt, dW, N, K, dxq, T)), ref, absdot, f"{fmt} extremes T={T}")
 
 
+Q8_0_ACT_CASES = [  # (fmt, N, K, T): Q8_0 activation blocks (Q4_0 x Q8_0, Q8_0 x Q8_0)
+    ("Q4_0", 16 * 9 + 5, 1024, 1), ("Q4_0", 21, 96, 2), ("Q4_0", 35, 160, 8), ("Q4_0", 77, 4096, 3),
+    ("Q8_0", 16 * 9 + 5, 1024, 1), ("Q8_0", 40, 4096, 2), ("Q8_0", 33, 768, 5), ("Q8_0", 16 * 20 + 7, 2048, 8),
+    ("Q8_0", 37, 14336, 2),  # rows streamed in chunks
+    ("Q4_0", 21, 16384, 1),
+]
+
+
+@pytest.mark.parametrize("fmt,N,K,T", Q8_0_ACT_CASES)
+def test_q8_0_activations_bit_exact_and_within_tolerance(ctx, fmt, N, K, T):
+    """The Q8_0 activation quantizer (bytes bit-exact) and the Q4_0 x Q8_0 /
+    Q8_0 x Q8_0 GEMV: per-block int32 coefficients bit-exact, outputs within
+    the fp32 tolerance of the oracle."""
+    W, x = _case(fmt, N, K, T, 3 * N + K + T + 11)
+    xq = orc.quantize("Q8_0", x)
+    got = to_host(ctx.quantize_act("Q8_0", to_dev(x)))
+    assert np.array_equal(got, xq), f"{np.count_nonzero(got != xq)} Q8_0 activation bytes differ"
+    dW, dxq = to_dev(W), to_dev(xq)
+    if K <= 4096:  # the dump stages whole rows (long rows stream in chunks only for the GEMV)
+        coefs = to_host(ctx.block_dots_qa(fmt, "Q8_0", dW, N, K, dxq, T))
+        assert np.array_equal(coefs, orc.gemv_coefs(fmt, W, N, K, xq, T, act="Q8_0"))
+    ref, absdot = orc.gemv_dequant(fmt, W, N, K, xq, T, act="Q8_0")
+    y = to_host(ctx.mul_mat_vec_qa(fmt, "Q8_0", dW, N, K, dxq, T))
+    check_outputs(y, ref, absdot, f"{fmt} x Q8_0 N={N} K={K} T={T}")
+    ctx.sync_status()
+
+
+def test_unsupported_activation_pairings_are_refused(ctx):
+    W = to_dev(syn.weights("Q4_K", 16, 256, syn.rng(57, 0)))
+    xq = to_dev(orc.quantize("Q8_0", syn.activations(1, 256, syn.rng(57, 1))))
+    with pytest.raises(ggq.GGQError, match="UNSUPPORTED"):
+        ctx.mul_mat_vec_qa("Q4_K", "Q8_0", W, 16, 256, xq, 1)
+    assert ggq.supported("Q8_0", "Q8_0", "mul_mat_vec") and ggq.supported("Q4_0", "Q8_0", "mul_mat_vec")
+    assert not ggq.supported("Q4_K", "Q8_0", "mul_mat_vec") and ggq.supported("Q4_0", "Q8_0", "quantize_act")
+
+
 LONG_ROWS = [  # (fmt, N, K, T): rows too long for whole-row stages, streamed in row chunks
     ("Q8_0", 16 * 160 + 7, 14336, 1),  # more tiles than SMs (a CTA streams several), ragged tail
     ("Q8_0", 37, 14336, 2),

@@ -290,6 +290,65 @@ def test_moe_all_experts_uniform_equals_dense(ctx):
     assert np.sum((y - ref["y"]) ** 2) / np.sum(ref["y"] ** 2) <= 1e-4
 
 
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_moe_prequantized_entry_is_bit_identical(ctx, T):
+    """ggq_moe_experts_q on x^ from ggq_quantize_act gives the very bytes of
+    ggq_moe_experts on x (the same kernels take the same x^), on the direct
+    route (1 and 3 tokens) and on expert-sorted tiles (8)."""
+    cfg = syn.MOE_DECODE
+    E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
+    host, dev = _banks(cfg, E)
+    w8 = ctx.moe_weights(cfg["gate"], dev["gate"], cfg["up"], dev["up"], cfg["down"], dev["down"])
+    g = syn.rng(cfg["index"], 5000 + T)
+    x = to_dev(syn.activations(T, H, g))
+    lg = to_dev(syn.router_logits(T, E, g))
+    y = to_host(ctx.moe_experts(w8, E, H, I, k, x, logits=lg))
+    xq = ctx.quantize_act("Q8_K", x)
+    d = {"xq": torch.full((T, H // 256 * 292), 7, dtype=torch.uint8, device="cuda")}
+    yq = to_host(ctx.moe_experts_q(w8, E, H, I, k, xq, lg, dump=d))
+    ctx.sync_status()
+    assert np.array_equal(yq, y)
+    assert np.array_equal(to_host(d["xq"]), to_host(xq))
+
+
+def test_moe_expert_load_counters(ctx):
+    """Expert-load telemetry: pairs per expert, calls and distinct experts per
+    call, accumulated on the device over direct-route and expert-sorted calls,
+    against the oracle's routing of the same logits."""
+    cfg = syn.MOE_DECODE
+    E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
+    host, dev = _banks(cfg, E)
+    w8 = ctx.moe_weights(cfg["gate"], dev["gate"], cfg["up"], dev["up"], cfg["down"], dev["down"])
+    pairs = torch.zeros(E, dtype=torch.int64, device="cuda")
+    calls = torch.zeros(2, dtype=torch.int64, device="cuda")
+    ctx.set_moe_counters(pairs, calls)
+    want_pairs = np.zeros(E, np.int64)
+    want_calls = np.zeros(2, np.int64)
+    try:
+        g = syn.rng(cfg["index"], 4242)
+        for T in (1, 2, 3, 4, 16, 1):
+            x = syn.activations(T, H, g)
+            logits = syn.router_logits(T, E, g)
+            ids, _ = orc.router(logits, k)
+            ctx.moe_experts(w8, E, H, I, k, to_dev(x), logits=to_dev(logits))
+            want_pairs += np.bincount(ids.ravel(), minlength=E)
+            want_calls += [1, len(np.unique(ids))]
+        ctx.sync_status()
+        assert np.array_equal(to_host(pairs), want_pairs)
+        assert np.array_equal(to_host(calls), want_calls)
+        # a layer with more experts than the buffer holds is refused while the telemetry is on
+        with pytest.raises(ggq.GGQError, match="SHAPE"):
+            ctx.moe_experts(w8, E + 1, H, I, k, to_dev(np.zeros((1, H), np.float32)),
+                            logits=to_dev(np.zeros((1, E + 1), np.float32)))
+    finally:
+        ctx.set_moe_counters(None, None)
+    # off: further calls leave the buffers alone
+    x = syn.activations(2, H, syn.rng(cfg["index"], 4243))
+    ctx.moe_experts(w8, E, H, I, k, to_dev(x), logits=to_dev(syn.router_logits(2, E, syn.rng(cfg["index"], 4244))))
+    ctx.sync_status()
+    assert np.array_equal(to_host(pairs), want_pairs) and np.array_equal(to_host(calls), want_calls)
+
+
 def test_moe_rejects_bad_arguments(ctx):
     cfg = syn.MOE_DECODE
     host, dev = _banks(cfg, cfg["E"])
