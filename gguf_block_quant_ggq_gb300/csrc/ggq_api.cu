@@ -302,7 +302,7 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
     const int red_bytes = 2 * kConsumerWarps * 130 * 4, x_bytes = p.T * p.xrow;  // partials: [2][16][130] floats
     p.x_bytes = static_cast<int>(align_up(static_cast<size_t>(red_bytes > x_bytes ? red_bytes : x_bytes), 128));
     p.x_bulk = (x_bytes % 16 == 0 && aligned16(p.xq)) ? 1 : 0;
-    const int fixed = p.x_bytes + kConsumerWarps * 4 * 32 * 4 + (2 * kMaxStages + 1) * 8 + 256;
+    const int fixed = p.x_bytes + kConsumerWarps * 4 * kMmavCStride * 4 + (2 * kMaxStages + 1) * 8 + 256;
     int stages = (kSmemLimit - fixed) / p.stage_stride;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return false;

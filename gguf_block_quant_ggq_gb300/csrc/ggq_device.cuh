@@ -155,6 +155,11 @@ __device__ __forceinline__ int ld_s16(saddr a) {
     return v;
 }
 __device__ __forceinline__ float ld_f32(saddr a) { return __uint_as_float(ld_s32(a)); }
+__device__ __forceinline__ float2 ld_f32x2(saddr a) {
+    uint32_t x, y;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(a));
+    return make_float2(__uint_as_float(x), __uint_as_float(y));
+}
 __device__ __forceinline__ float ld_h(saddr a) {
     uint32_t v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));

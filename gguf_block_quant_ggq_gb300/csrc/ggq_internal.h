@@ -103,6 +103,11 @@ struct GroupParams {
 // Decode GEMV at 2-8 tokens on the int8 tensor path (ggq_mmav.cuh): the
 // streaming geometry above, rows copied one by one into bank-padded rows, K
 // split into one chunk per consumer warp.
+// Floats per (warp, mma column pair) of the tensor-path GEMV's accumulator
+// start values in shared memory: 32 used, padded so that the four column pairs
+// of a warp fall on distinct banks.
+constexpr int kMmavCStride = 34;
+
 struct MmavParams {
     const uint8_t* W;
     int64_t rowbytes;   // bytes of one weight row in global (a multiple of 16)

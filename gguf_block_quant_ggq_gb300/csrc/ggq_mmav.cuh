@@ -145,8 +145,9 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
     X.dx1 = v1 ? ld_f32(r1) : 0.0f;
     if constexpr (F == F_Q6_K) {
         // f16 fragments of each 16-group (elements 4t, 4t+2 | 4t+1, 4t+3 of the
-        // group, as for Q4_K); C = -1056 * (sum of the group's activations): the
-        // codes enter as 1024 + code and the weights are code - 32
+        // group, as for Q4_K); C = -1056 (groups 0, 1 of a 128-element half: the
+        // codes enter as 1024 + code) or -1536 (groups 2, 3: 1024 + 16 code) times
+        // the sum of the group's activations, the weights being code - 32
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             if (16 * j < chunk) {
@@ -154,9 +155,10 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                 if (vg) s8x4_to_f16(ld_s32(rb + 4 + e + 4 * t), X.b[2 * j], X.b[2 * j + 1]);
                 const int bs0 = v0 ? ld_s16(r0 + 260 + 2 * (e >> 4)) : 0;
                 const int bs1 = v1 ? ld_s16(r1 + 260 + 2 * (e >> 4)) : 0;
+                const float cb = (e & 64) ? -1536.0f : -1056.0f;
                 if (g == 0) {
-                    cs[2 * j] = -1056.0f * static_cast<float>(bs0);
-                    cs[2 * j + 1] = -1056.0f * static_cast<float>(bs1);
+                    cs[2 * j] = cb * static_cast<float>(bs0);
+                    cs[2 * j + 1] = cb * static_cast<float>(bs1);
                 }
             }
         }
@@ -246,6 +248,104 @@ __device__ __forceinline__ void dump_add(int32_t* row, int idx, int v) {
 }
 __device__ __forceinline__ void dump_put(int32_t* row, int idx, int v) {
     if (row) row[idx] = v;
+}
+
+// One 32-bit word of a Q6_K superblock at a byte offset that is a multiple of
+// 4 from the superblock start; ODD: the superblock itself starts 2 bytes after
+// a word boundary, so the word is the middle of two aligned ones.
+template <bool ODD>
+__device__ __forceinline__ uint32_t q6_word(saddr a) {
+    if constexpr (ODD) return prmt(ld_s32(a - 2u), ld_s32(a + 2u), 0x5432u);
+    else return ld_s32(a);
+}
+
+// Q6_K part of a chunk (one or two 128-element halves of superblock b0 / b1 for
+// rows g and g+8).  Element 128h + 32g6 + l: low 4 bits in ql[64h + 32(g6&1) + l]
+// (nibble g6>>1), high 2 bits in qh[32h + l] (bits 2g6), scale of 16-group
+// (128h + 32g6 + l)/16.  f16 operands without moving any nibble: groups g6 = 0, 1
+// read 1024 + code (low nibble, the two high bits placed at bits 4-5), groups
+// g6 = 2, 3 read 1024 + 16 code (high nibble in place, the two bits at 8-9;
+// 16 code <= 1008, still an exact f16 integer).  The start value C removes 1056
+// or 1536 times the group's activation sum, so D is the exact dot of (code - 32)
+// and x, times 16 for groups 2 and 3; one m16n8k16 per 16-group (each group has
+// its own int8 scale), scaled in f32.
+template <bool ODD, bool DUMP>
+__device__ __forceinline__ void mmav_q6k(saddr b0, saddr b1, int e0, int chunk, const MmaX& X, saddr cs, int t,
+                                         float* acc, const MmavDump& dz) {
+    const int h0 = (e0 & 255) >> 7;
+    uint32_t sw0[4], sw1[4];  // int8 scales of the chunk's 16-groups, four per word
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        sw0[k] = q6_word<ODD>(b0 + 192u + 4u * k);
+        sw1[k] = q6_word<ODD>(b1 + 192u + 4u * k);
+    }
+    if (h0) {  // second half only: its eight scales are words 2 and 3
+        sw0[0] = sw0[2], sw0[1] = sw0[3], sw1[0] = sw1[2], sw1[1] = sw1[3];
+    }
+    uint32_t Mr = 0x64006400u;
+    asm("" : "+r"(Mr));
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ah[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // groups 0, 1 | 2, 3 (16x)
+    int ia[4] = {0, 0, 0, 0};  // dump: sum_j sc_j S_j in int32
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        if (128 * hh < chunk) {
+            const uint32_t h = static_cast<uint32_t>(h0 + hh);
+#pragma unroll
+            for (int lh = 0; lh < 2; ++lh) {
+                const uint32_t l = 16u * lh + 4u * t;
+                uint32_t A[4][4];  // [g6][row g even bytes, row g+8 even, row g odd, row g+8 odd]
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const saddr b = r ? b1 : b0;
+                    const uint32_t ql0 = q6_word<ODD>(b + 64u * h + l), ql1 = q6_word<ODD>(b + 64u * h + 32u + l);
+                    const uint32_t qh = q6_word<ODD>(b + 128u + 32u * h + l);
+                    const uint32_t ql0o = ql0 >> 8, ql1o = ql1 >> 8;  // bytes 1, 3 in the even positions
+                    // high bits of g6 = 0 / 2 at 4-5 / 8-9 (<< 4), of g6 = 1 / 3 likewise (<< 2);
+                    // the odd bytes' bits are 8 further up (>> 4, >> 6)
+                    const uint32_t h4 = qh << 4, h4o = qh >> 4, h2 = qh << 2, h2o = qh >> 6;
+                    A[0][r] = and_or<0x00300030u>(h4, and_or<0x000F000Fu>(ql0, Mr));
+                    A[0][2 + r] = and_or<0x00300030u>(h4o, and_or<0x000F000Fu>(ql0o, Mr));
+                    A[1][r] = and_or<0x00300030u>(h2, and_or<0x000F000Fu>(ql1, Mr));
+                    A[1][2 + r] = and_or<0x00300030u>(h2o, and_or<0x000F000Fu>(ql1o, Mr));
+                    A[2][r] = and_or<0x03000300u>(h4, and_or<0x00F000F0u>(ql0, Mr));
+                    A[2][2 + r] = and_or<0x03000300u>(h4o, and_or<0x00F000F0u>(ql0o, Mr));
+                    A[3][r] = and_or<0x03000300u>(h2, and_or<0x00F000F0u>(ql1, Mr));
+                    A[3][2 + r] = and_or<0x03000300u>(h2o, and_or<0x00F000F0u>(ql1o, Mr));
+                }
+#pragma unroll
+                for (int g6 = 0; g6 < 4; ++g6) {
+                    const int jl = 8 * hh + 2 * g6 + lh;  // 16-group within the chunk
+                    const float2 c = ld_f32x2(cs + 8u * jl);
+                    float D[4] = {c.x, c.y, c.x, c.y};
+                    mma_f16(D, A[g6][0], A[g6][1], A[g6][2], A[g6][3], X.b[2 * jl], X.b[2 * jl + 1]);
+                    const int i0 = byte_s(sw0[jl >> 2], jl & 3), i1 = byte_s(sw1[jl >> 2], jl & 3);
+                    const float sc0 = static_cast<float>(i0), sc1 = static_cast<float>(i1);
+                    float* const dst = g6 < 2 ? a : ah;
+                    dst[0] += sc0 * D[0];
+                    dst[1] += sc0 * D[1];
+                    dst[2] += sc1 * D[2];
+                    dst[3] += sc1 * D[3];
+                    if constexpr (DUMP) {
+                        const int sh = g6 < 2 ? 0 : 4;  // D of groups 2, 3 is 16 times the dot (exact)
+                        ia[0] += i0 * (__float2int_rn(D[0]) >> sh);
+                        ia[1] += i0 * (__float2int_rn(D[1]) >> sh);
+                        ia[2] += i1 * (__float2int_rn(D[2]) >> sh);
+                        ia[3] += i1 * (__float2int_rn(D[3]) >> sh);
+                    }
+                }
+            }
+        }
+    }
+    if constexpr (DUMP) {
+        const int sb = e0 >> 8;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dump_add(dz.q[q], sb, ia[q]);
+    }
+    const float d0 = ld_h(b0 + 208), d1 = ld_h(b1 + 208);
+    acc[0] = fmaf(0.0625f, ah[0], a[0]) * (X.dx0 * d0);
+    acc[1] = fmaf(0.0625f, ah[1], a[1]) * (X.dx1 * d0);
+    acc[2] = fmaf(0.0625f, ah[2], a[2]) * (X.dx0 * d1);
+    acc[3] = fmaf(0.0625f, ah[3], a[3]) * (X.dx1 * d1);
 }
 
 // 16 x 8 partial of one chunk: rows (g, g+8) at r0/r1, columns (2t, 2t+1).
@@ -374,78 +474,12 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         acc[2] = X.dx0 * (d1 * D[2] - dm1 * DM[2]);
         acc[3] = X.dx1 * (d1 * D[3] - dm1 * DM[3]);
     } else if constexpr (F == F_Q6_K) {
-        // chunk = one or two 128-element halves; element 128h + 32g6 + l of a
-        // superblock: low 4 bits in ql[64h + 32(g6&1) + l] (nibble g6>>1), high
-        // 2 bits in qh[32h + l] (bits 2g6), scale of 16-group (128h + 32g6 + l)/16.
-        // f16 operands 1024 + code (C removes 1056 x the activation sum: weight
-        // code - 32); one m16n8k16 per 16-group, scaled in f32
-        const int h0 = (e0 & 255) >> 7;
-        const saddr b0 = r0 + 210u * sb, b1 = r1 + 210u * sb;
-        uint32_t sw0[4], sw1[4];  // int8 scales of the chunk's 16-groups, four per word
-        ld_words_any<4>(b0 + 192, sw0);
-        ld_words_any<4>(b1 + 192, sw1);
-        if (h0) {  // second half only: its eight scales are words 2 and 3
-            sw0[0] = sw0[2], sw0[1] = sw0[3], sw1[0] = sw1[2], sw1[1] = sw1[3];
-        }
-        uint32_t Mr = 0x64006400u;
-        asm("" : "+r"(Mr));
-        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        int ia[4] = {0, 0, 0, 0};  // dump: sum_j sc_j S_j in int32 (each D is the exact S_j)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            if (128 * hh < chunk) {
-                const int h = h0 + hh;
-#pragma unroll
-                for (int lh = 0; lh < 2; ++lh) {
-                    const uint32_t l = 16u * lh + 4u * t;
-                    uint32_t ql[2][2], qh[2];  // [row][g6 & 1], [row]
-                    ld_words_any<1>(b0 + 64 * h + l, &ql[0][0]);
-                    ld_words_any<1>(b0 + 64 * h + 32 + l, &ql[0][1]);
-                    ld_words_any<1>(b0 + 128 + 32 * h + l, &qh[0]);
-                    ld_words_any<1>(b1 + 64 * h + l, &ql[1][0]);
-                    ld_words_any<1>(b1 + 64 * h + 32 + l, &ql[1][1]);
-                    ld_words_any<1>(b1 + 128 + 32 * h + l, &qh[1]);
-#pragma unroll
-                    for (int g6 = 0; g6 < 4; ++g6) {
-                        const int jl = 8 * hh + 2 * g6 + lh;  // 16-group within the chunk
-                        uint32_t A[4];  // (row g | row g+8) x (elements 0,2 | 1,3)
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const uint32_t w = (g6 >> 1) ? ql[r][g6 & 1] >> 4 : ql[r][g6 & 1];
-                            const uint32_t hb = g6 == 0 ? qh[r] << 4 : g6 == 1 ? qh[r] << 2 : g6 == 2 ? qh[r] : qh[r] >> 2;
-                            A[r] = and_or<0x00300030u>(hb, and_or<0x000F000Fu>(w, Mr));
-                            A[2 + r] = and_or<0x00300030u>(hb >> 8, and_or<0x000F000Fu>(w >> 8, Mr));
-                        }
-                        const float c0 = ld_f32(cs + 8u * jl), c1 = ld_f32(cs + 8u * jl + 4);
-                        float D[4] = {c0, c1, c0, c1};
-                        mma_f16(D, A[0], A[1], A[2], A[3], X.b[2 * jl], X.b[2 * jl + 1]);
-                        const int sj = jl;  // scale index within the chunk
-                        const float sc0 = static_cast<float>(byte_s(sw0[sj >> 2], sj & 3));
-                        const float sc1 = static_cast<float>(byte_s(sw1[sj >> 2], sj & 3));
-                        a[0] += sc0 * D[0];
-                        a[1] += sc0 * D[1];
-                        a[2] += sc1 * D[2];
-                        a[3] += sc1 * D[3];
-                        if constexpr (DUMP) {
-                            const int i0 = byte_s(sw0[sj >> 2], sj & 3), i1 = byte_s(sw1[sj >> 2], sj & 3);
-                            ia[0] += i0 * __float2int_rn(D[0]);
-                            ia[1] += i0 * __float2int_rn(D[1]);
-                            ia[2] += i1 * __float2int_rn(D[2]);
-                            ia[3] += i1 * __float2int_rn(D[3]);
-                        }
-                    }
-                }
-            }
-        }
-        if constexpr (DUMP) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dump_add(dz.q[q], sb, ia[q]);
-        }
-        const float d0 = ld_h(b0 + 208), d1 = ld_h(b1 + 208);
-        acc[0] = a[0] * (X.dx0 * d0);
-        acc[1] = a[1] * (X.dx1 * d0);
-        acc[2] = a[2] * (X.dx0 * d1);
-        acc[3] = a[3] * (X.dx1 * d1);
+        // superblocks are 210 bytes: at an odd index they start 2 bytes off a word
+        const uint32_t sbo = 210u * static_cast<uint32_t>(sb);
+        if ((r0 + sbo) & 2u)
+            mmav_q6k<true, DUMP>(r0 + sbo, r1 + sbo, e0, chunk, X, cs, t, acc, dz);
+        else
+            mmav_q6k<false, DUMP>(r0 + sbo, r1 + sbo, e0, chunk, X, cs, t, acc, dz);
     } else {  // Q8_0 and MXFP4: one scale per 32-block
         const int blk0 = e0 >> 5;  // even: chunks start at multiples of 64
         acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
@@ -511,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     uint8_t* ring = smem;
     uint8_t* xreg = smem + static_cast<size_t>(p.stages) * p.stage_stride;
     float* red = reinterpret_cast<float*>(xreg);
-    float* creg = reinterpret_cast<float*>(xreg + p.x_bytes);  // [16 warps][4][32]
-    uint64_t* full = reinterpret_cast<uint64_t*>(creg + kConsumerWarps * 4 * 32);
+    float* creg = reinterpret_cast<float*>(xreg + p.x_bytes);  // [16 warps][4][kMmavCStride]
+    uint64_t* full = reinterpret_cast<uint64_t*>(creg + kConsumerWarps * 4 * kMmavCStride);
     uint64_t* empty = full + kMaxStages;
     uint64_t* xbar = empty + kMaxStages;
 
@@ -592,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     const bool active = warp < p.nch;
     const int e0 = warp * p.chunk;
     MmaX X;
-    float* cs = creg + (warp * 4 + t) * 32;
+    float* cs = creg + (warp * 4 + t) * kMmavCStride;
     mmav_load_x<F>(smem_addr(xreg), p.xrow, active ? p.T : 0, p.chunk, e0, g, t, X, cs);
     mmav_sync();  // the region now holds partials
     const saddr ring_s = smem_addr(ring);
