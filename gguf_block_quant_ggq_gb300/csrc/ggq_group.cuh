@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kGroupThreads, 1) k_group(const GroupParams p)
                     uint8_t* dst = xring + static_cast<size_t>(s) * p.xslot;
                     for (int c = 0; c < nc; ++c)
                         bulk_g2s(dst + c * p.xstride, p.xq + col_row(off + ch * kGroupCols + c) * p.x_pitch,
-                                 static_cast<uint32_t>(p.xcopy), &xfull[s], 0ull);
+                                 static_cast<uint32_t>(p.xcopy), &xfull[s], policy_evict_last());
                 }
             }
             // never leave copies in flight

@@ -574,7 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
             const int64_t r0 = static_cast<int64_t>(item) * kTileRows;
             const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
             if (lane == 0) {
-                ok = mbar_wait(&empty[s], ph ^ 1u);
+                // with static weights, the stages after the first once the activations are in
+                // (their bulk copy's barrier; without it, once the previous kernel has finished)
+                if (p.early_weights && j == kEarlyStages) {
+                    if (p.x_bulk) ok = mbar_wait(xbar, 0u);
+                    else pdl_wait();
+                }
+                ok = ok && mbar_wait(&empty[s], ph ^ 1u);
                 if (ok) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nr * p.rowbytes));
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -612,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     if (p.x_bulk) {
         if (tid == 0) {
             mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(xbytes));
-            bulk_g2s(xreg, p.xq, static_cast<uint32_t>(xbytes), xbar, 0ull);
+            bulk_g2s(xreg, p.xq, static_cast<uint32_t>(xbytes), xbar, policy_evict_last());
         }
         xok = mbar_wait(xbar, 0u);
         if (!xok) set_error(p.err, DEV_ERR_TIMEOUT);

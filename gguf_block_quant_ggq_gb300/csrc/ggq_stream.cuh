@@ -62,8 +62,14 @@ __device__ __forceinline__ XRegion x_region(uint8_t* base, int rows, int K, bool
 // per-32 sums must be zero on entry (they are accumulated with atomics).
 // Q8_K work unit: one 32-element quant group (8 words) or the scale and the
 // sixteen sums of a block (9 words); two units per thread per round, all their
-// loads in flight together.
-template <bool Q81, bool PERM>
+// loads in flight together.  G: src is in global memory (read through L2), else
+// a raw copy of the rows already in shared memory.
+template <bool G>
+__device__ __forceinline__ uint32_t ld_act(const uint32_t* a) {
+    if constexpr (G) return __ldcg(a);
+    else return *a;
+}
+template <bool Q81, bool PERM, bool G = true>
 __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, const XRegion& x, int tid, int nthr,
                            int pitch = 0) {
     const int rb = xq_row_bytes(K);
@@ -86,12 +92,12 @@ __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, con
                                                                            static_cast<size_t>(cb[h]) * 292);
                     if (part[h] < 8) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) w[h][i] = __ldcg(bp + 1 + 8 * part[h] + i);
+                        for (int i = 0; i < 8; ++i) w[h][i] = ld_act<G>(bp + 1 + 8 * part[h] + i);
                         w[h][8] = 0u;
                     } else {
-                        w[h][0] = __ldcg(bp);
+                        w[h][0] = ld_act<G>(bp);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) w[h][1 + i] = __ldcg(bp + 65 + i);
+                        for (int i = 0; i < 8; ++i) w[h][1 + i] = ld_act<G>(bp + 65 + i);
                     }
                 }
             }
@@ -133,7 +139,7 @@ __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, con
         const int words = nb * 9;
         for (int i = tid; i < words; i += nthr) {
             const int b = i / 9, w = i - b * 9;
-            const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(b) * 36) + w);
+            const uint32_t v = ld_act<G>(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(b) * 36) + w);
             if (w == 0) {
                 x.d[b] = half_lo(v);
             } else {
@@ -147,14 +153,15 @@ __device__ void stage_acts(const uint8_t* __restrict__ src, int rows, int K, con
 
 // Stage packed Q8_0 activation rows (34-byte blocks: fp16 d, 32 quants) into
 // the per-32 structure-of-arrays region (the layout Q8_1 rows are staged in):
-// one thread per block, its 17 halfwords loaded together.
+// one thread per block, its 17 halfwords loaded together (G: from global).
+template <bool G = true>
 __device__ inline void stage_acts_q8_0(const uint8_t* __restrict__ src, int rows, int K, const XRegion& x, int tid, int nthr) {
     const int rb = xq_row_bytes(K), nbr = K >> 5;
     for (int b = tid; b < rows * nbr; b += nthr) {
         const uint16_t* h = reinterpret_cast<const uint16_t*>(src + static_cast<size_t>(b) * 34);
         uint32_t hw[17];
 #pragma unroll
-        for (int i = 0; i < 17; ++i) hw[i] = __ldg(h + i);
+        for (int i = 0; i < 17; ++i) hw[i] = G ? __ldg(h + i) : h[i];
         uint32_t w[8];
         int sum = 0;
 #pragma unroll
@@ -322,7 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     const XRegion xr_ = x_region(xreg, p.xrows, K, Q81);
     uint64_t* full = reinterpret_cast<uint64_t*>(xreg + p.x_bytes);
     uint64_t* empty = full + kMaxStages;
-    int* s_flag = reinterpret_cast<int*>(empty + kMaxStages);  // [1] abort
+    uint64_t* xready = empty + kMaxStages;  // the consumers hold their activations
+    uint64_t* xbar = xready + 1;            // the raw activation rows have landed
+    int* s_flag = reinterpret_cast<int*>(xbar + 1);  // [1] abort
 
     // ---- work items: 16-row tiles
     const int nitems = static_cast<int>((p.N + kTileRows - 1) / kTileRows);
@@ -336,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], kConsumerWarps);
             }
+            mbar_init(xready, 1);
+            mbar_init(xbar, 1);
             s_flag[0] = 0;
             s_flag[1] = 0;
             fence_barrier_init();
@@ -358,6 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                 const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
                 for (int kc = 0; kc < nkc; ++kc, ++j) {
                     const int s = j % p.stages;
+                    if (j == kEarlyStages) {  // the rest once the activations are in
+                        if (lane == 0) ok = mbar_wait(xready, 0u);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) {
+                            if (lane == 0) set_error(p.err, DEV_ERR_TIMEOUT);
+                            break;
+                        }
+                    }
                     const int64_t off = static_cast<int64_t>(kc) * p.chunk_bytes;
                     const int64_t cb = p.rowbytes - off < p.chunk_bytes ? p.rowbytes - off : p.chunk_bytes;
                     if (lane == 0) ok = mbar_wait(&empty[s], (static_cast<uint32_t>(j / p.stages) & 1u) ^ 1u);
@@ -409,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
             for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
                 const int s = j % p.stages;
                 const uint32_t ph = static_cast<uint32_t>(j / p.stages) & 1u;
+                if (j == kEarlyStages && !mbar_wait(xready, 0u)) {  // the rest once the activations are in
+                    set_error(p.err, DEV_ERR_TIMEOUT);
+                    break;
+                }
                 if (!mbar_wait(&empty[s], ph ^ 1u)) {
                     set_error(p.err, DEV_ERR_TIMEOUT);
                     break;
@@ -457,11 +480,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     }
     start_sync();  // barriers initialised, sums zeroed
     pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
-    if constexpr (AK == 1)
-        stage_acts_q8_0(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
-    else
-        stage_acts<Q81, F == F_MXFP4>(p.xq, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+    // The packed activation rows come in by one bulk copy into the last ring
+    // stage, which the producer leaves alone until xready, when they fit there:
+    // every CTA reads the same few KB, and word loads from 152 SMs queue on those
+    // few L2 lines (~1.8 us for one token).  Otherwise they are read directly.
+    const int xtot = p.xrows * (AK == 1 ? (K >> 5) * 34 : Q81 ? (K >> 5) * 36 : (K >> 8) * 292);
+    const bool xb = p.stages > kEarlyStages && xtot <= p.stage_stride && xtot % 16 == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.xq) & 15) == 0;
+    const uint8_t* xsrc = p.xq;
+    if (xb) {
+        uint8_t* const raw = ring + static_cast<size_t>(p.stages - 1) * p.stage_stride;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(xtot));
+            bulk_g2s(raw, p.xq, static_cast<uint32_t>(xtot), xbar, policy_evict_last());
+        }
+        if (!mbar_wait(xbar, 0u)) set_error(p.err, DEV_ERR_TIMEOUT);
+        xsrc = raw;
+    }
+    if constexpr (AK == 1) {
+        if (xb) stage_acts_q8_0<false>(xsrc, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+        else stage_acts_q8_0<true>(xsrc, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+    } else {
+        if (xb) stage_acts<Q81, F == F_MXFP4, false>(xsrc, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+        else stage_acts<Q81, F == F_MXFP4, true>(xsrc, p.xrows, K, xr_, ctid, kConsumerWarps * 32);
+    }
     consumer_sync();
+    if (tid == 0) mbar_arrive(xready);  // the producer may now stream the remaining weight stages
     XS xs;
     xs.q = smem_addr(xr_.q);
     xs.d = smem_addr(xr_.d);
