@@ -299,9 +299,23 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
     p.nch = p.K / chunk;
     p.wrow = bank_stride(2 * p.rowbytes);  // one stride per pair of rows
     p.stage_stride = static_cast<int>(align_up(static_cast<size_t>(kTileRows / 2 * p.wrow + 16), 128));
-    const int red_bytes = 2 * kConsumerWarps * 130 * 4, x_bytes = p.T * p.xrow;  // partials: [2][16][130] floats
+    // activation rows in shared memory: the padding (a multiple of 16 bytes, so
+    // each row stays one bulk copy) whose stride spreads the mma fragment words
+    // of tokens g = 0..7 (word g * stride + t, t = 0..3) over the most banks
+    p.xstride = p.xrow;
+    if (p.xrow % 16 == 0) {
+        int best = 33;
+        for (int pad = 0; pad < 128; pad += 16) {
+            const int sw = (p.xrow + pad) / 4;
+            int hits[32] = {0}, worst = 0;
+            for (int g = 0; g < 8; ++g)
+                for (int t = 0; t < 4; ++t) worst = std::max(worst, ++hits[(g * sw + t) % 32]);
+            if (worst < best) best = worst, p.xstride = p.xrow + pad;
+        }
+    }
+    const int red_bytes = 2 * kConsumerWarps * 130 * 4, x_bytes = p.T * p.xstride;  // partials: [2][16][130] floats
     p.x_bytes = static_cast<int>(align_up(static_cast<size_t>(red_bytes > x_bytes ? red_bytes : x_bytes), 128));
-    p.x_bulk = (x_bytes % 16 == 0 && aligned16(p.xq)) ? 1 : 0;
+    p.x_bulk = (p.xrow % 16 == 0 && aligned16(p.xq)) ? 1 : 0;
     const int fixed = p.x_bytes + kConsumerWarps * 4 * kMmavCStride * 4 + (2 * kMaxStages + 1) * 8 + 256;
     int stages = (kSmemLimit - fixed) / p.stage_stride;
     if (stages > kMaxStages) stages = kMaxStages;

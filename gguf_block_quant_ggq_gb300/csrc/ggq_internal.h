@@ -120,7 +120,8 @@ struct MmavParams {
     int64_t N;
     int K;
     const uint8_t* xq;  // packed Q8_K rows [T][K/256]
-    int xrow;           // bytes between activation rows
+    int xrow;           // bytes between activation rows (global)
+    int xstride;        // bytes between activation rows in shared memory (padded against bank conflicts)
     int T;
     float* Y;           // [T][N]
     int* err;

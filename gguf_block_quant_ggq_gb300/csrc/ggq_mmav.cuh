@@ -148,18 +148,30 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
         // group, as for Q4_K); C = -1056 (groups 0, 1 of a 128-element half: the
         // codes enter as 1024 + code) or -1536 (groups 2, 3: 1024 + 16 code) times
         // the sum of the group's activations, the weights being code - 32
+        // the start values of this thread's column pair t are shared by the
+        // warp's eight g-lanes: lane (g, t) computes those of groups g and g + 8
+        // (all lanes busy; the barrier after this function orders them)
+        uint32_t xw[16];
+        int bsv[2][2];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 16; ++j) xw[j] = 16 * j < chunk && vg ? ld_s32(rb + 4 + off + 16 * j + 4 * t) : 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = off + 16 * (g + 8 * h);
+            const bool in = 16 * (g + 8 * h) < chunk;
+            bsv[h][0] = in && v0 ? ld_s16(r0 + 260 + 2 * (e >> 4)) : 0;
+            bsv[h][1] = in && v1 ? ld_s16(r1 + 260 + 2 * (e >> 4)) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (16 * j < chunk && vg) s8x4_to_f16(xw[j], X.b[2 * j], X.b[2 * j + 1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = g + 8 * h;
             if (16 * j < chunk) {
-                const int e = off + 16 * j;
-                if (vg) s8x4_to_f16(ld_s32(rb + 4 + e + 4 * t), X.b[2 * j], X.b[2 * j + 1]);
-                const int bs0 = v0 ? ld_s16(r0 + 260 + 2 * (e >> 4)) : 0;
-                const int bs1 = v1 ? ld_s16(r1 + 260 + 2 * (e >> 4)) : 0;
-                const float cb = (e & 64) ? -1536.0f : -1056.0f;
-                if (g == 0) {
-                    cs[2 * j] = cb * static_cast<float>(bs0);
-                    cs[2 * j + 1] = cb * static_cast<float>(bs1);
-                }
+                const float cb = ((off + 16 * j) & 64) ? -1536.0f : -1056.0f;
+                *reinterpret_cast<float2*>(cs + 2 * j) =
+                    make_float2(cb * static_cast<float>(bsv[h][0]), cb * static_cast<float>(bsv[h][1]));
             }
         }
     } else {
@@ -358,12 +370,16 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         // f16 operands: a code q placed in the mantissa of 1024.0 reads 1024 + q
         // (low nibble; Q5_K adds its fifth bit at 16) or 1024 + 16q (high nibble
         // masked in place; fifth bit at 256).  One HFMA2 per operand word applies
-        // the 6-bit sub-block scale and removes the 1024: sc * q is an integer
-        // below 2048, exact in f16, so each mma adds exact products and the whole
-        // chunk accumulates in one f32 chain
+        // the 6-bit sub-block scale and removes the 1024, leaving 16 q sc 2^-24:
+        // the scale enters as the f16 whose bits are the scale byte (sc 2^-24, a
+        // subnormal; one PRMT) for high nibbles, shifted up by 4 bits (16 sc
+        // 2^-24) for low ones.  16 q sc < 2^15 has at most 11 significant bits,
+        // so the operand is exact (subnormal below 2^-14), each mma adds exact
+        // products and the chains hold exact multiples of 2^-20; the epilogue's
+        // weight scale takes the factor 2^20 back
         constexpr uint32_t SB = F == F_Q4_K ? 144u : 176u;
         constexpr uint32_t QS = F == F_Q4_K ? 16u : 48u;
-        const int js0 = (e0 & 255) >> 5;
+        const int js0 = CH == 256 ? 0 : (e0 & 255) >> 5;  // 256-input chunks start at a superblock
         const saddr b0 = r0 + SB * sb, b1 = r1 + SB * sb;
         const uint4 h0 = ld_s128(b0), h1 = ld_s128(b1);
         uint32_t s0l, s0h, m0l, m0h, s1l, s1h, m1l, m1h;
@@ -377,6 +393,10 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
                                                                    (static_cast<uint32_t>(idx) << 8)), Mr);
             return __hsub2(*reinterpret_cast<const __half2*>(&u),
                            __halves2half2(__ushort_as_half(0x6400u), __ushort_as_half(0x6400u)));
+        };
+        // (v 2^-24, v 2^-24) as f16 bits for byte idx of w: the byte itself in each half
+        const auto spair = [](uint32_t w, int idx) -> uint32_t {
+            return prmt(w, 0u, 0x4040u | static_cast<uint32_t>(idx) | (static_cast<uint32_t>(idx) << 8));
         };
         const auto as_u = [](__half2 h) -> uint32_t { return *reinterpret_cast<const uint32_t*>(&h); };
         const auto fma2 = [&](uint32_t a, __half2 m, __half2 c) -> uint32_t {
@@ -395,8 +415,6 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
             qh1b = ld_s32(b1 + 32 + 4 * t) >> js0;
         }
         const __half2 k1024 = __halves2half2(__ushort_as_half(0xE400u), __ushort_as_half(0xE400u));  // -1024
-        const __half2 k64 = __halves2half2(__ushort_as_half(0xD400u), __ushort_as_half(0xD400u));    // -64
-        const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00u), __ushort_as_half(0x2C00u));  // 1/16
         // chain ci of i-step i: 64-wide (Q5_K) or 128-wide (Q4_K) runs of the chunk
         constexpr int kChains = F == F_Q5_K ? 4 : 2;
         float Dc[kChains][4];
@@ -433,17 +451,19 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
                     }
                 }
                 // scales of sub-blocks i (low) and i + 1 (high) for rows g, g+8:
-                // low: q * sc = (1024 + q) * sc - 1024 sc; high: (1024 + 16q) * sc/16 - 64 sc
+                // low: (1024 + q) s - 1024 s with s = 16 sc 2^-24; high: (1024 + 16q) s -
+                // 1024 s with s = sc 2^-24; both leave 16 q sc 2^-24
                 const uint32_t w0s = i < 4 ? s0l : s0h, w1s = i < 4 ? s1l : s1h;
-                const __half2 sa0 = pair(w0s, i & 3), sa1 = pair(w1s, i & 3);
-                const __half2 sb0 = pair(w0s, (i + 1) & 3), sb1 = pair(w1s, (i + 1) & 3);
+                const uint32_t ua0 = spair(w0s, i & 3) << 4, ua1 = spair(w1s, i & 3) << 4;
+                const uint32_t ub0 = spair(w0s, (i + 1) & 3), ub1 = spair(w1s, (i + 1) & 3);
+                const __half2 sa0 = *reinterpret_cast<const __half2*>(&ua0), sa1 = *reinterpret_cast<const __half2*>(&ua1);
+                const __half2 sb0 = *reinterpret_cast<const __half2*>(&ub0), sb1 = *reinterpret_cast<const __half2*>(&ub1);
                 const __half2 ca0 = __hmul2(sa0, k1024), ca1 = __hmul2(sa1, k1024);
-                const __half2 cb0 = __hmul2(sb0, k64), cb1 = __hmul2(sb1, k64);
-                const __half2 hb0 = __hmul2(sb0, k16th), hb1 = __hmul2(sb1, k16th);
+                const __half2 cb0 = __hmul2(sb0, k1024), cb1 = __hmul2(sb1, k1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     L[k] = fma2(L[k], (k & 1) ? sa1 : sa0, (k & 1) ? ca1 : ca0);
-                    H[k] = fma2(H[k], (k & 1) ? hb1 : hb0, (k & 1) ? cb1 : cb0);
+                    H[k] = fma2(H[k], (k & 1) ? sb1 : sb0, (k & 1) ? cb1 : cb0);
                 }
                 mma_f16(D, L[0], L[1], L[2], L[3], X.b[4 * i], X.b[4 * i + 1]);
                 mma_f16(D, L[4], L[5], L[6], L[7], X.b[4 * i + 2], X.b[4 * i + 3]);
@@ -463,12 +483,14 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
             for (int q = 0; q < 4; ++q) {
                 int a = 0;
 #pragma unroll
-                for (int ci = 0; ci < kChains; ++ci) a += __float2int_rn(Dc[ci][q]);
+                for (int ci = 0; ci < kChains; ++ci) a += __float2int_rn(Dc[ci][q] * 1048576.0f);  // exact: 2^20
                 dump_add(dz.q[q], 2 * sbi, a);
                 dump_add(dz.q[q], 2 * sbi + 1, __float2int_rn(DM[q]));
             }
         }
-        const float d0 = half_lo(h0.x), dm0 = half_hi(h0.x), d1 = half_lo(h1.x), dm1 = half_hi(h1.x);
+        // the weight scale d times 2^20 (the operands' 2^-20, exact)
+        const float d0 = half_lo(h0.x) * 1048576.0f, dm0 = half_hi(h0.x), d1 = half_lo(h1.x) * 1048576.0f,
+                    dm1 = half_hi(h1.x);
         acc[0] = X.dx0 * (d0 * D[0] - dm0 * DM[0]);
         acc[1] = X.dx1 * (d0 * D[1] - dm0 * DM[1]);
         acc[2] = X.dx0 * (d1 * D[2] - dm1 * DM[2]);
@@ -613,19 +635,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     // ================= consumers
     mmav_start_sync();  // barriers initialised
     pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
-    const int xbytes = p.T * p.xrow;
+    // activation row r -> xreg + r * xstride (the padded stride puts the eight
+    // rows' fragment words on distinct banks)
     bool xok = true;
     if (p.x_bulk) {
-        if (tid == 0) {
-            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(xbytes));
-            bulk_g2s(xreg, p.xq, static_cast<uint32_t>(xbytes), xbar, policy_evict_last());
+        if (warp == 0) {  // lane r copies row r, after lane 0 has announced the bytes
+            if (lane == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(p.T * p.xrow));
+            __syncwarp();
+            if (lane < p.T)
+                bulk_g2s(xreg + static_cast<size_t>(lane) * p.xstride, p.xq + static_cast<size_t>(lane) * p.xrow,
+                         static_cast<uint32_t>(p.xrow), xbar, policy_evict_last());
         }
         xok = mbar_wait(xbar, 0u);
         if (!xok) set_error(p.err, DEV_ERR_TIMEOUT);
     } else {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.xq);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(xreg);
-        for (int i = tid; i < xbytes / 4; i += kConsumerWarps * 32) dst[i] = __ldg(src + i);
+        const int wr = p.xrow / 4;
+        for (int i = tid; i < p.T * wr; i += kConsumerWarps * 32) {
+            const int r = i / wr, w = i - r * wr;
+            reinterpret_cast<uint32_t*>(xreg + static_cast<size_t>(r) * p.xstride)[w] =
+                __ldg(reinterpret_cast<const uint32_t*>(p.xq + static_cast<size_t>(r) * p.xrow) + w);
+        }
         mmav_sync();
     }
     const int g = lane >> 2, t = lane & 3;
@@ -633,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
     const int e0 = warp * p.chunk;
     MmaX X;
     float* cs = creg + (warp * 4 + t) * kMmavCStride;
-    mmav_load_x<F>(smem_addr(xreg), p.xrow, active ? p.T : 0, p.chunk, e0, g, t, X, cs);
+    mmav_load_x<F>(smem_addr(xreg), p.xstride, active ? p.T : 0, p.chunk, e0, g, t, X, cs);
     mmav_sync();  // the region now holds partials
     const saddr ring_s = smem_addr(ring);
     int j = 0, s = 0;
