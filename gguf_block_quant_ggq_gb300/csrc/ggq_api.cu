@@ -437,15 +437,36 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
     return GGQ_OK;
 }
 
-// Expert banks that the expert-sorted route runs on the tcgen05 grouped GEMM
-// (128-row weight tiles): Q8_0 gate/up and Q4_K down.
-bool tc_gateup(int f, int64_t I, int64_t H) {
-    (void)H;
-    return f == F_Q8_0 && I % 128 == 0;
+// One tcgen05 grouped GEMM, dumping its integer core when asked.  Q8_0 and Q4_K
+// dump from the launch that computes the outputs.  MXFP4 folds each block's
+// power of two into its operand and sums a whole superblock in one accumulator,
+// so its integer core (one exact dot per 32-block) comes from a launch of the
+// same kernel in its per-block schedule, run first; the folded launch then
+// writes the outputs, which are therefore the same with and without the dump.
+cudaError_t gmmtc_run(int f, const GmmTcParams& t, bool dump, int grid, cudaStream_t st) {
+    if (!dump) return launch_gmmtc(f, t, grid, st);
+    cudaError_t e = launch_gmmtc_dump(f, t, grid, st);
+    if (e == cudaSuccess && f == F_MXFP4) e = launch_gmmtc(f, t, grid, st);
+    return e;
 }
-bool tc_down(int f, int64_t H, int64_t I) {
+
+// Expert banks that the expert-sorted route runs on the tcgen05 grouped GEMM
+// (128-row weight tiles): Q8_0 and MXFP4 gate/up, Q4_K and MXFP4 down.  MXFP4
+// goes there once the experts carry at least kMxTcPairs (token, expert) pairs
+// on average: each of its k-steps costs a fixed ~0.7 us of role hand-offs
+// whatever the column count, and below that load the int8 grouped kernel,
+// whose cost scales with the columns, is faster (measured on the 256-expert
+// H 4096 / I 2048 layer: 1.95 ms against 3.79 ms at 128 tokens, 4.20 ms against
+// 3.86 ms at 512 tokens).
+constexpr int64_t kMxTcPairs = 16;
+bool tc_format(int f, int64_t P, int64_t E) { return f != F_MXFP4 || P >= kMxTcPairs * E; }
+bool tc_gateup(int f, int64_t I, int64_t H, int64_t P, int64_t E) {
+    (void)H;
+    return (f == F_Q8_0 || f == F_MXFP4) && I % 128 == 0 && tc_format(f, P, E);
+}
+bool tc_down(int f, int64_t H, int64_t I, int64_t P, int64_t E) {
     (void)I;
-    return f == F_Q4_K && H % 128 == 0;
+    return (f == F_Q4_K || f == F_MXFP4) && H % 128 == 0 && tc_format(f, P, E);
 }
 
 // Largest token count on the direct tiny-batch route (ds4 PR #656 "Add ROCm
@@ -462,7 +483,7 @@ constexpr int kDirectFixed = 2 * kMaxStages * 8 + static_cast<int>(sizeof(Direct
 // tokens, and 16 down rows of I with h^ of the pairs; expert-sorted route: the
 // grouped int8 kernel's whole-row slots where the f16 / tcgen05 kernels (which
 // step through K) do not serve the format.
-const char* moe_width_refusal(int fg, int fd, int64_t H, int64_t I, int64_t T, int top_k) {
+const char* moe_width_refusal(int fg, int fd, int64_t E, int64_t H, int64_t I, int64_t T, int top_k) {
     int smem = 0;
     if (T <= kDirectMaxTokens) {
         StreamShape sh;
@@ -474,13 +495,13 @@ const char* moe_width_refusal(int fg, int fd, int64_t H, int64_t I, int64_t T, i
             return "moe_experts: I too wide for shared memory";
         return nullptr;
     }
-    if (!tc_gateup(fg, I, H) && !gmm_supported(fg)) {
+    if (!tc_gateup(fg, I, H, T * top_k, E) && !gmm_supported(fg)) {
         GroupParams g{};
         g.rowbytes = w_row_bytes(fg, H);
         g.K = static_cast<int>(H);
         if (!plan_group(g, 2, false, &smem)) return "moe_experts: H too wide for shared memory";
     }
-    if (!tc_down(fd, H, I) && !gmm_supported(fd)) {
+    if (!tc_down(fd, H, I, T * top_k, E) && !gmm_supported(fd)) {
         GroupParams d{};
         d.rowbytes = w_row_bytes(fd, I);
         d.K = static_cast<int>(I);
@@ -565,10 +586,10 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     float* const hdx = reinterpret_cast<float*>(base + ms.hdx);
     int smem = 0;
     bool h_dumped = false;  // the SwiGLU quantizer wrote dump->h itself
-    const bool tcg = tc_gateup(fg, I, H);
+    const bool tcg = tc_gateup(fg, I, H, P, E);
     if (tcg) {
-        // Q8_0 gate/up on tcgen05: g and u per pair, then h = silu(g) u fused into its quantizer
-        e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st);
+        // Q8_0 / MXFP4 gate/up on tcgen05: g and u per pair, then h = silu(g) u fused into its quantizer
+        e = launch_q8k_to_f16(xq, xp, I32(ms.perm), top_k, P, H, x16, xbs, xdx, dx_pitch(H), st, fg == F_MXFP4);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: x to f16 launch");
         GmmTcParams t{};
         const int r = gmmtc_encode(t, fg, g.W, g.W2, g.rowbytes, E * I, x16, xdx, dx_pitch(H), nullptr, P,
@@ -590,7 +611,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         t.coefs[0] = cg;
         t.coefs[1] = cu;
         t.ncoef = ncg;
-        e = cg ? launch_gmmtc_dump(fg, t, c->nsm, st) : launch_gmmtc(fg, t, c->nsm, st);
+        e = gmmtc_run(fg, t, cg != nullptr, c->nsm, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: gate/up launch");
         e = launch_quantize_silu(gbuf, ubuf, P, I, hq, hp, dump ? dump->h : nullptr, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: SwiGLU quantize launch");
@@ -639,9 +660,9 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     d.o = o;
     d.coefs[0] = d.coefs[1] = cd;
     d.ncoef = ncd;
-    if (tc_down(fd, H, I)) {
-        // Q4_K down on tcgen05
-        e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
+    if (tc_down(fd, H, I, P, E)) {
+        // Q4_K / MXFP4 down on tcgen05
+        e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st, fd == F_MXFP4);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
         GmmTcParams t{};
         const int r = gmmtc_encode(t, fd, d.W, nullptr, d.rowbytes, E * H, h16, hdx, dx_pitch(I), hbs, P,
@@ -659,7 +680,7 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
         t.out[0] = t.out[1] = o;
         t.coefs[0] = t.coefs[1] = cd;
         t.ncoef = ncd;
-        e = cd ? launch_gmmtc_dump(fd, t, c->nsm, st) : launch_gmmtc(fd, t, c->nsm, st);
+        e = gmmtc_run(fd, t, cd != nullptr, c->nsm, st);
     } else if (gmm_supported(fd)) {
         e = launch_q8k_to_f16(hq, hp, I32(ms.perm), 1, P, I, h16, hbs, hdx, dx_pitch(I), st);
         if (e != cudaSuccess) return cuda_fail(c, e, "moe sorted: h to f16 launch");
@@ -729,7 +750,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     if (top_k < 1 || top_k > 8 || E < top_k || E > 4096)
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: need 1 <= top_k <= 8 and top_k <= E <= 4096");
     if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
-    if (const char* why = moe_width_refusal(fg, fd, H, I, T, top_k)) return fail(c, GGQ_ERR_SHAPE, "%s", why);
+    if (const char* why = moe_width_refusal(fg, fd, E, H, I, T, top_k)) return fail(c, GGQ_ERR_SHAPE, "%s", why);
     if (c->tel_pairs && E > c->tel_experts)
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: E=%lld exceeds the %lld experts of the telemetry buffer",
                     static_cast<long long>(E), static_cast<long long>(c->tel_experts));

@@ -1,5 +1,6 @@
 // ggq_gmmtc.cuh -- the expert-sorted grouped GEMM on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory) for Q8_0 and Q4_K expert banks.
+// cores (tcgen05, accumulators in tensor memory) for Q8_0, Q4_K and MXFP4
+// expert banks.
 //
 // Same arithmetic as the keep-quant expert GEMM of vllm.cpp PR #523
 // "grouped + non-grouped keep-quant expert GEMM" (What changed: DotQ8_0 /
@@ -14,7 +15,17 @@
 //     <= 128 * 945 * 127 < 2^24: exact), and the mins term sum_j m_j * (16-group
 //     sums of x) is one more K = 16 MMA of the mins against the activations'
 //     exact group sums; the epilogue adds D d d_x after the first half and
-//     (D d - Dmin dmin) d_x after the second.
+//     (D d - Dmin dmin) d_x after the second;
+//   * MXFP4 (ds4 PR #656 "Add ROCm MXFP4 routed expert kernels", Summary:
+//     MXFP4 x Q8_K gate/up and down): bf16 operands.  A doubled E2M1 code
+//     (2v <= 12, 4 significant bits) times its block's E8M0 power of two is
+//     exact in bf16 for every scale whose products fit in f32, and so is an
+//     int8 activation; the power of two is folded into the decoded weight,
+//     every product is exact, and one accumulator spans a whole superblock
+//     (one drain and one d_x per 256 inputs, as Q4_K).  The f32 sums inside a
+//     superblock then round at 2^-24 relative when the block exponents differ;
+//     to dump the integer core, the same kernel keeps the codes unscaled and
+//     one accumulator per 32-block (the Q8_0 schedule), whose dots are exact.
 //
 // Work item: (expert, matrix, 128 weight rows, 128 activation columns).  The
 // activation operand is f16 rows in expert-sorted order (one per (token,
@@ -25,17 +36,17 @@
 //     bytes of the 128 weight rows (the 80-byte 16-aligned span holding the
 //     k-step's two blocks) and, at a superblock's end, the activation scales;
 //     4-stage ring, completion on one mbarrier per stage;
-//   * decode (warps 8-13): raw codes -> f16 weight tile in the same SW128
-//     K-major layout (3 buffers), then fence.proxy.async so the tensor core
-//     sees the generic-proxy stores;
+//   * decode (warps 8-13; MXFP4: 4-13): raw codes -> f16 (bf16) weight tile in
+//     the same SW128 K-major layout (4-5 buffers), then fence.proxy.async so the
+//     tensor core sees the generic-proxy stores;
 //   * MMA (one elected lane of warp 15): two K=16 MMAs per 32-block into one of
 //     two 128-column tensor-memory accumulators, tcgen05.commit to the
 //     accumulator's mbarrier (the thread's only commits: a tcgen05 instruction
 //     costs its issuing thread ~90 cycles); the epilogue, having seen a k-step's
 //     last accumulator land (every earlier MMA has then completed), releases the
 //     k-step's weight tile and ring slot;
-//   * epilogue (warps 0-7; warp w owns TMEM lanes 32 (w & 3) .. +31 = tile rows
-//     and 64 of the 128 columns): tcgen05.ld of each block accumulator,
+//   * epilogue (warps 0-7, MXFP4: 0-3; warp w owns TMEM lanes 32 (w & 3) .. +31
+//     = tile rows and 64 (MXFP4: all 128) columns): tcgen05.ld of each block accumulator,
 //     T += D * d_w (d_w: this thread's row), and at the superblock's end
 //     acc += T * d_x (d_x: per column) in a third tensor-memory region; at the
 //     item's end acc goes to the output rows (one f32 row per pair: lanes write
@@ -44,42 +55,59 @@
 // Every wait is bounded: a wait that gives up sets the error word and the
 // shared abort flag, and every role leaves its loop.
 #pragma once
+#include <cuda_bf16.h>
+
 #include "ggq_device.cuh"
 #include "ggq_internal.h"
 
 namespace ggq {
 
 constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64;
-constexpr int kTcStages = 4;  // TMA ring
-constexpr int kTcEpi = 256;   // epilogue threads (warps 0-7)
-constexpr int kTcDec = 192;   // decode threads (warps 8-13)
 constexpr int kTcTmaWarp = 14, kTcMmaWarp = 15;
 constexpr int kTcRaw = 80;  // raw bytes per weight row per k-step (Q8_0: the 16-aligned span of two 34-byte blocks)
+constexpr int kTcRawMx = 48;  // MXFP4: the 16-aligned span of two 17-byte blocks (34 bytes at an even offset < 16)
 constexpr int kTcMaxGroups = 4096;
-static_assert(kTcThreads == kTcEpi + kTcDec + 64, "warp roles");
+
+// Warp roles per format: epilogue warps 0 .. kEpi/32 - 1, decode warps up to 13,
+// then the TMA and MMA warps.  MXFP4 drains once per superblock and decodes
+// the most per weight (a table lookup per code), so it trades epilogue warps
+// for decode warps.
+template <int F, bool DUMP = false>
+struct TcRoles {
+    static constexpr int kEpi = F == F_MXFP4 && !DUMP ? 128 : 256;   // epilogue threads
+    static constexpr int kDec = kTcThreads - 64 - kEpi;      // decode threads
+    static constexpr int kEpiCols = kTcBN * 128 / kEpi;      // accumulator columns per epilogue warp (64 or 128)
+};
+static_assert(kTcThreads == TcRoles<F_Q8_0>::kEpi + TcRoles<F_Q8_0>::kDec + 64, "warp roles");
 
 // Shared-memory layout per format: the TMA ring, then the decoded weight tiles
 // (Q8_0: 5, Q4_K: 4 plus the two mins-term tiles), the item table, the barriers.
 // More weight tiles decouple the decode from the MMA's completion.
 template <int F>
 struct TcSmem {
-    static constexpr int kABufs = F == F_Q8_0 ? 5 : 4;
+    // TMA ring depth and decoded weight tiles: a stage is released only once its
+    // k-step's MMAs have completed, so the ring must cover the weight fetch, the
+    // decode and the MMA of several k-steps; Q4_K also holds the mins operands
+    static constexpr int kStages = F == F_MXFP4 ? 6 : F == F_Q8_0 ? 5 : 4;
+    static constexpr int kABufs = F == F_Q4_K ? 4 : 3;
     static constexpr int kB = kTcBN * kTcBK * 2;     // 16384, SW128 K-major
-    static constexpr int kRawRow = kTcRaw;           // raw bytes per weight row per k-step
+    static constexpr int kRawRow = F == F_MXFP4 ? kTcRawMx : kTcRaw;  // raw bytes per weight row per k-step
     static constexpr int kRaw = kTcBM * kRawRow;     // 10240
     static constexpr int kDX = kTcBN * 16;           // 2048: 4 superblock scales per column
     static constexpr int kStage = kB + kRaw + kDX;   // 28672 (28 KB: activation tiles stay 1024-aligned)
     static constexpr int kA = kTcBM * kTcBK * 2;     // 16384, SW128 K-major
-    static constexpr int oA = kTcStages * kStage;
+    static constexpr int oA = kStages * kStage;
     static constexpr int oMin = oA + kABufs * kA;    // Q4_K mins-term operands: two SW128 tiles
-    static constexpr int oPrefix = oMin + (F == F_Q8_0 ? 0 : 2 * kA);
+    static constexpr int oPrefix = oMin + (F == F_Q4_K ? 2 * kA : 0);
     static constexpr int kPrefix = (kTcMaxGroups + 1) * 4;
     static constexpr int oBars = (oPrefix + kPrefix + 7) / 8 * 8;
-    static constexpr int kBars = (2 * kTcStages + 2 * kABufs + 4) * 8 + 16;
+    static constexpr int kBars = (2 * kStages + 2 * kABufs + 4) * 8 + 16;
     static constexpr int kTotal = oBars + kBars + 1024;  // + alignment slack of the dynamic base
 };
 static_assert(TcSmem<F_Q8_0>::kStage % 1024 == 0 && TcSmem<F_Q8_0>::oA % 1024 == 0, "SW128 tiles need 1024-byte alignment");
-static_assert(TcSmem<F_Q8_0>::kTotal <= kSmemLimit && TcSmem<F_Q4_K>::kTotal <= kSmemLimit,
+static_assert(TcSmem<F_MXFP4>::kStage % 1024 == 0 && TcSmem<F_MXFP4>::oA % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+static_assert(TcSmem<F_Q8_0>::kTotal <= kSmemLimit && TcSmem<F_Q4_K>::kTotal <= kSmemLimit &&
+                  TcSmem<F_MXFP4>::kTotal <= kSmemLimit,
               "tcgen05 grouped GEMM shared memory");
 
 // tensor-memory columns: two block accumulators, then the item accumulator
@@ -91,9 +119,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
-// instruction descriptor: f32 accumulate, f16 A and B, both K-major, M = 128, N = n
-__host__ __device__ constexpr uint32_t tc_idesc(uint32_t n) {
-    return (1u << 4) | ((n >> 3) << 17) | ((static_cast<uint32_t>(kTcBM) >> 4) << 24);
+// instruction descriptor: f32 accumulate, f16 (bf16: both operands bf16) A and
+// B, both K-major, M = 128, N = n
+__host__ __device__ constexpr uint32_t tc_idesc(uint32_t n, bool bf16 = false) {
+    return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((n >> 3) << 17) |
+           ((static_cast<uint32_t>(kTcBM) >> 4) << 24);
 }
 // Items with at most this many columns load a 32-row activation box and run N = 32
 // MMAs (decode-sized token counts spread over many experts).
@@ -214,16 +244,62 @@ __device__ __forceinline__ void tc_dump32(const GmmTcParams& p, const TcItem& cu
     }
 }
 
+// The bf16 pair (2^(e-128), 2^(e-128)) for an E8M0 byte e: the power of two by
+// which the doubled E2M1 codes are scaled (bf16 holds it for every e below 255,
+// as a subnormal for e = 0, 1; e = 255 is NaN).
+__device__ __forceinline__ uint32_t tc_e8m0_bf16x2(uint32_t e) {
+    const uint32_t b = e == 255u ? 0x7FC0u : e >= 2u ? (e - 1u) << 7 : (e == 1u ? 0x40u : 0x20u);  // 255: NaN
+    return b | (b << 16);
+}
+
+// MXFP4 decode of one 32-block of one row into its 64-byte span of a SW128 bf16
+// tile row (chunks 4 blk .. 4 blk + 3, XOR-swizzled by the row): the doubled
+// E2M1 codes come from the PRMT lookup as 2v + 12 (ordered j, j+16, j+1, j+17),
+// are placed as 128 + (2v + 12) in bf16 (exponent 2^7, exact), and become
+// 2v * s with s = 2^(e-128) (production; exact in bf16 for every E8M0 value
+// whose products fit) or s = 1 (integer-core dump: the exact doubled codes).
+__device__ __forceinline__ void tc_mx_block(uint8_t* at, int r, int blk, const uint32_t* q, uint32_t s2) {
+    const uint32_t k43 = 0x43434343u;
+    const __nv_bfloat162 k140 = __halves2bfloat162(__ushort_as_bfloat16(0x430Cu), __ushort_as_bfloat16(0x430Cu));
+    const __nv_bfloat162 sv = *reinterpret_cast<const __nv_bfloat162*>(&s2);
+    const auto conv = [&](uint32_t x) -> uint32_t {
+        const __nv_bfloat162 v = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&x), k140), sv);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    };
+    uint32_t lo[8], hi[8];  // elements 0..15 and 16..31 as bf16 pairs
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t L = mx_lookup(q[w] & 0xFFFFu), H = mx_lookup(q[w] >> 16);  // (4w, 4w+16, 4w+1, 4w+17), (+2 ..)
+        lo[2 * w] = conv(prmt(L, k43, 0x4240u));
+        lo[2 * w + 1] = conv(prmt(H, k43, 0x4240u));
+        hi[2 * w] = conv(prmt(L, k43, 0x4341u));
+        hi[2 * w + 1] = conv(prmt(H, k43, 0x4341u));
+    }
+    uint8_t* const row = at + r * 128;
+    const int c0 = 4 * blk;
+    *reinterpret_cast<uint4*>(row + (((c0 + 0) ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    *reinterpret_cast<uint4*>(row + (((c0 + 2) ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(row + (((c0 + 3) ^ (r & 7)) << 4)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+}
+
 template <int F, bool DUMP>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__ GmmTcParams p) {
-    static_assert(F == F_Q8_0 || F == F_Q4_K, "tcgen05 grouped GEMM: Q8_0 and Q4_K banks");
-    constexpr bool Q8 = F == F_Q8_0;  // one accumulator and one weight scale per 32-block
+    static_assert(F == F_Q8_0 || F == F_Q4_K || F == F_MXFP4, "tcgen05 grouped GEMM: Q8_0, Q4_K and MXFP4 banks");
+    constexpr bool MX = F == F_MXFP4;
+    // PB: one accumulator and one weight scale per 32-block, applied by the
+    // epilogue (Q8_0; MXFP4 when dumping the integer core).  Otherwise one
+    // accumulator per half superblock (Q4_K) or superblock (MXFP4, whose
+    // power-of-two block scales are folded into the bf16 operand).
+    constexpr bool PB = F == F_Q8_0 || (MX && DUMP);
+    constexpr int kTcEpi = TcRoles<F, DUMP>::kEpi, kTcDec = TcRoles<F, DUMP>::kDec;
+    constexpr int kEpiCols = TcRoles<F, DUMP>::kEpiCols, kEpiChunks = kEpiCols / 32;
     constexpr int kRawRow = TcSmem<F>::kRawRow;
-    // tensor-memory columns: block (Q8_0) or superblock (Q4_K) accumulators 0..255,
-    // Q4_K mins term 256..383, item accumulator
-    constexpr uint32_t kAcc = Q8 ? 256u : 384u, kDmin = 256u;
+    // tensor-memory columns: block, half-superblock or superblock accumulators
+    // 0..255, Q4_K mins term 256..383, item accumulator
+    constexpr uint32_t kAcc = F == F_Q4_K ? 384u : 256u, kDmin = 256u;
     using SM = TcSmem<F>;
-    constexpr int kTcABufs = SM::kABufs;
+    constexpr int kTcABufs = SM::kABufs, kTcStages = SM::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* const smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -248,13 +324,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&full[s], 1);
-            // Q8_0: decode and epilogue threads (the epilogue has seen the k-step's MMAs complete);
-            // Q4_K: the MMA's commit, decode and epilogue threads
-            mbar_init(&empty[s], kTcDec + kTcEpi + (Q8 ? 0 : 1));
+            // PB: decode and epilogue threads (the epilogue has seen the k-step's MMAs complete);
+            // otherwise the MMA's commit, decode and epilogue threads
+            mbar_init(&empty[s], kTcDec + kTcEpi + (PB ? 0 : 1));
         }
         for (int a = 0; a < kTcABufs; ++a) {
             mbar_init(&afull[a], kTcDec);
-            mbar_init(&aempty[a], Q8 ? kTcEpi : 1);
+            mbar_init(&aempty[a], PB ? kTcEpi : 1);
         }
         for (int d = 0; d < 2; ++d) {
             mbar_init(&tfull[d], 1);
@@ -304,9 +380,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     const auto item_of = [&](int it) {
         return tc_item(p, s_pref, ngroups, mtiles, static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x));
     };
-    // raw bytes per k-step: Q8_0 the 80-byte spans; Q4_K headers [128][16], nibbles [128][32],
-    // then at a superblock's end the activation 16-group sums [128][32]
-    constexpr uint32_t kRawTx = Q8 ? SM::kRaw : kTcBM * 48;
+    // raw bytes per k-step: Q8_0 the 80-byte spans, MXFP4 the 48-byte spans; Q4_K
+    // headers [128][16], nibbles [128][32], then at a superblock's end the
+    // activation 16-group sums [128][32]
+    constexpr uint32_t kRawTx = F == F_Q4_K ? kTcBM * 48 : SM::kRaw;
     constexpr int kQsOff = kTcBM * 16, kBsOff = kTcBM * 48;
 
     if (warp == kTcTmaWarp) {
@@ -318,36 +395,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (c >= kTcStages && !tc_wait(&empty[s], ((c / kTcStages) - 1) & 1, abort, p.err)) break;
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
-                const bool dx_load = Q8 ? sb_end : (kt & 1) == 1;  // Q4_K: at each half superblock's end
+                const bool dx_load = F == F_Q4_K ? (kt & 1) == 1 : sb_end;  // Q4_K: at each half superblock's end
                 const bool narrow = cur.ncols <= kTcNarrow;  // 32 activation rows suffice
                 mbar_arrive_expect_tx(&full[s], (narrow ? kTcNarrow * 128 : SM::kB) + kRawTx + (dx_load ? SM::kDX : 0) +
-                                                    (sb_end && !Q8 ? kTcBN * 32 : 0));
+                                                    (sb_end && F == F_Q4_K ? kTcBN * 32 : 0));
                 tc_tma_2d(smem_addr(B16(s)), narrow ? &p.tm_b32 : &p.tm_b, kt * kTcBK, cur.y0, &full[s]);
-                if constexpr (Q8) {
+                if constexpr (F == F_Q8_0) {
                     tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (68 * kt) & ~15, cur.wrow, &full[s]);
+                } else if constexpr (MX) {
+                    tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[cur.m], (34 * kt) & ~15, cur.wrow, &full[s]);
                 } else {
                     const int x = (kt >> 2) * 144;
                     tc_tma_2d(smem_addr(RAW(s)), &p.tm_w[0], x, cur.wrow, &full[s]);
                     tc_tma_2d(smem_addr(RAW(s)) + kQsOff, &p.tm_w[1], x + 16 + 32 * (kt & 3), cur.wrow, &full[s]);
                 }
                 if (dx_load) tc_tma_2d(smem_addr(DXS(s)), &p.tm_dx, (kt >> 2) & ~3, cur.y0, &full[s]);
-                if (!Q8 && sb_end) tc_tma_2d(smem_addr(RAW(s)) + kBsOff, &p.tm_bs, (kt >> 2) * 16, cur.y0, &full[s]);
+                if (F == F_Q4_K && sb_end) tc_tma_2d(smem_addr(RAW(s)) + kBsOff, &p.tm_bs, (kt >> 2) * 16, cur.y0, &full[s]);
             }
             __syncwarp();
         }
     } else if (warp == kTcMmaWarp) {
         // ================================================================ MMA
-        uint32_t idesc = tc_idesc(kTcBN);
+        uint32_t idesc = tc_idesc(kTcBN, MX);
         for (int c = 0; c < total; ++c) {
             const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
-            if (kt == 0) idesc = tc_idesc(item_of(c / nk).ncols <= kTcNarrow ? kTcNarrow : kTcBN);
+            if (kt == 0) idesc = tc_idesc(item_of(c / nk).ncols <= kTcNarrow ? kTcNarrow : kTcBN, MX);
             if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
             if (!tc_wait(&afull[a], (c / kTcABufs) & 1, abort, p.err)) break;
             tc_fence_after();
             // descriptors are linear in the start address (16-byte units): K steps add 2 per 32 bytes
             const uint64_t adesc = umma_desc_sw128(smem_addr(ATILE(a))), bdesc = umma_desc_sw128(smem_addr(B16(s)));
             bool ok = true;
-            if constexpr (Q8) {
+            if constexpr (PB) {
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     const int gb = 2 * c + b, db = gb & 1;
@@ -365,23 +444,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     __syncwarp();
                 }
             } else {
-                // one accumulator per half superblock (2 k-steps): buffer 0 takes the first
-                // halves, buffer 1 the second halves and, beside it, the mins term.  nk is a
-                // multiple of 4, so c and kt agree on (c & 3).  Waiting for buffer 1's previous
-                // drain also frees the single mins region (the epilogue reads both together).
-                const int hsi = c >> 1, db = hsi & 1;
-                if ((kt & 1) == 0 && hsi >= 2 && !tc_wait(&tempty[db], ((hsi >> 1) - 1) & 1, abort, p.err)) ok = false;
+                // one accumulator per span of SP k-steps (Q4_K: a half superblock, buffer 0
+                // taking the first halves, buffer 1 the second halves and, beside it, the mins
+                // term; MXFP4: a superblock).  nk is a multiple of 4, so c and kt agree on
+                // (c & 3).  For Q4_K, waiting for buffer 1's previous drain also frees the
+                // single mins region (the epilogue reads both together).
+                constexpr int SH = MX ? 2 : 1, SP = 1 << SH;
+                const int hsi = c >> SH, db = hsi & 1;
+                const bool first = (kt & (SP - 1)) == 0, last = (kt & (SP - 1)) == SP - 1;
+                if (first && hsi >= 2 && !tc_wait(&tempty[db], ((hsi >> 1) - 1) & 1, abort, p.err)) ok = false;
                 if (ok) {
                     tc_fence_after();
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + static_cast<uint64_t>(2 * kk),
-                                   bdesc + static_cast<uint64_t>(2 * kk), idesc, static_cast<uint32_t>((kt & 1) != 0 || kk != 0));
-                        if ((kt & 3) == 3)
+                                   bdesc + static_cast<uint64_t>(2 * kk), idesc, static_cast<uint32_t>(!first || kk != 0));
+                        if (F == F_Q4_K && (kt & 3) == 3)
                             tc_mma(tmem + kDmin, umma_desc_sw128(smem_addr(min_a)), umma_desc_sw128(smem_addr(min_b)), idesc,
                                    0u);
-                        if ((kt & 1) == 1) tc_commit(&tfull[db]);
+                        if (last) tc_commit(&tfull[db]);
                         tc_commit(&aempty[a]);
                         tc_commit(&empty[s]);
                     }
@@ -400,14 +482,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             if (c >= kTcABufs && !tc_wait(&aempty[a], ((c / kTcABufs) - 1) & 1, abort, p.err)) break;
             const saddr raw = smem_addr(RAW(s));
             uint8_t* const at = ATILE(a);
-            if constexpr (Q8) {
+            if constexpr (MX) {
+                // unit: one 32-block of one row (row u >> 1, block u & 1): its E8M0 byte and 16 nibble bytes
+                const int o0 = (34 * kt) & 15;
+                for (int u = dt; u < 2 * kTcBM; u += kTcDec) {
+                    const int r = u >> 1, blk = u & 1;
+                    const saddr b = raw + static_cast<uint32_t>(r * kRawRow + o0 + 17 * blk);
+                    uint32_t q[4];
+                    ld_words_any<4>(b + 1, q);
+                    const uint32_t s2 = DUMP ? 0x3F803F80u : tc_e8m0_bf16x2(ld_u8(b));
+                    tc_mx_block(at, r, blk, q, s2);
+                }
+            } else if constexpr (F == F_Q8_0) {
                 const int o0 = (68 * kt) & 15;
                 uint32_t w[kUnits][4];
 #pragma unroll
                 for (int h = 0; h < kUnits; ++h) {
                     const int u = dt + kTcDec * h;  // row u >> 2, block (u >> 1) & 1, half u & 1
                     if (u < kTcBM * 4)
-                        ld_words_any<4>(raw + static_cast<uint32_t>((u >> 2) * kTcRaw + o0 + 34 * ((u >> 1) & 1) + 2 + 16 * (u & 1)), w[h]);
+                        ld_words_any<4>(raw + static_cast<uint32_t>((u >> 2) * kRawRow + o0 + 34 * ((u >> 1) & 1) + 2 + 16 * (u & 1)), w[h]);
                 }
 #pragma unroll
                 for (int h = 0; h < kUnits; ++h) {
@@ -500,29 +593,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         }
     } else {
         // ================================================================ epilogue
-        const int q = warp & 3, col0 = 64 * (warp >> 2), r = 32 * q + lane;
+        // warp w: tensor-memory lanes 32 (w & 3) .. +31 (tile rows) and kEpiCols columns
+        const int q = warp & 3, col0 = kEpiCols * (warp >> 2), r = 32 * q + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        float T[Q8 ? 64 : 1];
+        float T[PB ? kEpiCols : 1];
         bool live = true;
         for (int it = 0; it < my_items && live; ++it) {
             const TcItem cur = item_of(it);
             // column chunks h2 of this warp that hold accumulators (narrow items: the first 32 columns)
             const int ncol_acc = cur.ncols <= kTcNarrow ? kTcNarrow : kTcBN;
-            const bool act[2] = {col0 < ncol_acc, col0 + 32 < ncol_acc};
+            bool act[kEpiChunks];
+#pragma unroll
+            for (int h2 = 0; h2 < kEpiChunks; ++h2) act[h2] = col0 + 32 * h2 < ncol_acc;
             for (int kt = 0; kt < nk && live; ++kt) {
                 const int c = it * nk + kt, s = c % kTcStages;
                 const saddr raw = smem_addr(RAW(s));
-                if constexpr (Q8) {
-                    const int o0 = (68 * kt) & 15;
+                if constexpr (PB) {
+                    const int o0 = MX ? (34 * kt) & 15 : (68 * kt) & 15;
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         const int gb = 2 * c + b, db = gb & 1;
                         if (!tc_wait(&tfull[db], (gb >> 1) & 1, abort, p.err)) { live = false; break; }
                         tc_fence_after();
-                        const float dw = ld_h(raw + static_cast<uint32_t>(r * kRawRow + o0 + 34 * b));
+                        const saddr wb = raw + static_cast<uint32_t>(r * kRawRow + o0 + (MX ? 17 : 34) * b);
+                        const float dw = MX ? e8m0_half_scale(ld_u8(wb)) : ld_h(wb);
                         const bool first = b == 0 && (kt & 3) == 0;
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
+                        for (int h2 = 0; h2 < kEpiChunks; ++h2) {
                             if (!act[h2]) continue;
                             float v[32];
                             tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
@@ -538,7 +635,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     if ((kt & 3) == 3) {  // superblock end: acc += T * d_x (per column)
                         const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
+                        for (int h2 = 0; h2 < kEpiChunks; ++h2) {
                             if (!act[h2]) continue;
                             float a[32];
                             const uint32_t ta = lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2);
@@ -553,32 +650,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                             tmem_st32(ta, a);
                         }
                     }
-                } else if ((kt & 1) == 1) {
-                    // half-superblock end: acc += D d d_x (first half) or (D d - Dmin dmin) d_x (second)
-                    const int hsi = c >> 1, db = hsi & 1;
+                } else if (MX ? (kt & 3) == 3 : (kt & 1) == 1) {
+                    // MXFP4: superblock end, acc += D d_x (the block scales are in the operands);
+                    // Q4_K: half-superblock end, acc += D d d_x (first half) or (D d - Dmin dmin) d_x (second)
+                    const int hsi = c >> (MX ? 2 : 1), db = hsi & 1;
                     const bool second = (kt & 3) == 3;
                     if (!tc_wait(&tfull[db], (hsi >> 1) & 1, abort, p.err)) { live = false; break; }
                     tc_fence_after();
-                    const uint32_t dh = ld_s32(raw + static_cast<uint32_t>(r * 16));  // d, dmin of this row
-                    const float dd = half_lo(dh), dm = half_hi(dh);
+                    float dd = 1.0f, dm = 0.0f;
+                    if constexpr (!MX) {
+                        const uint32_t dh = ld_s32(raw + static_cast<uint32_t>(r * 16));  // d, dmin of this row
+                        dd = half_lo(dh), dm = half_hi(dh);
+                    }
                     const saddr dxs = smem_addr(DXS(s)) + 4u * ((kt >> 2) & 3);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
+                    for (int h2 = 0; h2 < kEpiChunks; ++h2) {
                         if (!act[h2]) continue;
                         float v[32], m[32], a[32];
                         tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
-                        if (second) {
+                        if (!MX && second) {
                             tmem_ld32(lane_base + kDmin + static_cast<uint32_t>(col0 + 32 * h2), m);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) m[j] = 0.0f;
                         }
-                        if constexpr (DUMP) {
+                        if constexpr (DUMP && !MX) {
                             tc_dump32(p, cur, r, col0 + 32 * h2, v, 2 * (kt >> 2), second);
                             if (second) tc_dump32(p, cur, r, col0 + 32 * h2, m, 2 * (kt >> 2) + 1, false);
                         }
                         const uint32_t ta = lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2);
-                        if (kt == 1) {
+                        if (kt == (MX ? 3 : 1)) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) a[j] = 0.0f;
                         } else {
@@ -599,7 +700,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             float* const out = p.out[cur.m];
             const int64_t row = static_cast<int64_t>(cur.mt) * kTcBM + r;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+            for (int h2 = 0; h2 < kEpiChunks; ++h2) {
                 if (!act[h2]) continue;
                 float a[32];
                 tmem_ld32(lane_base + kAcc + static_cast<uint32_t>(col0 + 32 * h2), a);

@@ -209,7 +209,8 @@ cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* curso
 cudaError_t launch_scatter(const int32_t* ids, int P, int E, const int* offsets, int* cursor, int* perm,
                            cudaStream_t s);
 cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, int div, int64_t rows, int64_t K,
-                              __half* x16, __half* bs16, float* dx, int64_t dx_pitch, cudaStream_t s);
+                              __half* x16, __half* bs16, float* dx, int64_t dx_pitch, cudaStream_t s,
+                              bool bf16 = false);
 // Tensor maps of one grouped GEMM launch (host encode; 0 or a CUresult).
 int gmm_encode(GmmParams& p, int kind, int fmt, const uint8_t* W, const uint8_t* W2, int64_t rowbytes, int64_t wrows,
                const __half* x16, const float* dx, int64_t dx_pitch, const __half* bs16, int64_t P, int K);

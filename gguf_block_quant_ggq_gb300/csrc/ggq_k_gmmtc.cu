@@ -1,4 +1,4 @@
-// ggq_k_gmmtc.cu -- tensor maps and launch of the tcgen05 grouped GEMM (Q8_0 and Q4_K banks).
+// ggq_k_gmmtc.cu -- tensor maps and launch of the tcgen05 grouped GEMM (Q8_0, Q4_K and MXFP4 banks).
 #include "ggq_gmmtc.cuh"
 
 #include <atomic>
@@ -17,9 +17,10 @@ int gmmtc_encode(GmmTcParams& p, int fmt, const uint8_t* W, const uint8_t* W2, i
     if (!r) r = encode_tmap_2d(&p.tm_bs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bs16 ? bs16 : x16, k / 16, np, k / 8, 16, kTcBN,
                                CU_TENSOR_MAP_SWIZZLE_NONE);
     const uint64_t rb = static_cast<uint64_t>(rowbytes), nr = static_cast<uint64_t>(wrows);
-    if (fmt == F_Q8_0) {
+    if (fmt == F_Q8_0 || fmt == F_MXFP4) {
+        const int box = fmt == F_Q8_0 ? kTcRaw : kTcRawMx;
         for (int m = 0; m < 2 && !r; ++m)
-            r = encode_tmap_2d(&p.tm_w[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, m ? (W2 ? W2 : W) : W, rb, nr, rb, kTcRaw, kTcBM,
+            r = encode_tmap_2d(&p.tm_w[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, m ? (W2 ? W2 : W) : W, rb, nr, rb, box, kTcBM,
                                CU_TENSOR_MAP_SWIZZLE_NONE);
     } else {
         if (!r) r = encode_tmap_2d(&p.tm_w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, W, rb, nr, rb, 16, kTcBM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -47,6 +48,7 @@ cudaError_t launch_gmmtc(int fmt, const GmmTcParams& p, int grid, cudaStream_t s
     switch (fmt) {
     case F_Q8_0: return launch_gmmtc_one<F_Q8_0, false>(p, grid, s);
     case F_Q4_K: return launch_gmmtc_one<F_Q4_K, false>(p, grid, s);
+    case F_MXFP4: return launch_gmmtc_one<F_MXFP4, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -55,6 +57,7 @@ cudaError_t launch_gmmtc_dump(int fmt, const GmmTcParams& p, int grid, cudaStrea
     switch (fmt) {
     case F_Q8_0: return launch_gmmtc_one<F_Q8_0, true>(p, grid, s);
     case F_Q4_K: return launch_gmmtc_one<F_Q4_K, true>(p, grid, s);
+    case F_MXFP4: return launch_gmmtc_one<F_MXFP4, true>(p, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

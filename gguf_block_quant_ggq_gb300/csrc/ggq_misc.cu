@@ -199,7 +199,9 @@ cudaError_t launch_quantize_silu(const float* g, const float* u, int64_t rows, i
 // f16 (exact), the 16-element group sums as f16 (|sum| <= 2032: exact) and the
 // block scales as f32.  Output row r takes input row map[r] / div (the
 // expert-sorted order of the (token, expert) pairs), or row r without a map.
-// One warp per block.
+// BF16: the quants as bf16 instead (the MXFP4 operands; exact too).  One warp
+// per block.
+template <bool BF16>
 __global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, const int* __restrict__ map, int div,
                              int64_t rows, int nbr, __half* __restrict__ x16, __half* __restrict__ bs16,
                              float* __restrict__ dx, int64_t dx_pitch) {
@@ -215,13 +217,24 @@ __global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, const
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const uint32_t u = __ldcg(qw + 2 * lane + i) ^ 0x80808080u;  // x + 128 in each byte
-        const uint32_t a = prmt(u, 0u, 0x4140u) | 0x64006400u, bb = prmt(u, 0u, 0x4342u) | 0x64006400u;
-        const __half2 off = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
-        const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), off);
-        const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&bb), off);
-        out[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
-        out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+        if constexpr (BF16) {
+            // an int8 value is exact in bf16: the top half of its f32 bits
+            const uint32_t w = __ldcg(qw + 2 * lane + i);
+            uint32_t h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                h[k] = __float_as_uint(static_cast<float>(static_cast<int8_t>((w >> (8 * k)) & 0xFFu))) >> 16;
+            out[2 * i] = h[0] | (h[1] << 16);
+            out[2 * i + 1] = h[2] | (h[3] << 16);
+        } else {
+            const uint32_t u = __ldcg(qw + 2 * lane + i) ^ 0x80808080u;  // x + 128 in each byte
+            const uint32_t a = prmt(u, 0u, 0x4140u) | 0x64006400u, bb = prmt(u, 0u, 0x4342u) | 0x64006400u;
+            const __half2 off = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+            const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), off);
+            const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&bb), off);
+            out[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+        }
     }
     const int64_t K = static_cast<int64_t>(nbr) * 256;
     *reinterpret_cast<uint4*>(x16 + r * K + c * 256 + 8 * lane) = make_uint4(out[0], out[1], out[2], out[3]);
@@ -233,11 +246,15 @@ __global__ void k_q8k_to_f16(const uint8_t* __restrict__ q, int64_t pitch, const
 }
 
 cudaError_t launch_q8k_to_f16(const uint8_t* q, int64_t pitch, const int* map, int div, int64_t rows, int64_t K,
-                              __half* x16, __half* bs16, float* dx, int64_t dx_pitch, cudaStream_t s) {
+                              __half* x16, __half* bs16, float* dx, int64_t dx_pitch, cudaStream_t s, bool bf16) {
     const int64_t nb = rows * (K / 256);
     if (nb == 0) return cudaSuccess;
-    return launch_pdl(k_q8k_to_f16, dim3(static_cast<unsigned>((nb * 32 + 255) / 256)), dim3(256), 0, s, q, pitch, map,
-                      div, rows, static_cast<int>(K / 256), x16, bs16, dx, dx_pitch);
+    const dim3 grid(static_cast<unsigned>((nb * 32 + 255) / 256));
+    if (bf16)
+        return launch_pdl(k_q8k_to_f16<true>, grid, dim3(256), 0, s, q, pitch, map, div, rows,
+                          static_cast<int>(K / 256), x16, bs16, dx, dx_pitch);
+    return launch_pdl(k_q8k_to_f16<false>, grid, dim3(256), 0, s, q, pitch, map, div, rows, static_cast<int>(K / 256),
+                      x16, bs16, dx, dx_pitch);
 }
 
 // One warp per token: top-k by logit (ties to the lower index) and the

@@ -230,9 +230,11 @@ def test_moe_q8_0_banks_sorted(ctx):
     _run_and_check(ctx, cfg, 16, 24, sample_tokens=6)
 
 
-@pytest.mark.parametrize("T", [5, 8, 32, 128])
+@pytest.mark.parametrize("T", [5, 8, 32, 64, 128])
 def test_moe_sorted_route_mxfp4(ctx, T):
-    """5 tokens and up: expert-sorted tiles on the grouped int8 tensor-core kernel."""
+    """5 tokens and up: expert-sorted tiles, on the grouped int8 tensor-core
+    kernel below 16 (token, expert) pairs per expert (here T < 64) and on the
+    tcgen05 grouped GEMM with bf16 operands from there (T = 64, 128)."""
     _run_and_check(ctx, syn.MOE_MXFP4, 32, T, sample_tokens=None if T <= 8 else 6)
 
 
