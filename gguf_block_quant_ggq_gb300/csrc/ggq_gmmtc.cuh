@@ -229,6 +229,29 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
     return ok;
 }
 
+// The same wait by one thread (the MMA role runs on one lane).
+__device__ __forceinline__ bool tc_wait1(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+    const bool ok = !*abort && mbar_wait(bar, parity);
+    if (!ok) {
+        *abort = 1;
+        set_error(err, DEV_ERR_TIMEOUT);
+    }
+    return ok;
+}
+
+// Position of k-step c in the rings, advanced without divisions (a role's
+// loop bookkeeping is on its critical path): TMA slot s and the phase of its
+// current use, decoded tile a and its phase, k-step kt of item it.
+struct TcPos {
+    int s = 0, a = 0, kt = 0, it = 0;
+    uint32_t fph = 0u, aph = 0u;
+    __device__ __forceinline__ void next(int stages, int abufs, int nk) {
+        if (++s == stages) s = 0, fph ^= 1u;
+        if (++a == abufs) a = 0, aph ^= 1u;
+        if (++kt == nk) kt = 0, ++it;
+    }
+};
+
 // Integer-core dump of 32 accumulator columns of this thread's row: the exact
 // integer each holds goes to coefficient idx of the column's pair (added to
 // what is there with `add`: the second half of a Q4_K superblock).
@@ -389,10 +412,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     if (warp == kTcTmaWarp) {
         // ================================================================ TMA
         TcItem cur{};
-        for (int c = 0; c < total; ++c) {
-            const int it = c / nk, kt = c - it * nk, s = c % kTcStages;
-            if (kt == 0) cur = item_of(it);
-            if (c >= kTcStages && !tc_wait(&empty[s], ((c / kTcStages) - 1) & 1, abort, p.err)) break;
+        TcPos q;
+        for (int c = 0; c < total; ++c, q.next(kTcStages, kTcABufs, nk)) {
+            const int kt = q.kt, s = q.s;
+            if (kt == 0) cur = item_of(q.it);
+            if (c >= kTcStages && !tc_wait(&empty[s], q.fph ^ 1u, abort, p.err)) break;
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
                 const bool dx_load = F == F_Q4_K ? (kt & 1) == 1 : sb_end;  // Q4_K: at each half superblock's end
@@ -415,24 +439,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             __syncwarp();
         }
     } else if (warp == kTcMmaWarp) {
-        // ================================================================ MMA
-        uint32_t idesc = tc_idesc(kTcBN, MX);
-        for (int c = 0; c < total; ++c) {
-            const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
-            if (kt == 0) idesc = tc_idesc(item_of(c / nk).ncols <= kTcNarrow ? kTcNarrow : kTcBN, MX);
-            if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
-            if (!tc_wait(&afull[a], (c / kTcABufs) & 1, abort, p.err)) break;
-            tc_fence_after();
-            // descriptors are linear in the start address (16-byte units): K steps add 2 per 32 bytes
-            const uint64_t adesc = umma_desc_sw128(smem_addr(ATILE(a))), bdesc = umma_desc_sw128(smem_addr(B16(s)));
-            bool ok = true;
-            if constexpr (PB) {
+        // ================================================================ MMA (one lane)
+        if (lane == 0) {
+            uint32_t idesc = tc_idesc(kTcBN, MX);
+            TcPos q;
+            for (int c = 0; c < total; ++c, q.next(kTcStages, kTcABufs, nk)) {
+                const int s = q.s, a = q.a, kt = q.kt;
+                if (kt == 0) idesc = tc_idesc(item_of(q.it).ncols <= kTcNarrow ? kTcNarrow : kTcBN, MX);
+                if (!tc_wait1(&full[s], q.fph, abort, p.err)) break;
+                if (!tc_wait1(&afull[a], q.aph, abort, p.err)) break;
+                tc_fence_after();
+                // descriptors are linear in the start address (16-byte units): K steps add 2 per 32 bytes
+                const uint64_t adesc = umma_desc_sw128(smem_addr(ATILE(a))), bdesc = umma_desc_sw128(smem_addr(B16(s)));
+                bool ok = true;
+                if constexpr (PB) {
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int gb = 2 * c + b, db = gb & 1;
-                    if (gb >= 2 && !tc_wait(&tempty[db], ((gb >> 1) - 1) & 1, abort, p.err)) { ok = false; break; }
-                    tc_fence_after();
-                    if (lane == 0) {
+                    for (int b = 0; b < 2; ++b) {
+                        const int gb = 2 * c + b, db = gb & 1;
+                        if (gb >= 2 && !tc_wait1(&tempty[db], ((gb >> 1) - 1) & 1, abort, p.err)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = static_cast<uint64_t>((2 * b + kk) * 2);
@@ -441,21 +466,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                         }
                         tc_commit(&tfull[db]);
                     }
-                    __syncwarp();
-                }
-            } else {
-                // one accumulator per span of SP k-steps (Q4_K: a half superblock, buffer 0
-                // taking the first halves, buffer 1 the second halves and, beside it, the mins
-                // term; MXFP4: a superblock).  nk is a multiple of 4, so c and kt agree on
-                // (c & 3).  For Q4_K, waiting for buffer 1's previous drain also frees the
-                // single mins region (the epilogue reads both together).
-                constexpr int SH = MX ? 2 : 1, SP = 1 << SH;
-                const int hsi = c >> SH, db = hsi & 1;
-                const bool first = (kt & (SP - 1)) == 0, last = (kt & (SP - 1)) == SP - 1;
-                if (first && hsi >= 2 && !tc_wait(&tempty[db], ((hsi >> 1) - 1) & 1, abort, p.err)) ok = false;
-                if (ok) {
-                    tc_fence_after();
-                    if (lane == 0) {
+                } else {
+                    // one accumulator per span of SP k-steps (Q4_K: a half superblock, buffer 0
+                    // taking the first halves, buffer 1 the second halves and, beside it, the mins
+                    // term; MXFP4: a superblock).  nk is a multiple of 4, so c and kt agree on
+                    // (c & 3).  For Q4_K, waiting for buffer 1's previous drain also frees the
+                    // single mins region (the epilogue reads both together).
+                    constexpr int SH = MX ? 2 : 1, SP = 1 << SH;
+                    const int hsi = c >> SH, db = hsi & 1;
+                    const bool first = (kt & (SP - 1)) == 0, last = (kt & (SP - 1)) == SP - 1;
+                    if (first && hsi >= 2 && !tc_wait1(&tempty[db], ((hsi >> 1) - 1) & 1, abort, p.err)) ok = false;
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + static_cast<uint64_t>(2 * kk),
@@ -467,19 +489,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                         tc_commit(&aempty[a]);
                         tc_commit(&empty[s]);
                     }
-                    __syncwarp();
                 }
+                if (!ok) break;
             }
-            if (!ok) break;
         }
+        __syncwarp();
     } else if (warp >= kTcEpi / 32) {
         // ================================================================ decode
         const int dt = tid - kTcEpi;
         constexpr int kUnits = (kTcBM * 4 + kTcDec - 1) / kTcDec;  // 16-output units of the 128 x 64 tile
-        for (int c = 0; c < total; ++c) {
-            const int s = c % kTcStages, a = c % kTcABufs, kt = c % nk;
-            if (!tc_wait(&full[s], (c / kTcStages) & 1, abort, p.err)) break;
-            if (c >= kTcABufs && !tc_wait(&aempty[a], ((c / kTcABufs) - 1) & 1, abort, p.err)) break;
+        TcPos q;
+        for (int c = 0; c < total; ++c, q.next(kTcStages, kTcABufs, nk)) {
+            const int s = q.s, a = q.a, kt = q.kt;
+            if (!tc_wait(&full[s], q.fph, abort, p.err)) break;
+            if (c >= kTcABufs && !tc_wait(&aempty[a], q.aph ^ 1u, abort, p.err)) break;
             const saddr raw = smem_addr(RAW(s));
             uint8_t* const at = ATILE(a);
             if constexpr (MX) {
@@ -598,6 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
         float T[PB ? kEpiCols : 1];
         bool live = true;
+        TcPos pos;
         for (int it = 0; it < my_items && live; ++it) {
             const TcItem cur = item_of(it);
             // column chunks h2 of this warp that hold accumulators (narrow items: the first 32 columns)
@@ -606,7 +630,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
 #pragma unroll
             for (int h2 = 0; h2 < kEpiChunks; ++h2) act[h2] = col0 + 32 * h2 < ncol_acc;
             for (int kt = 0; kt < nk && live; ++kt) {
-                const int c = it * nk + kt, s = c % kTcStages;
+                const int c = it * nk + kt, s = pos.s;
                 const saddr raw = smem_addr(RAW(s));
                 if constexpr (PB) {
                     const int o0 = MX ? (34 * kt) & 15 : (68 * kt) & 15;
@@ -629,7 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                         }
                         tc_fence_before();
                         mbar_arrive(&tempty[db]);
-                        if (b == 1) mbar_arrive(&aempty[c % kTcABufs]);  // every MMA of the k-step has completed
+                        if (b == 1) mbar_arrive(&aempty[pos.a]);  // every MMA of the k-step has completed
                     }
                     if (!live) break;
                     if ((kt & 3) == 3) {  // superblock end: acc += T * d_x (per column)
@@ -694,6 +718,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     mbar_arrive(&tempty[db]);
                 }
                 mbar_arrive(&empty[s]);
+                pos.next(kTcStages, kTcABufs, nk);
             }
             if (!live) break;
             // item end: this thread's row of the item's columns
