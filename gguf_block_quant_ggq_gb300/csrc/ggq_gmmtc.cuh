@@ -71,14 +71,23 @@ constexpr int kTcMaxGroups = 4096;
 // Warp roles per format: epilogue warps 0 .. kEpi/32 - 1, decode warps up to 13,
 // then the TMA and MMA warps.  MXFP4 drains once per superblock and decodes
 // the most per weight (a table lookup per code), so it trades epilogue warps
-// for decode warps.
+// for decode warps: eight of them (one 32-block per thread and k-step), none
+// on the MMA warp's SMSP (warps 7 and 11 stay idle), whose single issuing
+// thread otherwise waits for issue slots at every step of its loop.
 template <int F, bool DUMP = false>
 struct TcRoles {
-    static constexpr int kEpi = F == F_MXFP4 && !DUMP ? 128 : 256;   // epilogue threads
-    static constexpr int kDec = kTcThreads - 64 - kEpi;      // decode threads
-    static constexpr int kEpiCols = kTcBN * 128 / kEpi;      // accumulator columns per epilogue warp (64 or 128)
+    static constexpr bool kMx = F == F_MXFP4 && !DUMP;
+    static constexpr int kEpi = kMx ? 128 : 256;                   // epilogue threads
+    static constexpr int kDec = kMx ? 256 : kTcThreads - 64 - kEpi;  // decode threads
+    static constexpr int kEpiCols = kTcBN * 128 / kEpi;            // accumulator columns per epilogue warp (64 or 128)
+    // decode ordinal of a warp (its threads are dt = 32 * ordinal + lane), or -1
+    __device__ static int dec_ord(int warp) {
+        if (kMx) return warp == 7 || warp == 11 ? -1 : warp - 4 - (warp > 7) - (warp > 11);
+        return warp - kEpi / 32;
+    }
 };
 static_assert(kTcThreads == TcRoles<F_Q8_0>::kEpi + TcRoles<F_Q8_0>::kDec + 64, "warp roles");
+static_assert(TcRoles<F_MXFP4>::kEpi + TcRoles<F_MXFP4>::kDec + 2 * 32 + 64 == kTcThreads, "MXFP4 warp roles");
 
 // Shared-memory layout per format: the TMA ring, then the decoded weight tiles
 // (Q8_0: 5, Q4_K: 4 plus the two mins-term tiles), the item table, the barriers.
@@ -496,7 +505,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         __syncwarp();
     } else if (warp >= kTcEpi / 32) {
         // ================================================================ decode
-        const int dt = tid - kTcEpi;
+        const int ord = TcRoles<F, DUMP>::dec_ord(warp);
+        if (ord < 0) goto idle;  // no role (MXFP4: the warps on the MMA warp's SMSP)
+        const int dt = 32 * ord + lane;
         constexpr int kUnits = (kTcBM * 4 + kTcDec - 1) / kTcDec;  // 16-output units of the 128 x 64 tile
         TcPos q;
         for (int c = 0; c < total; ++c, q.next(kTcStages, kTcABufs, nk)) {
@@ -737,6 +748,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             }
         }
     }
+idle:
     tc_fence_before();
     __syncthreads();
     if (warp == kTcMmaWarp) {
