@@ -185,6 +185,23 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// (d0, d1) = (a0, a1) * b + (c0, c1) as one packed f32x2 FMA (round to nearest,
+// each lane exactly an fmaf): half the issue slots of two FFMAs.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), packed
+__device__ __forceinline__ void ffma2p(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 __device__ __forceinline__ void tc_tma_2d(saddr dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
@@ -660,7 +677,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                             tmem_ld32(lane_base + static_cast<uint32_t>(db * kTcBN + col0 + 32 * h2), v);
                             if constexpr (DUMP) tc_dump32(p, cur, r, col0 + 32 * h2, v, 2 * kt + b, false);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) T[32 * h2 + j] = first ? v[j] * dw : fmaf(v[j], dw, T[32 * h2 + j]);
+                            for (int j = 0; j < 32; j += 2) {
+                                float* const t = T + 32 * h2 + j;
+                                ffma2(t[0], t[1], v[j], v[j + 1], dw, first ? 0.0f : t[0], first ? 0.0f : t[1]);
+                            }
                         }
                         tc_fence_before();
                         mbar_arrive(&tempty[db]);
@@ -681,7 +701,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                                 tmem_ld32(ta, a);
                             }
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) a[j] = fmaf(T[32 * h2 + j], ld_f32(dxs + 16u * (col0 + 32 * h2 + j)), a[j]);
+                            for (int j = 0; j < 32; j += 2)
+                                ffma2p(a[j], a[j + 1], T[32 * h2 + j], T[32 * h2 + j + 1], ld_f32(dxs + 16u * (col0 + 32 * h2 + j)),
+                                       ld_f32(dxs + 16u * (col0 + 32 * h2 + j + 1)), a[j], a[j + 1]);
                             tmem_st32(ta, a);
                         }
                     }
@@ -721,8 +743,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                             tmem_ld32(ta, a);
                         }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            a[j] = fmaf(fmaf(v[j], dd, -m[j] * dm), ld_f32(dxs + 16u * (col0 + 32 * h2 + j)), a[j]);
+                        for (int j = 0; j < 32; j += 2) {
+                            float w0, w1;  // D d - Dmin dmin (MXFP4: D)
+                            ffma2(w0, w1, v[j], v[j + 1], dd, -m[j] * dm, -m[j + 1] * dm);
+                            ffma2p(a[j], a[j + 1], w0, w1, ld_f32(dxs + 16u * (col0 + 32 * h2 + j)),
+                                   ld_f32(dxs + 16u * (col0 + 32 * h2 + j + 1)), a[j], a[j + 1]);
+                        }
                         tmem_st32(ta, a);
                     }
                     tc_fence_before();
