@@ -110,7 +110,7 @@ struct TcSmem {
     static constexpr int oPrefix = oMin + (F == F_Q4_K ? 2 * kA : 0);
     static constexpr int kPrefix = (kTcMaxGroups + 1) * 4;
     static constexpr int oBars = (oPrefix + kPrefix + 7) / 8 * 8;
-    static constexpr int kBars = (2 * kStages + 2 * kABufs + 4) * 8 + 16;
+    static constexpr int kBars = (2 * kStages + 2 * kABufs + 6) * 8 + 16;
     static constexpr int kTotal = oBars + kBars + 1024;  // + alignment slack of the dynamic base
 };
 static_assert(TcSmem<F_Q8_0>::kStage % 1024 == 0 && TcSmem<F_Q8_0>::oA % 1024 == 0, "SW128 tiles need 1024-byte alignment");
@@ -346,7 +346,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     constexpr int kRawRow = TcSmem<F>::kRawRow;
     // tensor-memory columns: block, half-superblock or superblock accumulators
     // 0..255, Q4_K mins term 256..383, item accumulator
-    constexpr uint32_t kAcc = F == F_Q4_K ? 384u : 256u, kDmin = 256u;
+    // per-block schedule: three block accumulators (0..383), so the MMA runs a block
+    // further ahead of the epilogue's drains
+    constexpr int kTB = PB ? 3 : 2;
+    constexpr uint32_t kAcc = F == F_Q4_K || PB ? 384u : 256u, kDmin = 256u;
     using SM = TcSmem<F>;
     constexpr int kTcABufs = SM::kABufs, kTcStages = SM::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -360,8 +363,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
     uint64_t* const afull = empty + kTcStages;
     uint64_t* const aempty = afull + kTcABufs;
     uint64_t* const tfull = aempty + kTcABufs;
-    uint64_t* const tempty = tfull + 2;
-    uint32_t* const tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* const tempty = tfull + 3;
+    uint32_t* const tslot = reinterpret_cast<uint32_t*>(tempty + 3);
     volatile int* const abort = reinterpret_cast<volatile int*>(tslot + 1);
     const auto B16 = [&](int s) { return smem + s * SM::kStage; };
     const auto RAW = [&](int s) { return smem + s * SM::kStage + SM::kB; };
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
             mbar_init(&afull[a], kTcDec);
             mbar_init(&aempty[a], PB ? kTcEpi : 1);
         }
-        for (int d = 0; d < 2; ++d) {
+        for (int d = 0; d < kTB; ++d) {
             mbar_init(&tfull[d], 1);
             mbar_init(&tempty[d], kTcEpi);
         }
@@ -469,6 +472,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         if (lane == 0) {
             uint32_t idesc = tc_idesc(kTcBN, MX);
             TcPos q;
+            int tb = 0;           // per-block schedule: accumulator of the next block
+            uint32_t tph = 0u;    // and the phase of its use
             for (int c = 0; c < total; ++c, q.next(kTcStages, kTcABufs, nk)) {
                 const int s = q.s, a = q.a, kt = q.kt;
                 if (kt == 0) idesc = tc_idesc(item_of(q.it).ncols <= kTcNarrow ? kTcNarrow : kTcBN, MX);
@@ -481,16 +486,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                 if constexpr (PB) {
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
-                        const int gb = 2 * c + b, db = gb & 1;
-                        if (gb >= 2 && !tc_wait1(&tempty[db], ((gb >> 1) - 1) & 1, abort, p.err)) { ok = false; break; }
+                        const int gb = 2 * c + b;
+                        if (gb >= kTB && !tc_wait1(&tempty[tb], tph ^ 1u, abort, p.err)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = static_cast<uint64_t>((2 * b + kk) * 2);
-                            tc_mma(tmem + static_cast<uint32_t>(db * kTcBN), adesc + koff, bdesc + koff, idesc,
+                            tc_mma(tmem + static_cast<uint32_t>(tb * kTcBN), adesc + koff, bdesc + koff, idesc,
                                    static_cast<uint32_t>(kk));
                         }
-                        tc_commit(&tfull[db]);
+                        tc_commit(&tfull[tb]);
+                        if (++tb == kTB) tb = 0, tph ^= 1u;
                     }
                 } else {
                     // one accumulator per span of SP k-steps (Q4_K: a half superblock, buffer 0
@@ -650,6 +656,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         float T[PB ? kEpiCols : 1];
         bool live = true;
         TcPos pos;
+        int tb = 0;          // per-block schedule: accumulator of the next block
+        uint32_t tph = 0u;   // and the phase of its use
         for (int it = 0; it < my_items && live; ++it) {
             const TcItem cur = item_of(it);
             // column chunks h2 of this warp that hold accumulators (narrow items: the first 32 columns)
@@ -664,8 +672,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     const int o0 = MX ? (34 * kt) & 15 : (68 * kt) & 15;
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
-                        const int gb = 2 * c + b, db = gb & 1;
-                        if (!tc_wait(&tfull[db], (gb >> 1) & 1, abort, p.err)) { live = false; break; }
+                        const int db = tb;
+                        if (!tc_wait(&tfull[db], tph, abort, p.err)) { live = false; break; }
+                        if (++tb == kTB) tb = 0, tph ^= 1u;
                         tc_fence_after();
                         const saddr wb = raw + static_cast<uint32_t>(r * kRawRow + o0 + (MX ? 17 : 34) * b);
                         const float dw = MX ? e8m0_half_scale(ld_u8(wb)) : ld_h(wb);
