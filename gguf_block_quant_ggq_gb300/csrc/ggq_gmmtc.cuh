@@ -245,8 +245,22 @@ __device__ __forceinline__ TcItem tc_item(const GmmTcParams& p, const int* s_pre
 // Bounded wait by a whole warp (every lane polls); the result is the same in
 // every lane, so loops leave together.  On failure flags the CTA (abort) and
 // the error word.
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
-    bool ok = !*abort && mbar_wait(bar, parity);
+// Bounded wait that sleeps a little between probes: for the roles that wait
+// long (the epilogue between drains, the TMA warp for a free slot), so that
+// they leave the issue slots of their SMSP to the roles with work (the single
+// MMA thread shares one with an epilogue warp).
+__device__ __forceinline__ bool mbar_wait_nap(uint64_t* bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(64);
+        if (mbar_test(bar, parity)) return true;
+        if (clock64() - t0 > (1ll << 32)) return false;
+    }
+}
+
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, bool nap = false) {
+    bool ok = !*abort && (nap ? mbar_wait_nap(bar, parity) : mbar_wait(bar, parity));
     ok = __all_sync(0xFFFFFFFFu, ok);
     if (!ok) {
         *abort = 1;
@@ -445,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
         for (int c = 0; c < total; ++c, q.next(kTcStages, kTcABufs, nk)) {
             const int kt = q.kt, s = q.s;
             if (kt == 0) cur = item_of(q.it);
-            if (c >= kTcStages && !tc_wait(&empty[s], q.fph ^ 1u, abort, p.err)) break;
+            if (c >= kTcStages && !tc_wait(&empty[s], q.fph ^ 1u, abort, p.err, true)) break;
             if (lane == 0) {
                 const bool sb_end = (kt & 3) == 3;
                 const bool dx_load = F == F_Q4_K ? (kt & 1) == 1 : sb_end;  // Q4_K: at each half superblock's end
@@ -673,7 +687,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         const int db = tb;
-                        if (!tc_wait(&tfull[db], tph, abort, p.err)) { live = false; break; }
+                        if (!tc_wait(&tfull[db], tph, abort, p.err, true)) { live = false; break; }
                         if (++tb == kTB) tb = 0, tph ^= 1u;
                         tc_fence_after();
                         const saddr wb = raw + static_cast<uint32_t>(r * kRawRow + o0 + (MX ? 17 : 34) * b);
@@ -721,7 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gmmtc(const __grid_constant__
                     // Q4_K: half-superblock end, acc += D d d_x (first half) or (D d - Dmin dmin) d_x (second)
                     const int hsi = c >> (MX ? 2 : 1), db = hsi & 1;
                     const bool second = (kt & 3) == 3;
-                    if (!tc_wait(&tfull[db], (hsi >> 1) & 1, abort, p.err)) { live = false; break; }
+                    if (!tc_wait(&tfull[db], (hsi >> 1) & 1, abort, p.err, true)) { live = false; break; }
                     tc_fence_after();
                     float dd = 1.0f, dm = 0.0f;
                     if constexpr (!MX) {
