@@ -23,12 +23,10 @@ constexpr int kMaxDevices = 64;     // device ordinals with per-device launch st
 // stages (a few KB to tens of KB) keep about kInFlightBytes in flight.
 constexpr int kWholeRowStages = 3;
 constexpr int kInFlightBytes = 140 * 1024;
-// With static weights the decode GEMVs copy this many weight stages before the
-// previous kernel has finished; the rest follow once the CTA holds its
-// activations.  Those activation reads otherwise queue behind every SM's early
-// weight copies (measured: ~2.5 us to stage one token's activations behind
-// three 37 KB stages per SM).
-constexpr int kEarlyStages = 1;
+// Weight stages streamed before the activations are in (with static weights,
+// before the previous kernel has finished): the streaming kernel's whole-row
+// rings all but the last (which takes the activation rows), the tensor-path
+// GEMV one.
 
 enum Kind : int { KIND_GEMV = 0, KIND_DUMP = 1, KIND_GATEUP = 2, KIND_DOWN = 3, KIND_DOWNF = 4 };
 

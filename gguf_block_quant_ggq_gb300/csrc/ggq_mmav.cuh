@@ -597,8 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const MmavParams p) {
             const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
             if (lane == 0) {
                 // with static weights, the stages after the first once the activations are in
-                // (their bulk copy's barrier; without it, once the previous kernel has finished)
-                if (p.early_weights && j == kEarlyStages) {
+                // (their bulk copies' barrier; without it, once the previous kernel has finished):
+                // measured faster than streaming all but the last stage first
+                if (p.early_weights && j == 1) {
                     if (p.x_bulk) ok = mbar_wait(xbar, 0u);
                     else pdl_wait();
                 }

@@ -312,8 +312,11 @@ __device__ __noinline__ void row_coefs_one(saddr row, const XS& xs, int xrow, in
 }
 
 // AK: the activation blocks -- 0: the format's own pairing (Q8_1 for Q4_0, Q8_K
-// otherwise); 1: Q8_0 activation blocks (with Q4_0 or Q8_0 weights).
-template <int KIND, int F, int NT, int AK = 0>
+// otherwise); 1: Q8_0 activation blocks (with Q4_0 or Q8_0 weights).  CH: the
+// GEMV streams row chunks (p.chunk_units > 0), else whole rows.  The two are
+// separate instances: with both schedules in one kernel the row-chunk one ran
+// 1.4 us slower per launch on the 4096 x 14336 Q8_0 shape.
+template <int KIND, int F, int NT, int AK = 0, bool CH = false>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool Q81 = fmt_q81(F) || AK == 1;  // per-32 activation scales
@@ -332,6 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     uint64_t* xready = empty + kMaxStages;  // the consumers hold their activations
     uint64_t* xbar = xready + 1;            // the raw activation rows have landed
     int* s_flag = reinterpret_cast<int*>(xbar + 1);  // [1] abort
+
+    // Whole-row rings: the packed activation rows come in by one bulk copy into
+    // the ring's last stage when they fit there (every CTA reads the same few
+    // KB, and word loads from 152 SMs queue on those few L2 lines: ~1.8 us for
+    // one token), and the producer fills that stage only once the consumers
+    // hold their activations (xready).  Row-chunk rings (small stages, about
+    // six of them) measured slower that way: there the activations are read
+    // directly and every stage streams at once.
+    const int xtot = p.xrows * (AK == 1 ? (K >> 5) * 34 : Q81 ? (K >> 5) * 36 : (K >> 8) * 292);
+    const bool xb = !CH && p.stages >= 2 && xtot <= p.stage_stride && xtot % 16 == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.xq) & 15) == 0;
 
     // ---- work items: 16-row tiles
     const int nitems = static_cast<int>((p.N + kTileRows - 1) / kTileRows);
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         }
         __syncwarp();
         start_arrive();
-        if (KIND == KIND_GEMV && p.chunk_units > 0) {
+        if constexpr (KIND == KIND_GEMV && CH) {
             // rows too long for whole-row stages: stage j = (tile, chunk kc); lane i
             // brings row i's chunk.  A row slot holds global byte x at slot + (x -
             // x0), x0 the chunk start rounded down to 16 bytes: the 16-byte-aligned
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
                 const int nr = static_cast<int>(p.N - r0 < kTileRows ? p.N - r0 : kTileRows);
                 for (int kc = 0; kc < nkc; ++kc, ++j) {
                     const int s = j % p.stages;
-                    if (j == kEarlyStages) {  // the rest once the activations are in
+                    if (xb && j == p.stages - 1) {  // the last stage once the activations are in
                         if (lane == 0) ok = mbar_wait(xready, 0u);
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         if (!ok) {
@@ -428,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
             for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
                 const int s = j % p.stages;
                 const uint32_t ph = static_cast<uint32_t>(j / p.stages) & 1u;
-                if (j == kEarlyStages && !mbar_wait(xready, 0u)) {  // the rest once the activations are in
+                if (xb && j == p.stages - 1 && !mbar_wait(xready, 0u)) {  // the last stage once the activations are in
                     set_error(p.err, DEV_ERR_TIMEOUT);
                     break;
                 }
@@ -480,13 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     }
     start_sync();  // barriers initialised, sums zeroed
     pdl_wait();  // activations come from the previous kernel; outputs are written after it finished
-    // The packed activation rows come in by one bulk copy into the last ring
-    // stage, which the producer leaves alone until xready, when they fit there:
-    // every CTA reads the same few KB, and word loads from 152 SMs queue on those
-    // few L2 lines (~1.8 us for one token).  Otherwise they are read directly.
-    const int xtot = p.xrows * (AK == 1 ? (K >> 5) * 34 : Q81 ? (K >> 5) * 36 : (K >> 8) * 292);
-    const bool xb = p.stages > kEarlyStages && xtot <= p.stage_stride && xtot % 16 == 0 &&
-                    (reinterpret_cast<uintptr_t>(p.xq) & 15) == 0;
     const uint8_t* xsrc = p.xq;
     if (xb) {
         uint8_t* const raw = ring + static_cast<size_t>(p.stages - 1) * p.stage_stride;
@@ -516,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
 
     if constexpr (KIND == KIND_GEMV && NT == 1) {
         const int nu = units_per_row(K), nb32 = K >> 5;
-        if (nu <= 64 && p.chunk_units == 0) {
+        if (!CH && nu <= 64) {
             // One token, K <= 4096: lane l owns units l and l + 32 of every row,
             // so its activations stay in registers for the whole kernel.
             XUnit xa, xb;
@@ -551,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     }
 
     if constexpr (KIND == KIND_GEMV) {
-        if (p.chunk_units > 0) {
+        if constexpr (CH) {
             // chunked rows: the warp's row sums its chunks in acc[] and is reduced once per tile
             const int nu = units_per_row(K);
             const int nkc = (nu + p.chunk_units - 1) / p.chunk_units;
@@ -630,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
     }
 }
 
-template <int KIND, int F, int NT, int AK = 0>
+template <int KIND, int F, int NT, int AK = 0, bool CH = false>
 cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s) {
     // The dynamic shared-memory limit is a per-device function attribute: set it
     // on the first launch of each instantiation on each device (before capture).
@@ -640,21 +647,29 @@ cudaError_t launch_one(const StreamParams& p, int grid, int smem, cudaStream_t s
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(k_stream<KIND, F, NT, AK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        e = cudaFuncSetAttribute(k_stream<KIND, F, NT, AK, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    return launch_pdl(k_stream<KIND, F, NT, AK>, dim3(grid), dim3(kThreads), smem, s, p);
+    return launch_pdl(k_stream<KIND, F, NT, AK, CH>, dim3(grid), dim3(kThreads), smem, s, p);
 }
 
+template <int KIND, int F, int AK, bool CH>
+cudaError_t launch_nt_ch(int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
+    switch (nt) {
+    case 1: return launch_one<KIND, F, 1, AK, CH>(p, grid, smem, s);
+    case 2: return launch_one<KIND, F, 2, AK, CH>(p, grid, smem, s);
+    case 4: return launch_one<KIND, F, 4, AK, CH>(p, grid, smem, s);
+    default: return launch_one<KIND, F, 8, AK, CH>(p, grid, smem, s);
+    }
+}
+
+// The GEMV instance for nt tokens and the plan's schedule (row chunks or whole rows).
 template <int KIND, int F, int AK = 0>
 cudaError_t launch_nt(int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
-    switch (nt) {
-    case 1: return launch_one<KIND, F, 1, AK>(p, grid, smem, s);
-    case 2: return launch_one<KIND, F, 2, AK>(p, grid, smem, s);
-    case 4: return launch_one<KIND, F, 4, AK>(p, grid, smem, s);
-    default: return launch_one<KIND, F, 8, AK>(p, grid, smem, s);
-    }
+    if constexpr (KIND == KIND_GEMV)
+        if (p.chunk_units > 0) return launch_nt_ch<KIND, F, AK, true>(nt, p, grid, smem, s);
+    return launch_nt_ch<KIND, F, AK, false>(nt, p, grid, smem, s);
 }
 
 }  // namespace ggq
