@@ -823,10 +823,14 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         StreamShape sh;
         int G = 1;
         if (fused) {
-            for (int g = 8; g >= 1; --g) {
+            // one token: its top_k experts are known to be distinct, so G = top_k
+            // takes every expert's tile in one stage (one item per CTA: two
+            // stages are enough, the second one free for h)
+            const int gmax = T == 1 && top_k <= 8 ? top_k : 8;
+            for (int g = gmax; g >= 1; --g) {
                 if (g * (I / 64) > 256) continue;
                 if (plan_stream(g * kTileRows * p.rowbytes, P, p.K, false, &sh, direct_fixed) &&
-                    (sh.stages >= 3 || g == 1)) {
+                    (sh.stages >= 3 || g == 1 || (T == 1 && g == top_k && sh.stages >= 2))) {
                     G = g;
                     break;
                 }

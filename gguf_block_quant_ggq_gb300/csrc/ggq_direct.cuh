@@ -24,6 +24,7 @@
 // streaming kernel and use its dp4a consumer (row_accumulate).
 #pragma once
 #include <atomic>
+#include <type_traits>
 #include "ggq_stream.cuh"
 
 namespace ggq {
@@ -41,6 +42,13 @@ struct DirectPlan {
     int bad;                                      // a routed id was out of range
     int tok[kDirectMaxPairs];                     // token of pair p (p / top_k)
 };
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // Group the P <= 32 pairs (expert ids in s->ids) by distinct expert, in order
 // of first appearance.  One warp.
@@ -136,7 +144,6 @@ __device__ __forceinline__ void direct_route_token_reg(const float* __restrict__
         v[i] = lane + 32 * i < E ? __ldcg(l + lane + 32 * i) : 0.0f;
         key[i] = lane + 32 * i < E ? route_key(v[i]) : 0u;
     }
-    float lmax = 0.0f, wsum = 0.0f, myw = 0.0f;
     int myid = 0;
     for (int j = 0; j < k; ++j) {
         unsigned km = 0u;
@@ -145,28 +152,29 @@ __device__ __forceinline__ void direct_route_token_reg(const float* __restrict__
         km = __reduce_max_sync(0xffffffffu, km);
         unsigned im = 0xffffffffu;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (key[i] == km && im == 0xffffffffu) im = static_cast<unsigned>(lane + 32 * i);  // lowest of this lane
+        for (int i = 7; i >= 0; --i)
+            if (key[i] == km) im = static_cast<unsigned>(lane + 32 * i);  // lowest of this lane
         const int bi = static_cast<int>(__reduce_min_sync(0xffffffffu, im));
-        float bv = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            if (lane + 32 * i == bi) {
-                bv = v[i];
-                key[i] = 0u;
-            }
-        bv = __shfl_sync(0xffffffffu, bv, bi & 31);
-        if (j == 0) lmax = bv;
-        const float p = expf(bv - lmax);
-        wsum += p;
-        if (lane == j) {
-            myid = bi;
-            myw = p;
-        }
+            if (lane + 32 * i == bi) key[i] = 0u;
+        if (lane == j) myid = bi;
     }
+    // the softmax over the selected logits, after the rounds (lane j: the j-th
+    // selected; the sum taken in selection order)
+    float bv = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float t = __shfl_sync(0xffffffffu, v[i], myid & 31);
+        if ((myid >> 5) == i) bv = t;
+    }
+    const float lmax = __shfl_sync(0xffffffffu, bv, 0);
+    const float pj = expf(bv - lmax);
+    float wsum = 0.0f;
+    for (int j = 0; j < k; ++j) wsum += __shfl_sync(0xffffffffu, pj, j);
     if (lane < k) {
         ids[lane] = myid;
-        w[lane] = myw / wsum;
+        w[lane] = pj / wsum;
     }
 }
 
@@ -272,18 +280,60 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     const XRegion xr_ = x_region(xreg, xrows, K, false);
     uint64_t* full = reinterpret_cast<uint64_t*>(xreg + p.x_bytes);
     uint64_t* empty = full + kMaxStages;
-    DirectPlan* plan = reinterpret_cast<DirectPlan*>(empty + kMaxStages);
+    uint64_t* hbar = empty + kMaxStages;  // down: the fp32 h rows have landed (spare stage)
+    DirectPlan* plan = reinterpret_cast<DirectPlan*>(hbar + 2);
 
-    // ---- routing and grouping (every CTA), activation quantization
-    if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+    // ---- barriers (producer warp), routing (warps < T) and, in the gate/up
+    // kernel, the activations (the other consumer warps), side by side.  Named
+    // barriers: 3 = every thread (barriers initialised, plan, activations:
+    // the consumers wait on it), 4 = warp 0 and the producer warp (the plan:
+    // the producer's copies start as soon as it is known), 5 = the routing warps.
+    // gate/up: the activations of the T tokens, by consumer warps w0 .. 15
+    const auto stage_x = [&](int w0) {
+        if (warp >= w0 && warp < kConsumerWarps) {
+            const int sw = warp - w0, nsw = kConsumerWarps - w0;
+            // x^ given (the "Q8 prequant" entry): staged as it is
+            if (p.xq_in) stage_acts<false, F == F_MXFP4>(p.xq_in, xrows, K, xr_, tid - 32 * w0, 32 * nsw);
+            // else quantize x (every CTA; a few blocks per warp, their loads issued together)
+            const int nbr = K >> 8, nb = p.xq_in ? 0 : xrows * nbr;
+            for (int b0 = sw; b0 < nb; b0 += 4 * nsw) {
+                float4 va[4], vb[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int b = b0 + h * nsw;
+                    if (b < nb) {
+                        const float4* src = reinterpret_cast<const float4*>(p.X + static_cast<int64_t>(b) * 256);
+                        va[h] = __ldcg(src + 2 * lane);
+                        vb[h] = __ldcg(src + 2 * lane + 1);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int b = b0 + h * nsw;
+                    if (b < nb) {
+                        const int r = b / nbr, c = b - r * nbr;
+                        uint8_t* pk = (blockIdx.x == 0 && p.xq_dump) ? p.xq_dump + static_cast<int64_t>(b) * 292 : nullptr;
+                        warp_quant_to_smem<F == F_MXFP4>(va[h], vb[h], r, c, K, xr_, pk, lane);
+                    }
+                }
+            }
         }
-        fence_barrier_init();
-    }
-    // both kernels route from the same inputs with the same arithmetic
-    if (warp < p.T) {
+    };
+    const bool single = p.T == 1 && p.logits != nullptr;
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            for (int s = 0; s < p.stages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kConsumerWarps);
+            }
+            mbar_init(hbar, 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        named_arrive(3, kThreads);
+        named_sync(4, 64);
+    } else if (warp < p.T) {
+        // both kernels route from the same inputs with the same arithmetic
         if (p.logits) {
             if (p.E <= 256)
                 direct_route_token_reg(p.logits + static_cast<int64_t>(warp) * p.E, p.E, p.top_k,
@@ -295,11 +345,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
             plan->ids[warp * p.top_k + lane] = __ldcg(p.ids_in + warp * p.top_k + lane);
             plan->wt[warp * p.top_k + lane] = __ldcg(p.w_in + warp * p.top_k + lane);
         }
+        if (tid < P) plan->tok[tid] = tid / p.top_k;
+        if (single) {
+            // one token: its k experts are distinct (routing picks each once), so
+            // the routing warp lays out the plan itself -- pair j on expert slot j
+            // (routed ids given by the caller are grouped like several tokens')
+            __syncwarp();
+            const int e = lane < P ? plan->ids[lane] : 0;
+            const unsigned anybad = __ballot_sync(0xffffffffu, e < 0 || e >= p.E);
+            if (lane < P) {
+                plan->expert[lane] = e;
+                plan->npairs[lane] = 1;
+                plan->pair[lane][0] = lane;
+            }
+            if (lane == 0) {
+                plan->D = anybad ? 0 : P;
+                plan->bad = anybad != 0u;
+            }
+        } else {
+            named_sync(5, 32 * p.T);
+            if (warp == 0) direct_group(plan, P, p.E, lane);
+        }
+        if (warp == 0) named_arrive(4, 64);
+        named_sync(3, kThreads);
+    } else {
+        if constexpr (KIND == KIND_GATEUP) stage_x(p.T);
+        named_sync(3, kThreads);
     }
-    if (tid < P) plan->tok[tid] = tid / p.top_k;
-    __syncthreads();
-    if (warp == 0) direct_group(plan, P, p.E, lane);
-    __syncthreads();
     const int D = plan->D;
     if (KIND == KIND_GATEUP && blockIdx.x == 0 && tid < P) {
         p.ids[tid] = plan->ids[tid];
@@ -314,88 +386,77 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     const int tiles = static_cast<int>(p.N / kTileRows);
     const int nitems = KIND == KIND_GATEUP ? D * tiles : (D > 0 ? tiles : 0);
     if (static_cast<int>(blockIdx.x) >= nitems) return;
+    // stages per item: the gate and up tiles of one expert; G experts' tiles (fused
+    // down); one expert's tile (down with per-pair outputs)
+    const int per_item = KIND == KIND_GATEUP ? 1 : KIND == KIND_DOWNF ? (D + p.G - 1) / p.G : D;
 
     if (warp == kConsumerWarps) {
-        // ================= producer: one stage per (expert, tile) pair
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            if (DOWN && !p.early_weights) pdl_wait();  // the weights may come from earlier kernels
-            int j = 0, s = 0;
-            uint32_t ph = 0u;  // ring slot and phase of stage j
-            for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-                if constexpr (KIND == KIND_DOWNF) {
-                    // one stage per group of G experts: the item's tile of each
-                    for (int ug = 0; ug < D; ug += p.G, ++j, s = s + 1 == p.stages ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
-                        if (!mbar_wait(&empty[s], ph ^ 1u)) {
-                            set_error(p.err, DEV_ERR_TIMEOUT);
-                            goto drain;
-                        }
-                        const int gc = D - ug < p.G ? D - ug : p.G;
-                        const uint32_t bytes = static_cast<uint32_t>(kTileRows * p.rowbytes);  // multiple of 16
-                        uint8_t* dst = ring + static_cast<size_t>(s) * p.stage_stride;
-                        mbar_arrive_expect_tx(&full[s], gc * bytes);
-                        for (int g = 0; g < gc; ++g) {
-                            const int64_t e = plan->expert[ug + g];
-                            const int64_t off = (e * p.N + static_cast<int64_t>(item) * kTileRows) * p.rowbytes;
-                            bulk_g2s(dst + static_cast<size_t>(g) * bytes, p.W + off, bytes, &full[s], pol);
-                        }
-                    }
-                    continue;
+        // ================= producer: lane 0 waits for the slot and posts its bytes,
+        // then one lane per tile copy (copies of different experts' tiles are
+        // issued side by side)
+        const uint64_t pol = policy_evict_first();
+        if (DOWN && !p.early_weights) pdl_wait();  // the weights may come from earlier kernels
+        const uint32_t bytes = static_cast<uint32_t>(kTileRows * p.rowbytes);  // multiple of 16
+        int j = 0, s = 0;
+        uint32_t ph = 0u;  // ring slot and phase of stage j
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
+            for (int q = 0; q < per_item; ++q) {
+                if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) set_error(p.err, DEV_ERR_TIMEOUT);
+                    break;
                 }
-                const int ne = KIND == KIND_GATEUP ? 1 : D;
-                for (int q = 0; q < ne; ++q, ++j, s = s + 1 == p.stages ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
-                    const int u = KIND == KIND_GATEUP ? item / tiles : q;
+                const int ncp = KIND == KIND_GATEUP ? 2 : KIND == KIND_DOWNF ? (D - q * p.G < p.G ? D - q * p.G : p.G) : 1;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ncp) * bytes);
+                __syncwarp();
+                if (lane < ncp) {
+                    const int u = KIND == KIND_GATEUP ? item / tiles : KIND == KIND_DOWNF ? q * p.G + lane : q;
                     const int tile = KIND == KIND_GATEUP ? item - u * tiles : item;
-                    if (!mbar_wait(&empty[s], ph ^ 1u)) {
-                        set_error(p.err, DEV_ERR_TIMEOUT);
-                        goto drain;
-                    }
                     const int64_t e = plan->expert[u];
                     const int64_t off = (e * p.N + static_cast<int64_t>(tile) * kTileRows) * p.rowbytes;
-                    const uint32_t bytes = static_cast<uint32_t>(kTileRows * p.rowbytes);  // multiple of 16
-                    uint8_t* dst = ring + static_cast<size_t>(s) * p.stage_stride;
-                    mbar_arrive_expect_tx(&full[s], KIND == KIND_GATEUP ? 2 * bytes : bytes);
-                    bulk_g2s(dst, p.W + off, bytes, &full[s], pol);
-                    if (KIND == KIND_GATEUP) bulk_g2s(dst + bytes, p.W2 + off, bytes, &full[s], pol);
+                    const uint8_t* src = (KIND == KIND_GATEUP && lane == 1 ? p.W2 : p.W) + off;
+                    bulk_g2s(ring + static_cast<size_t>(s) * p.stage_stride + static_cast<size_t>(lane) * bytes, src,
+                             bytes, &full[s], pol);
+                }
+                ++j;
+                if (++s == p.stages) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-        drain:
+        }
+        // the copies still in flight land before the CTA exits
+        if (lane == 0)
             for (int q = (j > p.stages ? j - p.stages : 0); q < j; ++q)
                 if (!mbar_wait(&full[q % p.stages], static_cast<uint32_t>(q / p.stages) & 1u)) break;
-        }
         return;
     }
 
-    // ================= consumers: the activations into shared memory
-    if constexpr (KIND == KIND_GATEUP) {
-        // x^ given (the "Q8 prequant" entry): staged as it is
-        if (p.xq_in) stage_acts<false, F == F_MXFP4>(p.xq_in, xrows, K, xr_, tid, kConsumerWarps * 32);
-        // else quantize x (every CTA; a few blocks per warp, their loads issued together)
-        const int nbr = K >> 8, nb = p.xq_in ? 0 : xrows * nbr;
-        for (int b0 = warp; b0 < nb; b0 += 4 * kConsumerWarps) {
-            float4 va[4], vb[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int b = b0 + h * kConsumerWarps;
-                if (b < nb) {
-                    const float4* src = reinterpret_cast<const float4*>(p.X + static_cast<int64_t>(b) * 256);
-                    va[h] = __ldcg(src + 2 * lane);
-                    vb[h] = __ldcg(src + 2 * lane + 1);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int b = b0 + h * kConsumerWarps;
-                if (b < nb) {
-                    const int r = b / nbr, c = b - r * nbr;
-                    uint8_t* pk = (blockIdx.x == 0 && p.xq_dump) ? p.xq_dump + static_cast<int64_t>(b) * 292 : nullptr;
-                    warp_quant_to_smem<F == F_MXFP4>(va[h], vb[h], r, c, K, xr_, pk, lane);
-                }
-            }
-        }
-    } else {
-        // quantize h (every CTA: all pairs, K/256 blocks each; loads of four blocks in flight)
+    // ================= consumers (down): h^ into shared memory
+    if constexpr (DOWN) {
         pdl_wait();  // h comes from the gate/up kernel
+        // With a ring stage to spare (this CTA's items take fewer stages than the
+        // ring holds), the fp32 h rows come in by one bulk copy into the ring's
+        // last stage: every CTA reads all of h, and word loads from every SM
+        // queue on the same L2 lines.  Otherwise they are read directly.
+        const int my_items = (nitems - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                             static_cast<int>(gridDim.x);
+        const int hbytes = P * K * 4;
+        const bool hb = my_items * per_item < p.stages && hbytes <= p.stage_stride && hbytes % 16 == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.h) & 15) == 0;
+        const float* hsrc = p.h;
+        if (hb) {
+            uint8_t* const raw = ring + static_cast<size_t>(p.stages - 1) * p.stage_stride;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(hbar, static_cast<uint32_t>(hbytes));
+                bulk_g2s(raw, p.h, static_cast<uint32_t>(hbytes), hbar, policy_evict_last());
+            }
+            if (!mbar_wait(hbar, 0u)) set_error(p.err, DEV_ERR_TIMEOUT);
+            hsrc = reinterpret_cast<const float*>(raw);
+        }
+        // quantize h (every CTA: all pairs, K/256 blocks each; loads of four blocks in flight)
         const int nbr = K >> 8, nb = xrows * nbr;
         for (int b0 = warp; b0 < nb; b0 += 4 * kConsumerWarps) {
             float4 va[4], vb[4];
@@ -403,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
             for (int h = 0; h < 4; ++h) {
                 const int b = b0 + h * kConsumerWarps;
                 if (b < nb) {
-                    const float4* src = reinterpret_cast<const float4*>(p.h + static_cast<int64_t>(b) * 256);
-                    va[h] = __ldcg(src + 2 * lane);
-                    vb[h] = __ldcg(src + 2 * lane + 1);
+                    const float4* src = reinterpret_cast<const float4*>(hsrc + static_cast<int64_t>(b) * 256);
+                    va[h] = hb ? src[2 * lane] : __ldcg(src + 2 * lane);
+                    vb[h] = hb ? src[2 * lane + 1] : __ldcg(src + 2 * lane + 1);
                 }
             }
 #pragma unroll
@@ -418,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                 }
             }
         }
+        consumer_sync();
     }
-    consumer_sync();
     XS xs;
     xs.q = smem_addr(xr_.q);
     xs.d = smem_addr(xr_.d);
@@ -434,164 +495,198 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     const int nb32 = K >> 5;
     int vg[kDownUnits], vu[kDownUnits];
     if constexpr (KIND == KIND_DOWNF) {
-        const int nu = units_per_row(K);
+        // v = lane + 32 i = g nu + u, walked without a division per slot
+        const int nu = units_per_row(K), q32 = 32 / nu, r32 = 32 - q32 * nu;
+        int g = lane / nu, u = lane - g * nu;
 #pragma unroll
         for (int i = 0; i < kDownUnits; ++i) {
-            const int v = lane + 32 * i;
-            vg[i] = v < p.G * nu ? v / nu : kDirectMaxPairs;
-            vu[i] = v < p.G * nu ? v - vg[i] * nu : 0;
+            const bool in = lane + 32 * i < p.G * nu;
+            vg[i] = in ? g : kDirectMaxPairs;
+            vu[i] = in ? u : 0;
+            g += q32;
+            u += r32;
+            if (u >= nu) {
+                u -= nu;
+                ++g;
+            }
         }
     }
-    int s = 0;
-    uint32_t ph = 0u;  // ring slot and phase of the next stage
-    const auto next_stage = [&]() {
-        if (++s == p.stages) {
-            s = 0;
-            ph ^= 1u;
+    // The item loop, in two compiled copies for the gate/up kernel at one token:
+    // with rows of at most 32 units, lane l owns unit l of every row and holds
+    // its activations in registers (the dumping instance too, so that g and u
+    // do not depend on what is dumped); else the generic dot, without those
+    // registers held.
+    const auto run = [&](auto rx_tag) {
+        constexpr bool RX = decltype(rx_tag)::value;
+        XUnit xa;
+        bool va = false;
+        if constexpr (RX) {
+            va = lane < units_per_row(K);
+            if (va) load_xunit<F>(xs, lane, xa);
         }
-    };
-    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-        if constexpr (KIND == KIND_GATEUP) {
-            const int u = item / tiles, tile = item - u * tiles;
-            const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
-            const int np = plan->npairs[u];
-            int xr[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->tok[plan->pair[u][t]] : 0;
-            const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
-            const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
-            if (ready) {
-                float acc[2 * NT];
-#pragma unroll
-                for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
-                row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
-                row_accumulate<F, NT>(stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes), xs, xr, np,
-                                      acc + NT, lane);
-                const float v = warp_transpose_reduce<LV + 1>(acc, lane);  // index = gate/up * NT + slot
-                const float uval = __shfl_down_sync(0xffffffffu, v, NT << SH);
-                const int idx = lane >> SH;
-                if ((lane & ((1 << SH) - 1)) == 0 && idx < NT && idx < np) {
-                    const float hval = __fmul_rn(__fdiv_rn(v, 1.0f + expf(-v)), uval);
-                    const int64_t o = static_cast<int64_t>(plan->pair[u][idx]) * p.N + row;
-                    p.h[o] = hval;
-                    if (p.g_dump) p.g_dump[o] = v;
-                    if (p.u_dump) p.u_dump[o] = uval;
-                }
-                if constexpr (DUMP) {  // integer core of the gate and up rows for every pair on this expert
-                    for (int j = 0; j < np; ++j) {
-                        const int pr = plan->pair[u][j], tk = plan->tok[pr];
-                        const int64_t o = (static_cast<int64_t>(pr) * p.N + row) * p.ncoef;
-                        row_coefs_one<F>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, tk, p.coefs[0] + o, lane);
-                        row_coefs_one<F>(stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes), xs, tk,
-                                         p.coefs[1] + o, lane);
-                    }
-                }
-            } else {
-                set_error(p.err, DEV_ERR_TIMEOUT);
+        int s = 0;
+        uint32_t ph = 0u;  // ring slot and phase of the next stage
+        const auto next_stage = [&]() {
+            if (++s == p.stages) {
+                s = 0;
+                ph ^= 1u;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            next_stage();
-            if (!ready) break;
-        } else if constexpr (KIND == KIND_DOWN) {
-            const int tile = item;
-            const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
-            // y for the T tokens of this row, accumulated over the experts in plan order
-            float yacc = 0.0f;  // lane t (t < T) holds y[t][row] after each reduction
-            bool ok = true;
-            for (int u = 0; u < D; ++u) {
+        };
+        for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+            if constexpr (KIND == KIND_GATEUP) {
+                const int u = item / tiles, tile = item - u * tiles;
                 const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
                 const int np = plan->npairs[u];
                 int xr[NT];
-#pragma unroll
-                for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->pair[u][t] : 0;
-                if (ready && ok) {
-                    const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
-                    float acc[NT];
-#pragma unroll
-                    for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
-                    row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
-                    const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = slot
-                    const int slot = lane >> SH;
-                    const int pp = slot < np ? xr[slot] : -1;
-                    if constexpr (DUMP) {  // integer core of this down row for every pair on the expert
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->tok[plan->pair[u][t]] : 0;
+                const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+                const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
+                if (ready) {
+                    float acc[2 * NT];
+    #pragma unroll
+                    for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
+                    const saddr grow = stage + static_cast<uint32_t>(warp * p.rowbytes);
+                    const saddr urow = stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes);
+                    if constexpr (RX) {
+                        acc[0] = va ? unit_dot_rx<F>(grow, lane, nb32, xa) : 0.0f;
+                        acc[1] = va ? unit_dot_rx<F>(urow, lane, nb32, xa) : 0.0f;
+                    } else {
+                        row_accumulate<F, NT>(grow, xs, xr, np, acc, lane);
+                        row_accumulate<F, NT>(urow, xs, xr, np, acc + NT, lane);
+                    }
+                    const float v = warp_transpose_reduce<LV + 1>(acc, lane);  // index = gate/up * NT + slot
+                    const float uval = __shfl_down_sync(0xffffffffu, v, NT << SH);
+                    const int idx = lane >> SH;
+                    if ((lane & ((1 << SH) - 1)) == 0 && idx < NT && idx < np) {
+                        const float hval = __fmul_rn(__fdiv_rn(v, 1.0f + expf(-v)), uval);
+                        const int64_t o = static_cast<int64_t>(plan->pair[u][idx]) * p.N + row;
+                        p.h[o] = hval;
+                        if (p.g_dump) p.g_dump[o] = v;
+                        if (p.u_dump) p.u_dump[o] = uval;
+                    }
+                    if constexpr (DUMP) {  // integer core of the gate and up rows for every pair on this expert
                         for (int j = 0; j < np; ++j) {
-                            const int pr = plan->pair[u][j];
-                            row_coefs_one<F>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, pr,
-                                             p.coefs[0] + (static_cast<int64_t>(pr) * p.N + row) * p.ncoef, lane);
+                            const int pr = plan->pair[u][j], tk = plan->tok[pr];
+                            const int64_t o = (static_cast<int64_t>(pr) * p.N + row) * p.ncoef;
+                            row_coefs_one<F>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, tk, p.coefs[0] + o, lane);
+                            row_coefs_one<F>(stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes), xs, tk,
+                                             p.coefs[1] + o, lane);
                         }
                     }
-                    if (pp >= 0 && (lane & ((1 << SH) - 1)) == 0 && p.o_dump) p.o_dump[static_cast<int64_t>(pp) * p.N + row] = v;
-                    // move each slot's weighted value to the lane of its token
-                    const float contrib = pp >= 0 ? plan->wt[pp] * v : 0.0f;
-                    const int tok = pp >= 0 ? plan->tok[pp] : -1;
-#pragma unroll
-                    for (int q = 0; q < NT; ++q) {
-                        const float cq = __shfl_sync(0xffffffffu, contrib, q << SH);
-                        const int tq = __shfl_sync(0xffffffffu, tok, q << SH);
-                        if (q < np && lane == tq) yacc += cq;
-                    }
-                } else if (!ready) {
+                } else {
                     set_error(p.err, DEV_ERR_TIMEOUT);
-                    ok = false;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 next_stage();
-            }
-            if (ok && lane < p.T) p.Y[static_cast<int64_t>(lane) * p.N + row] = yacc;
-            if (!ok) break;
-        } else {
-            // fused down: y[t][row] = sum over experts and their pairs of w * (W_e row . h^_pair),
-            // each lane adding the weighted partials of its units into its token sums
-            const int64_t row = static_cast<int64_t>(item) * kTileRows + warp;
-            float acc[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-            bool ok = true;
-            for (int ug = 0; ug < D; ug += p.G) {
-                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
-                if (ready && ok) {
-                    const int gc = D - ug < p.G ? D - ug : p.G;
-                    const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
-#pragma unroll
-                    for (int i = 0; i < kDownUnits; ++i) {
-                        if (vg[i] < gc) {
-                            const int g = vg[i], ur = vu[i], u = ug + g;
-                            const int np = plan->npairs[u];
-                            const saddr rowp = stage + static_cast<uint32_t>((g * kTileRows + warp) * p.rowbytes);
-                            Unit un;
-                            load_unit<F>(rowp, ur, nb32, un);
-                            int xo[4];
-                            unit_offsets<F>(ur, xo);
-#pragma unroll
-                            for (int jj = 0; jj < NT; ++jj) {
-                                if (jj < np) {
-                                    const int pr = plan->pair[u][jj];
-                                    int A0, A1;
-                                    unit_ints<F>(un, xo, xs, pr, ur, A0, A1);
-                                    const float val = plan->wt[pr] * unit_value<F>(un, xs, pr, ur, A0, A1);
-                                    const int tk = plan->tok[pr];
-#pragma unroll
-                                    for (int t = 0; t < NT; ++t)
-                                        if (t == tk) acc[t] += val;
+                if (!ready) break;
+            } else if constexpr (KIND == KIND_DOWN) {
+                const int tile = item;
+                const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
+                // y for the T tokens of this row, accumulated over the experts in plan order
+                float yacc = 0.0f;  // lane t (t < T) holds y[t][row] after each reduction
+                bool ok = true;
+                for (int u = 0; u < D; ++u) {
+                    const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
+                    const int np = plan->npairs[u];
+                    int xr[NT];
+    #pragma unroll
+                    for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->pair[u][t] : 0;
+                    if (ready && ok) {
+                        const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+                        float acc[NT];
+    #pragma unroll
+                        for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
+                        row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
+                        const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = slot
+                        const int slot = lane >> SH;
+                        const int pp = slot < np ? xr[slot] : -1;
+                        if constexpr (DUMP) {  // integer core of this down row for every pair on the expert
+                            for (int j = 0; j < np; ++j) {
+                                const int pr = plan->pair[u][j];
+                                row_coefs_one<F>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, pr,
+                                                 p.coefs[0] + (static_cast<int64_t>(pr) * p.N + row) * p.ncoef, lane);
+                            }
+                        }
+                        if (pp >= 0 && (lane & ((1 << SH) - 1)) == 0 && p.o_dump) p.o_dump[static_cast<int64_t>(pp) * p.N + row] = v;
+                        // move each slot's weighted value to the lane of its token
+                        const float contrib = pp >= 0 ? plan->wt[pp] * v : 0.0f;
+                        const int tok = pp >= 0 ? plan->tok[pp] : -1;
+    #pragma unroll
+                        for (int q = 0; q < NT; ++q) {
+                            const float cq = __shfl_sync(0xffffffffu, contrib, q << SH);
+                            const int tq = __shfl_sync(0xffffffffu, tok, q << SH);
+                            if (q < np && lane == tq) yacc += cq;
+                        }
+                    } else if (!ready) {
+                        set_error(p.err, DEV_ERR_TIMEOUT);
+                        ok = false;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    next_stage();
+                }
+                if (ok && lane < p.T) p.Y[static_cast<int64_t>(lane) * p.N + row] = yacc;
+                if (!ok) break;
+            } else {
+                // fused down: y[t][row] = sum over experts and their pairs of w * (W_e row . h^_pair),
+                // each lane adding the weighted partials of its units into its token sums
+                const int64_t row = static_cast<int64_t>(item) * kTileRows + warp;
+                float acc[NT];
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+                bool ok = true;
+                for (int ug = 0; ug < D; ug += p.G) {
+                    const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
+                    if (ready && ok) {
+                        const int gc = D - ug < p.G ? D - ug : p.G;
+                        const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+    #pragma unroll
+                        for (int i = 0; i < kDownUnits; ++i) {
+                            if (vg[i] < gc) {
+                                const int g = vg[i], ur = vu[i], u = ug + g;
+                                const int np = plan->npairs[u];
+                                const saddr rowp = stage + static_cast<uint32_t>((g * kTileRows + warp) * p.rowbytes);
+                                Unit un;
+                                load_unit<F>(rowp, ur, nb32, un);
+                                int xo[4];
+                                unit_offsets<F>(ur, xo);
+    #pragma unroll
+                                for (int jj = 0; jj < NT; ++jj) {
+                                    if (jj < np) {
+                                        const int pr = plan->pair[u][jj];
+                                        int A0, A1;
+                                        unit_ints<F>(un, xo, xs, pr, ur, A0, A1);
+                                        const float val = plan->wt[pr] * unit_value<F>(un, xs, pr, ur, A0, A1);
+                                        const int tk = plan->tok[pr];
+    #pragma unroll
+                                        for (int t = 0; t < NT; ++t)
+                                            if (t == tk) acc[t] += val;
+                                    }
                                 }
                             }
                         }
+                    } else if (!ready) {
+                        set_error(p.err, DEV_ERR_TIMEOUT);
+                        ok = false;
                     }
-                } else if (!ready) {
-                    set_error(p.err, DEV_ERR_TIMEOUT);
-                    ok = false;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    next_stage();
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                next_stage();
+                const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = token
+                const int t = lane >> SH;
+                if (ok && (lane & ((1 << SH) - 1)) == 0 && t < p.T) p.Y[static_cast<int64_t>(t) * p.N + row] = v;
+                if (!ok) break;
             }
-            const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = token
-            const int t = lane >> SH;
-            if (ok && (lane & ((1 << SH) - 1)) == 0 && t < p.T) p.Y[static_cast<int64_t>(t) * p.N + row] = v;
-            if (!ok) break;
         }
+    };
+    if constexpr (KIND == KIND_GATEUP && NT == 1) {
+        if (units_per_row(K) <= 32) run(std::true_type{});
+        else run(std::false_type{});
+    } else {
+        run(std::false_type{});
     }
 }
 
