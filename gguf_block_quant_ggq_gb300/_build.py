@@ -117,7 +117,7 @@ if __name__ == "__main__":
             f.write("# Registers, stack and spills of every kernel instance (nvcc -Xptxas -v, sm_103a)\n\n"
                     "Command:\n\n    python -m gguf_block_quant_ggq_gb300._build --ptxas-summary "
                     f"{os.path.relpath(sys.argv[2], ROOT)}\n\n"
-                    "Template arguments: k_stream<kind, format, tokens, activation kind>, "
+                    "Template arguments: k_stream<kind, format, tokens, activation kind, row chunks>, "
                     "k_gemv_mma<format, dump, chunk width>, k_group<kind, format, dump>, "
                     "k_gmm<kind, format, dump>, k_gmmtc<format, dump>, k_direct<kind, format, "
                     "tokens, dump>; formats 0 Q4_0, 1 Q8_0, 2 Q4_K, 3 Q5_K, 4 Q6_K, 5 MXFP4.\n\n")
