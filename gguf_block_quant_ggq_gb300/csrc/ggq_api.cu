@@ -326,15 +326,18 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
     return true;
 }
 
-// Smallest token count that the decode GEMV sends to the tensor path.
-constexpr int kMmaMinTokens = 2;
+// Smallest token count that the decode GEMV sends to the tensor path: from two
+// tokens, except Q8_0 and Q5_K, whose two-token GEMV runs faster on the dp4a
+// streaming kernel (14336 x 4096 rows at two tokens: Q8_0 12.0 against 12.5 us,
+// Q5_K 12.4 against 12.7 us; Q4_K 10.6 against 10.0, Q6_K 16.9 against 14.1).
+int mma_min_tokens(int f) { return f == F_Q8_0 || f == F_Q5_K ? 3 : 2; }
 
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st, bool a80 = false) {
     const int f = fmt_of(w);
     const bool dump = kind == KIND_DUMP;
     const int ncoef = static_cast<int>(K / fmt_qk(f) * fmt_coefs(f));
-    if (!a80 && T >= kMmaMinTokens && f != F_Q4_0 && aligned16(Xq)) {
+    if (!a80 && T >= mma_min_tokens(f) && f != F_Q4_0 && aligned16(Xq)) {
         MmavParams m{};
         m.W = static_cast<const uint8_t*>(W);
         m.rowbytes = w_row_bytes(f, K);
