@@ -16,6 +16,10 @@ path:
     sub-scales uniform in [-32, 31] (reading of "6-bit sub-scales uniform").
   * MXFP4: E8M0 exponent byte uniform in 117..123 (scale 2^-10 .. 2^-4),
     E2M1 nibbles uniform over the 16 codes.
+  * Q2_K: fp16 d, dmin ~ U[1e-4, 1e-2]; scale/min bytes, 2-bit quants uniform
+    bytes (every 4-bit scale and min uniform in 0..15).
+  * Q3_K: fp16 d ~ U[1e-4, 1e-2]; high-bit mask, 2-bit quants and the 12
+    packed scale bytes uniform bytes (every 6-bit scale uniform in 0..63).
   * Activations and router logits ~ N(0, 1) fp32; the prefill workload adds a
     Zipf(1.1) expert bias -1.1*ln(rank) over a seeded permutation of ranks.
 """
@@ -23,9 +27,11 @@ from __future__ import annotations
 
 import numpy as np
 
-BLOCK_ELEMS = {"Q4_0": 32, "Q8_0": 32, "MXFP4": 32, "Q8_1": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256, "Q8_K": 256}
-BLOCK_BYTES = {"Q4_0": 18, "Q8_0": 34, "MXFP4": 17, "Q8_1": 36, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210, "Q8_K": 292}
-WEIGHT_FORMATS = ("Q4_0", "Q8_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4")
+BLOCK_ELEMS = {"Q4_0": 32, "Q8_0": 32, "MXFP4": 32, "Q8_1": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256, "Q8_K": 256,
+               "Q2_K": 256, "Q3_K": 256}
+BLOCK_BYTES = {"Q4_0": 18, "Q8_0": 34, "MXFP4": 17, "Q8_1": 36, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210, "Q8_K": 292,
+               "Q2_K": 84, "Q3_K": 110}
+WEIGHT_FORMATS = ("Q4_0", "Q8_0", "Q4_K", "Q5_K", "Q6_K", "MXFP4", "Q2_K", "Q3_K")
 
 BASE_SEED = 0x6767
 
@@ -68,6 +74,13 @@ def weights(fmt: str, rows: int, K: int, g: np.random.Generator, d_range=None) -
         out[:, 0:192] = g.integers(0, 256, (nb, 192), dtype=np.uint8)
         out[:, 192:208] = g.integers(-32, 32, (nb, 16), dtype=np.int8).view(np.uint8)
         out[:, 208:210] = _f16_bytes(g.uniform(lo, hi, nb).astype(np.float32))
+    elif fmt == "Q2_K":  # scales[16], qs[64], d, dmin
+        out[:, 0:80] = g.integers(0, 256, (nb, 80), dtype=np.uint8)
+        out[:, 80:82] = _f16_bytes(g.uniform(lo, hi, nb).astype(np.float32))
+        out[:, 82:84] = _f16_bytes(g.uniform(lo, hi, nb).astype(np.float32))
+    elif fmt == "Q3_K":  # hmask[32], qs[64], scales[12], d
+        out[:, 0:108] = g.integers(0, 256, (nb, 108), dtype=np.uint8)
+        out[:, 108:110] = _f16_bytes(g.uniform(lo, hi, nb).astype(np.float32))
     else:
         raise ValueError(fmt)
     return out.reshape(rows, (K // BLOCK_ELEMS[fmt]) * bb)

@@ -26,9 +26,11 @@ _lock = threading.Lock()
 _lib = None
 
 # The oracle's own format tags (see ggq_oracle.h).
-FMT = {"Q4_0": 0, "Q8_0": 1, "Q4_K": 2, "Q5_K": 3, "Q6_K": 4, "MXFP4": 5, "Q8_1": 6, "Q8_K": 7}
-BLOCK_ELEMS = {"Q4_0": 32, "Q8_0": 32, "MXFP4": 32, "Q8_1": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256, "Q8_K": 256}
-BLOCK_BYTES = {"Q4_0": 18, "Q8_0": 34, "MXFP4": 17, "Q8_1": 36, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210, "Q8_K": 292}
+FMT = {"Q4_0": 0, "Q8_0": 1, "Q4_K": 2, "Q5_K": 3, "Q6_K": 4, "MXFP4": 5, "Q8_1": 6, "Q8_K": 7, "Q2_K": 8, "Q3_K": 9}
+BLOCK_ELEMS = {"Q4_0": 32, "Q8_0": 32, "MXFP4": 32, "Q8_1": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256, "Q8_K": 256,
+               "Q2_K": 256, "Q3_K": 256}
+BLOCK_BYTES = {"Q4_0": 18, "Q8_0": 34, "MXFP4": 17, "Q8_1": 36, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210, "Q8_K": 292,
+               "Q2_K": 84, "Q3_K": 110}
 
 
 def build(force: bool = False) -> str:
@@ -63,6 +65,9 @@ def lib():
                 "orc_float_to_half": (ctypes.c_uint16, [ctypes.c_float]),
                 "orc_e2m1": (ctypes.c_double, [i32]),
                 "orc_kq_scale_min": (None, [p, i32, p, p]),
+                "orc_q3k_scale": (i32, [p, i32]),
+                "orc_coefs_per_block": (i32, [i32]),
+                "orc_block_bytes": (i32, [i32]),
                 "orc_dequant": (None, [i32, p, i64, i64, p]),
                 "orc_quantize_q8_1": (None, [p, i64, i64, p]),
                 "orc_quantize_q8_k": (None, [p, i64, i64, p]),
@@ -124,12 +129,18 @@ def kq_scale_min(scales12: np.ndarray, s: int) -> tuple[int, int]:
     return sc.value, m.value
 
 
+def q3k_scale(scales12: np.ndarray, s: int) -> int:
+    """Unsigned 6-bit scale of 16-element group s of a Q3_K block (signed: - 32)."""
+    a = np.ascontiguousarray(scales12, dtype=np.uint8)
+    return int(lib().orc_q3k_scale(_p(a), int(s)))
+
+
 def act_type(wtype: str) -> str:
     return "Q8_1" if wtype == "Q4_0" else "Q8_K"
 
 
 def coefs_per_block(wtype: str) -> int:
-    return 2 if wtype in ("Q4_K", "Q5_K") else 1
+    return int(lib().orc_coefs_per_block(FMT[wtype]))
 
 
 def row_bytes(fmt: str, K: int) -> int:

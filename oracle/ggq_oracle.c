@@ -16,7 +16,10 @@
  *   [VC523] vllm.cpp PR #523 "feat(rocm): grouped + non-grouped keep-quant
  *           expert GEMM" -- What changed: kMatmulBTQuant / kMatmulBTQuantGrouped,
  *           Q8_0/Q4_K/Q5_K/Q6_K weights, Q8_0 + Q8_K activation quantizers,
- *           integer superblock dots (DotQ8_0/DotQ4K/DotQ5K/DotQ6K) with dp4a.
+ *           integer superblock dots (DotQ8_0/DotQ4K/DotQ5K/DotQ6K) with dp4a;
+ *           Honest gaps: Q2_K and Q3_K follow the same skeleton (the review
+ *           there lists them among the formats its CPU keep-quant oracle
+ *           accepts).
  *   [DS656] ds4 PR #656 "Add ROCm MXFP4 routed expert kernels" -- Summary and
  *           Correctness: MXFP4 x Q8_K routed gate/up, SwiGLU, down.
  * The pages name the block formats but print no layout; the layouts below are
@@ -100,7 +103,7 @@ static float rdf32(const uint8_t* p) { float f; memcpy(&f, p, 4); return f; }
 int orc_block_elems(int type) {
     switch (type) {
     case ORC_Q4_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q8_1: return 32;
-    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: case ORC_Q2_K: case ORC_Q3_K: return 256;
     default: return 0;
     }
 }
@@ -115,6 +118,8 @@ int orc_block_bytes(int type) {
     case ORC_Q5_K: return 176; /* fp16 d, fp16 dmin, scales[12], qh[32], qs[128] */
     case ORC_Q6_K: return 210; /* ql[128], qh[64], int8 scales[16], fp16 d */
     case ORC_Q8_K: return 292; /* fp32 d, int8[256], int16 bsums[16] */
+    case ORC_Q2_K: return 84;  /* scales[16] (low nibble scale, high nibble min), qs[64], fp16 d, fp16 dmin */
+    case ORC_Q3_K: return 110; /* hmask[32], qs[64], scales[12] (16 packed 6-bit), fp16 d */
     default: return 0;
     }
 }
@@ -130,6 +135,16 @@ void orc_kq_scale_min(const uint8_t* sc12, int s, int* sc, int* m) {
     }
 }
 
+/* Q3_K: 6-bit scale of 16-element group s (0..15) from the 12 packed bytes:
+ * its low four bits are the low (s < 8) or high (s >= 8) nibble of byte s % 8,
+ * its high two bits are bits 2(s/4), 2(s/4)+1 of byte 8 + s % 4.  The group's
+ * signed scale is this value - 32. */
+int orc_q3k_scale(const uint8_t* sc12, int s) {
+    int lo = s < 8 ? (sc12[s] & 15) : (sc12[s - 8] >> 4);
+    int hi = (sc12[8 + s % 4] >> (2 * (s / 4))) & 3;
+    return lo | (hi << 4);
+}
+
 /* Integer quant of element i of one weight block, plus the per-element integer
  * scale factor where the format has one.  Values follow the closed forms:
  *   Q4_0: (nib - 8)                    value = d * q
@@ -137,7 +152,11 @@ void orc_kq_scale_min(const uint8_t* sc12, int s, int* sc, int* m) {
  *   Q4_K: nib in 0..15, sub-block s     value = d*sc_s*q - dmin*m_s
  *   Q5_K: nib + 16*hbit                 value = d*sc_s*q - dmin*m_s
  *   Q6_K: (6-bit) - 32, group j=i/16    value = d*sc_j*q
- *   MXFP4: doubled E2M1 code (integer)  value = q * 2^(e-128)          */
+ *   Q2_K: 2-bit q in 0..3, group j=i/16  value = d*sc_j*q - dmin*m_j
+ *   Q3_K: 2 low bits + high bit, in -4..3 value = d*(sc6_j - 32)*q
+ *   MXFP4: doubled E2M1 code (integer)  value = q * 2^(e-128)
+ * Q2_K / Q3_K element i = 128n + 32j + l takes bits 2j, 2j+1 of qs[32n + l];
+ * Q3_K adds bit 4n + j of hmask[l]: set keeps the value, clear subtracts 4. */
 static int elem_q(int type, const uint8_t* b, int i) {
     switch (type) {
     case ORC_Q4_0: {
@@ -167,6 +186,16 @@ static int elem_q(int type, const uint8_t* b, int i) {
         int hi = (qh[32 * h + l] >> (2 * g)) & 3;
         return (nib | (hi << 4)) - 32;
     }
+    case ORC_Q2_K: {
+        int n = i / 128, j = (i % 128) / 32, l = i % 32;
+        return (b[16 + 32 * n + l] >> (2 * j)) & 3;
+    }
+    case ORC_Q3_K: {
+        int n = i / 128, j = (i % 128) / 32, l = i % 32;
+        int lo = (b[32 + 32 * n + l] >> (2 * j)) & 3;
+        int hbit = (b[l] >> (4 * n + j)) & 1;
+        return lo - (hbit ? 0 : 4);
+    }
     default: return 0;
     }
 }
@@ -186,6 +215,11 @@ void orc_dequant_block(int type, const uint8_t* b, double* out) {
             break;
         }
         case ORC_Q6_K: out[i] = orc_half_to_double(rd16(b + 208)) * (int8_t)b[192 + i / 16] * q; break;
+        case ORC_Q2_K:
+            out[i] = orc_half_to_double(rd16(b + 80)) * (b[i / 16] & 15) * q -
+                     orc_half_to_double(rd16(b + 82)) * (b[i / 16] >> 4);
+            break;
+        case ORC_Q3_K: out[i] = orc_half_to_double(rd16(b + 108)) * (orc_q3k_scale(b + 96, i / 16) - 32) * q; break;
         case ORC_Q8_1: out[i] = orc_half_to_double(rd16(b)) * (int8_t)b[4 + i]; break;
         case ORC_Q8_K: out[i] = (double)rdf32(b) * (int8_t)b[4 + i]; break;
         }
@@ -286,9 +320,10 @@ void orc_quantize_q8_k(const float* x, int64_t T, int64_t K, uint8_t* out) {
 int orc_act_type(int wtype) { return wtype == ORC_Q4_0 ? ORC_Q8_1 : ORC_Q8_K; }
 
 /* Number of int32 coefficients per weight block that the block dot produces:
- * 32-element formats: one S per block; Q4_K/Q5_K: (A, B) per superblock; Q6_K: A. */
+ * 32-element formats: one S per block; Q4_K/Q5_K/Q2_K: (A, B) per superblock;
+ * Q6_K/Q3_K: A. */
 int orc_coefs_per_block(int wtype) {
-    return (wtype == ORC_Q4_K || wtype == ORC_Q5_K) ? 2 : 1;
+    return (wtype == ORC_Q4_K || wtype == ORC_Q5_K || wtype == ORC_Q2_K) ? 2 : 1;
 }
 
 /* Whether the library pairs weight format wtype with activation format atype:
@@ -322,7 +357,9 @@ static double act_d32(int atype, const uint8_t* xrow, int64_t j) {
  *   Q8_0 x Q8_K/Q8_0 : S_b = sum_j qw_j * qx_j
  *   MXFP4 x Q8_K: S_b = sum_j code2_j * qx_j          (doubled E2M1 codes)
  *   Q4_K/Q5_K x Q8_K: A = sum_s sc_s * S_s,  B = sum_s m_s * (bsum_2s + bsum_2s+1)
- *   Q6_K x Q8_K : A = sum_j sc_j * S_j,  S_j over 16 elements of q6 - 32        */
+ *   Q6_K x Q8_K : A = sum_j sc_j * S_j,  S_j over 16 elements of q6 - 32
+ *   Q2_K x Q8_K : A = sum_j sc_j * S_j,  B = sum_j m_j * bsum_j   (16-element groups j)
+ *   Q3_K x Q8_K : A = sum_j (sc6_j - 32) * S_j,  S_j over 16 elements of q3     */
 void orc_row_coefs_a(int wtype, int atype, const uint8_t* wrow, const uint8_t* xrow, int64_t K, int32_t* coefs) {
     int be = orc_block_elems(wtype), bb = orc_block_bytes(wtype), nc = orc_coefs_per_block(wtype);
     for (int64_t j = 0; j < K / be; ++j) {
@@ -342,6 +379,24 @@ void orc_row_coefs_a(int wtype, int atype, const uint8_t* wrow, const uint8_t* x
                     int32_t S = 0;
                     for (int i = 0; i < 16; ++i) S += elem_q(wtype, b, 16 * g + i) * qx[16 * g + i];
                     A += (int8_t)b[192 + g] * S;
+                }
+                out[0] = A;
+            } else if (wtype == ORC_Q2_K) {
+                int32_t A = 0, B = 0;
+                for (int g = 0; g < 16; ++g) {
+                    int32_t S = 0;
+                    for (int i = 0; i < 16; ++i) S += elem_q(wtype, b, 16 * g + i) * qx[16 * g + i];
+                    A += (b[g] & 15) * S;
+                    B += (b[g] >> 4) * rds16(xb + 260 + 2 * g);
+                }
+                out[0] = A;
+                out[1] = B;
+            } else if (wtype == ORC_Q3_K) {
+                int32_t A = 0;
+                for (int g = 0; g < 16; ++g) {
+                    int32_t S = 0;
+                    for (int i = 0; i < 16; ++i) S += elem_q(wtype, b, 16 * g + i) * qx[16 * g + i];
+                    A += (orc_q3k_scale(b + 96, g) - 32) * S;
                 }
                 out[0] = A;
             } else {
@@ -388,6 +443,13 @@ static double row_dot_int(int wtype, int atype, const uint8_t* wrow, const uint8
             break;
         case ORC_Q6_K:
             y += (double)rdf32(xrow + j * 292) * orc_half_to_double(rd16(b + 208)) * c[0];
+            break;
+        case ORC_Q2_K:
+            y += (double)rdf32(xrow + j * 292) *
+                 (orc_half_to_double(rd16(b + 80)) * c[0] - orc_half_to_double(rd16(b + 82)) * c[1]);
+            break;
+        case ORC_Q3_K:
+            y += (double)rdf32(xrow + j * 292) * orc_half_to_double(rd16(b + 108)) * c[0];
             break;
         }
     }

@@ -7,7 +7,10 @@
 #include <stdint.h>
 
 /* The oracle's own format tags (independent of the library's enum). */
-enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q5_K = 3, ORC_Q6_K = 4, ORC_MXFP4 = 5, ORC_Q8_1 = 6, ORC_Q8_K = 7 };
+enum {
+    ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_Q5_K = 3, ORC_Q6_K = 4, ORC_MXFP4 = 5, ORC_Q8_1 = 6, ORC_Q8_K = 7,
+    ORC_Q2_K = 8, ORC_Q3_K = 9
+};
 
 void orc_set_threads(int n);
 int orc_get_threads(void);
@@ -21,6 +24,7 @@ int orc_block_bytes(int type);
 int orc_act_type(int wtype);
 int orc_coefs_per_block(int wtype);
 void orc_kq_scale_min(const uint8_t* sc12, int s, int* sc, int* m);
+int orc_q3k_scale(const uint8_t* sc12, int s);
 
 void orc_dequant_block(int type, const uint8_t* b, double* out);
 void orc_dequant(int type, const uint8_t* blocks, int64_t rows, int64_t K, double* out);

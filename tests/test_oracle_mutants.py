@@ -54,6 +54,15 @@ MUTANTS = [
      "case ORC_Q8_0: return (const int8_t*)(xrow + j * 34 + 1);"),
     ("q8_k bsums over 8", "for (int i = 0; i < 16; ++i) s += q[16 * g + i];",
      "for (int i = 0; i < 8; ++i) s += q[16 * g + i];"),
+    ("q2_k bit pair", "return (b[16 + 32 * n + l] >> (2 * j)) & 3;", "return (b[16 + 32 * n + l] >> (2 * j + 1)) & 3;"),
+    ("q2_k half offset", "return (b[16 + 32 * n + l] >> (2 * j)) & 3;", "return (b[16 + 16 * n + l] >> (2 * j)) & 3;"),
+    ("q2_k min from the scale nibble", "(b[i / 16] >> 4);\n", "(b[i / 16] & 15);\n"),
+    ("q2_k integer mins dropped", "B += (b[g] >> 4) * rds16(xb + 260 + 2 * g);", ""),
+    ("q3_k high bit index", "int hbit = (b[l] >> (4 * n + j)) & 1;", "int hbit = (b[l] >> (4 * j + n)) & 1;"),
+    ("q3_k high bit sense", "return lo - (hbit ? 0 : 4);", "return lo - (hbit ? 4 : 0);"),
+    ("q3_k scale high bits", "int hi = (sc12[8 + s % 4] >> (2 * (s / 4))) & 3;", "int hi = (sc12[8 + s / 4] >> (2 * (s % 4))) & 3;"),
+    ("q3_k scale offset", "(orc_q3k_scale(b + 96, i / 16) - 32) * q;", "(orc_q3k_scale(b + 96, i / 16) - 31) * q;"),
+    ("q3_k integer scale group", "A += (orc_q3k_scale(b + 96, g) - 32) * S;", "A += (orc_q3k_scale(b + 96, g ^ 1) - 32) * S;"),
 ]
 
 

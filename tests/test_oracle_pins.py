@@ -219,6 +219,117 @@ def test_q6_k_every_bit_field_position():
             assert np.count_nonzero(v != base) == (1 if scales[i // 16] != 0 else 0)
 
 
+def _pack_q3k_scales(sc6):
+    """Inverse of the Q3_K scale layout: 16 unsigned 6-bit scales -> 12 bytes."""
+    b = np.zeros(12, np.uint8)
+    for s in range(16):
+        v = int(sc6[s])
+        if s < 8:
+            b[s] |= v & 15
+        else:
+            b[s - 8] |= (v & 15) << 4
+        b[8 + s % 4] |= ((v >> 4) & 3) << (2 * (s // 4))
+    return b
+
+
+def test_q3_k_scale_golden():
+    hdr, rows = _read_pairs("q3_k_scales_worked.txt")
+    b = np.frombuffer(hdr["bytes"], dtype=np.uint8)
+    for s, sc in rows:
+        assert orc.q3k_scale(b, int(s)) == int(sc)
+
+
+def test_q3_k_scale_roundtrip_exhaustive():
+    g = np.random.default_rng(5)
+    for s in range(16):
+        for v in range(64):
+            sc6 = g.integers(0, 64, 16)
+            sc6[s] = v
+            b = _pack_q3k_scales(sc6)
+            assert [orc.q3k_scale(b, t) for t in range(16)] == [int(x) for x in sc6]
+
+
+def _low_k_block(fmt, d, dmin, sc, m, q):
+    """Build one Q2_K / Q3_K block from integer fields (inverse of the layout):
+    element i = 128n + 32j + l holds its two low bits at bits 2j of qs[32n + l];
+    Q3_K's q in -4..3 keeps bit 4n + j of hmask[l] set for q >= 0 (q + 4 - 4)
+    and clear for q < 0 (low bits q + 4).  sc, m: per 16-element group (Q2_K:
+    4-bit scale and min; Q3_K: unsigned 6-bit scale, signed value sc - 32)."""
+    blk = np.zeros(84 if fmt == "Q2_K" else 110, np.uint8)
+    qs_off = 16 if fmt == "Q2_K" else 32
+    for i in range(256):
+        n, j, l = i // 128, (i % 128) // 32, i % 32
+        v = int(q[i])
+        if fmt == "Q3_K":
+            if v >= 0:
+                blk[l] |= 1 << (4 * n + j)
+            else:
+                v += 4
+        blk[qs_off + 32 * n + l] |= (v & 3) << (2 * j)
+    if fmt == "Q2_K":
+        blk[0:16] = (np.asarray(sc) & 15) | ((np.asarray(m) & 15) << 4)
+        blk[80:82] = np.array([np.float16(d)]).view(np.uint8)
+        blk[82:84] = np.array([np.float16(dmin)]).view(np.uint8)
+    else:
+        blk[96:108] = _pack_q3k_scales(sc)
+        blk[108:110] = np.array([np.float16(d)]).view(np.uint8)
+    return blk
+
+
+@pytest.mark.parametrize("fmt", ["Q2_K", "Q3_K"])
+def test_low_bit_kquant_element_closed_form(fmt):
+    g = np.random.default_rng(7)
+    d, dmin = np.float16(0.0137), np.float16(0.0059)
+    grp = np.arange(256) // 16
+    for rep in range(8):
+        if fmt == "Q2_K":
+            sc, m = g.integers(0, 16, 16), g.integers(0, 16, 16)
+            sc[rep], m[(rep + 5) % 16] = 15, 0
+            q = np.tile(np.arange(4), 64)[g.permutation(256)]
+            expect = float(d) * sc[grp] * q - float(dmin) * m[grp]
+        else:
+            sc, m = g.integers(0, 64, 16), None
+            sc[rep], sc[(rep + 9) % 16] = 63, 0
+            q = np.tile(np.arange(-4, 4), 32)[g.permutation(256)]
+            expect = float(d) * (sc[grp] - 32) * q
+        v = orc.dequant(fmt, _low_k_block(fmt, d, dmin, sc, m, q), 1, 256)[0]
+        assert np.array_equal(v, expect)
+
+
+@pytest.mark.parametrize("fmt", ["Q2_K", "Q3_K"])
+def test_low_bit_kquant_every_bit_position(fmt):
+    """One-hot bit pairs of qs (and, for Q3_K, bits of hmask): exactly one
+    element moves, at the index the layout defines: qs byte 32n + l, bit pair
+    j -> element 128n + 32j + l; hmask byte l, bit 4n + j -> the same element."""
+    d, dmin = np.float16(0.5), np.float16(0.25)
+    grp = np.arange(256) // 16
+    sc = np.arange(16) % 13 + 1 if fmt == "Q2_K" else (np.arange(16) * 3 + 33) % 64
+    m = np.arange(16) % 5 if fmt == "Q2_K" else None
+    zero = np.zeros(256, int) if fmt == "Q2_K" else np.full(256, -4)
+    blk = _low_k_block(fmt, d, dmin, sc, m, zero)
+    base = orc.dequant(fmt, blk, 1, 256)[0]
+    qs_off = 16 if fmt == "Q2_K" else 32
+    scale = (sc if fmt == "Q2_K" else sc - 32)[grp]
+    for byte in range(64):
+        for j in range(4):
+            x = blk.copy()
+            x[qs_off + byte] |= 1 << (2 * j)  # low bit of the pair: +1
+            v = orc.dequant(fmt, x, 1, 256)[0]
+            i = 128 * (byte // 32) + 32 * j + byte % 32
+            assert list(np.nonzero(v != base)[0]) == [i]
+            assert v[i] - base[i] == float(d) * scale[i]
+    if fmt == "Q3_K":
+        for l in range(32):
+            for bit in range(8):
+                x = blk.copy()
+                x[l] |= 1 << bit  # high bit: -4 -> 0
+                v = orc.dequant(fmt, x, 1, 256)[0]
+                i = 128 * (bit // 4) + 32 * (bit % 4) + l
+                diff = np.nonzero(v != base)[0]
+                assert list(diff) == ([i] if scale[i] != 0 else [])
+                assert v[i] - base[i] == 4 * float(d) * scale[i]
+
+
 def test_mxfp4_every_code_and_exponent():
     _, rows = _read_pairs("e2m1_codes.txt")
     table = {int(c): float(v) for c, v in rows}

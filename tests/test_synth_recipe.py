@@ -2,7 +2,8 @@
 determinism of the synthetic workloads, read straight from the block bytes.
 
 The recipe follows the workload definitions: fp16 scales uniform in their
-ranges, Q6_K int8 sub-scales in [-32, 31], MXFP4 E8M0 exponent bytes in
+ranges (Q2_K: d and dmin after the 80 bytes of scales and quants; Q3_K: d
+after 108), Q6_K int8 sub-scales in [-32, 31], MXFP4 E8M0 exponent bytes in
 117..123 (scales 2^-10 .. 2^-4), uniform quant bytes, N(0, 1) activations and
 logits, and for the prefill workload a Zipf(1.1) expert bias over a seeded
 permutation of ranks.
@@ -41,6 +42,15 @@ def test_weight_fields_stay_in_their_ranges(fmt):
         sc = B[:, 192:208].view(np.int8)
         assert sc.min() == -32 and sc.max() == 31
         quants = B[:, 0:192]
+    elif fmt == "Q2_K":  # scales[16], qs[64], d, dmin
+        for off in (80, 82):
+            v = _f16(B[:, off:off + 2])
+            assert v.min() >= lo16 and v.max() <= hi16
+        quants = B[:, 0:80]
+    elif fmt == "Q3_K":  # hmask[32], qs[64], scales[12], d
+        d = _f16(B[:, 108:110])
+        assert d.min() >= lo16 and d.max() <= hi16
+        quants = B[:, 0:108]
     else:  # MXFP4
         e = B[:, 0]
         assert e.min() == 117 and e.max() == 123
