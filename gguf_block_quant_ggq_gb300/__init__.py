@@ -15,12 +15,15 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libggq.so")
 
-TYPE = {"Q4_0": 2, "Q8_0": 8, "Q8_1": 9, "Q4_K": 12, "Q5_K": 13, "Q6_K": 14, "Q8_K": 15, "MXFP4": 39}
+TYPE = {"Q4_0": 2, "Q8_0": 8, "Q8_1": 9, "Q2_K": 10, "Q3_K": 11, "Q4_K": 12, "Q5_K": 13, "Q6_K": 14, "Q8_K": 15,
+        "MXFP4": 39}
 OP = {"quantize_act": 0, "dequant": 1, "mul_mat_vec": 2, "moe": 3}
 STATUS = {0: "GGQ_OK", 1: "GGQ_ERR_INVALID_ARG", 2: "GGQ_ERR_SHAPE", 3: "GGQ_ERR_UNSUPPORTED", 4: "GGQ_ERR_ARCH",
           5: "GGQ_ERR_CUDA", 6: "GGQ_ERR_CAPACITY", 7: "GGQ_ERR_CAPTURE_ALLOC", 8: "GGQ_ERR_DEVICE"}
-BLOCK_ELEMS = {"Q4_0": 32, "Q8_0": 32, "MXFP4": 32, "Q8_1": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256, "Q8_K": 256}
-BLOCK_BYTES = {"Q4_0": 18, "Q8_0": 34, "MXFP4": 17, "Q8_1": 36, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210, "Q8_K": 292}
+BLOCK_ELEMS = {"Q4_0": 32, "Q8_0": 32, "MXFP4": 32, "Q8_1": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256, "Q8_K": 256,
+               "Q2_K": 256, "Q3_K": 256}
+BLOCK_BYTES = {"Q4_0": 18, "Q8_0": 34, "MXFP4": 17, "Q8_1": 36, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210, "Q8_K": 292,
+               "Q2_K": 84, "Q3_K": 110}
 
 # Every entry point the header declares, with its ctypes signature.
 _P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
@@ -215,14 +218,14 @@ class Context:
         return Y
 
     def block_dots_qa(self, fmt: str, act: str, W, N: int, K: int, Xq, T: int, stream=None):
-        nc = K // BLOCK_ELEMS[fmt] * (2 if fmt in ("Q4_K", "Q5_K") else 1)
+        nc = K // BLOCK_ELEMS[fmt] * (2 if fmt in ("Q4_K", "Q5_K", "Q2_K") else 1)
         out = self._torch.empty((T, N, nc), dtype=self._torch.int32, device=Xq.device)
         self._check(load().ggq_block_dots_qa(self.handle, TYPE[fmt], TYPE[act], _ptr(W), N, K, _ptr(Xq), T,
                                              _ptr(out), self._stream(stream)))
         return out
 
     def block_dots(self, fmt: str, W, N: int, K: int, Xq, T: int, stream=None):
-        nc = K // BLOCK_ELEMS[fmt] * (2 if fmt in ("Q4_K", "Q5_K") else 1)
+        nc = K // BLOCK_ELEMS[fmt] * (2 if fmt in ("Q4_K", "Q5_K", "Q2_K") else 1)
         out = self._torch.empty((T, N, nc), dtype=self._torch.int32, device=Xq.device)
         self._check(load().ggq_block_dots(self.handle, TYPE[fmt], _ptr(W), N, K, _ptr(Xq), T, _ptr(out),
                                           self._stream(stream)))

@@ -24,6 +24,7 @@
 namespace ggq {
 cudaError_t launch_gemv_a(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_gemv_b(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
+cudaError_t launch_gemv_c(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_gemv_q80(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_gateup(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
 cudaError_t launch_direct_down(int fmt, int nt, const DirectParams& p, int grid, int smem, cudaStream_t s);
@@ -33,6 +34,7 @@ cudaError_t launch_direct_down_dump(int fmt, int nt, const DirectParams& p, int 
 
 cudaError_t launch_stream(int kind, int fmt, int nt, const StreamParams& p, int grid, int smem, cudaStream_t s) {
     if (fmt == F_Q4_0 || fmt == F_Q8_0 || fmt == F_MXFP4) return launch_gemv_a(kind, fmt, nt, p, grid, smem, s);
+    if (fmt == F_Q2_K || fmt == F_Q3_K) return launch_gemv_c(kind, fmt, nt, p, grid, smem, s);
     return launch_gemv_b(kind, fmt, nt, p, grid, smem, s);
 }
 }  // namespace ggq
@@ -59,9 +61,15 @@ int fmt_of(int t) {
     case GGQ_TYPE_Q5_K: return F_Q5_K;
     case GGQ_TYPE_Q6_K: return F_Q6_K;
     case GGQ_TYPE_MXFP4: return F_MXFP4;
+    case GGQ_TYPE_Q2_K: return F_Q2_K;
+    case GGQ_TYPE_Q3_K: return F_Q3_K;
     default: return -1;
     }
 }
+
+// The 2- and 3-bit K-quants run on the dp4a streaming GEMV only (no tensor-path,
+// grouped or MoE kernels for them).
+bool low_bit_kquant(int f) { return f == F_Q2_K || f == F_Q3_K; }
 
 const char* type_name(int t) {
     switch (t) {
@@ -73,6 +81,8 @@ const char* type_name(int t) {
     case GGQ_TYPE_Q6_K: return "Q6_K";
     case GGQ_TYPE_Q8_K: return "Q8_K";
     case GGQ_TYPE_MXFP4: return "MXFP4";
+    case GGQ_TYPE_Q2_K: return "Q2_K";
+    case GGQ_TYPE_Q3_K: return "Q3_K";
     default: return "unknown";
     }
 }
@@ -258,13 +268,13 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
         !(act == GGQ_TYPE_Q8_0 && (f == F_Q4_0 || f == F_Q8_0)))
         return fail(c, GGQ_ERR_UNSUPPORTED,
                     "mul_mat_vec: weight type %d (%s) with activation type %d (%s) is not supported; supported: "
-                    "Q4_0 x Q8_1, Q4_0 x Q8_0, Q8_0 x Q8_0, and Q8_0, Q4_K, Q5_K, Q6_K, MXFP4 x Q8_K",
+                    "Q4_0 x Q8_1, Q4_0 x Q8_0, Q8_0 x Q8_0, and Q8_0, Q2_K, Q3_K, Q4_K, Q5_K, Q6_K, MXFP4 x Q8_K",
                     w, type_name(w), act, type_name(act));
     const bool a80 = act == GGQ_TYPE_Q8_0;
     if (f < 0 || w == GGQ_TYPE_Q8_1 || w == GGQ_TYPE_Q8_K)
         return fail(c, GGQ_ERR_UNSUPPORTED,
-                    "mul_mat_vec: weight type %d (%s) is not supported; supported: Q4_0 x Q8_1, and Q8_0, Q4_K, "
-                    "Q5_K, Q6_K, MXFP4 x Q8_K",
+                    "mul_mat_vec: weight type %d (%s) is not supported; supported: Q4_0 x Q8_1, and Q8_0, Q2_K, "
+                    "Q3_K, Q4_K, Q5_K, Q6_K, MXFP4 x Q8_K",
                     w, type_name(w));
     if (!W || !X || !Y) return fail(c, GGQ_ERR_INVALID_ARG, "mul_mat_vec: null pointer");
     if (!aligned16(W) || !aligned16(X) || !aligned16(Y))
@@ -330,7 +340,8 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
 // tokens, except Q8_0 and Q5_K, whose two-token GEMV runs faster on the dp4a
 // streaming kernel (14336 x 4096 rows at two tokens: Q8_0 12.0 against 12.5 us,
 // Q5_K 12.4 against 12.7 us; Q4_K 10.6 against 10.0, Q6_K 16.9 against 14.1).
-int mma_min_tokens(int f) { return f == F_Q8_0 || f == F_Q5_K ? 3 : 2; }
+// Q2_K and Q3_K never take it.
+int mma_min_tokens(int f) { return low_bit_kquant(f) ? 1 << 30 : f == F_Q8_0 || f == F_Q5_K ? 3 : 2; }
 
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st, bool a80 = false) {
@@ -366,7 +377,7 @@ ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t 
             return GGQ_OK;
         }
     }
-    if (!a80 && T >= kGroupMinTokens && f != F_Q4_0 && K % 1024 == 0 && aligned16(Xq)) {
+    if (!a80 && T >= kGroupMinTokens && f != F_Q4_0 && !low_bit_kquant(f) && K % 1024 == 0 && aligned16(Xq)) {
         // several activation columns: the int8 tensor-core kernel (Q8_K rows are 16-byte multiples)
         GroupParams g{};
         g.W = static_cast<const uint8_t*>(W);
@@ -733,7 +744,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     const int fg = fmt_of(w->gate_type), fu = fmt_of(w->up_type), fd = fmt_of(w->down_type);
     for (int t : {w->gate_type, w->up_type, w->down_type}) {
         const int f = fmt_of(t);
-        if (f < 0 || f == F_Q4_0)
+        if (f < 0 || f == F_Q4_0 || low_bit_kquant(f))
             return fail(c, GGQ_ERR_UNSUPPORTED,
                         "moe_experts: expert weight type %d (%s) is not supported; supported with Q8_K activations: "
                         "Q8_0, Q4_K, Q5_K, Q6_K, MXFP4",
@@ -961,7 +972,7 @@ int ggq_supported(int w, int act, int op) {
         if (f < 0) return 0;
         if (act == GGQ_TYPE_Q8_0) return f == F_Q4_0 || f == F_Q8_0;
         return f == F_Q4_0 ? act == GGQ_TYPE_Q8_1 : act == GGQ_TYPE_Q8_K;
-    case GGQ_OP_MOE: return f >= 0 && f != F_Q4_0 && act == GGQ_TYPE_Q8_K;
+    case GGQ_OP_MOE: return f >= 0 && f != F_Q4_0 && !low_bit_kquant(f) && act == GGQ_TYPE_Q8_K;
     default: return 0;
     }
 }

@@ -19,14 +19,17 @@
 
 namespace ggq {
 
-enum Fmt : int { F_Q4_0 = 0, F_Q8_0 = 1, F_Q4_K = 2, F_Q5_K = 3, F_Q6_K = 4, F_MXFP4 = 5, F_COUNT = 6 };
+enum Fmt : int { F_Q4_0 = 0, F_Q8_0 = 1, F_Q4_K = 2, F_Q5_K = 3, F_Q6_K = 4, F_MXFP4 = 5, F_Q2_K = 6, F_Q3_K = 7, F_COUNT = 8 };
 
-__host__ __device__ constexpr int fmt_qk(int f) { return (f == F_Q4_K || f == F_Q5_K || f == F_Q6_K) ? 256 : 32; }
+__host__ __device__ constexpr int fmt_qk(int f) {
+    return (f == F_Q4_K || f == F_Q5_K || f == F_Q6_K || f == F_Q2_K || f == F_Q3_K) ? 256 : 32;
+}
 __host__ __device__ constexpr int fmt_bytes(int f) {
-    return f == F_Q4_0 ? 18 : f == F_Q8_0 ? 34 : f == F_Q4_K ? 144 : f == F_Q5_K ? 176 : f == F_Q6_K ? 210 : 17;
+    return f == F_Q4_0 ? 18 : f == F_Q8_0 ? 34 : f == F_Q4_K ? 144 : f == F_Q5_K ? 176 : f == F_Q6_K ? 210
+         : f == F_Q2_K ? 84 : f == F_Q3_K ? 110 : 17;
 }
 // int32 coefficients per weight block in the debug dump (see ggq_block_dots).
-__host__ __device__ constexpr int fmt_coefs(int f) { return (f == F_Q4_K || f == F_Q5_K) ? 2 : 1; }
+__host__ __device__ constexpr int fmt_coefs(int f) { return (f == F_Q4_K || f == F_Q5_K || f == F_Q2_K) ? 2 : 1; }
 __host__ __device__ constexpr bool fmt_q81(int f) { return f == F_Q4_0; }
 
 // Device error word values (a bounded wait ran out; a routed expert id out of range).
@@ -211,7 +214,7 @@ struct Unit {
     uint32_t w[16];
     int xo[4];
     int sc[4];     // integer scale per group (K-quants)
-    int mn[2];     // Q4_K/Q5_K mins of the unit's two sub-blocks
+    int mn[4];     // mins: Q4_K/Q5_K per sub-block (mn[0], mn[1]), Q2_K per group
     float da, db;  // K-quants: d and dmin (Q6_K: d); 32-block formats: scale of block 0 and block 1
 };
 
@@ -342,6 +345,44 @@ __device__ __forceinline__ void load_unit(saddr row, int u, int nblk32, Unit& un
                 un.w[8 + k] = ((q[k] >> 4) & 0x0F0F0F0Fu) | (((hq[k] >> (2 * cc + 1)) & 0x01010101u) << 4);
             }
         }
+    } else if constexpr (F == F_Q2_K || F == F_Q3_K) {
+        // element 128n + 32j + l: bits 2j, 2j+1 of qs[32n + l] (Q3_K: bit 4n + j of hmask[l]
+        // adds 4 to the stored code, which is q + 4).  Unit v = u&3 is elements 64v .. 64v+63:
+        // n = v>>1, j0 = 2(v&1); w[0..7] take shift j0 (groups 4v, 4v+1), w[8..15] shift j0+1.
+        const int sb = u >> 2, v = u & 3, n = v >> 1, j0 = 2 * (v & 1);
+        const saddr b = row + static_cast<uint32_t>(fmt_bytes(F)) * sb;
+        uint32_t q[8];
+        ld_words_any<8>(b + (F == F_Q2_K ? 16 : 32) + 32 * n, q);
+        if constexpr (F == F_Q2_K) {
+            const uint32_t s4 = ld_s32(b + 4 * v);  // scales[4v .. 4v+3]: low nibble scale, high nibble min
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                un.sc[g] = (s4 >> (8 * g)) & 15;
+                un.mn[g] = (s4 >> (8 * g + 4)) & 15;
+            }
+            un.da = ld_h(b + 80);
+            un.db = ld_h(b + 82);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                un.w[k] = (q[k] >> (2 * j0)) & 0x03030303u;
+                un.w[8 + k] = (q[k] >> (2 * j0 + 2)) & 0x03030303u;
+            }
+        } else {
+            uint32_t hm[8], sw[2];
+            ld_words_any<8>(b, hm);
+            ld_words_any<1>(b + 96 + 4 * (v & 1), sw);      // low nibbles of groups 4v .. 4v+3
+            ld_words_any<1>(b + 104, sw + 1);               // their high two bits
+            const uint32_t sc6 = ((v < 2 ? sw[0] : sw[0] >> 4) & 0x0F0F0F0Fu) | (((sw[1] >> (2 * v)) & 0x03030303u) << 4);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) un.sc[g] = static_cast<int>((sc6 >> (8 * g)) & 0xFFu) - 32;
+            un.da = ld_h(b + 108);
+            const int hb = 4 * n + j0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                un.w[k] = ((q[k] >> (2 * j0)) & 0x03030303u) | (((hm[k] >> hb) & 0x01010101u) << 2);
+                un.w[8 + k] = ((q[k] >> (2 * j0 + 2)) & 0x03030303u) | (((hm[k] >> (hb + 1)) & 0x01010101u) << 2);
+            }
+        }
     } else {  // F_Q6_K
         // element 128h + 32g + l: ql[64h + 32(g&1) + l] nibble g>>1, qh[32h + l] bits 2g..2g+1,
         // scale index (128h + 32g + l)/16.  Unit v = u&3: h = v>>1, g1 = v&1; w[0..7] are
@@ -410,6 +451,16 @@ __device__ __forceinline__ void unit_ints(const Unit& un, const int* xo, const X
     } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
         A0 = un.sc[0] * (S[0] + S[1]) + un.sc[2] * (S[2] + S[3]);
         A1 = un.mn[0] * static_cast<int>(ld_s32(s32 + 8 * u)) + un.mn[1] * static_cast<int>(ld_s32(s32 + 8 * u + 4));
+    } else if constexpr (F == F_Q2_K) {  // per group of 16: scale * S, min * sum(q)
+        const saddr bs = xs.bs + 2u * static_cast<uint32_t>(r * (xs.K >> 4));
+        A0 = un.sc[0] * S[0] + un.sc[1] * S[1] + un.sc[2] * S[2] + un.sc[3] * S[3];
+        A1 = un.mn[0] * ld_s16(bs + 2 * (xo[0] >> 4)) + un.mn[1] * ld_s16(bs + 2 * (xo[1] >> 4)) +
+             un.mn[2] * ld_s16(bs + 2 * (xo[2] >> 4)) + un.mn[3] * ld_s16(bs + 2 * (xo[3] >> 4));
+    } else if constexpr (F == F_Q3_K) {  // codes stored as q + 4: subtract 4 * sum(q) per group of 16
+        const saddr bs = xs.bs + 2u * static_cast<uint32_t>(r * (xs.K >> 4));
+        A0 = un.sc[0] * (S[0] - 4 * ld_s16(bs + 2 * (xo[0] >> 4))) + un.sc[1] * (S[1] - 4 * ld_s16(bs + 2 * (xo[1] >> 4))) +
+             un.sc[2] * (S[2] - 4 * ld_s16(bs + 2 * (xo[2] >> 4))) + un.sc[3] * (S[3] - 4 * ld_s16(bs + 2 * (xo[3] >> 4)));
+        A1 = 0;
     } else {  // Q6_K: 6-bit codes stored unsigned; subtract 32 * sum(q) per group of 16
         const saddr bs = xs.bs + 2u * static_cast<uint32_t>(r * (xs.K >> 4));
         A0 = un.sc[0] * (S[0] - 32 * ld_s16(bs + 2 * (xo[0] >> 4))) + un.sc[1] * (S[1] - 32 * ld_s16(bs + 2 * (xo[1] >> 4))) +
@@ -428,10 +479,10 @@ __device__ __forceinline__ float unit_value(const Unit& un, const XS& xs, int r,
     } else if constexpr (F == F_Q8_0 || F == F_MXFP4) {
         const float dx = ld_f32(xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 8) + (u >> 2)));
         return dx * (static_cast<float>(A0) * un.da + static_cast<float>(A1) * un.db);
-    } else if constexpr (F == F_Q6_K) {
+    } else if constexpr (F == F_Q6_K || F == F_Q3_K) {
         const float dx = ld_f32(xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 8) + (u >> 2)));
         return static_cast<float>(A0) * (dx * un.da);
-    } else {
+    } else {  // Q4_K, Q5_K, Q2_K: d * A - dmin * B
         const float dx = ld_f32(xs.d + 4u * static_cast<uint32_t>(r * (xs.K >> 8) + (u >> 2)));
         return dx * (un.da * static_cast<float>(A0) - un.db * static_cast<float>(A1));
     }
@@ -491,9 +542,10 @@ __device__ __forceinline__ void load_xunit(const XS& xs, int u, XUnit& xu) {
         } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
             xu.c[0] = s0;
             xu.c[1] = s1;
-        } else if constexpr (F == F_Q6_K) {
+        } else if constexpr (F == F_Q6_K || F == F_Q3_K || F == F_Q2_K) {
+            constexpr int off = F == F_Q6_K ? 32 : F == F_Q3_K ? 4 : 1;  // Q2_K: the sums for the mins
 #pragma unroll
-            for (int g = 0; g < 4; ++g) xu.c[g] = 32 * ld_s16(xs.bs + 2u * static_cast<uint32_t>(xo[g] >> 4));
+            for (int g = 0; g < 4; ++g) xu.c[g] = off * ld_s16(xs.bs + 2u * static_cast<uint32_t>(xo[g] >> 4));
         }
     }
 }
@@ -610,6 +662,24 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         const int A0 = s0 * lo + s1 * hi;
         const int A1 = m0 * xu.c[0] + m1 * xu.c[1];
         return xu.d0 * (da * static_cast<float>(A0) - dm * static_cast<float>(A1));
+    } else if constexpr (F == F_Q2_K || F == F_Q3_K) {  // (element layout as in load_unit)
+        Unit un;
+        load_unit<F>(row, u, nb32, un);
+        int S[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            S[k >> 2] = __dp4a(static_cast<int>(un.w[k]), static_cast<int>(xu.x[k]), S[k >> 2]);
+            S[2 + (k >> 2)] = __dp4a(static_cast<int>(un.w[8 + k]), static_cast<int>(xu.x[8 + k]), S[2 + (k >> 2)]);
+        }
+        if constexpr (F == F_Q2_K) {
+            const int A0 = un.sc[0] * S[0] + un.sc[1] * S[1] + un.sc[2] * S[2] + un.sc[3] * S[3];
+            const int A1 = un.mn[0] * xu.c[0] + un.mn[1] * xu.c[1] + un.mn[2] * xu.c[2] + un.mn[3] * xu.c[3];
+            return xu.d0 * (un.da * static_cast<float>(A0) - un.db * static_cast<float>(A1));
+        } else {
+            const int A0 = un.sc[0] * (S[0] - xu.c[0]) + un.sc[1] * (S[1] - xu.c[1]) + un.sc[2] * (S[2] - xu.c[2]) +
+                           un.sc[3] * (S[3] - xu.c[3]);
+            return static_cast<float>(A0) * (xu.d0 * un.da);
+        }
     } else {  // F_Q6_K (element layout as in load_unit)
         const int sb = u >> 2, v = u & 3, h = v >> 1, g1 = v & 1;
         const saddr b = row + 210u * sb;

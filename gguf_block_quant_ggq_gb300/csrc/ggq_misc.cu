@@ -107,6 +107,22 @@ __global__ void k_dequant(const uint8_t* __restrict__ blocks, int64_t nblocks, f
                 y[32 * s + l] = a * static_cast<float>(q) - m;
             }
         }
+    } else if constexpr (F == F_Q2_K || F == F_Q3_K) {
+        // element 128n + 32j + l: bits 2j, 2j+1 of qs[32n + l]; Q3_K: bit 4n + j of hmask[l]
+        // clear subtracts 4; Q2_K scale/min nibbles per 16, Q3_K packed 6-bit scales - 32
+        const float d = half_at(b + (F == F_Q2_K ? 80 : 108));
+        for (int e = 0; e < 256; ++e) {
+            const int n = e >> 7, j = (e >> 5) & 3, l = e & 31, g = e >> 4;
+            int q = (b[(F == F_Q2_K ? 16 : 32) + 32 * n + l] >> (2 * j)) & 3;
+            if constexpr (F == F_Q2_K) {
+                y[e] = d * static_cast<float>(b[g] & 15) * static_cast<float>(q) - half_at(b + 82) * static_cast<float>(b[g] >> 4);
+            } else {
+                if (!((b[l] >> (4 * n + j)) & 1)) q -= 4;
+                const int lo = g < 8 ? (b[96 + g] & 15) : (b[96 + g - 8] >> 4);
+                const int hi = (b[104 + (g & 3)] >> (2 * (g >> 2))) & 3;
+                y[e] = d * static_cast<float>((lo | (hi << 4)) - 32) * static_cast<float>(q);
+            }
+        }
     } else {  // Q6_K
         const float d = half_at(b + 208);
         for (int e = 0; e < 256; ++e) {
@@ -129,6 +145,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t* blocks, int64_t rows, int64_t
     case F_Q4_K: return launch_pdl(k_dequant<F_Q4_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
     case F_Q5_K: return launch_pdl(k_dequant<F_Q5_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
     case F_Q6_K: return launch_pdl(k_dequant<F_Q6_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    case F_Q2_K: return launch_pdl(k_dequant<F_Q2_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
+    case F_Q3_K: return launch_pdl(k_dequant<F_Q3_K>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
     default: return launch_pdl(k_dequant<F_MXFP4>, dim3(grid), dim3(128), 0, s, blocks, nb, out);
     }
     return cudaGetLastError();

@@ -52,6 +52,8 @@ int fmt_of_type(int t) {
     case GGQ_TYPE_Q5_K: return F_Q5_K;
     case GGQ_TYPE_Q6_K: return F_Q6_K;
     case GGQ_TYPE_MXFP4: return F_MXFP4;
+    case GGQ_TYPE_Q2_K: return F_Q2_K;
+    case GGQ_TYPE_Q3_K: return F_Q3_K;
     default: return -1;
     }
 }

@@ -36,6 +36,14 @@ inline void chunk_granule(int f, int64_t rowbytes, int* units, int* bytes) {
     case F_MXFP4: *units = 8, *bytes = 272; break;  // 16 blocks of 17 B
     case F_Q4_K: *units = 4, *bytes = 144; break;   // one superblock
     case F_Q5_K: *units = 4, *bytes = 176; break;   // one superblock
+    case F_Q2_K:                                    // superblocks of 84 B: four are 336 B
+        if (rowbytes % 16 == 0) *units = 16, *bytes = 336;
+        else *units = 4, *bytes = 84;
+        break;
+    case F_Q3_K:                                    // superblocks of 110 B: eight are 880 B
+        if (rowbytes % 16 == 0) *units = 32, *bytes = 880;
+        else *units = 4, *bytes = 110;
+        break;
     default:                                        // Q6_K: superblocks of 210 B
         if (rowbytes % 16 == 0) *units = 32, *bytes = 1680;
         else *units = 4, *bytes = 210;

@@ -3,9 +3,10 @@
  * routed-expert GEMMs over GGUF block-quantized weights, on one GB300 GPU
  * (sm_103a).
  *
- * Weights stay in their packed GGUF blocks (Q4_0, Q8_0, Q4_K, Q5_K, Q6_K,
- * MXFP4).  Activations are quantized on the fly to int8 blocks (Q8_1 for Q4_0,
- * Q8_K for every other format) and every dot is an exact integer block dot
+ * Weights stay in their packed GGUF blocks (Q4_0, Q8_0, Q2_K, Q3_K, Q4_K, Q5_K,
+ * Q6_K, MXFP4; Q2_K and Q3_K in the matrix-vector product only).  Activations
+ * are quantized on the fly to int8 blocks (Q8_1 for Q4_0, Q8_K for every other
+ * format) and every dot is an exact integer block dot
  * followed by a floating-point scale epilogue.
  *
  * Pages the operations follow (cited by title and section):
@@ -15,7 +16,8 @@
  *   vllm.cpp PR #523 "feat(rocm): grouped + non-grouped keep-quant expert
  *     GEMM", What changed: kMatmulBTQuant (op 74, non-grouped) and
  *     kMatmulBTQuantGrouped (op 75, grouped over expert_ids), Q8_0/Q4_K/Q5_K/
- *     Q6_K weights, Q8_0 + Q8_K activation quantizers; review: a per-dtype
+ *     Q6_K weights, Q8_0 + Q8_K activation quantizers; Honest gaps: the K-quants
+ *     Q2_K and Q3_K follow the same skeleton; review: a per-dtype
  *     availability query instead of a boolean, a refusal that names the
  *     unsupported formats, and a grow-only scratch pool with no per-call
  *     malloc, free or synchronisation (graph capture safe).
@@ -70,6 +72,8 @@ typedef enum ggq_type {
     GGQ_TYPE_Q4_0 = 2,   /* 32 weights: fp16 d, 16 B nibbles; w = (q - 8) d               */
     GGQ_TYPE_Q8_0 = 8,   /* 32 weights or activations: fp16 d, int8[32];  v = q d        */
     GGQ_TYPE_Q8_1 = 9,   /* 32 activations: fp16 d, fp16 s = d*sum(q), int8[32]            */
+    GGQ_TYPE_Q2_K = 10,  /* 256: scales[16] (4-bit scale, 4-bit min), 64 B 2-bit quants, d, dmin */
+    GGQ_TYPE_Q3_K = 11,  /* 256: 32 B high bits, 64 B 2-bit quants, 12 B 6-bit scales, fp16 d */
     GGQ_TYPE_Q4_K = 12,  /* 256: fp16 d, dmin, 12 B 6-bit scales/mins, 128 B nibbles       */
     GGQ_TYPE_Q5_K = 13,  /* 256: Q4_K header, 32 B high bits, 128 B nibbles                 */
     GGQ_TYPE_Q6_K = 14,  /* 256: 128 B low nibbles, 64 B high 2 bits, int8 scales[16], d   */
@@ -225,7 +229,10 @@ ggq_status ggq_mul_mat_vec_qa(ggq_ctx* ctx, int w, int act, const void* W, int64
  *     per 32-block (MXFP4 with doubled E2M1 codes);
  *   Q4_K/Q5_K x Q8_K (c = 2): A = sum_s sc_s S_s and B = sum_s m_s bsum_s per
  *     superblock, y += d_x (d A - dmin B);
- *   Q6_K x Q8_K (c = 1): A = sum_j sc_j S_j per superblock, y += d_x d A.
+ *   Q6_K x Q8_K (c = 1): A = sum_j sc_j S_j per superblock, y += d_x d A;
+ *   Q2_K x Q8_K (c = 2): A = sum_j sc_j S_j and B = sum_j m_j bsum_j over the 16
+ *     groups of 16, y += d_x (d A - dmin B);
+ *   Q3_K x Q8_K (c = 1): A = sum_j (sc_j - 32) S_j over the 16 groups, y += d_x d A.
  * Runs the kernel that ggq_mul_mat_vec_q picks for the same (w, N, K, T) --
  * the dp4a streaming kernel, the tensor-path GEMV (2-8 tokens) or the grouped
  * int8 tensor-core kernel -- in a variant that stores the integers its dp4a or

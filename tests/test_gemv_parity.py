@@ -114,6 +114,15 @@ def _extreme_block(fmt, sign):
         b[0:192] = 0xFF if sign > 0 else 0x00  # codes 63 (31 after the offset) or 0 (-32)
         b[192:208] = 127
         b[208:210] = one
+    elif fmt == "Q2_K":
+        b[0:16] = 0xFF  # scale 15, min 15 in every group
+        b[16:80] = 0xFF  # every 2-bit code 3
+        b[80:82], b[82:84] = one, one
+    elif fmt == "Q3_K":
+        b[0:32] = 0xFF if sign > 0 else 0x00  # high bits: codes 3 or -4 (with low bits 3 / 0)
+        b[32:96] = 0xFF if sign > 0 else 0x00
+        b[96:108] = 0x00  # every 6-bit scale 0: signed scale -32, the largest magnitude
+        b[108:110] = one
     return b
 
 
@@ -186,7 +195,11 @@ LONG_ROWS = [  # (fmt, N, K, T): rows too long for whole-row stages, streamed in
     ("Q5_K", 53, 14336, 3),
     ("Q4_0", 21, 16384, 1),
     ("MXFP4", 40, 16384, 2),
+    ("Q2_K", 16 * 40 + 9, 28672, 1),   # 4-superblock chunks
+    ("Q3_K", 37, 28672, 2),            # 8-superblock chunks
     # rows that are not 16-byte multiples: chunk ends copied byte by byte
+    ("Q2_K", 35, 26368, 1),            # 103 superblocks: 8652-byte rows
+    ("Q3_K", 16 * 9 + 7, 26368, 3),    # 11330-byte rows
     ("Q6_K", 16 * 9 + 7, 18944, 1),    # 74 superblocks: 15540-byte rows
     ("Q6_K", 35, 18944, 4),
     ("MXFP4", 40, 23296, 2),           # 12376-byte rows
@@ -243,7 +256,7 @@ def test_q4_0_workload_1024x4096(ctx):
     assert np.array_equal(to_host(ctx.quantize_act("Q8_1", to_dev(x))), xq)
 
 
-@pytest.mark.parametrize("fmt", ["Q8_0", "Q4_K", "Q5_K", "Q6_K"])
+@pytest.mark.parametrize("fmt", ["Q8_0", "Q4_K", "Q5_K", "Q6_K", "Q2_K", "Q3_K"])
 def test_full_size_14336x4096_sampled_rows(ctx, fmt):
     """Full workload size in the bench's launch configuration (T = 8 and 1);
     the oracle computes a sample of rows one by one, including both ends."""
@@ -270,11 +283,11 @@ def test_errors_are_refused_loudly(ctx):
     with pytest.raises(ggq.GGQError, match="SHAPE"):
         ctx.mul_mat_vec("Q4_K", W, 16, 255, x[:1])
     with pytest.raises(KeyError):
-        ctx.mul_mat_vec("Q2_K", W, 16, 256, x[:1])
+        ctx.mul_mat_vec("IQ2_XXS", W, 16, 256, x[:1])
     h = ggq.load()
     y = torch.empty((1, 16), dtype=torch.float32, device="cuda")
-    st = h.ggq_mul_mat_vec(ctx.handle, 10, W.data_ptr(), 16, 256, x.data_ptr(), 1, y.data_ptr(), None)
-    assert st == 3 and b"Q2_K" not in h.ggq_last_error(ctx.handle) and b"supported" in h.ggq_last_error(ctx.handle)
+    st = h.ggq_mul_mat_vec(ctx.handle, 16, W.data_ptr(), 16, 256, x.data_ptr(), 1, y.data_ptr(), None)  # IQ2_XXS
+    assert st == 3 and b"supported" in h.ggq_last_error(ctx.handle)
     fresh = ggq.Context(0)
     try:  # no reserve yet: the call refuses instead of allocating
         st = h.ggq_mul_mat_vec(fresh.handle, 12, W.data_ptr(), 16, 256, x.data_ptr(), 1, y.data_ptr(), None)
