@@ -662,7 +662,29 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         const int A0 = s0 * lo + s1 * hi;
         const int A1 = m0 * xu.c[0] + m1 * xu.c[1];
         return xu.d0 * (da * static_cast<float>(A0) - dm * static_cast<float>(A1));
-    } else if constexpr (F == F_Q2_K || F == F_Q3_K) {  // (element layout as in load_unit)
+    } else if constexpr (F == F_Q2_K) {  // (element layout as in load_unit)
+        // each 2-bit field is masked in place (4^j times its value, as unsigned
+        // bytes) and the exact factor is shifted out of the group's integer sum
+        const int sb = u >> 2, v = u & 3, n = v >> 1, j0 = 2 * (v & 1);
+        const saddr b = row + 84u * sb;
+        uint32_t q[8];
+        ld_words_any<8>(b + 16 + 32 * n, q);
+        const uint32_t s4 = ld_s32(b + 4 * v);
+        const uint32_t m0 = 0x03030303u << (2 * j0), m1 = m0 << 2;
+        int S[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            S[k >> 2] = dp4a_us(q[k] & m0, xu.x[k], S[k >> 2]);
+            S[2 + (k >> 2)] = dp4a_us(q[k] & m1, xu.x[8 + k], S[2 + (k >> 2)]);
+        }
+        int A0 = 0, A1 = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            A0 += static_cast<int>((s4 >> (8 * g)) & 15u) * (S[g] >> (2 * j0 + 2 * (g >> 1)));
+            A1 += static_cast<int>((s4 >> (8 * g + 4)) & 15u) * xu.c[g];
+        }
+        return xu.d0 * (ld_h(b + 80) * static_cast<float>(A0) - ld_h(b + 82) * static_cast<float>(A1));
+    } else if constexpr (F == F_Q3_K) {  // (element layout as in load_unit)
         Unit un;
         load_unit<F>(row, u, nb32, un);
         int S[4] = {0, 0, 0, 0};
@@ -671,15 +693,9 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
             S[k >> 2] = __dp4a(static_cast<int>(un.w[k]), static_cast<int>(xu.x[k]), S[k >> 2]);
             S[2 + (k >> 2)] = __dp4a(static_cast<int>(un.w[8 + k]), static_cast<int>(xu.x[8 + k]), S[2 + (k >> 2)]);
         }
-        if constexpr (F == F_Q2_K) {
-            const int A0 = un.sc[0] * S[0] + un.sc[1] * S[1] + un.sc[2] * S[2] + un.sc[3] * S[3];
-            const int A1 = un.mn[0] * xu.c[0] + un.mn[1] * xu.c[1] + un.mn[2] * xu.c[2] + un.mn[3] * xu.c[3];
-            return xu.d0 * (un.da * static_cast<float>(A0) - un.db * static_cast<float>(A1));
-        } else {
-            const int A0 = un.sc[0] * (S[0] - xu.c[0]) + un.sc[1] * (S[1] - xu.c[1]) + un.sc[2] * (S[2] - xu.c[2]) +
-                           un.sc[3] * (S[3] - xu.c[3]);
-            return static_cast<float>(A0) * (xu.d0 * un.da);
-        }
+        const int A0 = un.sc[0] * (S[0] - xu.c[0]) + un.sc[1] * (S[1] - xu.c[1]) + un.sc[2] * (S[2] - xu.c[2]) +
+                       un.sc[3] * (S[3] - xu.c[3]);
+        return static_cast<float>(A0) * (xu.d0 * un.da);
     } else {  // F_Q6_K (element layout as in load_unit)
         const int sb = u >> 2, v = u & 3, h = v >> 1, g1 = v & 1;
         const saddr b = row + 210u * sb;
