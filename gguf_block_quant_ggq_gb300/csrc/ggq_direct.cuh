@@ -518,11 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
     // registers held.
     const auto run = [&](auto rx_tag) {
         constexpr bool RX = decltype(rx_tag)::value;
-        XUnit xa;
-        bool va = false;
+        XUnit xa, xb;
+        bool va = false, vb = false;
         if constexpr (RX) {
             va = lane < units_per_row(K);
+            vb = lane + 32 < units_per_row(K);
             if (va) load_xunit<F>(xs, lane, xa);
+            if (vb) load_xunit<F>(xs, lane + 32, xb);
         }
         int s = 0;
         uint32_t ph = 0u;  // ring slot and phase of the next stage
@@ -549,8 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                     const saddr grow = stage + static_cast<uint32_t>(warp * p.rowbytes);
                     const saddr urow = stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes);
                     if constexpr (RX) {
-                        acc[0] = va ? unit_dot_rx<F>(grow, lane, nb32, xa) : 0.0f;
-                        acc[1] = va ? unit_dot_rx<F>(urow, lane, nb32, xa) : 0.0f;
+                        acc[0] = (va ? unit_dot_rx<F>(grow, lane, nb32, xa) : 0.0f) +
+                                 (vb ? unit_dot_rx<F>(grow, lane + 32, nb32, xb) : 0.0f);
+                        acc[1] = (va ? unit_dot_rx<F>(urow, lane, nb32, xa) : 0.0f) +
+                                 (vb ? unit_dot_rx<F>(urow, lane + 32, nb32, xb) : 0.0f);
                     } else {
                         row_accumulate<F, NT>(grow, xs, xr, np, acc, lane);
                         row_accumulate<F, NT>(urow, xs, xr, np, acc + NT, lane);
@@ -683,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
         }
     };
     if constexpr (KIND == KIND_GATEUP && NT == 1) {
-        if (units_per_row(K) <= 32) run(std::true_type{});
+        if (units_per_row(K) <= 64) run(std::true_type{});
         else run(std::false_type{});
     } else {
         run(std::false_type{});
