@@ -70,6 +70,15 @@ __device__ __forceinline__ void mma_k32_s8(int* d, uint32_t a0, uint32_t a1, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(c0), "r"(c1));
 }
 
+// The same, accumulating into d (exact int32 sums).
+__device__ __forceinline__ void mma_k32_s8_acc(int* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // (a & mask) | c in one LOP3 (mask an immediate, c a register).
 template <uint32_t MASK>
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
@@ -199,7 +208,7 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                     X.b[2 * i] = lo;
                     X.b[2 * i + 1] = hi;
                 }
-                if constexpr (F != F_Q8_0) {
+                if constexpr (F != F_Q8_0 && F != F_Q2_K) {
                     const uint32_t w0 = v0 ? ld_s32(r0 + 260 + 2 * (e >> 4)) : 0u;  // bsums 2js, 2js+1
                     const uint32_t w1 = v1 ? ld_s32(r1 + 260 + 2 * (e >> 4)) : 0u;
                     const int s0 = static_cast<int>(static_cast<int16_t>(w0 & 0xFFFFu)) +
@@ -212,8 +221,8 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                 }
             }
         }
-        if constexpr (F == F_Q4_K || F == F_Q5_K) {
-            // mins product: k slot q <-> 16-group q of the chunk (sub-block q/2)
+        if constexpr (F == F_Q4_K || F == F_Q5_K || F == F_Q2_K) {
+            // mins product: k slot q <-> 16-group q of the chunk (Q4_K/Q5_K: sub-block q/2)
             if (vg) {
                 const int q0 = 2 * t, q1 = 2 * t + 8;  // groups (q0, q0+1) and (q1, q1+1)
                 const int ng = chunk >> 4;
@@ -495,6 +504,58 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         acc[1] = X.dx1 * (d0 * D[1] - dm0 * DM[1]);
         acc[2] = X.dx0 * (d1 * D[2] - dm1 * DM[2]);
         acc[3] = X.dx1 * (d1 * D[3] - dm1 * DM[3]);
+    } else if constexpr (F == F_Q2_K) {
+        // int8 operands: each byte is a 2-bit code times its 16-group's 4-bit scale
+        // (at most 45: one multiply of the masked word by the scale, no carry between
+        // bytes), so one m16n8k32 s8 mma per 32 inputs adds sum_j sc_j S_j exactly;
+        // the mins sum_j m_j bsum_j is one f16 product with k slot q <-> 16-group q
+        // of the chunk (m <= 15 and bsum <= 2032 are exact in f16)
+        const saddr b0 = r0 + 84u * sb, b1 = r1 + 84u * sb;
+        const int is0 = (e0 & 255) >> 5;  // the chunk's first 32-input step in its superblock
+        uint32_t Mr = 0x64006400u;  // the magic exponent in a register
+        asm("" : "+r"(Mr));
+        // (m of groups gi, gi+1) as an f16 pair, gi even; zero past the superblock
+        const auto mpair = [&](saddr blk, int gi) -> uint32_t {
+            if (gi >= 16) return 0u;
+            const uint32_t w = ld_s32(blk + (gi & ~3));
+            const uint32_t k = static_cast<uint32_t>(gi & 3);
+            const uint32_t u = and_or<0x000F000Fu>(prmt(w, 0u, 0x4040u | k | ((k + 1) << 8)) >> 4, Mr);
+            const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&u),
+                                      __halves2half2(__ushort_as_half(0x6400u), __ushort_as_half(0x6400u)));
+            return *reinterpret_cast<const uint32_t*>(&h);
+        };
+        const int gq = 2 * is0 + 2 * t;  // groups of k slots 2t, 2t+1 (and + 8)
+        float DM[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16(DM, mpair(b0, gq), mpair(b1, gq), mpair(b0, gq + 8), mpair(b1, gq + 8), X.bm[0], X.bm[1]);
+        int A[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (32 * i < chunk) {
+                const int is = is0 + i, n = is >> 2, sh = 2 * (is & 3);
+                const uint32_t q = 16u + 32u * static_cast<uint32_t>(n) + 4u * t;
+                const uint32_t s0 = ld_s32(b0 + ((2 * is) & ~3)), s1 = ld_s32(b1 + ((2 * is) & ~3));
+                const int k0 = 8 * ((2 * is) & 3);  // bit offset of group 2is's scale byte
+                const uint32_t sc00 = (s0 >> k0) & 15u, sc01 = (s0 >> (k0 + 8)) & 15u;
+                const uint32_t sc10 = (s1 >> k0) & 15u, sc11 = (s1 >> (k0 + 8)) & 15u;
+                const uint32_t a0 = ((ld_s32(b0 + q) >> sh) & 0x03030303u) * sc00;       // row 2g, group 2is
+                const uint32_t a2 = ((ld_s32(b0 + q + 16) >> sh) & 0x03030303u) * sc01;  // row 2g, group 2is+1
+                const uint32_t a1 = ((ld_s32(b1 + q) >> sh) & 0x03030303u) * sc10;       // row 2g+1
+                const uint32_t a3 = ((ld_s32(b1 + q + 16) >> sh) & 0x03030303u) * sc11;
+                mma_k32_s8_acc(A, a0, a1, a2, a3, X.b[2 * i], X.b[2 * i + 1]);
+            }
+        }
+        if constexpr (DUMP) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dump_add(dz.q[q], 2 * sb, A[q]);
+                dump_add(dz.q[q], 2 * sb + 1, __float2int_rn(DM[q]));
+            }
+        }
+        const float d0 = ld_h(b0 + 80), dm0 = ld_h(b0 + 82), d1 = ld_h(b1 + 80), dm1 = ld_h(b1 + 82);
+        acc[0] = X.dx0 * (d0 * static_cast<float>(A[0]) - dm0 * DM[0]);
+        acc[1] = X.dx1 * (d0 * static_cast<float>(A[1]) - dm0 * DM[1]);
+        acc[2] = X.dx0 * (d1 * static_cast<float>(A[2]) - dm1 * DM[2]);
+        acc[3] = X.dx1 * (d1 * static_cast<float>(A[3]) - dm1 * DM[3]);
     } else if constexpr (F == F_Q6_K) {
         // superblocks are 210 bytes: at an odd index they start 2 bytes off a word
         const uint32_t sbo = 210u * static_cast<uint32_t>(sb);
