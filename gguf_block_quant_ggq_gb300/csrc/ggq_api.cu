@@ -340,9 +340,7 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
 // tokens, except Q8_0 and Q5_K, whose two-token GEMV runs faster on the dp4a
 // streaming kernel (14336 x 4096 rows at two tokens: Q8_0 12.0 against 12.5 us,
 // Q5_K 12.4 against 12.7 us; Q4_K 10.6 against 10.0, Q6_K 16.9 against 14.1).
-// Q3_K never takes it (its signed code times its signed scale does not fit the
-// int8 operands of the path's 2-bit sibling).
-int mma_min_tokens(int f) { return f == F_Q3_K ? 1 << 30 : f == F_Q8_0 || f == F_Q5_K ? 3 : 2; }
+int mma_min_tokens(int f) { return f == F_Q8_0 || f == F_Q5_K ? 3 : 2; }
 
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st, bool a80 = false) {

@@ -11,6 +11,7 @@ cudaError_t launch_mmav(int fmt, const MmavParams& p, int grid, int smem, cudaSt
     case F_Q6_K: return launch_mmav_one<F_Q6_K, false>(p, grid, smem, s);
     case F_MXFP4: return launch_mmav_one<F_MXFP4, false>(p, grid, smem, s);
     case F_Q2_K: return launch_mmav_one<F_Q2_K, false>(p, grid, smem, s);
+    case F_Q3_K: return launch_mmav_one<F_Q3_K, false>(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -198,7 +198,7 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                     // the activation fragment takes the same order
                     X.b[2 * i] = prmt(lo, hi, 0x5140u);
                     X.b[2 * i + 1] = prmt(lo, hi, 0x7362u);
-                } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
+                } else if constexpr (F == F_Q4_K || F == F_Q5_K || F == F_Q3_K) {
                     // f16 fragments; a thread's k slots (2t, 2t+1 | 2t+8, 2t+9) of a
                     // 16-step hold elements (4t, 4t+2 | 4t+1, 4t+3), matching the
                     // weight-side unpack of one 32-bit word
@@ -208,7 +208,7 @@ __device__ __forceinline__ void mmav_load_x(saddr xs, int xrow, int T, int chunk
                     X.b[2 * i] = lo;
                     X.b[2 * i + 1] = hi;
                 }
-                if constexpr (F != F_Q8_0 && F != F_Q2_K) {
+                if constexpr (F != F_Q8_0 && F != F_Q2_K && F != F_Q3_K) {
                     const uint32_t w0 = v0 ? ld_s32(r0 + 260 + 2 * (e >> 4)) : 0u;  // bsums 2js, 2js+1
                     const uint32_t w1 = v1 ? ld_s32(r1 + 260 + 2 * (e >> 4)) : 0u;
                     const int s0 = static_cast<int>(static_cast<int16_t>(w0 & 0xFFFFu)) +
@@ -556,6 +556,92 @@ __device__ __forceinline__ void mmav_chunk(saddr r0, saddr r1, int e0, int chunk
         acc[1] = X.dx1 * (d0 * static_cast<float>(A[1]) - dm0 * DM[1]);
         acc[2] = X.dx0 * (d1 * static_cast<float>(A[2]) - dm1 * DM[2]);
         acc[3] = X.dx1 * (d1 * static_cast<float>(A[3]) - dm1 * DM[3]);
+    } else if constexpr (F == F_Q3_K) {
+        // f16 operands: the code c = low2 + 4 hbit (0..7) taken as the subnormal f16
+        // c 2^-24; one HFMA2 with the 16-group's signed scale s = sc6 - 32 and the
+        // addend -4 s 2^-24 leaves q s 2^-24 with q = c - 4 exactly (|q s| <= 128: a
+        // subnormal multiple of 2^-24, and the fused operation rounds once, from the
+        // exact value).  The scales are in the operands, so one f32 chain per chunk
+        // holds sum_j s_j S_j 2^-24 exactly (|sum| < 2^24 units); the epilogue takes
+        // the factor 2^24 back.  Element order as for Q4_K: a word's bytes (0, 2)
+        // feed k slots (2t, 2t+1), bytes (1, 3) slots (2t+8, 2t+9)
+        const uint32_t sbo = 110u * static_cast<uint32_t>(sb);  // 2 bytes off a word at odd sb
+        const saddr b0 = r0 + sbo, b1 = r1 + sbo;
+        const int is0 = CH == 256 ? 0 : (e0 & 255) >> 5;  // 256-input chunks start at a superblock
+        // the lane's qs words of both 128-element halves n: every 32-input step of
+        // a half reads the same bytes at another shift.  [n][r], r as in w[] below
+        uint32_t W[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const uint32_t q = 32u + 32u * static_cast<uint32_t>(n) + 4u * t;
+            ld_words_any<1>(b0 + q, W[n]);
+            ld_words_any<1>(b0 + q + 16, W[n] + 1);
+            ld_words_any<1>(b1 + q, W[n] + 2);
+            ld_words_any<1>(b1 + q + 16, W[n] + 3);
+        }
+        uint32_t hm[4];  // hmask bytes 4t.. (groups 2is) and 16+4t.. (2is+1), rows 2g and 2g+1
+        ld_words_any<1>(b0 + 4 * t, hm);
+        ld_words_any<1>(b0 + 16 + 4 * t, hm + 1);
+        ld_words_any<1>(b1 + 4 * t, hm + 2);
+        ld_words_any<1>(b1 + 16 + 4 * t, hm + 3);
+        uint32_t sw0[3], sw1[3];  // the 12 packed scale bytes of each row
+        ld_words_any<3>(b0 + 96, sw0);
+        ld_words_any<3>(b1 + 96, sw1);
+        // unsigned 6-bit scales of groups 4v .. 4v+3, one per byte
+        const auto sc6w = [](const uint32_t* w, int v) -> uint32_t {
+            return ((v < 2 ? w[v & 1] : w[v & 1] >> 4) & 0x0F0F0F0Fu) | (((w[2] >> (2 * v)) & 0x03030303u) << 4);
+        };
+        // (s, s) as f16 for byte idx of a scale word: 1024 + sc6 in the mantissa, minus 1056
+        const auto spair = [](uint32_t w, int idx) -> __half2 {
+            const uint32_t u = (prmt(w, 0u, 0x4040u | static_cast<uint32_t>(idx) | (static_cast<uint32_t>(idx) << 8)) &
+                                0x00FF00FFu) | 0x64006400u;
+            return __hsub2(*reinterpret_cast<const __half2*>(&u),
+                           __halves2half2(__ushort_as_half(0x6420u), __ushort_as_half(0x6420u)));
+        };
+        const __half2 m4 = __halves2half2(__ushort_as_half(0x8004u), __ushort_as_half(0x8004u));  // -4 2^-24
+        const auto op = [](uint32_t cbits, __half2 sc, __half2 c4) -> uint32_t {
+            const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&cbits), sc, c4);
+            return *reinterpret_cast<const uint32_t*>(&r);
+        };
+        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (32 * i < chunk) {
+                const int is = is0 + i, j = is & 3, sh = 2 * j, hb = 4 * (is >> 2) + j;
+                // (row 2g, group 2is), (2g, 2is+1), (2g+1, 2is), (2g+1, 2is+1)
+                uint32_t w[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) w[r] = (is >> 2) ? W[1][r] : W[0][r];
+                const int v = is >> 1, k = 2 * (is & 1);  // groups 2is, 2is+1: bytes k, k+1 of word v
+                const uint32_t s0w = sc6w(sw0, v), s1w = sc6w(sw1, v);
+                const __half2 sa0 = spair(s0w, k), sb0 = spair(s0w, k + 1);
+                const __half2 sa1 = spair(s1w, k), sb1 = spair(s1w, k + 1);
+                const __half2 ca0 = __hmul2(sa0, m4), cb0 = __hmul2(sb0, m4);
+                const __half2 ca1 = __hmul2(sa1, m4), cb1 = __hmul2(sb1, m4);
+                uint32_t L[8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {  // r: (row, group) as in w[]
+                    const uint32_t lo = ((w[r] >> sh) & 0x00030003u) | (((hm[r] >> hb) & 0x00010001u) << 2);
+                    const uint32_t hi = ((w[r] >> (sh + 8)) & 0x00030003u) | (((hm[r] >> (hb + 8)) & 0x00010001u) << 2);
+                    const __half2 sc = r == 0 ? sa0 : r == 1 ? sb0 : r == 2 ? sa1 : sb1;
+                    const __half2 c4 = r == 0 ? ca0 : r == 1 ? cb0 : r == 2 ? ca1 : cb1;
+                    // operand index: row (r >> 1), k slots (lo: 0, hi: 1), 16-step (group r & 1)
+                    L[(r >> 1) + 4 * (r & 1)] = op(lo, sc, c4);
+                    L[(r >> 1) + 2 + 4 * (r & 1)] = op(hi, sc, c4);
+                }
+                mma_f16(D, L[0], L[1], L[2], L[3], X.b[4 * i], X.b[4 * i + 1]);
+                mma_f16(D, L[4], L[5], L[6], L[7], X.b[4 * i + 2], X.b[4 * i + 3]);
+            }
+        }
+        if constexpr (DUMP) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dump_add(dz.q[q], sb, __float2int_rn(D[q] * 16777216.0f));  // exact: 2^24
+        }
+        const float d0 = ld_h(b0 + 108) * 16777216.0f, d1 = ld_h(b1 + 108) * 16777216.0f;
+        acc[0] = X.dx0 * (d0 * D[0]);
+        acc[1] = X.dx1 * (d0 * D[1]);
+        acc[2] = X.dx0 * (d1 * D[2]);
+        acc[3] = X.dx1 * (d1 * D[3]);
     } else if constexpr (F == F_Q6_K) {
         // superblocks are 210 bytes: at an odd index they start 2 bytes off a word
         const uint32_t sbo = 210u * static_cast<uint32_t>(sb);
