@@ -120,7 +120,7 @@ if __name__ == "__main__":
                     "Template arguments: k_stream<kind, format, tokens, activation kind, row chunks>, "
                     "k_gemv_mma<format, dump, chunk width>, k_group<kind, format, dump>, "
                     "k_gmm<kind, format, dump>, k_gmmtc<format, dump>, k_direct<kind, format, "
-                    "tokens, dump>; formats 0 Q4_0, 1 Q8_0, 2 Q4_K, 3 Q5_K, 4 Q6_K, 5 MXFP4.\n\n")
+                    "tokens, dump>; formats 0 Q4_0, 1 Q8_0, 2 Q4_K, 3 Q5_K, 4 Q6_K, 5 MXFP4, 6 Q2_K, 7 Q3_K.\n\n")
             f.write(ptxas_summary())
     else:
         print(build(force=True))
