@@ -18,8 +18,8 @@ by one with events around each (which breaks the overlap of consecutive
 launches) are reported beside it.
 
 Secondary lines (same JSON, "workloads"): the Q4_0 1024 x 4096 GEMV, the
-Q2_K and Q3_K GEMV on the 14336 x 4096 shape (1 and 8 tokens), the
-4096 x 14336 long-row GEMV (Q8_0, Q6_K at 1 and 8 tokens), the MoE decode
+4096 x 14336 long-row GEMV (Q8_0, Q6_K at 1 and 8 tokens), the Q2_K and Q3_K
+GEMV on the 14336 x 4096 shape (1 and 8 tokens), the MoE decode
 layer (128 experts, H 2048, I 768, Q4_K gate/up, Q6_K down, top-8, 1-4
 tokens), the MXFP4 routed experts (256 experts, H 4096, I 2048, top-8, 1-512
 tokens) and the 4096-token prefill layer; MoE GB/s counts the distinct
@@ -560,32 +560,6 @@ def secondary_workloads(ctx, rt, hbm_peak):
                                      "us_per_call": round(ms * 1e3 / len(copies), 2)}
     del copies
 
-    # the 2- and 3-bit K-quants on the headline shape (14336 x 4096) at T = 1 and 8
-    # (the dp4a streaming kernel at every token count); 4 rotating copies > 2x L2
-    ctx.set_static_weights(True)
-    N2, K2 = syn.GEMV_KQUANT["N"], syn.GEMV_KQUANT["K"]
-    ctx.reserve(max_tokens=8, max_k=K2)
-    for fmt in ("Q2_K", "Q3_K"):
-        g2 = syn.rng(syn.GEMV_KQUANT["index"], 400 + syn.WEIGHT_FORMATS.index(fmt))
-        lc = [torch.from_numpy(syn.weights(fmt, N2, K2, g2)).cuda() for _ in range(4)]
-        for T in (1, 8):
-            x2 = torch.from_numpy(syn.activations(T, K2, g2)).cuda()
-            xq2 = torch.empty((T, syn.row_bytes("Q8_K", K2)), dtype=torch.uint8, device="cuda")
-            ctx.quantize_act("Q8_K", x2, out=xq2)
-            y2 = torch.empty((T, N2), dtype=torch.float32, device="cuda")
-            torch.cuda.synchronize()
-
-            def lowbit():
-                for Wc in lc:
-                    ctx.mul_mat_vec_q(fmt, Wc, N2, K2, xq2, T, Y=y2)
-
-            ms = _graph_time(lowbit, 10, rt, stream)
-            bytes_ = len(lc) * N2 * syn.row_bytes(fmt, K2)
-            out[f"{fmt.lower()}_gemv_{N2}x{K2}_T{T}"] = {
-                "GBps": round(bytes_ / (ms / 1e3) / 1e9, 1), "frac": round(bytes_ / (ms / 1e3) / 1e9 / hbm_peak, 4),
-                "us_per_call": round(ms * 1e3 / len(lc), 2)}
-        del lc
-
     # long rows: the 4096 x 14336 down-projection shape at T = 1 and 8 (rows of
     # 15232 B in Q8_0, 11760 B in Q6_K stream in row chunks); 3 rotating copies
     ctx.set_static_weights(True)
@@ -611,6 +585,33 @@ def secondary_workloads(ctx, rt, hbm_peak):
                 "GBps": round(bytes_ / (ms / 1e3) / 1e9, 1), "frac": round(bytes_ / (ms / 1e3) / 1e9 / hbm_peak, 4),
                 "us_per_call": round(ms * 1e3 / len(lcopies), 2)}
         del lcopies
+
+    # the 2- and 3-bit K-quants on the headline shape (14336 x 4096) at T = 1 and 8
+    # (the dp4a streaming kernel at every token count); 4 rotating copies > 2x L2
+    ctx.set_static_weights(True)
+    N2, K2 = syn.GEMV_KQUANT["N"], syn.GEMV_KQUANT["K"]
+    ctx.reserve(max_tokens=8, max_k=K2)
+    for fmt in ("Q2_K", "Q3_K"):
+        g2 = syn.rng(syn.GEMV_KQUANT["index"], 400 + syn.WEIGHT_FORMATS.index(fmt))
+        lc = [torch.from_numpy(syn.weights(fmt, N2, K2, g2)).cuda() for _ in range(4)]
+        for T in (1, 8):
+            x2 = torch.from_numpy(syn.activations(T, K2, g2)).cuda()
+            xq2 = torch.empty((T, syn.row_bytes("Q8_K", K2)), dtype=torch.uint8, device="cuda")
+            ctx.quantize_act("Q8_K", x2, out=xq2)
+            y2 = torch.empty((T, N2), dtype=torch.float32, device="cuda")
+            torch.cuda.synchronize()
+
+            def lowbit():
+                for Wc in lc:
+                    ctx.mul_mat_vec_q(fmt, Wc, N2, K2, xq2, T, Y=y2)
+
+            ms = _graph_time(lowbit, 10, rt, stream)
+            bytes_ = len(lc) * N2 * syn.row_bytes(fmt, K2)
+            out[f"{fmt.lower()}_gemv_{N2}x{K2}_T{T}"] = {
+                "GBps": round(bytes_ / (ms / 1e3) / 1e9, 1), "frac": round(bytes_ / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                "us_per_call": round(ms * 1e3 / len(lc), 2)}
+        del lc
+    torch.cuda.empty_cache()
 
     # MoE layers: rotate seeded router-logit sets so the expert sets differ per call
     ctx.set_static_weights(True)
