@@ -33,6 +33,8 @@ CALLS = [  # (fmt, N, K, T), run one after the other
     ("Q5_K", 61, 1024, 1),
     ("Q4_0", 77, 1024, 3),
     ("Q8_0", 37, 14336, 2),         # rows too long for whole-row stages: row chunks
+    ("Q2_K", 16 * 6 + 1, 4096, 3),
+    ("Q3_K", 45, 2048, 1),
 ]
 
 
