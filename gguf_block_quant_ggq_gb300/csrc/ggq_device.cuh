@@ -685,17 +685,36 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         }
         return xu.d0 * (ld_h(b + 80) * static_cast<float>(A0) - ld_h(b + 82) * static_cast<float>(A1));
     } else if constexpr (F == F_Q3_K) {  // (element layout as in load_unit)
-        Unit un;
-        load_unit<F>(row, u, nb32, un);
-        int S[4] = {0, 0, 0, 0};
+        // the two low bits masked in place (4^j times their value) and the high bit
+        // in place (2^hb times it), each in a dp4a of its own; the exact factors are
+        // shifted out of each group's sums: S' = S_low / 4^j + 4 S_high / 2^hb is the
+        // sum of (q + 4) x, and c[] holds 4 * sum(x) per group
+        const int sb = u >> 2, v = u & 3, n = v >> 1, j0 = 2 * (v & 1);
+        const saddr b = row + 110u * sb;
+        uint32_t q[8], hm[8], sw[2];
+        ld_words_any<8>(b + 32 + 32 * n, q);
+        ld_words_any<8>(b, hm);
+        ld_words_any<1>(b + 96 + 4 * (v & 1), sw);
+        ld_words_any<1>(b + 104, sw + 1);
+        const uint32_t sc6 = ((v < 2 ? sw[0] : sw[0] >> 4) & 0x0F0F0F0Fu) | (((sw[1] >> (2 * v)) & 0x03030303u) << 4);
+        const int hb = 4 * n + j0;
+        const uint32_t m0 = 0x03030303u << (2 * j0), m1 = m0 << 2;
+        const uint32_t h0 = 0x01010101u << hb, h1 = h0 << 1;
+        int L[4] = {0, 0, 0, 0}, H[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            S[k >> 2] = __dp4a(static_cast<int>(un.w[k]), static_cast<int>(xu.x[k]), S[k >> 2]);
-            S[2 + (k >> 2)] = __dp4a(static_cast<int>(un.w[8 + k]), static_cast<int>(xu.x[8 + k]), S[2 + (k >> 2)]);
+            L[k >> 2] = dp4a_us(q[k] & m0, xu.x[k], L[k >> 2]);
+            L[2 + (k >> 2)] = dp4a_us(q[k] & m1, xu.x[8 + k], L[2 + (k >> 2)]);
+            H[k >> 2] = dp4a_us(hm[k] & h0, xu.x[k], H[k >> 2]);
+            H[2 + (k >> 2)] = dp4a_us(hm[k] & h1, xu.x[8 + k], H[2 + (k >> 2)]);
         }
-        const int A0 = un.sc[0] * (S[0] - xu.c[0]) + un.sc[1] * (S[1] - xu.c[1]) + un.sc[2] * (S[2] - xu.c[2]) +
-                       un.sc[3] * (S[3] - xu.c[3]);
-        return static_cast<float>(A0) * (xu.d0 * un.da);
+        int A0 = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int Sg = (L[g] >> (2 * j0 + 2 * (g >> 1))) + 4 * (H[g] >> (hb + (g >> 1)));
+            A0 += (static_cast<int>((sc6 >> (8 * g)) & 0xFFu) - 32) * (Sg - xu.c[g]);
+        }
+        return static_cast<float>(A0) * (xu.d0 * ld_h(b + 108));
     } else {  // F_Q6_K (element layout as in load_unit)
         const int sb = u >> 2, v = u & 3, h = v >> 1, g1 = v & 1;
         const saddr b = row + 210u * sb;
