@@ -725,14 +725,22 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         const int sc0 = ld_s8(b + 192 + j0), sc1 = ld_s8(b + 192 + j0 + 1);
         const int sc2 = ld_s8(b + 192 + j0 + 4), sc3 = ld_s8(b + 192 + j0 + 5);
         const float da = ld_h(b + 208);
-        int S[4] = {0, 0, 0, 0};
+        // nibbles and high bit pairs masked in place, each in a dp4a of its own (high
+        // nibbles 16x, high pairs 4^g1 and 4^(g1+2) times their value); the exact
+        // factors are shifted out of each group's sums
+        const uint32_t m0 = 0x03030303u << (2 * g1), m1 = m0 << 4;
+        int N[4] = {0, 0, 0, 0}, P[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint32_t lo = (ql[k] & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1)) & 0x03030303u) << 4);
-            const uint32_t hi = ((ql[k] >> 4) & 0x0F0F0F0Fu) | (((qh[k] >> (2 * g1 + 4)) & 0x03030303u) << 4);
-            S[k >> 2] = __dp4a(static_cast<int>(lo), static_cast<int>(xu.x[k]), S[k >> 2]);
-            S[2 + (k >> 2)] = __dp4a(static_cast<int>(hi), static_cast<int>(xu.x[8 + k]), S[2 + (k >> 2)]);
+            N[k >> 2] = __dp4a(static_cast<int>(ql[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[k]), N[k >> 2]);
+            N[2 + (k >> 2)] = dp4a_us(ql[k] & 0xF0F0F0F0u, xu.x[8 + k], N[2 + (k >> 2)]);
+            P[k >> 2] = dp4a_us(qh[k] & m0, xu.x[k], P[k >> 2]);
+            P[2 + (k >> 2)] = dp4a_us(qh[k] & m1, xu.x[8 + k], P[2 + (k >> 2)]);
         }
+        int S[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            S[g] = (g < 2 ? N[g] : N[g] >> 4) + 16 * (P[g] >> (2 * g1 + (g < 2 ? 0 : 4)));
         const int A0 = sc0 * (S[0] - xu.c[0]) + sc1 * (S[1] - xu.c[1]) + sc2 * (S[2] - xu.c[2]) + sc3 * (S[3] - xu.c[3]);
         return static_cast<float>(A0) * (xu.d0 * da);
     }
