@@ -540,13 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                 const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
                 const int np = plan->npairs[u];
                 int xr[NT];
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->tok[plan->pair[u][t]] : 0;
                 const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
                 const int64_t row = static_cast<int64_t>(tile) * kTileRows + warp;
                 if (ready) {
                     float acc[2 * NT];
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.0f;
                     const saddr grow = stage + static_cast<uint32_t>(warp * p.rowbytes);
                     const saddr urow = stage + static_cast<uint32_t>((kTileRows + warp) * p.rowbytes);
@@ -595,12 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                     const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
                     const int np = plan->npairs[u];
                     int xr[NT];
-    #pragma unroll
+#pragma unroll
                     for (int t = 0; t < NT; ++t) xr[t] = t < np ? plan->pair[u][t] : 0;
                     if (ready && ok) {
                         const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
                         float acc[NT];
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < NT; ++i) acc[i] = 0.0f;
                         row_accumulate<F, NT>(stage + static_cast<uint32_t>(warp * p.rowbytes), xs, xr, np, acc, lane);
                         const float v = warp_transpose_reduce<LV>(acc, lane);  // lane >> SH = slot
@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                         // move each slot's weighted value to the lane of its token
                         const float contrib = pp >= 0 ? plan->wt[pp] * v : 0.0f;
                         const int tok = pp >= 0 ? plan->tok[pp] : -1;
-    #pragma unroll
+#pragma unroll
                         for (int q = 0; q < NT; ++q) {
                             const float cq = __shfl_sync(0xffffffffu, contrib, q << SH);
                             const int tq = __shfl_sync(0xffffffffu, tok, q << SH);
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                 // each lane adding the weighted partials of its units into its token sums
                 const int64_t row = static_cast<int64_t>(item) * kTileRows + warp;
                 float acc[NT];
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
                 bool ok = true;
                 for (int ug = 0; ug < D; ug += p.G) {
@@ -646,27 +646,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                     if (ready && ok) {
                         const int gc = D - ug < p.G ? D - ug : p.G;
                         const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
-    #pragma unroll
-                        for (int i = 0; i < kDownUnits; ++i) {
-                            if (vg[i] < gc) {
-                                const int g = vg[i], ur = vu[i], u = ug + g;
-                                const int np = plan->npairs[u];
+                        if constexpr (NT == 1) {
+                            // one token: each expert's pair reads its activation unit into
+                            // registers and takes the register-resident dot (the same integers
+                            // and epilogue as the path below, fewer instructions); the lane's
+                            // units walked in a rolled loop (v = lane + 32 i = g nu + ur)
+                            const int nu = units_per_row(K), q32 = 32 / nu, r32 = 32 - q32 * nu;
+                            int g = lane / nu, ur = lane - g * nu;
+#pragma unroll 1
+                            for (int i = 0; i < kDownUnits && g < gc; ++i) {
+                                const int u = ug + g;
+                                const int pr = plan->pair[u][0];
                                 const saddr rowp = stage + static_cast<uint32_t>((g * kTileRows + warp) * p.rowbytes);
-                                Unit un;
-                                load_unit<F>(rowp, ur, nb32, un);
-                                int xo[4];
-                                unit_offsets<F>(ur, xo);
-    #pragma unroll
-                                for (int jj = 0; jj < NT; ++jj) {
-                                    if (jj < np) {
-                                        const int pr = plan->pair[u][jj];
-                                        int A0, A1;
-                                        unit_ints<F>(un, xo, xs, pr, ur, A0, A1);
-                                        const float val = plan->wt[pr] * unit_value<F>(un, xs, pr, ur, A0, A1);
-                                        const int tk = plan->tok[pr];
-    #pragma unroll
-                                        for (int t = 0; t < NT; ++t)
-                                            if (t == tk) acc[t] += val;
+                                XS xp = xs;
+                                xp.q = xs.q + static_cast<uint32_t>(pr * xq_row_bytes(K));
+                                xp.d = xs.d + 4u * static_cast<uint32_t>(pr * (K >> 8));
+                                xp.s32 = xs.s32 + 4u * static_cast<uint32_t>(pr * (K >> 5));
+                                xp.bs = xs.bs + 2u * static_cast<uint32_t>(pr * (K >> 4));
+                                XUnit xu;
+                                load_xunit<F>(xp, ur, xu);
+                                acc[0] += plan->wt[pr] * unit_dot_rx<F>(rowp, ur, nb32, xu);
+                                g += q32;
+                                ur += r32;
+                                if (ur >= nu) {
+                                    ur -= nu;
+                                    ++g;
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < kDownUnits; ++i) {
+                                if (vg[i] < gc) {
+                                    const int g = vg[i], ur = vu[i], u = ug + g;
+                                    const int np = plan->npairs[u];
+                                    const saddr rowp = stage + static_cast<uint32_t>((g * kTileRows + warp) * p.rowbytes);
+                                    Unit un;
+                                    load_unit<F>(rowp, ur, nb32, un);
+                                    int xo[4];
+                                    unit_offsets<F>(ur, xo);
+#pragma unroll
+                                    for (int jj = 0; jj < NT; ++jj) {
+                                        if (jj < np) {
+                                            const int pr = plan->pair[u][jj];
+                                            int A0, A1;
+                                            unit_ints<F>(un, xo, xs, pr, ur, A0, A1);
+                                            const float val = plan->wt[pr] * unit_value<F>(un, xs, pr, ur, A0, A1);
+                                            const int tk = plan->tok[pr];
+#pragma unroll
+                                            for (int t = 0; t < NT; ++t)
+                                                if (t == tk) acc[t] += val;
+                                        }
                                     }
                                 }
                             }
