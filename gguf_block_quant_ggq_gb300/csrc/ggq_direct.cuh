@@ -555,6 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                                  (vb ? unit_dot_rx<F>(grow, lane + 32, nb32, xb) : 0.0f);
                         acc[1] = (va ? unit_dot_rx<F>(urow, lane, nb32, xa) : 0.0f) +
                                  (vb ? unit_dot_rx<F>(urow, lane + 32, nb32, xb) : 0.0f);
+                    } else if (np == 1) {
+                        // the expert's only pair: its token's activation units in registers
+                        // and the register-resident dot (the same integers and epilogue as
+                        // the generic path below, fewer instructions)
+                        const int nu = units_per_row(K), r = xr[0];
+                        XS xp = xs;
+                        xp.q = xs.q + static_cast<uint32_t>(r * xq_row_bytes(K));
+                        xp.d = xs.d + 4u * static_cast<uint32_t>(r * (K >> 8));
+                        xp.s32 = xs.s32 + 4u * static_cast<uint32_t>(r * (K >> 5));
+                        xp.bs = xs.bs + 2u * static_cast<uint32_t>(r * (K >> 4));
+                        float ag = 0.0f, au = 0.0f;
+                        for (int v = lane; v < nu; v += 32) {
+                            XUnit xu;
+                            load_xunit<F>(xp, v, xu);
+                            ag += unit_dot_rx<F>(grow, v, nb32, xu);
+                            au += unit_dot_rx<F>(urow, v, nb32, xu);
+                        }
+                        acc[0] = ag;
+                        acc[NT] = au;
                     } else {
                         row_accumulate<F, NT>(grow, xs, xr, np, acc, lane);
                         row_accumulate<F, NT>(urow, xs, xr, np, acc + NT, lane);
@@ -680,6 +699,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_direct(const DirectParams p) {
                                     const int g = vg[i], ur = vu[i], u = ug + g;
                                     const int np = plan->npairs[u];
                                     const saddr rowp = stage + static_cast<uint32_t>((g * kTileRows + warp) * p.rowbytes);
+                                    if (np == 1) {  // the expert's only pair: the register-resident dot
+                                        const int pr = plan->pair[u][0];
+                                        XS xp = xs;
+                                        xp.q = xs.q + static_cast<uint32_t>(pr * xq_row_bytes(K));
+                                        xp.d = xs.d + 4u * static_cast<uint32_t>(pr * (K >> 8));
+                                        xp.s32 = xs.s32 + 4u * static_cast<uint32_t>(pr * (K >> 5));
+                                        xp.bs = xs.bs + 2u * static_cast<uint32_t>(pr * (K >> 4));
+                                        XUnit xu;
+                                        load_xunit<F>(xp, ur, xu);
+                                        const float val = plan->wt[pr] * unit_dot_rx<F>(rowp, ur, nb32, xu);
+                                        const int tk = plan->tok[pr];
+#pragma unroll
+                                        for (int t = 0; t < NT; ++t)
+                                            if (t == tk) acc[t] += val;
+                                        continue;
+                                    }
                                     Unit un;
                                     load_unit<F>(rowp, ur, nb32, un);
                                     int xo[4];
