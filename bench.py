@@ -420,7 +420,7 @@ def run_gpu(args, rank, world):
     iso_achieved = sum_alg / (sum(isolated.values()) / 1e3) / 1e9
     # which kernel the library runs for (format, tokens): the dp4a streaming kernel at
     # one token and, for Q8_0 and Q5_K, at two; the tensor-path GEMV otherwise
-    streamed = [k for k in chain if k[1] == 1 or (k[1] == 2 and k[0] in ("Q8_0", "Q5_K"))]
+    streamed = [k for k in chain if k[1] <= 2]
     fam = {"k_gemv_mma": [k for k in chain if k not in streamed], "k_stream": streamed}
     families = {name: round(sum(alg_bytes[k] for k in ks) / (sum(chain[k] for k in ks) / 1e3) / 1e9 / hbm_peak, 4)
                 for name, ks in fam.items()}
@@ -487,8 +487,8 @@ def run_gpu(args, rank, world):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": round(sum_alg / len(chain)),
-                         "kernel": "decode GEMV kernels (k_stream dp4a at T=1 and Q8_0/Q5_K T=2, k_gemv_mma tensor "
-                                   "path otherwise): "
+                         "kernel": "decode GEMV kernels (k_stream dp4a at T=1 and 2, k_gemv_mma tensor "
+                                   "path at T=4 and 8): "
                                    "all 16 launches of a step; algorithmic bytes = packed W + Q8_K x + fp32 y",
                          "traffic_source": "mean dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch of "
                                            "one step (ncu; profiles/traffic_kquant_gemv_step.json), null when the "

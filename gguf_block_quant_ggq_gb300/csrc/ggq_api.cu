@@ -336,12 +336,12 @@ bool plan_mmav(int f, MmavParams& p, int* smem) {
     return true;
 }
 
-// Smallest token count that the decode GEMV sends to the tensor path: from two
-// tokens, except Q8_0, Q5_K, Q2_K and Q3_K, whose two-token GEMV runs faster on
-// the dp4a streaming kernel (14336 x 4096 rows at two tokens: Q8_0 12.0 against
-// 12.5 us, Q5_K 12.4 against 12.7, Q2_K 11.6 against 11.75, Q3_K 13.9 against
-// 15.0; Q4_K 10.6 against 10.0, Q6_K 16.9 against 14.1).
-int mma_min_tokens(int f) { return f == F_Q8_0 || f == F_Q5_K || f == F_Q2_K || f == F_Q3_K ? 3 : 2; }
+// Smallest token count that the decode GEMV sends to the tensor path: three.
+// At two tokens the dp4a streaming kernel keeps both tokens' activations in
+// registers and measured faster for every format (14336 x 4096 rows, chains of
+// launches: Q4_K 8.9 against 10.2 us, Q5_K 10.4 against 12.5 (activations
+// staged in shared memory), Q6_K 12.5 against 14.3, Q8_0 11.6 against 12.2).
+int mma_min_tokens(int) { return 3; }
 
 ggq_status launch_gemv_kind(ggq_ctx* c, int kind, int w, const void* W, int64_t N, int64_t K, const void* Xq,
                             int64_t T, float* Y, int32_t* coefs, cudaStream_t st, bool a80 = false) {

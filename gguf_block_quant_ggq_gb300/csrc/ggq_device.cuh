@@ -550,12 +550,14 @@ __device__ __forceinline__ void load_xunit(const XS& xs, int u, XUnit& xu) {
     }
 }
 
-// fp32 contribution of unit u of a row (shared memory) against one token's
-// register-resident activations.  High nibbles are masked in place (16x their
-// value, as unsigned bytes) and the exact factor 16 is shifted out of the
-// integer sum, which saves a shift per weight word.
-template <int F, bool A32 = (F == F_Q4_0)>
-__device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const XUnit& xu) {
+// fp32 contributions of unit u of a row (shared memory) against NX tokens'
+// register-resident activations xu[0..NX-1]: the weights are loaded and masked
+// once, each token takes its own dp4a chains and epilogue (per token the same
+// integers and operation order whatever NX).  High nibbles are masked in place
+// (16x their value, as unsigned bytes) and the exact factor 16 is shifted out
+// of the integer sum, which saves a shift per weight word.
+template <int F, bool A32, int NX>
+__device__ __forceinline__ void unit_dot_rxn(saddr row, int u, int nb32, const XUnit* xu, float* out) {
     if constexpr (F == F_Q4_0) {
         const saddr b = row + 36u * u;
         const bool two = 2 * u + 1 < nb32;
@@ -570,17 +572,27 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
 #pragma unroll
             for (int k = 0; k < 4; ++k) q1[k] = 0u;
         }
-        int l0 = 0, h0 = 0, l1 = 0, h1 = 0;
+        int l0[NX], h0[NX], l1[NX], h1[NX];
+#pragma unroll
+        for (int i = 0; i < NX; ++i) l0[i] = h0[i] = l1[i] = h1[i] = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            l0 = __dp4a(static_cast<int>(q0[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[k]), l0);
-            h0 = dp4a_us(q0[k] & 0xF0F0F0F0u, xu.x[4 + k], h0);
-            l1 = __dp4a(static_cast<int>(q1[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[8 + k]), l1);
-            h1 = dp4a_us(q1[k] & 0xF0F0F0F0u, xu.x[12 + k], h1);
+            const uint32_t wl0 = q0[k] & 0x0F0F0F0Fu, wh0 = q0[k] & 0xF0F0F0F0u;
+            const uint32_t wl1 = q1[k] & 0x0F0F0F0Fu, wh1 = q1[k] & 0xF0F0F0F0u;
+#pragma unroll
+            for (int i = 0; i < NX; ++i) {
+                l0[i] = __dp4a(static_cast<int>(wl0), static_cast<int>(xu[i].x[k]), l0[i]);
+                h0[i] = dp4a_us(wh0, xu[i].x[4 + k], h0[i]);
+                l1[i] = __dp4a(static_cast<int>(wl1), static_cast<int>(xu[i].x[8 + k]), l1[i]);
+                h1[i] = dp4a_us(wh1, xu[i].x[12 + k], h1[i]);
+            }
         }
-        const int A0 = l0 + (h0 >> 4) - xu.c[0];
-        const int A1 = l1 + (h1 >> 4) - xu.c[1];
-        return static_cast<float>(A0) * (da * xu.d0) + static_cast<float>(A1) * (db * xu.d1);
+#pragma unroll
+        for (int i = 0; i < NX; ++i) {
+            const int A0 = l0[i] + (h0[i] >> 4) - xu[i].c[0];
+            const int A1 = l1[i] + (h1[i] >> 4) - xu[i].c[1];
+            out[i] = static_cast<float>(A0) * (da * xu[i].d0) + static_cast<float>(A1) * (db * xu[i].d1);
+        }
     } else if constexpr (F == F_Q8_0) {
         const saddr b = row + 68u * u;
         const bool two = 2 * u + 1 < nb32;
@@ -595,14 +607,22 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
 #pragma unroll
             for (int k = 8; k < 16; ++k) w[k] = 0u;
         }
-        int S0 = 0, S1 = 0;
+        int S0[NX], S1[NX];
+#pragma unroll
+        for (int i = 0; i < NX; ++i) S0[i] = S1[i] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            S0 = __dp4a(static_cast<int>(w[k]), static_cast<int>(xu.x[k]), S0);
-            S1 = __dp4a(static_cast<int>(w[8 + k]), static_cast<int>(xu.x[8 + k]), S1);
+#pragma unroll
+            for (int i = 0; i < NX; ++i) {
+                S0[i] = __dp4a(static_cast<int>(w[k]), static_cast<int>(xu[i].x[k]), S0[i]);
+                S1[i] = __dp4a(static_cast<int>(w[8 + k]), static_cast<int>(xu[i].x[8 + k]), S1[i]);
+            }
         }
-        if constexpr (A32) return static_cast<float>(S0) * (da * xu.d0) + static_cast<float>(S1) * (db * xu.d1);
-        return xu.d0 * (static_cast<float>(S0) * da + static_cast<float>(S1) * db);
+#pragma unroll
+        for (int i = 0; i < NX; ++i) {
+            if constexpr (A32) out[i] = static_cast<float>(S0[i]) * (da * xu[i].d0) + static_cast<float>(S1[i]) * (db * xu[i].d1);
+            else out[i] = xu[i].d0 * (static_cast<float>(S0[i]) * da + static_cast<float>(S1[i]) * db);
+        }
     } else if constexpr (F == F_MXFP4) {
         const saddr b = row + 34u * u;
         const bool two = 2 * u + 1 < nb32;
@@ -617,15 +637,24 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
 #pragma unroll
             for (int k = 0; k < 4; ++k) q1[k] = 0u;
         }
-        int S0 = 0, S1 = 0;
+        int S0[NX], S1[NX];
+#pragma unroll
+        for (int i = 0; i < NX; ++i) S0[i] = S1[i] = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            S0 = __dp4a(static_cast<int>(mx_lookup(q0[k] & 0xFFFFu)), static_cast<int>(xu.x[2 * k]), S0);
-            S0 = __dp4a(static_cast<int>(mx_lookup(q0[k] >> 16)), static_cast<int>(xu.x[2 * k + 1]), S0);
-            S1 = __dp4a(static_cast<int>(mx_lookup(q1[k] & 0xFFFFu)), static_cast<int>(xu.x[8 + 2 * k]), S1);
-            S1 = __dp4a(static_cast<int>(mx_lookup(q1[k] >> 16)), static_cast<int>(xu.x[8 + 2 * k + 1]), S1);
+            const int a0 = static_cast<int>(mx_lookup(q0[k] & 0xFFFFu)), a1 = static_cast<int>(mx_lookup(q0[k] >> 16));
+            const int b0 = static_cast<int>(mx_lookup(q1[k] & 0xFFFFu)), b1 = static_cast<int>(mx_lookup(q1[k] >> 16));
+#pragma unroll
+            for (int i = 0; i < NX; ++i) {
+                S0[i] = __dp4a(a0, static_cast<int>(xu[i].x[2 * k]), S0[i]);
+                S0[i] = __dp4a(a1, static_cast<int>(xu[i].x[2 * k + 1]), S0[i]);
+                S1[i] = __dp4a(b0, static_cast<int>(xu[i].x[8 + 2 * k]), S1[i]);
+                S1[i] = __dp4a(b1, static_cast<int>(xu[i].x[8 + 2 * k + 1]), S1[i]);
+            }
         }
-        return xu.d0 * (static_cast<float>(S0 - xu.c[0]) * da + static_cast<float>(S1 - xu.c[1]) * db);
+#pragma unroll
+        for (int i = 0; i < NX; ++i)
+            out[i] = xu[i].d0 * (static_cast<float>(S0[i] - xu[i].c[0]) * da + static_cast<float>(S1[i] - xu[i].c[1]) * db);
     } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
         const int sb = u >> 2, cc = u & 3;
         const saddr b = row + (F == F_Q4_K ? 144u : 176u) * sb;
@@ -640,28 +669,42 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         const int s0 = (scw >> sh) & 0xFF, s1 = (scw >> (sh + 8)) & 0xFF;
         const int m0 = (mw >> sh) & 0xFF, m1 = (mw >> (sh + 8)) & 0xFF;
         const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-        int lo = 0, hi = 0;
+        int lo[NX], hi[NX];
+#pragma unroll
+        for (int i = 0; i < NX; ++i) lo[i] = hi[i] = 0;
         if constexpr (F == F_Q4_K) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                lo = __dp4a(static_cast<int>(q[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[k]), lo);
-                hi = dp4a_us(q[k] & 0xF0F0F0F0u, xu.x[8 + k], hi);
+                const uint32_t wl = q[k] & 0x0F0F0F0Fu, wh = q[k] & 0xF0F0F0F0u;
+#pragma unroll
+                for (int i = 0; i < NX; ++i) {
+                    lo[i] = __dp4a(static_cast<int>(wl), static_cast<int>(xu[i].x[k]), lo[i]);
+                    hi[i] = dp4a_us(wh, xu[i].x[8 + k], hi[i]);
+                }
             }
-            hi >>= 4;
+#pragma unroll
+            for (int i = 0; i < NX; ++i) hi[i] >>= 4;
         } else {
             const uint4 ha = ld_s128(b + 16), hb = ld_s128(b + 32);
             const uint32_t hq[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t h = hq[k] >> (2 * cc);
-                lo = __dp4a(static_cast<int>((q[k] & 0x0F0F0F0Fu) | ((h << 4) & 0x10101010u)), static_cast<int>(xu.x[k]), lo);
-                hi = __dp4a(static_cast<int>(((q[k] >> 4) & 0x0F0F0F0Fu) | ((h << 3) & 0x10101010u)),
-                            static_cast<int>(xu.x[8 + k]), hi);
+                const int wl = static_cast<int>((q[k] & 0x0F0F0F0Fu) | ((h << 4) & 0x10101010u));
+                const int wh = static_cast<int>(((q[k] >> 4) & 0x0F0F0F0Fu) | ((h << 3) & 0x10101010u));
+#pragma unroll
+                for (int i = 0; i < NX; ++i) {
+                    lo[i] = __dp4a(wl, static_cast<int>(xu[i].x[k]), lo[i]);
+                    hi[i] = __dp4a(wh, static_cast<int>(xu[i].x[8 + k]), hi[i]);
+                }
             }
         }
-        const int A0 = s0 * lo + s1 * hi;
-        const int A1 = m0 * xu.c[0] + m1 * xu.c[1];
-        return xu.d0 * (da * static_cast<float>(A0) - dm * static_cast<float>(A1));
+#pragma unroll
+        for (int i = 0; i < NX; ++i) {
+            const int A0 = s0 * lo[i] + s1 * hi[i];
+            const int A1 = m0 * xu[i].c[0] + m1 * xu[i].c[1];
+            out[i] = xu[i].d0 * (da * static_cast<float>(A0) - dm * static_cast<float>(A1));
+        }
     } else if constexpr (F == F_Q2_K) {  // (element layout as in load_unit)
         // each 2-bit field is masked in place (4^j times its value, as unsigned
         // bytes) and the exact factor is shifted out of the group's integer sum
@@ -671,19 +714,29 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         ld_words_any<8>(b + 16 + 32 * n, q);
         const uint32_t s4 = ld_s32(b + 4 * v);
         const uint32_t m0 = 0x03030303u << (2 * j0), m1 = m0 << 2;
-        int S[4] = {0, 0, 0, 0};
+        int S[NX][4];
+#pragma unroll
+        for (int i = 0; i < NX; ++i) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            S[k >> 2] = dp4a_us(q[k] & m0, xu.x[k], S[k >> 2]);
-            S[2 + (k >> 2)] = dp4a_us(q[k] & m1, xu.x[8 + k], S[2 + (k >> 2)]);
-        }
-        int A0 = 0, A1 = 0;
+            const uint32_t w0 = q[k] & m0, w1 = q[k] & m1;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            A0 += static_cast<int>((s4 >> (8 * g)) & 15u) * (S[g] >> (2 * j0 + 2 * (g >> 1)));
-            A1 += static_cast<int>((s4 >> (8 * g + 4)) & 15u) * xu.c[g];
+            for (int i = 0; i < NX; ++i) {
+                S[i][k >> 2] = dp4a_us(w0, xu[i].x[k], S[i][k >> 2]);
+                S[i][2 + (k >> 2)] = dp4a_us(w1, xu[i].x[8 + k], S[i][2 + (k >> 2)]);
+            }
         }
-        return xu.d0 * (ld_h(b + 80) * static_cast<float>(A0) - ld_h(b + 82) * static_cast<float>(A1));
+        const float dq = ld_h(b + 80), dmin = ld_h(b + 82);
+#pragma unroll
+        for (int i = 0; i < NX; ++i) {
+            int A0 = 0, A1 = 0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                A0 += static_cast<int>((s4 >> (8 * g)) & 15u) * (S[i][g] >> (2 * j0 + 2 * (g >> 1)));
+                A1 += static_cast<int>((s4 >> (8 * g + 4)) & 15u) * xu[i].c[g];
+            }
+            out[i] = xu[i].d0 * (dq * static_cast<float>(A0) - dmin * static_cast<float>(A1));
+        }
     } else if constexpr (F == F_Q3_K) {  // (element layout as in load_unit)
         // the two low bits masked in place (4^j times their value) and the high bit
         // in place (2^hb times it), each in a dp4a of its own; the exact factors are
@@ -700,21 +753,33 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         const int hb = 4 * n + j0;
         const uint32_t m0 = 0x03030303u << (2 * j0), m1 = m0 << 2;
         const uint32_t h0 = 0x01010101u << hb, h1 = h0 << 1;
-        int L[4] = {0, 0, 0, 0}, H[4] = {0, 0, 0, 0};
+        int L[NX][4], H[NX][4];
+#pragma unroll
+        for (int i = 0; i < NX; ++i)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) L[i][g] = H[i][g] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            L[k >> 2] = dp4a_us(q[k] & m0, xu.x[k], L[k >> 2]);
-            L[2 + (k >> 2)] = dp4a_us(q[k] & m1, xu.x[8 + k], L[2 + (k >> 2)]);
-            H[k >> 2] = dp4a_us(hm[k] & h0, xu.x[k], H[k >> 2]);
-            H[2 + (k >> 2)] = dp4a_us(hm[k] & h1, xu.x[8 + k], H[2 + (k >> 2)]);
-        }
-        int A0 = 0;
+            const uint32_t wl0 = q[k] & m0, wl1 = q[k] & m1, wh0 = hm[k] & h0, wh1 = hm[k] & h1;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int Sg = (L[g] >> (2 * j0 + 2 * (g >> 1))) + 4 * (H[g] >> (hb + (g >> 1)));
-            A0 += (static_cast<int>((sc6 >> (8 * g)) & 0xFFu) - 32) * (Sg - xu.c[g]);
+            for (int i = 0; i < NX; ++i) {
+                L[i][k >> 2] = dp4a_us(wl0, xu[i].x[k], L[i][k >> 2]);
+                L[i][2 + (k >> 2)] = dp4a_us(wl1, xu[i].x[8 + k], L[i][2 + (k >> 2)]);
+                H[i][k >> 2] = dp4a_us(wh0, xu[i].x[k], H[i][k >> 2]);
+                H[i][2 + (k >> 2)] = dp4a_us(wh1, xu[i].x[8 + k], H[i][2 + (k >> 2)]);
+            }
         }
-        return static_cast<float>(A0) * (xu.d0 * ld_h(b + 108));
+        const float dq = ld_h(b + 108);
+#pragma unroll
+        for (int i = 0; i < NX; ++i) {
+            int A0 = 0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int Sg = (L[i][g] >> (2 * j0 + 2 * (g >> 1))) + 4 * (H[i][g] >> (hb + (g >> 1)));
+                A0 += (static_cast<int>((sc6 >> (8 * g)) & 0xFFu) - 32) * (Sg - xu[i].c[g]);
+            }
+            out[i] = static_cast<float>(A0) * (xu[i].d0 * dq);
+        }
     } else {  // F_Q6_K (element layout as in load_unit)
         const int sb = u >> 2, v = u & 3, h = v >> 1, g1 = v & 1;
         const saddr b = row + 210u * sb;
@@ -729,21 +794,41 @@ __device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const X
         // nibbles 16x, high pairs 4^g1 and 4^(g1+2) times their value); the exact
         // factors are shifted out of each group's sums
         const uint32_t m0 = 0x03030303u << (2 * g1), m1 = m0 << 4;
-        int N[4] = {0, 0, 0, 0}, P[4] = {0, 0, 0, 0};
+        int N[NX][4], P[NX][4];
+#pragma unroll
+        for (int i = 0; i < NX; ++i)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) N[i][g] = P[i][g] = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            N[k >> 2] = __dp4a(static_cast<int>(ql[k] & 0x0F0F0F0Fu), static_cast<int>(xu.x[k]), N[k >> 2]);
-            N[2 + (k >> 2)] = dp4a_us(ql[k] & 0xF0F0F0F0u, xu.x[8 + k], N[2 + (k >> 2)]);
-            P[k >> 2] = dp4a_us(qh[k] & m0, xu.x[k], P[k >> 2]);
-            P[2 + (k >> 2)] = dp4a_us(qh[k] & m1, xu.x[8 + k], P[2 + (k >> 2)]);
-        }
-        int S[4];
+            const uint32_t wl = ql[k] & 0x0F0F0F0Fu, wh = ql[k] & 0xF0F0F0F0u, p0 = qh[k] & m0, p1 = qh[k] & m1;
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-            S[g] = (g < 2 ? N[g] : N[g] >> 4) + 16 * (P[g] >> (2 * g1 + (g < 2 ? 0 : 4)));
-        const int A0 = sc0 * (S[0] - xu.c[0]) + sc1 * (S[1] - xu.c[1]) + sc2 * (S[2] - xu.c[2]) + sc3 * (S[3] - xu.c[3]);
-        return static_cast<float>(A0) * (xu.d0 * da);
+            for (int i = 0; i < NX; ++i) {
+                N[i][k >> 2] = __dp4a(static_cast<int>(wl), static_cast<int>(xu[i].x[k]), N[i][k >> 2]);
+                N[i][2 + (k >> 2)] = dp4a_us(wh, xu[i].x[8 + k], N[i][2 + (k >> 2)]);
+                P[i][k >> 2] = dp4a_us(p0, xu[i].x[k], P[i][k >> 2]);
+                P[i][2 + (k >> 2)] = dp4a_us(p1, xu[i].x[8 + k], P[i][2 + (k >> 2)]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NX; ++i) {
+            int S[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                S[g] = (g < 2 ? N[i][g] : N[i][g] >> 4) + 16 * (P[i][g] >> (2 * g1 + (g < 2 ? 0 : 4)));
+            const int A0 = sc0 * (S[0] - xu[i].c[0]) + sc1 * (S[1] - xu[i].c[1]) + sc2 * (S[2] - xu[i].c[2]) +
+                           sc3 * (S[3] - xu[i].c[3]);
+            out[i] = static_cast<float>(A0) * (xu[i].d0 * da);
+        }
     }
+}
+
+// fp32 contribution of unit u of a row against one token's register-resident activations.
+template <int F, bool A32 = (F == F_Q4_0)>
+__device__ __forceinline__ float unit_dot_rx(saddr row, int u, int nb32, const XUnit& xu) {
+    float out[1];
+    unit_dot_rxn<F, A32, 1>(row, u, nb32, &xu, out);
+    return out[0];
 }
 
 // ---------------------------------------------------------------- reductions

@@ -1,4 +1,4 @@
-// ggq_mmav.cuh -- the decode GEMV at 2-8 tokens on the tensor cores.
+// ggq_mmav.cuh -- the decode GEMV at 3-8 tokens on the tensor cores.
 //
 // y[t][n] = sum over blocks of (weight scale) * (activation scale) * (integer
 // block dot), as in the keep-quant matmul of vllm.cpp PR #523 "grouped +

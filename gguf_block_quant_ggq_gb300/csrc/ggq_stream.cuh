@@ -557,6 +557,72 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const StreamParams p) {
         }
     }
 
+    if constexpr (KIND == KIND_GEMV && NT == 2) {
+        const int nu = units_per_row(K), nb32 = K >> 5;
+        if (!CH && nu <= 64 && p.T == 2) {
+            // Two tokens, K <= 4096: a lane holds both tokens' activations of one
+            // unit for the whole kernel and loads and masks each weight word once
+            // for both.  Up to 32 units a warp takes row w of the tile, unit = lane;
+            // above, warps 2i and 2i + 1 take rows 2i and 2i + 1, units lane and
+            // lane + 32, and the odd warp's four sums (row, token) reach the even
+            // warp through shared memory: two buffers by tile parity, one 64-thread
+            // named barrier per warp pair.
+            const bool split = nu > 32;
+            const int hh = split ? (warp & 1) : 0;
+            const int uu = lane + 32 * hh;
+            const bool vu = uu < nu;
+            XUnit x2[2];
+            if (vu) {
+                load_xunit<F, Q81>(xs, uu, x2[0]);
+                XS x1 = xs;
+                x1.q = xs.q + static_cast<uint32_t>(xq_row_bytes(K));
+                x1.d = xs.d + 4u * static_cast<uint32_t>(K / (Q81 ? 32 : 256));
+                x1.s32 = xs.s32 + 4u * static_cast<uint32_t>(K >> 5);
+                x1.bs = xs.bs + 2u * static_cast<uint32_t>(K >> 4);
+                load_xunit<F, Q81>(x1, uu, x2[1]);
+            }
+            consumer_sync();  // every warp holds its activations: the region now carries the partials
+            float* const red = reinterpret_cast<float*>(xr_.q);  // [2][8 pairs][4]
+            int j = 0;
+            for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++j) {
+                const int s = j % p.stages;
+                const uint32_t ph = static_cast<uint32_t>(j / p.stages) & 1u;
+                const bool ready = __all_sync(0xffffffffu, mbar_wait(&full[s], ph));  // warp-uniform
+                if (!ready) set_error(p.err, DEV_ERR_TIMEOUT);
+                const saddr stage = ring_s + static_cast<uint32_t>(s * p.stage_stride);
+                const int64_t r0 = static_cast<int64_t>(item) * kTileRows;
+                if (split) {
+                    // rows 2i, 2i + 1 of the tile: acc = {row 2i tok 0, row 2i tok 1, row 2i+1 tok 0, row 2i+1 tok 1}
+                    const int i2 = warp & ~1;
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    if (ready && vu) {
+                        if (r0 + i2 < p.N) unit_dot_rxn<F, Q81, 2>(stage + static_cast<uint32_t>(i2 * p.rowbytes), uu, nb32, x2, acc);
+                        if (r0 + i2 + 1 < p.N)
+                            unit_dot_rxn<F, Q81, 2>(stage + static_cast<uint32_t>((i2 + 1) * p.rowbytes), uu, nb32, x2, acc + 2);
+                    }
+                    float v = warp_transpose_reduce<2>(acc, lane);  // lane >> 3 = 2 row + token
+                    float* const slot = red + 32 * (j & 1) + 4 * (warp >> 1) + (lane >> 3);
+                    if (hh == 1 && (lane & 7) == 0) *slot = v;
+                    asm volatile("bar.sync %0, 64;" ::"r"(3 + (warp >> 1)) : "memory");
+                    if (hh == 0 && (lane & 7) == 0) {
+                        v += *slot;
+                        const int64_t r = r0 + i2 + (lane >> 4);
+                        if (ready && r < p.N) p.Y[((lane >> 3) & 1) * p.N + r] = v;
+                    }
+                } else {
+                    const int64_t r = r0 + warp;
+                    float acc[2] = {0.0f, 0.0f};
+                    if (ready && r < p.N && vu) unit_dot_rxn<F, Q81, 2>(stage + static_cast<uint32_t>(warp * p.rowbytes), uu, nb32, x2, acc);
+                    const float v = warp_transpose_reduce<1>(acc, lane);  // lane >> 4 = token
+                    if (ready && r < p.N && (lane & 15) == 0) p.Y[(lane >> 4) * p.N + r] = v;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            return;
+        }
+    }
+
     if constexpr (KIND == KIND_GEMV) {
         if constexpr (CH) {
             // chunked rows: the warp's row sums its chunks in acc[] and is reduced once per tile

@@ -234,7 +234,7 @@ ggq_status ggq_mul_mat_vec_qa(ggq_ctx* ctx, int w, int act, const void* W, int64
  *     groups of 16, y += d_x (d A - dmin B);
  *   Q3_K x Q8_K (c = 1): A = sum_j (sc_j - 32) S_j over the 16 groups, y += d_x d A.
  * Runs the kernel that ggq_mul_mat_vec_q picks for the same (w, N, K, T) --
- * the dp4a streaming kernel, the tensor-path GEMV (2-8 tokens) or the grouped
+ * the dp4a streaming kernel, the tensor-path GEMV (3-8 tokens) or the grouped
  * int8 tensor-core kernel -- in a variant that stores the integers its dp4a or
  * mma units produce instead of the outputs.  The tensor paths hold them in
  * f32 accumulators; every such chain is short enough that its partial sums
@@ -302,7 +302,7 @@ ggq_status ggq_moe_experts_q(ggq_ctx* ctx, const ggq_moe_weights* w, int64_t E, 
  * launch nothing.  Arguments and layouts are those of ggq_mul_mat_vec, on the
  * CURRENT device; other errors: GGQ_ERR_UNSUPPORTED, _INVALID_ARG, _SHAPE,
  * _ARCH (not sm_103), _CUDA.  Every token count runs on the dp4a streaming
- * kernel, whereas ggq_mul_mat_vec takes the tensor-path kernel at 2-8 tokens
+ * kernel, whereas ggq_mul_mat_vec takes the tensor-path kernel at 3-8 tokens
  * where it applies: the two agree within the fp32 tolerance of the keep-quant
  * dot (the integer dots are the same; the order of the fp32 sums is not).
  * The first call on a device checks the architecture and looks up the

@@ -71,6 +71,9 @@ SHAPES = [  # (N, K, T): several 16-row tiles with a ragged tail; one and severa
     (1, 256, 1), (17, 4096, 6), (50, 256, 7),
     (16 * 11 + 3, 1024, 3), (40, 2048, 5), (16 * 9 + 9, 3072, 7),
     (37, 8192, 3), (16 * 5 + 3, 8192, 8),  # K beyond the tensor-path GEMV: the grouped int8 kernel
+    # two tokens above 32 units a row: warp pairs split the units (K = 3072: the odd warp's
+    # upper 16 lanes idle); 16 * 7 + 3 rows leave the last tile's second warp pair a row alone
+    (16 * 7 + 3, 4096, 2), (45, 3072, 2),
 ]
 Q4_0_ODD_SHAPES = [(21, 96, 2), (40, 32, 1), (35, 160, 8)]  # K % 64 == 32: a half 64-weight unit per row
 
@@ -258,14 +261,14 @@ def test_q4_0_workload_1024x4096(ctx):
 
 @pytest.mark.parametrize("fmt", ["Q8_0", "Q4_K", "Q5_K", "Q6_K", "Q2_K", "Q3_K"])
 def test_full_size_14336x4096_sampled_rows(ctx, fmt):
-    """Full workload size in the bench's launch configuration (T = 8 and 1);
+    """Full workload size in the bench's launch configuration (T = 8, 2 and 1);
     the oracle computes a sample of rows one by one, including both ends."""
     cfg = syn.GEMV_KQUANT
     N, K = cfg["N"], cfg["K"]
     W = syn.weights(fmt, N, K, syn.rng(cfg["index"], FORMATS.index(fmt)))
     dW = to_dev(W)
     rows = np.unique(np.concatenate([[0, 1, 15, 16, N - 17, N - 1], syn.rng(53, 0).integers(0, N, 58)]))
-    for T in (8, 1):
+    for T in (8, 2, 1):
         x = syn.activations(T, K, syn.rng(cfg["index"], 100 + T))
         y = to_host(ctx.mul_mat_vec(fmt, dW, N, K, to_dev(x)))
         xq = orc.quantize("Q8_K", x)
