@@ -661,8 +661,8 @@ def secondary_workloads(ctx, rt, hbm_peak):
 
 def profile_case(args):
     """Small launch sequences for ncu captures (not a benchmark).
-    gemv: 4 warm-up launches of a 14336 x 4096 GEMV at T=1, then one at T=1 and
-          one at T=8, over 5 rotating weight copies (165 MB for Q4_K > L2).
+    gemv: 4 warm-up launches of a 14336 x 4096 GEMV at T=1, then one at T=1, one
+          at T=2 and one at T=8, over 5 rotating weight copies (165 MB for Q4_K > L2).
     longrow: the same for the 4096 x 14336 shape (rows streamed in chunks;
           3 rotating copies, 187 MB for Q8_0).
     moe:  the MoE decode layer (128 experts, H 2048, I 768, Q4_K/Q6_K, top-8)
@@ -707,10 +707,11 @@ def profile_case(args):
         fmt = args.fmt
         Ws = [torch.from_numpy(syn.weights(fmt, N, K, syn.rng(1, i))).cuda() for i in range(5)]
         xq = {T: ctx.quantize_act("Q8_K", torch.from_numpy(syn.activations(T, K, syn.rng(1, 50 + T))).cuda())
-              for T in (1, 8)}
+              for T in (1, 2, 8)}
         for i in range(4):
             ctx.mul_mat_vec_q(fmt, Ws[i % 5], N, K, xq[1], 1)
         ctx.mul_mat_vec_q(fmt, Ws[4], N, K, xq[1], 1)
+        ctx.mul_mat_vec_q(fmt, Ws[1], N, K, xq[2], 2)
         ctx.mul_mat_vec_q(fmt, Ws[0], N, K, xq[8], 8)
     else:
         cfg = {"moe": syn.MOE_DECODE, "mxfp4": syn.MOE_MXFP4, "prefill": syn.MOE_PREFILL}[args.profile_case]
