@@ -229,6 +229,13 @@ __device__ __forceinline__ uint32_t mx_lookup(uint32_t sel) {
     return prmt(MX_POS_LO, MX_POS_HI, sel) | prmt(MX_NEG_LO, MX_NEG_HI, sel ^ 0x8888u);
 }
 
+// Doubled E2M1 magnitudes by the code's low three bits: 0, 1, 2, 3 | 4, 6, 8, 12.
+// With these tables a selector nibble whose bit 3 is set (a negative code) reads
+// 0 (the replicated sign bit of a byte below 128), so one PRMT of the codes
+// yields the positive codes' magnitudes and one of the codes with bit 3 flipped
+// the negative codes' magnitudes, four codes each (selector bits 0-15).
+constexpr uint32_t MX_MAG_LO = 0x03020100u, MX_MAG_HI = 0x0C080604u;
+
 __device__ __forceinline__ float e8m0_half_scale(uint32_t e) {
     // 2^(e-128): the doubled E2M1 codes carry the other factor of two.
     if (e >= 2u && e < 255u) return __int_as_float(static_cast<int>((e - 1u) << 23));
@@ -637,24 +644,35 @@ __device__ __forceinline__ void unit_dot_rxn(saddr row, int u, int nb32, const X
 #pragma unroll
             for (int k = 0; k < 4; ++k) q1[k] = 0u;
         }
-        int S0[NX], S1[NX];
+        // positive and negative codes' magnitudes in dp4a chains of their own:
+        // S = P - N is the exact integer sum of (2 value) x of each block
+        uint32_t tl = MX_MAG_LO, th = MX_MAG_HI;
+        asm("" : "+r"(tl), "+r"(th));  // the two table words stay in registers
+        int P0[NX], N0[NX], P1[NX], N1[NX];
 #pragma unroll
-        for (int i = 0; i < NX; ++i) S0[i] = S1[i] = 0;
+        for (int i = 0; i < NX; ++i) P0[i] = N0[i] = P1[i] = N1[i] = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int a0 = static_cast<int>(mx_lookup(q0[k] & 0xFFFFu)), a1 = static_cast<int>(mx_lookup(q0[k] >> 16));
-            const int b0 = static_cast<int>(mx_lookup(q1[k] & 0xFFFFu)), b1 = static_cast<int>(mx_lookup(q1[k] >> 16));
+            const uint32_t f0 = q0[k] ^ 0x88888888u, f1 = q1[k] ^ 0x88888888u;
+            const int pa0 = static_cast<int>(prmt(tl, th, q0[k])), pa1 = static_cast<int>(prmt(tl, th, q0[k] >> 16));
+            const int na0 = static_cast<int>(prmt(tl, th, f0)), na1 = static_cast<int>(prmt(tl, th, f0 >> 16));
+            const int pb0 = static_cast<int>(prmt(tl, th, q1[k])), pb1 = static_cast<int>(prmt(tl, th, q1[k] >> 16));
+            const int nb0 = static_cast<int>(prmt(tl, th, f1)), nb1 = static_cast<int>(prmt(tl, th, f1 >> 16));
 #pragma unroll
             for (int i = 0; i < NX; ++i) {
-                S0[i] = __dp4a(a0, static_cast<int>(xu[i].x[2 * k]), S0[i]);
-                S0[i] = __dp4a(a1, static_cast<int>(xu[i].x[2 * k + 1]), S0[i]);
-                S1[i] = __dp4a(b0, static_cast<int>(xu[i].x[8 + 2 * k]), S1[i]);
-                S1[i] = __dp4a(b1, static_cast<int>(xu[i].x[8 + 2 * k + 1]), S1[i]);
+                P0[i] = __dp4a(pa0, static_cast<int>(xu[i].x[2 * k]), P0[i]);
+                P0[i] = __dp4a(pa1, static_cast<int>(xu[i].x[2 * k + 1]), P0[i]);
+                N0[i] = __dp4a(na0, static_cast<int>(xu[i].x[2 * k]), N0[i]);
+                N0[i] = __dp4a(na1, static_cast<int>(xu[i].x[2 * k + 1]), N0[i]);
+                P1[i] = __dp4a(pb0, static_cast<int>(xu[i].x[8 + 2 * k]), P1[i]);
+                P1[i] = __dp4a(pb1, static_cast<int>(xu[i].x[8 + 2 * k + 1]), P1[i]);
+                N1[i] = __dp4a(nb0, static_cast<int>(xu[i].x[8 + 2 * k]), N1[i]);
+                N1[i] = __dp4a(nb1, static_cast<int>(xu[i].x[8 + 2 * k + 1]), N1[i]);
             }
         }
 #pragma unroll
         for (int i = 0; i < NX; ++i)
-            out[i] = xu[i].d0 * (static_cast<float>(S0[i] - xu[i].c[0]) * da + static_cast<float>(S1[i] - xu[i].c[1]) * db);
+            out[i] = xu[i].d0 * (static_cast<float>(P0[i] - N0[i]) * da + static_cast<float>(P1[i] - N1[i]) * db);
     } else if constexpr (F == F_Q4_K || F == F_Q5_K) {
         const int sb = u >> 2, cc = u & 3;
         const saddr b = row + (F == F_Q4_K ? 144u : 176u) * sb;
