@@ -29,7 +29,8 @@ CALLS = [  # (fmt, N, K, T), run one after the other
     ("Q4_K", 300, 4096, 8),
     ("Q4_K", 16 * 9 + 5, 4096, 1),  # one token: activations held in registers
     ("Q6_K", 16 * 7 + 3, 2048, 4),
-    ("MXFP4", 16 * 5 + 9, 4096, 2),
+    ("MXFP4", 16 * 5 + 9, 4096, 2),   # two tokens: both in registers, warp pairs split the units
+    ("Q6_K", 16 * 7 + 3, 3072, 2),
     ("Q5_K", 61, 1024, 1),
     ("Q4_0", 77, 1024, 3),
     ("Q8_0", 37, 14336, 2),         # rows too long for whole-row stages: row chunks
