@@ -511,6 +511,15 @@ def run_gpu(args, rank, world):
     ctx.close()
 
 
+def _moe_route(T, E, k):
+    """The route ggq_moe_experts takes (expert-load counters off): one direct
+    launch pair up to 4 tokens, direct calls of 4 tokens up to 32 tokens while
+    the pairs number at most 2 E, else expert-sorted tiles."""
+    if T <= 4:
+        return "direct"
+    return "direct, calls of 4 tokens" if T <= 32 and T * k <= 2 * E else "expert-sorted"
+
+
 def _graph_time(fn, reps, rt, stream, warm=2):
     """Capture fn() once; return the mean ms of one replay over `reps` replays."""
     import torch
@@ -645,7 +654,7 @@ def secondary_workloads(ctx, rt, hbm_peak):
             out[name] = {"GBps": round(gbps, 1), "frac": round(gbps / hbm_peak, 4),
                          "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R,
                          "int_TOPS": round(ops / (ms / 1e3) / 1e12, 2),
-                         "route": "direct" if T <= 4 else "expert-sorted"}
+                         "route": _moe_route(T, E, k)}
             if T > 4 and cfg["gate"] in ("Q8_0", "Q4_K") and cfg["down"] in ("Q8_0", "Q4_K"):
                 # the grouped GEMM runs the integer multiply-adds on 16-bit tensor cores (f16
                 # operands holding integers): against the measured dense 16-bit peak

@@ -188,8 +188,11 @@ def _run_and_check(ctx, cfg, E, T, routed=False, seed=0, sample_tokens=None):
     return flips
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 6, 13])
 def test_moe_decode_q4k_q6k(ctx, T):
+    """The decode layer on the direct route: one launch pair up to 4 tokens,
+    calls of at most 4 tokens above (6 = 4 + 2, 13 = 4 + 4 + 4 + 1), every
+    dumped array written at its tokens' rows."""
     cfg = syn.MOE_DECODE
     _run_and_check(ctx, cfg, cfg["E"], T)
 
@@ -232,9 +235,10 @@ def test_moe_q8_0_banks_sorted(ctx):
 
 @pytest.mark.parametrize("T", [5, 8, 32, 64, 128])
 def test_moe_sorted_route_mxfp4(ctx, T):
-    """5 tokens and up: expert-sorted tiles, on the grouped int8 tensor-core
-    kernel below 16 (token, expert) pairs per expert (here T < 64) and on the
-    tcgen05 grouped GEMM with bf16 operands from there (T = 64, 128)."""
+    """MXFP4 over a 32-expert bank: 5 and 8 tokens as direct-route calls of 4
+    tokens (pairs <= 2 E), 32 and up on expert-sorted tiles, on the grouped
+    int8 tensor-core kernel below 16 (token, expert) pairs per expert (T = 32)
+    and on the tcgen05 grouped GEMM with bf16 operands from there (64, 128)."""
     _run_and_check(ctx, syn.MOE_MXFP4, 32, T, sample_tokens=None if T <= 8 else 6)
 
 
@@ -245,8 +249,10 @@ def test_moe_q5k_banks_sorted(ctx):
     _run_and_check(ctx, cfg, 16, 12, sample_tokens=5)
 
 
-@pytest.mark.parametrize("T", [5, 16])
+@pytest.mark.parametrize("T", [5, 16, 40])
 def test_moe_sorted_route_q4k_q6k(ctx, T):
+    """The 128-expert decode layer above 4 tokens: calls of 4 tokens on the
+    direct route at 5 and 16 tokens, expert-sorted tiles at 40 (pairs > 2 E)."""
     cfg = syn.MOE_DECODE
     _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 8 else 6)
 
@@ -265,8 +271,9 @@ def test_moe_prefill_4096_tokens_zipf(ctx):
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 32, 128, 512])
 def test_moe_mxfp4_full_bank_256_experts(ctx, T):
     """The MXFP4 workload at full size (256 experts, H 4096, I 2048, top-8) at
-    every token count it names: 1-4 on the direct route, 5 and up on
-    expert-sorted tiles; larger counts check the pairs of sampled tokens."""
+    every token count it names: 1-4 on the direct route, 5 and 32 as direct
+    calls of 4 tokens, 128 and 512 on expert-sorted tiles; larger counts check
+    the pairs of sampled tokens."""
     cfg = syn.MOE_MXFP4
     _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 5 else 6)
 
@@ -292,11 +299,11 @@ def test_moe_all_experts_uniform_equals_dense(ctx):
     assert np.sum((y - ref["y"]) ** 2) / np.sum(ref["y"] ** 2) <= 1e-4
 
 
-@pytest.mark.parametrize("T", [1, 3, 8])
+@pytest.mark.parametrize("T", [1, 3, 8, 40])
 def test_moe_prequantized_entry_is_bit_identical(ctx, T):
     """ggq_moe_experts_q on x^ from ggq_quantize_act gives the very bytes of
     ggq_moe_experts on x (the same kernels take the same x^), on the direct
-    route (1 and 3 tokens) and on expert-sorted tiles (8)."""
+    route (1 and 3 tokens, 8 as two calls of 4) and on expert-sorted tiles (40)."""
     cfg = syn.MOE_DECODE
     E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
     host, dev = _banks(cfg, E)
