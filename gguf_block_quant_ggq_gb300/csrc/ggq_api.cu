@@ -743,7 +743,8 @@ ggq_status moe_sorted(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
 
 ggq_status moe_direct(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k, int fg,
                       int fd, const float* X, const uint8_t* xq_in, const float* logits, const int32_t* ids,
-                      const float* weights, int64_t T, float* Y, const ggq_moe_dump* dump, void* stream);
+                      const float* weights, int64_t T, float* Y, const ggq_moe_dump* dump, void* stream,
+                      int32_t* ids_out);
 
 ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k, const float* X,
                    const uint8_t* xq_in, const float* logits, const int32_t* ids, const float* weights, int64_t T,
@@ -776,9 +777,8 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         return fail(c, GGQ_ERR_SHAPE, "moe_experts: need 1 <= top_k <= 8 and top_k <= E <= 4096");
     if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
     // more than four tokens: direct-route calls of four tokens each where they fit and
-    // measured faster (not with the expert-load counters on, whose calls and distinct
-    // experts are counted per routing pass: those calls take the sorted tiles)
-    const bool chunked = T > kDirectMaxTokens && direct_chunks(T, E, top_k) && !c->tel_pairs &&
+    // measured faster
+    const bool chunked = T > kDirectMaxTokens && direct_chunks(T, E, top_k) &&
                          moe_width_refusal(fg, fd, E, H, I, kDirectMaxTokens, top_k) == nullptr;
     if (!chunked)
         if (const char* why = moe_width_refusal(fg, fd, E, H, I, T, top_k)) return fail(c, GGQ_ERR_SHAPE, "%s", why);
@@ -787,7 +787,17 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
                     static_cast<long long>(E), static_cast<long long>(c->tel_experts));
     if (T > kDirectMaxTokens && !chunked)
         return moe_sorted(c, w, E, H, I, top_k, X, xq_in, logits, ids, weights, T, Y, dump, stream);
-    if (!chunked) return moe_direct(c, w, E, H, I, top_k, fg, fd, X, xq_in, logits, ids, weights, T, Y, dump, stream);
+    if (!chunked)
+        return moe_direct(c, w, E, H, I, top_k, fg, fd, X, xq_in, logits, ids, weights, T, Y, dump, stream, nullptr);
+    // with the expert-load counters on, the launches keep every pair's routed id
+    // after the direct route's scratch and one small kernel counts the whole call
+    const size_t ids_at = moe_scratch(kDirectMaxTokens, H, I, top_k).total;
+    int32_t* ids_all = nullptr;
+    if (c->tel_pairs) {
+        const ggq_status s = need_scratch(c, ids_at + align_up(static_cast<size_t>(T * top_k) * 4));
+        if (s != GGQ_OK) return s;
+        ids_all = reinterpret_cast<int32_t*>(c->pool + ids_at);
+    }
     const int64_t xrow = H / 256 * 292, ncg = H / fmt_qk(fg) * fmt_coefs(fg), ncd = I / fmt_qk(fd) * fmt_coefs(fd);
     for (int64_t t0 = 0; t0 < T; t0 += kDirectMaxTokens) {
         const int64_t tc = T - t0 < kDirectMaxTokens ? T - t0 : kDirectMaxTokens;
@@ -810,16 +820,25 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
         const ggq_status s = moe_direct(c, w, E, H, I, top_k, fg, fd, X ? X + t0 * H : nullptr,
                                         xq_in ? xq_in + t0 * xrow : nullptr, logits ? logits + t0 * E : nullptr,
                                         ids ? ids + p0 : nullptr, weights ? weights + p0 : nullptr, tc, Y + t0 * H,
-                                        dump ? &dc : nullptr, stream);
+                                        dump ? &dc : nullptr, stream, ids_all ? ids_all + p0 : nullptr);
         if (s != GGQ_OK) return s;
+    }
+    if (ids_all) {
+        cudaError_t e = launch_moe_count(ids_all, static_cast<int>(T * top_k), static_cast<int>(E), c->tel_pairs,
+                                         c->tel_calls, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(c, e, "moe counters launch");
     }
     return GGQ_OK;
 }
 
-// The direct route for T <= 4 tokens (arguments checked by moe_run).
+// The direct route for T <= 4 tokens (arguments checked by moe_run).  ids_out:
+// where the routed ids go instead of the scratch (one launch of a several-launch
+// call, whose expert-load counters are taken afterwards from all its ids; the
+// launches themselves then count nothing), or null.
 ggq_status moe_direct(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, int64_t I, int top_k, int fg,
                       int fd, const float* X, const uint8_t* xq_in, const float* logits, const int32_t* ids,
-                      const float* weights, int64_t T, float* Y, const ggq_moe_dump* dump, void* stream) {
+                      const float* weights, int64_t T, float* Y, const ggq_moe_dump* dump, void* stream,
+                      int32_t* ids_out) {
     const MoeScratch ms = moe_scratch(T, H, I, top_k);
     ggq_status s = need_scratch(c, ms.total);
     if (s != GGQ_OK) return s;
@@ -834,7 +853,7 @@ ggq_status moe_direct(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     p.logits = logits;
     p.ids_in = ids;
     p.w_in = weights;
-    p.ids = reinterpret_cast<int32_t*>(c->pool + ms.ids);
+    p.ids = ids_out ? ids_out : reinterpret_cast<int32_t*>(c->pool + ms.ids);
     p.w = reinterpret_cast<float*>(c->pool + ms.w);
     p.h = reinterpret_cast<float*>(c->pool + ms.h);
     p.xq_dump = dump && !xq_in ? static_cast<uint8_t*>(dump->xq) : nullptr;
@@ -846,8 +865,8 @@ ggq_status moe_direct(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H
     p.coefs[0] = dump ? dump->coefs_gate : nullptr;
     p.coefs[1] = dump ? dump->coefs_up : nullptr;
     p.ncoef = static_cast<int>(H / fmt_qk(fg) * fmt_coefs(fg));
-    p.tel_pairs = c->tel_pairs;
-    p.tel_calls = c->tel_calls;
+    p.tel_pairs = ids_out ? nullptr : c->tel_pairs;
+    p.tel_calls = ids_out ? nullptr : c->tel_calls;
     p.Y = Y;
     p.err = &c->ctrl->err;
     const int nt = pow2_tokens(T);
@@ -992,6 +1011,7 @@ ggq_status ggq_reserve(ggq_ctx* c, const ggq_plan* plan, void* stream) {
         const int64_t E = plan->n_experts > 0 ? plan->n_experts : 4096;
         size_t m = moe_scratch(T < kDirectMaxTokens ? T : kDirectMaxTokens, plan->hidden, plan->inter, k).total;
         if (T > kDirectMaxTokens) {
+            m += align_up(static_cast<size_t>(T * k) * 4);  // direct calls of 4 tokens: every routed id kept
             const size_t ms = sorted_scratch(T, E, plan->hidden, plan->inter, k).total;
             if (ms > m) m = ms;
         }

@@ -201,6 +201,8 @@ cudaError_t launch_route_sorted(const float* logits, const int32_t* ids_in, cons
                                 int E, int k, int H, uint8_t* xq, int64_t x_pitch, int32_t* ids, float* w,
                                 int* counts, int* err, cudaStream_t s);
 // tel_pairs / tel_calls: optional expert-load telemetry (pairs per expert; calls and distinct experts).
+cudaError_t launch_moe_count(const int32_t* ids, int P, int E, unsigned long long* tel_pairs,
+                             unsigned long long* tel_calls, cudaStream_t s);
 cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
                               int* group_off, int* group_cnt, cudaStream_t s, unsigned long long* tel_pairs = nullptr,
                               unsigned long long* tel_calls = nullptr);

@@ -420,6 +420,43 @@ __global__ void __launch_bounds__(1024) k_group_plan(const int* __restrict__ cou
     }
 }
 
+// Expert-load telemetry of a call that ran as several direct-route launches:
+// from the routed ids of all its pairs, the pairs per expert and one call with
+// its distinct experts (ids outside [0, E) are skipped: the launches report them).
+__global__ void __launch_bounds__(256) k_moe_count(const int32_t* __restrict__ ids, int P, int E,
+                                                   unsigned long long* tel_pairs, unsigned long long* tel_calls) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ int cnt[4096];
+    __shared__ int distinct;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+    if (tid == 0) distinct = 0;
+    __syncthreads();
+    for (int q = tid; q < P; q += blockDim.x) {
+        const int e = ids[q];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    int nd = 0;
+    for (int e = tid; e < E; e += blockDim.x)
+        if (cnt[e] > 0) {
+            atomicAdd(tel_pairs + e, static_cast<unsigned long long>(cnt[e]));
+            ++nd;
+        }
+    atomicAdd(&distinct, nd);
+    __syncthreads();
+    if (tid == 0) {
+        atomicAdd(tel_calls, 1ull);
+        atomicAdd(tel_calls + 1, static_cast<unsigned long long>(distinct));
+    }
+}
+
+cudaError_t launch_moe_count(const int32_t* ids, int P, int E, unsigned long long* tel_pairs,
+                             unsigned long long* tel_calls, cudaStream_t s) {
+    return launch_pdl(k_moe_count, dim3(1), dim3(256), 0, s, ids, P, E, tel_pairs, tel_calls);
+}
+
 cudaError_t launch_group_plan(const int* counts, int E, int* offsets, int* cursor, int* ngroups, int* group_expert,
                               int* group_off, int* group_cnt, cudaStream_t s, unsigned long long* tel_pairs,
                               unsigned long long* tel_calls) {

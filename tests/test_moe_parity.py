@@ -335,7 +335,7 @@ def test_moe_expert_load_counters(ctx):
     want_calls = np.zeros(2, np.int64)
     try:
         g = syn.rng(cfg["index"], 4242)
-        for T in (1, 2, 3, 4, 16, 1):
+        for T in (1, 2, 3, 4, 16, 40, 1):  # 16: direct calls of 4 tokens, 40: expert-sorted tiles
             x = syn.activations(T, H, g)
             logits = syn.router_logits(T, E, g)
             ids, _ = orc.router(logits, k)
