@@ -23,7 +23,9 @@ GEMV on the 14336 x 4096 shape (1 and 8 tokens), the MoE decode
 layer (128 experts, H 2048, I 768, Q4_K gate/up, Q6_K down, top-8, 1-4
 tokens), the MXFP4 routed experts (256 experts, H 4096, I 2048, top-8, 1-512
 tokens) and the 4096-token prefill layer; MoE GB/s counts the distinct
-experts actually selected.
+experts actually selected.  From 5 tokens the MoE lines run the workloads'
+own route (expert-sorted tiles); where the library's default differs (direct
+calls of 4 tokens, up to 32 tokens), a "_direct4" line times that beside it.
 
 --impl reference times the CPU oracle on a bounded sample of the same workload.
 """
@@ -512,9 +514,9 @@ def run_gpu(args, rank, world):
 
 
 def _moe_route(T, E, k):
-    """The route ggq_moe_experts takes (expert-load counters off): one direct
-    launch pair up to 4 tokens, direct calls of 4 tokens up to 32 tokens while
-    the pairs number at most 2 E, else expert-sorted tiles."""
+    """The route ggq_moe_experts takes by default: one direct launch pair up to
+    4 tokens, direct calls of 4 tokens up to 32 tokens while the pairs number
+    at most 2 E, else expert-sorted tiles."""
     if T <= 4:
         return "direct"
     return "direct, calls of 4 tokens" if T <= 32 and T * k <= 2 * E else "expert-sorted"
@@ -647,14 +649,24 @@ def secondary_workloads(ctx, rt, hbm_peak):
                 for r in range(R):
                     ctx.moe_experts(w8, E, H, I, k, xs[r], logits=lgd[r], Y=ys, reserve=False)
 
-            ms = _graph_time(moe, 3 if T > 512 else 5, rt, stream)
-            gbps = distinct * per_expert / (ms / 1e3) / 1e9
+            # 5 tokens and up: the workload's own route (expert-sorted tiles, the direct
+            # route held to 4 tokens) under the workload's name, and the library's
+            # default (direct calls of 4 tokens where those apply) beside it
+            base = f"moe_{cfg['gate'].lower()}_{cfg['down'].lower()}_E{E}_H{H}_I{I}_T{T}"
+            runs = [(base, 4 if T > 4 else 32)]
+            if T > 4 and _moe_route(T, E, k) != "expert-sorted":
+                runs.append((base + "_direct4", 32))
             ops = 2.0 * T * k * 3 * I * H * R  # int multiply-adds x 2
-            name = f"moe_{cfg['gate'].lower()}_{cfg['down'].lower()}_E{E}_H{H}_I{I}_T{T}"
-            out[name] = {"GBps": round(gbps, 1), "frac": round(gbps / hbm_peak, 4),
-                         "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R,
-                         "int_TOPS": round(ops / (ms / 1e3) / 1e12, 2),
-                         "route": _moe_route(T, E, k)}
+            for name, dmax in runs:
+                ctx.set_direct_route_max_tokens(dmax)
+                ms = _graph_time(moe, 3 if T > 512 else 5, rt, stream)
+                gbps = distinct * per_expert / (ms / 1e3) / 1e9
+                out[name] = {"GBps": round(gbps, 1), "frac": round(gbps / hbm_peak, 4),
+                             "us_per_layer": round(ms * 1e3 / R, 2), "distinct_experts_per_layer": distinct / R,
+                             "int_TOPS": round(ops / (ms / 1e3) / 1e12, 2),
+                             "route": _moe_route(T, E, k) if dmax > 4 else ("direct" if T <= 4 else "expert-sorted")}
+            ctx.set_direct_route_max_tokens(32)
+            name = base
             if T > 4 and cfg["gate"] in ("Q8_0", "Q4_K") and cfg["down"] in ("Q8_0", "Q4_K"):
                 # the grouped GEMM runs the integer multiply-adds on 16-bit tensor cores (f16
                 # operands holding integers): against the measured dense 16-bit peak

@@ -34,6 +34,7 @@ SIGNATURES = {
     "ggq_reserve": (_I32, [_P, _P, _P]),
     "ggq_scratch_bytes": (ctypes.c_size_t, [_P]),
     "ggq_set_static_weights": (_I32, [_P, _I32]),
+    "ggq_set_direct_route_max_tokens": (_I32, [_P, _I32]),
     "ggq_supported": (_I32, [_I32, _I32, _I32]),
     "ggq_quantize_act": (_I32, [_P, _I32, _P, _I64, _I64, _P, _P]),
     "ggq_dequant": (_I32, [_P, _I32, _P, _I64, _I64, _P, _P]),
@@ -166,6 +167,9 @@ class Context:
 
     def set_static_weights(self, on: bool = True):
         self._check(load().ggq_set_static_weights(self.handle, 1 if on else 0))
+
+    def set_direct_route_max_tokens(self, max_tokens: int = 32):
+        self._check(load().ggq_set_direct_route_max_tokens(self.handle, int(max_tokens)))
 
     def scratch_bytes(self) -> int:
         return load().ggq_scratch_bytes(self.handle)

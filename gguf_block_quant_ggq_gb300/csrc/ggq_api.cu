@@ -172,6 +172,7 @@ struct ggq_ctx {
     std::vector<void*> retired;
     Ctrl* ctrl = nullptr;
     int static_weights = 0;  // weights never written while calls are in flight
+    int direct_max = 32;     // largest token count of the direct MoE route (calls of <= 4 tokens above 4)
     unsigned long long* tel_pairs = nullptr;  // expert-load telemetry (caller's device buffers)
     unsigned long long* tel_calls = nullptr;
     int64_t tel_experts = 0;
@@ -487,13 +488,13 @@ bool tc_down(int f, int64_t H, int64_t I, int64_t P, int64_t E) {
 constexpr int kDirectMaxTokens = 4;
 
 // Whether T > 4 tokens run as direct-route calls of at most four tokens each
-// instead of expert-sorted tiles: up to 32 tokens while the pairs number at
-// most twice the experts (few experts shared between the calls).  Measured on
+// instead of expert-sorted tiles: up to `limit` tokens (default 32) while the
+// pairs number at most twice the experts (few experts shared between the calls).  Measured on
 // the 128-expert Q4_K/Q6_K layer (H 2048, I 768) at 5 / 8 / 16 / 32 tokens:
 // 57 / 79 / 158 / 316 us against 216 / 298 / 450 / 617 us on sorted tiles;
 // on the 256-expert MXFP4 layer (H 4096, I 2048): 170 / 258 / 517 / 1028 us
 // against 297 / 438 / 764 / 1195 us, and 1545 against 1489 us at 48 tokens.
-bool direct_chunks(int64_t T, int64_t E, int top_k) { return T <= 32 && T * top_k <= 2 * E; }
+bool direct_chunks(int64_t T, int64_t E, int top_k, int limit) { return T <= limit && T * top_k <= 2 * E; }
 
 // Fixed shared memory of a direct-route kernel besides its ring and activations.
 constexpr int kDirectFixed = 2 * kMaxStages * 8 + static_cast<int>(sizeof(DirectPlan)) + 256;
@@ -778,7 +779,7 @@ ggq_status moe_run(ggq_ctx* c, const ggq_moe_weights* w, int64_t E, int64_t H, i
     if (T < 1) return fail(c, GGQ_ERR_SHAPE, "moe_experts: T=%lld", static_cast<long long>(T));
     // more than four tokens: direct-route calls of four tokens each where they fit and
     // measured faster
-    const bool chunked = T > kDirectMaxTokens && direct_chunks(T, E, top_k) &&
+    const bool chunked = T > kDirectMaxTokens && direct_chunks(T, E, top_k, c->direct_max) &&
                          moe_width_refusal(fg, fd, E, H, I, kDirectMaxTokens, top_k) == nullptr;
     if (!chunked)
         if (const char* why = moe_width_refusal(fg, fd, E, H, I, T, top_k)) return fail(c, GGQ_ERR_SHAPE, "%s", why);
@@ -995,6 +996,14 @@ size_t ggq_scratch_bytes(const ggq_ctx* c) { return c ? c->pool_bytes : 0; }
 ggq_status ggq_set_static_weights(ggq_ctx* c, int static_weights) {
     if (!c) return GGQ_ERR_INVALID_ARG;
     c->static_weights = static_weights ? 1 : 0;
+    return GGQ_OK;
+}
+
+ggq_status ggq_set_direct_route_max_tokens(ggq_ctx* c, int max_tokens) {
+    if (!c) return GGQ_ERR_INVALID_ARG;
+    if (max_tokens < kDirectMaxTokens || max_tokens > 32)
+        return fail(c, GGQ_ERR_INVALID_ARG, "set_direct_route_max_tokens: %d is outside [4, 32]", max_tokens);
+    c->direct_max = max_tokens;
     return GGQ_OK;
 }
 

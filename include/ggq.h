@@ -171,6 +171,18 @@ size_t ggq_scratch_bytes(const ggq_ctx* ctx);
  * enqueued after it. */
 ggq_status ggq_set_static_weights(ggq_ctx* ctx, int static_weights);
 
+/* Largest token count that ggq_moe_experts serves on the direct route (ds4 PR
+ * #656 "Add ROCm MXFP4 routed expert kernels", Summary: the direct kernels
+ * take 2-4 tokens, 5 and up go to expert-sorted tiles).  Above 4 tokens the
+ * direct route runs as calls of at most 4 tokens each, and only while the
+ * (token, expert) pairs number at most twice the experts; beyond that the
+ * call takes expert-sorted tiles.  Default 32 (measured faster than the tiles
+ * up to there on the decode layers); 4 keeps the page's split exactly.
+ * max_tokens outside [4, 32] returns GGQ_ERR_INVALID_ARG.  Takes effect for
+ * calls enqueued after it; results agree within the fp32 tolerance either way
+ * (the integer dots are the same, the order of the fp32 sums is not). */
+ggq_status ggq_set_direct_route_max_tokens(ggq_ctx* ctx, int max_tokens);
+
 /* Per-format availability: 1 if (weight format w, activation format act, op)
  * runs on this library, else 0.  For GGQ_OP_QUANTIZE_ACT w is ignored and act
  * is Q8_1 or Q8_K; for GGQ_OP_DEQUANT act is ignored.  Callers decide at load

@@ -249,10 +249,19 @@ def test_moe_q5k_banks_sorted(ctx):
     _run_and_check(ctx, cfg, 16, 12, sample_tokens=5)
 
 
-@pytest.mark.parametrize("T", [5, 16, 40])
-def test_moe_sorted_route_q4k_q6k(ctx, T):
+@pytest.mark.parametrize("T,dmax", [(5, 32), (16, 32), (5, 4), (16, 4), (40, 32)])
+def test_moe_sorted_route_q4k_q6k(ctx, T, dmax):
     """The 128-expert decode layer above 4 tokens: calls of 4 tokens on the
-    direct route at 5 and 16 tokens, expert-sorted tiles at 40 (pairs > 2 E)."""
+    direct route at 5 and 16 tokens by default, expert-sorted tiles with the
+    direct route held to 4 tokens (the ds4 page's split) and at 40 (pairs > 2 E)."""
+    ctx.set_direct_route_max_tokens(dmax)
+    try:
+        _sorted_q4k_q6k(ctx, T)
+    finally:
+        ctx.set_direct_route_max_tokens(32)
+
+
+def _sorted_q4k_q6k(ctx, T):
     cfg = syn.MOE_DECODE
     _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 8 else 6)
 
@@ -276,6 +285,25 @@ def test_moe_mxfp4_full_bank_256_experts(ctx, T):
     the pairs of sampled tokens."""
     cfg = syn.MOE_MXFP4
     _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 5 else 6)
+
+
+@pytest.mark.parametrize("T", [5, 32])
+def test_moe_mxfp4_full_bank_sorted_tiles(ctx, T):
+    """The MXFP4 workload at 5 and 32 tokens on the route it names, expert-sorted
+    tiles (the direct route held to 4 tokens)."""
+    cfg = syn.MOE_MXFP4
+    ctx.set_direct_route_max_tokens(4)
+    try:
+        _run_and_check(ctx, cfg, cfg["E"], T, sample_tokens=None if T <= 5 else 6)
+    finally:
+        ctx.set_direct_route_max_tokens(32)
+
+
+def test_direct_route_limit_is_checked(ctx):
+    for bad in (3, 33, 0):
+        with pytest.raises(ggq.GGQError, match="INVALID_ARG"):
+            ctx.set_direct_route_max_tokens(bad)
+    ctx.set_direct_route_max_tokens(32)
 
 
 def test_moe_all_experts_uniform_equals_dense(ctx):
