@@ -742,6 +742,7 @@ def profile_case(args):
                  for n, r, c in (("gate", I, H), ("up", I, H), ("down", H, I))]
         w8 = ctx.moe_weights(cfg["gate"], banks[0], cfg["up"], banks[1], cfg["down"], banks[2])
         T = args.tokens
+        ctx.set_direct_route_max_tokens(args.direct_max)
         for r in range(3):
             x = torch.from_numpy(syn.activations(T, H, g)).cuda()
             lg = torch.from_numpy(syn.router_logits(T, E, g, cfg.get("zipf"))).cuda()
@@ -815,6 +816,8 @@ def main():
                          "(metrics gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum) "
                          "to profiles/traffic_kquant_gemv_step.json")
     ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--direct-max", type=int, default=32,
+                    help="--profile-case moe/mxfp4/prefill: the direct MoE route's token limit (4: sorted tiles from 5)")
     args = ap.parse_args()
     if args.summarize_ncu:
         summarize_ncu(args.summarize_ncu)
