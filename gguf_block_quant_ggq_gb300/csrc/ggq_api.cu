@@ -296,7 +296,7 @@ ggq_status gemv_checks(ggq_ctx* c, int w, const void* W, int64_t N, int64_t K, c
     return GGQ_OK;
 }
 
-// Shared-memory plan of the tensor-path decode GEMV (2-8 tokens); false when
+// Shared-memory plan of the tensor-path decode GEMV (3-8 tokens); false when
 // the shape is not covered (rows not a multiple of 16 bytes, K above 16 chunks
 // of 256, Q6_K chunks below 128 inputs, or no room for two stages).
 bool plan_mmav(int f, MmavParams& p, int* smem) {

@@ -1,4 +1,4 @@
-// ggq_k_mmav.cu -- instantiations of the tensor-path decode GEMV (2-8 tokens).
+// ggq_k_mmav.cu -- instantiations of the tensor-path decode GEMV (3-8 tokens).
 #include "ggq_mmav.cuh"
 
 namespace ggq {
