@@ -212,6 +212,49 @@ __device__ __forceinline__ void group_superblock(saddr r0, saddr r1, int sb, con
         acc[3] += static_cast<float>(iA[3]) * (x1 * d1);
     } else {  // Q8_0, MXFP4: eight 32-blocks, one scale each
         const float x0 = gx_d(x, c0, sb), x1 = gx_d(x, c1, sb);
+        if constexpr (F == F_MXFP4 && !DUMP) {
+            if (x.ncols == 1) {
+                // one column (an expert that carries one pair): dp4a instead of an mma
+                // that would fill one of its eight columns.  Lane (g, tig) takes the
+                // fragment's codes (rows g, g + 8; elements 4 tig .. + 3 and 16 + 4 tig
+                // .. + 3) as doubled magnitudes of the positive and, with selector bit
+                // 3 flipped, of the negative codes, in the lookup's element order, and
+                // the column's activations in the same order; the four lanes of a row
+                // add their parts, so each block's integer and its scale product are
+                // those of the mma path
+                uint32_t tl = MX_MAG_LO, th = MX_MAG_HI;
+                asm("" : "+r"(tl), "+r"(th));
+                const saddr xr = gx_row(x, 0) + 292u * sb + 4u + 4u * tig;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const int blk = 8 * sb + s;
+                    const saddr p0 = r0 + 17u * blk, p1 = r1 + 17u * blk;
+                    uint32_t q0, q1;
+                    ld_words_any<1>(p0 + 1 + 4 * tig, &q0);
+                    ld_words_any<1>(p1 + 1 + 4 * tig, &q1);
+                    const uint32_t xlo = ld_s32(xr + 32u * s), xhi = ld_s32(xr + 32u * s + 16u);
+                    const int u0 = static_cast<int>(prmt(xlo, xhi, 0x5140u)), u1 = static_cast<int>(prmt(xlo, xhi, 0x7362u));
+                    const uint32_t f0 = q0 ^ 0x88888888u, f1 = q1 ^ 0x88888888u;
+                    int P0 = __dp4a(static_cast<int>(prmt(tl, th, q0)), u0, 0);
+                    P0 = __dp4a(static_cast<int>(prmt(tl, th, q0 >> 16)), u1, P0);
+                    int N0 = __dp4a(static_cast<int>(prmt(tl, th, f0)), u0, 0);
+                    N0 = __dp4a(static_cast<int>(prmt(tl, th, f0 >> 16)), u1, N0);
+                    int P1 = __dp4a(static_cast<int>(prmt(tl, th, q1)), u0, 0);
+                    P1 = __dp4a(static_cast<int>(prmt(tl, th, q1 >> 16)), u1, P1);
+                    int N1 = __dp4a(static_cast<int>(prmt(tl, th, f1)), u0, 0);
+                    N1 = __dp4a(static_cast<int>(prmt(tl, th, f1 >> 16)), u1, N1);
+                    int d0 = P0 - N0, d1 = P1 - N1;
+                    d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
+                    d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+                    d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
+                    d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+                    const float w0 = e8m0_half_scale(ld_u8(p0)), w1 = e8m0_half_scale(ld_u8(p1));
+                    acc[0] += static_cast<float>(d0) * (w0 * x0);  // column 0: lanes with tig 0
+                    acc[2] += static_cast<float>(d1) * (w1 * x0);
+                }
+                return;
+            }
+        }
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const int blk = 8 * sb + s;
