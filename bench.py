@@ -430,18 +430,35 @@ def run_gpu(args, rank, world):
                                "isolated_us": round(isolated[(f, T)] * 1e3, 2)}
                  for (f, T), ms in chain.items()}
 
-    # ---- end to end through the public API with host buffers
-    y_host = {k: torch.empty(v.shape, dtype=torch.float32).pin_memory() for k, v in y_dev.items()}
-    h2d = sum(x_host[T].numel() * 4 for T in TOKENS)
-    d2h = sum(v.numel() * 4 for v in y_dev.values())
+    # ---- end to end through the public API with host buffers: the step's inputs
+    # (every token count's x, one pinned buffer) in one host-to-device copy, the
+    # step's calls (ggq_quantize_act per token count, ggq_mul_mat_vec_q per GEMV),
+    # and all 16 outputs (one device buffer) back in one device-to-host copy
+    rows_x = sum(TOKENS)
+    xh_all = torch.empty((rows_x, K), dtype=torch.float32).pin_memory()
+    xd_all = torch.empty((rows_x, K), dtype=torch.float32, device="cuda")
+    xh, xd, r = {}, {}, 0
+    for T in TOKENS:
+        xh[T], xd[T] = xh_all[r:r + T], xd_all[r:r + T]
+        xh[T].copy_(x_host[T])
+        r += T
+    yd_all = torch.empty((len(FMTS) * rows_x, N), dtype=torch.float32, device="cuda")
+    yh_all = torch.empty((len(FMTS) * rows_x, N), dtype=torch.float32).pin_memory()
+    yd, r = {}, 0
+    for f in FMTS:
+        for T in TOKENS:
+            yd[(f, T)] = yd_all[r:r + T]
+            r += T
+    h2d = xh_all.numel() * 4
+    d2h = yh_all.numel() * 4
 
     def e2e_step():
+        xd_all.copy_(xh_all, non_blocking=True)
         for T in TOKENS:
-            x_dev[T].copy_(x_host[T], non_blocking=True)
+            ctx.quantize_act("Q8_K", xd[T], out=xq_dev[T])
         for (f, T, c) in plan:
-            ctx.mul_mat_vec(f, Wdev[f][c], N, K, x_dev[T], Y=y_dev[(f, T)], reserve=False)
-        for k, v in y_dev.items():
-            y_host[k].copy_(v, non_blocking=True)
+            ctx.mul_mat_vec_q(f, Wdev[f][c], N, K, xq_dev[T], T, Y=yd[(f, T)])
+        yh_all.copy_(yd_all, non_blocking=True)
 
     ctx.set_static_weights(False)  # the public call as a generic caller makes it
     with torch.cuda.stream(stream):
